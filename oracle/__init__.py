@@ -1,0 +1,163 @@
+"""CPU oracle for the sum-reduction library -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline legs of
+``bench.py`` may import this package.  The library (``libtcr``) never does,
+and this package imports nothing from it: the two share no code.
+
+The arithmetic lives in ``tcr_oracle.c`` (plain C, binary32 additions with
+no contraction, an exact fixed-point accumulator for the exact sum); this
+module only compiles it with gcc and marshals numpy arrays through ctypes.
+
+Functions (sources are cited in ``tcr_oracle.c``):
+
+``exact_sum``          exact sum rounded once to binary64, and sum of |x|
+                       ("GPU Tensor Cores for fast Arithmetic Reductions",
+                       Abstract: the arithmetic reduction of n numbers).
+``fixed_order``        balanced binary32 tree over index order, -0.0 pad
+                       ("Taming Bitwise Behavior in GPU Kernels with Tensor
+                       Core", Abstract: balanced-tree reduction order).
+``shuffle_tree``       declared order of the conventional reduction
+                       (grid-stride accumulation, warp butterfly, block tree,
+                       grid tree).
+``*_rows``             the same, one result per row.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "tcr_oracle.c")
+_LIB = os.path.join(_HERE, "_build", "liboracle.so")
+
+F16 = 0
+BF16 = 1
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``tcr_oracle.c`` into ``_build/liboracle.so`` (gcc, OpenMP)."""
+    os.makedirs(os.path.dirname(_LIB), exist_ok=True)
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    tmp = f"{_LIB}.{os.getpid()}.tmp"
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
+           "-fopenmp", "-shared", "-fPIC", "-Wall", "-Wextra", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            u16p = ctypes.POINTER(ctypes.c_uint16)
+            f32p = ctypes.POINTER(ctypes.c_float)
+            f64p = ctypes.POINTER(ctypes.c_double)
+            sz, i = ctypes.c_size_t, ctypes.c_int
+            lib.oracle_exact_sum.argtypes = [u16p, sz, i, i, f64p, f64p]
+            lib.oracle_exact_sum.restype = None
+            lib.oracle_exact_sum_rows.argtypes = [u16p, sz, sz, i, i, f64p, f64p]
+            lib.oracle_exact_sum_rows.restype = None
+            lib.oracle_fixed_order_f32.argtypes = [u16p, sz, i, i]
+            lib.oracle_fixed_order_f32.restype = ctypes.c_float
+            lib.oracle_fixed_order_rows_f32.argtypes = [u16p, sz, sz, i, i, f32p]
+            lib.oracle_fixed_order_rows_f32.restype = None
+            lib.oracle_shuffle_tree_f32.argtypes = [u16p, sz, i, i, i, i]
+            lib.oracle_shuffle_tree_f32.restype = ctypes.c_float
+            lib.oracle_shuffle_tree_rows_f32.argtypes = [u16p, sz, sz, i, i, i, i, f32p]
+            lib.oracle_shuffle_tree_rows_f32.restype = None
+            lib.oracle_leaves_f32.argtypes = [u16p, sz, i, f32p]
+            lib.oracle_leaves_f32.restype = None
+            _lib = lib
+    return _lib
+
+
+def _bits(x) -> np.ndarray:
+    """The raw 16-bit patterns of ``x`` (uint16, C-contiguous)."""
+    a = np.asarray(x)
+    if a.dtype == np.float16:
+        a = a.view(np.uint16)
+    if a.dtype != np.uint16:
+        raise TypeError(f"oracle inputs are 16-bit patterns, got {a.dtype}")
+    return np.ascontiguousarray(a)
+
+
+def _u16p(a):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_uint16))
+
+
+def default_threads() -> int:
+    return max(1, len(os.sched_getaffinity(0)))
+
+
+def exact_sum(x, dtype: int, threads: int | None = None) -> tuple[float, float]:
+    """(exact sum rounded to binary64, exact sum of |x| rounded to binary64)."""
+    a = _bits(x).reshape(-1)
+    s, m = ctypes.c_double(), ctypes.c_double()
+    _load().oracle_exact_sum(_u16p(a), a.size, dtype, threads or default_threads(),
+                             ctypes.byref(s), ctypes.byref(m))
+    return s.value, m.value
+
+
+def exact_sum_rows(x, dtype: int, threads: int | None = None):
+    a = _bits(x)
+    rows, cols = a.shape
+    s = np.empty(rows, np.float64)
+    m = np.empty(rows, np.float64)
+    _load().oracle_exact_sum_rows(
+        _u16p(a), rows, cols, dtype, threads or default_threads(),
+        s.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
+        m.ctypes.data_as(ctypes.POINTER(ctypes.c_double)))
+    return s, m
+
+
+def fixed_order(x, dtype: int, threads: int | None = None) -> np.float32:
+    a = _bits(x).reshape(-1)
+    return np.float32(_load().oracle_fixed_order_f32(_u16p(a), a.size, dtype,
+                                                     threads or default_threads()))
+
+
+def fixed_order_rows(x, dtype: int, threads: int | None = None) -> np.ndarray:
+    a = _bits(x)
+    rows, cols = a.shape
+    out = np.empty(rows, np.float32)
+    _load().oracle_fixed_order_rows_f32(_u16p(a), rows, cols, dtype,
+                                        threads or default_threads(),
+                                        out.ctypes.data_as(ctypes.POINTER(ctypes.c_float)))
+    return out
+
+
+def shuffle_tree(x, dtype: int, team_threads: int, team_blocks: int,
+                 threads: int | None = None) -> np.float32:
+    a = _bits(x).reshape(-1)
+    return np.float32(_load().oracle_shuffle_tree_f32(
+        _u16p(a), a.size, dtype, team_threads, team_blocks, threads or default_threads()))
+
+
+def shuffle_tree_rows(x, dtype: int, team_threads: int, team_blocks: int,
+                      threads: int | None = None) -> np.ndarray:
+    a = _bits(x)
+    rows, cols = a.shape
+    out = np.empty(rows, np.float32)
+    _load().oracle_shuffle_tree_rows_f32(_u16p(a), rows, cols, dtype, team_threads,
+                                         team_blocks, threads or default_threads(),
+                                         out.ctypes.data_as(ctypes.POINTER(ctypes.c_float)))
+    return out
+
+
+def leaves(x, dtype: int) -> np.ndarray:
+    a = _bits(x).reshape(-1)
+    out = np.empty(a.size, np.float32)
+    _load().oracle_leaves_f32(_u16p(a), a.size, dtype,
+                              out.ctypes.data_as(ctypes.POINTER(ctypes.c_float)))
+    return out

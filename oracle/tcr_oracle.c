@@ -1,0 +1,423 @@
+/*
+ * tcr_oracle.c -- CPU oracle for the sum-reduction library.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is a plain, slow, obviously correct
+ * restatement of what the reductions compute.  Only the test-suite, the
+ * smoke check and the benchmark's CPU-baseline leg load it; the library
+ * (the CUDA path) never does, and the two share no code, header or table.
+ *
+ * What the reduction is, and where each function comes from:
+ *
+ *  - "GPU Tensor Cores for fast Arithmetic Reductions" (arXiv 2001.05585),
+ *    Abstract: the problem is the arithmetic reduction (sum) of n numbers;
+ *    chain sub-results are kept as 32-bit floats and all of them are then
+ *    reduced into a final 32-bit result.  The tensor-core method's exact
+ *    rounding is not fixed by the page, so its oracle is the plain
+ *    definition: the exact sum (oracle_exact_sum), against which the
+ *    tensor-core result is held to an error bound.
+ *
+ *  - "Taming Bitwise Behavior in GPU Kernels with Tensor Core" (arXiv
+ *    2609.11356), Abstract: reduction order is the primary cause of bitwise
+ *    differences (with partial-sum precision, FMA and rounding placement);
+ *    a fixed balanced-tree order makes results reproducible, and an order is
+ *    pinned down by a descriptor.  oracle_fixed_order_f32 is the balanced
+ *    binary32 tree over index order; oracle_shuffle_tree_f32 is the declared
+ *    order of the conventional (grid-stride + butterfly) reduction.
+ *
+ * Readings taken where the pages are silent (each one is also listed in the
+ * design notes):
+ *  - Leaves are the exact binary32 values of the binary16 / bfloat16 inputs.
+ *  - The balanced tree is over index order with power-of-two aligned
+ *    subtrees; the input is padded to the next power of two with -0.0,
+ *    which is the identity of IEEE round-to-nearest addition for every x
+ *    (including +0 and -0), so the pad equals "an absent child passes its
+ *    sibling up".
+ *  - Every addition is one binary32 add, round to nearest even, no fused
+ *    multiply-add, no flush of subnormals.  The file is compiled with
+ *    -ffp-contract=off and without fast-math, and only additions occur.
+ *  - The empty sum is +0.0.
+ *
+ * Parity pins (the tests under tests/ check every function here against
+ * brute-force rational sums, invariants, an independent vectorised
+ * emulation and hand-worked trees).
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define DT_F16 0
+#define DT_BF16 1
+
+/* ------------------------------------------------------------------ */
+/* Decoding one 16-bit input (IEEE 754 binary16, or bfloat16 = the upper
+ * half of binary32).  A finite value is (-1)^neg * m * 2^e with integer m. */
+
+typedef struct {
+    int neg;      /* sign bit */
+    int special;  /* 0 finite, 1 infinity, 2 NaN */
+    uint32_t m;   /* integer significand (implicit bit included if normal) */
+    int e;        /* exponent of the significand's unit bit */
+} decoded_t;
+
+static decoded_t decode16(uint16_t h, int dtype)
+{
+    decoded_t d;
+    d.neg = (h >> 15) & 1;
+    d.special = 0;
+    if (dtype == DT_F16) {
+        /* binary16: 5 exponent bits (bias 15), 10 fraction bits */
+        uint32_t ex = (h >> 10) & 0x1f, fr = h & 0x3ff;
+        if (ex == 0x1f) {
+            d.special = fr ? 2 : 1; d.m = 0; d.e = 0;
+        } else if (ex == 0) {            /* subnormal: fr * 2^-24 */
+            d.m = fr; d.e = -24;
+        } else {                         /* (1024 + fr) * 2^(ex - 15 - 10) */
+            d.m = 1024 + fr; d.e = (int)ex - 25;
+        }
+    } else {
+        /* bfloat16: 8 exponent bits (bias 127), 7 fraction bits */
+        uint32_t ex = (h >> 7) & 0xff, fr = h & 0x7f;
+        if (ex == 0xff) {
+            d.special = fr ? 2 : 1; d.m = 0; d.e = 0;
+        } else if (ex == 0) {            /* subnormal: fr * 2^-133 */
+            d.m = fr; d.e = -133;
+        } else {                         /* (128 + fr) * 2^(ex - 127 - 7) */
+            d.m = 128 + fr; d.e = (int)ex - 134;
+        }
+    }
+    return d;
+}
+
+/* The exact binary32 value of one input (every binary16 and bfloat16 value
+ * is a binary32 value, so the conversion through double is exact). */
+static float leaf_f32(uint16_t h, int dtype)
+{
+    decoded_t d = decode16(h, dtype);
+    if (d.special == 2) return NAN;
+    if (d.special == 1) return d.neg ? -INFINITY : INFINITY;
+    double v = ldexp((double)d.m, d.e);
+    float f = (float)v;
+    return d.neg ? -f : f;
+}
+
+/* ------------------------------------------------------------------ */
+/* Exact sum: a two's-complement fixed-point accumulator of 5 x 64 bits
+ * whose bit 0 weighs 2^-133 (the smallest bfloat16 subnormal; the smallest
+ * binary16 subnormal 2^-24 is a multiple of it).  The largest bfloat16 is
+ * below 2^128, so 2^40 terms stay below 2^168, far inside 319 bits. */
+
+#define ACC_LIMBS 5
+#define ACC_LSB_EXP (-133)
+
+typedef struct { uint64_t w[ACC_LIMBS]; } acc_t;
+
+static void acc_add(acc_t *a, const acc_t *b)
+{
+    uint64_t carry = 0;
+    for (int i = 0; i < ACC_LIMBS; i++) {
+        uint64_t s = a->w[i] + carry;
+        uint64_t c1 = s < carry;
+        uint64_t t = s + b->w[i];
+        uint64_t c2 = t < s;
+        a->w[i] = t;
+        carry = c1 + c2;
+    }
+}
+
+static void acc_negate(acc_t *a)
+{
+    for (int i = 0; i < ACC_LIMBS; i++) a->w[i] = ~a->w[i];
+    acc_t one;
+    memset(&one, 0, sizeof one);
+    one.w[0] = 1;
+    acc_add(a, &one);
+}
+
+/* acc += (neg ? -1 : 1) * m * 2^pos, 0 <= pos < 64 * (ACC_LIMBS - 1) */
+static void acc_add_term(acc_t *a, uint64_t m, int pos, int neg)
+{
+    acc_t t;
+    memset(&t, 0, sizeof t);
+    int limb = pos / 64, sh = pos % 64;
+    t.w[limb] = m << sh;
+    if (sh != 0) t.w[limb + 1] = m >> (64 - sh);
+    if (neg) acc_negate(&t);
+    acc_add(a, &t);
+}
+
+static int acc_bit(const acc_t *a, int i) { return (int)((a->w[i / 64] >> (i % 64)) & 1u); }
+
+/* Round the exact value held in the accumulator to the nearest binary64
+ * (ties to even).  The accumulator's quantum 2^-133 is far above binary64's
+ * subnormal range, so only the 53-bit significand limit applies. */
+static double acc_to_double(const acc_t *a)
+{
+    acc_t mag = *a;
+    int neg = (int)((mag.w[ACC_LIMBS - 1] >> 63) & 1u);
+    if (neg) acc_negate(&mag);
+    int top = -1;
+    for (int i = ACC_LIMBS * 64 - 1; i >= 0; i--)
+        if (acc_bit(&mag, i)) { top = i; break; }
+    if (top < 0) return 0.0;
+    uint64_t sig = 0;
+    int low = top - 52;             /* lowest kept bit position */
+    if (low < 0) low = 0;
+    for (int i = top; i >= low; i--) sig = (sig << 1) | (uint64_t)acc_bit(&mag, i);
+    if (low > 0) {
+        int round = acc_bit(&mag, low - 1), sticky = 0;
+        for (int i = low - 2; i >= 0; i--)
+            if (acc_bit(&mag, i)) { sticky = 1; break; }
+        if (round && (sticky || (sig & 1u))) sig += 1;   /* may carry to 2^53: still exact in double */
+    }
+    double v = ldexp((double)sig, low + ACC_LSB_EXP);
+    return neg ? -v : v;
+}
+
+/* Exact summation by exponent buckets: every finite input is +-m * 2^e with
+ * an integer m < 2^11 and one of 254 exponents e >= -133.  Integer sums of m
+ * per exponent are exact (|sum| < 2^11 * n < 2^63 for n < 2^52), and the
+ * buckets are then added into the long accumulator, m_e * 2^e each. */
+#define N_EXP 256
+
+typedef struct {
+    int64_t signed_m[N_EXP];    /* sum of +-m for inputs with exponent e = index - 133 */
+    uint64_t abs_m[N_EXP];      /* sum of m for the same inputs */
+    size_t pos_inf, neg_inf, nan;
+} exact_state_t;
+
+static void exact_accumulate(exact_state_t *st, const uint16_t *x, size_t n, int dtype)
+{
+    for (size_t i = 0; i < n; i++) {
+        decoded_t d = decode16(x[i], dtype);
+        if (d.special == 2) { st->nan++; continue; }
+        if (d.special == 1) { if (d.neg) st->neg_inf++; else st->pos_inf++; continue; }
+        int pos = d.e - ACC_LSB_EXP;
+        st->signed_m[pos] += d.neg ? -(int64_t)d.m : (int64_t)d.m;
+        st->abs_m[pos] += d.m;
+    }
+}
+
+/*
+ * oracle_exact_sum: the exact sum of the n inputs, rounded once to binary64
+ * (round to nearest even), and the exact sum of their magnitudes, rounded
+ * the same way.  Non-finite inputs follow IEEE: any NaN, or +Inf together
+ * with -Inf, gives NaN; otherwise an infinity gives that infinity.
+ * Threads only split the index range; integer addition is exact, so the
+ * result does not depend on the thread count.
+ */
+void oracle_exact_sum(const uint16_t *x, size_t n, int dtype, int threads,
+                      double *sum_out, double *abs_out)
+{
+    int nt = threads > 0 ? threads : 1;
+#ifndef _OPENMP
+    nt = 1;
+#endif
+    exact_state_t *parts = (exact_state_t *)calloc((size_t)nt, sizeof(exact_state_t));
+    size_t per = (n + (size_t)nt - 1) / (size_t)nt;
+#pragma omp parallel for num_threads(nt) schedule(static, 1)
+    for (int t = 0; t < nt; t++) {
+        size_t lo = (size_t)t * per, hi = lo + per;
+        if (lo > n) lo = n;
+        if (hi > n) hi = n;
+        exact_accumulate(&parts[t], x + lo, hi - lo, dtype);
+    }
+    exact_state_t tot;
+    memset(&tot, 0, sizeof tot);
+    for (int t = 0; t < nt; t++) {
+        for (int e = 0; e < N_EXP; e++) {
+            tot.signed_m[e] += parts[t].signed_m[e];
+            tot.abs_m[e] += parts[t].abs_m[e];
+        }
+        tot.pos_inf += parts[t].pos_inf;
+        tot.neg_inf += parts[t].neg_inf;
+        tot.nan += parts[t].nan;
+    }
+    free(parts);
+    if (tot.nan || (tot.pos_inf && tot.neg_inf)) {
+        *sum_out = NAN;
+        *abs_out = tot.nan ? NAN : INFINITY;
+        return;
+    }
+    if (tot.pos_inf || tot.neg_inf) {
+        *sum_out = tot.pos_inf ? INFINITY : -INFINITY;
+        *abs_out = INFINITY;
+        return;
+    }
+    acc_t sum, abs_sum;
+    memset(&sum, 0, sizeof sum);
+    memset(&abs_sum, 0, sizeof abs_sum);
+    for (int e = 0; e < N_EXP; e++) {
+        int64_t sm = tot.signed_m[e];
+        uint64_t mag = sm < 0 ? (uint64_t)0 - (uint64_t)sm : (uint64_t)sm;
+        if (mag) acc_add_term(&sum, mag, e, sm < 0);
+        if (tot.abs_m[e]) acc_add_term(&abs_sum, tot.abs_m[e], e, 0);
+    }
+    *sum_out = acc_to_double(&sum);
+    *abs_out = acc_to_double(&abs_sum);
+}
+
+void oracle_exact_sum_rows(const uint16_t *x, size_t rows, size_t cols, int dtype,
+                           int threads, double *sum_out, double *abs_out)
+{
+    int nt = threads > 0 ? threads : 1;
+#pragma omp parallel for num_threads(nt) schedule(dynamic, 64)
+    for (size_t r = 0; r < rows; r++)
+        oracle_exact_sum(x + r * cols, cols, dtype, 1, &sum_out[r], &abs_out[r]);
+}
+
+/* ------------------------------------------------------------------ */
+/* Balanced binary32 trees. */
+
+static int ceil_log2(size_t n)
+{
+    int h = 0;
+    while (((size_t)1 << h) < n) h++;
+    return h;
+}
+
+/* Node of height h whose leftmost leaf is input lo: the sum of its two
+ * children, left + right, in binary32.  Leaves past n are the -0.0 pad.
+ * A subtree that lies wholly in the pad has the value -0.0 (every leaf is
+ * -0.0 and -0.0 + -0.0 = -0.0), so it is returned without descending. */
+static float tree_node16(const uint16_t *x, size_t n, int dtype, size_t lo, int h)
+{
+    if (lo >= n) return -0.0f;
+    if (h == 0) return leaf_f32(x[lo], dtype);
+    size_t half = (size_t)1 << (h - 1);
+    float left = tree_node16(x, n, dtype, lo, h - 1);
+    float right = tree_node16(x, n, dtype, lo + half, h - 1);
+    return left + right;
+}
+
+/* Same tree over binary32 values a[0..m), padded with -0.0. */
+static float tree_node32(const float *a, size_t m, size_t lo, int h)
+{
+    if (lo >= m) return -0.0f;
+    if (h == 0) return a[lo];
+    size_t half = (size_t)1 << (h - 1);
+    float left = tree_node32(a, m, lo, h - 1);
+    float right = tree_node32(a, m, lo + half, h - 1);
+    return left + right;
+}
+
+static float tree_f32(const float *a, size_t m)
+{
+    if (m == 0) return -0.0f;
+    return tree_node32(a, m, 0, ceil_log2(m));
+}
+
+/*
+ * oracle_fixed_order_f32: the balanced binary32 tree over the n inputs in
+ * index order.  Threads evaluate disjoint subtrees of the same tree; the
+ * top levels are then formed from those subtree values in the same shape,
+ * so the result is that of the single recursive definition.
+ */
+float oracle_fixed_order_f32(const uint16_t *x, size_t n, int dtype, int threads)
+{
+    if (n == 0) return 0.0f;
+    int H = ceil_log2(n);
+    int k = H < 10 ? H : 10;                 /* 2^k subtrees of height H - k */
+    size_t parts = (size_t)1 << k;
+    float *node = (float *)malloc(parts * sizeof(float));
+    int nt = threads > 0 ? threads : 1;
+#pragma omp parallel for num_threads(nt) schedule(dynamic, 1)
+    for (size_t i = 0; i < parts; i++)
+        node[i] = tree_node16(x, n, dtype, i << (H - k), H - k);
+    float r = tree_node32(node, parts, 0, k);
+    free(node);
+    return r;
+}
+
+void oracle_fixed_order_rows_f32(const uint16_t *x, size_t rows, size_t cols, int dtype,
+                                 int threads, float *out)
+{
+    int nt = threads > 0 ? threads : 1;
+#pragma omp parallel for num_threads(nt) schedule(dynamic, 64)
+    for (size_t r = 0; r < rows; r++)
+        out[r] = oracle_fixed_order_f32(x + r * cols, cols, dtype, 1);
+}
+
+/* ------------------------------------------------------------------ */
+/* Declared order of the conventional reduction (SHUFFLE_TREE).
+ *
+ * A segment of L inputs is split into vectors of 8 consecutive inputs
+ * (v = inputs 8v .. 8v+7, the last one padded with -0.0).  It is reduced by
+ * a team of G blocks of Bt threads (T = G*Bt threads, thread g = b*Bt + t):
+ *   1. vector value   = balanced tree over its 8 leaves;
+ *   2. thread value   = acc, acc starts at -0.0 and for v = g, g+T, g+2T, ...
+ *                       acc = acc + vector value (in that order);
+ *   3. warp value     = butterfly over the 32 lanes of the warp: for the
+ *                       offsets 16, 8, 4, 2, 1 in turn, every lane i replaces
+ *                       its value by value[i] + value[i xor offset];
+ *                       the warp value is what lane 0 holds at the end;
+ *   4. block value    = balanced tree over the block's Bt/32 warp values,
+ *                       in warp-index order;
+ *   5. segment value  = balanced tree over the G block values in block
+ *                       order, padded with -0.0.
+ */
+static float vector_tree8(const uint16_t *x, size_t L, int dtype, size_t v)
+{
+    float e[8];
+    for (int k = 0; k < 8; k++) {
+        size_t i = 8 * v + (size_t)k;
+        e[k] = i < L ? leaf_f32(x[i], dtype) : -0.0f;
+    }
+    return ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
+}
+
+static float shuffle_block_value(const uint16_t *x, size_t L, int dtype, int Bt, int G, int b)
+{
+    size_t T = (size_t)G * (size_t)Bt;
+    size_t nvec = (L + 7) / 8;
+    int W = Bt / 32;
+    float warp_value[32];
+    for (int w = 0; w < W; w++) {
+        float lane[32], next[32];
+        for (int j = 0; j < 32; j++) {
+            size_t g = (size_t)b * (size_t)Bt + (size_t)w * 32 + (size_t)j;
+            float acc = -0.0f;
+            for (size_t v = g; v < nvec; v += T) acc = acc + vector_tree8(x, L, dtype, v);
+            lane[j] = acc;
+        }
+        for (int off = 16; off >= 1; off /= 2) {
+            for (int j = 0; j < 32; j++) next[j] = lane[j] + lane[j ^ off];
+            memcpy(lane, next, sizeof lane);
+        }
+        warp_value[w] = lane[0];
+    }
+    return tree_f32(warp_value, (size_t)W);
+}
+
+float oracle_shuffle_tree_f32(const uint16_t *x, size_t L, int dtype, int Bt, int G, int threads)
+{
+    if (L == 0) return 0.0f;
+    if (Bt < 32 || Bt > 1024 || (Bt & (Bt - 1)) != 0 || G < 1) return NAN;
+    float *block = (float *)malloc((size_t)G * sizeof(float));
+    int nt = threads > 0 ? threads : 1;
+#pragma omp parallel for num_threads(nt) schedule(dynamic, 1)
+    for (int b = 0; b < G; b++) block[b] = shuffle_block_value(x, L, dtype, Bt, G, b);
+    float r = tree_f32(block, (size_t)G);
+    free(block);
+    return r;
+}
+
+void oracle_shuffle_tree_rows_f32(const uint16_t *x, size_t rows, size_t cols, int dtype,
+                                  int Bt, int G, int threads, float *out)
+{
+    int nt = threads > 0 ? threads : 1;
+#pragma omp parallel for num_threads(nt) schedule(dynamic, 64)
+    for (size_t r = 0; r < rows; r++)
+        out[r] = oracle_shuffle_tree_f32(x + r * cols, cols, dtype, Bt, G, 1);
+}
+
+/* Exact binary32 value of each input (used by the tests to compare the
+ * decoder with independent conversions). */
+void oracle_leaves_f32(const uint16_t *x, size_t n, int dtype, float *out)
+{
+    for (size_t i = 0; i < n; i++) out[i] = leaf_f32(x[i], dtype);
+}

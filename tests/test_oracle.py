@@ -1,0 +1,346 @@
+"""Pins for the CPU oracle, checked against things other than itself.
+
+Each test ties an oracle function to brute force, an invariant of the
+mathematics, an independent implementation written differently, or a value
+worked out by hand (``tests/golden``).  A plausible slip in the oracle -- a
+dropped term, a wrong index or shift, a wrong rounding rule, a transposed
+tree -- fails at least one of them.
+"""
+from fractions import Fraction
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from arithmetic_reduction_tensor_gb300 import synth
+
+F16, BF16 = oracle.F16, oracle.BF16
+
+
+# ---------------------------------------------------------------- helpers
+
+def np_leaves(bits, dtype):
+    """binary32 values decoded by numpy (independent of the oracle's decoder)."""
+    bits = np.asarray(bits, np.uint16)
+    if dtype == F16:
+        return bits.view(np.float16).astype(np.float32)
+    return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def frac_sum(bits, dtype):
+    """Exact rational sum and sum of magnitudes of finite inputs."""
+    vals = np_leaves(bits, dtype).astype(np.float64)
+    s = sum((Fraction(float(v)) for v in vals), Fraction(0))
+    a = sum((Fraction(abs(float(v))) for v in vals), Fraction(0))
+    return s, a
+
+
+@np.errstate(over="ignore", invalid="ignore")
+def np_tree(values_f32):
+    """Balanced binary32 tree, level by level with numpy, -0.0 pad."""
+    v = np.asarray(values_f32, np.float32)
+    n = v.size
+    if n == 0:
+        return np.float32(0.0)
+    size = 1
+    while size < n:
+        size *= 2
+    a = np.full(size, -0.0, np.float32)
+    a[:n] = v
+    while a.size > 1:
+        a = a[0::2] + a[1::2]
+    return a[0]
+
+
+@np.errstate(over="ignore", invalid="ignore")
+def np_shuffle(bits, dtype, bt, g):
+    """Vectorised emulation of the declared SHUFFLE_TREE order."""
+    v = np_leaves(bits, dtype)
+    L = v.size
+    if L == 0:
+        return np.float32(0.0)
+    nvec = (L + 7) // 8
+    e = np.full(nvec * 8, -0.0, np.float32)
+    e[:L] = v
+    e = e.reshape(nvec, 8)
+    vec = ((e[:, 0] + e[:, 1]) + (e[:, 2] + e[:, 3])) + ((e[:, 4] + e[:, 5]) + (e[:, 6] + e[:, 7]))
+    T = bt * g
+    acc = np.full(T, -0.0, np.float32)
+    for start in range(0, nvec, T):
+        m = min(T, nvec - start)
+        acc[:m] = acc[:m] + vec[start:start + m]
+    lanes = acc.reshape(-1, 32)
+    idx = np.arange(32)
+    for off in (16, 8, 4, 2, 1):
+        lanes = lanes + lanes[:, idx ^ off]
+    warp = lanes[:, 0].reshape(g, bt // 32)
+    while warp.shape[1] > 1:
+        warp = warp[:, 0::2] + warp[:, 1::2]
+    return np_tree(warp[:, 0])
+
+
+def same_f32(a, b):
+    a, b = np.float32(a), np.float32(b)
+    if np.isnan(a) or np.isnan(b):
+        return bool(np.isnan(a) and np.isnan(b))
+    return a.tobytes() == b.tobytes()
+
+
+def special_patterns(dtype):
+    """Bit patterns at the edges of each format: zeros, subnormals, extremes."""
+    if dtype == F16:
+        return [0x0000, 0x8000, 0x0001, 0x8001, 0x03FF, 0x83FF, 0x0400, 0x8400,
+                0x3C00, 0xBC00, 0x7BFF, 0xFBFF, 0x3BFF, 0x3C01]
+    return [0x0000, 0x8000, 0x0001, 0x8001, 0x007F, 0x807F, 0x0080, 0x8080,
+            0x3F80, 0xBF80, 0x7F7F, 0xFF7F, 0x3F7F, 0x3F81]
+
+
+def random_finite(rng, n, dtype):
+    """Random finite bit patterns (any exponent, both signs, subnormals)."""
+    b = rng.integers(0, 1 << 16, n, dtype=np.uint32).astype(np.uint16)
+    exp_mask = 0x7C00 if dtype == F16 else 0x7F80
+    bad = (b & exp_mask) == exp_mask
+    b[bad] &= np.uint16(0xBFFF)      # clear the top exponent bit: finite again
+    return b
+
+
+# ---------------------------------------------------------------- decoder
+
+@pytest.mark.parametrize("dtype", [F16, BF16])
+def test_leaves_match_numpy_for_every_pattern(dtype):
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    got = oracle.leaves(bits, dtype)
+    ref = np_leaves(bits, dtype)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan].view(np.uint32), ref[~nan].view(np.uint32))
+
+
+# ---------------------------------------------------------------- exact sum
+
+@pytest.mark.parametrize("dtype", [F16, BF16])
+@pytest.mark.parametrize("seed", range(6))
+def test_exact_sum_brute_force(dtype, seed):
+    rng = np.random.default_rng(100 + seed)
+    n = int(rng.integers(1, 65))
+    bits = np.concatenate([random_finite(rng, n, dtype),
+                           np.array(special_patterns(dtype), np.uint16)])
+    rng.shuffle(bits)
+    s, a = oracle.exact_sum(bits, dtype, threads=3)
+    fs, fa = frac_sum(bits, dtype)
+    assert s == float(fs)      # float(Fraction) rounds to nearest even
+    assert a == float(fa)
+
+
+@pytest.mark.parametrize("dtype", [F16, BF16])
+def test_exact_sum_permutation_invariant(dtype):
+    bits = synth.generate(200_003, "normal", dtype, seed=11)
+    rng = np.random.default_rng(5)
+    perm = bits[rng.permutation(bits.size)]
+    assert oracle.exact_sum(bits, dtype) == oracle.exact_sum(perm, dtype, threads=7)
+
+
+@pytest.mark.parametrize("dtype", [F16, BF16])
+def test_exact_sum_all_ones_is_n(dtype):
+    one = 0x3C00 if dtype == F16 else 0x3F80
+    n = 3_000_017
+    s, a = oracle.exact_sum(np.full(n, one, np.uint16), dtype)
+    assert s == float(n) and a == float(n)
+
+
+@pytest.mark.parametrize("dtype", [F16, BF16])
+def test_exact_sum_x_and_minus_x_cancel(dtype):
+    bits = synth.generate(500_000, "uniform_pm1", dtype, seed=12)
+    both = np.concatenate([bits, bits ^ np.uint16(0x8000)])
+    s, a = oracle.exact_sum(both, dtype)
+    s1, a1 = oracle.exact_sum(bits, dtype)
+    assert s == 0.0
+    assert a == 2 * a1
+
+
+def test_exact_sum_rounding_needs_sticky_and_ties_to_even():
+    # bfloat16 can hold 2^-52, 2^-53 and 2^-133 exactly.
+    def bf(x):
+        return int(np.float32(x).view(np.uint32) >> 16)
+    tie_to_even_down = np.array([bf(1.0), bf(2.0 ** -53)], np.uint16)
+    assert oracle.exact_sum(tie_to_even_down, BF16)[0] == 1.0
+    tie_to_even_up = np.array([bf(1.0), bf(2.0 ** -52), bf(2.0 ** -53)], np.uint16)
+    assert oracle.exact_sum(tie_to_even_up, BF16)[0] == 1.0 + 2.0 ** -51
+    sticky = np.array([bf(1.0), bf(2.0 ** -53), 0x0001], np.uint16)   # + 2^-133
+    assert oracle.exact_sum(sticky, BF16)[0] == 1.0 + 2.0 ** -52
+
+
+def test_exact_sum_extremes():
+    big = np.full(1 << 20, 0x7F7F, np.uint16)          # largest bfloat16
+    s, _ = oracle.exact_sum(big, BF16)
+    assert s == float(Fraction(float(np_leaves([0x7F7F], BF16)[0])) * (1 << 20))
+    f16max = np.full(1 << 20, 0x7BFF, np.uint16)       # 65504
+    assert oracle.exact_sum(f16max, F16)[0] == 65504.0 * (1 << 20)
+    tiny = np.full(1000, 0x0001, np.uint16)             # 2^-24 each
+    assert oracle.exact_sum(tiny, F16)[0] == 1000 * 2.0 ** -24
+
+
+@pytest.mark.parametrize("dtype", [F16, BF16])
+def test_exact_sum_non_finite(dtype):
+    inf = 0x7C00 if dtype == F16 else 0x7F80
+    nan = 0x7E00 if dtype == F16 else 0x7FC0
+    one = 0x3C00 if dtype == F16 else 0x3F80
+    assert oracle.exact_sum(np.array([one, inf], np.uint16), dtype)[0] == math.inf
+    assert oracle.exact_sum(np.array([one, inf | 0x8000], np.uint16), dtype)[0] == -math.inf
+    assert math.isnan(oracle.exact_sum(np.array([inf, inf | 0x8000], np.uint16), dtype)[0])
+    assert math.isnan(oracle.exact_sum(np.array([one, nan], np.uint16), dtype)[0])
+
+
+def test_exact_sum_rows_match_whole_rows():
+    x = synth.generate(37 * 301, "normal", F16, seed=13).reshape(37, 301)
+    s, a = oracle.exact_sum_rows(x, F16)
+    for r in range(37):
+        assert (s[r], a[r]) == oracle.exact_sum(x[r], F16, threads=1)
+
+
+def test_exact_sum_empty():
+    assert oracle.exact_sum(np.zeros(0, np.uint16), F16) == (0.0, 0.0)
+
+
+# ---------------------------------------------------------------- fixed order
+
+def _read_tree16(golden_dir):
+    vals = {}
+    with open(os.path.join(golden_dir, "fixed_order_tree16.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, rest = line.split(None, 1)
+            vals[key] = rest
+    bits = np.array([int(b, 16) for b in vals["bits"].split()], np.uint16)
+    return bits, vals
+
+
+def test_fixed_order_hand_worked_tree(golden_dir):
+    bits, vals = _read_tree16(golden_dir)
+    got = oracle.fixed_order(bits, F16, threads=1)
+    assert got == np.float32(float(Fraction(vals["fixed_order"])))
+    # the same inputs in other orders give the other two printed values
+    seq = np.float32(0.0)
+    for v in np_leaves(bits, F16):
+        seq = np.float32(seq + v)
+    assert seq == np.float32(float(Fraction(vals["sequential"])))
+    exact = Fraction(oracle.exact_sum(bits, F16)[0])
+    assert np.float32(float(exact)) == np.float32(float(Fraction(vals["exact_f32"])))
+    assert got != seq and got != np.float32(float(exact))
+
+
+@pytest.mark.parametrize("dtype", [F16, BF16])
+@pytest.mark.parametrize("n", [1, 2, 3, 7, 8, 9, 15, 16, 17, 255, 256, 257, 1000, 4095, 4097,
+                               65536, 65537, 100_003])
+def test_fixed_order_matches_levelwise_numpy(dtype, n):
+    rng = np.random.default_rng(n)
+    bits = random_finite(rng, n, dtype) if n < 5000 else synth.generate(n, "normal", dtype, seed=n)
+    got = oracle.fixed_order(bits, dtype, threads=4)
+    ref = np_tree(np_leaves(bits, dtype))
+    assert same_f32(got, ref)
+
+
+def test_fixed_order_thread_count_does_not_change_result():
+    bits = synth.generate(1_000_003, "uniform_pm1", F16, seed=14)
+    r = [oracle.fixed_order(bits, F16, threads=t) for t in (1, 2, 5, 8)]
+    assert all(x.tobytes() == r[0].tobytes() for x in r)
+
+
+def test_fixed_order_negative_zero_pad_is_identity():
+    bits = synth.generate(1000, "uniform_pm1", F16, seed=15)
+    padded = np.concatenate([bits, np.full(24, 0x8000, np.uint16)])   # 1024 = next power of two
+    assert same_f32(oracle.fixed_order(bits, F16), oracle.fixed_order(padded, F16))
+
+
+def test_fixed_order_integer_inputs_are_exact():
+    # small integers: every partial sum is an integer below 2^24, so every
+    # order gives the exact sum
+    rng = np.random.default_rng(16)
+    v = rng.integers(-64, 65, 300_001).astype(np.float16)
+    bits = v.view(np.uint16)
+    assert float(oracle.fixed_order(bits, F16)) == oracle.exact_sum(bits, F16)[0]
+
+
+def test_fixed_order_degenerate_cases():
+    assert oracle.fixed_order(np.zeros(0, np.uint16), F16).tobytes() == np.float32(0.0).tobytes()
+    assert oracle.fixed_order(np.array([0x3555], np.uint16), F16) == np.float16(0.333251953125)
+    negz = oracle.fixed_order(np.full(5, 0x8000, np.uint16), F16)
+    assert negz.tobytes() == np.float32(-0.0).tobytes()
+    assert np.isnan(oracle.fixed_order(np.array([0x3C00, 0x7E00, 0x3C00], np.uint16), F16))
+
+
+def test_fixed_order_rows_match_whole_rows():
+    x = synth.generate(29 * 1031, "uniform_pm1", BF16, seed=17).reshape(29, 1031)
+    got = oracle.fixed_order_rows(x, BF16)
+    for r in range(29):
+        assert same_f32(got[r], oracle.fixed_order(x[r], BF16, threads=1))
+
+
+# ---------------------------------------------------------------- shuffle tree
+
+def _read_shuffle_cases(golden_dir):
+    cases = []
+    with open(os.path.join(golden_dir, "shuffle_tree_cases.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            name, bt, g, L, items, result = [p.strip() for p in line.split("|")]
+            bits = np.zeros(int(L), np.uint16)
+            for it in items.split(","):
+                i, b = it.split("=")
+                bits[int(i)] = int(b, 16)
+            cases.append((name, int(bt), int(g), bits, Fraction(result)))
+    return cases
+
+
+def test_shuffle_tree_hand_worked_cases(golden_dir):
+    cases = _read_shuffle_cases(golden_dir)
+    assert len(cases) == 4
+    for name, bt, g, bits, expect in cases:
+        got = oracle.shuffle_tree(bits, F16, bt, g, threads=1)
+        assert got == np.float32(float(expect)), name
+
+
+@pytest.mark.parametrize("dtype", [F16, BF16])
+@pytest.mark.parametrize("L,bt,g", [(1, 32, 1), (8, 32, 1), (9, 32, 1), (255, 32, 1), (256, 32, 1),
+                                    (1000, 32, 1), (4097, 32, 1), (8192, 32, 1), (10_000, 64, 1),
+                                    (10_000, 128, 3), (33_333, 256, 2), (65_536, 1024, 1),
+                                    (70_001, 32, 7), (100_000, 512, 5)])
+def test_shuffle_tree_matches_vectorised_emulation(dtype, L, bt, g):
+    rng = np.random.default_rng(L + bt + g)
+    bits = random_finite(rng, L, dtype) if L < 5000 else synth.generate(L, "normal", dtype, seed=L)
+    got = oracle.shuffle_tree(bits, dtype, bt, g, threads=3)
+    assert same_f32(got, np_shuffle(bits, dtype, bt, g))
+
+
+@pytest.mark.parametrize("bt,g", [(32, 1), (64, 2), (256, 5), (1024, 3)])
+def test_shuffle_tree_integer_inputs_are_exact(bt, g):
+    rng = np.random.default_rng(bt * g)
+    bits = rng.integers(-64, 65, 123_457).astype(np.float16).view(np.uint16)
+    assert float(oracle.shuffle_tree(bits, F16, bt, g)) == oracle.exact_sum(bits, F16)[0]
+
+
+def test_shuffle_tree_single_vector_is_the_eight_leaf_tree():
+    # with at most one vector, only lane 0 holds data: the result is the
+    # 8-leaf balanced tree, i.e. the fixed-order tree of those inputs
+    rng = np.random.default_rng(18)
+    for L in range(1, 9):
+        bits = random_finite(rng, L, F16)
+        assert same_f32(oracle.shuffle_tree(bits, F16, 32, 1), oracle.fixed_order(bits, F16))
+
+
+def test_shuffle_tree_rows_match_whole_rows():
+    x = synth.generate(23 * 9001, "normal", F16, seed=19).reshape(23, 9001)
+    got = oracle.shuffle_tree_rows(x, F16, 64, 2)
+    for r in range(23):
+        assert same_f32(got[r], oracle.shuffle_tree(x[r], F16, 64, 2, threads=1))
+
+
+def test_shuffle_tree_empty_is_positive_zero():
+    assert oracle.shuffle_tree(np.zeros(0, np.uint16), F16, 32, 1).tobytes() == \
+        np.float32(0.0).tobytes()
