@@ -1,1 +1,178 @@
-"""Tensor-core and fixed-order sum reduction for GB300 (binding placeholder)."""
+"""tcr: tensor-core and fixed-order sum reduction on one GB300 GPU.
+
+A thin ctypes binding of ``libtcr.so`` (``include/tcr.h``), with the C
+names.  It only marshals arguments: every step of every reduction runs in
+the library's CUDA kernels.  PyTorch supplies device memory and streams.
+
+    import torch
+    import arithmetic_reduction_tensor_gb300 as tcr
+    x = torch.randn(1 << 20, device="cuda", dtype=torch.float16)
+    s = tcr.tcr_reduce_sum(x, tcr.Mode(tcr.FIXED_ORDER))        # 1-element fp32
+    r = tcr.tcr_reduce_rows(x.view(1024, 1024), tcr.Mode(tcr.MMA_CHAIN, R=4))
+
+The library must have been built (``python -m arithmetic_reduction_tensor_gb300.build``
+or ``__graft_entry__.build()``); without it every call raises -- there is
+no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from .build import LIB_PATH
+
+__all__ = [
+    "MMA_CHAIN", "SHUFFLE_TREE", "FIXED_ORDER", "F16", "BF16",
+    "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_CUDA",
+    "ORDER_TENSOR_CORE", "ORDER_GRID_STRIDE", "ORDER_BALANCED_TREE",
+    "tcr_mode", "tcr_order_desc", "Mode", "TcrError", "c_api",
+    "tcr_reduce_sum", "tcr_reduce_rows", "tcr_order_descriptor", "tcr_status_string",
+]
+
+MMA_CHAIN, SHUFFLE_TREE, FIXED_ORDER = 0, 1, 2
+F16, BF16 = 0, 1
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA = 0, 1, 2, 3
+ORDER_TENSOR_CORE, ORDER_GRID_STRIDE, ORDER_BALANCED_TREE = 0, 1, 2
+
+KIND_NAMES = {MMA_CHAIN: "MMA_CHAIN", SHUFFLE_TREE: "SHUFFLE_TREE", FIXED_ORDER: "FIXED_ORDER"}
+
+
+class tcr_mode(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int), ("R", ctypes.c_int),
+                ("block_threads", ctypes.c_int), ("dtype", ctypes.c_int)]
+
+    def __repr__(self):
+        return (f"Mode({KIND_NAMES.get(self.kind, self.kind)}, R={self.R}, "
+                f"block_threads={self.block_threads}, dtype={'bf16' if self.dtype else 'f16'})")
+
+
+class tcr_order_desc(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int), ("order", ctypes.c_int),
+                ("segment_len", ctypes.c_size_t), ("segments", ctypes.c_size_t),
+                ("vector_len", ctypes.c_int), ("team_threads", ctypes.c_int),
+                ("team_blocks", ctypes.c_int), ("chain_R", ctypes.c_int),
+                ("pad_negative_zero", ctypes.c_int), ("launch_grid", ctypes.c_int),
+                ("launch_block", ctypes.c_int), ("chunk_log2", ctypes.c_int),
+                ("partials", ctypes.c_size_t), ("launches", ctypes.c_int)]
+
+    def as_dict(self):
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+def Mode(kind: int, R: int = 0, block_threads: int = 0, dtype: int = F16) -> tcr_mode:
+    """A ``tcr_mode`` (R is used by MMA_CHAIN only; 0 means the default)."""
+    return tcr_mode(kind, R, block_threads, dtype)
+
+
+class TcrError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {tcr_status_string(status)} (status {status})")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def c_api() -> ctypes.CDLL:
+    """The loaded ``libtcr.so`` with the C signatures of ``include/tcr.h``."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"libtcr is not built ({LIB_PATH} missing); run "
+                    "`python -m arithmetic_reduction_tensor_gb300.build` -- there is no fallback")
+            lib = ctypes.CDLL(LIB_PATH)
+            vp, sz = ctypes.c_void_p, ctypes.c_size_t
+            lib.tcr_reduce_sum.argtypes = [vp, sz, vp, tcr_mode, vp]
+            lib.tcr_reduce_sum.restype = ctypes.c_int
+            lib.tcr_reduce_rows.argtypes = [vp, sz, sz, vp, tcr_mode, vp]
+            lib.tcr_reduce_rows.restype = ctypes.c_int
+            lib.tcr_order_descriptor.argtypes = [sz, sz, sz, tcr_mode, ctypes.POINTER(tcr_order_desc)]
+            lib.tcr_order_descriptor.restype = ctypes.c_int
+            lib.tcr_status_string.argtypes = [ctypes.c_int]
+            lib.tcr_status_string.restype = ctypes.c_char_p
+            _lib = lib
+    return _lib
+
+
+def tcr_status_string(status: int) -> str:
+    return c_api().tcr_status_string(status).decode()
+
+
+# ------------------------------------------------------------------ torch
+
+def _dtype_code(t, mode: tcr_mode) -> int:
+    import torch
+    if t.dtype == torch.float16:
+        code = F16
+    elif t.dtype == torch.bfloat16:
+        code = BF16
+    elif t.dtype in (torch.int16, torch.uint16):
+        return mode.dtype          # raw 16-bit patterns: the mode says what they are
+    else:
+        raise TypeError(f"inputs must be float16, bfloat16 or 16-bit patterns, got {t.dtype}")
+    if mode.dtype != code:
+        raise ValueError(f"mode.dtype {mode.dtype} does not match tensor dtype {t.dtype}")
+    return code
+
+
+def _stream_handle(device, stream) -> int:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check_out(out, device, count: int):
+    import torch
+    if out is None:
+        return torch.empty(max(count, 1), dtype=torch.float32, device=device)
+    if out.dtype != torch.float32 or out.device != device or not out.is_contiguous() or out.numel() < count:
+        raise ValueError("out must be a contiguous float32 tensor on the input's device "
+                         f"with at least {count} elements")
+    return out
+
+
+def tcr_reduce_sum(x, mode: tcr_mode, out=None, stream=None):
+    """out[0] = sum of the contiguous CUDA tensor ``x`` (``tcr_reduce_sum``)."""
+    import torch
+    if not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous CUDA tensor")
+    m = tcr_mode(mode.kind, mode.R, mode.block_threads, _dtype_code(x, mode))
+    out = _check_out(out, x.device, 1)
+    with torch.cuda.device(x.device):
+        st = c_api().tcr_reduce_sum(x.data_ptr() if x.numel() else None, x.numel(),
+                                    out.data_ptr(), m, _stream_handle(x.device, stream))
+    if st != OK:
+        raise TcrError(st, "tcr_reduce_sum")
+    return out
+
+
+def tcr_reduce_rows(x, mode: tcr_mode, out=None, stream=None):
+    """out[r] = sum of row r of the contiguous 2-D CUDA tensor ``x`` (``tcr_reduce_rows``)."""
+    import torch
+    if not x.is_cuda or not x.is_contiguous() or x.dim() != 2:
+        raise ValueError("x must be a contiguous 2-D CUDA tensor")
+    rows, cols = x.shape
+    m = tcr_mode(mode.kind, mode.R, mode.block_threads, _dtype_code(x, mode))
+    out = _check_out(out, x.device, rows)
+    with torch.cuda.device(x.device):
+        st = c_api().tcr_reduce_rows(x.data_ptr() if x.numel() else None, rows, cols,
+                                     out.data_ptr(), m, _stream_handle(x.device, stream))
+    if st != OK:
+        raise TcrError(st, "tcr_reduce_rows")
+    return out[:rows] if rows else out[:0]
+
+
+def tcr_order_descriptor(n: int = 0, rows: int = 0, cols: int = 0,
+                         mode: tcr_mode | None = None) -> dict:
+    """The declared order and launch plan of a call (``tcr_order_descriptor``)."""
+    d = tcr_order_desc()
+    st = c_api().tcr_order_descriptor(n, rows, cols, mode if mode is not None else Mode(FIXED_ORDER),
+                                      ctypes.byref(d))
+    if st != OK:
+        raise TcrError(st, "tcr_order_descriptor")
+    return d.as_dict()

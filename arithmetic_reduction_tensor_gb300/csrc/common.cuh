@@ -1,0 +1,184 @@
+// common.cuh -- device helpers shared by the reduction kernels.
+//
+// Inputs are 16-bit patterns (binary16 or bfloat16).  A "vector" is 8
+// consecutive inputs = 16 bytes = one 128-bit load per lane; a warp load
+// of 32 vectors covers 256 inputs, exactly one 16x16 tensor-core A tile.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_fp16.h>
+
+namespace tcr {
+
+constexpr int kF16 = 0;
+constexpr int kBF16 = 1;
+constexpr unsigned kFull = 0xffffffffu;
+
+// -0.0 in both 16-bit formats, twice per 32-bit word: the padding of the
+// ordered modes (the identity of round-to-nearest addition for every x).
+constexpr uint32_t kNegZero2 = 0x80008000u;
+
+// ---------------------------------------------------------------- loads
+
+// 16-byte streaming load through the read-only path.  Every input byte is
+// read exactly once, so the line is not kept in L1.
+__device__ __forceinline__ uint4 ld_stream(const uint16_t *p)
+{
+    uint4 v;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t pack2(uint16_t lo, uint16_t hi)
+{
+    return (uint32_t)lo | ((uint32_t)hi << 16);
+}
+
+// Vector v of a segment of `len` inputs at `seg` (any 2-byte alignment):
+// the inputs past `len` read as `fill` (a 16-bit pattern).
+__device__ __forceinline__ uint4 ld_vec_masked(const uint16_t *seg, size_t len, size_t v,
+                                               uint16_t fill)
+{
+    uint16_t e[8];
+#pragma unroll
+    for (int k = 0; k < 8; k++) {
+        size_t i = 8 * v + (size_t)k;
+        e[k] = i < len ? __ldg(seg + i) : fill;
+    }
+    return make_uint4(pack2(e[0], e[1]), pack2(e[2], e[3]), pack2(e[4], e[5]), pack2(e[6], e[7]));
+}
+
+// Vector v: a single 16-byte load when the segment start is 16-byte
+// aligned (ALIGNED) and the vector lies wholly inside the segment,
+// the element-wise masked load otherwise.  Both give the same 8 patterns.
+template <bool ALIGNED>
+__device__ __forceinline__ uint4 ld_vec(const uint16_t *seg, size_t len, size_t v, uint16_t fill)
+{
+    if (ALIGNED && 8 * v + 8 <= len) return ld_stream(seg + 8 * v);
+    return ld_vec_masked(seg, len, v, fill);
+}
+
+// ---------------------------------------------------------------- leaves
+
+// Exact binary32 value of the low / high 16-bit input of a 32-bit word
+// (little-endian: the low half is the lower index).
+template <int DT>
+__device__ __forceinline__ float leaf_lo(uint32_t w)
+{
+    if constexpr (DT == kF16) {
+        return __half2float(__ushort_as_half((unsigned short)(w & 0xffffu)));
+    } else {
+        return __uint_as_float(w << 16);
+    }
+}
+
+template <int DT>
+__device__ __forceinline__ float leaf_hi(uint32_t w)
+{
+    if constexpr (DT == kF16) {
+        return __half2float(__ushort_as_half((unsigned short)(w >> 16)));
+    } else {
+        return __uint_as_float(w & 0xffff0000u);
+    }
+}
+
+// Balanced tree over the 8 inputs of a vector:
+// ((e0 + e1) + (e2 + e3)) + ((e4 + e5) + (e6 + e7)).
+template <int DT>
+__device__ __forceinline__ float tree8(uint4 q)
+{
+    float p0 = __fadd_rn(leaf_lo<DT>(q.x), leaf_hi<DT>(q.x));
+    float p1 = __fadd_rn(leaf_lo<DT>(q.y), leaf_hi<DT>(q.y));
+    float p2 = __fadd_rn(leaf_lo<DT>(q.z), leaf_hi<DT>(q.z));
+    float p3 = __fadd_rn(leaf_lo<DT>(q.w), leaf_hi<DT>(q.w));
+    return __fadd_rn(__fadd_rn(p0, p1), __fadd_rn(p2, p3));
+}
+
+// ---------------------------------------------------------------- trees
+
+// Binary counter over a sequence of equal-height subtree values pushed in
+// index order: after pushing c values it holds the aligned subtrees of the
+// binary decomposition of c, and finish() returns the balanced tree over
+// the c values padded with -0.0 to a power of two.  Indices into s[] are
+// compile-time constants after unrolling, so s[] stays in registers.
+template <int LEVELS>
+struct TreeCounter {
+    float s[LEVELS];
+    uint32_t count;
+
+    __device__ __forceinline__ TreeCounter() : count(0u) {}
+
+    __device__ __forceinline__ void push(float v)
+    {
+#pragma unroll
+        for (int l = 0; l < LEVELS; l++) {
+            if ((count >> l) & 1u) {
+                v = __fadd_rn(s[l], v);        // left sibling + right sibling
+            } else {
+                s[l] = v;
+                break;
+            }
+        }
+        count++;
+    }
+
+    // Right-most partial subtree first: each higher stored subtree is the
+    // left sibling of everything pushed after it; a missing right sibling
+    // is -0.0, which passes its left sibling up unchanged.
+    __device__ __forceinline__ float finish() const
+    {
+        float v = -0.0f;
+#pragma unroll
+        for (int l = 0; l < LEVELS; l++)
+            if ((count >> l) & 1u) v = __fadd_rn(s[l], v);
+        return v;
+    }
+};
+
+// Balanced tree over the values of lanes 0..31 in lane order (offsets
+// 1, 2, 4, 8, 16): every lane ends with the root.
+__device__ __forceinline__ float warp_tree_lane_order(float v)
+{
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) v = __fadd_rn(v, __shfl_xor_sync(kFull, v, off));
+    return v;
+}
+
+// ---------------------------------------------------------------- MMA
+
+// D += A * ones for one m16n8k16 tile: A is 16x16 inputs held 8 per lane
+// (a0..a7 in the four 32-bit registers of q), B is the 16x8 all-ones
+// matrix, D the 16x8 fp32 accumulator (d0, d1: row lane/4; d2, d3: row
+// lane/4 + 8; every column of D holds the same row sums).
+template <int DT>
+__device__ __forceinline__ void mma_ones(float &d0, float &d1, float &d2, float &d3,
+                                         uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3)
+{
+    if constexpr (DT == kF16) {
+        const uint32_t one2 = 0x3c003c00u;    // binary16 1.0, twice
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+            "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};\n"
+            : "+f"(d0), "+f"(d1), "+f"(d2), "+f"(d3)
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(one2), "r"(one2));
+    } else {
+        const uint32_t one2 = 0x3f803f80u;    // bfloat16 1.0, twice
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+            "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};\n"
+            : "+f"(d0), "+f"(d1), "+f"(d2), "+f"(d3)
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(one2), "r"(one2));
+    }
+}
+
+__host__ __device__ __forceinline__ int ceil_log2_sz(size_t n)
+{
+    int h = 0;
+    while (((size_t)1 << h) < n) h++;
+    return h;
+}
+
+}  // namespace tcr

@@ -1,0 +1,124 @@
+// k_shuffle.cu -- SHUFFLE_TREE: the conventional GPU reduction, with its
+// order declared.
+//
+// "GPU Tensor Cores for fast Arithmetic Reductions" (arXiv 2001.05585),
+// Abstract, measures its method against a conventional GPU reduction; this
+// is that reduction, written so that its order is a descriptor ("Taming
+// Bitwise Behavior in GPU Kernels with Tensor Core", arXiv 2609.11356,
+// Abstract): a team of G blocks of Bt threads reduces one segment;
+//   thread g = b*Bt + t accumulates, starting from -0.0, the 8-input trees
+//   of vectors g, g + G*Bt, g + 2*G*Bt, ... in that order;
+//   a warp combines its lanes by the butterfly with offsets 16, 8, 4, 2, 1;
+//   a block is the balanced tree over its warps; the segment is the
+//   balanced tree over its G blocks (the combine kernel, when G > 1).
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace tcr {
+
+constexpr int kShuffleUnroll = 8;    // vectors in flight per thread
+
+__device__ __forceinline__ float warp_butterfly_16_to_1(float acc)
+{
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(kFull, acc, off));
+    return acc;
+}
+
+// Thread value: -0.0 + vector(first) + vector(first + stride) + ... in
+// order.  A vector index past nvec contributes -0.0, the identity.
+template <int DT, bool ALIGNED>
+__device__ __forceinline__ float grid_stride_acc(const uint16_t *seg, size_t len, size_t first,
+                                                 size_t stride)
+{
+    const size_t nvec = (len + 7) / 8;
+    float acc = -0.0f;
+    for (size_t v0 = first; v0 < nvec; v0 += kShuffleUnroll * stride) {
+        uint4 q[kShuffleUnroll];
+#pragma unroll
+        for (int u = 0; u < kShuffleUnroll; u++) {
+            size_t v = v0 + (size_t)u * stride;
+            q[u] = v < nvec ? ld_vec<ALIGNED>(seg, len, v, 0x8000u)
+                            : make_uint4(kNegZero2, kNegZero2, kNegZero2, kNegZero2);
+        }
+#pragma unroll
+        for (int u = 0; u < kShuffleUnroll; u++) acc = __fadd_rn(acc, tree8<DT>(q[u]));
+    }
+    return acc;
+}
+
+template <int DT, bool ALIGNED>
+__global__ void __launch_bounds__(1024)
+shuffle_block_kernel(const uint16_t *__restrict__ x, size_t seg_len, int G,
+                     float *__restrict__ dst)
+{
+    __shared__ float warp_val[32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    const size_t s = blockIdx.x / (unsigned)G;
+    const size_t b = blockIdx.x - s * (unsigned)G;
+    const uint16_t *seg = x + s * seg_len;
+    const size_t stride = (size_t)G * blockDim.x;
+    float acc = grid_stride_acc<DT, ALIGNED>(seg, seg_len, b * blockDim.x + threadIdx.x, stride);
+    acc = warp_butterfly_16_to_1(acc);
+    if (lane == 0) warp_val[warp] = acc;
+    __syncthreads();
+    if (warp == 0) {
+        float w = warp_tree_lane_order(lane < nwarps ? warp_val[lane] : -0.0f);
+        if (lane == 0) dst[blockIdx.x] = w;
+    }
+}
+
+template <int DT, bool ALIGNED>
+__global__ void __launch_bounds__(1024)
+shuffle_rows_warp_kernel(const uint16_t *__restrict__ x, size_t rows, size_t cols,
+                         float *__restrict__ out)
+{
+    const int lane = threadIdx.x & 31;
+    const size_t gw = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const size_t nw = ((size_t)gridDim.x * blockDim.x) >> 5;
+    for (size_t r = gw; r < rows; r += nw) {
+        float acc = grid_stride_acc<DT, ALIGNED>(x + r * cols, cols, (size_t)lane, 32);
+        acc = warp_butterfly_16_to_1(acc);
+        if (lane == 0) out[r] = acc;
+    }
+}
+
+// ---------------------------------------------------------------- host
+
+#define TCR_PICK(KERNEL, dtype, aligned)                                                   \
+    ((dtype) == kF16 ? ((aligned) ? KERNEL<kF16, true> : KERNEL<kF16, false>)              \
+                     : ((aligned) ? KERNEL<kBF16, true> : KERNEL<kBF16, false>))
+
+cudaError_t launch_shuffle_block(int dtype, bool aligned, const uint16_t *x, size_t seg_len,
+                                 size_t segments, int G, float *dst, int block,
+                                 cudaStream_t stream)
+{
+    auto k = TCR_PICK(shuffle_block_kernel, dtype, aligned);
+    k<<<(unsigned)(segments * (size_t)G), block, 0, stream>>>(x, seg_len, G, dst);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_shuffle_rows_warp(int dtype, bool aligned, const uint16_t *x, size_t rows,
+                                     size_t cols, float *out, int grid, int block,
+                                     cudaStream_t stream)
+{
+    auto k = TCR_PICK(shuffle_rows_warp_kernel, dtype, aligned);
+    k<<<grid, block, 0, stream>>>(x, rows, cols, out);
+    return cudaGetLastError();
+}
+
+int occupancy_shuffle(bool rows, int dtype, bool aligned, int block)
+{
+    int n = 0;
+    cudaError_t e = rows ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                               &n, TCR_PICK(shuffle_rows_warp_kernel, dtype, aligned), block, 0)
+                         : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                               &n, TCR_PICK(shuffle_block_kernel, dtype, aligned), block, 0);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+}  // namespace tcr

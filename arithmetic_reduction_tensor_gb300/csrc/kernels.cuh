@@ -1,0 +1,63 @@
+// kernels.cuh -- launchers of the reduction kernels (host side).
+//
+// Every launcher enqueues one kernel on `stream` and returns the launch
+// status (cudaGetLastError).  Sizes are in inputs (16-bit elements).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace tcr {
+
+// Inputs per warp group of the tree kernels: 8 warp loads of 256 inputs.
+constexpr size_t kGroup = 2048;
+// Inputs per warp of one CTA work unit (chunk) of the chunked kernels.
+constexpr int kWarpSpanLog2 = 13;
+// Longest row served by one warp (tree kernels) or one 16-row warp tile
+// (tensor-core rows kernel); longer rows go through the chunked kernels.
+constexpr size_t kRowsWarpMaxCols = 16384;
+
+// ---- FIXED_ORDER (balanced tree over index order)
+// Chunked: CTA work unit u = (segment u / cps, chunk u % cps); the chunk of
+// 2^chunk_log2 inputs is split evenly over the CTA's warps; dst[u] is the
+// chunk's aligned subtree.
+cudaError_t launch_fixed_chunk(int dtype, bool aligned, const uint16_t *x, size_t seg_len,
+                               size_t units, size_t cps, int chunk_log2, float *dst, int grid,
+                               int block, cudaStream_t stream);
+// One warp per row, rows <= kRowsWarpMaxCols inputs long: out[r] = row tree.
+cudaError_t launch_fixed_rows_warp(int dtype, bool aligned, const uint16_t *x, size_t rows,
+                                   size_t cols, float *out, int grid, int block,
+                                   cudaStream_t stream);
+
+// ---- SHUFFLE_TREE (declared grid-stride order)
+// Block team: grid = segments * G CTAs of Bt threads; CTA (s, b) writes its
+// block value to dst[s * G + b].
+cudaError_t launch_shuffle_block(int dtype, bool aligned, const uint16_t *x, size_t seg_len,
+                                 size_t segments, int G, float *dst, int block,
+                                 cudaStream_t stream);
+// Warp team (Bt = 32, G = 1): one warp per row, out[r] = warp value.
+cudaError_t launch_shuffle_rows_warp(int dtype, bool aligned, const uint16_t *x, size_t rows,
+                                     size_t cols, float *out, int grid, int block,
+                                     cudaStream_t stream);
+
+// ---- MMA_CHAIN (tensor-core chains of R MMAs against a ones matrix)
+cudaError_t launch_mma_chunk(int dtype, bool aligned, int R, const uint16_t *x, size_t seg_len,
+                             size_t units, size_t cps, int chunk_log2, float *dst, int grid,
+                             int block, cudaStream_t stream);
+// One warp per 16 consecutive rows, rows <= kRowsWarpMaxCols inputs long.
+cudaError_t launch_mma_rows(int dtype, bool aligned, int R, const uint16_t *x, size_t rows,
+                            size_t cols, float *out, int grid, int block, cudaStream_t stream);
+
+// ---- combine: out[s] = balanced tree over partials[s*count .. s*count+count-1]
+// padded with -0.0; one CTA of 1024 threads per segment.
+cudaError_t launch_combine(const float *partials, size_t segments, size_t count, float *out,
+                           cudaStream_t stream);
+
+// Resident CTAs per SM of each kernel at a block size (occupancy API);
+// `rows` selects the per-row variant.  0 if the query fails.
+int occupancy_fixed(bool rows, int dtype, bool aligned, int block);
+int occupancy_shuffle(bool rows, int dtype, bool aligned, int block);
+int occupancy_mma(bool rows, int dtype, bool aligned, int R, int block);
+
+}  // namespace tcr

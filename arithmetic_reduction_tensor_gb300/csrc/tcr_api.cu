@@ -1,0 +1,430 @@
+// tcr_api.cu -- the C ABI of libtcr: argument checks, launch planning,
+// stream-ordered scratch and the launch sequence of every call.
+//
+// The calls follow "GPU Tensor Cores for fast Arithmetic Reductions"
+// (arXiv 2001.05585), Abstract: the arithmetic reduction of n numbers into
+// one 32-bit result (tcr_reduce_sum), and the same per row (tcr_reduce_rows).
+// The order descriptor restates for sums the descriptor of reduction order
+// of "Taming Bitwise Behavior in GPU Kernels with Tensor Core" (arXiv
+// 2609.11356), Abstract.
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "../../include/tcr.h"
+#include "kernels.cuh"
+
+namespace {
+
+using namespace tcr;
+
+constexpr size_t kMaxInputs = (size_t)1 << 40;
+constexpr int kDefaultBlock = 256;
+// GB300: 152 SMs.  Used only by the declared SHUFFLE_TREE team rule (so the
+// declared order is the same on every device) and as the launch-plan SM
+// count when no device can be queried.
+constexpr int kRuleSMs = 152;
+
+// -------------------------------------------------------------- devices
+
+struct DeviceState {
+    bool init = false;
+    int sms = kRuleSMs;
+    cudaMemPool_t pool = nullptr;
+};
+
+std::mutex g_mu;
+std::vector<DeviceState> g_dev;
+
+struct OccKey {
+    int dev, fam, rows, dtype, aligned, R, block;
+    bool operator==(const OccKey &o) const { return std::memcmp(this, &o, sizeof *this) == 0; }
+};
+std::vector<std::pair<OccKey, int>> g_occ;
+
+int current_device()
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return -1;
+    }
+    return dev;
+}
+
+int sm_count(int dev)
+{
+    if (dev < 0) return kRuleSMs;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if ((int)g_dev.size() <= dev) g_dev.resize(dev + 1);
+    DeviceState &d = g_dev[dev];
+    if (!d.init) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
+            d.sms = n;
+        else
+            (void)cudaGetLastError();
+        d.init = true;
+    }
+    return d.sms;
+}
+
+// The library's stream-ordered pool on `dev`.  Its release threshold keeps
+// freed blocks reserved, so a steady stream of calls does not go back to
+// the driver for memory.
+cudaMemPool_t pool_for(int dev)
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    if ((int)g_dev.size() <= dev) g_dev.resize(dev + 1);
+    DeviceState &d = g_dev[dev];
+    if (!d.pool) {
+        cudaMemPoolProps props;
+        std::memset(&props, 0, sizeof props);
+        props.allocType = cudaMemAllocationTypePinned;
+        props.handleTypes = cudaMemHandleTypeNone;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t p = nullptr;
+        if (cudaMemPoolCreate(&p, &props) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return nullptr;
+        }
+        uint64_t keep = UINT64_MAX;
+        (void)cudaMemPoolSetAttribute(p, cudaMemPoolAttrReleaseThreshold, &keep);
+        d.pool = p;
+    }
+    return d.pool;
+}
+
+enum Family { kFixedF, kShuffleF, kMmaF };
+
+int occupancy(int dev, Family fam, bool rows, int dtype, bool aligned, int R, int block)
+{
+    OccKey key{dev, (int)fam, rows ? 1 : 0, dtype, aligned ? 1 : 0, R, block};
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        for (auto &e : g_occ)
+            if (e.first == key) return e.second;
+    }
+    int n = 0;
+    if (dev >= 0) {
+        switch (fam) {
+        case kFixedF: n = occupancy_fixed(rows, dtype, aligned, block); break;
+        case kShuffleF: n = occupancy_shuffle(rows, dtype, aligned, block); break;
+        case kMmaF: n = occupancy_mma(rows, dtype, aligned, R, block); break;
+        }
+    }
+    if (n <= 0) n = 1;
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_occ.emplace_back(key, n);
+    return n;
+}
+
+// -------------------------------------------------------------- planning
+
+enum Path {
+    kPathEmpty,          // nothing to reduce: memset out to +0.0
+    kPathChunk,          // FIXED / MMA chunked kernel (+ combine if cps > 1)
+    kPathFixedRowsWarp,  // FIXED, one warp per row
+    kPathMmaRows,        // MMA, one warp per 16 rows
+    kPathShuffleBlock,   // SHUFFLE block team (+ combine if G > 1)
+    kPathShuffleRowsWarp // SHUFFLE warp team, one warp per row
+};
+
+struct Plan {
+    int kind, dtype, R, block;
+    bool aligned;
+    Path path;
+    size_t segments, seg_len;
+    int grid, chunk_log2;
+    size_t cps, units;       // chunks per segment, CTA work units
+    int team_threads, team_blocks;
+    size_t partials;         // fp32 scratch entries (0: writes out directly)
+    size_t combine_count;    // partials per segment for the combine
+    int launches;
+};
+
+int log2_exact(int v)
+{
+    int l = 0;
+    while ((1 << l) < v) l++;
+    return l;
+}
+
+// Default chain length by block size, from the Abstract of arXiv
+// 2001.05585 (R = 4 or 5 for 32- and 128-thread blocks, R = 1 for large
+// ones).
+int default_R(int block)
+{
+    if (block <= 128) return 4;
+    if (block <= 256) return 2;
+    return 1;
+}
+
+// The declared SHUFFLE_TREE team for a segment of L inputs at block size B:
+// one warp for short segments, else G blocks of B threads with about 16
+// vectors per thread, at most 152 * 1024 threads in the team.
+void shuffle_team(size_t L, int B, int *Bt, int *G)
+{
+    if (L <= 8192) {
+        *Bt = 32;
+        *G = 1;
+        return;
+    }
+    const size_t per_block = (size_t)8 * (size_t)B * 16;
+    size_t g = (L + per_block - 1) / per_block;
+    const size_t gmax = (size_t)kRuleSMs * 1024 / (size_t)B;
+    if (g > gmax) g = gmax;
+    if (g < 1) g = 1;
+    *Bt = B;
+    *G = (int)g;
+}
+
+tcr_status check_mode(const tcr_mode &m, int *block, int *R)
+{
+    if (m.kind < TCR_MMA_CHAIN || m.kind > TCR_FIXED_ORDER) return TCR_ERR_INVALID_ARG;
+    if (m.dtype != TCR_F16 && m.dtype != TCR_BF16) return TCR_ERR_INVALID_ARG;
+    int b = m.block_threads == 0 ? kDefaultBlock : m.block_threads;
+    if (b < 32 || b > 1024 || (b & (b - 1)) != 0) return TCR_ERR_INVALID_ARG;
+    int r = 0;
+    if (m.kind == TCR_MMA_CHAIN) {
+        if (m.R < 0 || m.R > 8) return TCR_ERR_INVALID_ARG;
+        r = m.R == 0 ? default_R(b) : m.R;
+    }
+    *block = b;
+    *R = r;
+    return TCR_OK;
+}
+
+void plan_chunked(Plan &p, int dev, Family fam)
+{
+    // each warp of a CTA covers 2^13 inputs of the CTA's chunk
+    p.path = kPathChunk;
+    p.chunk_log2 = kWarpSpanLog2 + log2_exact(p.block / 32);
+    p.cps = (p.seg_len + ((size_t)1 << p.chunk_log2) - 1) >> p.chunk_log2;
+    p.units = p.segments * p.cps;
+    const size_t resident = (size_t)sm_count(dev) *
+                            (size_t)occupancy(dev, fam, false, p.dtype, p.aligned, p.R, p.block);
+    p.grid = (int)(p.units < resident ? p.units : resident);
+    p.partials = p.cps > 1 ? p.units : 0;
+    p.combine_count = p.cps;
+    p.launches = p.cps > 1 ? 2 : 1;
+}
+
+// Plans tcr_reduce_sum (rows == 0: one segment of n) or tcr_reduce_rows.
+Plan make_plan(size_t segments, size_t seg_len, bool rows_call, const tcr_mode &m, int block,
+               int R, bool aligned, int dev)
+{
+    Plan p;
+    std::memset(&p, 0, sizeof p);
+    p.kind = m.kind;
+    p.dtype = m.dtype;
+    p.R = R;
+    p.block = block;
+    p.aligned = aligned;
+    p.segments = segments;
+    p.seg_len = seg_len;
+    if (segments == 0 || seg_len == 0) {
+        p.path = kPathEmpty;
+        return p;
+    }
+    const size_t sms = (size_t)sm_count(dev);
+    if (m.kind == TCR_SHUFFLE_TREE) {
+        shuffle_team(seg_len, block, &p.team_threads, &p.team_blocks);
+        if (p.team_threads == 32 && p.team_blocks == 1) {
+            // a team of one warp: pack one segment per warp, 8 per CTA
+            p.path = kPathShuffleRowsWarp;
+            p.block = kDefaultBlock;
+            const size_t warps_per_cta = (size_t)p.block / 32;
+            const size_t need = (segments + warps_per_cta - 1) / warps_per_cta;
+            const size_t resident =
+                sms * (size_t)occupancy(dev, kShuffleF, true, p.dtype, aligned, 0, p.block);
+            p.grid = (int)(need < resident ? need : resident);
+            p.launches = 1;
+        } else {
+            p.path = kPathShuffleBlock;
+            p.grid = (int)(segments * (size_t)p.team_blocks);
+            p.partials = p.team_blocks > 1 ? segments * (size_t)p.team_blocks : 0;
+            p.combine_count = (size_t)p.team_blocks;
+            p.launches = p.team_blocks > 1 ? 2 : 1;
+        }
+        return p;
+    }
+    const Family fam = m.kind == TCR_FIXED_ORDER ? kFixedF : kMmaF;
+    if (rows_call && seg_len <= kRowsWarpMaxCols) {
+        const size_t warps_per_cta = (size_t)block / 32;
+        size_t work_warps = m.kind == TCR_FIXED_ORDER ? segments : (segments + 15) / 16;
+        const size_t need = (work_warps + warps_per_cta - 1) / warps_per_cta;
+        const size_t resident = sms * (size_t)occupancy(dev, fam, true, p.dtype, aligned, R, block);
+        p.path = m.kind == TCR_FIXED_ORDER ? kPathFixedRowsWarp : kPathMmaRows;
+        p.grid = (int)(need < resident ? need : resident);
+        p.launches = 1;
+        return p;
+    }
+    plan_chunked(p, dev, fam);
+    return p;
+}
+
+bool fault_injected(const char *what)
+{
+    const char *e = std::getenv("TCR_FAULT_INJECT");
+    return e && std::strcmp(e, what) == 0;
+}
+
+tcr_status run_plan(const Plan &p, const uint16_t *x, float *out, cudaStream_t s, int dev)
+{
+    if (p.path == kPathEmpty) {
+        if (fault_injected("launch")) return TCR_ERR_CUDA;
+        if (cudaMemsetAsync(out, 0, p.segments * sizeof(float), s) != cudaSuccess) return TCR_ERR_CUDA;
+        return TCR_OK;
+    }
+    float *partials = nullptr;
+    if (p.partials) {
+        if (fault_injected("alloc")) return TCR_ERR_CUDA;
+        cudaMemPool_t pool = pool_for(dev);
+        if (!pool) return TCR_ERR_CUDA;
+        if (cudaMallocFromPoolAsync((void **)&partials, p.partials * sizeof(float), pool, s) !=
+            cudaSuccess)
+            return TCR_ERR_CUDA;
+    }
+    if (fault_injected("launch")) {
+        if (partials) (void)cudaFreeAsync(partials, s);
+        return TCR_ERR_CUDA;
+    }
+    float *dst = partials ? partials : out;
+    cudaError_t e = cudaSuccess;
+    switch (p.path) {
+    case kPathChunk:
+        e = p.kind == TCR_FIXED_ORDER
+                ? launch_fixed_chunk(p.dtype, p.aligned, x, p.seg_len, p.units, p.cps,
+                                     p.chunk_log2, dst, p.grid, p.block, s)
+                : launch_mma_chunk(p.dtype, p.aligned, p.R, x, p.seg_len, p.units, p.cps,
+                                   p.chunk_log2, dst, p.grid, p.block, s);
+        break;
+    case kPathFixedRowsWarp:
+        e = launch_fixed_rows_warp(p.dtype, p.aligned, x, p.segments, p.seg_len, dst, p.grid,
+                                   p.block, s);
+        break;
+    case kPathMmaRows:
+        e = launch_mma_rows(p.dtype, p.aligned, p.R, x, p.segments, p.seg_len, dst, p.grid,
+                            p.block, s);
+        break;
+    case kPathShuffleBlock:
+        e = launch_shuffle_block(p.dtype, p.aligned, x, p.seg_len, p.segments, p.team_blocks, dst,
+                                 p.team_threads, s);
+        break;
+    case kPathShuffleRowsWarp:
+        e = launch_shuffle_rows_warp(p.dtype, p.aligned, x, p.segments, p.seg_len, dst, p.grid,
+                                     p.block, s);
+        break;
+    default:
+        e = cudaErrorInvalidValue;
+        break;
+    }
+    if (e == cudaSuccess && partials)
+        e = launch_combine(partials, p.segments, p.combine_count, out, s);
+    if (partials) {
+        cudaError_t f = cudaFreeAsync(partials, s);
+        if (e == cudaSuccess) e = f;
+    }
+    return e == cudaSuccess ? TCR_OK : TCR_ERR_CUDA;
+}
+
+tcr_status check_common(const void *x, size_t total, const float *out, const tcr_mode &mode,
+                        int *block, int *R)
+{
+    if (!out || ((uintptr_t)out & 3u) != 0) return TCR_ERR_INVALID_ARG;
+    if (total >= kMaxInputs) return TCR_ERR_INVALID_ARG;
+    if (total > 0 && (!x || ((uintptr_t)x & 1u) != 0)) return TCR_ERR_INVALID_ARG;
+    return check_mode(mode, block, R);
+}
+
+bool mul_overflows(size_t a, size_t b)
+{
+    return a != 0 && b > SIZE_MAX / a;
+}
+
+}  // namespace
+
+extern "C" {
+
+tcr_status tcr_reduce_sum(const void *x, size_t n, float *out, tcr_mode mode, void *stream)
+{
+    int block = 0, R = 0;
+    tcr_status st = check_common(x, n, out, mode, &block, &R);
+    if (st != TCR_OK) return st;
+    const int dev = current_device();
+    if (dev < 0) return TCR_ERR_CUDA;
+    const bool aligned = ((uintptr_t)x & 15u) == 0;
+    Plan p = make_plan(1, n, false, mode, block, R, aligned, dev);
+    return run_plan(p, (const uint16_t *)x, out, (cudaStream_t)stream, dev);
+}
+
+tcr_status tcr_reduce_rows(const void *x, size_t rows, size_t cols, float *out, tcr_mode mode,
+                           void *stream)
+{
+    if (mul_overflows(rows, cols)) return TCR_ERR_INVALID_ARG;
+    if (rows == 0) {
+        int block = 0, R = 0;
+        return check_mode(mode, &block, &R);
+    }
+    int block = 0, R = 0;
+    tcr_status st = check_common(x, rows * cols, out, mode, &block, &R);
+    if (st != TCR_OK) return st;
+    const int dev = current_device();
+    if (dev < 0) return TCR_ERR_CUDA;
+    const bool aligned = ((uintptr_t)x & 15u) == 0 && (cols % 8) == 0;
+    Plan p = make_plan(rows, cols, true, mode, block, R, aligned, dev);
+    return run_plan(p, (const uint16_t *)x, out, (cudaStream_t)stream, dev);
+}
+
+tcr_status tcr_order_descriptor(size_t n, size_t rows, size_t cols, tcr_mode mode,
+                                tcr_order_desc *desc)
+{
+    if (!desc) return TCR_ERR_INVALID_ARG;
+    int block = 0, R = 0;
+    tcr_status st = check_mode(mode, &block, &R);
+    if (st != TCR_OK) return st;
+    const bool rows_call = rows > 0;
+    if (rows_call && mul_overflows(rows, cols)) return TCR_ERR_INVALID_ARG;
+    const size_t segments = rows_call ? rows : 1;
+    const size_t seg_len = rows_call ? cols : n;
+    if (segments * seg_len >= kMaxInputs) return TCR_ERR_INVALID_ARG;
+    const int dev = current_device();
+    // the plan of an aligned input; a misaligned one differs only in speed
+    Plan p = make_plan(segments, seg_len, rows_call, mode, block, R, true, dev);
+    std::memset(desc, 0, sizeof *desc);
+    desc->kind = mode.kind;
+    desc->order = mode.kind == TCR_MMA_CHAIN      ? TCR_ORDER_TENSOR_CORE
+                  : mode.kind == TCR_SHUFFLE_TREE ? TCR_ORDER_GRID_STRIDE
+                                                  : TCR_ORDER_BALANCED_TREE;
+    desc->segment_len = seg_len;
+    desc->segments = segments;
+    desc->vector_len = 8;
+    desc->chain_R = mode.kind == TCR_MMA_CHAIN ? R : 0;
+    desc->pad_negative_zero = 1;
+    if (mode.kind == TCR_SHUFFLE_TREE) {
+        shuffle_team(seg_len, block, &desc->team_threads, &desc->team_blocks);
+    }
+    desc->launch_grid = p.grid;
+    desc->launch_block = p.path == kPathShuffleBlock ? p.team_threads : p.block;
+    desc->chunk_log2 = p.path == kPathChunk ? p.chunk_log2 : 0;
+    desc->partials = p.partials;
+    desc->launches = p.launches;
+    return TCR_OK;
+}
+
+const char *tcr_status_string(tcr_status status)
+{
+    switch (status) {
+    case TCR_OK: return "success";
+    case TCR_ERR_INVALID_ARG: return "invalid argument";
+    case TCR_ERR_UNSUPPORTED: return "unsupported request";
+    case TCR_ERR_CUDA: return "CUDA allocation or launch failure";
+    default: return "unknown status";
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,540 @@
+#!/usr/bin/env python3
+"""Reduction throughput on GB300: GB/s and fraction of measured HBM peak.
+
+One step is one pass of the whole reduction path over one batch of
+synthetic inputs resident in HBM:
+
+  x_sum  = 2^30 binary16 values, uniform on [-1, 1), seed 4     (2 GiB)
+  x_rows = 65536 x 4096 binary16 values, N(0, 1), seed 2        (512 MiB)
+  tcr_reduce_sum(x_sum)   in MMA_CHAIN, FIXED_ORDER, SHUFFLE_TREE
+  tcr_reduce_rows(x_rows) in MMA_CHAIN, FIXED_ORDER, SHUFFLE_TREE
+
+``value`` is the algorithmic bytes of a step (2 bytes read per input plus
+4 bytes written per result) times the steps of all ranks, over the slowest
+rank's device time (CUDA events on the launching stream).  Both inputs are
+far larger than the 129 MB L2, so no flush is needed between calls.
+
+``--impl reference`` times the CPU oracle instead (the reference arm),
+on a bounded sample of the same workload.  ``--sweep`` prints one line per
+(R, block) point of the MMA_CHAIN sweep on 2^28 values in [0, 1).
+Multi-GPU: every rank runs the same workload on its own GPU (replicas; the
+path has no exchange step), one process per GPU under torchrun.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "reduction GB/s and % of GB300 HBM peak (2^30 fp16 sum; 65536×4096 rows)"
+UNIT = "GB/s"
+N_SUM = 1 << 30
+ROWS, COLS = 65536, 4096
+WORKLOAD = "sum of 2^30 fp16 U[-1,1) seed 4 + rows 65536x4096 fp16 N(0,1) seed 2, all three modes"
+FALLBACK_HBM_GBS = 6800.0
+
+# kernel launched by each call (the first, reduction launch)
+KERNEL_OF = {
+    "sum/MMA_CHAIN": "mma_chunk_kernel",
+    "sum/FIXED_ORDER": "fixed_chunk_kernel",
+    "sum/SHUFFLE_TREE": "shuffle_block_kernel",
+    "rows/MMA_CHAIN": "mma_rows_kernel",
+    "rows/FIXED_ORDER": "fixed_rows_warp_kernel",
+    "rows/SHUFFLE_TREE": "shuffle_rows_warp_kernel",
+}
+
+
+# ------------------------------------------------------------ process setup
+
+def dist_info():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(world: int, backend: str):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend)
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    """The largest value over all ranks (the slowest rank's time)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def whole_job_gbps(bytes_per_step: float, steps: int, world: int, seconds: float) -> float:
+    """Aggregate GB/s of all ranks: every rank moves bytes_per_step per step."""
+    return bytes_per_step * steps * world / seconds / 1e9
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "arithmetic_reduction_tensor_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken
+    on the current kernel sources (a line 'traffic <kernel> <bytes> <hash>')."""
+    d = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(d):
+        return None
+    want = source_hash()
+    for name in sorted(os.listdir(d)):
+        if not name.endswith((".md", ".txt")):
+            continue
+        with open(os.path.join(d, name)) as f:
+            for line in f:
+                parts = line.strip().strip("`").split()
+                if len(parts) == 4 and parts[0] == "traffic" and parts[1] == kernel:
+                    if parts[3] == want:
+                        return float(parts[2])
+    return None
+
+
+# ------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled while the work runs."""
+    FIELDS = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        out = {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        if self.proc is None:
+            return out
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                p = [c.strip() for c in line.split(",")]
+                if len(p) < 10:
+                    continue
+                if self.uuid and self.uuid not in p[1]:
+                    continue
+                try:
+                    sm.append(float(p[2]))
+                    smax.append(float(p[3]))
+                except ValueError:
+                    continue
+                for name, flag in zip(names, p[6:10]):
+                    if flag.lower() == "active":
+                        reasons.add(name)
+        os.unlink(self.path)
+        if sm:
+            out = {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                   "reasons": sorted(reasons), "samples": len(sm)}
+        return out
+
+
+# ------------------------------------------------------------ workload
+
+def make_inputs(device):
+    import torch
+    from arithmetic_reduction_tensor_gb300 import synth
+    xs = synth.generate(N_SUM, "uniform_pm1", synth.F16, seed=4)
+    xr = synth.generate(ROWS * COLS, "normal", synth.F16, seed=2)
+    x_sum = torch.from_numpy(xs.view(np.int16)).to(device)
+    x_rows = torch.from_numpy(xr.view(np.int16)).to(device).view(ROWS, COLS)
+    return xs, xr, x_sum, x_rows
+
+
+def build_calls(x_sum, x_rows):
+    """[(name, fn(), algorithmic bytes, kernel launches)] for one step."""
+    import torch
+    import arithmetic_reduction_tensor_gb300 as tcr
+    dev = x_sum.device
+    outs = torch.empty(3 + 3 * ROWS, dtype=torch.float32, device=dev)
+    calls = []
+    for i, kind in enumerate((tcr.MMA_CHAIN, tcr.FIXED_ORDER, tcr.SHUFFLE_TREE)):
+        m = tcr.Mode(kind)
+        name = "sum/" + tcr.KIND_NAMES[kind]
+        o = outs[i:i + 1]
+        d = tcr.tcr_order_descriptor(n=N_SUM, mode=m)
+        calls.append((name, (lambda m=m, o=o: tcr.tcr_reduce_sum(x_sum, m, out=o)),
+                      2 * N_SUM + 4, d["launches"]))
+    for i, kind in enumerate((tcr.MMA_CHAIN, tcr.FIXED_ORDER, tcr.SHUFFLE_TREE)):
+        m = tcr.Mode(kind)
+        name = "rows/" + tcr.KIND_NAMES[kind]
+        o = outs[3 + i * ROWS:3 + (i + 1) * ROWS]
+        d = tcr.tcr_order_descriptor(rows=ROWS, cols=COLS, mode=m)
+        calls.append((name, (lambda m=m, o=o: tcr.tcr_reduce_rows(x_rows, m, out=o)),
+                      2 * ROWS * COLS + 4 * ROWS, d["launches"]))
+    return calls, outs
+
+
+def time_device(calls, steps: int, warmup: int, world: int):
+    import torch
+    for _ in range(warmup):
+        for _, fn, _, _ in calls:
+            fn()
+    stream = torch.cuda.current_stream()
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in calls] for _ in range(steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for s in range(steps):
+        for c, (_, fn, _, _) in enumerate(calls):
+            ev[s][c][0].record(stream)
+            fn()
+            ev[s][c][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    total_s = t0.elapsed_time(t1) / 1e3
+    per_call_ms = [[ev[s][c][0].elapsed_time(ev[s][c][1]) for s in range(steps)]
+                   for c in range(len(calls))]
+    return total_s, per_call_ms
+
+
+def time_e2e(xs, xr, calls_factory, steps: int, world: int):
+    """Each step: pinned host -> device copy of both inputs, the six calls,
+    device -> host copy of every result; CUDA events around all of it."""
+    import torch
+    dev = torch.device("cuda", torch.cuda.current_device())
+    h_sum = torch.from_numpy(xs.view(np.int16)).pin_memory()
+    h_rows = torch.from_numpy(xr.view(np.int16)).pin_memory()
+    d_sum = torch.empty_like(h_sum, device=dev)
+    d_rows = torch.empty_like(h_rows, device=dev).view(ROWS, COLS)
+    calls, outs = calls_factory(d_sum, d_rows)
+    h_out = torch.empty(outs.numel(), dtype=torch.float32).pin_memory()
+    stream = torch.cuda.current_stream()
+
+    def step():
+        d_sum.copy_(h_sum, non_blocking=True)
+        d_rows.view(-1).copy_(h_rows, non_blocking=True)
+        for _, fn, _, _ in calls:
+            fn()
+        h_out.copy_(outs, non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    barrier(world)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    h2d = h_sum.numel() * 2 + h_rows.numel() * 2
+    d2h = h_out.numel() * 4
+    return t0.elapsed_time(t1) / 1e3, h2d, d2h
+
+
+# ------------------------------------------------------------ CPU oracle
+
+def oracle_pass(xs_sample, xr_sample, threads: int):
+    """The oracle's work for one step of the workload, on a sample:
+    what each of the six calls is checked against."""
+    import oracle
+    from tests import spec
+    oracle.exact_sum(xs_sample, oracle.F16, threads)
+    oracle.fixed_order(xs_sample, oracle.F16, threads)
+    oracle.shuffle_tree(xs_sample, oracle.F16, *spec.shuffle_team(xs_sample.size), threads=threads)
+    oracle.exact_sum_rows(xr_sample, oracle.F16, threads)
+    oracle.fixed_order_rows(xr_sample, oracle.F16, threads)
+    oracle.shuffle_tree_rows(xr_sample, oracle.F16, *spec.shuffle_team(COLS), threads=threads)
+    return 3 * 2 * xs_sample.size + 3 * (2 * xr_sample.size + 4 * xr_sample.shape[0])
+
+
+def cpu_samples(xs, xr, budget_s: float, threads: int):
+    """Sizes the sample so one oracle pass takes about budget_s seconds."""
+    n0, r0 = 1 << 22, 1 << 10
+    t = time.perf_counter()
+    oracle_pass(xs[:n0], xr[:r0 * COLS].reshape(r0, COLS), threads)
+    dt = max(time.perf_counter() - t, 1e-3)
+    scale = max(1.0, budget_s / dt)
+    n = int(min(N_SUM, n0 * scale))
+    r = int(min(ROWS, r0 * scale))
+    return xs[:n], xr[:r * COLS].reshape(r, COLS)
+
+
+def cpu_baseline(xs, xr, budget_s: float = 10.0):
+    import oracle
+    threads = oracle.default_threads()
+    s, r = cpu_samples(xs, xr, budget_s, threads)
+    t = time.perf_counter()
+    nbytes = oracle_pass(s, r, threads)
+    dt = time.perf_counter() - t
+    return {"value": round(nbytes / dt / 1e9, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"first {s.size} of the 2^30 sum inputs and first {r.shape[0]} of the 65536 "
+                      f"rows; exact sum, fixed-order tree and shuffle-tree emulation of each",
+            "seconds": round(dt, 3)}
+
+
+# ------------------------------------------------------------ arms
+
+def reference_arm(args):
+    """The oracle timed as the reference arm, on a bounded sample per step."""
+    import oracle
+    from arithmetic_reduction_tensor_gb300 import synth
+    rank, world, _ = dist_info()
+    if rank != 0:
+        return 0
+    threads = oracle.default_threads()
+    budget = max(0.05, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
+    n_probe = 1 << 26
+    xs = synth.generate(n_probe, "uniform_pm1", synth.F16, seed=4)
+    xr = synth.generate(4096 * COLS, "normal", synth.F16, seed=2)
+    s, r = cpu_samples(xs, xr.reshape(-1), budget, threads)
+    for _ in range(args.warmup):
+        oracle_pass(s, r, threads)
+    t = time.perf_counter()
+    nbytes = 0
+    for _ in range(args.steps):
+        nbytes += oracle_pass(s, r, threads)
+    dt = time.perf_counter() - t
+    value = nbytes / dt / 1e9
+    sample = (f"per step: first {s.size} of the 2^30 sum inputs and first {r.shape[0]} of the "
+              f"65536 rows; exact sum, fixed-order tree and shuffle-tree emulation of each")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "sample": sample},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def sweep_arm(args):
+    """MMA_CHAIN R x block sweep against SHUFFLE_TREE on 2^28 values in [0, 1)."""
+    import torch
+    import arithmetic_reduction_tensor_gb300 as tcr
+    from arithmetic_reduction_tensor_gb300 import synth
+    torch.cuda.set_device(0)
+    n = 1 << 28
+    x = torch.from_numpy(synth.generate(n, "uniform01", synth.F16, seed=1).view(np.int16)).cuda()
+    out = torch.empty(1, dtype=torch.float32, device="cuda")
+    peak, _ = load_peaks()
+    points = [(tcr.SHUFFLE_TREE, 0, b) for b in (32, 128, 256, 1024)]
+    points += [(tcr.FIXED_ORDER, 0, b) for b in (32, 128, 256, 1024)]
+    points += [(tcr.MMA_CHAIN, R, b) for R in (1, 2, 4, 5) for b in (32, 128, 256, 1024)]
+    for kind, R, b in points:
+        m = tcr.Mode(kind, R=R, block_threads=b)
+        for _ in range(3):
+            tcr.tcr_reduce_sum(x, m, out=out)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(args.steps):
+            tcr.tcr_reduce_sum(x, m, out=out)
+        e1.record()
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / args.steps
+        gbps = 2 * n / us / 1e3
+        print(json.dumps({"sweep": "sum 2^28 fp16 U[0,1) seed 1", "kind": tcr.KIND_NAMES[kind],
+                          "R": R, "block": b, "us": round(us, 2), "gbps": round(gbps, 1),
+                          "frac": round(gbps / peak, 4)}), flush=True)
+    return 0
+
+
+def profile_arm(args):
+    """A small case for ncu: each sum mode once on 2^28 fp16 values (512 MiB,
+    larger than L2) and each rows mode once on 16384 x 4096 rows."""
+    import torch
+    import arithmetic_reduction_tensor_gb300 as tcr
+    from arithmetic_reduction_tensor_gb300 import synth
+    torch.cuda.set_device(0)
+    n = 1 << 28
+    x = torch.from_numpy(synth.generate(n, "uniform_pm1", synth.F16, seed=4).view(np.int16)).cuda()
+    r = torch.from_numpy(synth.generate(16384 * COLS, "normal", synth.F16, seed=2).view(np.int16))
+    r = r.cuda().view(16384, COLS)
+    for _ in range(args.steps):
+        for kind in (tcr.MMA_CHAIN, tcr.FIXED_ORDER, tcr.SHUFFLE_TREE):
+            tcr.tcr_reduce_sum(x, tcr.Mode(kind))
+            tcr.tcr_reduce_rows(r, tcr.Mode(kind))
+    torch.cuda.synchronize()
+    print("profile case done", flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["tcr", "reference"], default="tcr")
+    ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--profile-case", action="store_true",
+                    help="run the small ncu case (2^28 sum, 16384 x 4096 rows) and exit")
+    ap.add_argument("--e2e-steps", type=int, default=0, help="0: max(3, steps // 40)")
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    rank, world, local = dist_info()
+    if world != args.gpus:
+        if world == 1 and args.gpus > 1:
+            ap.error("--gpus N > 1 runs under torchrun, one process per GPU")
+    if args.impl == "reference":
+        return reference_arm(args)
+
+    import torch
+    import arithmetic_reduction_tensor_gb300 as tcr
+    from arithmetic_reduction_tensor_gb300.build import build_library
+
+    if args.sweep:
+        build_library()
+        return sweep_arm(args)
+    if args.profile_case:
+        build_library()
+        return profile_arm(args)
+
+    torch.cuda.set_device(local)
+    init_dist(world, "nccl")
+    build_library()
+    tcr.c_api()
+    device = torch.device("cuda", local)
+    xs, xr, x_sum, x_rows = make_inputs(device)
+    calls, _ = build_calls(x_sum, x_rows)
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(local).uuid)
+    except Exception:
+        pass
+    clocks = ClockSampler(uuid)
+    clocks.start()
+    total_s, per_call_ms = time_device(calls, args.steps, args.warmup, world)
+    e2e_steps = args.e2e_steps or max(3, args.steps // 40)
+    del x_sum, x_rows, calls
+    torch.cuda.empty_cache()
+    e2e_s, h2d, d2h = time_e2e(xs, xr, build_calls, e2e_steps, world)
+    clk = clocks.stop()
+
+    meta = build_calls_meta()
+    bytes_per_step = sum(m[1] for m in meta)
+    max_s = max_over_ranks(total_s, world)
+    max_e2e = max_over_ranks(e2e_s, world)
+    value = whole_job_gbps(bytes_per_step, args.steps, world, max_s)
+    e2e_value = whole_job_gbps(bytes_per_step, e2e_steps, world, max_e2e)
+    peak, peak_src = load_peaks()
+
+    calls_out = {}
+    for (name, nbytes, launches), ms in zip(meta, per_call_ms):
+        avg_us = statistics.fmean(ms) * 1e3
+        gbps = nbytes / avg_us / 1e3
+        calls_out[name] = {"us": round(avg_us, 2), "gbps": round(gbps, 1),
+                           "frac": round(gbps / peak, 4), "launches": launches}
+    dom = max(calls_out, key=lambda k: calls_out[k]["us"])
+    launches = sum(m[2] for m in meta) * args.steps
+
+    if rank != 0:
+        return 0
+    cpu = cpu_baseline(xs, xr, args.cpu_budget) if world == 1 else None
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(max_s / args.steps * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "l2": "inputs 2 GiB and 512 MiB, larger than L2; no flush",
+                   "input_dtype": "fp16", "accumulate": "fp32", "block_threads": 256,
+                   "mma_chain_R": tcr.tcr_order_descriptor(n=N_SUM, mode=tcr.Mode(tcr.MMA_CHAIN))["chain_R"]},
+        "frac_of_peak": round(value / world / peak, 4),
+        "peak_gbs": peak, "peak_source": peak_src,
+        "calls": calls_out,
+        "roofline": {"bound": "hbm", "kernel": KERNEL_OF[dom], "call": dom,
+                     "achieved": calls_out[dom]["gbps"], "peak": peak, "unit": "GB/s",
+                     "frac": calls_out[dom]["frac"], "traffic": recorded_traffic(KERNEL_OF[dom]),
+                     "duration": "whole call (reduction + combine launch)",
+                     "peak_source": peak_src},
+        "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": launches,
+        "clocks": clk,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def build_calls_meta():
+    """(name, algorithmic bytes, launches) of the six calls of a step."""
+    import arithmetic_reduction_tensor_gb300 as tcr
+    meta = []
+    for kind in (tcr.MMA_CHAIN, tcr.FIXED_ORDER, tcr.SHUFFLE_TREE):
+        d = tcr.tcr_order_descriptor(n=N_SUM, mode=tcr.Mode(kind))
+        meta.append(("sum/" + tcr.KIND_NAMES[kind], 2 * N_SUM + 4, d["launches"]))
+    for kind in (tcr.MMA_CHAIN, tcr.FIXED_ORDER, tcr.SHUFFLE_TREE):
+        d = tcr.tcr_order_descriptor(rows=ROWS, cols=COLS, mode=tcr.Mode(kind))
+        meta.append(("rows/" + tcr.KIND_NAMES[kind], 2 * ROWS * COLS + 4 * ROWS, d["launches"]))
+    return meta
+
+
+if __name__ == "__main__":
+    sys.exit(main())

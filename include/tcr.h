@@ -1,0 +1,206 @@
+/*
+ * tcr.h -- tensor-core and fixed-order sum reduction on one GB300 GPU.
+ *
+ * The operation is the one stated by "GPU Tensor Cores for fast Arithmetic
+ * Reductions" (arXiv 2001.05585), Abstract: the arithmetic reduction (sum)
+ * of n numbers into one 32-bit floating-point result.  Inputs are binary16
+ * or bfloat16; every result is binary32.  Three ways of computing it are
+ * offered (tcr_kind):
+ *
+ *   TCR_MMA_CHAIN     the page's method: the inputs are laid out as 16x16
+ *                     tiles and multiplied by an all-ones matrix on the tensor
+ *                     cores, R multiply-accumulates chained into one fp32
+ *                     accumulator; each chain's sub-result is then added, in
+ *                     fp32, into the final result (same Abstract: sub-results
+ *                     of each chain of R MMAs kept as 32-bit floats, then all
+ *                     reduced into a final 32-bit result).  The order inside
+ *                     the tensor core is the hardware's, so results are held
+ *                     to an error bound, not to bits:
+ *                     |result - exact| <= 2^-20 * sum|x_i| + 1e-6.
+ *   TCR_SHUFFLE_TREE  the conventional GPU reduction the same Abstract
+ *                     compares against, with its order declared (see
+ *                     tcr_order_desc): grid-stride accumulation of 8-input
+ *                     vectors, a warp butterfly, a tree over warps and a
+ *                     tree over blocks.  Bit-identical to the CPU emulation
+ *                     of that order.
+ *   TCR_FIXED_ORDER   a balanced binary tree over index order, padded with
+ *                     -0.0 to a power of two ("Taming Bitwise Behavior in
+ *                     GPU Kernels with Tensor Core", arXiv 2609.11356,
+ *                     Abstract: balanced-tree reduction, a descriptor of
+ *                     reduction order, one bit-equivalence class).  The result
+ *                     depends on the inputs and n only -- not on the launch
+ *                     configuration, the block size or the GPU -- and is
+ *                     bit-identical to the CPU emulation of that tree.
+ *
+ * All additions outside the tensor core are binary32, round to nearest
+ * even, with no fused multiply-add and no flushing of subnormals.
+ *
+ * Memory and streams.  x and out are device pointers owned by the caller.
+ * Calls are asynchronous on `stream` (a cudaStream_t; NULL means the legacy
+ * default stream): *out is valid once the stream reaches the point of the
+ * call.  A call that needs scratch memory takes it from a library-owned,
+ * stream-ordered pool on the current device (cudaMallocFromPoolAsync /
+ * cudaFreeAsync on `stream`), so concurrent calls on different streams do
+ * not share scratch.  The library keeps no other state between calls except
+ * per-device launch-plan caches.  Every call runs on the current device.
+ *
+ * Errors.  Invalid arguments return TCR_ERR_INVALID_ARG before any GPU work
+ * and leave *out untouched.  A CUDA error (allocation or launch) returns
+ * TCR_ERR_CUDA; the CUDA error itself is left to cudaGetLastError /
+ * cudaPeekAtLastError of the caller's runtime.
+ */
+#ifndef TCR_H
+#define TCR_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define TCR_API __attribute__((visibility("default")))
+#else
+#define TCR_API
+#endif
+
+typedef enum {
+    TCR_OK = 0,
+    TCR_ERR_INVALID_ARG = 1,   /* bad pointer, size, alignment or mode field */
+    TCR_ERR_UNSUPPORTED = 2,   /* well-formed request the library does not serve */
+    TCR_ERR_CUDA = 3           /* a CUDA allocation or launch failed */
+} tcr_status;
+
+typedef enum {
+    TCR_MMA_CHAIN = 0,
+    TCR_SHUFFLE_TREE = 1,
+    TCR_FIXED_ORDER = 2
+} tcr_kind;
+
+typedef enum {
+    TCR_F16 = 0,    /* IEEE 754 binary16 */
+    TCR_BF16 = 1    /* bfloat16: the upper 16 bits of a binary32 */
+} tcr_dtype;
+
+/*
+ * How to reduce.
+ *   kind           tcr_kind.
+ *   R              TCR_MMA_CHAIN only: tensor-core MMAs per chain, 1..8, or
+ *                  0 for the default of the block size (the Abstract of
+ *                  arXiv 2001.05585 finds R = 4 or 5 best for small thread
+ *                  blocks and R = 1 for large ones).  Ignored otherwise.
+ *   block_threads  threads per CTA: 0 for the default (256) or one of 32,
+ *                  64, 128, 256, 512, 1024.  For TCR_SHUFFLE_TREE it is part
+ *                  of the declared order; for TCR_FIXED_ORDER it changes
+ *                  only speed, never the result.
+ *   dtype          tcr_dtype of the inputs.
+ */
+typedef struct {
+    int kind;
+    int R;
+    int block_threads;
+    int dtype;
+} tcr_mode;
+
+/*
+ * tcr_reduce_sum -- out[0] = sum of x[0 .. n-1].
+ *   x       device pointer to n contiguous 16-bit inputs, 2-byte aligned (any
+ *           16-byte misalignment is served by a slower load path with the
+ *           same order).  May be NULL only when n == 0.
+ *   n       number of inputs, 0 <= n < 2^40.  n == 0 writes +0.0.
+ *   out     device pointer to one float, 4-byte aligned.
+ *   mode    see tcr_mode.
+ *   stream  cudaStream_t.
+ * Launches one reduction kernel and, when it leaves more than one partial,
+ * one combine kernel on the same stream; the partials live in pool scratch
+ * of 4 bytes per partial (tcr_order_descriptor reports the count).
+ */
+TCR_API tcr_status tcr_reduce_sum(const void *x, size_t n, float *out, tcr_mode mode, void *stream);
+
+/*
+ * tcr_reduce_rows -- out[r] = sum of x[r*cols .. r*cols + cols-1], r < rows.
+ *   x       device pointer to a row-major rows x cols matrix of 16-bit inputs
+ *           (row stride = cols), 2-byte aligned.  May be NULL only when
+ *           rows * cols == 0.
+ *   rows    number of rows (0 does nothing); cols: inputs per row (0 writes
+ *           +0.0 to every out[r]).  rows * cols < 2^40.
+ *   out     device pointer to rows floats, 4-byte aligned.
+ * Each row is reduced exactly as tcr_reduce_sum would reduce it alone for
+ * TCR_FIXED_ORDER and TCR_SHUFFLE_TREE (the order depends on cols only, never
+ * on rows: results are batch invariant).  Short rows need no scratch and one
+ * launch; long rows use per-row partials and a combine launch.
+ */
+TCR_API tcr_status tcr_reduce_rows(const void *x, size_t rows, size_t cols, float *out, tcr_mode mode,
+                           void *stream);
+
+/* Declared reduction orders (tcr_order_desc.order). */
+typedef enum {
+    TCR_ORDER_TENSOR_CORE = 0,      /* MMA_CHAIN: inner order is the tensor core's */
+    TCR_ORDER_GRID_STRIDE = 1,      /* SHUFFLE_TREE: see tcr_order_desc */
+    TCR_ORDER_BALANCED_TREE = 2     /* FIXED_ORDER: balanced tree over index order */
+} tcr_order;
+
+/*
+ * The order a call reduces in, and how it is launched -- what the CPU
+ * emulation needs to reproduce a result bit for bit (the descriptor of
+ * reduction order of arXiv 2609.11356, Abstract, restated for 1-D sums and
+ * rows).
+ *
+ *   order            tcr_order.
+ *   segment_len      inputs per reduced segment (n, or cols).
+ *   segments         number of results (1, or rows).
+ *   vector_len       inputs per vector leaf group (8).
+ *   team_threads     SHUFFLE_TREE: threads per block Bt of the team that
+ *                    reduces one segment (32 means one warp per segment).
+ *   team_blocks      SHUFFLE_TREE: blocks G per segment.  Thread g = b*Bt + t
+ *                    accumulates vectors g, g + G*Bt, g + 2*G*Bt, ... into an
+ *                    fp32 value that starts at -0.0; a warp combines its lanes
+ *                    by the butterfly with offsets 16, 8, 4, 2, 1 (lane i adds
+ *                    lane i^offset); a block is the balanced tree over its
+ *                    warps; a segment is the balanced tree over its G blocks,
+ *                    padded with -0.0.  A vector's value is the balanced tree
+ *                    over its 8 inputs, missing inputs being -0.0.
+ *   chain_R          MMA_CHAIN: MMAs per chain (after defaults).
+ *   pad_negative_zero 1: padding inputs and absent subtrees are -0.0.
+ *   launch_grid, launch_block, chunk_log2, partials, launches
+ *                    the launch plan of the first (reduction) kernel, the
+ *                    inputs per CTA work unit (log2; 0 if not chunked), the
+ *                    number of fp32 partials written to scratch (0 if none)
+ *                    and the number of kernel launches.  For FIXED_ORDER they
+ *                    never change the result.
+ */
+typedef struct {
+    int kind;
+    int order;
+    size_t segment_len;
+    size_t segments;
+    int vector_len;
+    int team_threads;
+    int team_blocks;
+    int chain_R;
+    int pad_negative_zero;
+    int launch_grid;
+    int launch_block;
+    int chunk_log2;
+    size_t partials;
+    int launches;
+} tcr_order_desc;
+
+/*
+ * tcr_order_descriptor -- fill *desc for the call tcr_reduce_sum(n) when
+ * rows == 0, or tcr_reduce_rows(rows, cols) when rows > 0 (n is then
+ * ignored).  Host only; queries the current device's SM count for the
+ * launch plan.  Returns TCR_ERR_INVALID_ARG for the same arguments the
+ * reduction would reject.
+ */
+TCR_API tcr_status tcr_order_descriptor(size_t n, size_t rows, size_t cols, tcr_mode mode,
+                                tcr_order_desc *desc);
+
+/* Static English text for a status code; never NULL. */
+TCR_API const char *tcr_status_string(tcr_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TCR_H */

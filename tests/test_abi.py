@@ -1,0 +1,137 @@
+"""The C ABI without a GPU: the library loads, exports every entry point
+``include/tcr.h`` declares, rejects bad arguments before any GPU work and
+describes the declared orders."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import arithmetic_reduction_tensor_gb300 as tcr
+from arithmetic_reduction_tensor_gb300.build import build_library, LIB_PATH
+from tests import spec
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_library()
+    return tcr.c_api()
+
+
+def declared_entry_points():
+    names = []
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if h.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", h)).read()
+            names += re.findall(r"TCR_API\s+[\w\s\*]+?\b(tcr_\w+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_entry_points()
+    for n in ("tcr_reduce_sum", "tcr_reduce_rows", "tcr_order_descriptor", "tcr_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (tcr_\w+)", out))
+    assert set(declared_entry_points()) <= exported
+    # nothing else of ours leaks out of the shared object
+    assert {s for s in exported if s.startswith("tcr")} == set(declared_entry_points())
+    for n in declared_entry_points():
+        assert hasattr(lib, n)
+
+
+def test_status_strings(lib):
+    for st in range(4):
+        assert isinstance(tcr.tcr_status_string(st), str) and tcr.tcr_status_string(st)
+    assert tcr.tcr_status_string(99) == "unknown status"
+
+
+FAKE = 0x7F0000000000      # never dereferenced: every case below fails validation
+
+
+@pytest.mark.parametrize("args", [
+    # (x, n, out, mode)
+    (FAKE, 10, None, tcr.Mode(tcr.FIXED_ORDER)),                 # out NULL
+    (FAKE, 10, FAKE + 2, tcr.Mode(tcr.FIXED_ORDER)),             # out misaligned
+    (None, 10, FAKE, tcr.Mode(tcr.FIXED_ORDER)),                 # x NULL with n > 0
+    (FAKE + 1, 10, FAKE, tcr.Mode(tcr.FIXED_ORDER)),             # x not 2-byte aligned
+    (FAKE, 1 << 40, FAKE, tcr.Mode(tcr.FIXED_ORDER)),            # n too large
+    (FAKE, 10, FAKE, tcr.Mode(7)),                               # unknown kind
+    (FAKE, 10, FAKE, tcr.Mode(tcr.FIXED_ORDER, dtype=5)),        # unknown dtype
+    (FAKE, 10, FAKE, tcr.Mode(tcr.MMA_CHAIN, R=9)),              # R out of range
+    (FAKE, 10, FAKE, tcr.Mode(tcr.MMA_CHAIN, R=-1)),
+    (FAKE, 10, FAKE, tcr.Mode(tcr.SHUFFLE_TREE, block_threads=48)),   # not a power of two
+    (FAKE, 10, FAKE, tcr.Mode(tcr.SHUFFLE_TREE, block_threads=2048)),
+    (FAKE, 10, FAKE, tcr.Mode(tcr.SHUFFLE_TREE, block_threads=16)),
+])
+def test_sum_rejects_bad_arguments_before_gpu_work(lib, args):
+    x, n, out, mode = args
+    assert lib.tcr_reduce_sum(x, n, out, mode, None) == tcr.ERR_INVALID_ARG
+
+
+def test_rows_rejects_bad_arguments(lib):
+    m = tcr.Mode(tcr.FIXED_ORDER)
+    assert lib.tcr_reduce_rows(FAKE, 1 << 21, 1 << 21, FAKE, m, None) == tcr.ERR_INVALID_ARG
+    assert lib.tcr_reduce_rows(FAKE, 1 << 40, 1 << 40, FAKE, m, None) == tcr.ERR_INVALID_ARG
+    assert lib.tcr_reduce_rows(FAKE, 3, 5, None, m, None) == tcr.ERR_INVALID_ARG
+    assert lib.tcr_reduce_rows(FAKE, 3, 5, FAKE, tcr.Mode(tcr.MMA_CHAIN, R=11), None) == \
+        tcr.ERR_INVALID_ARG
+    # no rows: nothing to do, any pointers
+    assert lib.tcr_reduce_rows(None, 0, 5, None, m, None) == tcr.OK
+
+
+def test_descriptor_rejects_bad_arguments(lib):
+    d = tcr.tcr_order_desc()
+    assert lib.tcr_order_descriptor(10, 0, 0, tcr.Mode(9), ctypes.byref(d)) == tcr.ERR_INVALID_ARG
+    assert lib.tcr_order_descriptor(10, 0, 0, tcr.Mode(0), None) == tcr.ERR_INVALID_ARG
+    assert lib.tcr_order_descriptor(1 << 40, 0, 0, tcr.Mode(0), ctypes.byref(d)) == \
+        tcr.ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("L", [1, 100, 8192, 8193, 10_000, 1 << 20, 1 << 28, 1 << 30])
+@pytest.mark.parametrize("block", [0, 32, 128, 1024])
+def test_shuffle_descriptor_matches_the_declared_rule(lib, L, block):
+    m = tcr.Mode(tcr.SHUFFLE_TREE, block_threads=block)
+    bt, g = spec.shuffle_team(L, block)
+    for d in (tcr.tcr_order_descriptor(n=L, mode=m), tcr.tcr_order_descriptor(rows=3, cols=L, mode=m)):
+        assert d["order"] == tcr.ORDER_GRID_STRIDE
+        assert (d["team_threads"], d["team_blocks"]) == (bt, g)
+        assert d["vector_len"] == 8 and d["pad_negative_zero"] == 1
+        assert d["partials"] == (0 if g == 1 else d["segments"] * g)
+
+
+def test_fixed_descriptor_is_the_balanced_tree(lib):
+    for blk in (32, 256, 1024):
+        d = tcr.tcr_order_descriptor(n=(1 << 30) + 5, mode=tcr.Mode(tcr.FIXED_ORDER, block_threads=blk))
+        assert d["order"] == tcr.ORDER_BALANCED_TREE and d["segments"] == 1
+        assert d["chunk_log2"] == 13 + {32: 0, 256: 3, 1024: 5}[blk]
+        assert d["partials"] == -(-((1 << 30) + 5) // (1 << d["chunk_log2"]))
+        assert d["launches"] == 2
+
+
+def test_mma_descriptor_defaults_R_by_block(lib):
+    for blk in (32, 64, 128, 256, 512, 1024):
+        d = tcr.tcr_order_descriptor(n=1 << 20, mode=tcr.Mode(tcr.MMA_CHAIN, block_threads=blk))
+        assert d["chain_R"] == spec.default_R(blk)
+        assert d["order"] == tcr.ORDER_TENSOR_CORE
+    d = tcr.tcr_order_descriptor(n=1 << 20, mode=tcr.Mode(tcr.MMA_CHAIN, R=5))
+    assert d["chain_R"] == 5
+
+
+def test_rows_descriptor_short_rows_need_no_scratch(lib):
+    for kind in (tcr.FIXED_ORDER, tcr.MMA_CHAIN, tcr.SHUFFLE_TREE):
+        d = tcr.tcr_order_descriptor(rows=65536, cols=4096, mode=tcr.Mode(kind))
+        assert d["partials"] == 0 and d["launches"] == 1 and d["segments"] == 65536
+
+
+def test_python_binding_fails_loudly_without_cuda_tensors():
+    torch = pytest.importorskip("torch")
+    with pytest.raises(ValueError):
+        tcr.tcr_reduce_sum(torch.zeros(4, dtype=torch.float16), tcr.Mode(tcr.FIXED_ORDER))
