@@ -104,11 +104,21 @@ def load_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def source_hash() -> str:
+# source file of each kernel; a recorded DRAM traffic figure is stale once
+# that file or the shared device headers change
+KERNEL_SOURCE = {
+    "mma_chunk_kernel": "k_mma.cu", "mma_rows_kernel": "k_mma.cu",
+    "fixed_chunk_kernel": "k_fixed.cu", "fixed_rows_warp_kernel": "k_fixed.cu",
+    "shuffle_block_kernel": "k_shuffle.cu", "shuffle_rows_warp_kernel": "k_shuffle.cu",
+    "combine_kernel": "k_combine.cu",
+}
+
+
+def source_hash(kernel: str) -> str:
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "arithmetic_reduction_tensor_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in ("common.cuh", "kernels.cuh", KERNEL_SOURCE[kernel]):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
@@ -120,7 +130,7 @@ def recorded_traffic(kernel: str):
     d = os.path.join(ROOT, "profiles")
     if not os.path.isdir(d):
         return None
-    want = source_hash()
+    want = source_hash(kernel)
     for name in sorted(os.listdir(d)):
         if not name.endswith((".md", ".txt")):
             continue
@@ -166,28 +176,34 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as f:
-            for line in f:
-                p = [c.strip() for c in line.split(",")]
-                if len(p) < 10:
-                    continue
-                if self.uuid and self.uuid not in p[1]:
-                    continue
-                try:
-                    sm.append(float(p[2]))
-                    smax.append(float(p[3]))
-                except ValueError:
-                    continue
-                for name, flag in zip(names, p[6:10]):
-                    if flag.lower() == "active":
-                        reasons.add(name)
+            lines = f.readlines()
         os.unlink(self.path)
-        if sm:
-            out = {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
-                   "reasons": sorted(reasons), "samples": len(sm)}
+        return parse_clock_csv(lines, self.uuid) or out
         return out
+
+
+def parse_clock_csv(lines, uuid=None):
+    """Median SM clock, max clock and the throttle reasons seen, from
+    nvidia-smi CSV lines (noheader, nounits) of ClockSampler.FIELDS."""
+    sm, smax, reasons = [], [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for line in lines:
+        p = [c.strip() for c in line.split(",")]
+        if len(p) < 10 or (uuid and uuid not in p[1]):
+            continue
+        try:
+            sm.append(float(p[2]))
+            smax.append(float(p[3]))
+        except ValueError:
+            continue
+        for name, flag in zip(names, p[6:10]):
+            if flag.lower() == "active":
+                reasons.add(name)
+    if not sm:
+        return None
+    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+            "reasons": sorted(reasons), "samples": len(sm)}
 
 
 # ------------------------------------------------------------ workload
