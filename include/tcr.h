@@ -133,6 +133,36 @@ TCR_API tcr_status tcr_reduce_sum(const void *x, size_t n, float *out, tcr_mode 
 TCR_API tcr_status tcr_reduce_rows(const void *x, size_t rows, size_t cols, float *out, tcr_mode mode,
                            void *stream);
 
+/*
+ * tcr_reduce_sum_noalloc -- tcr_reduce_sum for callers that must not
+ * allocate device memory while they run: a service that reserved its whole
+ * device-memory budget at start-up and treats any later allocation as a
+ * fault, code running while another component owns the device allocator,
+ * or a host thread with a deadline that cannot wait for the allocator.
+ * The pages have no counterpart to this entry point; it is an interface
+ * choice of this library.
+ *
+ * Same arguments and results as tcr_reduce_sum (caller-owned x and out),
+ * but the partials live in one fixed array of 65536 floats (256 KiB) in
+ * device memory, held by every GPU that loads the library until the
+ * process exits; no cudaMalloc, cudaFree or other allocating call is made.
+ *   - Serves TCR_FIXED_ORDER and TCR_MMA_CHAIN; TCR_SHUFFLE_TREE returns
+ *     TCR_ERR_UNSUPPORTED.
+ *   - n is limited to 65536 chunks of 2^(13 + log2(block_threads / 32))
+ *     inputs (2^32 inputs at the default 256 threads, 2^29 at 32); a larger
+ *     n returns TCR_ERR_UNSUPPORTED before any GPU work.
+ *   - The first call on each device looks up the array's device address
+ *     with that device current; make that first call before any stream
+ *     capture.
+ *   - All calls on a device share the array, which keeps the last call's
+ *     contents (nothing needs clearing: each call writes every partial it
+ *     reads).  Calls that overlap on the GPU race on it: order them on one
+ *     stream or with events.
+ * Results are the same as tcr_reduce_sum's for the same mode.
+ */
+TCR_API tcr_status tcr_reduce_sum_noalloc(const void *x, size_t n, float *out, tcr_mode mode,
+                                          void *stream);
+
 /* Declared reduction orders (tcr_order_desc.order). */
 typedef enum {
     TCR_ORDER_TENSOR_CORE = 0,      /* MMA_CHAIN: inner order is the tensor core's */
