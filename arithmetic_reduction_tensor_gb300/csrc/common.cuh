@@ -85,15 +85,37 @@ __device__ __forceinline__ float leaf_hi(uint32_t w)
     }
 }
 
+// The sum of the two inputs packed in a 32-bit word, low + high, binary32
+// round to nearest.  For bfloat16 the two leaves (word << 16 and
+// word & 0xffff0000) are formed and added in one asm statement, which keeps
+// the compiler from hoisting the unpacking of many words at once: the
+// kernels that hold a group of loads in flight fit their register budget.
+template <int DT>
+__device__ __forceinline__ float pair_sum(uint32_t w)
+{
+    if constexpr (DT == kF16) {
+        return __fadd_rn(leaf_lo<DT>(w), leaf_hi<DT>(w));
+    } else {
+        float r;
+        asm("{\n\t.reg .b32 lo, hi;\n\t"
+            "shl.b32 lo, %1, 16;\n\t"
+            "and.b32 hi, %1, 0xffff0000;\n\t"
+            "add.rn.f32 %0, lo, hi;\n\t}"
+            : "=f"(r)
+            : "r"(w));
+        return r;
+    }
+}
+
 // Balanced tree over the 8 inputs of a vector:
 // ((e0 + e1) + (e2 + e3)) + ((e4 + e5) + (e6 + e7)).
 template <int DT>
 __device__ __forceinline__ float tree8(uint4 q)
 {
-    float p0 = __fadd_rn(leaf_lo<DT>(q.x), leaf_hi<DT>(q.x));
-    float p1 = __fadd_rn(leaf_lo<DT>(q.y), leaf_hi<DT>(q.y));
-    float p2 = __fadd_rn(leaf_lo<DT>(q.z), leaf_hi<DT>(q.z));
-    float p3 = __fadd_rn(leaf_lo<DT>(q.w), leaf_hi<DT>(q.w));
+    const float p0 = pair_sum<DT>(q.x);
+    const float p1 = pair_sum<DT>(q.y);
+    const float p2 = pair_sum<DT>(q.z);
+    const float p3 = pair_sum<DT>(q.w);
     return __fadd_rn(__fadd_rn(p0, p1), __fadd_rn(p2, p3));
 }
 
@@ -113,13 +135,18 @@ struct TreeCounter {
 
     __device__ __forceinline__ void push(float v)
     {
+        // carry up through the levels whose bit of count is set: the new
+        // value is the right sibling of the subtree stored there
+        bool carry = true;
 #pragma unroll
         for (int l = 0; l < LEVELS; l++) {
-            if ((count >> l) & 1u) {
-                v = __fadd_rn(s[l], v);        // left sibling + right sibling
-            } else {
-                s[l] = v;
-                break;
+            if (carry) {
+                if ((count >> l) & 1u) {
+                    v = __fadd_rn(s[l], v);        // left sibling + right sibling
+                } else {
+                    s[l] = v;
+                    carry = false;
+                }
             }
         }
         count++;
@@ -172,6 +199,22 @@ __device__ __forceinline__ void mma_ones(float &d0, float &d1, float &d2, float 
             : "+f"(d0), "+f"(d1), "+f"(d2), "+f"(d3)
             : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(one2), "r"(one2));
     }
+}
+
+// ---------------------------------------------------------------- PDL
+
+// Programmatic dependent launch: a producing kernel lets the next kernel
+// on the stream start launching; the consumer waits until the producer has
+// completed and its writes are visible.  Both are no-ops for a kernel
+// launched without the attribute.
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_wait_primary()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 __host__ __device__ __forceinline__ int ceil_log2_sz(size_t n)

@@ -11,38 +11,41 @@
 //   a warp combines its lanes by the butterfly with offsets 16, 8, 4, 2, 1;
 //   a block is the balanced tree over its warps; the segment is the
 //   balanced tree over its G blocks (the combine kernel, when G > 1).
-#include "common.cuh"
-#include "kernels.cuh"
+#include "stream.cuh"
 
 namespace tcr {
 
 constexpr int kShuffleUnroll = 8;    // vectors in flight per thread
 
-__device__ __forceinline__ float warp_butterfly_16_to_1(float acc)
-{
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(kFull, acc, off));
-    return acc;
-}
-
-// Thread value: -0.0 + vector(first) + vector(first + stride) + ... in
-// order.  A vector index past nvec contributes -0.0, the identity.
+// Block team: thread value = -0.0 + vector(first) + vector(first + stride)
+// + ... in order, a vector being its 8-input tree; vectors past the
+// segment are -0.0, the identity.  Software-pipelined: the next 8 vectors
+// are loaded before the current 8 are added.
 template <int DT, bool ALIGNED>
 __device__ __forceinline__ float grid_stride_acc(const uint16_t *seg, size_t len, size_t first,
                                                  size_t stride)
 {
     const size_t nvec = (len + 7) / 8;
+    const uint4 pad = make_uint4(kNegZero2, kNegZero2, kNegZero2, kNegZero2);
+    uint4 q[kShuffleUnroll];
+#pragma unroll
+    for (int u = 0; u < kShuffleUnroll; u++) {
+        const size_t v = first + (size_t)u * stride;
+        q[u] = v < nvec ? ld_vec<ALIGNED>(seg, len, v, 0x8000u) : pad;
+    }
     float acc = -0.0f;
     for (size_t v0 = first; v0 < nvec; v0 += kShuffleUnroll * stride) {
-        uint4 q[kShuffleUnroll];
+        float t[kShuffleUnroll];
+#pragma unroll
+        for (int u = 0; u < kShuffleUnroll; u++) t[u] = tree8<DT>(q[u]);
+        const size_t n0 = v0 + kShuffleUnroll * stride;
 #pragma unroll
         for (int u = 0; u < kShuffleUnroll; u++) {
-            size_t v = v0 + (size_t)u * stride;
-            q[u] = v < nvec ? ld_vec<ALIGNED>(seg, len, v, 0x8000u)
-                            : make_uint4(kNegZero2, kNegZero2, kNegZero2, kNegZero2);
+            const size_t v = n0 + (size_t)u * stride;
+            q[u] = v < nvec ? ld_vec<ALIGNED>(seg, len, v, 0x8000u) : pad;
         }
 #pragma unroll
-        for (int u = 0; u < kShuffleUnroll; u++) acc = __fadd_rn(acc, tree8<DT>(q[u]));
+        for (int u = 0; u < kShuffleUnroll; u++) acc = __fadd_rn(acc, t[u]);
     }
     return acc;
 }
@@ -59,7 +62,9 @@ shuffle_block_kernel(const uint16_t *__restrict__ x, size_t seg_len, int G,
     const uint16_t *seg = x + s * seg_len;
     const size_t stride = (size_t)G * blockDim.x;
     float acc = grid_stride_acc<DT, ALIGNED>(seg, seg_len, b * blockDim.x + threadIdx.x, stride);
-    acc = warp_butterfly_16_to_1(acc);
+    pdl_launch_dependents();
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(kFull, acc, off));
     if (lane == 0) warp_val[warp] = acc;
     __syncthreads();
     if (warp == 0) {
@@ -68,19 +73,14 @@ shuffle_block_kernel(const uint16_t *__restrict__ x, size_t seg_len, int G,
     }
 }
 
+// Warp team (Bt = 32, G = 1): one warp per segment; the warp stream's
+// group order visits lane j's vectors j, j+32, j+64, ... in order.
 template <int DT, bool ALIGNED>
-__global__ void __launch_bounds__(1024)
+__global__ void __launch_bounds__(kRowsBlock, kRowsMinCtas)
 shuffle_rows_warp_kernel(const uint16_t *__restrict__ x, size_t rows, size_t cols,
                          float *__restrict__ out)
 {
-    const int lane = threadIdx.x & 31;
-    const size_t gw = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const size_t nw = ((size_t)gridDim.x * blockDim.x) >> 5;
-    for (size_t r = gw; r < rows; r += nw) {
-        float acc = grid_stride_acc<DT, ALIGNED>(x + r * cols, cols, (size_t)lane, 32);
-        acc = warp_butterfly_16_to_1(acc);
-        if (lane == 0) out[r] = acc;
-    }
+    rows_body<ShuffleReducer<DT>, ALIGNED>(x, rows, cols, out);
 }
 
 // ---------------------------------------------------------------- host

@@ -14,9 +14,13 @@ namespace tcr {
 constexpr size_t kGroup = 2048;
 // Inputs per warp of one CTA work unit (chunk) of the chunked kernels.
 constexpr int kWarpSpanLog2 = 13;
-// Longest row served by one warp (tree kernels) or one 16-row warp tile
-// (tensor-core rows kernel); longer rows go through the chunked kernels.
+// Longest row served by one warp; longer rows go through the chunked
+// kernels (FIXED_ORDER, MMA_CHAIN) or the block team (SHUFFLE_TREE).
 constexpr size_t kRowsWarpMaxCols = 16384;
+// CTA size of the one-warp-per-row kernels, and the CTAs per SM their
+// register budget is set for (65536 / (256 * 3) -> up to 80 registers).
+constexpr int kRowsBlock = 256;
+constexpr int kRowsMinCtas = 3;
 
 // ---- FIXED_ORDER (balanced tree over index order)
 // Chunked: CTA work unit u = (segment u / cps, chunk u % cps); the chunk of
@@ -45,7 +49,7 @@ cudaError_t launch_shuffle_rows_warp(int dtype, bool aligned, const uint16_t *x,
 cudaError_t launch_mma_chunk(int dtype, bool aligned, int R, const uint16_t *x, size_t seg_len,
                              size_t units, size_t cps, int chunk_log2, float *dst, int grid,
                              int block, cudaStream_t stream);
-// One warp per 16 consecutive rows, rows <= kRowsWarpMaxCols inputs long.
+// One warp per row, rows <= kRowsWarpMaxCols inputs long.
 cudaError_t launch_mma_rows(int dtype, bool aligned, int R, const uint16_t *x, size_t rows,
                             size_t cols, float *out, int grid, int block, cudaStream_t stream);
 

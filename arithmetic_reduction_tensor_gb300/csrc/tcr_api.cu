@@ -128,7 +128,7 @@ enum Path {
     kPathEmpty,          // nothing to reduce: memset out to +0.0
     kPathChunk,          // FIXED / MMA chunked kernel (+ combine if cps > 1)
     kPathFixedRowsWarp,  // FIXED, one warp per row
-    kPathMmaRows,        // MMA, one warp per 16 rows
+    kPathMmaRows,        // MMA, one warp per row
     kPathShuffleBlock,   // SHUFFLE block team (+ combine if G > 1)
     kPathShuffleRowsWarp // SHUFFLE warp team, one warp per row
 };
@@ -153,14 +153,14 @@ int log2_exact(int v)
     return l;
 }
 
-// Default chain length by block size, from the Abstract of arXiv
-// 2001.05585 (R = 4 or 5 for 32- and 128-thread blocks, R = 1 for large
-// ones).
-int default_R(int block)
+// Default chain length.  The Abstract of arXiv 2001.05585 finds R = 4 or 5
+// best for 32- and 128-thread blocks and R = 1 for large ones; on GB300 the
+// sum of 2^28 values is fastest at R = 4 for every block size (R = 1 and 2
+// flush more often and hold more live registers), so R = 4 is the default
+// throughout.
+int default_R(int)
 {
-    if (block <= 128) return 4;
-    if (block <= 256) return 2;
-    return 1;
+    return 4;
 }
 
 // The declared SHUFFLE_TREE team for a segment of L inputs at block size B:
@@ -236,7 +236,7 @@ Plan make_plan(size_t segments, size_t seg_len, bool rows_call, const tcr_mode &
         if (p.team_threads == 32 && p.team_blocks == 1) {
             // a team of one warp: pack one segment per warp, 8 per CTA
             p.path = kPathShuffleRowsWarp;
-            p.block = kDefaultBlock;
+            p.block = kRowsBlock;
             const size_t warps_per_cta = (size_t)p.block / 32;
             const size_t need = (segments + warps_per_cta - 1) / warps_per_cta;
             const size_t resident =
@@ -254,9 +254,11 @@ Plan make_plan(size_t segments, size_t seg_len, bool rows_call, const tcr_mode &
     }
     const Family fam = m.kind == TCR_FIXED_ORDER ? kFixedF : kMmaF;
     if (rows_call && seg_len <= kRowsWarpMaxCols) {
+        // one warp per row: the CTA size is a launch detail (the result does
+        // not depend on it), fixed at kRowsBlock threads
+        p.block = block = kRowsBlock;
         const size_t warps_per_cta = (size_t)block / 32;
-        size_t work_warps = m.kind == TCR_FIXED_ORDER ? segments : (segments + 15) / 16;
-        const size_t need = (work_warps + warps_per_cta - 1) / warps_per_cta;
+        const size_t need = (segments + warps_per_cta - 1) / warps_per_cta;
         const size_t resident = sms * (size_t)occupancy(dev, fam, true, p.dtype, aligned, R, block);
         p.path = m.kind == TCR_FIXED_ORDER ? kPathFixedRowsWarp : kPathMmaRows;
         p.grid = (int)(need < resident ? need : resident);

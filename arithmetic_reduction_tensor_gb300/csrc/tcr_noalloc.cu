@@ -95,7 +95,7 @@ extern "C" tcr_status tcr_reduce_sum_noalloc(const void *x, size_t n, float *out
     int R = 0;
     if (mode.kind == TCR_MMA_CHAIN) {
         if (mode.R < 0 || mode.R > 8) return TCR_ERR_INVALID_ARG;
-        R = mode.R != 0 ? mode.R : (block <= 128 ? 4 : (block <= 256 ? 2 : 1));
+        R = mode.R != 0 ? mode.R : 4;    // the same default as tcr_reduce_sum
     } else if (mode.kind == TCR_SHUFFLE_TREE) {
         return TCR_ERR_UNSUPPORTED;
     } else if (mode.kind != TCR_FIXED_ORDER) {

@@ -49,7 +49,7 @@ KERNEL_OF = {
     "sum/MMA_CHAIN": "mma_chunk_kernel",
     "sum/FIXED_ORDER": "fixed_chunk_kernel",
     "sum/SHUFFLE_TREE": "shuffle_block_kernel",
-    "rows/MMA_CHAIN": "mma_rows_kernel",
+    "rows/MMA_CHAIN": "mma_rows_warp_kernel",
     "rows/FIXED_ORDER": "fixed_rows_warp_kernel",
     "rows/SHUFFLE_TREE": "shuffle_rows_warp_kernel",
 }
@@ -107,7 +107,7 @@ def load_peaks():
 # source file of each kernel; a recorded DRAM traffic figure is stale once
 # that file or the shared device headers change
 KERNEL_SOURCE = {
-    "mma_chunk_kernel": "k_mma.cu", "mma_rows_kernel": "k_mma.cu",
+    "mma_chunk_kernel": "k_mma.cu", "mma_rows_warp_kernel": "k_mma.cu",
     "fixed_chunk_kernel": "k_fixed.cu", "fixed_rows_warp_kernel": "k_fixed.cu",
     "shuffle_block_kernel": "k_shuffle.cu", "shuffle_rows_warp_kernel": "k_shuffle.cu",
     "combine_kernel": "k_combine.cu",
@@ -118,7 +118,7 @@ def source_hash(kernel: str) -> str:
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "arithmetic_reduction_tensor_gb300", "csrc")
-    for f in ("common.cuh", "kernels.cuh", KERNEL_SOURCE[kernel]):
+    for f in ("common.cuh", "kernels.cuh", "stream.cuh", KERNEL_SOURCE[kernel]):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
@@ -420,15 +420,15 @@ def sweep_arm(args):
 
 def profile_arm(args):
     """A small case for ncu: each sum mode once on 2^28 fp16 values (512 MiB,
-    larger than L2) and each rows mode once on 16384 x 4096 rows."""
+    larger than L2) and each rows mode once on 32768 x 4096 rows (256 MiB)."""
     import torch
     import arithmetic_reduction_tensor_gb300 as tcr
     from arithmetic_reduction_tensor_gb300 import synth
     torch.cuda.set_device(0)
     n = 1 << 28
     x = torch.from_numpy(synth.generate(n, "uniform_pm1", synth.F16, seed=4).view(np.int16)).cuda()
-    r = torch.from_numpy(synth.generate(16384 * COLS, "normal", synth.F16, seed=2).view(np.int16))
-    r = r.cuda().view(16384, COLS)
+    r = torch.from_numpy(synth.generate(32768 * COLS, "normal", synth.F16, seed=2).view(np.int16))
+    r = r.cuda().view(32768, COLS)
     for _ in range(args.steps):
         for kind in (tcr.MMA_CHAIN, tcr.FIXED_ORDER, tcr.SHUFFLE_TREE):
             tcr.tcr_reduce_sum(x, tcr.Mode(kind))
@@ -446,7 +446,7 @@ def main():
     ap.add_argument("--impl", choices=["tcr", "reference"], default="tcr")
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--profile-case", action="store_true",
-                    help="run the small ncu case (2^28 sum, 16384 x 4096 rows) and exit")
+                    help="run the small ncu case (2^28 sum, 32768 x 4096 rows) and exit")
     ap.add_argument("--e2e-steps", type=int, default=0, help="0: max(3, steps // 40)")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     args = ap.parse_args()

@@ -86,9 +86,10 @@ typedef enum {
  * How to reduce.
  *   kind           tcr_kind.
  *   R              TCR_MMA_CHAIN only: tensor-core MMAs per chain, 1..8, or
- *                  0 for the default of the block size (the Abstract of
- *                  arXiv 2001.05585 finds R = 4 or 5 best for small thread
- *                  blocks and R = 1 for large ones).  Ignored otherwise.
+ *                  0 for the default, 4 (the Abstract of arXiv 2001.05585
+ *                  finds R = 4 or 5 best for small thread blocks and R = 1
+ *                  for large ones; on GB300 R = 4 is fastest at every block
+ *                  size).  Ignored otherwise.
  *   block_threads  threads per CTA: 0 for the default (256) or one of 32,
  *                  64, 128, 256, 512, 1024.  For TCR_SHUFFLE_TREE it is part
  *                  of the declared order; for TCR_FIXED_ORDER it changes

@@ -21,10 +21,8 @@ def shuffle_team(L: int, block: int = 0) -> tuple[int, int]:
 
 
 def default_R(block: int = 0) -> int:
-    """MMA chain length by block size (R = 4 for blocks up to 128 threads,
-    2 at 256, 1 above)."""
-    B = block or DEFAULT_BLOCK
-    return 4 if B <= 128 else (2 if B <= 256 else 1)
+    """Default MMA chain length: 4 at every block size."""
+    return 4
 
 
 def mma_tolerance(abs_sum: float) -> float:
