@@ -96,3 +96,24 @@ def test_sum_2p30_f16_fixed_order_ten_runs():
     assert_within_mma_tolerance(run_sum(t, tcr.Mode(tcr.MMA_CHAIN)), exact, abs_sum)
     assert same_bits(run_sum(t, tcr.Mode(tcr.SHUFFLE_TREE)),
                      oracle.shuffle_tree(x, F16, *spec.shuffle_team(x.size)))
+
+
+def test_sum_past_2p32_inputs():
+    """The largest case: 2^32 + 1000 binary16 inputs (8 GiB), so every index
+    and pointer offset of the kernels runs past 32 bits."""
+    n = (1 << 32) + 1000
+    x = synth.generate(n, "uniform_pm1", F16, seed=5)
+    t = to_dev(x)
+    assert same_bits(run_sum(t, tcr.Mode(tcr.FIXED_ORDER)), oracle.fixed_order(x, F16))
+    assert same_bits(run_sum(t, tcr.Mode(tcr.SHUFFLE_TREE)),
+                     oracle.shuffle_tree(x, F16, *spec.shuffle_team(n)))
+    exact, abs_sum = oracle.exact_sum(x, F16)
+    assert_within_mma_tolerance(run_sum(t, tcr.Mode(tcr.MMA_CHAIN)), exact, abs_sum)
+    # the first 2^32 inputs as 65536 rows of 65536: long rows through the
+    # chunked kernels, row offsets past 2^32 bytes
+    rows, cols = 65536, 65536
+    xr = t[:rows * cols].view(rows, cols)
+    got = tcr.tcr_reduce_rows(xr, tcr.Mode(tcr.FIXED_ORDER)).cpu().numpy()
+    sel = [0, 1, 32768, 65534, 65535]
+    ref = np.array([oracle.fixed_order(x[r * cols:(r + 1) * cols], F16, threads=1) for r in sel])
+    assert same_bits(got[sel], ref)
