@@ -23,19 +23,20 @@ import threading
 from .build import LIB_PATH
 
 __all__ = [
-    "MMA_CHAIN", "SHUFFLE_TREE", "FIXED_ORDER", "F16", "BF16",
+    "MMA_CHAIN", "SHUFFLE_TREE", "FIXED_ORDER", "MMA_CHAIN_TMEM", "F16", "BF16",
     "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_CUDA",
     "ORDER_TENSOR_CORE", "ORDER_GRID_STRIDE", "ORDER_BALANCED_TREE",
     "tcr_mode", "tcr_order_desc", "Mode", "TcrError", "c_api",
     "tcr_reduce_sum", "tcr_reduce_rows", "tcr_order_descriptor", "tcr_status_string",
 ]
 
-MMA_CHAIN, SHUFFLE_TREE, FIXED_ORDER = 0, 1, 2
+MMA_CHAIN, SHUFFLE_TREE, FIXED_ORDER, MMA_CHAIN_TMEM = 0, 1, 2, 3
 F16, BF16 = 0, 1
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA = 0, 1, 2, 3
 ORDER_TENSOR_CORE, ORDER_GRID_STRIDE, ORDER_BALANCED_TREE = 0, 1, 2
 
-KIND_NAMES = {MMA_CHAIN: "MMA_CHAIN", SHUFFLE_TREE: "SHUFFLE_TREE", FIXED_ORDER: "FIXED_ORDER"}
+KIND_NAMES = {MMA_CHAIN: "MMA_CHAIN", SHUFFLE_TREE: "SHUFFLE_TREE", FIXED_ORDER: "FIXED_ORDER",
+              MMA_CHAIN_TMEM: "MMA_CHAIN_TMEM"}
 
 
 class tcr_mode(ctypes.Structure):

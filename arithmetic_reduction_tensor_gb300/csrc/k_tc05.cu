@@ -1,0 +1,433 @@
+// k_tc05.cu -- MMA_CHAIN on the fifth-generation tensor cores (tcgen05):
+// inputs staged into shared memory by bulk asynchronous copies, tensor-core
+// MMAs against an all-ones matrix issued by one thread, the accumulator in
+// tensor memory (TMEM).
+//
+// The method is that of "GPU Tensor Cores for fast Arithmetic Reductions"
+// (arXiv 2001.05585), Abstract: the sum of n numbers as chains of m x m
+// MMAs; each chain of R MMAs keeps its sub-result in 32-bit floating point
+// and the sub-results are then reduced into one 32-bit result.  Here one
+// MMA is tcgen05.mma.cta_group::1.kind::f16 with M = 128, N = 16, K = 16:
+// A is a 4 KiB tile of 2048 inputs (128 rows x 16), B is 16 x 16 ones, so
+// every column of the 128 x 16 fp32 D holds the 128 row sums.  Since B is
+// all ones the sum of column 0 is the sum of the tile whatever element sits
+// in whatever slot, so a contiguous 4 KiB of input is a valid A tile as it
+// lies in memory: no layout transform, no swizzle.
+//
+// CTA roles (192 threads, one persistent CTA per SM):
+//   warp 0, lane 0   producer: 32 KiB bulk copies (8 tiles) global -> a
+//                    4-stage shared-memory ring, completion by mbarrier
+//                    transaction count;
+//   warp 1           owns the TMEM allocation; lane 0 issues the MMAs:
+//                    R per chain into one of two D buffers, the first of a
+//                    chain without accumulate, tcgen05.commit after a chain
+//                    (D full) and after a stage (stage free);
+//   warps 2..5       epilogue: each thread reads its TMEM lane of column 0
+//                    of a full D buffer, adds it to its fp32 accumulator and
+//                    frees the buffer; at the end of a work unit (2^16
+//                    inputs) the 128 accumulators and any tail inputs past
+//                    the last whole tile are reduced into the unit's partial.
+//
+// Every wait on an mbarrier gives up after about one second: the CTA then
+// raises a device-wide fault flag, drains its own copies and MMAs (again
+// with a limit), frees its TMEM and writes NaN as its partials, so a broken
+// pipeline shows up as a NaN result, never as a hang.
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace tcr {
+
+constexpr int kTcTileInputs = 2048;                 // one MMA: 128 x 16 inputs
+constexpr int kTcTileBytes = kTcTileInputs * 2;     // 4 KiB
+constexpr int kTcTilesPerStage = 8;                 // 32 KiB bulk copies
+constexpr int kTcStageBytes = kTcTileBytes * kTcTilesPerStage;
+constexpr int kTcStages = 4;                        // 128 KiB in flight per SM
+constexpr int kTcUnitLog2 = 16;                     // work unit: 2^16 inputs
+constexpr int kTcTilesPerUnit = (1 << kTcUnitLog2) / kTcTileInputs;   // 32
+constexpr int kTcThreads = 192;
+constexpr int kTcEpilogueThreads = 128;
+constexpr uint32_t kTcTmemCols = 128;               // D buffers at columns 0 and 64
+constexpr uint32_t kTcDBufferStride = 64;
+constexpr uint64_t kWaitLimitNs = 1000000000ull;    // about one second
+
+// Dynamic shared memory layout (offsets from a 1024-byte aligned base).
+constexpr int kTcOffRing = 0;
+constexpr int kTcOffOnes = kTcOffRing + kTcStages * kTcStageBytes;     // 512 B of ones
+constexpr int kTcOffBars = kTcOffOnes + 1024;
+// barriers: full[S], empty[S], dfull[2], dempty[2], drain
+constexpr int kTcNumBars = 2 * kTcStages + 5;
+constexpr int kTcOffMisc = kTcOffBars + 8 * kTcNumBars;                 // tmem addr, abort, red[4]
+constexpr int kTcSmemBytes = kTcOffMisc + 64 + 1024;                    // + alignment slack
+
+__device__ unsigned int g_tc05_fault;               // non-zero once any wait gave up
+
+// ---------------------------------------------------------------- PTX
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ uint64_t global_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase of parity `parity` of `bar` to complete, giving up
+// after about a second (or at once when another role already gave up).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile uint32_t *abort)
+{
+    const uint64_t t0 = global_ns();
+    for (;;) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort) return false;
+        if (global_ns() - t0 > kWaitLimitNs) {
+            *abort = 1u;
+            atomicOr(&g_tc05_fault, 1u);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void *src, uint32_t bytes,
+                                              uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor, no swizzle, K-major: 8-row x 16-byte
+// core matrices; lbo = byte step between core matrices along K, sbo = byte
+// step between 8-row groups; bits 46..48 hold the fixed value 0b001.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo)
+{
+    return (uint64_t)((addr >> 4) & 0x3fffu) | ((uint64_t)((lbo >> 4) & 0x3fffu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3fffu) << 32) | (1ull << 46);
+}
+
+// Instruction descriptor of kind::f16: D fp32 (bits 4-5 = 1), A and B
+// binary16 (0) or bfloat16 (1) in bits 7-9 and 10-12, both K-major, N >> 3
+// in bits 17-22, M >> 4 in bits 24-28.
+template <int DT>
+__device__ __forceinline__ uint32_t instr_desc()
+{
+    constexpr uint32_t ab = DT == kF16 ? 0u : 1u;
+    return (1u << 4) | (ab << 7) | (ab << 10) | ((16u >> 3) << 17) | ((128u >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive once on `bar` when every tcgen05 operation this thread issued so
+// far has completed.
+__device__ __forceinline__ void tc_commit(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ float tc_ld_lane(uint32_t taddr)
+{
+    uint32_t v;
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(v) : "r"(taddr) : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+    return __uint_as_float(v);
+}
+
+__device__ __forceinline__ void named_sync(uint32_t id, uint32_t threads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// ---------------------------------------------------------------- kernel
+
+// Work unit u covers inputs [u * 2^16, min(n, (u+1) * 2^16)); its whole
+// 2048-input tiles go through the tensor cores, the inputs past the last
+// whole tile of the array (fewer than 2048) are added by the epilogue.
+__device__ __forceinline__ int unit_tiles(size_t n, size_t u)
+{
+    const size_t base = u << kTcUnitLog2;
+    const size_t left = n - base;
+    const size_t t = left / kTcTileInputs;
+    return (int)(t < (size_t)kTcTilesPerUnit ? t : (size_t)kTcTilesPerUnit);
+}
+
+template <int DT, int R>
+__global__ void __launch_bounds__(kTcThreads, 1)
+mma_tmem_kernel(const uint16_t *__restrict__ x, size_t n, size_t units, float *__restrict__ dst)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const uint32_t sbase = smem_addr(smem);
+    const uint32_t ring = sbase + kTcOffRing;
+    const uint32_t ones = sbase + kTcOffOnes;
+    const uint32_t bars = sbase + kTcOffBars;
+    auto full_bar = [&](int s) { return bars + 8u * (uint32_t)s; };
+    auto empty_bar = [&](int s) { return bars + 8u * (uint32_t)(kTcStages + s); };
+    auto dfull_bar = [&](int b) { return bars + 8u * (uint32_t)(2 * kTcStages + b); };
+    auto dempty_bar = [&](int b) { return bars + 8u * (uint32_t)(2 * kTcStages + 2 + b); };
+    const uint32_t drain_bar = bars + 8u * (uint32_t)(2 * kTcStages + 4);
+    uint32_t *misc = (uint32_t *)(smem + kTcOffMisc);
+    volatile uint32_t *tmem_holder = misc;
+    volatile uint32_t *abort = misc + 1;
+    float *red = (float *)(misc + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // ones matrix B (16 x 16 inputs, 512 bytes), barriers, flags
+    {
+        const uint32_t one2 = DT == kF16 ? 0x3c003c00u : 0x3f803f80u;
+        uint32_t *o = (uint32_t *)(smem + kTcOffOnes);
+        for (int i = threadIdx.x; i < 128; i += blockDim.x) o[i] = one2;
+    }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kTcStages; s++) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; b++) {
+            mbar_init(dfull_bar(b), 1);
+            mbar_init(dempty_bar(b), kTcEpilogueThreads);
+        }
+        mbar_init(drain_bar, 1);
+        *abort = 0u;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    // make the generic-proxy writes (ones, barriers) visible to the async proxy
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(smem_addr((const void *)tmem_holder)), "r"(kTcTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == 0) {
+        // ---------------- producer
+        if (lane == 0) {
+            int s = 0;
+            uint32_t phase = 0;
+            bool armed[kTcStages];
+            uint32_t armed_phase[kTcStages];
+#pragma unroll
+            for (int i = 0; i < kTcStages; i++) {
+                armed[i] = false;
+                armed_phase[i] = 0;
+            }
+            for (size_t u = blockIdx.x; u < units && !*abort; u += gridDim.x) {
+                const int tiles = unit_tiles(n, u);
+                const uint16_t *src = x + (u << kTcUnitLog2);
+                for (int t0 = 0; t0 < tiles; t0 += kTcTilesPerStage) {
+                    const int nt = min(kTcTilesPerStage, tiles - t0);
+                    if (!mbar_wait(empty_bar(s), phase ^ 1u, abort)) break;
+                    const uint32_t bytes = (uint32_t)nt * kTcTileBytes;
+                    mbar_arrive_expect_tx(full_bar(s), bytes);
+                    bulk_copy_g2s(ring + (uint32_t)s * kTcStageBytes, src + (size_t)t0 * kTcTileInputs,
+                                  bytes, full_bar(s));
+                    armed[s] = true;
+                    armed_phase[s] = phase;
+                    if (++s == kTcStages) {
+                        s = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (*abort) {
+                // let the copies already issued land before the CTA exits
+#pragma unroll
+                for (int i = 0; i < kTcStages; i++) {
+                    if (!armed[i]) continue;
+                    const uint64_t t0 = global_ns();
+                    while (!mbar_try_wait(full_bar(i), armed_phase[i]) &&
+                           global_ns() - t0 < kWaitLimitNs) {
+                    }
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---------------- MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = instr_desc<DT>();
+            const uint64_t b_desc = smem_desc(ones, 128, 256);
+            int s = 0, b = 0;
+            uint32_t phase = 0, dphase[2] = {0u, 0u};
+            for (size_t u = blockIdx.x; u < units && !*abort; u += gridDim.x) {
+                const int tiles = unit_tiles(n, u);
+                int in_chain = 0;
+                for (int t0 = 0; t0 < tiles && !*abort; t0 += kTcTilesPerStage) {
+                    const int nt = min(kTcTilesPerStage, tiles - t0);
+                    if (!mbar_wait(full_bar(s), phase, abort)) break;
+                    tc_fence_after();
+                    const uint32_t stage = ring + (uint32_t)s * kTcStageBytes;
+                    for (int t = 0; t < nt; t++) {
+                        if (in_chain == 0) {
+                            // the chain's D buffer must have been read out
+                            if (!mbar_wait(dempty_bar(b), dphase[b] ^ 1u, abort)) break;
+                            tc_fence_after();
+                        }
+                        const uint64_t a_desc = smem_desc(stage + (uint32_t)t * kTcTileBytes, 128, 256);
+                        tc_mma(tmem + (uint32_t)b * kTcDBufferStride, a_desc, b_desc, idesc,
+                               in_chain > 0 ? 1u : 0u);
+                        ++in_chain;
+                        const bool last_of_unit = t0 + t + 1 == tiles;
+                        if (in_chain == R || last_of_unit) {
+                            tc_commit(dfull_bar(b));          // chain sub-result ready
+                            dphase[b] ^= 1u;
+                            b ^= 1;
+                            in_chain = 0;
+                        }
+                    }
+                    tc_commit(empty_bar(s));                  // stage may be refilled
+                    if (++s == kTcStages) {
+                        s = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // every MMA issued has completed once the drain barrier flips
+            tc_commit(drain_bar);
+            const uint64_t t0 = global_ns();
+            while (!mbar_try_wait(drain_bar, 0u) && global_ns() - t0 < kWaitLimitNs) {
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---------------- epilogue: warps 2..5, TMEM lanes 32*(warp%4) ..
+        const int et = threadIdx.x - 64;                   // 0..127
+        const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+        int b = 0;
+        uint32_t dphase[2] = {0u, 0u};
+        for (size_t u = blockIdx.x; u < units; u += gridDim.x) {
+            const int tiles = unit_tiles(n, u);
+            const int chains = (tiles + R - 1) / R;
+            float acc = 0.f;
+            for (int c = 0; c < chains && !*abort; c++) {
+                if (!mbar_wait(dfull_bar(b), dphase[b], abort)) break;
+                tc_fence_after();
+                const float v = tc_ld_lane(tmem + lane_base + (uint32_t)b * kTcDBufferStride);
+                acc = __fadd_rn(acc, v);
+                tc_fence_before();
+                mbar_arrive(dempty_bar(b));
+                dphase[b] ^= 1u;
+                b ^= 1;
+            }
+            // inputs of this unit past its whole tiles (only in the last unit)
+            const size_t base = u << kTcUnitLog2;
+            const size_t tail_lo = base + (size_t)tiles * kTcTileInputs;
+            size_t tail_hi = base + ((size_t)1 << kTcUnitLog2);
+            if (tail_hi > n) tail_hi = n;
+            for (size_t i = tail_lo + (size_t)et; i < tail_hi; i += kTcEpilogueThreads)
+                acc = __fadd_rn(acc, DT == kF16 ? leaf_lo<kF16>(__ldg(x + i)) : leaf_lo<kBF16>(__ldg(x + i)));
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(kFull, acc, off));
+            if (lane == 0) red[warp - 2] = acc;
+            named_sync(1, kTcEpilogueThreads);
+            if (et == 0) {
+                float v = __fadd_rn(__fadd_rn(red[0], red[1]), __fadd_rn(red[2], red[3]));
+                dst[u] = *abort ? __int_as_float(0x7fc00000) : v;
+            }
+            named_sync(1, kTcEpilogueThreads);
+        }
+    }
+
+    pdl_launch_dependents();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kTcTmemCols)
+                     : "memory");
+    }
+}
+
+// ---------------------------------------------------------------- host
+
+template <int DT>
+static void *pick_dt(int R)
+{
+    switch (R) {
+    case 1: return (void *)mma_tmem_kernel<DT, 1>;
+    case 2: return (void *)mma_tmem_kernel<DT, 2>;
+    case 3: return (void *)mma_tmem_kernel<DT, 3>;
+    case 4: return (void *)mma_tmem_kernel<DT, 4>;
+    case 5: return (void *)mma_tmem_kernel<DT, 5>;
+    case 6: return (void *)mma_tmem_kernel<DT, 6>;
+    case 7: return (void *)mma_tmem_kernel<DT, 7>;
+    case 8: return (void *)mma_tmem_kernel<DT, 8>;
+    default: return nullptr;
+    }
+}
+
+size_t tmem_units(size_t n)
+{
+    return (n + ((size_t)1 << kTcUnitLog2) - 1) >> kTcUnitLog2;
+}
+
+int tmem_block_threads() { return kTcThreads; }
+
+int tmem_unit_log2() { return kTcUnitLog2; }
+
+cudaError_t launch_mma_tmem(int dtype, int R, const uint16_t *x, size_t n, float *dst, int grid,
+                            cudaStream_t stream)
+{
+    void *k = dtype == kF16 ? pick_dt<kF16>(R) : pick_dt<kBF16>(R);
+    if (!k) return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmemBytes);
+    if (e != cudaSuccess) return e;
+    size_t units = tmem_units(n);
+    void *args[] = {(void *)&x, (void *)&n, (void *)&units, (void *)&dst};
+    return cudaLaunchKernel(k, dim3(grid), dim3(kTcThreads), args, kTcSmemBytes, stream);
+}
+
+}  // namespace tcr

@@ -53,6 +53,15 @@ cudaError_t launch_mma_chunk(int dtype, bool aligned, int R, const uint16_t *x, 
 cudaError_t launch_mma_rows(int dtype, bool aligned, int R, const uint16_t *x, size_t rows,
                             size_t cols, float *out, int grid, int block, cudaStream_t stream);
 
+// ---- MMA_CHAIN on tcgen05 (bulk copies into shared memory, D in TMEM):
+// one persistent CTA per SM; dst[u] is the partial of work unit u (2^16
+// inputs, see tmem_unit_log2); x must be 16-byte aligned.
+cudaError_t launch_mma_tmem(int dtype, int R, const uint16_t *x, size_t n, float *dst, int grid,
+                            cudaStream_t stream);
+size_t tmem_units(size_t n);
+int tmem_block_threads();
+int tmem_unit_log2();
+
 // ---- combine: out[s] = balanced tree over partials[s*count .. s*count+count-1]
 // padded with -0.0; one CTA of 1024 threads per segment.
 cudaError_t launch_combine(const float *partials, size_t segments, size_t count, float *out,

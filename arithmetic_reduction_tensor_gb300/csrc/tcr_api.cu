@@ -130,7 +130,8 @@ enum Path {
     kPathFixedRowsWarp,  // FIXED, one warp per row
     kPathMmaRows,        // MMA, one warp per row
     kPathShuffleBlock,   // SHUFFLE block team (+ combine if G > 1)
-    kPathShuffleRowsWarp // SHUFFLE warp team, one warp per row
+    kPathShuffleRowsWarp, // SHUFFLE warp team, one warp per row
+    kPathTmem            // MMA_CHAIN on tcgen05 (+ combine if units > 1)
 };
 
 struct Plan {
@@ -184,12 +185,12 @@ void shuffle_team(size_t L, int B, int *Bt, int *G)
 
 tcr_status check_mode(const tcr_mode &m, int *block, int *R)
 {
-    if (m.kind < TCR_MMA_CHAIN || m.kind > TCR_FIXED_ORDER) return TCR_ERR_INVALID_ARG;
+    if (m.kind < TCR_MMA_CHAIN || m.kind > TCR_MMA_CHAIN_TMEM) return TCR_ERR_INVALID_ARG;
     if (m.dtype != TCR_F16 && m.dtype != TCR_BF16) return TCR_ERR_INVALID_ARG;
     int b = m.block_threads == 0 ? kDefaultBlock : m.block_threads;
     if (b < 32 || b > 1024 || (b & (b - 1)) != 0) return TCR_ERR_INVALID_ARG;
     int r = 0;
-    if (m.kind == TCR_MMA_CHAIN) {
+    if (m.kind == TCR_MMA_CHAIN || m.kind == TCR_MMA_CHAIN_TMEM) {
         if (m.R < 0 || m.R > 8) return TCR_ERR_INVALID_ARG;
         r = m.R == 0 ? default_R(b) : m.R;
     }
@@ -252,6 +253,19 @@ Plan make_plan(size_t segments, size_t seg_len, bool rows_call, const tcr_mode &
         }
         return p;
     }
+    if (m.kind == TCR_MMA_CHAIN_TMEM && aligned) {
+        // one persistent CTA per SM (its shared-memory ring fills the SM)
+        p.path = kPathTmem;
+        p.block = tmem_block_threads();
+        p.chunk_log2 = tmem_unit_log2();
+        p.units = tmem_units(seg_len);
+        p.cps = p.units;
+        p.grid = (int)(p.units < sms ? p.units : sms);
+        p.partials = p.units > 1 ? p.units : 0;
+        p.combine_count = p.units;
+        p.launches = p.units > 1 ? 2 : 1;
+        return p;
+    }
     const Family fam = m.kind == TCR_FIXED_ORDER ? kFixedF : kMmaF;
     if (rows_call && seg_len <= kRowsWarpMaxCols) {
         // one warp per row: the CTA size is a launch detail (the result does
@@ -298,6 +312,9 @@ tcr_status run_plan(const Plan &p, const uint16_t *x, float *out, cudaStream_t s
     float *dst = partials ? partials : out;
     cudaError_t e = cudaSuccess;
     switch (p.path) {
+    case kPathTmem:
+        e = launch_mma_tmem(p.dtype, p.R, x, p.seg_len, dst, p.grid, s);
+        break;
     case kPathChunk:
         e = p.kind == TCR_FIXED_ORDER
                 ? launch_fixed_chunk(p.dtype, p.aligned, x, p.seg_len, p.units, p.cps,
@@ -375,6 +392,7 @@ tcr_status tcr_reduce_rows(const void *x, size_t rows, size_t cols, float *out, 
     int block = 0, R = 0;
     tcr_status st = check_common(x, rows * cols, out, mode, &block, &R);
     if (st != TCR_OK) return st;
+    if (mode.kind == TCR_MMA_CHAIN_TMEM) return TCR_ERR_UNSUPPORTED;
     const int dev = current_device();
     if (dev < 0) return TCR_ERR_CUDA;
     const bool aligned = ((uintptr_t)x & 15u) == 0 && (cols % 8) == 0;
@@ -394,25 +412,26 @@ tcr_status tcr_order_descriptor(size_t n, size_t rows, size_t cols, tcr_mode mod
     const size_t segments = rows_call ? rows : 1;
     const size_t seg_len = rows_call ? cols : n;
     if (segments * seg_len >= kMaxInputs) return TCR_ERR_INVALID_ARG;
+    if (rows_call && mode.kind == TCR_MMA_CHAIN_TMEM) return TCR_ERR_UNSUPPORTED;
     const int dev = current_device();
     // the plan of an aligned input; a misaligned one differs only in speed
     Plan p = make_plan(segments, seg_len, rows_call, mode, block, R, true, dev);
     std::memset(desc, 0, sizeof *desc);
     desc->kind = mode.kind;
-    desc->order = mode.kind == TCR_MMA_CHAIN      ? TCR_ORDER_TENSOR_CORE
-                  : mode.kind == TCR_SHUFFLE_TREE ? TCR_ORDER_GRID_STRIDE
-                                                  : TCR_ORDER_BALANCED_TREE;
+    desc->order = mode.kind == TCR_SHUFFLE_TREE  ? TCR_ORDER_GRID_STRIDE
+                  : mode.kind == TCR_FIXED_ORDER ? TCR_ORDER_BALANCED_TREE
+                                                 : TCR_ORDER_TENSOR_CORE;
     desc->segment_len = seg_len;
     desc->segments = segments;
     desc->vector_len = 8;
-    desc->chain_R = mode.kind == TCR_MMA_CHAIN ? R : 0;
+    desc->chain_R = (mode.kind == TCR_MMA_CHAIN || mode.kind == TCR_MMA_CHAIN_TMEM) ? R : 0;
     desc->pad_negative_zero = 1;
     if (mode.kind == TCR_SHUFFLE_TREE) {
         shuffle_team(seg_len, block, &desc->team_threads, &desc->team_blocks);
     }
     desc->launch_grid = p.grid;
     desc->launch_block = p.path == kPathShuffleBlock ? p.team_threads : p.block;
-    desc->chunk_log2 = p.path == kPathChunk ? p.chunk_log2 : 0;
+    desc->chunk_log2 = (p.path == kPathChunk || p.path == kPathTmem) ? p.chunk_log2 : 0;
     desc->partials = p.partials;
     desc->launches = p.launches;
     return TCR_OK;

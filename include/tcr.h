@@ -23,6 +23,15 @@
  *                     vectors, a warp butterfly, a tree over warps and a
  *                     tree over blocks.  Bit-identical to the CPU emulation
  *                     of that order.
+ *   TCR_MMA_CHAIN_TMEM  the same method on the fifth-generation tensor cores:
+ *                     inputs staged into shared memory by bulk asynchronous
+ *                     copies, tcgen05.mma (M = 128, N = 16, K = 16; one MMA
+ *                     per 2048 inputs) with the accumulator in tensor memory,
+ *                     R MMAs per chain, chain sub-results read out to fp32
+ *                     registers.  Same error bound as TCR_MMA_CHAIN.  Sums
+ *                     only (tcr_reduce_rows returns TCR_ERR_UNSUPPORTED);
+ *                     an x that is not 16-byte aligned is reduced by the
+ *                     TCR_MMA_CHAIN kernel instead.
  *   TCR_FIXED_ORDER   a balanced binary tree over index order, padded with
  *                     -0.0 to a power of two ("Taming Bitwise Behavior in
  *                     GPU Kernels with Tensor Core", arXiv 2609.11356,
@@ -74,7 +83,8 @@ typedef enum {
 typedef enum {
     TCR_MMA_CHAIN = 0,
     TCR_SHUFFLE_TREE = 1,
-    TCR_FIXED_ORDER = 2
+    TCR_FIXED_ORDER = 2,
+    TCR_MMA_CHAIN_TMEM = 3
 } tcr_kind;
 
 typedef enum {

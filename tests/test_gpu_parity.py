@@ -273,3 +273,48 @@ def test_fault_injection_leaves_out_untouched(what, monkeypatch):
     st = lib.tcr_reduce_sum(x.data_ptr(), x.numel(), out.data_ptr(), tcr.Mode(tcr.FIXED_ORDER),
                             torch.cuda.current_stream().cuda_stream)
     assert st == tcr.OK and out.item() != 42.0
+
+
+# ------------------------------------------------------------ MMA_CHAIN on tcgen05
+
+TMEM_SIZES = [1, 7, 2047, 2048, 2049, 16384, 16385, 65535, 65536, 65537, 200_000,
+              1 << 20, (1 << 22) + 2047, (1 << 24) + 13]
+
+
+@pytest.mark.parametrize("dtype", [F16, BF16])
+@pytest.mark.parametrize("n", TMEM_SIZES)
+@pytest.mark.parametrize("R", [0, 1, 5, 8])
+def test_mma_chain_tmem_sum_within_tolerance(dtype, n, R):
+    x = inputs(n, dtype, "uniform01")
+    got = gpu_sum(x, tcr.Mode(tcr.MMA_CHAIN_TMEM, R=R, dtype=dtype))
+    assert_within_mma_tolerance(got, *oracle.exact_sum(x, dtype))
+
+
+def test_mma_chain_tmem_signed_inputs_and_stability():
+    x = inputs(3_000_017, BF16, "pow2", seed=3)
+    t = dev(x)
+    first = tcr.tcr_reduce_sum(t, tcr.Mode(tcr.MMA_CHAIN_TMEM, dtype=BF16)).cpu().numpy()
+    assert_within_mma_tolerance(first[0], *oracle.exact_sum(x, BF16))
+    for _ in range(5):
+        again = tcr.tcr_reduce_sum(t, tcr.Mode(tcr.MMA_CHAIN_TMEM, dtype=BF16)).cpu().numpy()
+        assert same_bits(again, first)
+
+
+def test_mma_chain_tmem_misaligned_and_rows():
+    x = inputs(100_003, F16)
+    t = dev(x)[3:]                      # not 16-byte aligned: served by the mma.sync kernel
+    got = np.float32(tcr.tcr_reduce_sum(t, tcr.Mode(tcr.MMA_CHAIN_TMEM)).cpu().numpy()[0])
+    assert_within_mma_tolerance(got, *oracle.exact_sum(x[3:], F16))
+    with pytest.raises(tcr.TcrError) as e:
+        tcr.tcr_reduce_rows(dev(x[:100_000]).view(100, 1000), tcr.Mode(tcr.MMA_CHAIN_TMEM))
+    assert e.value.status == tcr.ERR_UNSUPPORTED
+
+
+def test_mma_chain_tmem_non_finite():
+    x = inputs(300_000, F16)
+    y = x.copy()
+    y[123_456] = 0x7E00
+    assert np.isnan(gpu_sum(y, tcr.Mode(tcr.MMA_CHAIN_TMEM)))
+    y = x.copy()
+    y[5] = 0x7C00
+    assert gpu_sum(y, tcr.Mode(tcr.MMA_CHAIN_TMEM)) == np.inf
