@@ -16,10 +16,10 @@
 //
 // CTA roles (192 threads, one persistent CTA per SM):
 //   warp 0, lane 0   producer: 32 KiB bulk copies (8 tiles) global -> a
-//                    4-stage shared-memory ring, completion by mbarrier
+//                    6-stage shared-memory ring, completion by mbarrier
 //                    transaction count;
 //   warp 1           owns the TMEM allocation; lane 0 issues the MMAs:
-//                    R per chain into one of two D buffers, the first of a
+//                    R per chain into one of 8 D buffers, the first of a
 //                    chain without accumulate, tcgen05.commit after a chain
 //                    (D full) and after a stage (stage free);
 //   warps 2..5       epilogue: each thread reads its TMEM lane of column 0
@@ -32,6 +32,10 @@
 // raises a device-wide fault flag, drains its own copies and MMAs (again
 // with a limit), frees its TMEM and writes NaN as its partials, so a broken
 // pipeline shows up as a NaN result, never as a hang.
+#include <mutex>
+#include <utility>
+#include <vector>
+
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -41,21 +45,22 @@ constexpr int kTcTileInputs = 2048;                 // one MMA: 128 x 16 inputs
 constexpr int kTcTileBytes = kTcTileInputs * 2;     // 4 KiB
 constexpr int kTcTilesPerStage = 8;                 // 32 KiB bulk copies
 constexpr int kTcStageBytes = kTcTileBytes * kTcTilesPerStage;
-constexpr int kTcStages = 4;                        // 128 KiB in flight per SM
+constexpr int kTcStages = 6;                        // 192 KiB in flight per SM
 constexpr int kTcUnitLog2 = 16;                     // work unit: 2^16 inputs
 constexpr int kTcTilesPerUnit = (1 << kTcUnitLog2) / kTcTileInputs;   // 32
 constexpr int kTcThreads = 192;
 constexpr int kTcEpilogueThreads = 128;
-constexpr uint32_t kTcTmemCols = 128;               // D buffers at columns 0 and 64
-constexpr uint32_t kTcDBufferStride = 64;
+constexpr int kTcDBuffers = 8;                      // chains the MMA may run ahead
+constexpr uint32_t kTcDBufferStride = 32;           // columns per D buffer (N = 16 used)
+constexpr uint32_t kTcTmemCols = kTcDBuffers * kTcDBufferStride;    // 256
 constexpr uint64_t kWaitLimitNs = 1000000000ull;    // about one second
 
 // Dynamic shared memory layout (offsets from a 1024-byte aligned base).
 constexpr int kTcOffRing = 0;
 constexpr int kTcOffOnes = kTcOffRing + kTcStages * kTcStageBytes;     // 512 B of ones
 constexpr int kTcOffBars = kTcOffOnes + 1024;
-// barriers: full[S], empty[S], dfull[2], dempty[2], drain
-constexpr int kTcNumBars = 2 * kTcStages + 5;
+// barriers: full[S], empty[S], dfull[B], dempty[B], drain
+constexpr int kTcNumBars = 2 * kTcStages + 2 * kTcDBuffers + 1;
 constexpr int kTcOffMisc = kTcOffBars + 8 * kTcNumBars;                 // tmem addr, abort, red[4]
 constexpr int kTcSmemBytes = kTcOffMisc + 64 + 1024;                    // + alignment slack
 
@@ -105,17 +110,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 }
 
 // Wait for the phase of parity `parity` of `bar` to complete, giving up
-// after about a second (or at once when another role already gave up).
+// after about a second (or soon after another role gave up).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile uint32_t *abort)
 {
+    if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
-    for (;;) {
+    for (uint32_t i = 1;; i++) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (*abort) return false;
-        if (global_ns() - t0 > kWaitLimitNs) {
-            *abort = 1u;
-            atomicOr(&g_tc05_fault, 1u);
-            return false;
+        if ((i & 63u) == 0u) {
+            if (*abort) return false;
+            if (global_ns() - t0 > kWaitLimitNs) {
+                *abort = 1u;
+                atomicOr(&g_tc05_fault, 1u);
+                return false;
+            }
         }
     }
 }
@@ -210,8 +218,8 @@ mma_tmem_kernel(const uint16_t *__restrict__ x, size_t n, size_t units, float *_
     auto full_bar = [&](int s) { return bars + 8u * (uint32_t)s; };
     auto empty_bar = [&](int s) { return bars + 8u * (uint32_t)(kTcStages + s); };
     auto dfull_bar = [&](int b) { return bars + 8u * (uint32_t)(2 * kTcStages + b); };
-    auto dempty_bar = [&](int b) { return bars + 8u * (uint32_t)(2 * kTcStages + 2 + b); };
-    const uint32_t drain_bar = bars + 8u * (uint32_t)(2 * kTcStages + 4);
+    auto dempty_bar = [&](int b) { return bars + 8u * (uint32_t)(2 * kTcStages + kTcDBuffers + b); };
+    const uint32_t drain_bar = bars + 8u * (uint32_t)(2 * kTcStages + 2 * kTcDBuffers);
     uint32_t *misc = (uint32_t *)(smem + kTcOffMisc);
     volatile uint32_t *tmem_holder = misc;
     volatile uint32_t *abort = misc + 1;
@@ -230,7 +238,7 @@ mma_tmem_kernel(const uint16_t *__restrict__ x, size_t n, size_t units, float *_
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
         }
-        for (int b = 0; b < 2; b++) {
+        for (int b = 0; b < kTcDBuffers; b++) {
             mbar_init(dfull_bar(b), 1);
             mbar_init(dempty_bar(b), kTcEpilogueThreads);
         }
@@ -299,8 +307,24 @@ mma_tmem_kernel(const uint16_t *__restrict__ x, size_t n, size_t units, float *_
         if (lane == 0) {
             const uint32_t idesc = instr_desc<DT>();
             const uint64_t b_desc = smem_desc(ones, 128, 256);
+            // descriptor of tile 0 of stage 0; a tile is 4096 bytes further
+            // (256 in the descriptor's 16-byte units), a stage 8 tiles
+            const uint64_t ring_desc = smem_desc(ring, 128, 256);
+            constexpr uint64_t kTileStep = kTcTileBytes >> 4;
+            constexpr uint64_t kStageStep = kTcStageBytes >> 4;
             int s = 0, b = 0;
-            uint32_t phase = 0, dphase[2] = {0u, 0u};
+            uint32_t phase = 0, dphase = 0u;     // bit b: uses of D buffer b so far, mod 2
+            auto begin_chain = [&]() -> bool {
+                // the chain's D buffer must have been read out
+                if (!mbar_wait(dempty_bar(b), ((dphase >> b) & 1u) ^ 1u, abort)) return false;
+                tc_fence_after();
+                return true;
+            };
+            auto end_chain = [&]() {
+                tc_commit(dfull_bar(b));          // chain sub-result ready
+                dphase ^= 1u << b;
+                if (++b == kTcDBuffers) b = 0;
+            };
             for (size_t u = blockIdx.x; u < units && !*abort; u += gridDim.x) {
                 const int tiles = unit_tiles(n, u);
                 int in_chain = 0;
@@ -308,23 +332,26 @@ mma_tmem_kernel(const uint16_t *__restrict__ x, size_t n, size_t units, float *_
                     const int nt = min(kTcTilesPerStage, tiles - t0);
                     if (!mbar_wait(full_bar(s), phase, abort)) break;
                     tc_fence_after();
-                    const uint32_t stage = ring + (uint32_t)s * kTcStageBytes;
-                    for (int t = 0; t < nt; t++) {
-                        if (in_chain == 0) {
-                            // the chain's D buffer must have been read out
-                            if (!mbar_wait(dempty_bar(b), dphase[b] ^ 1u, abort)) break;
-                            tc_fence_after();
+                    const uint64_t sdesc = ring_desc + (uint64_t)s * kStageStep;
+                    bool ok = true;
+                    if (kTcTilesPerStage % R == 0 && nt == kTcTilesPerStage) {
+                        // whole stage, chains aligned to it: static boundaries
+#pragma unroll
+                        for (int t = 0; t < kTcTilesPerStage; t++) {
+                            if (t % R == 0 && !(ok = begin_chain())) break;
+                            tc_mma(tmem + (uint32_t)b * kTcDBufferStride, sdesc + (uint64_t)t * kTileStep,
+                                   b_desc, idesc, t % R != 0 ? 1u : 0u);
+                            if (t % R == R - 1) end_chain();
                         }
-                        const uint64_t a_desc = smem_desc(stage + (uint32_t)t * kTcTileBytes, 128, 256);
-                        tc_mma(tmem + (uint32_t)b * kTcDBufferStride, a_desc, b_desc, idesc,
-                               in_chain > 0 ? 1u : 0u);
-                        ++in_chain;
-                        const bool last_of_unit = t0 + t + 1 == tiles;
-                        if (in_chain == R || last_of_unit) {
-                            tc_commit(dfull_bar(b));          // chain sub-result ready
-                            dphase[b] ^= 1u;
-                            b ^= 1;
-                            in_chain = 0;
+                    } else {
+                        for (int t = 0; t < nt; t++) {
+                            if (in_chain == 0 && !(ok = begin_chain())) break;
+                            tc_mma(tmem + (uint32_t)b * kTcDBufferStride, sdesc + (uint64_t)t * kTileStep,
+                                   b_desc, idesc, in_chain > 0 ? 1u : 0u);
+                            if (++in_chain == R || t0 + t + 1 == tiles) {
+                                end_chain();
+                                in_chain = 0;
+                            }
                         }
                     }
                     tc_commit(empty_bar(s));                  // stage may be refilled
@@ -332,6 +359,7 @@ mma_tmem_kernel(const uint16_t *__restrict__ x, size_t n, size_t units, float *_
                         s = 0;
                         phase ^= 1u;
                     }
+                    if (!ok) break;
                 }
             }
             // every MMA issued has completed once the drain barrier flips
@@ -346,20 +374,20 @@ mma_tmem_kernel(const uint16_t *__restrict__ x, size_t n, size_t units, float *_
         const int et = threadIdx.x - 64;                   // 0..127
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
         int b = 0;
-        uint32_t dphase[2] = {0u, 0u};
+        uint32_t dphase = 0u;
         for (size_t u = blockIdx.x; u < units; u += gridDim.x) {
             const int tiles = unit_tiles(n, u);
             const int chains = (tiles + R - 1) / R;
             float acc = 0.f;
             for (int c = 0; c < chains && !*abort; c++) {
-                if (!mbar_wait(dfull_bar(b), dphase[b], abort)) break;
+                if (!mbar_wait(dfull_bar(b), (dphase >> b) & 1u, abort)) break;
                 tc_fence_after();
                 const float v = tc_ld_lane(tmem + lane_base + (uint32_t)b * kTcDBufferStride);
                 acc = __fadd_rn(acc, v);
                 tc_fence_before();
                 mbar_arrive(dempty_bar(b));
-                dphase[b] ^= 1u;
-                b ^= 1;
+                dphase ^= 1u << b;
+                if (++b == kTcDBuffers) b = 0;
             }
             // inputs of this unit past its whole tiles (only in the last unit)
             const size_t base = u << kTcUnitLog2;
@@ -423,8 +451,23 @@ cudaError_t launch_mma_tmem(int dtype, int R, const uint16_t *x, size_t n, float
 {
     void *k = dtype == kF16 ? pick_dt<kF16>(R) : pick_dt<kBF16>(R);
     if (!k) return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmemBytes);
-    if (e != cudaSuccess) return e;
+    // the shared-memory opt-in is a per-kernel attribute; set it once per
+    // device and kernel instance
+    static std::mutex mu;
+    static std::vector<std::pair<int, void *>> done;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaGetLastError();
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        bool set = false;
+        for (auto &d : done) set |= (d.first == dev && d.second == k);
+        if (!set) {
+            cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 kTcSmemBytes);
+            if (e != cudaSuccess) return e;
+            done.emplace_back(dev, k);
+        }
+    }
     size_t units = tmem_units(n);
     void *args[] = {(void *)&x, (void *)&n, (void *)&units, (void *)&dst};
     return cudaLaunchKernel(k, dim3(grid), dim3(kTcThreads), args, kTcSmemBytes, stream);

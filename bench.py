@@ -6,7 +6,8 @@ synthetic inputs resident in HBM:
 
   x_sum  = 2^30 binary16 values, uniform on [-1, 1), seed 4     (2 GiB)
   x_rows = 65536 x 4096 binary16 values, N(0, 1), seed 2        (512 MiB)
-  tcr_reduce_sum(x_sum)   in MMA_CHAIN, FIXED_ORDER, SHUFFLE_TREE
+  tcr_reduce_sum(x_sum)   in MMA_CHAIN, FIXED_ORDER, SHUFFLE_TREE and
+                          MMA_CHAIN_TMEM (the tcgen05 form of MMA_CHAIN)
   tcr_reduce_rows(x_rows) in MMA_CHAIN, FIXED_ORDER, SHUFFLE_TREE
 
 ``value`` is the algorithmic bytes of a step (2 bytes read per input plus
@@ -41,7 +42,8 @@ METRIC = "reduction GB/s and % of GB300 HBM peak (2^30 fp16 sum; 65536×4096 row
 UNIT = "GB/s"
 N_SUM = 1 << 30
 ROWS, COLS = 65536, 4096
-WORKLOAD = "sum of 2^30 fp16 U[-1,1) seed 4 + rows 65536x4096 fp16 N(0,1) seed 2, all three modes"
+WORKLOAD = ("sum of 2^30 fp16 U[-1,1) seed 4 in MMA_CHAIN, FIXED_ORDER, SHUFFLE_TREE, MMA_CHAIN_TMEM"
+            " + rows 65536x4096 fp16 N(0,1) seed 2 in MMA_CHAIN, FIXED_ORDER, SHUFFLE_TREE")
 FALLBACK_HBM_GBS = 6800.0
 
 # kernel launched by each call (the first, reduction launch)
@@ -52,6 +54,7 @@ KERNEL_OF = {
     "rows/MMA_CHAIN": "mma_rows_warp_kernel",
     "rows/FIXED_ORDER": "fixed_rows_warp_kernel",
     "rows/SHUFFLE_TREE": "shuffle_rows_warp_kernel",
+    "sum/MMA_CHAIN_TMEM": "mma_tmem_kernel",
 }
 
 
@@ -110,7 +113,7 @@ KERNEL_SOURCE = {
     "mma_chunk_kernel": "k_mma.cu", "mma_rows_warp_kernel": "k_mma.cu",
     "fixed_chunk_kernel": "k_fixed.cu", "fixed_rows_warp_kernel": "k_fixed.cu",
     "shuffle_block_kernel": "k_shuffle.cu", "shuffle_rows_warp_kernel": "k_shuffle.cu",
-    "combine_kernel": "k_combine.cu",
+    "combine_kernel": "k_combine.cu", "mma_tmem_kernel": "k_tc05.cu",
 }
 
 
@@ -223,7 +226,7 @@ def build_calls(x_sum, x_rows):
     import torch
     import arithmetic_reduction_tensor_gb300 as tcr
     dev = x_sum.device
-    outs = torch.empty(3 + 3 * ROWS, dtype=torch.float32, device=dev)
+    outs = torch.empty(4 + 3 * ROWS, dtype=torch.float32, device=dev)
     calls = []
     for i, kind in enumerate((tcr.MMA_CHAIN, tcr.FIXED_ORDER, tcr.SHUFFLE_TREE)):
         m = tcr.Mode(kind)
@@ -239,6 +242,12 @@ def build_calls(x_sum, x_rows):
         d = tcr.tcr_order_descriptor(rows=ROWS, cols=COLS, mode=m)
         calls.append((name, (lambda m=m, o=o: tcr.tcr_reduce_rows(x_rows, m, out=o)),
                       2 * ROWS * COLS + 4 * ROWS, d["launches"]))
+    # the tensor-core method once more, on the fifth-generation tensor cores
+    m = tcr.Mode(tcr.MMA_CHAIN_TMEM)
+    d = tcr.tcr_order_descriptor(n=N_SUM, mode=m)
+    o = outs[3 + 3 * ROWS:4 + 3 * ROWS]
+    calls.append(("sum/MMA_CHAIN_TMEM", (lambda m=m, o=o: tcr.tcr_reduce_sum(x_sum, m, out=o)),
+                  2 * N_SUM + 4, d["launches"]))
     return calls, outs
 
 
@@ -292,10 +301,10 @@ def time_e2e(xs, xr, calls_factory, steps: int, world: int):
         copy_stream.wait_stream(stream)          # previous step's rows calls are done
         with torch.cuda.stream(copy_stream):
             d_rows.view(-1).copy_(h_rows, non_blocking=True)
-        for _, fn, _, _ in calls[:n_sum_calls]:
+        for _, fn, _, _ in calls[:n_sum_calls] + calls[2 * n_sum_calls:]:
             fn()
         stream.wait_stream(copy_stream)
-        for _, fn, _, _ in calls[n_sum_calls:]:
+        for _, fn, _, _ in calls[n_sum_calls:2 * n_sum_calls]:
             fn()
         h_out.copy_(outs, non_blocking=True)
 
@@ -396,7 +405,8 @@ def reference_arm(args):
 
 
 def sweep_arm(args):
-    """MMA_CHAIN R x block sweep against SHUFFLE_TREE on 2^28 values in [0, 1)."""
+    """MMA_CHAIN R x block sweep against SHUFFLE_TREE and FIXED_ORDER on 2^28
+    values in [0, 1), and MMA_CHAIN_TMEM by R (its CTA shape is fixed)."""
     import torch
     import arithmetic_reduction_tensor_gb300 as tcr
     from arithmetic_reduction_tensor_gb300 import synth
@@ -408,6 +418,7 @@ def sweep_arm(args):
     points = [(tcr.SHUFFLE_TREE, 0, b) for b in (32, 128, 256, 1024)]
     points += [(tcr.FIXED_ORDER, 0, b) for b in (32, 128, 256, 1024)]
     points += [(tcr.MMA_CHAIN, R, b) for R in (1, 2, 4, 5) for b in (32, 128, 256, 1024)]
+    points += [(tcr.MMA_CHAIN_TMEM, R, 0) for R in (1, 2, 4, 5, 8)]
     for kind, R, b in points:
         m = tcr.Mode(kind, R=R, block_threads=b)
         for _ in range(3):
@@ -429,7 +440,8 @@ def sweep_arm(args):
 
 def profile_arm(args):
     """A small case for ncu: each sum mode once on 2^28 fp16 values (512 MiB,
-    larger than L2) and each rows mode once on 32768 x 4096 rows (256 MiB)."""
+    larger than L2), each rows mode once on 32768 x 4096 rows (256 MiB), and
+    the tcgen05 MMA_CHAIN sum."""
     import torch
     import arithmetic_reduction_tensor_gb300 as tcr
     from arithmetic_reduction_tensor_gb300 import synth
@@ -442,6 +454,7 @@ def profile_arm(args):
         for kind in (tcr.MMA_CHAIN, tcr.FIXED_ORDER, tcr.SHUFFLE_TREE):
             tcr.tcr_reduce_sum(x, tcr.Mode(kind))
             tcr.tcr_reduce_rows(r, tcr.Mode(kind))
+        tcr.tcr_reduce_sum(x, tcr.Mode(tcr.MMA_CHAIN_TMEM))
     torch.cuda.synchronize()
     print("profile case done", flush=True)
     return 0
@@ -558,6 +571,8 @@ def build_calls_meta():
     for kind in (tcr.MMA_CHAIN, tcr.FIXED_ORDER, tcr.SHUFFLE_TREE):
         d = tcr.tcr_order_descriptor(rows=ROWS, cols=COLS, mode=tcr.Mode(kind))
         meta.append(("rows/" + tcr.KIND_NAMES[kind], 2 * ROWS * COLS + 4 * ROWS, d["launches"]))
+    d = tcr.tcr_order_descriptor(n=N_SUM, mode=tcr.Mode(tcr.MMA_CHAIN_TMEM))
+    meta.append(("sum/MMA_CHAIN_TMEM", 2 * N_SUM + 4, d["launches"]))
     return meta
 
 
