@@ -74,6 +74,24 @@ combine_kernel(const float *__restrict__ partials, size_t count, float *__restri
     }
 }
 
+// Many segments with few partials each (long rows): one thread per segment
+// pushes its partials into a binary counter -- the same balanced tree,
+// padded with -0.0, as combine_kernel forms.
+constexpr size_t kCombineRowsMaxCount = 64;
+
+__global__ void __launch_bounds__(256)
+combine_rows_kernel(const float *__restrict__ partials, size_t segments, size_t count,
+                    float *__restrict__ out)
+{
+    pdl_wait_primary();
+    const size_t r = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (r >= segments) return;
+    const float *p = partials + r * count;
+    TreeCounter<7> tc;
+    for (size_t i = 0; i < count; i++) tc.push(__ldg(p + i));
+    out[r] = tc.finish();
+}
+
 // Launched with programmatic stream serialization: the combine's launch
 // overlaps the end of the kernel before it, and pdl_wait_primary() holds
 // its threads until that kernel's partials are complete and visible.
@@ -81,8 +99,6 @@ cudaError_t launch_combine(const float *partials, size_t segments, size_t count,
                            cudaStream_t stream)
 {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)segments);
-    cfg.blockDim = dim3(1024);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -90,6 +106,13 @@ cudaError_t launch_combine(const float *partials, size_t segments, size_t count,
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (count <= kCombineRowsMaxCount && segments > 1) {
+        cfg.gridDim = dim3((unsigned)((segments + 255) / 256));
+        cfg.blockDim = dim3(256);
+        return cudaLaunchKernelEx(&cfg, combine_rows_kernel, partials, segments, count, out);
+    }
+    cfg.gridDim = dim3((unsigned)segments);
+    cfg.blockDim = dim3(1024);
     return cudaLaunchKernelEx(&cfg, combine_kernel, partials, count, out);
 }
 

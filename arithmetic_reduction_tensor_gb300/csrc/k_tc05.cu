@@ -32,6 +32,8 @@
 // raises a device-wide fault flag, drains its own copies and MMAs (again
 // with a limit), frees its TMEM and writes NaN as its partials, so a broken
 // pipeline shows up as a NaN result, never as a hang.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <mutex>
 #include <utility>
 #include <vector>
@@ -419,7 +421,257 @@ mma_tmem_kernel(const uint16_t *__restrict__ x, size_t n, size_t units, float *_
     }
 }
 
+// ---------------------------------------------------------------- rows
+
+// Rows: D's 128 lanes are 128 consecutive data rows.  A 2-D tensor map over
+// the row-major matrix (dims: cols, rows) with an 8-column x 128-row box
+// lands one column group of a row block as 128 rows x 16 bytes, row after
+// row; eight such boxes side by side (2 KiB apart) hold 128 rows x 64
+// columns in the no-swizzle K-major layout of 8-row x 16-byte core
+// matrices (8-row step 128 bytes, K step 2048 bytes), i.e. four MMAs of
+// K = 16.  The column of D read out after a chain holds the 128 rows' sums
+// over that chain's columns.  Work unit: 128 rows x kTcRowsChunkCols
+// columns, one partial per row and unit; the tensor map zero-fills rows and
+// columns past the matrix.
+constexpr int kTcRowsChunkCols = 512;                 // columns per work unit
+constexpr int kTcRowsBoxCols = 64;                    // columns per stage
+constexpr int kTcRowsStageBytes = 128 * kTcRowsBoxCols * 2;   // 16 KiB
+constexpr int kTcRowsStages = 12;                     // 192 KiB ring
+constexpr int kTcRowsOffOnes = kTcRowsStages * kTcRowsStageBytes;
+constexpr int kTcRowsOffBars = kTcRowsOffOnes + 1024;
+constexpr int kTcRowsNumBars = 2 * kTcRowsStages + 2 * kTcDBuffers + 1;
+constexpr int kTcRowsOffMisc = kTcRowsOffBars + 8 * kTcRowsNumBars;
+constexpr int kTcRowsSmemBytes = kTcRowsOffMisc + 64 + 1024;
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
+                                            uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];"
+        ::"r"(dst), "l"((uint64_t)map), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+
+template <int DT, int R>
+__global__ void __launch_bounds__(kTcThreads, 1)
+mma_tmem_rows_kernel(const __grid_constant__ CUtensorMap tmap, size_t rows, size_t cols,
+                     size_t cpr, size_t units, float *__restrict__ dst)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const uint32_t sbase = smem_addr(smem);
+    const uint32_t ring = sbase;
+    const uint32_t ones = sbase + kTcRowsOffOnes;
+    const uint32_t bars = sbase + kTcRowsOffBars;
+    auto full_bar = [&](int s) { return bars + 8u * (uint32_t)s; };
+    auto empty_bar = [&](int s) { return bars + 8u * (uint32_t)(kTcRowsStages + s); };
+    auto dfull_bar = [&](int b) { return bars + 8u * (uint32_t)(2 * kTcRowsStages + b); };
+    auto dempty_bar = [&](int b) { return bars + 8u * (uint32_t)(2 * kTcRowsStages + kTcDBuffers + b); };
+    const uint32_t drain_bar = bars + 8u * (uint32_t)(2 * kTcRowsStages + 2 * kTcDBuffers);
+    uint32_t *misc = (uint32_t *)(smem + kTcRowsOffMisc);
+    volatile uint32_t *tmem_holder = misc;
+    volatile uint32_t *abort = misc + 1;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // boxes (64 columns) of work unit u
+    auto unit_boxes = [&](size_t u) -> int {
+        const size_t c0 = (u % cpr) * kTcRowsChunkCols;
+        const size_t nc = cols - c0 < (size_t)kTcRowsChunkCols ? cols - c0 : (size_t)kTcRowsChunkCols;
+        return (int)((nc + kTcRowsBoxCols - 1) / kTcRowsBoxCols);
+    };
+
+    {
+        const uint32_t one2 = DT == kF16 ? 0x3c003c00u : 0x3f803f80u;
+        uint32_t *o = (uint32_t *)(smem + kTcRowsOffOnes);
+        for (int i = threadIdx.x; i < 128; i += blockDim.x) o[i] = one2;
+    }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kTcRowsStages; s++) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < kTcDBuffers; b++) {
+            mbar_init(dfull_bar(b), 1);
+            mbar_init(dempty_bar(b), kTcEpilogueThreads);
+        }
+        mbar_init(drain_bar, 1);
+        *abort = 0u;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmap) : "memory");
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(smem_addr((const void *)tmem_holder)), "r"(kTcTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == 0) {
+        // ---------------- producer: eight 8-column x 128-row boxes per stage
+        if (lane == 0) {
+            int s = 0;
+            uint32_t phase = 0;
+            bool armed[kTcRowsStages];
+            uint32_t armed_phase[kTcRowsStages];
+            for (int i = 0; i < kTcRowsStages; i++) {
+                armed[i] = false;
+                armed_phase[i] = 0;
+            }
+            for (size_t u = blockIdx.x; u < units && !*abort; u += gridDim.x) {
+                const int row0 = (int)((u / cpr) * 128);
+                const int col0 = (int)((u % cpr) * kTcRowsChunkCols);
+                const int boxes = unit_boxes(u);
+                for (int j = 0; j < boxes; j++) {
+                    if (!mbar_wait(empty_bar(s), phase ^ 1u, abort)) break;
+                    mbar_arrive_expect_tx(full_bar(s), kTcRowsStageBytes);
+                    const uint32_t st = ring + (uint32_t)s * kTcRowsStageBytes;
+#pragma unroll
+                    for (int g = 0; g < 8; g++)
+                        tma_load_2d(st + (uint32_t)g * 2048u, &tmap, col0 + j * kTcRowsBoxCols + 8 * g,
+                                    row0, full_bar(s));
+                    armed[s] = true;
+                    armed_phase[s] = phase;
+                    if (++s == kTcRowsStages) {
+                        s = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (*abort) {
+                for (int i = 0; i < kTcRowsStages; i++) {
+                    if (!armed[i]) continue;
+                    const uint64_t t0 = global_ns();
+                    while (!mbar_try_wait(full_bar(i), armed_phase[i]) &&
+                           global_ns() - t0 < kWaitLimitNs) {
+                    }
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---------------- MMA issuer: four MMAs (K = 16) per stage
+        if (lane == 0) {
+            const uint32_t idesc = instr_desc<DT>();
+            const uint64_t b_desc = smem_desc(ones, 128, 256);
+            const uint64_t ring_desc = smem_desc(ring, 2048, 128);
+            constexpr uint64_t kKStep = 4096u >> 4;                  // two column groups
+            constexpr uint64_t kStageStep = (uint64_t)kTcRowsStageBytes >> 4;
+            int s = 0, b = 0;
+            uint32_t phase = 0, dphase = 0u;
+            auto begin_chain = [&]() -> bool {
+                if (!mbar_wait(dempty_bar(b), ((dphase >> b) & 1u) ^ 1u, abort)) return false;
+                tc_fence_after();
+                return true;
+            };
+            auto end_chain = [&]() {
+                tc_commit(dfull_bar(b));
+                dphase ^= 1u << b;
+                if (++b == kTcDBuffers) b = 0;
+            };
+            for (size_t u = blockIdx.x; u < units && !*abort; u += gridDim.x) {
+                const int boxes = unit_boxes(u);
+                const int mmas = 4 * boxes;
+                int in_chain = 0;
+                bool ok = true;
+                for (int j = 0; j < boxes && ok; j++) {
+                    if (!mbar_wait(full_bar(s), phase, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t sdesc = ring_desc + (uint64_t)s * kStageStep;
+                    if (4 % R == 0) {
+#pragma unroll
+                        for (int k = 0; k < 4; k++) {
+                            if (k % R == 0 && !(ok = begin_chain())) break;
+                            tc_mma(tmem + (uint32_t)b * kTcDBufferStride, sdesc + (uint64_t)k * kKStep,
+                                   b_desc, idesc, k % R != 0 ? 1u : 0u);
+                            if (k % R == R - 1) end_chain();
+                        }
+                    } else {
+                        for (int k = 0; k < 4; k++) {
+                            if (in_chain == 0 && !(ok = begin_chain())) break;
+                            tc_mma(tmem + (uint32_t)b * kTcDBufferStride, sdesc + (uint64_t)k * kKStep,
+                                   b_desc, idesc, in_chain > 0 ? 1u : 0u);
+                            if (++in_chain == R || 4 * j + k + 1 == mmas) {
+                                end_chain();
+                                in_chain = 0;
+                            }
+                        }
+                    }
+                    tc_commit(empty_bar(s));
+                    if (++s == kTcRowsStages) {
+                        s = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+            }
+            tc_commit(drain_bar);
+            const uint64_t t0 = global_ns();
+            while (!mbar_try_wait(drain_bar, 0u) && global_ns() - t0 < kWaitLimitNs) {
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---------------- epilogue: thread m holds row row0 + m of the unit
+        const int et = threadIdx.x - 64;
+        const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+        const int m = 32 * (warp & 3) + lane;              // TMEM lane = row in the block
+        (void)et;
+        int b = 0;
+        uint32_t dphase = 0u;
+        for (size_t u = blockIdx.x; u < units; u += gridDim.x) {
+            const int chains = (4 * unit_boxes(u) + R - 1) / R;
+            float acc = 0.f;
+            for (int c = 0; c < chains && !*abort; c++) {
+                if (!mbar_wait(dfull_bar(b), (dphase >> b) & 1u, abort)) break;
+                tc_fence_after();
+                acc = __fadd_rn(acc, tc_ld_lane(tmem + lane_base + (uint32_t)b * kTcDBufferStride));
+                tc_fence_before();
+                mbar_arrive(dempty_bar(b));
+                dphase ^= 1u << b;
+                if (++b == kTcDBuffers) b = 0;
+            }
+            const size_t row = (u / cpr) * 128 + (size_t)m;
+            if (row < rows) dst[row * cpr + (u % cpr)] = *abort ? __int_as_float(0x7fc00000) : acc;
+        }
+    }
+
+    pdl_launch_dependents();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kTcTmemCols)
+                     : "memory");
+    }
+}
+
 // ---------------------------------------------------------------- host
+
+// The shared-memory opt-in is a per-kernel attribute: set it once per
+// device and kernel instance.
+static cudaError_t set_smem_once(void *k, int bytes)
+{
+    static std::mutex mu;
+    static std::vector<std::pair<int, void *>> done;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaGetLastError();
+    std::lock_guard<std::mutex> lk(mu);
+    for (auto &d : done)
+        if (d.first == dev && d.second == k) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done.emplace_back(dev, k);
+    return e;
+}
 
 template <int DT>
 static void *pick_dt(int R)
@@ -451,26 +703,81 @@ cudaError_t launch_mma_tmem(int dtype, int R, const uint16_t *x, size_t n, float
 {
     void *k = dtype == kF16 ? pick_dt<kF16>(R) : pick_dt<kBF16>(R);
     if (!k) return cudaErrorInvalidValue;
-    // the shared-memory opt-in is a per-kernel attribute; set it once per
-    // device and kernel instance
-    static std::mutex mu;
-    static std::vector<std::pair<int, void *>> done;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return cudaGetLastError();
-    {
-        std::lock_guard<std::mutex> lk(mu);
-        bool set = false;
-        for (auto &d : done) set |= (d.first == dev && d.second == k);
-        if (!set) {
-            cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 kTcSmemBytes);
-            if (e != cudaSuccess) return e;
-            done.emplace_back(dev, k);
-        }
-    }
+    cudaError_t e = set_smem_once(k, kTcSmemBytes);
+    if (e != cudaSuccess) return e;
     size_t units = tmem_units(n);
     void *args[] = {(void *)&x, (void *)&n, (void *)&units, (void *)&dst};
     return cudaLaunchKernel(k, dim3(grid), dim3(kTcThreads), args, kTcSmemBytes, stream);
+}
+
+template <int DT>
+static void *pick_rows_dt(int R)
+{
+    switch (R) {
+    case 1: return (void *)mma_tmem_rows_kernel<DT, 1>;
+    case 2: return (void *)mma_tmem_rows_kernel<DT, 2>;
+    case 3: return (void *)mma_tmem_rows_kernel<DT, 3>;
+    case 4: return (void *)mma_tmem_rows_kernel<DT, 4>;
+    case 5: return (void *)mma_tmem_rows_kernel<DT, 5>;
+    case 6: return (void *)mma_tmem_rows_kernel<DT, 6>;
+    case 7: return (void *)mma_tmem_rows_kernel<DT, 7>;
+    case 8: return (void *)mma_tmem_rows_kernel<DT, 8>;
+    default: return nullptr;
+    }
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point, so the
+// library does not link the driver library itself.
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
+        else
+            (void)cudaGetLastError();
+    });
+    return fn;
+}
+
+size_t tmem_rows_chunks(size_t cols)
+{
+    return (cols + kTcRowsChunkCols - 1) / kTcRowsChunkCols;
+}
+
+size_t tmem_rows_units(size_t rows, size_t cols)
+{
+    return ((rows + 127) / 128) * tmem_rows_chunks(cols);
+}
+
+cudaError_t launch_mma_tmem_rows(int dtype, int R, const uint16_t *x, size_t rows, size_t cols,
+                                 float *dst, int grid, cudaStream_t stream)
+{
+    void *k = dtype == kF16 ? pick_rows_dt<kF16>(R) : pick_rows_dt<kBF16>(R);
+    if (!k) return cudaErrorInvalidValue;
+    PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    if (!encode) return cudaErrorNotSupported;
+    alignas(64) CUtensorMap map;
+    const cuuint64_t gdim[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t gstride[1] = {(cuuint64_t)cols * 2};
+    const cuuint32_t box[2] = {8, 128};
+    const cuuint32_t estride[2] = {1, 1};
+    if (encode(&map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, (void *)x, gdim, gstride, box, estride,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    cudaError_t e = set_smem_once(k, kTcRowsSmemBytes);
+    if (e != cudaSuccess) return e;
+    size_t cpr = tmem_rows_chunks(cols);
+    size_t units = tmem_rows_units(rows, cols);
+    void *args[] = {(void *)&map, (void *)&rows, (void *)&cols, (void *)&cpr, (void *)&units,
+                    (void *)&dst};
+    return cudaLaunchKernel(k, dim3(grid), dim3(kTcThreads), args, kTcRowsSmemBytes, stream);
 }
 
 }  // namespace tcr

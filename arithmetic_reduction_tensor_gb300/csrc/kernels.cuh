@@ -61,9 +61,18 @@ cudaError_t launch_mma_tmem(int dtype, int R, const uint16_t *x, size_t n, float
 size_t tmem_units(size_t n);
 int tmem_block_threads();
 int tmem_unit_log2();
+// Rows: D's 128 lanes are 128 consecutive rows, the inputs reach shared
+// memory by 2-D tensor-map copies; dst[row * chunks + c] is row `row`'s
+// partial over column chunk c (tmem_rows_chunks(cols) chunks per row).
+// x must be 16-byte aligned and cols a multiple of 8, rows and cols < 2^31.
+cudaError_t launch_mma_tmem_rows(int dtype, int R, const uint16_t *x, size_t rows, size_t cols,
+                                 float *dst, int grid, cudaStream_t stream);
+size_t tmem_rows_chunks(size_t cols);
+size_t tmem_rows_units(size_t rows, size_t cols);
 
 // ---- combine: out[s] = balanced tree over partials[s*count .. s*count+count-1]
-// padded with -0.0; one CTA of 1024 threads per segment.
+// padded with -0.0; one CTA of 1024 threads per segment, or one thread per
+// segment when count is small (the same tree either way).
 cudaError_t launch_combine(const float *partials, size_t segments, size_t count, float *out,
                            cudaStream_t stream);
 

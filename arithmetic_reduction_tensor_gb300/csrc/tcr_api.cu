@@ -131,7 +131,8 @@ enum Path {
     kPathMmaRows,        // MMA, one warp per row
     kPathShuffleBlock,   // SHUFFLE block team (+ combine if G > 1)
     kPathShuffleRowsWarp, // SHUFFLE warp team, one warp per row
-    kPathTmem            // MMA_CHAIN on tcgen05 (+ combine if units > 1)
+    kPathTmem,           // MMA_CHAIN on tcgen05 (+ combine if units > 1)
+    kPathTmemRows        // MMA_CHAIN rows on tcgen05 (+ combine if chunks > 1)
 };
 
 struct Plan {
@@ -253,7 +254,20 @@ Plan make_plan(size_t segments, size_t seg_len, bool rows_call, const tcr_mode &
         }
         return p;
     }
-    if (m.kind == TCR_MMA_CHAIN_TMEM && aligned) {
+    if (m.kind == TCR_MMA_CHAIN_TMEM && rows_call && aligned && segments < ((size_t)1 << 31) &&
+        seg_len < ((size_t)1 << 31)) {
+        // 128 rows per MMA tile, 2-D tensor-map copies; one CTA per SM
+        p.path = kPathTmemRows;
+        p.block = tmem_block_threads();
+        p.cps = tmem_rows_chunks(seg_len);
+        p.units = tmem_rows_units(segments, seg_len);
+        p.grid = (int)(p.units < sms ? p.units : sms);
+        p.partials = p.cps > 1 ? segments * p.cps : 0;
+        p.combine_count = p.cps;
+        p.launches = p.cps > 1 ? 2 : 1;
+        return p;
+    }
+    if (m.kind == TCR_MMA_CHAIN_TMEM && !rows_call && aligned) {
         // one persistent CTA per SM (its shared-memory ring fills the SM)
         p.path = kPathTmem;
         p.block = tmem_block_threads();
@@ -314,6 +328,9 @@ tcr_status run_plan(const Plan &p, const uint16_t *x, float *out, cudaStream_t s
     switch (p.path) {
     case kPathTmem:
         e = launch_mma_tmem(p.dtype, p.R, x, p.seg_len, dst, p.grid, s);
+        break;
+    case kPathTmemRows:
+        e = launch_mma_tmem_rows(p.dtype, p.R, x, p.segments, p.seg_len, dst, p.grid, s);
         break;
     case kPathChunk:
         e = p.kind == TCR_FIXED_ORDER
@@ -392,7 +409,6 @@ tcr_status tcr_reduce_rows(const void *x, size_t rows, size_t cols, float *out, 
     int block = 0, R = 0;
     tcr_status st = check_common(x, rows * cols, out, mode, &block, &R);
     if (st != TCR_OK) return st;
-    if (mode.kind == TCR_MMA_CHAIN_TMEM) return TCR_ERR_UNSUPPORTED;
     const int dev = current_device();
     if (dev < 0) return TCR_ERR_CUDA;
     const bool aligned = ((uintptr_t)x & 15u) == 0 && (cols % 8) == 0;
@@ -412,7 +428,6 @@ tcr_status tcr_order_descriptor(size_t n, size_t rows, size_t cols, tcr_mode mod
     const size_t segments = rows_call ? rows : 1;
     const size_t seg_len = rows_call ? cols : n;
     if (segments * seg_len >= kMaxInputs) return TCR_ERR_INVALID_ARG;
-    if (rows_call && mode.kind == TCR_MMA_CHAIN_TMEM) return TCR_ERR_UNSUPPORTED;
     const int dev = current_device();
     // the plan of an aligned input; a misaligned one differs only in speed
     Plan p = make_plan(segments, seg_len, rows_call, mode, block, R, true, dev);

@@ -300,14 +300,41 @@ def test_mma_chain_tmem_signed_inputs_and_stability():
         assert same_bits(again, first)
 
 
-def test_mma_chain_tmem_misaligned_and_rows():
+def test_mma_chain_tmem_misaligned():
     x = inputs(100_003, F16)
     t = dev(x)[3:]                      # not 16-byte aligned: served by the mma.sync kernel
     got = np.float32(tcr.tcr_reduce_sum(t, tcr.Mode(tcr.MMA_CHAIN_TMEM)).cpu().numpy()[0])
     assert_within_mma_tolerance(got, *oracle.exact_sum(x[3:], F16))
-    with pytest.raises(tcr.TcrError) as e:
-        tcr.tcr_reduce_rows(dev(x[:100_000]).view(100, 1000), tcr.Mode(tcr.MMA_CHAIN_TMEM))
-    assert e.value.status == tcr.ERR_UNSUPPORTED
+    rows, cols = 37, 1001               # odd cols: the rows go through the mma.sync kernel
+    xr = x[:rows * cols].reshape(rows, cols)
+    s, a = oracle.exact_sum_rows(xr, F16)
+    assert_within_mma_tolerance(gpu_rows(xr, tcr.Mode(tcr.MMA_CHAIN_TMEM)), s, a)
+
+
+TMEM_ROW_SHAPES = [(1, 8), (3, 64), (127, 512), (128, 512), (129, 520), (200, 4096), (256, 1000),
+                   (1000, 4096), (5, 100_000), (300, 8192), (4099, 640)]
+
+
+@pytest.mark.parametrize("dtype", [F16, BF16])
+@pytest.mark.parametrize("shape", TMEM_ROW_SHAPES)
+@pytest.mark.parametrize("R", [0, 1, 3, 8])
+def test_mma_chain_tmem_rows_within_tolerance(dtype, shape, R):
+    rows, cols = shape
+    x = inputs(rows * cols, dtype, "uniform01", seed=rows + cols).reshape(rows, cols)
+    s, a = oracle.exact_sum_rows(x, dtype)
+    assert_within_mma_tolerance(gpu_rows(x, tcr.Mode(tcr.MMA_CHAIN_TMEM, R=R, dtype=dtype)), s, a)
+
+
+def test_mma_chain_tmem_rows_signed_and_stable():
+    rows, cols = 3000, 2048
+    x = inputs(rows * cols, BF16, "pow2", seed=9).reshape(rows, cols)
+    t = dev(x)
+    first = tcr.tcr_reduce_rows(t, tcr.Mode(tcr.MMA_CHAIN_TMEM, dtype=BF16)).cpu().numpy()
+    s, a = oracle.exact_sum_rows(x, BF16)
+    assert_within_mma_tolerance(first, s, a)
+    for _ in range(3):
+        assert same_bits(tcr.tcr_reduce_rows(t, tcr.Mode(tcr.MMA_CHAIN_TMEM, dtype=BF16)).cpu().numpy(),
+                         first)
 
 
 def test_mma_chain_tmem_non_finite():
@@ -318,3 +345,32 @@ def test_mma_chain_tmem_non_finite():
     y = x.copy()
     y[5] = 0x7C00
     assert gpu_sum(y, tcr.Mode(tcr.MMA_CHAIN_TMEM)) == np.inf
+
+
+# ------------------------------------------------------------ guard canaries
+
+CANARY = np.float32(-12345.678)
+
+
+@pytest.mark.parametrize("kind", [tcr.FIXED_ORDER, tcr.SHUFFLE_TREE, tcr.MMA_CHAIN, tcr.MMA_CHAIN_TMEM])
+@pytest.mark.parametrize("n", [0, 1, 2049, 65537, 1 << 22])
+def test_sum_writes_exactly_one_result(kind, n):
+    x = dev(inputs(n, F16)) if n else torch.empty(0, dtype=torch.int16, device="cuda")
+    buf = torch.full((64,), float(CANARY), device="cuda")
+    tcr.tcr_reduce_sum(x, tcr.Mode(kind), out=buf[32:33])
+    got = buf.cpu().numpy()
+    assert np.all(got[:32] == CANARY) and np.all(got[33:] == CANARY)
+    assert got[32] != CANARY
+
+
+@pytest.mark.parametrize("kind", [tcr.FIXED_ORDER, tcr.SHUFFLE_TREE, tcr.MMA_CHAIN, tcr.MMA_CHAIN_TMEM])
+@pytest.mark.parametrize("shape", [(1, 5), (17, 100), (33, 4096), (5, 20_000), (3, 1 << 20),
+                                   (130, 1024)])
+def test_rows_write_exactly_rows_results(kind, shape):
+    rows, cols = shape
+    x = dev(inputs(rows * cols, F16)).view(rows, cols)
+    buf = torch.full((rows + 64,), float(CANARY), device="cuda")
+    tcr.tcr_reduce_rows(x, tcr.Mode(kind), out=buf[32:32 + rows])
+    got = buf.cpu().numpy()
+    assert np.all(got[:32] == CANARY) and np.all(got[32 + rows:] == CANARY)
+    assert np.all(got[32:32 + rows] != CANARY)
