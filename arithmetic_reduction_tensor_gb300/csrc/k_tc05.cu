@@ -424,24 +424,36 @@ mma_tmem_kernel(const uint16_t *__restrict__ x, size_t n, size_t units, float *_
 // ---------------------------------------------------------------- rows
 
 // Rows: D's 128 lanes are 128 consecutive data rows.  A 2-D tensor map over
-// the row-major matrix (dims: cols, rows) with an 8-column x 128-row box
-// lands one column group of a row block as 128 rows x 16 bytes, row after
-// row; eight such boxes side by side (2 KiB apart) hold 128 rows x 64
-// columns in the no-swizzle K-major layout of 8-row x 16-byte core
-// matrices (8-row step 128 bytes, K step 2048 bytes), i.e. four MMAs of
-// K = 16.  The column of D read out after a chain holds the 128 rows' sums
-// over that chain's columns.  Work unit: 128 rows x kTcRowsChunkCols
-// columns, one partial per row and unit; the tensor map zero-fills rows and
-// columns past the matrix.
+// the row-major matrix (dims: cols, rows) with a 64-column x 128-row box and
+// the 128-byte swizzle lands a row block as 128 rows of 128 bytes (8-row
+// atoms of 1024 bytes, the 16-byte chunks of row r permuted by r mod 8) --
+// the SWIZZLE_128B K-major layout the MMA descriptor names, so one box is
+// four MMAs of K = 16, the k-th starting 32 bytes further.  The swizzle only
+// permutes chunks within a row, so each MMA row still holds one data row.
+// The column of D read out after a chain holds the 128 rows' sums over that
+// chain's columns.  Work unit: 128 rows x kTcRowsChunkCols columns, one
+// partial per row and unit; the tensor map zero-fills rows and columns past
+// the matrix.
 constexpr int kTcRowsChunkCols = 512;                 // columns per work unit
-constexpr int kTcRowsBoxCols = 64;                    // columns per stage
-constexpr int kTcRowsStageBytes = 128 * kTcRowsBoxCols * 2;   // 16 KiB
-constexpr int kTcRowsStages = 12;                     // 192 KiB ring
+constexpr int kTcRowsBoxCols = 64;                    // columns per tensor-map box
+constexpr int kTcRowsBoxBytes = 128 * kTcRowsBoxCols * 2;     // 16 KiB
+constexpr int kTcRowsBoxesPerStage = 2;               // 32 KiB, 8 MMAs per stage
+constexpr int kTcRowsStageBytes = kTcRowsBoxBytes * kTcRowsBoxesPerStage;
+constexpr int kTcRowsStages = 6;                      // 192 KiB ring
 constexpr int kTcRowsOffOnes = kTcRowsStages * kTcRowsStageBytes;
 constexpr int kTcRowsOffBars = kTcRowsOffOnes + 1024;
 constexpr int kTcRowsNumBars = 2 * kTcRowsStages + 2 * kTcDBuffers + 1;
 constexpr int kTcRowsOffMisc = kTcRowsOffBars + 8 * kTcRowsNumBars;
 constexpr int kTcRowsSmemBytes = kTcRowsOffMisc + 64 + 1024;
+
+// SWIZZLE_128B K-major descriptor: 8-row groups 1024 bytes apart (the
+// leading-dimension field is not used by this layout), swizzle code 2 in
+// bits 61..63; the atom base is 1024-byte aligned, so the base offset is 0.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr)
+{
+    return (uint64_t)((addr >> 4) & 0x3fffu) | ((uint64_t)1 << 16) |
+           ((uint64_t)(1024u >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
                                             uint32_t bar)
@@ -513,7 +525,7 @@ mma_tmem_rows_kernel(const __grid_constant__ CUtensorMap tmap, size_t rows, size
     const uint32_t tmem = *tmem_holder;
 
     if (warp == 0) {
-        // ---------------- producer: eight 8-column x 128-row boxes per stage
+        // ---------------- producer: one 64-column x 128-row box per stage
         if (lane == 0) {
             int s = 0;
             uint32_t phase = 0;
@@ -527,14 +539,13 @@ mma_tmem_rows_kernel(const __grid_constant__ CUtensorMap tmap, size_t rows, size
                 const int row0 = (int)((u / cpr) * 128);
                 const int col0 = (int)((u % cpr) * kTcRowsChunkCols);
                 const int boxes = unit_boxes(u);
-                for (int j = 0; j < boxes; j++) {
+                for (int j = 0; j < boxes; j += kTcRowsBoxesPerStage) {
+                    const int nb = min(kTcRowsBoxesPerStage, boxes - j);
                     if (!mbar_wait(empty_bar(s), phase ^ 1u, abort)) break;
-                    mbar_arrive_expect_tx(full_bar(s), kTcRowsStageBytes);
-                    const uint32_t st = ring + (uint32_t)s * kTcRowsStageBytes;
-#pragma unroll
-                    for (int g = 0; g < 8; g++)
-                        tma_load_2d(st + (uint32_t)g * 2048u, &tmap, col0 + j * kTcRowsBoxCols + 8 * g,
-                                    row0, full_bar(s));
+                    mbar_arrive_expect_tx(full_bar(s), (uint32_t)nb * kTcRowsBoxBytes);
+                    for (int q = 0; q < nb; q++)
+                        tma_load_2d(ring + (uint32_t)s * kTcRowsStageBytes + (uint32_t)q * kTcRowsBoxBytes,
+                                    &tmap, col0 + (j + q) * kTcRowsBoxCols, row0, full_bar(s));
                     armed[s] = true;
                     armed_phase[s] = phase;
                     if (++s == kTcRowsStages) {
@@ -559,9 +570,11 @@ mma_tmem_rows_kernel(const __grid_constant__ CUtensorMap tmap, size_t rows, size
         if (lane == 0) {
             const uint32_t idesc = instr_desc<DT>();
             const uint64_t b_desc = smem_desc(ones, 128, 256);
-            const uint64_t ring_desc = smem_desc(ring, 2048, 128);
-            constexpr uint64_t kKStep = 4096u >> 4;                  // two column groups
+            const uint64_t ring_desc = smem_desc_sw128(ring);
+            constexpr uint64_t kKStep = 32u >> 4;                    // 16 columns = 32 bytes
+            constexpr uint64_t kBoxStep = (uint64_t)kTcRowsBoxBytes >> 4;
             constexpr uint64_t kStageStep = (uint64_t)kTcRowsStageBytes >> 4;
+            constexpr int kMmasPerStage = 4 * kTcRowsBoxesPerStage;
             int s = 0, b = 0;
             uint32_t phase = 0, dphase = 0u;
             auto begin_chain = [&]() -> bool {
@@ -579,25 +592,29 @@ mma_tmem_rows_kernel(const __grid_constant__ CUtensorMap tmap, size_t rows, size
                 const int mmas = 4 * boxes;
                 int in_chain = 0;
                 bool ok = true;
-                for (int j = 0; j < boxes && ok; j++) {
+                for (int j = 0; j < boxes && ok; j += kTcRowsBoxesPerStage) {
+                    const int nm = 4 * min(kTcRowsBoxesPerStage, boxes - j);
                     if (!mbar_wait(full_bar(s), phase, abort)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint64_t sdesc = ring_desc + (uint64_t)s * kStageStep;
-                    if (4 % R == 0) {
+                    // MMA k of the stage: box k / 4, 32-byte slice k % 4
+                    if (kMmasPerStage % R == 0 && nm == kMmasPerStage) {
 #pragma unroll
-                        for (int k = 0; k < 4; k++) {
+                        for (int k = 0; k < kMmasPerStage; k++) {
                             if (k % R == 0 && !(ok = begin_chain())) break;
-                            tc_mma(tmem + (uint32_t)b * kTcDBufferStride, sdesc + (uint64_t)k * kKStep,
+                            tc_mma(tmem + (uint32_t)b * kTcDBufferStride,
+                                   sdesc + (uint64_t)(k / 4) * kBoxStep + (uint64_t)(k % 4) * kKStep,
                                    b_desc, idesc, k % R != 0 ? 1u : 0u);
                             if (k % R == R - 1) end_chain();
                         }
                     } else {
-                        for (int k = 0; k < 4; k++) {
+                        for (int k = 0; k < nm; k++) {
                             if (in_chain == 0 && !(ok = begin_chain())) break;
-                            tc_mma(tmem + (uint32_t)b * kTcDBufferStride, sdesc + (uint64_t)k * kKStep,
+                            tc_mma(tmem + (uint32_t)b * kTcDBufferStride,
+                                   sdesc + (uint64_t)(k / 4) * kBoxStep + (uint64_t)(k % 4) * kKStep,
                                    b_desc, idesc, in_chain > 0 ? 1u : 0u);
                             if (++in_chain == R || 4 * j + k + 1 == mmas) {
                                 end_chain();
@@ -765,10 +782,10 @@ cudaError_t launch_mma_tmem_rows(int dtype, int R, const uint16_t *x, size_t row
     alignas(64) CUtensorMap map;
     const cuuint64_t gdim[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     const cuuint64_t gstride[1] = {(cuuint64_t)cols * 2};
-    const cuuint32_t box[2] = {8, 128};
+    const cuuint32_t box[2] = {kTcRowsBoxCols, 128};
     const cuuint32_t estride[2] = {1, 1};
     if (encode(&map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, (void *)x, gdim, gstride, box, estride,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     cudaError_t e = set_smem_once(k, kTcRowsSmemBytes);

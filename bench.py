@@ -6,9 +6,9 @@ synthetic inputs resident in HBM:
 
   x_sum  = 2^30 binary16 values, uniform on [-1, 1), seed 4     (2 GiB)
   x_rows = 65536 x 4096 binary16 values, N(0, 1), seed 2        (512 MiB)
-  tcr_reduce_sum(x_sum)   in MMA_CHAIN, FIXED_ORDER, SHUFFLE_TREE and
-                          MMA_CHAIN_TMEM (the tcgen05 form of MMA_CHAIN)
-  tcr_reduce_rows(x_rows) in MMA_CHAIN, FIXED_ORDER, SHUFFLE_TREE
+  tcr_reduce_sum(x_sum)   in MMA_CHAIN, FIXED_ORDER, SHUFFLE_TREE, MMA_CHAIN_TMEM
+  tcr_reduce_rows(x_rows) in MMA_CHAIN, FIXED_ORDER, SHUFFLE_TREE, MMA_CHAIN_TMEM
+  (MMA_CHAIN_TMEM: the tcgen05 / tensor-memory form of MMA_CHAIN)
 
 ``value`` is the algorithmic bytes of a step (2 bytes read per input plus
 4 bytes written per result) times the steps of all ranks, over the slowest
@@ -42,8 +42,8 @@ METRIC = "reduction GB/s and % of GB300 HBM peak (2^30 fp16 sum; 65536×4096 row
 UNIT = "GB/s"
 N_SUM = 1 << 30
 ROWS, COLS = 65536, 4096
-WORKLOAD = ("sum of 2^30 fp16 U[-1,1) seed 4 in MMA_CHAIN, FIXED_ORDER, SHUFFLE_TREE, MMA_CHAIN_TMEM"
-            " + rows 65536x4096 fp16 N(0,1) seed 2 in MMA_CHAIN, FIXED_ORDER, SHUFFLE_TREE")
+WORKLOAD = ("sum of 2^30 fp16 U[-1,1) seed 4 + rows 65536x4096 fp16 N(0,1) seed 2, each in"
+            " MMA_CHAIN, FIXED_ORDER, SHUFFLE_TREE and MMA_CHAIN_TMEM")
 FALLBACK_HBM_GBS = 6800.0
 
 # kernel launched by each call (the first, reduction launch)
@@ -55,6 +55,7 @@ KERNEL_OF = {
     "rows/FIXED_ORDER": "fixed_rows_warp_kernel",
     "rows/SHUFFLE_TREE": "shuffle_rows_warp_kernel",
     "sum/MMA_CHAIN_TMEM": "mma_tmem_kernel",
+    "rows/MMA_CHAIN_TMEM": "mma_tmem_rows_kernel",
 }
 
 
@@ -114,6 +115,7 @@ KERNEL_SOURCE = {
     "fixed_chunk_kernel": "k_fixed.cu", "fixed_rows_warp_kernel": "k_fixed.cu",
     "shuffle_block_kernel": "k_shuffle.cu", "shuffle_rows_warp_kernel": "k_shuffle.cu",
     "combine_kernel": "k_combine.cu", "mma_tmem_kernel": "k_tc05.cu",
+    "mma_tmem_rows_kernel": "k_tc05.cu",
 }
 
 
@@ -226,7 +228,7 @@ def build_calls(x_sum, x_rows):
     import torch
     import arithmetic_reduction_tensor_gb300 as tcr
     dev = x_sum.device
-    outs = torch.empty(4 + 3 * ROWS, dtype=torch.float32, device=dev)
+    outs = torch.empty(4 + 4 * ROWS, dtype=torch.float32, device=dev)
     calls = []
     for i, kind in enumerate((tcr.MMA_CHAIN, tcr.FIXED_ORDER, tcr.SHUFFLE_TREE)):
         m = tcr.Mode(kind)
@@ -248,6 +250,10 @@ def build_calls(x_sum, x_rows):
     o = outs[3 + 3 * ROWS:4 + 3 * ROWS]
     calls.append(("sum/MMA_CHAIN_TMEM", (lambda m=m, o=o: tcr.tcr_reduce_sum(x_sum, m, out=o)),
                   2 * N_SUM + 4, d["launches"]))
+    d = tcr.tcr_order_descriptor(rows=ROWS, cols=COLS, mode=m)
+    o = outs[4 + 3 * ROWS:4 + 4 * ROWS]
+    calls.append(("rows/MMA_CHAIN_TMEM", (lambda m=m, o=o: tcr.tcr_reduce_rows(x_rows, m, out=o)),
+                  2 * ROWS * COLS + 4 * ROWS, d["launches"]))
     return calls, outs
 
 
@@ -294,17 +300,18 @@ def time_e2e(xs, xr, calls_factory, steps: int, world: int):
     h_out = torch.empty(outs.numel(), dtype=torch.float32).pin_memory()
     stream = torch.cuda.current_stream()
     copy_stream = torch.cuda.Stream()
-    n_sum_calls = 3
 
     def step():
         d_sum.copy_(h_sum, non_blocking=True)
         copy_stream.wait_stream(stream)          # previous step's rows calls are done
         with torch.cuda.stream(copy_stream):
             d_rows.view(-1).copy_(h_rows, non_blocking=True)
-        for _, fn, _, _ in calls[:n_sum_calls] + calls[2 * n_sum_calls:]:
+        sums = [c for c in calls if c[0].startswith("sum/")]
+        rows_calls = [c for c in calls if c[0].startswith("rows/")]
+        for _, fn, _, _ in sums:
             fn()
         stream.wait_stream(copy_stream)
-        for _, fn, _, _ in calls[n_sum_calls:2 * n_sum_calls]:
+        for _, fn, _, _ in rows_calls:
             fn()
         h_out.copy_(outs, non_blocking=True)
 
@@ -455,6 +462,7 @@ def profile_arm(args):
             tcr.tcr_reduce_sum(x, tcr.Mode(kind))
             tcr.tcr_reduce_rows(r, tcr.Mode(kind))
         tcr.tcr_reduce_sum(x, tcr.Mode(tcr.MMA_CHAIN_TMEM))
+        tcr.tcr_reduce_rows(r, tcr.Mode(tcr.MMA_CHAIN_TMEM))
     torch.cuda.synchronize()
     print("profile case done", flush=True)
     return 0
@@ -573,6 +581,8 @@ def build_calls_meta():
         meta.append(("rows/" + tcr.KIND_NAMES[kind], 2 * ROWS * COLS + 4 * ROWS, d["launches"]))
     d = tcr.tcr_order_descriptor(n=N_SUM, mode=tcr.Mode(tcr.MMA_CHAIN_TMEM))
     meta.append(("sum/MMA_CHAIN_TMEM", 2 * N_SUM + 4, d["launches"]))
+    d = tcr.tcr_order_descriptor(rows=ROWS, cols=COLS, mode=tcr.Mode(tcr.MMA_CHAIN_TMEM))
+    meta.append(("rows/MMA_CHAIN_TMEM", 2 * ROWS * COLS + 4 * ROWS, d["launches"]))
     return meta
 
 
