@@ -28,6 +28,7 @@ __all__ = [
     "ORDER_TENSOR_CORE", "ORDER_GRID_STRIDE", "ORDER_BALANCED_TREE",
     "tcr_mode", "tcr_order_desc", "Mode", "TcrError", "c_api",
     "tcr_reduce_sum", "tcr_reduce_rows", "tcr_order_descriptor", "tcr_status_string",
+    "tcr_device_faults", "FAULT_PIPELINE_WAIT",
 ]
 
 MMA_CHAIN, SHUFFLE_TREE, FIXED_ORDER, MMA_CHAIN_TMEM = 0, 1, 2, 3
@@ -93,6 +94,8 @@ def c_api() -> ctypes.CDLL:
             lib.tcr_reduce_rows.restype = ctypes.c_int
             lib.tcr_order_descriptor.argtypes = [sz, sz, sz, tcr_mode, ctypes.POINTER(tcr_order_desc)]
             lib.tcr_order_descriptor.restype = ctypes.c_int
+            lib.tcr_device_faults.argtypes = [ctypes.POINTER(ctypes.c_uint), ctypes.c_int]
+            lib.tcr_device_faults.restype = ctypes.c_int
             lib.tcr_status_string.argtypes = [ctypes.c_int]
             lib.tcr_status_string.restype = ctypes.c_char_p
             _lib = lib
@@ -101,6 +104,18 @@ def c_api() -> ctypes.CDLL:
 
 def tcr_status_string(status: int) -> str:
     return c_api().tcr_status_string(status).decode()
+
+
+FAULT_PIPELINE_WAIT = 1
+
+
+def tcr_device_faults(clear: bool = False) -> int:
+    """The current device's fault word (``tcr_device_faults``); synchronous."""
+    v = ctypes.c_uint(0)
+    st = c_api().tcr_device_faults(ctypes.byref(v), 1 if clear else 0)
+    if st != OK:
+        raise TcrError(st, "tcr_device_faults")
+    return v.value
 
 
 # ------------------------------------------------------------------ torch

@@ -209,7 +209,8 @@ __device__ __forceinline__ int unit_tiles(size_t n, size_t u)
 
 template <int DT, int R>
 __global__ void __launch_bounds__(kTcThreads, 1)
-mma_tmem_kernel(const uint16_t *__restrict__ x, size_t n, size_t units, float *__restrict__ dst)
+mma_tmem_kernel(const uint16_t *__restrict__ x, size_t n, size_t units, float *__restrict__ dst,
+                uint32_t inject_stall)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -322,8 +323,14 @@ mma_tmem_kernel(const uint16_t *__restrict__ x, size_t n, size_t units, float *_
                 tc_fence_after();
                 return true;
             };
+            // A host-requested stall leaves the first chain unpublished, so
+            // the epilogue's wait runs out its limit (failure-path test).
+            bool withhold = inject_stall != 0u;
             auto end_chain = [&]() {
-                tc_commit(dfull_bar(b));          // chain sub-result ready
+                if (withhold)
+                    withhold = false;
+                else
+                    tc_commit(dfull_bar(b));      // chain sub-result ready
                 dphase ^= 1u << b;
                 if (++b == kTcDBuffers) b = 0;
             };
@@ -468,7 +475,7 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
 template <int DT, int R>
 __global__ void __launch_bounds__(kTcThreads, 1)
 mma_tmem_rows_kernel(const __grid_constant__ CUtensorMap tmap, size_t rows, size_t cols,
-                     size_t cpr, size_t units, float *__restrict__ dst)
+                     size_t cpr, size_t units, float *__restrict__ dst, uint32_t inject_stall)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -582,8 +589,12 @@ mma_tmem_rows_kernel(const __grid_constant__ CUtensorMap tmap, size_t rows, size
                 tc_fence_after();
                 return true;
             };
+            bool withhold = inject_stall != 0u;
             auto end_chain = [&]() {
-                tc_commit(dfull_bar(b));
+                if (withhold)
+                    withhold = false;
+                else
+                    tc_commit(dfull_bar(b));
                 dphase ^= 1u << b;
                 if (++b == kTcDBuffers) b = 0;
             };
@@ -716,14 +727,15 @@ int tmem_block_threads() { return kTcThreads; }
 int tmem_unit_log2() { return kTcUnitLog2; }
 
 cudaError_t launch_mma_tmem(int dtype, int R, const uint16_t *x, size_t n, float *dst, int grid,
-                            cudaStream_t stream)
+                            bool inject_stall, cudaStream_t stream)
 {
     void *k = dtype == kF16 ? pick_dt<kF16>(R) : pick_dt<kBF16>(R);
     if (!k) return cudaErrorInvalidValue;
     cudaError_t e = set_smem_once(k, kTcSmemBytes);
     if (e != cudaSuccess) return e;
     size_t units = tmem_units(n);
-    void *args[] = {(void *)&x, (void *)&n, (void *)&units, (void *)&dst};
+    uint32_t stall = inject_stall ? 1u : 0u;
+    void *args[] = {(void *)&x, (void *)&n, (void *)&units, (void *)&dst, (void *)&stall};
     return cudaLaunchKernel(k, dim3(grid), dim3(kTcThreads), args, kTcSmemBytes, stream);
 }
 
@@ -773,7 +785,7 @@ size_t tmem_rows_units(size_t rows, size_t cols)
 }
 
 cudaError_t launch_mma_tmem_rows(int dtype, int R, const uint16_t *x, size_t rows, size_t cols,
-                                 float *dst, int grid, cudaStream_t stream)
+                                 float *dst, int grid, bool inject_stall, cudaStream_t stream)
 {
     void *k = dtype == kF16 ? pick_rows_dt<kF16>(R) : pick_rows_dt<kBF16>(R);
     if (!k) return cudaErrorInvalidValue;
@@ -792,9 +804,18 @@ cudaError_t launch_mma_tmem_rows(int dtype, int R, const uint16_t *x, size_t row
     if (e != cudaSuccess) return e;
     size_t cpr = tmem_rows_chunks(cols);
     size_t units = tmem_rows_units(rows, cols);
+    uint32_t stall = inject_stall ? 1u : 0u;
     void *args[] = {(void *)&map, (void *)&rows, (void *)&cols, (void *)&cpr, (void *)&units,
-                    (void *)&dst};
+                    (void *)&dst, (void *)&stall};
     return cudaLaunchKernel(k, dim3(grid), dim3(kTcThreads), args, kTcRowsSmemBytes, stream);
+}
+
+cudaError_t read_device_faults(unsigned int *flags, bool clear)
+{
+    cudaError_t e = cudaMemcpyFromSymbol(flags, g_tc05_fault, sizeof(unsigned int));
+    if (e != cudaSuccess || !clear) return e;
+    const unsigned int zero = 0u;
+    return cudaMemcpyToSymbol(g_tc05_fault, &zero, sizeof(unsigned int));
 }
 
 }  // namespace tcr

@@ -56,8 +56,10 @@ cudaError_t launch_mma_rows(int dtype, bool aligned, int R, const uint16_t *x, s
 // ---- MMA_CHAIN on tcgen05 (bulk copies into shared memory, D in TMEM):
 // one persistent CTA per SM; dst[u] is the partial of work unit u (2^16
 // inputs, see tmem_unit_log2); x must be 16-byte aligned.
+// inject_stall: withhold the first chain's publication so that a wait runs
+// out its limit (tests of the failure path only).
 cudaError_t launch_mma_tmem(int dtype, int R, const uint16_t *x, size_t n, float *dst, int grid,
-                            cudaStream_t stream);
+                            bool inject_stall, cudaStream_t stream);
 size_t tmem_units(size_t n);
 int tmem_block_threads();
 int tmem_unit_log2();
@@ -66,7 +68,10 @@ int tmem_unit_log2();
 // partial over column chunk c (tmem_rows_chunks(cols) chunks per row).
 // x must be 16-byte aligned and cols a multiple of 8, rows and cols < 2^31.
 cudaError_t launch_mma_tmem_rows(int dtype, int R, const uint16_t *x, size_t rows, size_t cols,
-                                 float *dst, int grid, cudaStream_t stream);
+                                 float *dst, int grid, bool inject_stall, cudaStream_t stream);
+// The device word the tcgen05 kernels set when a wait gave up (bit 0);
+// synchronous; optionally cleared after reading.
+cudaError_t read_device_faults(unsigned int *flags, bool clear);
 size_t tmem_rows_chunks(size_t cols);
 size_t tmem_rows_units(size_t rows, size_t cols);
 

@@ -327,10 +327,11 @@ tcr_status run_plan(const Plan &p, const uint16_t *x, float *out, cudaStream_t s
     cudaError_t e = cudaSuccess;
     switch (p.path) {
     case kPathTmem:
-        e = launch_mma_tmem(p.dtype, p.R, x, p.seg_len, dst, p.grid, s);
+        e = launch_mma_tmem(p.dtype, p.R, x, p.seg_len, dst, p.grid, fault_injected("stall"), s);
         break;
     case kPathTmemRows:
-        e = launch_mma_tmem_rows(p.dtype, p.R, x, p.segments, p.seg_len, dst, p.grid, s);
+        e = launch_mma_tmem_rows(p.dtype, p.R, x, p.segments, p.seg_len, dst, p.grid,
+                                 fault_injected("stall"), s);
         break;
     case kPathChunk:
         e = p.kind == TCR_FIXED_ORDER
@@ -450,6 +451,13 @@ tcr_status tcr_order_descriptor(size_t n, size_t rows, size_t cols, tcr_mode mod
     desc->partials = p.partials;
     desc->launches = p.launches;
     return TCR_OK;
+}
+
+tcr_status tcr_device_faults(unsigned int *flags, int clear)
+{
+    if (!flags) return TCR_ERR_INVALID_ARG;
+    if (current_device() < 0) return TCR_ERR_CUDA;
+    return read_device_faults(flags, clear != 0) == cudaSuccess ? TCR_OK : TCR_ERR_CUDA;
 }
 
 const char *tcr_status_string(tcr_status status)

@@ -237,6 +237,20 @@ typedef struct {
 TCR_API tcr_status tcr_order_descriptor(size_t n, size_t rows, size_t cols, tcr_mode mode,
                                 tcr_order_desc *desc);
 
+/*
+ * tcr_device_faults -- the fault word of the current device: bit 0
+ * (TCR_FAULT_PIPELINE_WAIT) is set when a wait inside a TCR_MMA_CHAIN_TMEM
+ * kernel gave up after its limit of about one second (the kernel then
+ * drained its own copies and tensor-core work, freed its tensor memory and
+ * wrote NaN partials, so that call's result is NaN).  The word stays set
+ * until cleared: clear != 0 resets it after reading.  Synchronous with
+ * respect to the device (call it after the work in question has finished).
+ * Returns TCR_ERR_INVALID_ARG for a NULL flags, TCR_ERR_CUDA if the device
+ * cannot be read.
+ */
+#define TCR_FAULT_PIPELINE_WAIT 1u
+TCR_API tcr_status tcr_device_faults(unsigned int *flags, int clear);
+
 /* Static English text for a status code; never NULL. */
 TCR_API const char *tcr_status_string(tcr_status status);
 

@@ -131,6 +131,10 @@ def test_rows_descriptor_short_rows_need_no_scratch(lib):
         assert d["partials"] == 0 and d["launches"] == 1 and d["segments"] == 65536
 
 
+def test_device_faults_rejects_null(lib):
+    assert lib.tcr_device_faults(None, 0) == tcr.ERR_INVALID_ARG
+
+
 def test_python_binding_fails_loudly_without_cuda_tensors():
     torch = pytest.importorskip("torch")
     with pytest.raises(ValueError):
