@@ -8,19 +8,9 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
-namespace tcr {
+#include "config.cuh"
 
-// Inputs per warp group of the tree kernels: 8 warp loads of 256 inputs.
-constexpr size_t kGroup = 2048;
-// Inputs per warp of one CTA work unit (chunk) of the chunked kernels.
-constexpr int kWarpSpanLog2 = 13;
-// Longest row served by one warp; longer rows go through the chunked
-// kernels (FIXED_ORDER, MMA_CHAIN) or the block team (SHUFFLE_TREE).
-constexpr size_t kRowsWarpMaxCols = 16384;
-// CTA size of the one-warp-per-row kernels, and the CTAs per SM their
-// register budget is set for (65536 / (256 * 3) -> up to 80 registers).
-constexpr int kRowsBlock = 256;
-constexpr int kRowsMinCtas = 3;
+namespace tcr {
 
 // ---- FIXED_ORDER (balanced tree over index order)
 // Chunked: CTA work unit u = (segment u / cps, chunk u % cps); the chunk of

@@ -109,7 +109,8 @@ def load_peaks():
 
 
 # source file of each kernel; a recorded DRAM traffic figure is stale once
-# that file or the shared device headers change
+# that file or the shared device headers (helpers, work-split constants,
+# warp stream) change
 KERNEL_SOURCE = {
     "mma_chunk_kernel": "k_mma.cu", "mma_rows_warp_kernel": "k_mma.cu",
     "fixed_chunk_kernel": "k_fixed.cu", "fixed_rows_warp_kernel": "k_fixed.cu",
@@ -123,7 +124,7 @@ def source_hash(kernel: str) -> str:
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "arithmetic_reduction_tensor_gb300", "csrc")
-    for f in ("common.cuh", "kernels.cuh", "stream.cuh", KERNEL_SOURCE[kernel]):
+    for f in ("common.cuh", "config.cuh", "stream.cuh", KERNEL_SOURCE[kernel]):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
