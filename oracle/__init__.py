@@ -19,6 +19,8 @@ Functions (sources are cited in ``tcr_oracle.c``):
 ``shuffle_tree``       declared order of the conventional reduction
                        (grid-stride accumulation, warp butterfly, block tree,
                        grid tree).
+``*_sq``, ``exact_sum_squares``
+                       the same over the leaves x_i^2 (sum of squares).
 ``*_rows``             the same, one result per row.
 """
 from __future__ import annotations
@@ -70,11 +72,19 @@ def _load():
             lib.oracle_exact_sum_rows.restype = None
             lib.oracle_fixed_order_f32.argtypes = [u16p, sz, i, i]
             lib.oracle_fixed_order_f32.restype = ctypes.c_float
-            lib.oracle_fixed_order_rows_f32.argtypes = [u16p, sz, sz, i, i, f32p]
+            lib.oracle_exact_sum_squares.argtypes = [u16p, sz, i, i, f64p, f64p]
+            lib.oracle_exact_sum_squares.restype = None
+            lib.oracle_exact_sum_squares_rows.argtypes = [u16p, sz, sz, i, i, f64p, f64p]
+            lib.oracle_exact_sum_squares_rows.restype = None
+            lib.oracle_fixed_order_sq_f32.argtypes = [u16p, sz, i, i]
+            lib.oracle_fixed_order_sq_f32.restype = ctypes.c_float
+            lib.oracle_shuffle_tree_sq_f32.argtypes = [u16p, sz, i, i, i, i]
+            lib.oracle_shuffle_tree_sq_f32.restype = ctypes.c_float
+            lib.oracle_fixed_order_rows_f32.argtypes = [u16p, sz, sz, i, i, i, f32p]
             lib.oracle_fixed_order_rows_f32.restype = None
             lib.oracle_shuffle_tree_f32.argtypes = [u16p, sz, i, i, i, i]
             lib.oracle_shuffle_tree_f32.restype = ctypes.c_float
-            lib.oracle_shuffle_tree_rows_f32.argtypes = [u16p, sz, sz, i, i, i, i, f32p]
+            lib.oracle_shuffle_tree_rows_f32.argtypes = [u16p, sz, sz, i, i, i, i, i, f32p]
             lib.oracle_shuffle_tree_rows_f32.restype = None
             lib.oracle_leaves_f32.argtypes = [u16p, sz, i, f32p]
             lib.oracle_leaves_f32.restype = None
@@ -109,12 +119,22 @@ def exact_sum(x, dtype: int, threads: int | None = None) -> tuple[float, float]:
     return s.value, m.value
 
 
-def exact_sum_rows(x, dtype: int, threads: int | None = None):
+def exact_sum_squares(x, dtype: int, threads: int | None = None) -> tuple[float, float]:
+    """(exact sum of x_i^2 rounded to binary64, the same value)."""
+    a = _bits(x).reshape(-1)
+    s, m = ctypes.c_double(), ctypes.c_double()
+    _load().oracle_exact_sum_squares(_u16p(a), a.size, dtype, threads or default_threads(),
+                                     ctypes.byref(s), ctypes.byref(m))
+    return s.value, m.value
+
+
+def exact_sum_rows(x, dtype: int, threads: int | None = None, squares: bool = False):
     a = _bits(x)
     rows, cols = a.shape
     s = np.empty(rows, np.float64)
     m = np.empty(rows, np.float64)
-    _load().oracle_exact_sum_rows(
+    fn = _load().oracle_exact_sum_squares_rows if squares else _load().oracle_exact_sum_rows
+    fn(
         _u16p(a), rows, cols, dtype, threads or default_threads(),
         s.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
         m.ctypes.data_as(ctypes.POINTER(ctypes.c_double)))
@@ -127,11 +147,19 @@ def fixed_order(x, dtype: int, threads: int | None = None) -> np.float32:
                                                      threads or default_threads()))
 
 
-def fixed_order_rows(x, dtype: int, threads: int | None = None) -> np.ndarray:
+def fixed_order_sq(x, dtype: int, threads: int | None = None) -> np.float32:
+    """Balanced binary32 tree over the leaves x_i^2."""
+    a = _bits(x).reshape(-1)
+    return np.float32(_load().oracle_fixed_order_sq_f32(_u16p(a), a.size, dtype,
+                                                        threads or default_threads()))
+
+
+def fixed_order_rows(x, dtype: int, threads: int | None = None,
+                     squares: bool = False) -> np.ndarray:
     a = _bits(x)
     rows, cols = a.shape
     out = np.empty(rows, np.float32)
-    _load().oracle_fixed_order_rows_f32(_u16p(a), rows, cols, dtype,
+    _load().oracle_fixed_order_rows_f32(_u16p(a), rows, cols, dtype, 1 if squares else 0,
                                         threads or default_threads(),
                                         out.ctypes.data_as(ctypes.POINTER(ctypes.c_float)))
     return out
@@ -144,12 +172,21 @@ def shuffle_tree(x, dtype: int, team_threads: int, team_blocks: int,
         _u16p(a), a.size, dtype, team_threads, team_blocks, threads or default_threads()))
 
 
+def shuffle_tree_sq(x, dtype: int, team_threads: int, team_blocks: int,
+                    threads: int | None = None) -> np.float32:
+    """The declared SHUFFLE_TREE order over the leaves x_i^2."""
+    a = _bits(x).reshape(-1)
+    return np.float32(_load().oracle_shuffle_tree_sq_f32(
+        _u16p(a), a.size, dtype, team_threads, team_blocks, threads or default_threads()))
+
+
 def shuffle_tree_rows(x, dtype: int, team_threads: int, team_blocks: int,
-                      threads: int | None = None) -> np.ndarray:
+                      threads: int | None = None, squares: bool = False) -> np.ndarray:
     a = _bits(x)
     rows, cols = a.shape
     out = np.empty(rows, np.float32)
-    _load().oracle_shuffle_tree_rows_f32(_u16p(a), rows, cols, dtype, team_threads,
+    _load().oracle_shuffle_tree_rows_f32(_u16p(a), rows, cols, dtype, 1 if squares else 0,
+                                         team_threads,
                                          team_blocks, threads or default_threads(),
                                          out.ctypes.data_as(ctypes.POINTER(ctypes.c_float)))
     return out

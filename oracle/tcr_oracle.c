@@ -106,13 +106,15 @@ static float leaf_f32(uint16_t h, int dtype)
 }
 
 /* ------------------------------------------------------------------ */
-/* Exact sum: a two's-complement fixed-point accumulator of 5 x 64 bits
- * whose bit 0 weighs 2^-133 (the smallest bfloat16 subnormal; the smallest
- * binary16 subnormal 2^-24 is a multiple of it).  The largest bfloat16 is
- * below 2^128, so 2^40 terms stay below 2^168, far inside 319 bits. */
+/* Exact sums: a two's-complement fixed-point accumulator of 9 x 64 bits
+ * whose bit 0 weighs 2^-266 -- the square of the smallest bfloat16
+ * subnormal 2^-133, so that every input (a multiple of 2^-133) and every
+ * square of an input (a multiple of 2^-266) is an integer multiple of it.
+ * The largest square of a bfloat16 is below 2^256, so 2^40 terms stay below
+ * 2^296, far inside 575 bits. */
 
-#define ACC_LIMBS 5
-#define ACC_LSB_EXP (-133)
+#define ACC_LIMBS 9
+#define ACC_LSB_EXP (-266)
 
 typedef struct { uint64_t w[ACC_LIMBS]; } acc_t;
 
@@ -179,10 +181,11 @@ static double acc_to_double(const acc_t *a)
 }
 
 /* Exact summation by exponent buckets: every finite input is +-m * 2^e with
- * an integer m < 2^11 and one of 254 exponents e >= -133.  Integer sums of m
- * per exponent are exact (|sum| < 2^11 * n < 2^63 for n < 2^52), and the
- * buckets are then added into the long accumulator, m_e * 2^e each. */
-#define N_EXP 256
+ * an integer m < 2^11 and e >= -133, and its square is m^2 * 2^(2e) with
+ * m^2 < 2^22 and 2e >= -266.  Integer sums of m (or m^2) per exponent are
+ * exact (below 2^22 * n < 2^63 for n < 2^40), and the buckets are then added
+ * into the long accumulator, m_e * 2^e each.  Bucket index = e + 266. */
+#define N_EXP 512
 
 typedef struct {
     int64_t signed_m[N_EXP];    /* sum of +-m for inputs with exponent e = index - 133 */
@@ -190,15 +193,26 @@ typedef struct {
     size_t pos_inf, neg_inf, nan;
 } exact_state_t;
 
-static void exact_accumulate(exact_state_t *st, const uint16_t *x, size_t n, int dtype)
+/* squares != 0: accumulate x^2 (always >= 0) instead of x. */
+static void exact_accumulate(exact_state_t *st, const uint16_t *x, size_t n, int dtype, int squares)
 {
     for (size_t i = 0; i < n; i++) {
         decoded_t d = decode16(x[i], dtype);
         if (d.special == 2) { st->nan++; continue; }
-        if (d.special == 1) { if (d.neg) st->neg_inf++; else st->pos_inf++; continue; }
-        int pos = d.e - ACC_LSB_EXP;
-        st->signed_m[pos] += d.neg ? -(int64_t)d.m : (int64_t)d.m;
-        st->abs_m[pos] += d.m;
+        if (d.special == 1) {
+            if (d.neg && !squares) st->neg_inf++; else st->pos_inf++;
+            continue;
+        }
+        if (squares) {
+            int pos = 2 * d.e - ACC_LSB_EXP;
+            uint64_t m2 = (uint64_t)d.m * (uint64_t)d.m;
+            st->signed_m[pos] += (int64_t)m2;
+            st->abs_m[pos] += m2;
+        } else {
+            int pos = d.e - ACC_LSB_EXP;
+            st->signed_m[pos] += d.neg ? -(int64_t)d.m : (int64_t)d.m;
+            st->abs_m[pos] += d.m;
+        }
     }
 }
 
@@ -210,8 +224,8 @@ static void exact_accumulate(exact_state_t *st, const uint16_t *x, size_t n, int
  * Threads only split the index range; integer addition is exact, so the
  * result does not depend on the thread count.
  */
-void oracle_exact_sum(const uint16_t *x, size_t n, int dtype, int threads,
-                      double *sum_out, double *abs_out)
+static void exact_sum_any(const uint16_t *x, size_t n, int dtype, int squares, int threads,
+                          double *sum_out, double *abs_out)
 {
     int nt = threads > 0 ? threads : 1;
 #ifndef _OPENMP
@@ -224,7 +238,7 @@ void oracle_exact_sum(const uint16_t *x, size_t n, int dtype, int threads,
         size_t lo = (size_t)t * per, hi = lo + per;
         if (lo > n) lo = n;
         if (hi > n) hi = n;
-        exact_accumulate(&parts[t], x + lo, hi - lo, dtype);
+        exact_accumulate(&parts[t], x + lo, hi - lo, dtype, squares);
     }
     exact_state_t tot;
     memset(&tot, 0, sizeof tot);
@@ -261,13 +275,36 @@ void oracle_exact_sum(const uint16_t *x, size_t n, int dtype, int threads,
     *abs_out = acc_to_double(&abs_sum);
 }
 
+void oracle_exact_sum(const uint16_t *x, size_t n, int dtype, int threads, double *sum_out,
+                      double *abs_out)
+{
+    exact_sum_any(x, n, dtype, 0, threads, sum_out, abs_out);
+}
+
+/* The exact sum of x_i^2, rounded once to binary64 (abs_out receives the
+ * same value: every term is non-negative). */
+void oracle_exact_sum_squares(const uint16_t *x, size_t n, int dtype, int threads,
+                              double *sum_out, double *abs_out)
+{
+    exact_sum_any(x, n, dtype, 1, threads, sum_out, abs_out);
+}
+
 void oracle_exact_sum_rows(const uint16_t *x, size_t rows, size_t cols, int dtype,
                            int threads, double *sum_out, double *abs_out)
 {
     int nt = threads > 0 ? threads : 1;
 #pragma omp parallel for num_threads(nt) schedule(dynamic, 64)
     for (size_t r = 0; r < rows; r++)
-        oracle_exact_sum(x + r * cols, cols, dtype, 1, &sum_out[r], &abs_out[r]);
+        exact_sum_any(x + r * cols, cols, dtype, 0, 1, &sum_out[r], &abs_out[r]);
+}
+
+void oracle_exact_sum_squares_rows(const uint16_t *x, size_t rows, size_t cols, int dtype,
+                                   int threads, double *sum_out, double *abs_out)
+{
+    int nt = threads > 0 ? threads : 1;
+#pragma omp parallel for num_threads(nt) schedule(dynamic, 64)
+    for (size_t r = 0; r < rows; r++)
+        exact_sum_any(x + r * cols, cols, dtype, 1, 1, &sum_out[r], &abs_out[r]);
 }
 
 /* ------------------------------------------------------------------ */
@@ -280,17 +317,27 @@ static int ceil_log2(size_t n)
     return h;
 }
 
+/* The leaf of input h: its binary32 value, or for sums of squares the
+ * binary32 product of that value with itself (one rounding to nearest even;
+ * the product of two binary16 or bfloat16 values is exact in binary64). */
+static float leaf_op(uint16_t h, int dtype, int squares)
+{
+    float f = leaf_f32(h, dtype);
+    if (!squares) return f;
+    return (float)((double)f * (double)f);
+}
+
 /* Node of height h whose leftmost leaf is input lo: the sum of its two
  * children, left + right, in binary32.  Leaves past n are the -0.0 pad.
  * A subtree that lies wholly in the pad has the value -0.0 (every leaf is
  * -0.0 and -0.0 + -0.0 = -0.0), so it is returned without descending. */
-static float tree_node16(const uint16_t *x, size_t n, int dtype, size_t lo, int h)
+static float tree_node16(const uint16_t *x, size_t n, int dtype, int squares, size_t lo, int h)
 {
     if (lo >= n) return -0.0f;
-    if (h == 0) return leaf_f32(x[lo], dtype);
+    if (h == 0) return leaf_op(x[lo], dtype, squares);
     size_t half = (size_t)1 << (h - 1);
-    float left = tree_node16(x, n, dtype, lo, h - 1);
-    float right = tree_node16(x, n, dtype, lo + half, h - 1);
+    float left = tree_node16(x, n, dtype, squares, lo, h - 1);
+    float right = tree_node16(x, n, dtype, squares, lo + half, h - 1);
     return left + right;
 }
 
@@ -317,7 +364,7 @@ static float tree_f32(const float *a, size_t m)
  * top levels are then formed from those subtree values in the same shape,
  * so the result is that of the single recursive definition.
  */
-float oracle_fixed_order_f32(const uint16_t *x, size_t n, int dtype, int threads)
+static float fixed_order_any(const uint16_t *x, size_t n, int dtype, int squares, int threads)
 {
     if (n == 0) return 0.0f;
     int H = ceil_log2(n);
@@ -327,19 +374,30 @@ float oracle_fixed_order_f32(const uint16_t *x, size_t n, int dtype, int threads
     int nt = threads > 0 ? threads : 1;
 #pragma omp parallel for num_threads(nt) schedule(dynamic, 1)
     for (size_t i = 0; i < parts; i++)
-        node[i] = tree_node16(x, n, dtype, i << (H - k), H - k);
+        node[i] = tree_node16(x, n, dtype, squares, i << (H - k), H - k);
     float r = tree_node32(node, parts, 0, k);
     free(node);
     return r;
 }
 
+float oracle_fixed_order_f32(const uint16_t *x, size_t n, int dtype, int threads)
+{
+    return fixed_order_any(x, n, dtype, 0, threads);
+}
+
+/* The same tree over the leaves x_i^2 (sum of squares). */
+float oracle_fixed_order_sq_f32(const uint16_t *x, size_t n, int dtype, int threads)
+{
+    return fixed_order_any(x, n, dtype, 1, threads);
+}
+
 void oracle_fixed_order_rows_f32(const uint16_t *x, size_t rows, size_t cols, int dtype,
-                                 int threads, float *out)
+                                 int squares, int threads, float *out)
 {
     int nt = threads > 0 ? threads : 1;
 #pragma omp parallel for num_threads(nt) schedule(dynamic, 64)
     for (size_t r = 0; r < rows; r++)
-        out[r] = oracle_fixed_order_f32(x + r * cols, cols, dtype, 1);
+        out[r] = fixed_order_any(x + r * cols, cols, dtype, squares, 1);
 }
 
 /* ------------------------------------------------------------------ */
@@ -360,17 +418,18 @@ void oracle_fixed_order_rows_f32(const uint16_t *x, size_t rows, size_t cols, in
  *   5. segment value  = balanced tree over the G block values in block
  *                       order, padded with -0.0.
  */
-static float vector_tree8(const uint16_t *x, size_t L, int dtype, size_t v)
+static float vector_tree8(const uint16_t *x, size_t L, int dtype, int squares, size_t v)
 {
     float e[8];
     for (int k = 0; k < 8; k++) {
         size_t i = 8 * v + (size_t)k;
-        e[k] = i < L ? leaf_f32(x[i], dtype) : -0.0f;
+        e[k] = i < L ? leaf_op(x[i], dtype, squares) : -0.0f;
     }
     return ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
 }
 
-static float shuffle_block_value(const uint16_t *x, size_t L, int dtype, int Bt, int G, int b)
+static float shuffle_block_value(const uint16_t *x, size_t L, int dtype, int squares, int Bt, int G,
+                                 int b)
 {
     size_t T = (size_t)G * (size_t)Bt;
     size_t nvec = (L + 7) / 8;
@@ -381,7 +440,7 @@ static float shuffle_block_value(const uint16_t *x, size_t L, int dtype, int Bt,
         for (int j = 0; j < 32; j++) {
             size_t g = (size_t)b * (size_t)Bt + (size_t)w * 32 + (size_t)j;
             float acc = -0.0f;
-            for (size_t v = g; v < nvec; v += T) acc = acc + vector_tree8(x, L, dtype, v);
+            for (size_t v = g; v < nvec; v += T) acc = acc + vector_tree8(x, L, dtype, squares, v);
             lane[j] = acc;
         }
         for (int off = 16; off >= 1; off /= 2) {
@@ -393,26 +452,39 @@ static float shuffle_block_value(const uint16_t *x, size_t L, int dtype, int Bt,
     return tree_f32(warp_value, (size_t)W);
 }
 
-float oracle_shuffle_tree_f32(const uint16_t *x, size_t L, int dtype, int Bt, int G, int threads)
+static float shuffle_tree_any(const uint16_t *x, size_t L, int dtype, int squares, int Bt, int G,
+                              int threads)
 {
     if (L == 0) return 0.0f;
     if (Bt < 32 || Bt > 1024 || (Bt & (Bt - 1)) != 0 || G < 1) return NAN;
     float *block = (float *)malloc((size_t)G * sizeof(float));
     int nt = threads > 0 ? threads : 1;
 #pragma omp parallel for num_threads(nt) schedule(dynamic, 1)
-    for (int b = 0; b < G; b++) block[b] = shuffle_block_value(x, L, dtype, Bt, G, b);
+    for (int b = 0; b < G; b++) block[b] = shuffle_block_value(x, L, dtype, squares, Bt, G, b);
     float r = tree_f32(block, (size_t)G);
     free(block);
     return r;
 }
 
+float oracle_shuffle_tree_f32(const uint16_t *x, size_t L, int dtype, int Bt, int G, int threads)
+{
+    return shuffle_tree_any(x, L, dtype, 0, Bt, G, threads);
+}
+
+/* The same declared order over the leaves x_i^2 (sum of squares). */
+float oracle_shuffle_tree_sq_f32(const uint16_t *x, size_t L, int dtype, int Bt, int G,
+                                 int threads)
+{
+    return shuffle_tree_any(x, L, dtype, 1, Bt, G, threads);
+}
+
 void oracle_shuffle_tree_rows_f32(const uint16_t *x, size_t rows, size_t cols, int dtype,
-                                  int Bt, int G, int threads, float *out)
+                                  int squares, int Bt, int G, int threads, float *out)
 {
     int nt = threads > 0 ? threads : 1;
 #pragma omp parallel for num_threads(nt) schedule(dynamic, 64)
     for (size_t r = 0; r < rows; r++)
-        out[r] = oracle_shuffle_tree_f32(x + r * cols, cols, dtype, Bt, G, 1);
+        out[r] = shuffle_tree_any(x + r * cols, cols, dtype, squares, Bt, G, 1);
 }
 
 /* Exact binary32 value of each input (used by the tests to compare the

@@ -344,3 +344,107 @@ def test_shuffle_tree_rows_match_whole_rows():
 def test_shuffle_tree_empty_is_positive_zero():
     assert oracle.shuffle_tree(np.zeros(0, np.uint16), F16, 32, 1).tobytes() == \
         np.float32(0.0).tobytes()
+
+
+# ---------------------------------------------------------------- sum of squares
+
+def np_square_leaves(bits, dtype):
+    """binary32 squares by numpy (one rounding of the exact product)."""
+    v = np_leaves(bits, dtype).astype(np.float32)
+    with np.errstate(over="ignore", under="ignore", invalid="ignore"):
+        return v * v
+
+
+@pytest.mark.parametrize("dtype", [F16, BF16])
+@pytest.mark.parametrize("seed", range(6))
+def test_exact_sum_squares_brute_force(dtype, seed):
+    rng = np.random.default_rng(200 + seed)
+    n = int(rng.integers(1, 65))
+    bits = np.concatenate([random_finite(rng, n, dtype),
+                           np.array(special_patterns(dtype), np.uint16)])
+    s, a = oracle.exact_sum_squares(bits, dtype, threads=3)
+    vals = np_leaves(bits, dtype).astype(np.float64)
+    exact = sum((Fraction(float(v)) ** 2 for v in vals), Fraction(0))
+    assert s == float(exact) and a == s
+
+
+@pytest.mark.parametrize("dtype", [F16, BF16])
+def test_exact_sum_squares_invariants(dtype):
+    bits = synth.generate(300_001, "normal", dtype, seed=31)
+    s1, _ = oracle.exact_sum_squares(bits, dtype)
+    s2, _ = oracle.exact_sum_squares(bits ^ np.uint16(0x8000), dtype)    # x -> -x
+    assert s1 == s2 > 0
+    three = int(np.float16(3.0).view(np.uint16)) if dtype == F16 else 0x4040
+    assert oracle.exact_sum_squares(np.full(1_000_003, three, np.uint16), dtype)[0] == 9.0 * 1_000_003
+    # the extremes of the formats: bfloat16 squares reach 2^-266 and 2^255
+    if dtype == BF16:
+        tiny = np.full(7, 0x0001, np.uint16)
+        assert oracle.exact_sum_squares(tiny, BF16)[0] == 7 * 2.0 ** -266
+        big = np.array([0x7F7F], np.uint16)
+        b = float(np_leaves(big, BF16)[0])
+        assert oracle.exact_sum_squares(big, BF16)[0] == float(Fraction(b) ** 2)
+    inf = 0x7C00 if dtype == F16 else 0x7F80
+    assert oracle.exact_sum_squares(np.array([inf | 0x8000, inf], np.uint16), dtype)[0] == math.inf
+
+
+def test_fixed_order_sq_hand_worked_tree(golden_dir):
+    # squares of [2^-12 x8, 1.0, 2^-12 x7] are the leaves of the hand-worked
+    # 16-leaf tree: 2^-24 x8, 1.0, 2^-24 x7 -> 1 + 7 * 2^-23
+    _, vals = _read_tree16(golden_dir)
+    bits = np.array([0x0C00] * 8 + [0x3C00] + [0x0C00] * 7, np.uint16)
+    assert oracle.fixed_order_sq(bits, F16, threads=1) == np.float32(float(Fraction(vals["fixed_order"])))
+
+
+@pytest.mark.parametrize("dtype", [F16, BF16])
+@pytest.mark.parametrize("n", [1, 7, 8, 9, 255, 256, 1000, 4097, 65537, 100_003])
+def test_fixed_order_sq_matches_levelwise_numpy(dtype, n):
+    rng = np.random.default_rng(n + 7)
+    bits = random_finite(rng, n, dtype) if n < 5000 else synth.generate(n, "normal", dtype, seed=n)
+    got = oracle.fixed_order_sq(bits, dtype, threads=4)
+    assert same_f32(got, np_tree(np_square_leaves(bits, dtype)))
+
+
+@np.errstate(over="ignore", invalid="ignore")
+def np_shuffle_sq(bits, dtype, bt, g):
+    """Vectorised emulation of the declared order over squared leaves."""
+    v = np_square_leaves(bits, dtype)
+    L = v.size
+    nvec = (L + 7) // 8
+    e = np.full(nvec * 8, -0.0, np.float32)
+    e[:L] = v
+    e = e.reshape(nvec, 8)
+    vec = ((e[:, 0] + e[:, 1]) + (e[:, 2] + e[:, 3])) + ((e[:, 4] + e[:, 5]) + (e[:, 6] + e[:, 7]))
+    T = bt * g
+    acc = np.full(T, -0.0, np.float32)
+    for start in range(0, nvec, T):
+        m = min(T, nvec - start)
+        acc[:m] = acc[:m] + vec[start:start + m]
+    lanes = acc.reshape(-1, 32)
+    idx = np.arange(32)
+    for off in (16, 8, 4, 2, 1):
+        lanes = lanes + lanes[:, idx ^ off]
+    warp = lanes[:, 0].reshape(g, bt // 32)
+    while warp.shape[1] > 1:
+        warp = warp[:, 0::2] + warp[:, 1::2]
+    return np_tree(warp[:, 0])
+
+
+@pytest.mark.parametrize("dtype", [F16, BF16])
+@pytest.mark.parametrize("L,bt,g", [(9, 32, 1), (1000, 32, 1), (8192, 32, 1), (10_000, 128, 3),
+                                    (70_001, 32, 7), (100_000, 512, 5)])
+def test_shuffle_tree_sq_matches_vectorised_emulation(dtype, L, bt, g):
+    rng = np.random.default_rng(L + 11)
+    bits = random_finite(rng, L, dtype) if L < 5000 else synth.generate(L, "normal", dtype, seed=L)
+    assert same_f32(oracle.shuffle_tree_sq(bits, dtype, bt, g, threads=3),
+                    np_shuffle_sq(bits, dtype, bt, g))
+
+
+def test_sum_squares_rows_match_whole_rows():
+    x = synth.generate(19 * 9001, "normal", F16, seed=33).reshape(19, 9001)
+    s, _ = oracle.exact_sum_rows(x, F16, squares=True)
+    f = oracle.fixed_order_rows(x, F16, squares=True)
+    t = oracle.shuffle_tree_rows(x, F16, 128, 2, squares=True)
+    for r in range(19):
+        assert s[r] == oracle.exact_sum_squares(x[r], F16, threads=1)[0]
+        assert same_f32(f[r], oracle.fixed_order_sq(x[r], F16, threads=1))
+        assert same_f32(t[r], oracle.shuffle_tree_sq(x[r], F16, 128, 2, threads=1))
