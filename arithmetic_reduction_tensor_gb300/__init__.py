@@ -27,8 +27,8 @@ __all__ = [
     "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_CUDA",
     "ORDER_TENSOR_CORE", "ORDER_GRID_STRIDE", "ORDER_BALANCED_TREE",
     "tcr_mode", "tcr_order_desc", "Mode", "TcrError", "c_api",
-    "tcr_reduce_sum", "tcr_reduce_rows", "tcr_order_descriptor", "tcr_status_string",
-    "tcr_device_faults", "FAULT_PIPELINE_WAIT",
+    "tcr_reduce_sum", "tcr_reduce_rows", "tcr_reduce_sum_squares", "tcr_reduce_rows_sum_squares",
+    "tcr_order_descriptor", "tcr_status_string", "tcr_device_faults", "FAULT_PIPELINE_WAIT",
 ]
 
 MMA_CHAIN, SHUFFLE_TREE, FIXED_ORDER, MMA_CHAIN_TMEM = 0, 1, 2, 3
@@ -92,6 +92,10 @@ def c_api() -> ctypes.CDLL:
             lib.tcr_reduce_sum.restype = ctypes.c_int
             lib.tcr_reduce_rows.argtypes = [vp, sz, sz, vp, tcr_mode, vp]
             lib.tcr_reduce_rows.restype = ctypes.c_int
+            lib.tcr_reduce_sum_squares.argtypes = [vp, sz, vp, tcr_mode, vp]
+            lib.tcr_reduce_sum_squares.restype = ctypes.c_int
+            lib.tcr_reduce_rows_sum_squares.argtypes = [vp, sz, sz, vp, tcr_mode, vp]
+            lib.tcr_reduce_rows_sum_squares.restype = ctypes.c_int
             lib.tcr_order_descriptor.argtypes = [sz, sz, sz, tcr_mode, ctypes.POINTER(tcr_order_desc)]
             lib.tcr_order_descriptor.restype = ctypes.c_int
             lib.tcr_device_faults.argtypes = [ctypes.POINTER(ctypes.c_uint), ctypes.c_int]
@@ -152,23 +156,21 @@ def _check_out(out, device, count: int):
     return out
 
 
-def tcr_reduce_sum(x, mode: tcr_mode, out=None, stream=None):
-    """out[0] = sum of the contiguous CUDA tensor ``x`` (``tcr_reduce_sum``)."""
+def _sum_call(name, x, mode, out, stream):
     import torch
     if not x.is_cuda or not x.is_contiguous():
         raise ValueError("x must be a contiguous CUDA tensor")
     m = tcr_mode(mode.kind, mode.R, mode.block_threads, _dtype_code(x, mode))
     out = _check_out(out, x.device, 1)
     with torch.cuda.device(x.device):
-        st = c_api().tcr_reduce_sum(x.data_ptr() if x.numel() else None, x.numel(),
+        st = getattr(c_api(), name)(x.data_ptr() if x.numel() else None, x.numel(),
                                     out.data_ptr(), m, _stream_handle(x.device, stream))
     if st != OK:
-        raise TcrError(st, "tcr_reduce_sum")
+        raise TcrError(st, name)
     return out
 
 
-def tcr_reduce_rows(x, mode: tcr_mode, out=None, stream=None):
-    """out[r] = sum of row r of the contiguous 2-D CUDA tensor ``x`` (``tcr_reduce_rows``)."""
+def _rows_call(name, x, mode, out, stream):
     import torch
     if not x.is_cuda or not x.is_contiguous() or x.dim() != 2:
         raise ValueError("x must be a contiguous 2-D CUDA tensor")
@@ -176,11 +178,31 @@ def tcr_reduce_rows(x, mode: tcr_mode, out=None, stream=None):
     m = tcr_mode(mode.kind, mode.R, mode.block_threads, _dtype_code(x, mode))
     out = _check_out(out, x.device, rows)
     with torch.cuda.device(x.device):
-        st = c_api().tcr_reduce_rows(x.data_ptr() if x.numel() else None, rows, cols,
-                                     out.data_ptr(), m, _stream_handle(x.device, stream))
+        st = getattr(c_api(), name)(x.data_ptr() if x.numel() else None, rows, cols,
+                                    out.data_ptr(), m, _stream_handle(x.device, stream))
     if st != OK:
-        raise TcrError(st, "tcr_reduce_rows")
+        raise TcrError(st, name)
     return out[:rows] if rows else out[:0]
+
+
+def tcr_reduce_sum(x, mode: tcr_mode, out=None, stream=None):
+    """out[0] = sum of the contiguous CUDA tensor ``x`` (``tcr_reduce_sum``)."""
+    return _sum_call("tcr_reduce_sum", x, mode, out, stream)
+
+
+def tcr_reduce_rows(x, mode: tcr_mode, out=None, stream=None):
+    """out[r] = sum of row r of the contiguous 2-D CUDA tensor ``x`` (``tcr_reduce_rows``)."""
+    return _rows_call("tcr_reduce_rows", x, mode, out, stream)
+
+
+def tcr_reduce_sum_squares(x, mode: tcr_mode, out=None, stream=None):
+    """out[0] = sum of x_i^2 (``tcr_reduce_sum_squares``)."""
+    return _sum_call("tcr_reduce_sum_squares", x, mode, out, stream)
+
+
+def tcr_reduce_rows_sum_squares(x, mode: tcr_mode, out=None, stream=None):
+    """out[r] = sum of the squares of row r (``tcr_reduce_rows_sum_squares``)."""
+    return _rows_call("tcr_reduce_rows_sum_squares", x, mode, out, stream)
 
 
 def tcr_order_descriptor(n: int = 0, rows: int = 0, cols: int = 0,

@@ -9,6 +9,8 @@
 #include <cstdint>
 #include <cuda_fp16.h>
 
+#include "config.cuh"
+
 namespace tcr {
 
 constexpr int kF16 = 0;
@@ -85,37 +87,51 @@ __device__ __forceinline__ float leaf_hi(uint32_t w)
     }
 }
 
-// The sum of the two inputs packed in a 32-bit word, low + high, binary32
-// round to nearest.  For bfloat16 the two leaves (word << 16 and
-// word & 0xffff0000) are formed and added in one asm statement, which keeps
-// the compiler from hoisting the unpacking of many words at once: the
-// kernels that hold a group of loads in flight fit their register budget.
-template <int DT>
-__device__ __forceinline__ float pair_sum(uint32_t w)
+// The two leaves of a 32-bit word combined, low + high, binary32 round to
+// nearest; for kOpSquares the leaves are the squares of the two inputs.
+// For bfloat16 the unpacking (word << 16, word & 0xffff0000) and the
+// arithmetic are one asm statement, which keeps the compiler from hoisting
+// the unpacking of many words at once: the kernels that hold a group of
+// loads in flight fit their register budget.
+template <int DT, int OP>
+__device__ __forceinline__ float pair_val(uint32_t w)
 {
     if constexpr (DT == kF16) {
-        return __fadd_rn(leaf_lo<DT>(w), leaf_hi<DT>(w));
+        const float lo = leaf_lo<DT>(w), hi = leaf_hi<DT>(w);
+        if constexpr (OP == kOpSquares) return __fadd_rn(__fmul_rn(lo, lo), __fmul_rn(hi, hi));
+        return __fadd_rn(lo, hi);
     } else {
         float r;
-        asm("{\n\t.reg .b32 lo, hi;\n\t"
-            "shl.b32 lo, %1, 16;\n\t"
-            "and.b32 hi, %1, 0xffff0000;\n\t"
-            "add.rn.f32 %0, lo, hi;\n\t}"
-            : "=f"(r)
-            : "r"(w));
+        if constexpr (OP == kOpSquares) {
+            asm("{\n\t.reg .b32 lo, hi;\n\t"
+                "shl.b32 lo, %1, 16;\n\t"
+                "and.b32 hi, %1, 0xffff0000;\n\t"
+                "mul.rn.f32 lo, lo, lo;\n\t"
+                "mul.rn.f32 hi, hi, hi;\n\t"
+                "add.rn.f32 %0, lo, hi;\n\t}"
+                : "=f"(r)
+                : "r"(w));
+        } else {
+            asm("{\n\t.reg .b32 lo, hi;\n\t"
+                "shl.b32 lo, %1, 16;\n\t"
+                "and.b32 hi, %1, 0xffff0000;\n\t"
+                "add.rn.f32 %0, lo, hi;\n\t}"
+                : "=f"(r)
+                : "r"(w));
+        }
         return r;
     }
 }
 
-// Balanced tree over the 8 inputs of a vector:
+// Balanced tree over the 8 leaves of a vector:
 // ((e0 + e1) + (e2 + e3)) + ((e4 + e5) + (e6 + e7)).
-template <int DT>
+template <int DT, int OP = kOpSum>
 __device__ __forceinline__ float tree8(uint4 q)
 {
-    const float p0 = pair_sum<DT>(q.x);
-    const float p1 = pair_sum<DT>(q.y);
-    const float p2 = pair_sum<DT>(q.z);
-    const float p3 = pair_sum<DT>(q.w);
+    const float p0 = pair_val<DT, OP>(q.x);
+    const float p1 = pair_val<DT, OP>(q.y);
+    const float p2 = pair_val<DT, OP>(q.z);
+    const float p3 = pair_val<DT, OP>(q.w);
     return __fadd_rn(__fadd_rn(p0, p1), __fadd_rn(p2, p3));
 }
 
@@ -198,6 +214,29 @@ __device__ __forceinline__ void mma_ones(float &d0, float &d1, float &d2, float 
             "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};\n"
             : "+f"(d0), "+f"(d1), "+f"(d2), "+f"(d3)
             : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(one2), "r"(one2));
+    }
+}
+
+// D += A * B for one m16n8k16 tile with B given by registers: b0 holds
+// B[2t][g], B[2t+1][g] and b1 holds B[2t+8][g], B[2t+9][g] (g = lane/4,
+// t = lane%4).
+template <int DT>
+__device__ __forceinline__ void mma_ab(float &d0, float &d1, float &d2, float &d3, uint32_t a0,
+                                       uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                       uint32_t b1)
+{
+    if constexpr (DT == kF16) {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+            "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};\n"
+            : "+f"(d0), "+f"(d1), "+f"(d2), "+f"(d3)
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    } else {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+            "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};\n"
+            : "+f"(d0), "+f"(d1), "+f"(d2), "+f"(d3)
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
     }
 }
 

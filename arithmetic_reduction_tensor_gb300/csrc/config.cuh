@@ -8,6 +8,12 @@
 
 namespace tcr {
 
+// Operations on the leaves: the sum of the inputs, or the sum of their
+// squares (each square one binary32 multiplication, round to nearest, of an
+// exact binary32 value -- exact for binary16 inputs).
+constexpr int kOpSum = 0;
+constexpr int kOpSquares = 1;
+
 // Inputs per warp group of the tree kernels: 8 warp loads of 256 inputs.
 constexpr size_t kGroup = 2048;
 // Inputs per warp of one CTA work unit (chunk) of the chunked kernels.

@@ -18,55 +18,74 @@
 
 namespace tcr {
 
-template <int DT, bool ALIGNED>
+template <int DT, int OP, bool ALIGNED>
 __global__ void __launch_bounds__(1024)
 fixed_chunk_kernel(const uint16_t *__restrict__ x, size_t seg_len, size_t units, size_t cps,
                    int chunk_log2, float *__restrict__ dst)
 {
     // a chunk of 2^13 inputs per warp: 4 groups per span, < 2^3
-    chunk_body<FixedReducer<DT, 3>, ALIGNED>(x, seg_len, units, cps, chunk_log2, dst);
+    chunk_body<FixedReducer<DT, OP, 3>, ALIGNED>(x, seg_len, units, cps, chunk_log2, dst);
 }
 
-template <int DT, bool ALIGNED>
+template <int DT, int OP, bool ALIGNED>
 __global__ void __launch_bounds__(kRowsBlock, kRowsMinCtas)
 fixed_rows_warp_kernel(const uint16_t *__restrict__ x, size_t rows, size_t cols,
                        float *__restrict__ out)
 {
     // rows of at most kRowsWarpMaxCols = 8 groups, < 2^4
-    rows_body<FixedReducer<DT, 4>, ALIGNED>(x, rows, cols, out);
+    rows_body<FixedReducer<DT, OP, 4>, ALIGNED>(x, rows, cols, out);
 }
 
 // ---------------------------------------------------------------- host
 
-#define TCR_PICK(KERNEL, dtype, aligned)                                                   \
-    ((dtype) == kF16 ? ((aligned) ? KERNEL<kF16, true> : KERNEL<kF16, false>)              \
-                     : ((aligned) ? KERNEL<kBF16, true> : KERNEL<kBF16, false>))
+template <template <int, int, bool> class K, typename F>
+static F pick(int dtype, int op, bool aligned)
+{
+    if (dtype == kF16) {
+        if (op == kOpSquares) return aligned ? (F)K<kF16, kOpSquares, true>::fn : (F)K<kF16, kOpSquares, false>::fn;
+        return aligned ? (F)K<kF16, kOpSum, true>::fn : (F)K<kF16, kOpSum, false>::fn;
+    }
+    if (op == kOpSquares) return aligned ? (F)K<kBF16, kOpSquares, true>::fn : (F)K<kBF16, kOpSquares, false>::fn;
+    return aligned ? (F)K<kBF16, kOpSum, true>::fn : (F)K<kBF16, kOpSum, false>::fn;
+}
 
-cudaError_t launch_fixed_chunk(int dtype, bool aligned, const uint16_t *x, size_t seg_len,
+template <int DT, int OP, bool A>
+struct ChunkK {
+    static constexpr auto fn = fixed_chunk_kernel<DT, OP, A>;
+};
+template <int DT, int OP, bool A>
+struct RowsK {
+    static constexpr auto fn = fixed_rows_warp_kernel<DT, OP, A>;
+};
+
+using ChunkFn = void (*)(const uint16_t *, size_t, size_t, size_t, int, float *);
+using RowsFn = void (*)(const uint16_t *, size_t, size_t, float *);
+
+cudaError_t launch_fixed_chunk(int dtype, int op, bool aligned, const uint16_t *x, size_t seg_len,
                                size_t units, size_t cps, int chunk_log2, float *dst, int grid,
                                int block, cudaStream_t stream)
 {
-    auto k = TCR_PICK(fixed_chunk_kernel, dtype, aligned);
+    ChunkFn k = pick<ChunkK, ChunkFn>(dtype, op, aligned);
     k<<<grid, block, 0, stream>>>(x, seg_len, units, cps, chunk_log2, dst);
     return cudaGetLastError();
 }
 
-cudaError_t launch_fixed_rows_warp(int dtype, bool aligned, const uint16_t *x, size_t rows,
+cudaError_t launch_fixed_rows_warp(int dtype, int op, bool aligned, const uint16_t *x, size_t rows,
                                    size_t cols, float *out, int grid, int block,
                                    cudaStream_t stream)
 {
-    auto k = TCR_PICK(fixed_rows_warp_kernel, dtype, aligned);
+    RowsFn k = pick<RowsK, RowsFn>(dtype, op, aligned);
     k<<<grid, block, 0, stream>>>(x, rows, cols, out);
     return cudaGetLastError();
 }
 
-int occupancy_fixed(bool rows, int dtype, bool aligned, int block)
+int occupancy_fixed(bool rows, int dtype, int op, bool aligned, int block)
 {
     int n = 0;
     cudaError_t e = rows ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                               &n, TCR_PICK(fixed_rows_warp_kernel, dtype, aligned), block, 0)
+                               &n, pick<RowsK, RowsFn>(dtype, op, aligned), block, 0)
                          : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                               &n, TCR_PICK(fixed_chunk_kernel, dtype, aligned), block, 0);
+                               &n, pick<ChunkK, ChunkFn>(dtype, op, aligned), block, 0);
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
         return 0;

@@ -14,81 +14,92 @@
 // reduced in fp32: lane accumulators, the butterfly over row groups, the
 // tree over a CTA's warps, and the combine kernel over CTA chunks.  Rows
 // use one warp per row, so every load is a contiguous 512 bytes of the row.
+// The sum of squares uses the same tiles with D = A * A^T (MmaSqReducer):
+// a genuine contraction, two MMAs per tile.
+#include <type_traits>
+
 #include "stream.cuh"
 
 namespace tcr {
 
-template <int DT, int R, bool ALIGNED>
+template <int DT, int R, int OP>
+using MmaRed = typename std::conditional<OP == kOpSquares, MmaSqReducer<DT, R>, MmaReducer<DT, R>>::type;
+
+template <int DT, int R, int OP, bool ALIGNED>
 __global__ void __launch_bounds__(1024)
 mma_chunk_kernel(const uint16_t *__restrict__ x, size_t seg_len, size_t units, size_t cps,
                  int chunk_log2, float *__restrict__ dst)
 {
-    chunk_body<MmaReducer<DT, R>, ALIGNED>(x, seg_len, units, cps, chunk_log2, dst);
+    chunk_body<MmaRed<DT, R, OP>, ALIGNED>(x, seg_len, units, cps, chunk_log2, dst);
 }
 
-template <int DT, int R, bool ALIGNED>
+template <int DT, int R, int OP, bool ALIGNED>
 __global__ void __launch_bounds__(kRowsBlock, kRowsMinCtas)
 mma_rows_warp_kernel(const uint16_t *__restrict__ x, size_t rows, size_t cols,
                      float *__restrict__ out)
 {
-    rows_body<MmaReducer<DT, R>, ALIGNED>(x, rows, cols, out);
+    rows_body<MmaRed<DT, R, OP>, ALIGNED>(x, rows, cols, out);
 }
 
 // ---------------------------------------------------------------- host
 
-template <int R>
-static void *pick_r(bool rows, int dtype, bool aligned)
+template <int DT, int R, int OP>
+static void *pick_dro(bool rows, bool aligned)
 {
-    if (rows) {
-        if (dtype == kF16) return aligned ? (void *)mma_rows_warp_kernel<kF16, R, true>
-                                          : (void *)mma_rows_warp_kernel<kF16, R, false>;
-        return aligned ? (void *)mma_rows_warp_kernel<kBF16, R, true>
-                       : (void *)mma_rows_warp_kernel<kBF16, R, false>;
-    }
-    if (dtype == kF16) return aligned ? (void *)mma_chunk_kernel<kF16, R, true>
-                                      : (void *)mma_chunk_kernel<kF16, R, false>;
-    return aligned ? (void *)mma_chunk_kernel<kBF16, R, true>
-                   : (void *)mma_chunk_kernel<kBF16, R, false>;
+    if (rows) return aligned ? (void *)mma_rows_warp_kernel<DT, R, OP, true>
+                             : (void *)mma_rows_warp_kernel<DT, R, OP, false>;
+    return aligned ? (void *)mma_chunk_kernel<DT, R, OP, true>
+                   : (void *)mma_chunk_kernel<DT, R, OP, false>;
 }
 
-static void *pick(bool rows, int dtype, bool aligned, int R)
+template <int R>
+static void *pick_r(bool rows, int dtype, int op, bool aligned)
+{
+    if (dtype == kF16)
+        return op == kOpSquares ? pick_dro<kF16, R, kOpSquares>(rows, aligned)
+                                : pick_dro<kF16, R, kOpSum>(rows, aligned);
+    return op == kOpSquares ? pick_dro<kBF16, R, kOpSquares>(rows, aligned)
+                            : pick_dro<kBF16, R, kOpSum>(rows, aligned);
+}
+
+static void *pick(bool rows, int dtype, int op, bool aligned, int R)
 {
     switch (R) {
-    case 1: return pick_r<1>(rows, dtype, aligned);
-    case 2: return pick_r<2>(rows, dtype, aligned);
-    case 3: return pick_r<3>(rows, dtype, aligned);
-    case 4: return pick_r<4>(rows, dtype, aligned);
-    case 5: return pick_r<5>(rows, dtype, aligned);
-    case 6: return pick_r<6>(rows, dtype, aligned);
-    case 7: return pick_r<7>(rows, dtype, aligned);
-    case 8: return pick_r<8>(rows, dtype, aligned);
+    case 1: return pick_r<1>(rows, dtype, op, aligned);
+    case 2: return pick_r<2>(rows, dtype, op, aligned);
+    case 3: return pick_r<3>(rows, dtype, op, aligned);
+    case 4: return pick_r<4>(rows, dtype, op, aligned);
+    case 5: return pick_r<5>(rows, dtype, op, aligned);
+    case 6: return pick_r<6>(rows, dtype, op, aligned);
+    case 7: return pick_r<7>(rows, dtype, op, aligned);
+    case 8: return pick_r<8>(rows, dtype, op, aligned);
     default: return nullptr;
     }
 }
 
-cudaError_t launch_mma_chunk(int dtype, bool aligned, int R, const uint16_t *x, size_t seg_len,
-                             size_t units, size_t cps, int chunk_log2, float *dst, int grid,
-                             int block, cudaStream_t stream)
+cudaError_t launch_mma_chunk(int dtype, int op, bool aligned, int R, const uint16_t *x,
+                             size_t seg_len, size_t units, size_t cps, int chunk_log2, float *dst,
+                             int grid, int block, cudaStream_t stream)
 {
-    void *k = pick(false, dtype, aligned, R);
+    void *k = pick(false, dtype, op, aligned, R);
     if (!k) return cudaErrorInvalidValue;
     void *args[] = {(void *)&x, (void *)&seg_len, (void *)&units, (void *)&cps,
                     (void *)&chunk_log2, (void *)&dst};
     return cudaLaunchKernel(k, dim3(grid), dim3(block), args, 0, stream);
 }
 
-cudaError_t launch_mma_rows(int dtype, bool aligned, int R, const uint16_t *x, size_t rows,
+cudaError_t launch_mma_rows(int dtype, int op, bool aligned, int R, const uint16_t *x, size_t rows,
                             size_t cols, float *out, int grid, int block, cudaStream_t stream)
 {
-    void *k = pick(true, dtype, aligned, R);
+    void *k = pick(true, dtype, op, aligned, R);
     if (!k) return cudaErrorInvalidValue;
     void *args[] = {(void *)&x, (void *)&rows, (void *)&cols, (void *)&out};
     return cudaLaunchKernel(k, dim3(grid), dim3(block), args, 0, stream);
 }
 
-int occupancy_mma(bool rows, int dtype, bool aligned, int R, int block)
+int occupancy_mma(bool rows, int dtype, int op, bool aligned, int R, int block)
 {
-    void *k = pick(rows, dtype, aligned, R);
+    void *k = pick(rows, dtype, op, aligned, R);
     int n = 0;
     if (!k || cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, block, 0) != cudaSuccess) {
         (void)cudaGetLastError();

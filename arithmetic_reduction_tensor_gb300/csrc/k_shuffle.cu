@@ -21,7 +21,7 @@ constexpr int kShuffleUnroll = 8;    // vectors in flight per thread
 // + ... in order, a vector being its 8-input tree; vectors past the
 // segment are -0.0, the identity.  Software-pipelined: the next 8 vectors
 // are loaded before the current 8 are added.
-template <int DT, bool ALIGNED>
+template <int DT, int OP, bool ALIGNED>
 __device__ __forceinline__ float grid_stride_acc(const uint16_t *seg, size_t len, size_t first,
                                                  size_t stride)
 {
@@ -37,7 +37,7 @@ __device__ __forceinline__ float grid_stride_acc(const uint16_t *seg, size_t len
     for (size_t v0 = first; v0 < nvec; v0 += kShuffleUnroll * stride) {
         float t[kShuffleUnroll];
 #pragma unroll
-        for (int u = 0; u < kShuffleUnroll; u++) t[u] = tree8<DT>(q[u]);
+        for (int u = 0; u < kShuffleUnroll; u++) t[u] = tree8<DT, OP>(q[u]);
         const size_t n0 = v0 + kShuffleUnroll * stride;
 #pragma unroll
         for (int u = 0; u < kShuffleUnroll; u++) {
@@ -50,7 +50,7 @@ __device__ __forceinline__ float grid_stride_acc(const uint16_t *seg, size_t len
     return acc;
 }
 
-template <int DT, bool ALIGNED>
+template <int DT, int OP, bool ALIGNED>
 __global__ void __launch_bounds__(1024)
 shuffle_block_kernel(const uint16_t *__restrict__ x, size_t seg_len, int G,
                      float *__restrict__ dst)
@@ -61,7 +61,7 @@ shuffle_block_kernel(const uint16_t *__restrict__ x, size_t seg_len, int G,
     const size_t b = blockIdx.x - s * (unsigned)G;
     const uint16_t *seg = x + s * seg_len;
     const size_t stride = (size_t)G * blockDim.x;
-    float acc = grid_stride_acc<DT, ALIGNED>(seg, seg_len, b * blockDim.x + threadIdx.x, stride);
+    float acc = grid_stride_acc<DT, OP, ALIGNED>(seg, seg_len, b * blockDim.x + threadIdx.x, stride);
     pdl_launch_dependents();
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(kFull, acc, off));
@@ -75,45 +75,64 @@ shuffle_block_kernel(const uint16_t *__restrict__ x, size_t seg_len, int G,
 
 // Warp team (Bt = 32, G = 1): one warp per segment; the warp stream's
 // group order visits lane j's vectors j, j+32, j+64, ... in order.
-template <int DT, bool ALIGNED>
+template <int DT, int OP, bool ALIGNED>
 __global__ void __launch_bounds__(kRowsBlock, kRowsMinCtas)
 shuffle_rows_warp_kernel(const uint16_t *__restrict__ x, size_t rows, size_t cols,
                          float *__restrict__ out)
 {
-    rows_body<ShuffleReducer<DT>, ALIGNED>(x, rows, cols, out);
+    rows_body<ShuffleReducer<DT, OP>, ALIGNED>(x, rows, cols, out);
 }
 
 // ---------------------------------------------------------------- host
 
-#define TCR_PICK(KERNEL, dtype, aligned)                                                   \
-    ((dtype) == kF16 ? ((aligned) ? KERNEL<kF16, true> : KERNEL<kF16, false>)              \
-                     : ((aligned) ? KERNEL<kBF16, true> : KERNEL<kBF16, false>))
+template <template <int, int, bool> class K, typename F>
+static F pick(int dtype, int op, bool aligned)
+{
+    if (dtype == kF16) {
+        if (op == kOpSquares) return aligned ? (F)K<kF16, kOpSquares, true>::fn : (F)K<kF16, kOpSquares, false>::fn;
+        return aligned ? (F)K<kF16, kOpSum, true>::fn : (F)K<kF16, kOpSum, false>::fn;
+    }
+    if (op == kOpSquares) return aligned ? (F)K<kBF16, kOpSquares, true>::fn : (F)K<kBF16, kOpSquares, false>::fn;
+    return aligned ? (F)K<kBF16, kOpSum, true>::fn : (F)K<kBF16, kOpSum, false>::fn;
+}
 
-cudaError_t launch_shuffle_block(int dtype, bool aligned, const uint16_t *x, size_t seg_len,
+template <int DT, int OP, bool A>
+struct BlockK {
+    static constexpr auto fn = shuffle_block_kernel<DT, OP, A>;
+};
+template <int DT, int OP, bool A>
+struct RowsK {
+    static constexpr auto fn = shuffle_rows_warp_kernel<DT, OP, A>;
+};
+
+using BlockFn = void (*)(const uint16_t *, size_t, int, float *);
+using RowsFn = void (*)(const uint16_t *, size_t, size_t, float *);
+
+cudaError_t launch_shuffle_block(int dtype, int op, bool aligned, const uint16_t *x, size_t seg_len,
                                  size_t segments, int G, float *dst, int block,
                                  cudaStream_t stream)
 {
-    auto k = TCR_PICK(shuffle_block_kernel, dtype, aligned);
+    BlockFn k = pick<BlockK, BlockFn>(dtype, op, aligned);
     k<<<(unsigned)(segments * (size_t)G), block, 0, stream>>>(x, seg_len, G, dst);
     return cudaGetLastError();
 }
 
-cudaError_t launch_shuffle_rows_warp(int dtype, bool aligned, const uint16_t *x, size_t rows,
+cudaError_t launch_shuffle_rows_warp(int dtype, int op, bool aligned, const uint16_t *x, size_t rows,
                                      size_t cols, float *out, int grid, int block,
                                      cudaStream_t stream)
 {
-    auto k = TCR_PICK(shuffle_rows_warp_kernel, dtype, aligned);
+    RowsFn k = pick<RowsK, RowsFn>(dtype, op, aligned);
     k<<<grid, block, 0, stream>>>(x, rows, cols, out);
     return cudaGetLastError();
 }
 
-int occupancy_shuffle(bool rows, int dtype, bool aligned, int block)
+int occupancy_shuffle(bool rows, int dtype, int op, bool aligned, int block)
 {
     int n = 0;
     cudaError_t e = rows ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                               &n, TCR_PICK(shuffle_rows_warp_kernel, dtype, aligned), block, 0)
+                               &n, pick<RowsK, RowsFn>(dtype, op, aligned), block, 0)
                          : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                               &n, TCR_PICK(shuffle_block_kernel, dtype, aligned), block, 0);
+                               &n, pick<BlockK, BlockFn>(dtype, op, aligned), block, 0);
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
         return 0;

@@ -1,7 +1,8 @@
 // kernels.cuh -- launchers of the reduction kernels (host side).
 //
 // Every launcher enqueues one kernel on `stream` and returns the launch
-// status (cudaGetLastError).  Sizes are in inputs (16-bit elements).
+// status (cudaGetLastError).  Sizes are in inputs (16-bit elements).  `op`
+// is kOpSum (the sum of the inputs) or kOpSquares (the sum of their squares).
 #pragma once
 
 #include <cstddef>
@@ -16,31 +17,31 @@ namespace tcr {
 // Chunked: CTA work unit u = (segment u / cps, chunk u % cps); the chunk of
 // 2^chunk_log2 inputs is split evenly over the CTA's warps; dst[u] is the
 // chunk's aligned subtree.
-cudaError_t launch_fixed_chunk(int dtype, bool aligned, const uint16_t *x, size_t seg_len,
+cudaError_t launch_fixed_chunk(int dtype, int op, bool aligned, const uint16_t *x, size_t seg_len,
                                size_t units, size_t cps, int chunk_log2, float *dst, int grid,
                                int block, cudaStream_t stream);
 // One warp per row, rows <= kRowsWarpMaxCols inputs long: out[r] = row tree.
-cudaError_t launch_fixed_rows_warp(int dtype, bool aligned, const uint16_t *x, size_t rows,
+cudaError_t launch_fixed_rows_warp(int dtype, int op, bool aligned, const uint16_t *x, size_t rows,
                                    size_t cols, float *out, int grid, int block,
                                    cudaStream_t stream);
 
 // ---- SHUFFLE_TREE (declared grid-stride order)
 // Block team: grid = segments * G CTAs of Bt threads; CTA (s, b) writes its
 // block value to dst[s * G + b].
-cudaError_t launch_shuffle_block(int dtype, bool aligned, const uint16_t *x, size_t seg_len,
+cudaError_t launch_shuffle_block(int dtype, int op, bool aligned, const uint16_t *x, size_t seg_len,
                                  size_t segments, int G, float *dst, int block,
                                  cudaStream_t stream);
 // Warp team (Bt = 32, G = 1): one warp per row, out[r] = warp value.
-cudaError_t launch_shuffle_rows_warp(int dtype, bool aligned, const uint16_t *x, size_t rows,
+cudaError_t launch_shuffle_rows_warp(int dtype, int op, bool aligned, const uint16_t *x, size_t rows,
                                      size_t cols, float *out, int grid, int block,
                                      cudaStream_t stream);
 
 // ---- MMA_CHAIN (tensor-core chains of R MMAs against a ones matrix)
-cudaError_t launch_mma_chunk(int dtype, bool aligned, int R, const uint16_t *x, size_t seg_len,
+cudaError_t launch_mma_chunk(int dtype, int op, bool aligned, int R, const uint16_t *x, size_t seg_len,
                              size_t units, size_t cps, int chunk_log2, float *dst, int grid,
                              int block, cudaStream_t stream);
 // One warp per row, rows <= kRowsWarpMaxCols inputs long.
-cudaError_t launch_mma_rows(int dtype, bool aligned, int R, const uint16_t *x, size_t rows,
+cudaError_t launch_mma_rows(int dtype, int op, bool aligned, int R, const uint16_t *x, size_t rows,
                             size_t cols, float *out, int grid, int block, cudaStream_t stream);
 
 // ---- MMA_CHAIN on tcgen05 (bulk copies into shared memory, D in TMEM):
@@ -73,8 +74,8 @@ cudaError_t launch_combine(const float *partials, size_t segments, size_t count,
 
 // Resident CTAs per SM of each kernel at a block size (occupancy API);
 // `rows` selects the per-row variant.  0 if the query fails.
-int occupancy_fixed(bool rows, int dtype, bool aligned, int block);
-int occupancy_shuffle(bool rows, int dtype, bool aligned, int block);
-int occupancy_mma(bool rows, int dtype, bool aligned, int R, int block);
+int occupancy_fixed(bool rows, int dtype, int op, bool aligned, int block);
+int occupancy_shuffle(bool rows, int dtype, int op, bool aligned, int block);
+int occupancy_mma(bool rows, int dtype, int op, bool aligned, int R, int block);
 
 }  // namespace tcr

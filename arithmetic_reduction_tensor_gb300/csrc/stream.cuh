@@ -88,8 +88,10 @@ __device__ __forceinline__ float group_tree(const float (&t)[8], int lane)
 
 // FIXED_ORDER: the groups of a span are consecutive aligned subtrees; they
 // merge in a binary counter, so any count of groups gives the balanced tree
-// padded with -0.0.  LEVELS bounds the groups per span (< 2^LEVELS).
-template <int DT, int LEVELS>
+// padded with -0.0.  LEVELS bounds the groups per span (< 2^LEVELS).  For
+// sums of squares the pad's leaf is (-0.0)^2 = +0.0, which is the identity
+// too, since every leaf is then at least +0.0.
+template <int DT, int OP, int LEVELS>
 struct FixedReducer {
     static constexpr uint16_t kFill = 0x8000;    // -0.0
     TreeCounter<LEVELS> tc;
@@ -98,7 +100,7 @@ struct FixedReducer {
     __device__ __forceinline__ void take(const uint4 (&q)[8])
     {
 #pragma unroll
-        for (int k = 0; k < 8; k++) t[k] = tree8<DT>(q[k]);
+        for (int k = 0; k < 8; k++) t[k] = tree8<DT, OP>(q[k]);
     }
     __device__ __forceinline__ void reduce(int lane) { tc.push(group_tree(t, lane)); }
     __device__ __forceinline__ float value(int) const { return tc.finish(); }
@@ -108,7 +110,7 @@ struct FixedReducer {
 // j, j+32, j+64, ... in that order (group after group, load k after load
 // k-1), starting from -0.0; the warp value is the butterfly with offsets
 // 16, 8, 4, 2, 1.  Vectors past the segment are -0.0, the identity.
-template <int DT>
+template <int DT, int OP>
 struct ShuffleReducer {
     static constexpr uint16_t kFill = 0x8000;
     float acc = -0.0f;
@@ -117,7 +119,7 @@ struct ShuffleReducer {
     __device__ __forceinline__ void take(const uint4 (&q)[8])
     {
 #pragma unroll
-        for (int k = 0; k < 8; k++) t[k] = tree8<DT>(q[k]);
+        for (int k = 0; k < 8; k++) t[k] = tree8<DT, OP>(q[k]);
     }
     __device__ __forceinline__ void reduce(int)
     {
@@ -170,6 +172,50 @@ struct MmaReducer {
         a = __fadd_rn(a, __shfl_xor_sync(kFull, a, 4));
         a = __fadd_rn(a, __shfl_xor_sync(kFull, a, 8));
         a = __fadd_rn(a, __shfl_xor_sync(kFull, a, 16));
+        return a;
+    }
+};
+
+// MMA_CHAIN, sum of squares: a dense contraction on the tensor cores.  For
+// a 16 x 16 tile A, D = A * A^T has the row sums of squares on its diagonal.
+// In the m16n8k16 fragments the B operand of A^T's first 8 columns
+// (B[k][n] = A[n][k], n < 8) is exactly the lane's own A registers a0a1 and
+// a4a5, and that of the last 8 columns is a2a3 and a6a7: two MMAs per tile,
+// no data movement.  The diagonal D[g][g] (rows 0..7) lands in d0 / d1 and
+// D[g+8][g] (rows 8..15) in d2 / d3 of lane (g, t = g/2).  Chains of R tiles
+// flush those two values into the lane's fp32 accumulator; the warp value is
+// the sum over all lanes (eight of them hold values).
+template <int DT, int R>
+struct MmaSqReducer {
+    static constexpr uint16_t kFill = 0x0000;
+    float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;    // A * (rows 0..7)^T
+    float q0 = 0.f, q1 = 0.f, q2 = 0.f, q3 = 0.f;    // A * (rows 8..15)^T
+    float acc = 0.f;
+    int cnt = 0;
+
+    __device__ __forceinline__ void flush()
+    {
+        const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+        if (t == (g >> 1)) acc = __fadd_rn(acc, (g & 1) ? __fadd_rn(p1, q3) : __fadd_rn(p0, q2));
+        p0 = p1 = p2 = p3 = q0 = q1 = q2 = q3 = 0.f;
+        cnt = 0;
+    }
+    __device__ __forceinline__ void take(const uint4 (&q)[8])
+    {
+#pragma unroll
+        for (int k = 0; k < 8; k++) {
+            mma_ab<DT>(p0, p1, p2, p3, q[k].x, q[k].y, q[k].z, q[k].w, q[k].x, q[k].z);
+            mma_ab<DT>(q0, q1, q2, q3, q[k].x, q[k].y, q[k].z, q[k].w, q[k].y, q[k].w);
+            if (++cnt == R) flush();
+        }
+    }
+    __device__ __forceinline__ void reduce(int) {}
+    __device__ __forceinline__ float value(int)
+    {
+        if (cnt) flush();
+        float a = acc;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) a = __fadd_rn(a, __shfl_xor_sync(kFull, a, off));
         return a;
     }
 };

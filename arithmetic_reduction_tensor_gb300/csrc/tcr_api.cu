@@ -100,9 +100,9 @@ cudaMemPool_t pool_for(int dev)
 
 enum Family { kFixedF, kShuffleF, kMmaF };
 
-int occupancy(int dev, Family fam, bool rows, int dtype, bool aligned, int R, int block)
+int occupancy(int dev, Family fam, bool rows, int dtype, int op, bool aligned, int R, int block)
 {
-    OccKey key{dev, (int)fam, rows ? 1 : 0, dtype, aligned ? 1 : 0, R, block};
+    OccKey key{dev, (int)fam, (rows ? 1 : 0) | (op << 1), dtype, aligned ? 1 : 0, R, block};
     {
         std::lock_guard<std::mutex> lk(g_mu);
         for (auto &e : g_occ)
@@ -111,9 +111,9 @@ int occupancy(int dev, Family fam, bool rows, int dtype, bool aligned, int R, in
     int n = 0;
     if (dev >= 0) {
         switch (fam) {
-        case kFixedF: n = occupancy_fixed(rows, dtype, aligned, block); break;
-        case kShuffleF: n = occupancy_shuffle(rows, dtype, aligned, block); break;
-        case kMmaF: n = occupancy_mma(rows, dtype, aligned, R, block); break;
+        case kFixedF: n = occupancy_fixed(rows, dtype, op, aligned, block); break;
+        case kShuffleF: n = occupancy_shuffle(rows, dtype, op, aligned, block); break;
+        case kMmaF: n = occupancy_mma(rows, dtype, op, aligned, R, block); break;
         }
     }
     if (n <= 0) n = 1;
@@ -136,7 +136,7 @@ enum Path {
 };
 
 struct Plan {
-    int kind, dtype, R, block;
+    int kind, dtype, op, R, block;
     bool aligned;
     Path path;
     size_t segments, seg_len;
@@ -208,7 +208,7 @@ void plan_chunked(Plan &p, int dev, Family fam)
     p.cps = (p.seg_len + ((size_t)1 << p.chunk_log2) - 1) >> p.chunk_log2;
     p.units = p.segments * p.cps;
     const size_t resident = (size_t)sm_count(dev) *
-                            (size_t)occupancy(dev, fam, false, p.dtype, p.aligned, p.R, p.block);
+                            (size_t)occupancy(dev, fam, false, p.dtype, p.op, p.aligned, p.R, p.block);
     p.grid = (int)(p.units < resident ? p.units : resident);
     p.partials = p.cps > 1 ? p.units : 0;
     p.combine_count = p.cps;
@@ -216,13 +216,17 @@ void plan_chunked(Plan &p, int dev, Family fam)
 }
 
 // Plans tcr_reduce_sum (rows == 0: one segment of n) or tcr_reduce_rows.
-Plan make_plan(size_t segments, size_t seg_len, bool rows_call, const tcr_mode &m, int block,
-               int R, bool aligned, int dev)
+Plan make_plan(size_t segments, size_t seg_len, bool rows_call, const tcr_mode &m, int op,
+               int block, int R, bool aligned, int dev)
 {
     Plan p;
     std::memset(&p, 0, sizeof p);
     p.kind = m.kind;
+    // the tcgen05 kernels reduce plain sums; sums of squares of that kind run
+    // the mma.sync contraction (MmaSqReducer)
+    if (p.kind == TCR_MMA_CHAIN_TMEM && op != kOpSum) p.kind = TCR_MMA_CHAIN;
     p.dtype = m.dtype;
+    p.op = op;
     p.R = R;
     p.block = block;
     p.aligned = aligned;
@@ -242,7 +246,7 @@ Plan make_plan(size_t segments, size_t seg_len, bool rows_call, const tcr_mode &
             const size_t warps_per_cta = (size_t)p.block / 32;
             const size_t need = (segments + warps_per_cta - 1) / warps_per_cta;
             const size_t resident =
-                sms * (size_t)occupancy(dev, kShuffleF, true, p.dtype, aligned, 0, p.block);
+                sms * (size_t)occupancy(dev, kShuffleF, true, p.dtype, op, aligned, 0, p.block);
             p.grid = (int)(need < resident ? need : resident);
             p.launches = 1;
         } else {
@@ -254,7 +258,7 @@ Plan make_plan(size_t segments, size_t seg_len, bool rows_call, const tcr_mode &
         }
         return p;
     }
-    if (m.kind == TCR_MMA_CHAIN_TMEM && rows_call && aligned && segments < ((size_t)1 << 31) &&
+    if (p.kind == TCR_MMA_CHAIN_TMEM && rows_call && aligned && segments < ((size_t)1 << 31) &&
         seg_len < ((size_t)1 << 31)) {
         // 128 rows per MMA tile, 2-D tensor-map copies; one CTA per SM
         p.path = kPathTmemRows;
@@ -267,7 +271,7 @@ Plan make_plan(size_t segments, size_t seg_len, bool rows_call, const tcr_mode &
         p.launches = p.cps > 1 ? 2 : 1;
         return p;
     }
-    if (m.kind == TCR_MMA_CHAIN_TMEM && !rows_call && aligned) {
+    if (p.kind == TCR_MMA_CHAIN_TMEM && !rows_call && aligned) {
         // one persistent CTA per SM (its shared-memory ring fills the SM)
         p.path = kPathTmem;
         p.block = tmem_block_threads();
@@ -287,7 +291,8 @@ Plan make_plan(size_t segments, size_t seg_len, bool rows_call, const tcr_mode &
         p.block = block = kRowsBlock;
         const size_t warps_per_cta = (size_t)block / 32;
         const size_t need = (segments + warps_per_cta - 1) / warps_per_cta;
-        const size_t resident = sms * (size_t)occupancy(dev, fam, true, p.dtype, aligned, R, block);
+        const size_t resident =
+            sms * (size_t)occupancy(dev, fam, true, p.dtype, op, aligned, R, block);
         p.path = m.kind == TCR_FIXED_ORDER ? kPathFixedRowsWarp : kPathMmaRows;
         p.grid = (int)(need < resident ? need : resident);
         p.launches = 1;
@@ -335,26 +340,26 @@ tcr_status run_plan(const Plan &p, const uint16_t *x, float *out, cudaStream_t s
         break;
     case kPathChunk:
         e = p.kind == TCR_FIXED_ORDER
-                ? launch_fixed_chunk(p.dtype, p.aligned, x, p.seg_len, p.units, p.cps,
+                ? launch_fixed_chunk(p.dtype, p.op, p.aligned, x, p.seg_len, p.units, p.cps,
                                      p.chunk_log2, dst, p.grid, p.block, s)
-                : launch_mma_chunk(p.dtype, p.aligned, p.R, x, p.seg_len, p.units, p.cps,
+                : launch_mma_chunk(p.dtype, p.op, p.aligned, p.R, x, p.seg_len, p.units, p.cps,
                                    p.chunk_log2, dst, p.grid, p.block, s);
         break;
     case kPathFixedRowsWarp:
-        e = launch_fixed_rows_warp(p.dtype, p.aligned, x, p.segments, p.seg_len, dst, p.grid,
-                                   p.block, s);
+        e = launch_fixed_rows_warp(p.dtype, p.op, p.aligned, x, p.segments, p.seg_len, dst,
+                                   p.grid, p.block, s);
         break;
     case kPathMmaRows:
-        e = launch_mma_rows(p.dtype, p.aligned, p.R, x, p.segments, p.seg_len, dst, p.grid,
-                            p.block, s);
+        e = launch_mma_rows(p.dtype, p.op, p.aligned, p.R, x, p.segments, p.seg_len, dst,
+                            p.grid, p.block, s);
         break;
     case kPathShuffleBlock:
-        e = launch_shuffle_block(p.dtype, p.aligned, x, p.seg_len, p.segments, p.team_blocks, dst,
-                                 p.team_threads, s);
+        e = launch_shuffle_block(p.dtype, p.op, p.aligned, x, p.seg_len, p.segments,
+                                 p.team_blocks, dst, p.team_threads, s);
         break;
     case kPathShuffleRowsWarp:
-        e = launch_shuffle_rows_warp(p.dtype, p.aligned, x, p.segments, p.seg_len, dst, p.grid,
-                                     p.block, s);
+        e = launch_shuffle_rows_warp(p.dtype, p.op, p.aligned, x, p.segments, p.seg_len, dst,
+                                     p.grid, p.block, s);
         break;
     default:
         e = cudaErrorInvalidValue;
@@ -383,11 +388,8 @@ bool mul_overflows(size_t a, size_t b)
     return a != 0 && b > SIZE_MAX / a;
 }
 
-}  // namespace
-
-extern "C" {
-
-tcr_status tcr_reduce_sum(const void *x, size_t n, float *out, tcr_mode mode, void *stream)
+tcr_status reduce_sum_op(const void *x, size_t n, float *out, const tcr_mode &mode, int op,
+                         void *stream)
 {
     int block = 0, R = 0;
     tcr_status st = check_common(x, n, out, mode, &block, &R);
@@ -395,12 +397,12 @@ tcr_status tcr_reduce_sum(const void *x, size_t n, float *out, tcr_mode mode, vo
     const int dev = current_device();
     if (dev < 0) return TCR_ERR_CUDA;
     const bool aligned = ((uintptr_t)x & 15u) == 0;
-    Plan p = make_plan(1, n, false, mode, block, R, aligned, dev);
+    Plan p = make_plan(1, n, false, mode, op, block, R, aligned, dev);
     return run_plan(p, (const uint16_t *)x, out, (cudaStream_t)stream, dev);
 }
 
-tcr_status tcr_reduce_rows(const void *x, size_t rows, size_t cols, float *out, tcr_mode mode,
-                           void *stream)
+tcr_status reduce_rows_op(const void *x, size_t rows, size_t cols, float *out,
+                          const tcr_mode &mode, int op, void *stream)
 {
     if (mul_overflows(rows, cols)) return TCR_ERR_INVALID_ARG;
     if (rows == 0) {
@@ -413,8 +415,34 @@ tcr_status tcr_reduce_rows(const void *x, size_t rows, size_t cols, float *out, 
     const int dev = current_device();
     if (dev < 0) return TCR_ERR_CUDA;
     const bool aligned = ((uintptr_t)x & 15u) == 0 && (cols % 8) == 0;
-    Plan p = make_plan(rows, cols, true, mode, block, R, aligned, dev);
+    Plan p = make_plan(rows, cols, true, mode, op, block, R, aligned, dev);
     return run_plan(p, (const uint16_t *)x, out, (cudaStream_t)stream, dev);
+}
+
+}  // namespace
+
+extern "C" {
+
+tcr_status tcr_reduce_sum(const void *x, size_t n, float *out, tcr_mode mode, void *stream)
+{
+    return reduce_sum_op(x, n, out, mode, kOpSum, stream);
+}
+
+tcr_status tcr_reduce_rows(const void *x, size_t rows, size_t cols, float *out, tcr_mode mode,
+                           void *stream)
+{
+    return reduce_rows_op(x, rows, cols, out, mode, kOpSum, stream);
+}
+
+tcr_status tcr_reduce_sum_squares(const void *x, size_t n, float *out, tcr_mode mode, void *stream)
+{
+    return reduce_sum_op(x, n, out, mode, kOpSquares, stream);
+}
+
+tcr_status tcr_reduce_rows_sum_squares(const void *x, size_t rows, size_t cols, float *out,
+                                       tcr_mode mode, void *stream)
+{
+    return reduce_rows_op(x, rows, cols, out, mode, kOpSquares, stream);
 }
 
 tcr_status tcr_order_descriptor(size_t n, size_t rows, size_t cols, tcr_mode mode,
@@ -431,7 +459,7 @@ tcr_status tcr_order_descriptor(size_t n, size_t rows, size_t cols, tcr_mode mod
     if (segments * seg_len >= kMaxInputs) return TCR_ERR_INVALID_ARG;
     const int dev = current_device();
     // the plan of an aligned input; a misaligned one differs only in speed
-    Plan p = make_plan(segments, seg_len, rows_call, mode, block, R, true, dev);
+    Plan p = make_plan(segments, seg_len, rows_call, mode, kOpSum, block, R, true, dev);
     std::memset(desc, 0, sizeof *desc);
     desc->kind = mode.kind;
     desc->order = mode.kind == TCR_SHUFFLE_TREE  ? TCR_ORDER_GRID_STRIDE

@@ -122,18 +122,18 @@ extern "C" tcr_status tcr_reduce_sum_noalloc(const void *x, size_t n, float *out
     if (st != TCR_OK) return st;
 
     const bool aligned = ((uintptr_t)x & 15u) == 0;
-    int occ = mode.kind == TCR_FIXED_ORDER ? occupancy_fixed(false, mode.dtype, aligned, block)
-                                           : occupancy_mma(false, mode.dtype, aligned, R, block);
+    int occ = mode.kind == TCR_FIXED_ORDER ? occupancy_fixed(false, mode.dtype, kOpSum, aligned, block)
+                                           : occupancy_mma(false, mode.dtype, kOpSum, aligned, R, block);
     if (occ <= 0) occ = 1;
     const size_t resident = (size_t)d.sms * (size_t)occ;
     const int grid = (int)(cps < resident ? cps : resident);
     float *dst = cps > 1 ? d.partials : out;
     const uint16_t *xs = (const uint16_t *)x;
     cudaError_t e = mode.kind == TCR_FIXED_ORDER
-                        ? launch_fixed_chunk(mode.dtype, aligned, xs, n, cps, cps, chunk_log2, dst,
-                                             grid, block, s)
-                        : launch_mma_chunk(mode.dtype, aligned, R, xs, n, cps, cps, chunk_log2, dst,
-                                           grid, block, s);
+                        ? launch_fixed_chunk(mode.dtype, kOpSum, aligned, xs, n, cps, cps,
+                                             chunk_log2, dst, grid, block, s)
+                        : launch_mma_chunk(mode.dtype, kOpSum, aligned, R, xs, n, cps, cps,
+                                           chunk_log2, dst, grid, block, s);
     if (e == cudaSuccess && cps > 1) e = launch_combine(d.partials, 1, cps, out, s);
     return e == cudaSuccess ? TCR_OK : TCR_ERR_CUDA;
 }

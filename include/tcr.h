@@ -145,6 +145,30 @@ TCR_API tcr_status tcr_reduce_rows(const void *x, size_t rows, size_t cols, floa
                            void *stream);
 
 /*
+ * tcr_reduce_sum_squares, tcr_reduce_rows_sum_squares -- the sum of x_i^2
+ * (over all inputs, or per row), a reduction with a fused pre-op in the
+ * sense of the cascaded reductions named by the "RedFuser" title in the
+ * first page's list of work built on the method.  Arguments, layout, modes
+ * and errors are those of tcr_reduce_sum / tcr_reduce_rows.
+ *   TCR_FIXED_ORDER, TCR_SHUFFLE_TREE  the same declared orders over the
+ *                     leaves fl32(x_i * x_i) (one binary32 multiplication,
+ *                     round to nearest; exact for binary16), bit-identical
+ *                     to the CPU emulation of those orders.
+ *   TCR_MMA_CHAIN     a dense contraction on the tensor cores: for each
+ *                     16 x 16 tile A, D = A * A^T holds the rows' sums of
+ *                     squares on its diagonal (two m16n8k16 MMAs per tile,
+ *                     chains of R flushed to fp32).  Error bound
+ *                     |result - exact| <= 2^-20 * sum x_i^2 + 1e-6.
+ *   TCR_MMA_CHAIN_TMEM  runs as TCR_MMA_CHAIN.
+ * tcr_order_descriptor describes these calls as well: the order does not
+ * depend on the leaves.
+ */
+TCR_API tcr_status tcr_reduce_sum_squares(const void *x, size_t n, float *out, tcr_mode mode,
+                                          void *stream);
+TCR_API tcr_status tcr_reduce_rows_sum_squares(const void *x, size_t rows, size_t cols,
+                                               float *out, tcr_mode mode, void *stream);
+
+/*
  * tcr_reduce_sum_noalloc -- tcr_reduce_sum for callers that must not
  * allocate device memory while they run: a service that reserved its whole
  * device-memory budget at start-up and treats any later allocation as a
