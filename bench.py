@@ -469,6 +469,42 @@ def profile_arm(args):
     return 0
 
 
+def extras_arm(args):
+    """Beyond the hot path: the sum of squares (2^30 sum and 65536 x 4096
+    rows, every mode), one JSON line per call."""
+    import torch
+    import arithmetic_reduction_tensor_gb300 as tcr
+    from arithmetic_reduction_tensor_gb300 import synth
+    torch.cuda.set_device(0)
+    peak, _ = load_peaks()
+    xs = torch.from_numpy(synth.generate(N_SUM, "uniform_pm1", synth.F16, seed=4).view(np.int16)).cuda()
+    xr = torch.from_numpy(synth.generate(ROWS * COLS, "normal", synth.F16, seed=2).view(np.int16))
+    xr = xr.cuda().view(ROWS, COLS)
+    out = torch.empty(ROWS, dtype=torch.float32, device="cuda")
+    calls = []
+    for kind in (tcr.MMA_CHAIN, tcr.FIXED_ORDER, tcr.SHUFFLE_TREE):
+        m = tcr.Mode(kind)
+        calls.append(("sum_squares/" + tcr.KIND_NAMES[kind], 2 * N_SUM + 4,
+                      lambda m=m: tcr.tcr_reduce_sum_squares(xs, m, out=out[:1])))
+        calls.append(("rows_sum_squares/" + tcr.KIND_NAMES[kind], 2 * ROWS * COLS + 4 * ROWS,
+                      lambda m=m: tcr.tcr_reduce_rows_sum_squares(xr, m, out=out)))
+    for name, nbytes, fn in calls:
+        for _ in range(args.warmup):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(args.steps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / args.steps
+        gbps = nbytes / us / 1e3
+        print(json.dumps({"extra": name, "us": round(us, 2), "gbps": round(gbps, 1),
+                          "frac": round(gbps / peak, 4), "steps": args.steps}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -476,6 +512,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["tcr", "reference"], default="tcr")
     ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--extras", action="store_true",
+                    help="time the sum of squares calls (beyond the hot path) and exit")
     ap.add_argument("--profile-case", action="store_true",
                     help="run the small ncu case (2^28 sum, 32768 x 4096 rows) and exit")
     ap.add_argument("--e2e-steps", type=int, default=0, help="0: max(3, steps // 40)")
@@ -501,6 +539,9 @@ def main():
     if args.profile_case:
         build_library()
         return profile_arm(args)
+    if args.extras:
+        build_library()
+        return extras_arm(args)
 
     torch.cuda.set_device(local)
     init_dist(world, "nccl")
