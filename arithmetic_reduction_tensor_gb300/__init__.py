@@ -28,7 +28,8 @@ __all__ = [
     "ORDER_TENSOR_CORE", "ORDER_GRID_STRIDE", "ORDER_BALANCED_TREE",
     "tcr_mode", "tcr_order_desc", "Mode", "TcrError", "c_api",
     "tcr_reduce_sum", "tcr_reduce_rows", "tcr_reduce_sum_squares", "tcr_reduce_rows_sum_squares",
-    "tcr_order_descriptor", "tcr_status_string", "tcr_device_faults", "FAULT_PIPELINE_WAIT",
+    "tcr_order_descriptor", "tcr_order_equivalent", "tcr_status_string", "tcr_device_faults",
+    "FAULT_PIPELINE_WAIT",
 ]
 
 MMA_CHAIN, SHUFFLE_TREE, FIXED_ORDER, MMA_CHAIN_TMEM = 0, 1, 2, 3
@@ -98,6 +99,10 @@ def c_api() -> ctypes.CDLL:
             lib.tcr_reduce_rows_sum_squares.restype = ctypes.c_int
             lib.tcr_order_descriptor.argtypes = [sz, sz, sz, tcr_mode, ctypes.POINTER(tcr_order_desc)]
             lib.tcr_order_descriptor.restype = ctypes.c_int
+            lib.tcr_order_equivalent.argtypes = [ctypes.POINTER(tcr_order_desc),
+                                                 ctypes.POINTER(tcr_order_desc),
+                                                 ctypes.POINTER(ctypes.c_int)]
+            lib.tcr_order_equivalent.restype = ctypes.c_int
             lib.tcr_device_faults.argtypes = [ctypes.POINTER(ctypes.c_uint), ctypes.c_int]
             lib.tcr_device_faults.restype = ctypes.c_int
             lib.tcr_status_string.argtypes = [ctypes.c_int]
@@ -205,12 +210,29 @@ def tcr_reduce_rows_sum_squares(x, mode: tcr_mode, out=None, stream=None):
     return _rows_call("tcr_reduce_rows_sum_squares", x, mode, out, stream)
 
 
-def tcr_order_descriptor(n: int = 0, rows: int = 0, cols: int = 0,
-                         mode: tcr_mode | None = None) -> dict:
-    """The declared order and launch plan of a call (``tcr_order_descriptor``)."""
+def _descriptor(n, rows, cols, mode) -> tcr_order_desc:
     d = tcr_order_desc()
     st = c_api().tcr_order_descriptor(n, rows, cols, mode if mode is not None else Mode(FIXED_ORDER),
                                       ctypes.byref(d))
     if st != OK:
         raise TcrError(st, "tcr_order_descriptor")
-    return d.as_dict()
+    return d
+
+
+def tcr_order_descriptor(n: int = 0, rows: int = 0, cols: int = 0,
+                         mode: tcr_mode | None = None) -> dict:
+    """The declared order and launch plan of a call (``tcr_order_descriptor``)."""
+    return _descriptor(n, rows, cols, mode).as_dict()
+
+
+def tcr_order_equivalent(call_a: dict, call_b: dict) -> bool:
+    """Whether two calls, each given as the keyword arguments of
+    ``tcr_order_descriptor`` (n / rows / cols / mode), are in one
+    bit-equivalence class (``tcr_order_equivalent``)."""
+    a = _descriptor(call_a.get("n", 0), call_a.get("rows", 0), call_a.get("cols", 0), call_a.get("mode"))
+    b = _descriptor(call_b.get("n", 0), call_b.get("rows", 0), call_b.get("cols", 0), call_b.get("mode"))
+    eq = ctypes.c_int(0)
+    st = c_api().tcr_order_equivalent(ctypes.byref(a), ctypes.byref(b), ctypes.byref(eq))
+    if st != OK:
+        raise TcrError(st, "tcr_order_equivalent")
+    return bool(eq.value)

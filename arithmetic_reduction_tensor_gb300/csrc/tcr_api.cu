@@ -481,6 +481,34 @@ tcr_status tcr_order_descriptor(size_t n, size_t rows, size_t cols, tcr_mode mod
     return TCR_OK;
 }
 
+tcr_status tcr_order_equivalent(const tcr_order_desc *a, const tcr_order_desc *b,
+                                int *equivalent)
+{
+    if (!a || !b || !equivalent) return TCR_ERR_INVALID_ARG;
+    *equivalent = 0;
+    if (a->kind != b->kind || a->order != b->order || a->segment_len != b->segment_len)
+        return TCR_OK;
+    switch (a->order) {
+    case TCR_ORDER_BALANCED_TREE:
+        *equivalent = 1;
+        break;
+    case TCR_ORDER_GRID_STRIDE: {
+        const size_t nvec = (a->segment_len + 7) / 8;
+        const size_t ta = (size_t)a->team_threads * (size_t)a->team_blocks;
+        const size_t tb = (size_t)b->team_threads * (size_t)b->team_blocks;
+        // one vector per thread at most: lane values are the vector trees,
+        // combined by the butterfly and one balanced tree over warps
+        *equivalent = (ta == tb) || (ta >= nvec && tb >= nvec);
+        break;
+    }
+    default:
+        *equivalent = a->chain_R == b->chain_R && a->launch_block == b->launch_block &&
+                      a->chunk_log2 == b->chunk_log2;
+        break;
+    }
+    return TCR_OK;
+}
+
 tcr_status tcr_device_faults(unsigned int *flags, int clear)
 {
     if (!flags) return TCR_ERR_INVALID_ARG;

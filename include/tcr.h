@@ -262,6 +262,27 @@ TCR_API tcr_status tcr_order_descriptor(size_t n, size_t rows, size_t cols, tcr_
                                 tcr_order_desc *desc);
 
 /*
+ * tcr_order_equivalent -- *equivalent = 1 when the two described calls give
+ * bit-identical results for every input, 0 when the descriptors cannot show
+ * that.  Decided from the descriptors alone, in the spirit of the
+ * bit-equivalence classes of "Taming Bitwise Behavior in GPU Kernels with
+ * Tensor Core" (arXiv 2609.11356), Abstract (an autotuner restricted to one
+ * class).  Same kind, dtype and segment_len are required; then
+ *   TCR_FIXED_ORDER   always equivalent (the tree depends on the length only);
+ *   TCR_SHUFFLE_TREE  the block and grid trees are both balanced over power-
+ *                     of-two warp counts, so together they are one balanced
+ *                     tree over warp index: the order is fixed by the team
+ *                     size T = team_threads * team_blocks alone, and by
+ *                     nothing at all once T >= the number of 8-input vectors
+ *                     (every thread then holds at most one);
+ *   TCR_MMA_CHAIN(_TMEM) equivalent when chain_R, launch_block and chunk_log2
+ *                     match (the tensor core's own order is fixed per shape).
+ * Host only.  Returns TCR_ERR_INVALID_ARG for NULL pointers.
+ */
+TCR_API tcr_status tcr_order_equivalent(const tcr_order_desc *a, const tcr_order_desc *b,
+                                        int *equivalent);
+
+/*
  * tcr_device_faults -- the fault word of the current device: bit 0
  * (TCR_FAULT_PIPELINE_WAIT) is set when a wait inside a TCR_MMA_CHAIN_TMEM
  * kernel gave up after its limit of about one second (the kernel then

@@ -374,3 +374,20 @@ def test_rows_write_exactly_rows_results(kind, shape):
     got = buf.cpu().numpy()
     assert np.all(got[:32] == CANARY) and np.all(got[32 + rows:] == CANARY)
     assert np.all(got[32:32 + rows] != CANARY)
+
+
+# ------------------------------------------------------------ equivalence classes on the GPU
+
+@pytest.mark.parametrize("n", [1 << 20, 3_000_000])
+def test_shuffle_tree_block_sizes_in_one_class_give_identical_bits(n):
+    x = inputs(n, F16)
+    t = dev(x)
+    ref = None
+    for b in (32, 64, 128, 256, 512, 1024):
+        eq = tcr.tcr_order_equivalent(dict(n=n, mode=tcr.Mode(tcr.SHUFFLE_TREE)),
+                                      dict(n=n, mode=tcr.Mode(tcr.SHUFFLE_TREE, block_threads=b)))
+        got = tcr.tcr_reduce_sum(t, tcr.Mode(tcr.SHUFFLE_TREE, block_threads=b)).cpu().numpy()
+        if eq:
+            if ref is None:
+                ref = got
+            assert same_bits(got, ref)
