@@ -20,32 +20,63 @@ constexpr int kShuffleUnroll = 8;    // vectors in flight per thread
 // Block team: thread value = -0.0 + vector(first) + vector(first + stride)
 // + ... in order, a vector being its 8-input tree; vectors past the
 // segment are -0.0, the identity.  Software-pipelined: the next 8 vectors
-// are loaded before the current 8 are added.
+// are loaded before the current 8 are added.  While every vector of a batch
+// is whole (and the segment 16-byte aligned) the loads walk a pointer with
+// no bounds checks; the ragged end continues, in the same order, with the
+// checked loads.
 template <int DT, int OP, bool ALIGNED>
 __device__ __forceinline__ float grid_stride_acc(const uint16_t *seg, size_t len, size_t first,
                                                  size_t stride)
 {
+    constexpr int U = kShuffleUnroll;
     const size_t nvec = (len + 7) / 8;
     const uint4 pad = make_uint4(kNegZero2, kNegZero2, kNegZero2, kNegZero2);
-    uint4 q[kShuffleUnroll];
+    float acc = -0.0f;
+    size_t v0 = first;
+    if (ALIGNED) {
+        const size_t nfull = len / 8;               // whole vectors
+        if (v0 + (size_t)(U - 1) * stride < nfull) {
+            const size_t step = 8 * stride;
+            const uint16_t *p = seg + 8 * v0;
+            uint4 q[U];
 #pragma unroll
-    for (int u = 0; u < kShuffleUnroll; u++) {
-        const size_t v = first + (size_t)u * stride;
+            for (int u = 0; u < U; u++) q[u] = ld_stream(p + (size_t)u * step);
+            for (;;) {
+                float t[U];
+#pragma unroll
+                for (int u = 0; u < U; u++) t[u] = tree8<DT, OP>(q[u]);
+                v0 += (size_t)U * stride;
+                p += (size_t)U * step;
+                const bool more = v0 + (size_t)(U - 1) * stride < nfull;
+                if (more) {
+#pragma unroll
+                    for (int u = 0; u < U; u++) q[u] = ld_stream(p + (size_t)u * step);
+                }
+#pragma unroll
+                for (int u = 0; u < U; u++) acc = __fadd_rn(acc, t[u]);
+                if (!more) break;
+            }
+        }
+    }
+    if (v0 >= nvec) return acc;
+    uint4 q[U];
+#pragma unroll
+    for (int u = 0; u < U; u++) {
+        const size_t v = v0 + (size_t)u * stride;
         q[u] = v < nvec ? ld_vec<ALIGNED>(seg, len, v, 0x8000u) : pad;
     }
-    float acc = -0.0f;
-    for (size_t v0 = first; v0 < nvec; v0 += kShuffleUnroll * stride) {
-        float t[kShuffleUnroll];
+    for (; v0 < nvec; v0 += (size_t)U * stride) {
+        float t[U];
 #pragma unroll
-        for (int u = 0; u < kShuffleUnroll; u++) t[u] = tree8<DT, OP>(q[u]);
-        const size_t n0 = v0 + kShuffleUnroll * stride;
+        for (int u = 0; u < U; u++) t[u] = tree8<DT, OP>(q[u]);
+        const size_t n0 = v0 + (size_t)U * stride;
 #pragma unroll
-        for (int u = 0; u < kShuffleUnroll; u++) {
+        for (int u = 0; u < U; u++) {
             const size_t v = n0 + (size_t)u * stride;
             q[u] = v < nvec ? ld_vec<ALIGNED>(seg, len, v, 0x8000u) : pad;
         }
 #pragma unroll
-        for (int u = 0; u < kShuffleUnroll; u++) acc = __fadd_rn(acc, t[u]);
+        for (int u = 0; u < U; u++) acc = __fadd_rn(acc, t[u]);
     }
     return acc;
 }
