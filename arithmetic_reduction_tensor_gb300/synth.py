@@ -1,7 +1,7 @@
 """Seeded synthetic inputs for the reduction tests and benchmark.
 
 This module holds no reduction arithmetic: it only turns (seed, index) into
-16-bit input patterns.  Both the CPU oracle side and the GPU side of every
+input patterns (16-bit for binary16 / bfloat16, 32-bit for binary32).  Both the CPU oracle side and the GPU side of every
 test consume the same bytes produced here.
 
 Generator (counter based, so any slice can be produced independently):
@@ -22,12 +22,12 @@ Distributions (the workload recipes of the benchmark configurations):
                  r = sqrt(-2 ln(1 - u(2k))), t = 2 pi u(2k+1);
                  element 2k = r cos t, element 2k+1 = r sin t
 ``pow2``         sign = bit 63 of word(i); e = -20 + (low 32 bits mod 31);
-                 the value is sign * 2^e (exact in bfloat16 and binary16)
+                 the value is sign * 2^e (exact in every storage type)
 
-Rounding to the 16-bit storage type: binary16 takes the binary64 value
-rounded to nearest even in one step (numpy's float64 -> float16 cast);
-bfloat16 takes the binary64 value rounded to binary32 and then to bfloat16,
-nearest even at each step.  ``pow2`` values are exact and need no rounding.
+Rounding to the storage type: binary16 and binary32 take the binary64 value
+rounded to nearest even in one step (numpy's casts); bfloat16 takes the
+binary64 value rounded to binary32 and then to bfloat16, nearest even at
+each step.  ``pow2`` values are exact and need no rounding.
 """
 from __future__ import annotations
 
@@ -38,6 +38,7 @@ import numpy as np
 
 F16 = 0
 BF16 = 1
+F32 = 2
 
 GAMMA = np.uint64(0x9E3779B97F4A7C15)
 _M1 = np.uint64(0xBF58476D1CE4E5B9)
@@ -67,6 +68,8 @@ def _uniform(seed: int, start: int, count: int) -> np.ndarray:
 
 
 def _to_bits(v: np.ndarray, dtype: int) -> np.ndarray:
+    if dtype == F32:
+        return v.astype(np.float32).view(np.uint32)
     if dtype == F16:
         return v.astype(np.float16).view(np.uint16)
     f = v.astype(np.float32).view(np.uint32)
@@ -97,6 +100,9 @@ def _chunk(dist: str, dtype: int, seed: int, start: int, count: int) -> np.ndarr
         w = _words(seed, start, count)
         sign = (w >> np.uint64(63)).astype(np.uint16)
         e = ((w & np.uint64(0xFFFFFFFF)) % np.uint64(31)).astype(np.int32) - 20
+        if dtype == F32:
+            return ((sign.astype(np.uint32) << np.uint32(31))
+                    | ((e + 127).astype(np.uint32) << np.uint32(23)))
         if dtype == BF16:
             return (sign << np.uint16(15)) | ((e + 127).astype(np.uint16) << np.uint16(7))
         # binary16: 2^e is normal for e >= -14 (biased exponent e + 15) and
@@ -110,8 +116,9 @@ def _chunk(dist: str, dtype: int, seed: int, start: int, count: int) -> np.ndarr
 
 def generate(n: int, dist: str, dtype: int = F16, seed: int = 0, start: int = 0,
              threads: int | None = None) -> np.ndarray:
-    """``n`` 16-bit patterns (uint16) of elements ``start .. start+n-1``."""
-    out = np.empty(n, np.uint16)
+    """The patterns of elements ``start .. start+n-1``: uint16 for F16 and
+    BF16, uint32 for F32."""
+    out = np.empty(n, np.uint32 if dtype == F32 else np.uint16)
     if n == 0:
         return out
     starts = list(range(0, n, _CHUNK))
@@ -131,7 +138,9 @@ def generate(n: int, dist: str, dtype: int = F16, seed: int = 0, start: int = 0,
 
 
 def as_float(bits: np.ndarray, dtype: int) -> np.ndarray:
-    """binary32 view of 16-bit patterns, for display and host-side checks."""
+    """binary32 view of the patterns, for display and host-side checks."""
+    if dtype == F32:
+        return bits.view(np.float32)
     if dtype == F16:
         return bits.view(np.float16).astype(np.float32)
     return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32)

@@ -22,6 +22,9 @@ Functions (sources are cited in ``tcr_oracle.c``):
 ``*_sq``, ``exact_sum_squares``
                        the same over the leaves x_i^2 (sum of squares).
 ``*_rows``             the same, one result per row.
+
+Inputs are binary16 / bfloat16 patterns (uint16, or float16 arrays) or
+binary32 values (float32 or uint32 patterns, dtype ``F32``).
 """
 from __future__ import annotations
 
@@ -38,6 +41,7 @@ _LIB = os.path.join(_HERE, "_build", "liboracle.so")
 
 F16 = 0
 BF16 = 1
+F32 = 2
 
 _lock = threading.Lock()
 _lib = None
@@ -62,7 +66,7 @@ def _load():
     with _lock:
         if _lib is None:
             lib = ctypes.CDLL(build())
-            u16p = ctypes.POINTER(ctypes.c_uint16)
+            u16p = ctypes.c_void_p      # 16-bit or (binary32) 32-bit patterns
             f32p = ctypes.POINTER(ctypes.c_float)
             f64p = ctypes.POINTER(ctypes.c_double)
             sz, i = ctypes.c_size_t, ctypes.c_int
@@ -92,18 +96,25 @@ def _load():
     return _lib
 
 
-def _bits(x) -> np.ndarray:
-    """The raw 16-bit patterns of ``x`` (uint16, C-contiguous)."""
+def _bits(x, dtype: int) -> np.ndarray:
+    """The raw patterns of ``x``, C-contiguous: uint16 for F16 / BF16,
+    uint32 for F32."""
     a = np.asarray(x)
-    if a.dtype == np.float16:
-        a = a.view(np.uint16)
-    if a.dtype != np.uint16:
-        raise TypeError(f"oracle inputs are 16-bit patterns, got {a.dtype}")
+    if dtype == F32:
+        if a.dtype == np.float32:
+            a = a.view(np.uint32)
+        if a.dtype != np.uint32:
+            raise TypeError(f"binary32 oracle inputs are float32 or uint32 patterns, got {a.dtype}")
+    else:
+        if a.dtype == np.float16:
+            a = a.view(np.uint16)
+        if a.dtype != np.uint16:
+            raise TypeError(f"16-bit oracle inputs are uint16 patterns, got {a.dtype}")
     return np.ascontiguousarray(a)
 
 
 def _u16p(a):
-    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_uint16))
+    return ctypes.c_void_p(a.ctypes.data)
 
 
 def default_threads() -> int:
@@ -112,7 +123,7 @@ def default_threads() -> int:
 
 def exact_sum(x, dtype: int, threads: int | None = None) -> tuple[float, float]:
     """(exact sum rounded to binary64, exact sum of |x| rounded to binary64)."""
-    a = _bits(x).reshape(-1)
+    a = _bits(x, dtype).reshape(-1)
     s, m = ctypes.c_double(), ctypes.c_double()
     _load().oracle_exact_sum(_u16p(a), a.size, dtype, threads or default_threads(),
                              ctypes.byref(s), ctypes.byref(m))
@@ -121,7 +132,7 @@ def exact_sum(x, dtype: int, threads: int | None = None) -> tuple[float, float]:
 
 def exact_sum_squares(x, dtype: int, threads: int | None = None) -> tuple[float, float]:
     """(exact sum of x_i^2 rounded to binary64, the same value)."""
-    a = _bits(x).reshape(-1)
+    a = _bits(x, dtype).reshape(-1)
     s, m = ctypes.c_double(), ctypes.c_double()
     _load().oracle_exact_sum_squares(_u16p(a), a.size, dtype, threads or default_threads(),
                                      ctypes.byref(s), ctypes.byref(m))
@@ -129,7 +140,7 @@ def exact_sum_squares(x, dtype: int, threads: int | None = None) -> tuple[float,
 
 
 def exact_sum_rows(x, dtype: int, threads: int | None = None, squares: bool = False):
-    a = _bits(x)
+    a = _bits(x, dtype)
     rows, cols = a.shape
     s = np.empty(rows, np.float64)
     m = np.empty(rows, np.float64)
@@ -142,21 +153,21 @@ def exact_sum_rows(x, dtype: int, threads: int | None = None, squares: bool = Fa
 
 
 def fixed_order(x, dtype: int, threads: int | None = None) -> np.float32:
-    a = _bits(x).reshape(-1)
+    a = _bits(x, dtype).reshape(-1)
     return np.float32(_load().oracle_fixed_order_f32(_u16p(a), a.size, dtype,
                                                      threads or default_threads()))
 
 
 def fixed_order_sq(x, dtype: int, threads: int | None = None) -> np.float32:
     """Balanced binary32 tree over the leaves x_i^2."""
-    a = _bits(x).reshape(-1)
+    a = _bits(x, dtype).reshape(-1)
     return np.float32(_load().oracle_fixed_order_sq_f32(_u16p(a), a.size, dtype,
                                                         threads or default_threads()))
 
 
 def fixed_order_rows(x, dtype: int, threads: int | None = None,
                      squares: bool = False) -> np.ndarray:
-    a = _bits(x)
+    a = _bits(x, dtype)
     rows, cols = a.shape
     out = np.empty(rows, np.float32)
     _load().oracle_fixed_order_rows_f32(_u16p(a), rows, cols, dtype, 1 if squares else 0,
@@ -167,7 +178,7 @@ def fixed_order_rows(x, dtype: int, threads: int | None = None,
 
 def shuffle_tree(x, dtype: int, team_threads: int, team_blocks: int,
                  threads: int | None = None) -> np.float32:
-    a = _bits(x).reshape(-1)
+    a = _bits(x, dtype).reshape(-1)
     return np.float32(_load().oracle_shuffle_tree_f32(
         _u16p(a), a.size, dtype, team_threads, team_blocks, threads or default_threads()))
 
@@ -175,14 +186,14 @@ def shuffle_tree(x, dtype: int, team_threads: int, team_blocks: int,
 def shuffle_tree_sq(x, dtype: int, team_threads: int, team_blocks: int,
                     threads: int | None = None) -> np.float32:
     """The declared SHUFFLE_TREE order over the leaves x_i^2."""
-    a = _bits(x).reshape(-1)
+    a = _bits(x, dtype).reshape(-1)
     return np.float32(_load().oracle_shuffle_tree_sq_f32(
         _u16p(a), a.size, dtype, team_threads, team_blocks, threads or default_threads()))
 
 
 def shuffle_tree_rows(x, dtype: int, team_threads: int, team_blocks: int,
                       threads: int | None = None, squares: bool = False) -> np.ndarray:
-    a = _bits(x)
+    a = _bits(x, dtype)
     rows, cols = a.shape
     out = np.empty(rows, np.float32)
     _load().oracle_shuffle_tree_rows_f32(_u16p(a), rows, cols, dtype, 1 if squares else 0,
@@ -193,7 +204,7 @@ def shuffle_tree_rows(x, dtype: int, team_threads: int, team_blocks: int,
 
 
 def leaves(x, dtype: int) -> np.ndarray:
-    a = _bits(x).reshape(-1)
+    a = _bits(x, dtype).reshape(-1)
     out = np.empty(a.size, np.float32)
     _load().oracle_leaves_f32(_u16p(a), a.size, dtype,
                               out.ctypes.data_as(ctypes.POINTER(ctypes.c_float)))

@@ -26,7 +26,8 @@
  *
  * Readings taken where the pages are silent (each one is also listed in the
  * design notes):
- *  - Leaves are the exact binary32 values of the binary16 / bfloat16 inputs.
+ *  - Leaves are the exact binary32 values of the binary16 / bfloat16 /
+ *    binary32 inputs (binary32 inputs are their own leaves).
  *  - The balanced tree is over index order with power-of-two aligned
  *    subtrees; the input is padded to the next power of two with -0.0,
  *    which is the identity of IEEE round-to-nearest addition for every x
@@ -52,10 +53,13 @@
 
 #define DT_F16 0
 #define DT_BF16 1
+#define DT_F32 2
 
 /* ------------------------------------------------------------------ */
-/* Decoding one 16-bit input (IEEE 754 binary16, or bfloat16 = the upper
- * half of binary32).  A finite value is (-1)^neg * m * 2^e with integer m. */
+/* Decoding one input (IEEE 754 binary16, bfloat16 = the upper half of
+ * binary32, or binary32 itself).  A finite value is (-1)^neg * m * 2^e with
+ * an integer m.  Inputs are arrays of 16-bit patterns, or of 32-bit
+ * patterns for binary32; raw_at() reads pattern i of either. */
 
 typedef struct {
     int neg;      /* sign bit */
@@ -64,11 +68,37 @@ typedef struct {
     int e;        /* exponent of the significand's unit bit */
 } decoded_t;
 
-static decoded_t decode16(uint16_t h, int dtype)
+static uint32_t raw_at(const void *x, size_t i, int dtype)
+{
+    if (dtype == DT_F32) return ((const uint32_t *)x)[i];
+    return ((const uint16_t *)x)[i];
+}
+
+/* The address of pattern i (the start of row i / cols, for row calls). */
+static const void *raw_ptr(const void *x, size_t i, int dtype)
+{
+    if (dtype == DT_F32) return (const uint32_t *)x + i;
+    return (const uint16_t *)x + i;
+}
+
+static decoded_t decode(uint32_t h, int dtype)
 {
     decoded_t d;
-    d.neg = (h >> 15) & 1;
     d.special = 0;
+    if (dtype == DT_F32) {
+        /* binary32: 8 exponent bits (bias 127), 23 fraction bits */
+        uint32_t ex = (h >> 23) & 0xff, fr = h & 0x7fffff;
+        d.neg = (int)(h >> 31);
+        if (ex == 0xff) {
+            d.special = fr ? 2 : 1; d.m = 0; d.e = 0;
+        } else if (ex == 0) {            /* subnormal: fr * 2^-149 */
+            d.m = fr; d.e = -149;
+        } else {                         /* (2^23 + fr) * 2^(ex - 127 - 23) */
+            d.m = (1u << 23) + fr; d.e = (int)ex - 150;
+        }
+        return d;
+    }
+    d.neg = (h >> 15) & 1;
     if (dtype == DT_F16) {
         /* binary16: 5 exponent bits (bias 15), 10 fraction bits */
         uint32_t ex = (h >> 10) & 0x1f, fr = h & 0x3ff;
@@ -95,9 +125,9 @@ static decoded_t decode16(uint16_t h, int dtype)
 
 /* The exact binary32 value of one input (every binary16 and bfloat16 value
  * is a binary32 value, so the conversion through double is exact). */
-static float leaf_f32(uint16_t h, int dtype)
+static float leaf_f32(uint32_t h, int dtype)
 {
-    decoded_t d = decode16(h, dtype);
+    decoded_t d = decode(h, dtype);
     if (d.special == 2) return NAN;
     if (d.special == 1) return d.neg ? -INFINITY : INFINITY;
     double v = ldexp((double)d.m, d.e);
@@ -106,15 +136,15 @@ static float leaf_f32(uint16_t h, int dtype)
 }
 
 /* ------------------------------------------------------------------ */
-/* Exact sums: a two's-complement fixed-point accumulator of 9 x 64 bits
- * whose bit 0 weighs 2^-266 -- the square of the smallest bfloat16
- * subnormal 2^-133, so that every input (a multiple of 2^-133) and every
- * square of an input (a multiple of 2^-266) is an integer multiple of it.
- * The largest square of a bfloat16 is below 2^256, so 2^40 terms stay below
- * 2^296, far inside 575 bits. */
+/* Exact sums: a two's-complement fixed-point accumulator of 10 x 64 bits
+ * whose bit 0 weighs 2^-298 -- the square of the smallest binary32
+ * subnormal 2^-149, so that every input (a multiple of 2^-149) and every
+ * square of an input (a multiple of 2^-298) is an integer multiple of it.
+ * The largest square of a binary32 or bfloat16 is below 2^256, so 2^40
+ * terms stay below 2^296, far inside 639 bits. */
 
-#define ACC_LIMBS 9
-#define ACC_LSB_EXP (-266)
+#define ACC_LIMBS 10
+#define ACC_LSB_EXP (-298)
 
 typedef struct { uint64_t w[ACC_LIMBS]; } acc_t;
 
@@ -140,14 +170,16 @@ static void acc_negate(acc_t *a)
     acc_add(a, &one);
 }
 
-/* acc += (neg ? -1 : 1) * m * 2^pos, 0 <= pos < 64 * (ACC_LIMBS - 1) */
-static void acc_add_term(acc_t *a, uint64_t m, int pos, int neg)
+/* acc += (neg ? -1 : 1) * m * 2^pos, m < 2^128, 0 <= pos < 64 * (ACC_LIMBS - 2) */
+static void acc_add_term(acc_t *a, unsigned __int128 m, int pos, int neg)
 {
     acc_t t;
     memset(&t, 0, sizeof t);
     int limb = pos / 64, sh = pos % 64;
-    t.w[limb] = m << sh;
-    if (sh != 0) t.w[limb + 1] = m >> (64 - sh);
+    const uint64_t lo = (uint64_t)m, hi = (uint64_t)(m >> 64);
+    t.w[limb] = lo << sh;
+    t.w[limb + 1] = (sh ? lo >> (64 - sh) : 0) | (hi << sh);
+    if (sh != 0) t.w[limb + 2] = hi >> (64 - sh);
     if (neg) acc_negate(&t);
     acc_add(a, &t);
 }
@@ -155,7 +187,7 @@ static void acc_add_term(acc_t *a, uint64_t m, int pos, int neg)
 static int acc_bit(const acc_t *a, int i) { return (int)((a->w[i / 64] >> (i % 64)) & 1u); }
 
 /* Round the exact value held in the accumulator to the nearest binary64
- * (ties to even).  The accumulator's quantum 2^-133 is far above binary64's
+ * (ties to even).  The accumulator's quantum 2^-298 is far above binary64's
  * subnormal range, so only the 53-bit significand limit applies. */
 static double acc_to_double(const acc_t *a)
 {
@@ -181,23 +213,26 @@ static double acc_to_double(const acc_t *a)
 }
 
 /* Exact summation by exponent buckets: every finite input is +-m * 2^e with
- * an integer m < 2^11 and e >= -133, and its square is m^2 * 2^(2e) with
- * m^2 < 2^22 and 2e >= -266.  Integer sums of m (or m^2) per exponent are
- * exact (below 2^22 * n < 2^63 for n < 2^40), and the buckets are then added
- * into the long accumulator, m_e * 2^e each.  Bucket index = e + 266. */
-#define N_EXP 512
+ * an integer m < 2^24 and e >= -149, and its square is m^2 * 2^(2e) with
+ * m^2 < 2^48 and 2e >= -298.  Integer sums of m (or m^2) per exponent are
+ * exact in 128 bits (below 2^48 * n < 2^88 for n < 2^40), and the buckets
+ * are then added into the long accumulator, m_e * 2^e each.  Bucket index =
+ * exponent + 298. */
+#define N_EXP 560
 
 typedef struct {
-    int64_t signed_m[N_EXP];    /* sum of +-m for inputs with exponent e = index - 133 */
-    uint64_t abs_m[N_EXP];      /* sum of m for the same inputs */
+    __int128 signed_m[N_EXP];            /* sum of +-m (or m^2) per exponent */
+    unsigned __int128 abs_m[N_EXP];      /* sum of m (or m^2) per exponent */
     size_t pos_inf, neg_inf, nan;
 } exact_state_t;
 
-/* squares != 0: accumulate x^2 (always >= 0) instead of x. */
-static void exact_accumulate(exact_state_t *st, const uint16_t *x, size_t n, int dtype, int squares)
+/* squares != 0: accumulate x^2 (always >= 0) instead of x.  Inputs
+ * lo .. lo+n-1 of x. */
+static void exact_accumulate(exact_state_t *st, const void *x, size_t lo, size_t n, int dtype,
+                             int squares)
 {
-    for (size_t i = 0; i < n; i++) {
-        decoded_t d = decode16(x[i], dtype);
+    for (size_t i = lo; i < lo + n; i++) {
+        decoded_t d = decode(raw_at(x, i, dtype), dtype);
         if (d.special == 2) { st->nan++; continue; }
         if (d.special == 1) {
             if (d.neg && !squares) st->neg_inf++; else st->pos_inf++;
@@ -206,11 +241,11 @@ static void exact_accumulate(exact_state_t *st, const uint16_t *x, size_t n, int
         if (squares) {
             int pos = 2 * d.e - ACC_LSB_EXP;
             uint64_t m2 = (uint64_t)d.m * (uint64_t)d.m;
-            st->signed_m[pos] += (int64_t)m2;
+            st->signed_m[pos] += (__int128)m2;
             st->abs_m[pos] += m2;
         } else {
             int pos = d.e - ACC_LSB_EXP;
-            st->signed_m[pos] += d.neg ? -(int64_t)d.m : (int64_t)d.m;
+            st->signed_m[pos] += d.neg ? -(__int128)d.m : (__int128)d.m;
             st->abs_m[pos] += d.m;
         }
     }
@@ -224,7 +259,7 @@ static void exact_accumulate(exact_state_t *st, const uint16_t *x, size_t n, int
  * Threads only split the index range; integer addition is exact, so the
  * result does not depend on the thread count.
  */
-static void exact_sum_any(const uint16_t *x, size_t n, int dtype, int squares, int threads,
+static void exact_sum_any(const void *x, size_t n, int dtype, int squares, int threads,
                           double *sum_out, double *abs_out)
 {
     int nt = threads > 0 ? threads : 1;
@@ -238,7 +273,7 @@ static void exact_sum_any(const uint16_t *x, size_t n, int dtype, int squares, i
         size_t lo = (size_t)t * per, hi = lo + per;
         if (lo > n) lo = n;
         if (hi > n) hi = n;
-        exact_accumulate(&parts[t], x + lo, hi - lo, dtype, squares);
+        exact_accumulate(&parts[t], x, lo, hi - lo, dtype, squares);
     }
     exact_state_t tot;
     memset(&tot, 0, sizeof tot);
@@ -266,8 +301,9 @@ static void exact_sum_any(const uint16_t *x, size_t n, int dtype, int squares, i
     memset(&sum, 0, sizeof sum);
     memset(&abs_sum, 0, sizeof abs_sum);
     for (int e = 0; e < N_EXP; e++) {
-        int64_t sm = tot.signed_m[e];
-        uint64_t mag = sm < 0 ? (uint64_t)0 - (uint64_t)sm : (uint64_t)sm;
+        __int128 sm = tot.signed_m[e];
+        unsigned __int128 mag = sm < 0 ? (unsigned __int128)0 - (unsigned __int128)sm
+                                       : (unsigned __int128)sm;
         if (mag) acc_add_term(&sum, mag, e, sm < 0);
         if (tot.abs_m[e]) acc_add_term(&abs_sum, tot.abs_m[e], e, 0);
     }
@@ -275,7 +311,7 @@ static void exact_sum_any(const uint16_t *x, size_t n, int dtype, int squares, i
     *abs_out = acc_to_double(&abs_sum);
 }
 
-void oracle_exact_sum(const uint16_t *x, size_t n, int dtype, int threads, double *sum_out,
+void oracle_exact_sum(const void *x, size_t n, int dtype, int threads, double *sum_out,
                       double *abs_out)
 {
     exact_sum_any(x, n, dtype, 0, threads, sum_out, abs_out);
@@ -283,28 +319,28 @@ void oracle_exact_sum(const uint16_t *x, size_t n, int dtype, int threads, doubl
 
 /* The exact sum of x_i^2, rounded once to binary64 (abs_out receives the
  * same value: every term is non-negative). */
-void oracle_exact_sum_squares(const uint16_t *x, size_t n, int dtype, int threads,
+void oracle_exact_sum_squares(const void *x, size_t n, int dtype, int threads,
                               double *sum_out, double *abs_out)
 {
     exact_sum_any(x, n, dtype, 1, threads, sum_out, abs_out);
 }
 
-void oracle_exact_sum_rows(const uint16_t *x, size_t rows, size_t cols, int dtype,
+void oracle_exact_sum_rows(const void *x, size_t rows, size_t cols, int dtype,
                            int threads, double *sum_out, double *abs_out)
 {
     int nt = threads > 0 ? threads : 1;
 #pragma omp parallel for num_threads(nt) schedule(dynamic, 64)
     for (size_t r = 0; r < rows; r++)
-        exact_sum_any(x + r * cols, cols, dtype, 0, 1, &sum_out[r], &abs_out[r]);
+        exact_sum_any(raw_ptr(x, r * cols, dtype), cols, dtype, 0, 1, &sum_out[r], &abs_out[r]);
 }
 
-void oracle_exact_sum_squares_rows(const uint16_t *x, size_t rows, size_t cols, int dtype,
+void oracle_exact_sum_squares_rows(const void *x, size_t rows, size_t cols, int dtype,
                                    int threads, double *sum_out, double *abs_out)
 {
     int nt = threads > 0 ? threads : 1;
 #pragma omp parallel for num_threads(nt) schedule(dynamic, 64)
     for (size_t r = 0; r < rows; r++)
-        exact_sum_any(x + r * cols, cols, dtype, 1, 1, &sum_out[r], &abs_out[r]);
+        exact_sum_any(raw_ptr(x, r * cols, dtype), cols, dtype, 1, 1, &sum_out[r], &abs_out[r]);
 }
 
 /* ------------------------------------------------------------------ */
@@ -319,8 +355,9 @@ static int ceil_log2(size_t n)
 
 /* The leaf of input h: its binary32 value, or for sums of squares the
  * binary32 product of that value with itself (one rounding to nearest even;
- * the product of two binary16 or bfloat16 values is exact in binary64). */
-static float leaf_op(uint16_t h, int dtype, int squares)
+ * the product of two binary32 values -- 24-bit significands, exponents
+ * within binary64's normal range -- is exact in binary64). */
+static float leaf_op(uint32_t h, int dtype, int squares)
 {
     float f = leaf_f32(h, dtype);
     if (!squares) return f;
@@ -331,13 +368,13 @@ static float leaf_op(uint16_t h, int dtype, int squares)
  * children, left + right, in binary32.  Leaves past n are the -0.0 pad.
  * A subtree that lies wholly in the pad has the value -0.0 (every leaf is
  * -0.0 and -0.0 + -0.0 = -0.0), so it is returned without descending. */
-static float tree_node16(const uint16_t *x, size_t n, int dtype, int squares, size_t lo, int h)
+static float tree_node_in(const void *x, size_t n, int dtype, int squares, size_t lo, int h)
 {
     if (lo >= n) return -0.0f;
-    if (h == 0) return leaf_op(x[lo], dtype, squares);
+    if (h == 0) return leaf_op(raw_at(x, lo, dtype), dtype, squares);
     size_t half = (size_t)1 << (h - 1);
-    float left = tree_node16(x, n, dtype, squares, lo, h - 1);
-    float right = tree_node16(x, n, dtype, squares, lo + half, h - 1);
+    float left = tree_node_in(x, n, dtype, squares, lo, h - 1);
+    float right = tree_node_in(x, n, dtype, squares, lo + half, h - 1);
     return left + right;
 }
 
@@ -364,7 +401,7 @@ static float tree_f32(const float *a, size_t m)
  * top levels are then formed from those subtree values in the same shape,
  * so the result is that of the single recursive definition.
  */
-static float fixed_order_any(const uint16_t *x, size_t n, int dtype, int squares, int threads)
+static float fixed_order_any(const void *x, size_t n, int dtype, int squares, int threads)
 {
     if (n == 0) return 0.0f;
     int H = ceil_log2(n);
@@ -374,39 +411,41 @@ static float fixed_order_any(const uint16_t *x, size_t n, int dtype, int squares
     int nt = threads > 0 ? threads : 1;
 #pragma omp parallel for num_threads(nt) schedule(dynamic, 1)
     for (size_t i = 0; i < parts; i++)
-        node[i] = tree_node16(x, n, dtype, squares, i << (H - k), H - k);
+        node[i] = tree_node_in(x, n, dtype, squares, i << (H - k), H - k);
     float r = tree_node32(node, parts, 0, k);
     free(node);
     return r;
 }
 
-float oracle_fixed_order_f32(const uint16_t *x, size_t n, int dtype, int threads)
+float oracle_fixed_order_f32(const void *x, size_t n, int dtype, int threads)
 {
     return fixed_order_any(x, n, dtype, 0, threads);
 }
 
 /* The same tree over the leaves x_i^2 (sum of squares). */
-float oracle_fixed_order_sq_f32(const uint16_t *x, size_t n, int dtype, int threads)
+float oracle_fixed_order_sq_f32(const void *x, size_t n, int dtype, int threads)
 {
     return fixed_order_any(x, n, dtype, 1, threads);
 }
 
-void oracle_fixed_order_rows_f32(const uint16_t *x, size_t rows, size_t cols, int dtype,
+void oracle_fixed_order_rows_f32(const void *x, size_t rows, size_t cols, int dtype,
                                  int squares, int threads, float *out)
 {
     int nt = threads > 0 ? threads : 1;
 #pragma omp parallel for num_threads(nt) schedule(dynamic, 64)
     for (size_t r = 0; r < rows; r++)
-        out[r] = fixed_order_any(x + r * cols, cols, dtype, squares, 1);
+        out[r] = fixed_order_any(raw_ptr(x, r * cols, dtype), cols, dtype, squares, 1);
 }
 
 /* ------------------------------------------------------------------ */
 /* Declared order of the conventional reduction (SHUFFLE_TREE).
  *
- * A segment of L inputs is split into vectors of 8 consecutive inputs
- * (v = inputs 8v .. 8v+7, the last one padded with -0.0).  It is reduced by
- * a team of G blocks of Bt threads (T = G*Bt threads, thread g = b*Bt + t):
- *   1. vector value   = balanced tree over its 8 leaves;
+ * A segment of L inputs is split into vectors of V consecutive inputs, the
+ * inputs of 16 bytes: V = 8 for binary16 and bfloat16, V = 4 for binary32
+ * (v = inputs V*v .. V*v+V-1, the last one padded with -0.0).  It is
+ * reduced by a team of G blocks of Bt threads (T = G*Bt threads, thread
+ * g = b*Bt + t):
+ *   1. vector value   = balanced tree over its V leaves;
  *   2. thread value   = acc, acc starts at -0.0 and for v = g, g+T, g+2T, ...
  *                       acc = acc + vector value (in that order);
  *   3. warp value     = butterfly over the 32 lanes of the warp: for the
@@ -418,21 +457,26 @@ void oracle_fixed_order_rows_f32(const uint16_t *x, size_t rows, size_t cols, in
  *   5. segment value  = balanced tree over the G block values in block
  *                       order, padded with -0.0.
  */
-static float vector_tree8(const uint16_t *x, size_t L, int dtype, int squares, size_t v)
+static size_t vector_len(int dtype) { return dtype == DT_F32 ? 4 : 8; }
+
+static float vector_tree(const void *x, size_t L, int dtype, int squares, size_t v)
 {
+    const size_t V = vector_len(dtype);
     float e[8];
-    for (int k = 0; k < 8; k++) {
-        size_t i = 8 * v + (size_t)k;
-        e[k] = i < L ? leaf_op(x[i], dtype, squares) : -0.0f;
+    for (size_t k = 0; k < V; k++) {
+        size_t i = V * v + k;
+        e[k] = i < L ? leaf_op(raw_at(x, i, dtype), dtype, squares) : -0.0f;
     }
+    if (V == 4) return (e[0] + e[1]) + (e[2] + e[3]);
     return ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
 }
 
-static float shuffle_block_value(const uint16_t *x, size_t L, int dtype, int squares, int Bt, int G,
+static float shuffle_block_value(const void *x, size_t L, int dtype, int squares, int Bt, int G,
                                  int b)
 {
     size_t T = (size_t)G * (size_t)Bt;
-    size_t nvec = (L + 7) / 8;
+    size_t V = vector_len(dtype);
+    size_t nvec = (L + V - 1) / V;
     int W = Bt / 32;
     float warp_value[32];
     for (int w = 0; w < W; w++) {
@@ -440,7 +484,7 @@ static float shuffle_block_value(const uint16_t *x, size_t L, int dtype, int squ
         for (int j = 0; j < 32; j++) {
             size_t g = (size_t)b * (size_t)Bt + (size_t)w * 32 + (size_t)j;
             float acc = -0.0f;
-            for (size_t v = g; v < nvec; v += T) acc = acc + vector_tree8(x, L, dtype, squares, v);
+            for (size_t v = g; v < nvec; v += T) acc = acc + vector_tree(x, L, dtype, squares, v);
             lane[j] = acc;
         }
         for (int off = 16; off >= 1; off /= 2) {
@@ -452,7 +496,7 @@ static float shuffle_block_value(const uint16_t *x, size_t L, int dtype, int squ
     return tree_f32(warp_value, (size_t)W);
 }
 
-static float shuffle_tree_any(const uint16_t *x, size_t L, int dtype, int squares, int Bt, int G,
+static float shuffle_tree_any(const void *x, size_t L, int dtype, int squares, int Bt, int G,
                               int threads)
 {
     if (L == 0) return 0.0f;
@@ -466,30 +510,30 @@ static float shuffle_tree_any(const uint16_t *x, size_t L, int dtype, int square
     return r;
 }
 
-float oracle_shuffle_tree_f32(const uint16_t *x, size_t L, int dtype, int Bt, int G, int threads)
+float oracle_shuffle_tree_f32(const void *x, size_t L, int dtype, int Bt, int G, int threads)
 {
     return shuffle_tree_any(x, L, dtype, 0, Bt, G, threads);
 }
 
 /* The same declared order over the leaves x_i^2 (sum of squares). */
-float oracle_shuffle_tree_sq_f32(const uint16_t *x, size_t L, int dtype, int Bt, int G,
+float oracle_shuffle_tree_sq_f32(const void *x, size_t L, int dtype, int Bt, int G,
                                  int threads)
 {
     return shuffle_tree_any(x, L, dtype, 1, Bt, G, threads);
 }
 
-void oracle_shuffle_tree_rows_f32(const uint16_t *x, size_t rows, size_t cols, int dtype,
+void oracle_shuffle_tree_rows_f32(const void *x, size_t rows, size_t cols, int dtype,
                                   int squares, int Bt, int G, int threads, float *out)
 {
     int nt = threads > 0 ? threads : 1;
 #pragma omp parallel for num_threads(nt) schedule(dynamic, 64)
     for (size_t r = 0; r < rows; r++)
-        out[r] = shuffle_tree_any(x + r * cols, cols, dtype, squares, Bt, G, 1);
+        out[r] = shuffle_tree_any(raw_ptr(x, r * cols, dtype), cols, dtype, squares, Bt, G, 1);
 }
 
 /* Exact binary32 value of each input (used by the tests to compare the
  * decoder with independent conversions). */
-void oracle_leaves_f32(const uint16_t *x, size_t n, int dtype, float *out)
+void oracle_leaves_f32(const void *x, size_t n, int dtype, float *out)
 {
-    for (size_t i = 0; i < n; i++) out[i] = leaf_f32(x[i], dtype);
+    for (size_t i = 0; i < n; i++) out[i] = leaf_f32(raw_at(x, i, dtype), dtype);
 }

@@ -16,13 +16,15 @@ import pytest
 import oracle
 from arithmetic_reduction_tensor_gb300 import synth
 
-F16, BF16 = oracle.F16, oracle.BF16
+F16, BF16, F32 = oracle.F16, oracle.BF16, oracle.F32
 
 
 # ---------------------------------------------------------------- helpers
 
 def np_leaves(bits, dtype):
     """binary32 values decoded by numpy (independent of the oracle's decoder)."""
+    if dtype == F32:
+        return np.asarray(bits, np.uint32).view(np.float32)
     bits = np.asarray(bits, np.uint16)
     if dtype == F16:
         return bits.view(np.float16).astype(np.float32)
@@ -55,17 +57,21 @@ def np_tree(values_f32):
 
 
 @np.errstate(over="ignore", invalid="ignore")
-def np_shuffle(bits, dtype, bt, g):
-    """Vectorised emulation of the declared SHUFFLE_TREE order."""
-    v = np_leaves(bits, dtype)
+def np_shuffle(bits, dtype, bt, g, leaf_values=None):
+    """Vectorised emulation of the declared SHUFFLE_TREE order (vectors of
+    16 bytes: 8 inputs of 16 bits, 4 of binary32)."""
+    v = np_leaves(bits, dtype) if leaf_values is None else leaf_values
     L = v.size
     if L == 0:
         return np.float32(0.0)
-    nvec = (L + 7) // 8
-    e = np.full(nvec * 8, -0.0, np.float32)
+    V = 4 if dtype == F32 else 8
+    nvec = (L + V - 1) // V
+    e = np.full(nvec * V, -0.0, np.float32)
     e[:L] = v
-    e = e.reshape(nvec, 8)
-    vec = ((e[:, 0] + e[:, 1]) + (e[:, 2] + e[:, 3])) + ((e[:, 4] + e[:, 5]) + (e[:, 6] + e[:, 7]))
+    e = e.reshape(nvec, V)
+    while e.shape[1] > 1:
+        e = e[:, 0::2] + e[:, 1::2]
+    vec = e[:, 0]
     T = bt * g
     acc = np.full(T, -0.0, np.float32)
     for start in range(0, nvec, T):
@@ -90,6 +96,10 @@ def same_f32(a, b):
 
 def special_patterns(dtype):
     """Bit patterns at the edges of each format: zeros, subnormals, extremes."""
+    if dtype == F32:
+        return [0x00000000, 0x80000000, 0x00000001, 0x80000001, 0x007FFFFF, 0x807FFFFF,
+                0x00800000, 0x80800000, 0x3F800000, 0xBF800000, 0x7F7FFFFF, 0xFF7FFFFF,
+                0x3F7FFFFF, 0x3F800001]
     if dtype == F16:
         return [0x0000, 0x8000, 0x0001, 0x8001, 0x03FF, 0x83FF, 0x0400, 0x8400,
                 0x3C00, 0xBC00, 0x7BFF, 0xFBFF, 0x3BFF, 0x3C01]
@@ -99,6 +109,11 @@ def special_patterns(dtype):
 
 def random_finite(rng, n, dtype):
     """Random finite bit patterns (any exponent, both signs, subnormals)."""
+    if dtype == F32:
+        b = rng.integers(0, 1 << 32, n, dtype=np.uint64).astype(np.uint32)
+        bad = (b & np.uint32(0x7F800000)) == np.uint32(0x7F800000)
+        b[bad] &= np.uint32(0xBFFFFFFF)
+        return b
     b = rng.integers(0, 1 << 16, n, dtype=np.uint32).astype(np.uint16)
     exp_mask = 0x7C00 if dtype == F16 else 0x7F80
     bad = (b & exp_mask) == exp_mask
@@ -404,29 +419,9 @@ def test_fixed_order_sq_matches_levelwise_numpy(dtype, n):
     assert same_f32(got, np_tree(np_square_leaves(bits, dtype)))
 
 
-@np.errstate(over="ignore", invalid="ignore")
 def np_shuffle_sq(bits, dtype, bt, g):
     """Vectorised emulation of the declared order over squared leaves."""
-    v = np_square_leaves(bits, dtype)
-    L = v.size
-    nvec = (L + 7) // 8
-    e = np.full(nvec * 8, -0.0, np.float32)
-    e[:L] = v
-    e = e.reshape(nvec, 8)
-    vec = ((e[:, 0] + e[:, 1]) + (e[:, 2] + e[:, 3])) + ((e[:, 4] + e[:, 5]) + (e[:, 6] + e[:, 7]))
-    T = bt * g
-    acc = np.full(T, -0.0, np.float32)
-    for start in range(0, nvec, T):
-        m = min(T, nvec - start)
-        acc[:m] = acc[:m] + vec[start:start + m]
-    lanes = acc.reshape(-1, 32)
-    idx = np.arange(32)
-    for off in (16, 8, 4, 2, 1):
-        lanes = lanes + lanes[:, idx ^ off]
-    warp = lanes[:, 0].reshape(g, bt // 32)
-    while warp.shape[1] > 1:
-        warp = warp[:, 0::2] + warp[:, 1::2]
-    return np_tree(warp[:, 0])
+    return np_shuffle(bits, dtype, bt, g, leaf_values=np_square_leaves(bits, dtype))
 
 
 @pytest.mark.parametrize("dtype", [F16, BF16])
@@ -448,3 +443,125 @@ def test_sum_squares_rows_match_whole_rows():
         assert s[r] == oracle.exact_sum_squares(x[r], F16, threads=1)[0]
         assert same_f32(f[r], oracle.fixed_order_sq(x[r], F16, threads=1))
         assert same_f32(t[r], oracle.shuffle_tree_sq(x[r], F16, 128, 2, threads=1))
+
+
+# ---------------------------------------------------------------- binary32 inputs
+
+def test_leaves_f32_are_the_patterns_themselves():
+    rng = np.random.default_rng(40)
+    bits = np.concatenate([random_finite(rng, 200_000, F32),
+                           np.array(special_patterns(F32), np.uint32),
+                           np.array([0x7F800000, 0xFF800000, 0x7FC00000, 0xFF812345], np.uint32)])
+    got = oracle.leaves(bits, F32)
+    nan = np.isnan(bits.view(np.float32))
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got.view(np.uint32)[~nan], bits[~nan])
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_exact_sum_f32_brute_force(seed):
+    rng = np.random.default_rng(300 + seed)
+    n = int(rng.integers(1, 65))
+    bits = np.concatenate([random_finite(rng, n, F32), np.array(special_patterns(F32), np.uint32)])
+    rng.shuffle(bits)
+    s, a = oracle.exact_sum(bits, F32, threads=3)
+    fs, fa = frac_sum(bits, F32)
+    assert s == float(fs) and a == float(fa)
+    s2, _ = oracle.exact_sum_squares(bits, F32, threads=2)
+    exact = sum((Fraction(float(v)) ** 2 for v in np_leaves(bits, F32).astype(np.float64)),
+                Fraction(0))
+    assert s2 == float(exact)
+
+
+def test_exact_sum_f32_rounding_and_extremes():
+    def f(x):
+        return int(np.float32(x).view(np.uint32))
+    # ties to even and sticky, with the smallest binary32 subnormal 2^-149
+    assert oracle.exact_sum(np.array([f(1.0), f(2.0 ** -53)], np.uint32), F32)[0] == 1.0
+    sticky = np.array([f(1.0), f(2.0 ** -53), 0x00000001], np.uint32)
+    assert oracle.exact_sum(sticky, F32)[0] == 1.0 + 2.0 ** -52
+    # 2^20 copies of the largest binary32: the per-exponent integer sum and,
+    # for the squares, m^2 sums beyond 2^64 must stay exact
+    big = np.full(1 << 20, 0x7F7FFFFF, np.uint32)
+    fmax = Fraction(float(np.float32(np.finfo(np.float32).max)))
+    assert oracle.exact_sum(big, F32)[0] == float(fmax * (1 << 20))
+    assert oracle.exact_sum_squares(big, F32)[0] == float(fmax ** 2 * (1 << 20))
+    m = np.full(3_000_001, 0x3F7FFFFF, np.uint32)    # 1 - 2^-24: m^2 near 2^48
+    one_less = Fraction(float(np.float32(1.0) - np.float32(2.0 ** -24)))
+    assert oracle.exact_sum_squares(m, F32)[0] == float(one_less ** 2 * 3_000_001)
+    tiny = np.full(7, 0x00000001, np.uint32)          # squares 2^-298 each
+    assert oracle.exact_sum_squares(tiny, F32)[0] == 7 * 2.0 ** -298
+    both = np.concatenate([big, big ^ np.uint32(0x80000000)])
+    assert oracle.exact_sum(both, F32)[0] == 0.0
+
+
+def test_exact_sum_f32_non_finite():
+    one, inf, nan = 0x3F800000, 0x7F800000, 0x7FC00000
+    assert oracle.exact_sum(np.array([one, inf], np.uint32), F32)[0] == math.inf
+    assert oracle.exact_sum(np.array([one, inf | 0x80000000], np.uint32), F32)[0] == -math.inf
+    assert math.isnan(oracle.exact_sum(np.array([inf, inf | 0x80000000], np.uint32), F32)[0])
+    assert math.isnan(oracle.exact_sum(np.array([one, nan], np.uint32), F32)[0])
+    assert oracle.exact_sum_squares(np.array([inf | 0x80000000], np.uint32), F32)[0] == math.inf
+
+
+@pytest.mark.parametrize("n", [1, 3, 4, 5, 8, 1000, 4097, 65537, 100_003])
+def test_fixed_order_f32_matches_levelwise_numpy(n):
+    rng = np.random.default_rng(n + 41)
+    bits = random_finite(rng, n, F32) if n < 5000 else synth.generate(n, "normal", F32, seed=n)
+    assert same_f32(oracle.fixed_order(bits, F32, threads=4), np_tree(np_leaves(bits, F32)))
+    assert same_f32(oracle.fixed_order_sq(bits, F32, threads=3),
+                    np_tree(np_square_leaves(bits, F32)))
+
+
+@pytest.mark.parametrize("L,bt,g", [(1, 32, 1), (4, 32, 1), (5, 32, 1), (128, 32, 1), (129, 32, 1),
+                                    (4096, 32, 1), (4097, 32, 1), (10_000, 64, 1),
+                                    (10_000, 128, 3), (70_001, 32, 7), (100_000, 512, 5)])
+def test_shuffle_tree_f32_matches_vectorised_emulation(L, bt, g):
+    rng = np.random.default_rng(L + bt + g + 42)
+    bits = random_finite(rng, L, F32) if L < 5000 else synth.generate(L, "normal", F32, seed=L)
+    assert same_f32(oracle.shuffle_tree(bits, F32, bt, g, threads=3),
+                    np_shuffle(bits, F32, bt, g))
+    assert same_f32(oracle.shuffle_tree_sq(bits, F32, bt, g, threads=2),
+                    np_shuffle_sq(bits, F32, bt, g))
+
+
+def test_shuffle_tree_f32_vector_is_four_inputs():
+    # one binary32 vector holds 4 inputs: up to 4 inputs, the declared order
+    # is their 4-leaf tree (the fixed-order tree); a fifth input starts
+    # lane 1's vector, joined by the butterfly rather than inside the tree
+    rng = np.random.default_rng(43)
+    for L in range(1, 5):
+        bits = random_finite(rng, L, F32)
+        assert same_f32(oracle.shuffle_tree(bits, F32, 32, 1), oracle.fixed_order(bits, F32))
+    # nine inputs make three vectors of 4 (lanes 0, 1, 2); the butterfly
+    # adds lane 2 to lane 0 (offset 2) before lane 1 (offset 1).  With
+    # x0 = 1, x4 = 2^-24, x8 = 3 * 2^-25 and zeros elsewhere:
+    #   (1 + 3*2^-25) + 2^-24 = (1 + 2^-23) + 2^-24 -> tie, even: 1 + 2^-22
+    # whereas vectors of 8 would give (1 + 2^-24) + 3*2^-25 = 1 + 2^-23.
+    bits = np.zeros(9, np.uint32)
+    bits[0], bits[4] = 0x3F800000, 0x33800000
+    bits[8] = int(np.float32(3 * 2.0 ** -25).view(np.uint32))
+    assert oracle.shuffle_tree(bits, F32, 32, 1) == np.float32(1 + 2.0 ** -22)
+    assert oracle.fixed_order(bits, F32) == np.float32(1 + 2.0 ** -23)
+    assert same_f32(oracle.shuffle_tree(bits, F32, 32, 1), np_shuffle(bits, F32, 32, 1))
+
+
+def test_f32_rows_match_whole_rows():
+    x = synth.generate(17 * 3001, "normal", F32, seed=44).reshape(17, 3001)
+    s, a = oracle.exact_sum_rows(x, F32)
+    f = oracle.fixed_order_rows(x, F32)
+    t = oracle.shuffle_tree_rows(x, F32, 64, 2, squares=True)
+    for r in range(17):
+        assert (s[r], a[r]) == oracle.exact_sum(x[r], F32, threads=1)
+        assert same_f32(f[r], oracle.fixed_order(x[r], F32, threads=1))
+        assert same_f32(t[r], oracle.shuffle_tree_sq(x[r], F32, 64, 2, threads=1))
+
+
+def test_f32_inputs_holding_16_bit_values_sum_like_them():
+    # a binary32 array holding binary16 values has the same exact sum and the
+    # same fixed-order result (the order is over index, not over bytes)
+    h = synth.generate(50_001, "normal", F16, seed=45)
+    w = synth.as_float(h, F16).view(np.uint32)
+    assert oracle.exact_sum(w, F32) == oracle.exact_sum(h, F16)
+    assert same_f32(oracle.fixed_order(w, F32), oracle.fixed_order(h, F16))
+    assert oracle.exact_sum_squares(w, F32) == oracle.exact_sum_squares(h, F16)

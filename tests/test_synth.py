@@ -42,3 +42,24 @@ def test_distributions_have_the_stated_ranges():
         p = synth.as_float(synth.generate(1 << 18, "pow2", dt, seed=3), dt)
         e = np.log2(np.abs(p))
         assert np.all(e == np.round(e)) and e.min() == -20 and e.max() == 10
+
+
+def test_binary32_patterns_round_the_same_binary64_values():
+    # the binary32 stream is the binary64 values of the 16-bit streams,
+    # rounded once to binary32 instead of to 16 bits
+    for dist in ("uniform_pm1", "uniform01", "normal"):
+        b32 = synth.generate(4096, dist, synth.F32, seed=5)
+        assert b32.dtype == np.uint32
+        f32 = b32.view(np.float32)
+        f16 = synth.as_float(synth.generate(4096, dist, synth.F16, seed=5), synth.F16)
+        via32 = f32.astype(np.float16).astype(np.float32)
+        # rounding twice (64 -> 32 -> 16) may differ from once only where the
+        # binary32 value lies exactly halfway between two binary16 values
+        differ = via32 != f16
+        assert differ.sum() <= 4
+        lo = np.minimum(via32, f16)[differ].astype(np.float64)
+        hi = np.maximum(via32, f16)[differ].astype(np.float64)
+        assert np.array_equal(f32[differ].astype(np.float64), (lo + hi) / 2)
+    p = synth.as_float(synth.generate(1 << 16, "pow2", synth.F32, seed=3), synth.F32)
+    p16 = synth.as_float(synth.generate(1 << 16, "pow2", synth.F16, seed=3), synth.F16)
+    assert np.array_equal(p, p16)
