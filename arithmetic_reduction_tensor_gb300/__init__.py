@@ -23,7 +23,7 @@ import threading
 from .build import LIB_PATH
 
 __all__ = [
-    "MMA_CHAIN", "SHUFFLE_TREE", "FIXED_ORDER", "MMA_CHAIN_TMEM", "F16", "BF16",
+    "MMA_CHAIN", "SHUFFLE_TREE", "FIXED_ORDER", "MMA_CHAIN_TMEM", "F16", "BF16", "F32",
     "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_CUDA",
     "ORDER_TENSOR_CORE", "ORDER_GRID_STRIDE", "ORDER_BALANCED_TREE",
     "tcr_mode", "tcr_order_desc", "Mode", "TcrError", "c_api",
@@ -33,7 +33,8 @@ __all__ = [
 ]
 
 MMA_CHAIN, SHUFFLE_TREE, FIXED_ORDER, MMA_CHAIN_TMEM = 0, 1, 2, 3
-F16, BF16 = 0, 1
+F16, BF16, F32 = 0, 1, 2
+DTYPE_NAMES = {F16: "f16", BF16: "bf16", F32: "f32"}
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA = 0, 1, 2, 3
 ORDER_TENSOR_CORE, ORDER_GRID_STRIDE, ORDER_BALANCED_TREE = 0, 1, 2
 
@@ -47,7 +48,8 @@ class tcr_mode(ctypes.Structure):
 
     def __repr__(self):
         return (f"Mode({KIND_NAMES.get(self.kind, self.kind)}, R={self.R}, "
-                f"block_threads={self.block_threads}, dtype={'bf16' if self.dtype else 'f16'})")
+                f"block_threads={self.block_threads}, "
+                f"dtype={DTYPE_NAMES.get(self.dtype, self.dtype)})")
 
 
 class tcr_order_desc(ctypes.Structure):
@@ -57,7 +59,8 @@ class tcr_order_desc(ctypes.Structure):
                 ("team_blocks", ctypes.c_int), ("chain_R", ctypes.c_int),
                 ("pad_negative_zero", ctypes.c_int), ("launch_grid", ctypes.c_int),
                 ("launch_block", ctypes.c_int), ("chunk_log2", ctypes.c_int),
-                ("partials", ctypes.c_size_t), ("launches", ctypes.c_int)]
+                ("partials", ctypes.c_size_t), ("launches", ctypes.c_int),
+                ("dtype", ctypes.c_int)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -135,10 +138,19 @@ def _dtype_code(t, mode: tcr_mode) -> int:
         code = F16
     elif t.dtype == torch.bfloat16:
         code = BF16
+    elif t.dtype == torch.float32:
+        code = F32
     elif t.dtype in (torch.int16, torch.uint16):
+        if mode.dtype not in (F16, BF16):
+            raise ValueError("16-bit patterns need mode.dtype F16 or BF16")
         return mode.dtype          # raw 16-bit patterns: the mode says what they are
+    elif t.dtype in (torch.int32, torch.uint32):
+        if mode.dtype != F32:
+            raise ValueError("32-bit patterns need mode.dtype F32")
+        return F32
     else:
-        raise TypeError(f"inputs must be float16, bfloat16 or 16-bit patterns, got {t.dtype}")
+        raise TypeError("inputs must be float16, bfloat16, float32 or their raw patterns, "
+                        f"got {t.dtype}")
     if mode.dtype != code:
         raise ValueError(f"mode.dtype {mode.dtype} does not match tensor dtype {t.dtype}")
     return code

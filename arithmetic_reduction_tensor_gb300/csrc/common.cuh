@@ -1,8 +1,9 @@
 // common.cuh -- device helpers shared by the reduction kernels.
 //
-// Inputs are 16-bit patterns (binary16 or bfloat16).  A "vector" is 8
-// consecutive inputs = 16 bytes = one 128-bit load per lane; a warp load
-// of 32 vectors covers 256 inputs, exactly one 16x16 tensor-core A tile.
+// Inputs are 16-bit patterns (binary16 or bfloat16) or binary32 values.  A
+// "vector" is 16 bytes = one 128-bit load per lane: 8 inputs of 16 bits or
+// 4 of binary32.  A warp load of 32 vectors is 512 bytes: 256 16-bit inputs
+// (exactly one 16x16 tensor-core A tile) or 128 binary32 inputs.
 #pragma once
 
 #include <cstddef>
@@ -15,17 +16,43 @@ namespace tcr {
 
 constexpr int kF16 = 0;
 constexpr int kBF16 = 1;
+constexpr int kF32 = 2;
 constexpr unsigned kFull = 0xffffffffu;
 
-// -0.0 in both 16-bit formats, twice per 32-bit word: the padding of the
+// The storage of an input type: its pattern type T, the inputs per 16-byte
+// vector, and the 32-bit word of -0.0 patterns -- the padding of the
 // ordered modes (the identity of round-to-nearest addition for every x).
-constexpr uint32_t kNegZero2 = 0x80008000u;
+template <int DT>
+struct Elem {
+    using T = uint16_t;
+    static constexpr int kPerVec = 8;
+    static constexpr uint32_t kNegZeroWord = 0x80008000u;
+};
+template <>
+struct Elem<kF32> {
+    using T = uint32_t;
+    static constexpr int kPerVec = 4;
+    static constexpr uint32_t kNegZeroWord = 0x80000000u;
+};
+
+// Inputs per warp group (8 warp loads of 32 vectors) and per warp span
+// (2^kWarpSpanBytesLog2 bytes) of an input type.
+template <int DT>
+__host__ __device__ constexpr size_t group_len()
+{
+    return (size_t)256 * Elem<DT>::kPerVec;
+}
+template <int DT>
+__host__ __device__ constexpr size_t span_len()
+{
+    return ((size_t)1 << kWarpSpanBytesLog2) / sizeof(typename Elem<DT>::T);
+}
 
 // ---------------------------------------------------------------- loads
 
 // 16-byte streaming load through the read-only path.  Every input byte is
 // read exactly once, so the line is not kept in L1.
-__device__ __forceinline__ uint4 ld_stream(const uint16_t *p)
+__device__ __forceinline__ uint4 ld_stream(const void *p)
 {
     uint4 v;
     asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -39,28 +66,51 @@ __device__ __forceinline__ uint32_t pack2(uint16_t lo, uint16_t hi)
     return (uint32_t)lo | ((uint32_t)hi << 16);
 }
 
-// Vector v of a segment of `len` inputs at `seg` (any 2-byte alignment):
-// the inputs past `len` read as `fill` (a 16-bit pattern).
-__device__ __forceinline__ uint4 ld_vec_masked(const uint16_t *seg, size_t len, size_t v,
-                                               uint16_t fill)
+// The fill word of a vector: -0.0 patterns (NEGZERO) or zero bits.
+template <int DT, bool NEGZERO>
+__device__ __forceinline__ uint32_t fill_word()
 {
-    uint16_t e[8];
+    return NEGZERO ? Elem<DT>::kNegZeroWord : 0u;
+}
+
+// Vector v of a segment of `len` inputs at `seg` (any alignment of the
+// pattern type): the inputs past `len` read as the fill (-0.0 when
+// NEGZERO, else zero bits).
+template <int DT, bool NEGZERO>
+__device__ __forceinline__ uint4 ld_vec_masked(const typename Elem<DT>::T *seg, size_t len,
+                                               size_t v)
+{
+    if constexpr (DT == kF32) {
+        const uint32_t f = fill_word<DT, NEGZERO>();
+        uint32_t e[4];
 #pragma unroll
-    for (int k = 0; k < 8; k++) {
-        size_t i = 8 * v + (size_t)k;
-        e[k] = i < len ? __ldg(seg + i) : fill;
+        for (int k = 0; k < 4; k++) {
+            const size_t i = 4 * v + (size_t)k;
+            e[k] = i < len ? __ldg(seg + i) : f;
+        }
+        return make_uint4(e[0], e[1], e[2], e[3]);
+    } else {
+        const uint16_t f = NEGZERO ? (uint16_t)0x8000u : (uint16_t)0u;
+        uint16_t e[8];
+#pragma unroll
+        for (int k = 0; k < 8; k++) {
+            const size_t i = 8 * v + (size_t)k;
+            e[k] = i < len ? __ldg(seg + i) : f;
+        }
+        return make_uint4(pack2(e[0], e[1]), pack2(e[2], e[3]), pack2(e[4], e[5]),
+                          pack2(e[6], e[7]));
     }
-    return make_uint4(pack2(e[0], e[1]), pack2(e[2], e[3]), pack2(e[4], e[5]), pack2(e[6], e[7]));
 }
 
 // Vector v: a single 16-byte load when the segment start is 16-byte
-// aligned (ALIGNED) and the vector lies wholly inside the segment,
-// the element-wise masked load otherwise.  Both give the same 8 patterns.
-template <bool ALIGNED>
-__device__ __forceinline__ uint4 ld_vec(const uint16_t *seg, size_t len, size_t v, uint16_t fill)
+// aligned (ALIGNED) and the vector lies wholly inside the segment, the
+// element-wise masked load otherwise.  Both give the same patterns.
+template <int DT, bool ALIGNED, bool NEGZERO>
+__device__ __forceinline__ uint4 ld_vec(const typename Elem<DT>::T *seg, size_t len, size_t v)
 {
-    if (ALIGNED && 8 * v + 8 <= len) return ld_stream(seg + 8 * v);
-    return ld_vec_masked(seg, len, v, fill);
+    constexpr int V = Elem<DT>::kPerVec;
+    if (ALIGNED && V * v + V <= len) return ld_stream(seg + V * v);
+    return ld_vec_masked<DT, NEGZERO>(seg, len, v);
 }
 
 // ---------------------------------------------------------------- leaves
@@ -123,16 +173,53 @@ __device__ __forceinline__ float pair_val(uint32_t w)
     }
 }
 
-// Balanced tree over the 8 leaves of a vector:
-// ((e0 + e1) + (e2 + e3)) + ((e4 + e5) + (e6 + e7)).
-template <int DT, int OP = kOpSum>
-__device__ __forceinline__ float tree8(uint4 q)
+// The leaf of one binary32 input: the value, or its square (one binary32
+// multiplication, round to nearest).
+template <int OP>
+__device__ __forceinline__ float leaf32(uint32_t w)
 {
-    const float p0 = pair_val<DT, OP>(q.x);
-    const float p1 = pair_val<DT, OP>(q.y);
-    const float p2 = pair_val<DT, OP>(q.z);
-    const float p3 = pair_val<DT, OP>(q.w);
-    return __fadd_rn(__fadd_rn(p0, p1), __fadd_rn(p2, p3));
+    const float v = __uint_as_float(w);
+    if constexpr (OP == kOpSquares) return __fmul_rn(v, v);
+    return v;
+}
+
+// Balanced tree over the leaves of a vector: for 16-bit inputs
+// ((e0 + e1) + (e2 + e3)) + ((e4 + e5) + (e6 + e7)), for binary32
+// (e0 + e1) + (e2 + e3).
+template <int DT, int OP = kOpSum>
+__device__ __forceinline__ float vec_tree(uint4 q)
+{
+    if constexpr (DT == kF32) {
+        // one asm statement, like pair_val for bfloat16: the additions stay
+        // where the vector is consumed, so its registers free early
+        float r;
+        if constexpr (OP == kOpSquares) {
+            asm("{\n\t.reg .f32 a, b, c, d;\n\t"
+                "mul.rn.f32 a, %1, %1;\n\t"
+                "mul.rn.f32 b, %2, %2;\n\t"
+                "mul.rn.f32 c, %3, %3;\n\t"
+                "mul.rn.f32 d, %4, %4;\n\t"
+                "add.rn.f32 a, a, b;\n\t"
+                "add.rn.f32 c, c, d;\n\t"
+                "add.rn.f32 %0, a, c;\n\t}"
+                : "=f"(r)
+                : "r"(q.x), "r"(q.y), "r"(q.z), "r"(q.w));
+        } else {
+            asm("{\n\t.reg .f32 a, c;\n\t"
+                "add.rn.f32 a, %1, %2;\n\t"
+                "add.rn.f32 c, %3, %4;\n\t"
+                "add.rn.f32 %0, a, c;\n\t}"
+                : "=f"(r)
+                : "r"(q.x), "r"(q.y), "r"(q.z), "r"(q.w));
+        }
+        return r;
+    } else {
+        const float p0 = pair_val<DT, OP>(q.x);
+        const float p1 = pair_val<DT, OP>(q.y);
+        const float p2 = pair_val<DT, OP>(q.z);
+        const float p3 = pair_val<DT, OP>(q.w);
+        return __fadd_rn(__fadd_rn(p0, p1), __fadd_rn(p2, p3));
+    }
 }
 
 // ---------------------------------------------------------------- trees

@@ -14,13 +14,16 @@ namespace tcr {
 constexpr int kOpSum = 0;
 constexpr int kOpSquares = 1;
 
-// Inputs per warp group of the tree kernels: 8 warp loads of 256 inputs.
-constexpr size_t kGroup = 2048;
-// Inputs per warp of one CTA work unit (chunk) of the chunked kernels.
-constexpr int kWarpSpanLog2 = 13;
-// Longest row served by one warp; longer rows go through the chunked
-// kernels (FIXED_ORDER, MMA_CHAIN) or the block team (SHUFFLE_TREE).
-constexpr size_t kRowsWarpMaxCols = 16384;
+// Bytes per warp group of the stream kernels: 8 warp loads of 512 bytes
+// (2048 16-bit inputs, 1024 binary32 inputs).
+constexpr size_t kGroupBytes = 4096;
+// Bytes per warp of one CTA work unit (chunk) of the chunked kernels:
+// 2^14 = 4 groups (2^13 16-bit inputs, 2^12 binary32 inputs).
+constexpr int kWarpSpanBytesLog2 = 14;
+// Longest row served by one warp, in bytes (8 groups: 16384 16-bit or 8192
+// binary32 inputs); longer rows go through the chunked kernels
+// (FIXED_ORDER, MMA_CHAIN) or the block team (SHUFFLE_TREE).
+constexpr size_t kRowsWarpMaxBytes = 32768;
 // CTA size of the one-warp-per-row kernels, and the CTAs per SM their
 // register budget is set for (65536 / (256 * 3) -> up to 80 registers).
 constexpr int kRowsBlock = 256;

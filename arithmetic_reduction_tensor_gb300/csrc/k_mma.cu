@@ -15,7 +15,9 @@
 // tree over a CTA's warps, and the combine kernel over CTA chunks.  Rows
 // use one warp per row, so every load is a contiguous 512 bytes of the row.
 // The sum of squares uses the same tiles with D = A * A^T (MmaSqReducer):
-// a genuine contraction, two MMAs per tile.
+// a genuine contraction, two MMAs per tile.  Binary32 inputs are split
+// exactly into three bfloat16 parts on the CUDA cores and the parts summed
+// on the tensor cores, three MMAs per 256 inputs (MmaSplitReducer).
 #include <type_traits>
 
 #include "stream.cuh"
@@ -23,11 +25,13 @@
 namespace tcr {
 
 template <int DT, int R, int OP>
-using MmaRed = typename std::conditional<OP == kOpSquares, MmaSqReducer<DT, R>, MmaReducer<DT, R>>::type;
+using MmaRed = typename std::conditional<
+    DT == kF32, MmaSplitReducer<R, OP>,
+    typename std::conditional<OP == kOpSquares, MmaSqReducer<DT, R>, MmaReducer<DT, R>>::type>::type;
 
 template <int DT, int R, int OP, bool ALIGNED>
 __global__ void __launch_bounds__(1024)
-mma_chunk_kernel(const uint16_t *__restrict__ x, size_t seg_len, size_t units, size_t cps,
+mma_chunk_kernel(const void *__restrict__ x, size_t seg_len, size_t units, size_t cps,
                  int chunk_log2, float *__restrict__ dst)
 {
     chunk_body<MmaRed<DT, R, OP>, ALIGNED>(x, seg_len, units, cps, chunk_log2, dst);
@@ -35,7 +39,7 @@ mma_chunk_kernel(const uint16_t *__restrict__ x, size_t seg_len, size_t units, s
 
 template <int DT, int R, int OP, bool ALIGNED>
 __global__ void __launch_bounds__(kRowsBlock, kRowsMinCtas)
-mma_rows_warp_kernel(const uint16_t *__restrict__ x, size_t rows, size_t cols,
+mma_rows_warp_kernel(const void *__restrict__ x, size_t rows, size_t cols,
                      float *__restrict__ out)
 {
     rows_body<MmaRed<DT, R, OP>, ALIGNED>(x, rows, cols, out);
@@ -52,14 +56,22 @@ static void *pick_dro(bool rows, bool aligned)
                    : (void *)mma_chunk_kernel<DT, R, OP, false>;
 }
 
+template <int DT, int R>
+static void *pick_dr(bool rows, int op, bool aligned)
+{
+    return op == kOpSquares ? pick_dro<DT, R, kOpSquares>(rows, aligned)
+                            : pick_dro<DT, R, kOpSum>(rows, aligned);
+}
+
 template <int R>
 static void *pick_r(bool rows, int dtype, int op, bool aligned)
 {
-    if (dtype == kF16)
-        return op == kOpSquares ? pick_dro<kF16, R, kOpSquares>(rows, aligned)
-                                : pick_dro<kF16, R, kOpSum>(rows, aligned);
-    return op == kOpSquares ? pick_dro<kBF16, R, kOpSquares>(rows, aligned)
-                            : pick_dro<kBF16, R, kOpSum>(rows, aligned);
+    switch (dtype) {
+    case kF16: return pick_dr<kF16, R>(rows, op, aligned);
+    case kBF16: return pick_dr<kBF16, R>(rows, op, aligned);
+    case kF32: return pick_dr<kF32, R>(rows, op, aligned);
+    default: return nullptr;
+    }
 }
 
 static void *pick(bool rows, int dtype, int op, bool aligned, int R)
@@ -77,7 +89,7 @@ static void *pick(bool rows, int dtype, int op, bool aligned, int R)
     }
 }
 
-cudaError_t launch_mma_chunk(int dtype, int op, bool aligned, int R, const uint16_t *x,
+cudaError_t launch_mma_chunk(int dtype, int op, bool aligned, int R, const void *x,
                              size_t seg_len, size_t units, size_t cps, int chunk_log2, float *dst,
                              int grid, int block, cudaStream_t stream)
 {
@@ -88,7 +100,7 @@ cudaError_t launch_mma_chunk(int dtype, int op, bool aligned, int R, const uint1
     return cudaLaunchKernel(k, dim3(grid), dim3(block), args, 0, stream);
 }
 
-cudaError_t launch_mma_rows(int dtype, int op, bool aligned, int R, const uint16_t *x, size_t rows,
+cudaError_t launch_mma_rows(int dtype, int op, bool aligned, int R, const void *x, size_t rows,
                             size_t cols, float *out, int grid, int block, cudaStream_t stream)
 {
     void *k = pick(true, dtype, op, aligned, R);

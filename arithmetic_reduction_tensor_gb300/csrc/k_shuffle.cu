@@ -6,8 +6,9 @@
 // is that reduction, written so that its order is a descriptor ("Taming
 // Bitwise Behavior in GPU Kernels with Tensor Core", arXiv 2609.11356,
 // Abstract): a team of G blocks of Bt threads reduces one segment;
-//   thread g = b*Bt + t accumulates, starting from -0.0, the 8-input trees
-//   of vectors g, g + G*Bt, g + 2*G*Bt, ... in that order;
+//   thread g = b*Bt + t accumulates, starting from -0.0, the trees of the
+//   16-byte vectors (8 inputs of 16 bits, 4 of binary32) g, g + G*Bt,
+//   g + 2*G*Bt, ... in that order;
 //   a warp combines its lanes by the butterfly with offsets 16, 8, 4, 2, 1;
 //   a block is the balanced tree over its warps; the segment is the
 //   balanced tree over its G blocks (the combine kernel, when G > 1).
@@ -18,33 +19,35 @@ namespace tcr {
 constexpr int kShuffleUnroll = 8;    // vectors in flight per thread
 
 // Block team: thread value = -0.0 + vector(first) + vector(first + stride)
-// + ... in order, a vector being its 8-input tree; vectors past the
-// segment are -0.0, the identity.  Software-pipelined: the next 8 vectors
-// are loaded before the current 8 are added.  While every vector of a batch
-// is whole (and the segment 16-byte aligned) the loads walk a pointer with
-// no bounds checks; the ragged end continues, in the same order, with the
-// checked loads.
+// + ... in order, a vector being the tree over its 16 bytes of inputs;
+// vectors past the segment are -0.0, the identity.  Software-pipelined:
+// the next 8 vectors are loaded before the current 8 are added.  While
+// every vector of a batch is whole (and the segment 16-byte aligned) the
+// loads walk a pointer with no bounds checks; the ragged end continues, in
+// the same order, with the checked loads.
 template <int DT, int OP, bool ALIGNED>
-__device__ __forceinline__ float grid_stride_acc(const uint16_t *seg, size_t len, size_t first,
-                                                 size_t stride)
+__device__ __forceinline__ float grid_stride_acc(const typename Elem<DT>::T *seg, size_t len,
+                                                 size_t first, size_t stride)
 {
     constexpr int U = kShuffleUnroll;
-    const size_t nvec = (len + 7) / 8;
-    const uint4 pad = make_uint4(kNegZero2, kNegZero2, kNegZero2, kNegZero2);
+    constexpr int V = Elem<DT>::kPerVec;
+    const size_t nvec = (len + V - 1) / V;
+    const uint32_t nz = Elem<DT>::kNegZeroWord;
+    const uint4 pad = make_uint4(nz, nz, nz, nz);
     float acc = -0.0f;
     size_t v0 = first;
     if (ALIGNED) {
-        const size_t nfull = len / 8;               // whole vectors
+        const size_t nfull = len / V;               // whole vectors
         if (v0 + (size_t)(U - 1) * stride < nfull) {
-            const size_t step = 8 * stride;
-            const uint16_t *p = seg + 8 * v0;
+            const size_t step = V * stride;
+            const typename Elem<DT>::T *p = seg + V * v0;
             uint4 q[U];
 #pragma unroll
             for (int u = 0; u < U; u++) q[u] = ld_stream(p + (size_t)u * step);
             for (;;) {
                 float t[U];
 #pragma unroll
-                for (int u = 0; u < U; u++) t[u] = tree8<DT, OP>(q[u]);
+                for (int u = 0; u < U; u++) t[u] = vec_tree<DT, OP>(q[u]);
                 v0 += (size_t)U * stride;
                 p += (size_t)U * step;
                 const bool more = v0 + (size_t)(U - 1) * stride < nfull;
@@ -63,17 +66,17 @@ __device__ __forceinline__ float grid_stride_acc(const uint16_t *seg, size_t len
 #pragma unroll
     for (int u = 0; u < U; u++) {
         const size_t v = v0 + (size_t)u * stride;
-        q[u] = v < nvec ? ld_vec<ALIGNED>(seg, len, v, 0x8000u) : pad;
+        q[u] = v < nvec ? ld_vec<DT, ALIGNED, true>(seg, len, v) : pad;
     }
     for (; v0 < nvec; v0 += (size_t)U * stride) {
         float t[U];
 #pragma unroll
-        for (int u = 0; u < U; u++) t[u] = tree8<DT, OP>(q[u]);
+        for (int u = 0; u < U; u++) t[u] = vec_tree<DT, OP>(q[u]);
         const size_t n0 = v0 + (size_t)U * stride;
 #pragma unroll
         for (int u = 0; u < U; u++) {
             const size_t v = n0 + (size_t)u * stride;
-            q[u] = v < nvec ? ld_vec<ALIGNED>(seg, len, v, 0x8000u) : pad;
+            q[u] = v < nvec ? ld_vec<DT, ALIGNED, true>(seg, len, v) : pad;
         }
 #pragma unroll
         for (int u = 0; u < U; u++) acc = __fadd_rn(acc, t[u]);
@@ -83,14 +86,14 @@ __device__ __forceinline__ float grid_stride_acc(const uint16_t *seg, size_t len
 
 template <int DT, int OP, bool ALIGNED>
 __global__ void __launch_bounds__(1024)
-shuffle_block_kernel(const uint16_t *__restrict__ x, size_t seg_len, int G,
-                     float *__restrict__ dst)
+shuffle_block_kernel(const void *__restrict__ xv, size_t seg_len, int G, float *__restrict__ dst)
 {
+    using T = typename Elem<DT>::T;
     __shared__ float warp_val[32];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
     const size_t s = blockIdx.x / (unsigned)G;
     const size_t b = blockIdx.x - s * (unsigned)G;
-    const uint16_t *seg = x + s * seg_len;
+    const T *seg = static_cast<const T *>(xv) + s * seg_len;
     const size_t stride = (size_t)G * blockDim.x;
     float acc = grid_stride_acc<DT, OP, ALIGNED>(seg, seg_len, b * blockDim.x + threadIdx.x, stride);
     pdl_launch_dependents();
@@ -108,7 +111,7 @@ shuffle_block_kernel(const uint16_t *__restrict__ x, size_t seg_len, int G,
 // group order visits lane j's vectors j, j+32, j+64, ... in order.
 template <int DT, int OP, bool ALIGNED>
 __global__ void __launch_bounds__(kRowsBlock, kRowsMinCtas)
-shuffle_rows_warp_kernel(const uint16_t *__restrict__ x, size_t rows, size_t cols,
+shuffle_rows_warp_kernel(const void *__restrict__ x, size_t rows, size_t cols,
                          float *__restrict__ out)
 {
     rows_body<ShuffleReducer<DT, OP>, ALIGNED>(x, rows, cols, out);
@@ -116,55 +119,58 @@ shuffle_rows_warp_kernel(const uint16_t *__restrict__ x, size_t rows, size_t col
 
 // ---------------------------------------------------------------- host
 
-template <template <int, int, bool> class K, typename F>
-static F pick(int dtype, int op, bool aligned)
+template <int DT, int OP>
+static const void *pick_do(bool rows, bool aligned)
 {
-    if (dtype == kF16) {
-        if (op == kOpSquares) return aligned ? (F)K<kF16, kOpSquares, true>::fn : (F)K<kF16, kOpSquares, false>::fn;
-        return aligned ? (F)K<kF16, kOpSum, true>::fn : (F)K<kF16, kOpSum, false>::fn;
-    }
-    if (op == kOpSquares) return aligned ? (F)K<kBF16, kOpSquares, true>::fn : (F)K<kBF16, kOpSquares, false>::fn;
-    return aligned ? (F)K<kBF16, kOpSum, true>::fn : (F)K<kBF16, kOpSum, false>::fn;
+    if (rows) return aligned ? (const void *)shuffle_rows_warp_kernel<DT, OP, true>
+                             : (const void *)shuffle_rows_warp_kernel<DT, OP, false>;
+    return aligned ? (const void *)shuffle_block_kernel<DT, OP, true>
+                   : (const void *)shuffle_block_kernel<DT, OP, false>;
 }
 
-template <int DT, int OP, bool A>
-struct BlockK {
-    static constexpr auto fn = shuffle_block_kernel<DT, OP, A>;
-};
-template <int DT, int OP, bool A>
-struct RowsK {
-    static constexpr auto fn = shuffle_rows_warp_kernel<DT, OP, A>;
-};
+template <int DT>
+static const void *pick_d(bool rows, int op, bool aligned)
+{
+    return op == kOpSquares ? pick_do<DT, kOpSquares>(rows, aligned)
+                            : pick_do<DT, kOpSum>(rows, aligned);
+}
 
-using BlockFn = void (*)(const uint16_t *, size_t, int, float *);
-using RowsFn = void (*)(const uint16_t *, size_t, size_t, float *);
+static const void *pick(bool rows, int dtype, int op, bool aligned)
+{
+    switch (dtype) {
+    case kF16: return pick_d<kF16>(rows, op, aligned);
+    case kBF16: return pick_d<kBF16>(rows, op, aligned);
+    case kF32: return pick_d<kF32>(rows, op, aligned);
+    default: return nullptr;
+    }
+}
 
-cudaError_t launch_shuffle_block(int dtype, int op, bool aligned, const uint16_t *x, size_t seg_len,
+cudaError_t launch_shuffle_block(int dtype, int op, bool aligned, const void *x, size_t seg_len,
                                  size_t segments, int G, float *dst, int block,
                                  cudaStream_t stream)
 {
-    BlockFn k = pick<BlockK, BlockFn>(dtype, op, aligned);
-    k<<<(unsigned)(segments * (size_t)G), block, 0, stream>>>(x, seg_len, G, dst);
-    return cudaGetLastError();
+    const void *k = pick(false, dtype, op, aligned);
+    if (!k) return cudaErrorInvalidValue;
+    void *args[] = {(void *)&x, (void *)&seg_len, (void *)&G, (void *)&dst};
+    return cudaLaunchKernel(k, dim3((unsigned)(segments * (size_t)G)), dim3(block), args, 0,
+                            stream);
 }
 
-cudaError_t launch_shuffle_rows_warp(int dtype, int op, bool aligned, const uint16_t *x, size_t rows,
+cudaError_t launch_shuffle_rows_warp(int dtype, int op, bool aligned, const void *x, size_t rows,
                                      size_t cols, float *out, int grid, int block,
                                      cudaStream_t stream)
 {
-    RowsFn k = pick<RowsK, RowsFn>(dtype, op, aligned);
-    k<<<grid, block, 0, stream>>>(x, rows, cols, out);
-    return cudaGetLastError();
+    const void *k = pick(true, dtype, op, aligned);
+    if (!k) return cudaErrorInvalidValue;
+    void *args[] = {(void *)&x, (void *)&rows, (void *)&cols, (void *)&out};
+    return cudaLaunchKernel(k, dim3(grid), dim3(block), args, 0, stream);
 }
 
 int occupancy_shuffle(bool rows, int dtype, int op, bool aligned, int block)
 {
+    const void *k = pick(rows, dtype, op, aligned);
     int n = 0;
-    cudaError_t e = rows ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                               &n, pick<RowsK, RowsFn>(dtype, op, aligned), block, 0)
-                         : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                               &n, pick<BlockK, BlockFn>(dtype, op, aligned), block, 0);
-    if (e != cudaSuccess) {
+    if (!k || cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, block, 0) != cudaSuccess) {
         (void)cudaGetLastError();
         return 0;
     }

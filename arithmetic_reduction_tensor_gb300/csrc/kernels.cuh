@@ -1,8 +1,9 @@
 // kernels.cuh -- launchers of the reduction kernels (host side).
 //
 // Every launcher enqueues one kernel on `stream` and returns the launch
-// status (cudaGetLastError).  Sizes are in inputs (16-bit elements).  `op`
-// is kOpSum (the sum of the inputs) or kOpSquares (the sum of their squares).
+// status.  Sizes are in inputs; x points to 16-bit patterns (dtype kF16,
+// kBF16) or binary32 values (kF32).  `op` is kOpSum (the sum of the inputs)
+// or kOpSquares (the sum of their squares).
 #pragma once
 
 #include <cstddef>
@@ -17,31 +18,31 @@ namespace tcr {
 // Chunked: CTA work unit u = (segment u / cps, chunk u % cps); the chunk of
 // 2^chunk_log2 inputs is split evenly over the CTA's warps; dst[u] is the
 // chunk's aligned subtree.
-cudaError_t launch_fixed_chunk(int dtype, int op, bool aligned, const uint16_t *x, size_t seg_len,
+cudaError_t launch_fixed_chunk(int dtype, int op, bool aligned, const void *x, size_t seg_len,
                                size_t units, size_t cps, int chunk_log2, float *dst, int grid,
                                int block, cudaStream_t stream);
-// One warp per row, rows <= kRowsWarpMaxCols inputs long: out[r] = row tree.
-cudaError_t launch_fixed_rows_warp(int dtype, int op, bool aligned, const uint16_t *x, size_t rows,
+// One warp per row, rows <= kRowsWarpMaxBytes long: out[r] = row tree.
+cudaError_t launch_fixed_rows_warp(int dtype, int op, bool aligned, const void *x, size_t rows,
                                    size_t cols, float *out, int grid, int block,
                                    cudaStream_t stream);
 
 // ---- SHUFFLE_TREE (declared grid-stride order)
 // Block team: grid = segments * G CTAs of Bt threads; CTA (s, b) writes its
 // block value to dst[s * G + b].
-cudaError_t launch_shuffle_block(int dtype, int op, bool aligned, const uint16_t *x, size_t seg_len,
+cudaError_t launch_shuffle_block(int dtype, int op, bool aligned, const void *x, size_t seg_len,
                                  size_t segments, int G, float *dst, int block,
                                  cudaStream_t stream);
 // Warp team (Bt = 32, G = 1): one warp per row, out[r] = warp value.
-cudaError_t launch_shuffle_rows_warp(int dtype, int op, bool aligned, const uint16_t *x, size_t rows,
+cudaError_t launch_shuffle_rows_warp(int dtype, int op, bool aligned, const void *x, size_t rows,
                                      size_t cols, float *out, int grid, int block,
                                      cudaStream_t stream);
 
 // ---- MMA_CHAIN (tensor-core chains of R MMAs against a ones matrix)
-cudaError_t launch_mma_chunk(int dtype, int op, bool aligned, int R, const uint16_t *x, size_t seg_len,
+cudaError_t launch_mma_chunk(int dtype, int op, bool aligned, int R, const void *x, size_t seg_len,
                              size_t units, size_t cps, int chunk_log2, float *dst, int grid,
                              int block, cudaStream_t stream);
-// One warp per row, rows <= kRowsWarpMaxCols inputs long.
-cudaError_t launch_mma_rows(int dtype, int op, bool aligned, int R, const uint16_t *x, size_t rows,
+// One warp per row, rows <= kRowsWarpMaxBytes long.
+cudaError_t launch_mma_rows(int dtype, int op, bool aligned, int R, const void *x, size_t rows,
                             size_t cols, float *out, int grid, int block, cudaStream_t stream);
 
 // ---- MMA_CHAIN on tcgen05 (bulk copies into shared memory, D in TMEM):

@@ -1,16 +1,19 @@
 // stream.cuh -- the warp stream shared by the chunked and per-row kernels.
 //
-// A warp walks its inputs in groups of 2048 (8 warp loads of 256): lane j
-// of warp load k of a group holds vector 32*k + j of the group, so each
-// load instruction is one coalesced 512-byte transaction.  The loop is
-// software-pipelined: the 8 loads of the next group (of the same span, or
-// of the warp's next work unit) are issued before the current group's
-// dependent arithmetic runs, so a warp keeps 4 KiB of loads in flight
-// while it shuffles.  A reducer policy turns groups into the mode's result:
+// A warp walks its inputs in groups of 8 warp loads of 32 vectors (4 KiB:
+// 2048 16-bit inputs, 1024 binary32 inputs): lane j of warp load k of a
+// group holds vector 32*k + j of the group, so each load instruction is one
+// coalesced 512-byte transaction.  The loop is software-pipelined: the 8
+// loads of the next group (of the same span, or of the warp's next work
+// unit) are issued before the current group's dependent arithmetic runs,
+// so a warp keeps 4 KiB of loads in flight while it shuffles.  A reducer policy turns groups into the mode's result:
 //
 //   FixedReducer    balanced tree over index order (FIXED_ORDER)
 //   ShuffleReducer  grid-stride accumulation of one warp team (SHUFFLE_TREE)
 //   MmaReducer      tensor-core chains of R MMAs against ones (MMA_CHAIN)
+//   MmaSqReducer    tensor-core A * A^T diagonals (MMA_CHAIN, squares)
+//   MmaSplitReducer binary32 inputs split exactly into three bfloat16
+//                   parts, then chains against ones (MMA_CHAIN)
 //
 // Each policy splits a group into take() -- which consumes the 8 loaded
 // vectors into registers -- and reduce(), the dependent part that runs while
@@ -23,32 +26,36 @@
 namespace tcr {
 
 // The 8 vectors of the group starting at input gbase of a segment of len
-// inputs; inputs past len read as the 16-bit pattern FILL.
-template <bool ALIGNED, uint16_t FILL>
-__device__ __forceinline__ void load_group(uint4 (&q)[8], const uint16_t *seg, size_t len,
-                                           size_t gbase, int lane)
+// inputs; inputs past len read as -0.0 (NEGZERO) or zero bits.
+template <int DT, bool ALIGNED, bool NEGZERO>
+__device__ __forceinline__ void load_group(uint4 (&q)[8], const typename Elem<DT>::T *seg,
+                                           size_t len, size_t gbase, int lane)
 {
-    if (ALIGNED && gbase + kGroup <= len) {
+    constexpr int V = Elem<DT>::kPerVec;
+    if (ALIGNED && gbase + group_len<DT>() <= len) {
 #pragma unroll
-        for (int k = 0; k < 8; k++) q[k] = ld_stream(seg + gbase + 256 * k + 8 * lane);
+        for (int k = 0; k < 8; k++) q[k] = ld_stream(seg + gbase + 32 * V * k + V * lane);
     } else {
-        const uint32_t f2 = (uint32_t)FILL * 0x10001u;
+        const uint32_t f = fill_word<DT, NEGZERO>();
 #pragma unroll
         for (int k = 0; k < 8; k++) {
-            const size_t vec = gbase / 8 + 32 * (size_t)k + (size_t)lane;
-            q[k] = 8 * vec < len ? ld_vec<ALIGNED>(seg, len, vec, FILL) : make_uint4(f2, f2, f2, f2);
+            const size_t vec = gbase / V + 32 * (size_t)k + (size_t)lane;
+            q[k] = V * vec < len ? ld_vec<DT, ALIGNED, NEGZERO>(seg, len, vec)
+                                 : make_uint4(f, f, f, f);
         }
     }
 }
 
 // ---------------------------------------------------------------- trees
 
-// t[k]: the lane's 8-input subtree of warp load k (k = 0..7) of a group.
-// Returns the aligned subtree of the whole group (2048 inputs) in every
-// lane.  Levels 4..6 are a reduce-scatter butterfly that halves the values
-// each lane carries (12 shuffles per group instead of 43).  Additions are
-// commutative bit for bit, so which lane of a pair forms a node does not
-// matter; which two children it adds is fixed.
+// t[k]: the lane's vector subtree of warp load k (k = 0..7) of a group.
+// Returns the aligned subtree of the whole group (256 vectors) in every
+// lane.  The first three levels above the vectors are a reduce-scatter
+// butterfly that halves the values each lane carries (12 shuffles per
+// group instead of 43).  Level names below count 16-bit inputs (a binary32
+// vector holds 4 inputs, so every span there is half as long).  Additions
+// are commutative bit for bit, so which lane of a pair forms a node does
+// not matter; which two children it adds is fixed.
 __device__ __forceinline__ float group_tree(const float (&t)[8], int lane)
 {
     const bool b0 = lane & 1, b1 = lane & 2, b2 = lane & 4;
@@ -93,33 +100,35 @@ __device__ __forceinline__ float group_tree(const float (&t)[8], int lane)
 // too, since every leaf is then at least +0.0.
 template <int DT, int OP, int LEVELS>
 struct FixedReducer {
-    static constexpr uint16_t kFill = 0x8000;    // -0.0
+    static constexpr int kDT = DT;
+    static constexpr bool kNegZeroPad = true;
     TreeCounter<LEVELS> tc;
     float t[8];
 
     __device__ __forceinline__ void take(const uint4 (&q)[8])
     {
 #pragma unroll
-        for (int k = 0; k < 8; k++) t[k] = tree8<DT, OP>(q[k]);
+        for (int k = 0; k < 8; k++) t[k] = vec_tree<DT, OP>(q[k]);
     }
     __device__ __forceinline__ void reduce(int lane) { tc.push(group_tree(t, lane)); }
     __device__ __forceinline__ float value(int) const { return tc.finish(); }
 };
 
-// SHUFFLE_TREE, one-warp team: lane j adds the 8-input trees of vectors
+// SHUFFLE_TREE, one-warp team: lane j adds the vector trees of vectors
 // j, j+32, j+64, ... in that order (group after group, load k after load
 // k-1), starting from -0.0; the warp value is the butterfly with offsets
 // 16, 8, 4, 2, 1.  Vectors past the segment are -0.0, the identity.
 template <int DT, int OP>
 struct ShuffleReducer {
-    static constexpr uint16_t kFill = 0x8000;
+    static constexpr int kDT = DT;
+    static constexpr bool kNegZeroPad = true;
     float acc = -0.0f;
     float t[8];
 
     __device__ __forceinline__ void take(const uint4 (&q)[8])
     {
 #pragma unroll
-        for (int k = 0; k < 8; k++) t[k] = tree8<DT, OP>(q[k]);
+        for (int k = 0; k < 8; k++) t[k] = vec_tree<DT, OP>(q[k]);
     }
     __device__ __forceinline__ void reduce(int)
     {
@@ -144,7 +153,8 @@ struct ShuffleReducer {
 // equal lane%4 hold the same column: offsets 4, 8, 16).
 template <int DT, int R>
 struct MmaReducer {
-    static constexpr uint16_t kFill = 0x0000;
+    static constexpr int kDT = DT;
+    static constexpr bool kNegZeroPad = false;
     float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
     float acc_lo = 0.f, acc_hi = 0.f;
     int cnt = 0;
@@ -187,7 +197,8 @@ struct MmaReducer {
 // the sum over all lanes (eight of them hold values).
 template <int DT, int R>
 struct MmaSqReducer {
-    static constexpr uint16_t kFill = 0x0000;
+    static constexpr int kDT = DT;
+    static constexpr bool kNegZeroPad = false;
     float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;    // A * (rows 0..7)^T
     float q0 = 0.f, q1 = 0.f, q2 = 0.f, q3 = 0.f;    // A * (rows 8..15)^T
     float acc = 0.f;
@@ -220,6 +231,84 @@ struct MmaSqReducer {
     }
 };
 
+// MMA_CHAIN for binary32 inputs.  Every binary32 x is split exactly into
+// three bfloat16 parts, x = hi + mid + lo: hi is x rounded toward zero to
+// bfloat16 (its top 8 significant bits), r = x - hi is exact (the low 16
+// bits of the significand), mid is r's top 8 significant bits and
+// lo = r - mid holds at most 8, so lo is a bfloat16 too.  The split is
+// exact whenever lo is a normal number or zero; below 2^-126 lo loses the
+// bits under 2^-133, less than 2^-133 per input.  A non-finite x has its
+// whole value in hi (cvt keeps infinities and NaNs) and a zero residual.
+// Per two warp loads (256 inputs) three m16n8k16 MMAs against ones run:
+// the hi parts of both loads as one A tile into D_hi, and each load's mid
+// and lo parts (128 + 128 bfloat16) as one A tile into D_ml.  Chains of R
+// tiles (R MMAs into D_hi, 2R into D_ml) flush into the lane's fp32
+// accumulators as MmaReducer does.  For sums of squares the leaf
+// fl32(x * x) is split instead of x.
+template <int OP>
+__device__ __forceinline__ void split_bf16x3(uint32_t ua, uint32_t ub, uint32_t &hi,
+                                             uint32_t &mid, uint32_t &lo)
+{
+    const float a = leaf32<OP>(ua), b = leaf32<OP>(ub);
+    // packed {a in the low half, b in the high half}, rounded toward zero
+    asm("cvt.rz.bf16x2.f32 %0, %1, %2;" : "=r"(hi) : "f"(b), "f"(a));
+    float ra = __fsub_rn(a, __uint_as_float(__float_as_uint(a) & 0xffff0000u));
+    float rb = __fsub_rn(b, __uint_as_float(__float_as_uint(b) & 0xffff0000u));
+    // a NaN residual comes only from a non-finite leaf: drop it (min and max
+    // return the non-NaN operand), leaving the leaf's value to hi
+    ra = fminf(fmaxf(ra, 0.0f), ra);
+    rb = fminf(fmaxf(rb, 0.0f), rb);
+    const uint32_t ma = __float_as_uint(ra) & 0xffff0000u, mb = __float_as_uint(rb) & 0xffff0000u;
+    mid = __byte_perm(ma, mb, 0x7632);
+    const float la = __fsub_rn(ra, __uint_as_float(ma)), lb = __fsub_rn(rb, __uint_as_float(mb));
+    lo = __byte_perm(__float_as_uint(la), __float_as_uint(lb), 0x7632);
+}
+
+template <int R, int OP>
+struct MmaSplitReducer {
+    static constexpr int kDT = kF32;
+    static constexpr bool kNegZeroPad = false;
+    float h0 = 0.f, h1 = 0.f, h2 = 0.f, h3 = 0.f;    // D_hi
+    float m0 = 0.f, m1 = 0.f, m2 = 0.f, m3 = 0.f;    // D_ml
+    float acc_lo = 0.f, acc_hi = 0.f;
+    int cnt = 0;
+
+    __device__ __forceinline__ void flush()
+    {
+        acc_lo = __fadd_rn(acc_lo, h0);
+        acc_hi = __fadd_rn(acc_hi, h2);
+        acc_lo = __fadd_rn(acc_lo, m0);
+        acc_hi = __fadd_rn(acc_hi, m2);
+        h0 = h1 = h2 = h3 = m0 = m1 = m2 = m3 = 0.f;
+        cnt = 0;
+    }
+    __device__ __forceinline__ void take(const uint4 (&q)[8])
+    {
+#pragma unroll
+        for (int k = 0; k < 8; k += 2) {
+            uint32_t ha0, ma0, la0, ha1, ma1, la1, hb0, mb0, lb0, hb1, mb1, lb1;
+            split_bf16x3<OP>(q[k].x, q[k].y, ha0, ma0, la0);
+            split_bf16x3<OP>(q[k].z, q[k].w, ha1, ma1, la1);
+            split_bf16x3<OP>(q[k + 1].x, q[k + 1].y, hb0, mb0, lb0);
+            split_bf16x3<OP>(q[k + 1].z, q[k + 1].w, hb1, mb1, lb1);
+            mma_ones<kBF16>(h0, h1, h2, h3, ha0, ha1, hb0, hb1);
+            mma_ones<kBF16>(m0, m1, m2, m3, ma0, ma1, la0, la1);
+            mma_ones<kBF16>(m0, m1, m2, m3, mb0, mb1, lb0, lb1);
+            if (++cnt == R) flush();
+        }
+    }
+    __device__ __forceinline__ void reduce(int) {}
+    __device__ __forceinline__ float value(int)
+    {
+        if (cnt) flush();
+        float a = __fadd_rn(acc_lo, acc_hi);
+        a = __fadd_rn(a, __shfl_xor_sync(kFull, a, 4));
+        a = __fadd_rn(a, __shfl_xor_sync(kFull, a, 8));
+        a = __fadd_rn(a, __shfl_xor_sync(kFull, a, 16));
+        return a;
+    }
+};
+
 // ---------------------------------------------------------------- kernels
 
 // Chunked: CTA work unit u = (segment u / cps, chunk u % cps); the chunk of
@@ -227,27 +316,32 @@ struct MmaSqReducer {
 // the balanced tree over the CTA's warp values (warp order, -0.0 pad).
 // Persistent: CTA b takes units b, b + grid, b + 2*grid, ...
 template <class Red, bool ALIGNED>
-__device__ __forceinline__ void chunk_body(const uint16_t *__restrict__ x, size_t seg_len,
+__device__ __forceinline__ void chunk_body(const void *__restrict__ xv, size_t seg_len,
                                            size_t units, size_t cps, int chunk_log2,
                                            float *__restrict__ dst)
 {
+    constexpr int DT = Red::kDT;
+    constexpr bool NZ = Red::kNegZeroPad;
+    using T = typename Elem<DT>::T;
+    const T *__restrict__ x = static_cast<const T *>(xv);
     __shared__ float warp_val[32];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-    // every warp span is 2^kWarpSpanLog2 inputs (chunk_log2 = kWarpSpanLog2
-    // + log2 warps), so the groups per span are a compile-time constant
-    constexpr size_t span = (size_t)1 << kWarpSpanLog2;
-    constexpr int ngroups = (int)(span / kGroup);
+    // every warp span is 2^kWarpSpanBytesLog2 bytes (chunk_log2 = log2 of
+    // the span's inputs + log2 warps), so the groups per span are a
+    // compile-time constant
+    constexpr size_t span = span_len<DT>();
+    constexpr int ngroups = (int)(span / group_len<DT>());
     size_t u = blockIdx.x;
     if (u < units) {
         size_t s = u / cps;
-        const uint16_t *seg = x + s * seg_len;
+        const T *seg = x + s * seg_len;
         size_t base = ((u - s * cps) << chunk_log2) + (size_t)warp * span;
         uint4 q[8];
-        load_group<ALIGNED, Red::kFill>(q, seg, seg_len, base, lane);
+        load_group<DT, ALIGNED, NZ>(q, seg, seg_len, base, lane);
         for (;;) {
             const size_t nu = u + gridDim.x;
             const bool has_next = nu < units;
-            const uint16_t *nseg = seg;
+            const T *nseg = seg;
             size_t nbase = 0;
             if (has_next) {
                 const size_t ns = nu / cps;
@@ -261,10 +355,10 @@ __device__ __forceinline__ void chunk_body(const uint16_t *__restrict__ x, size_
             for (int g = 0; g < ngroups; g++) {
                 red.take(q);
                 if (g + 1 < ngroups)
-                    load_group<ALIGNED, Red::kFill>(q, seg, seg_len, base + (size_t)(g + 1) * kGroup,
-                                                    lane);
+                    load_group<DT, ALIGNED, NZ>(q, seg, seg_len,
+                                                base + (size_t)(g + 1) * group_len<DT>(), lane);
                 else if (has_next)
-                    load_group<ALIGNED, Red::kFill>(q, nseg, seg_len, nbase, lane);
+                    load_group<DT, ALIGNED, NZ>(q, nseg, seg_len, nbase, lane);
                 red.reduce(lane);
             }
             const float v = red.value(lane);
@@ -287,16 +381,21 @@ __device__ __forceinline__ void chunk_body(const uint16_t *__restrict__ x, size_
 // One warp per row (rows of at most 2^LEVELS groups): out[r] is the row's
 // value.  Persistent: warp w takes rows w, w + warps, w + 2*warps, ...
 template <class Red, bool ALIGNED>
-__device__ __forceinline__ void rows_body(const uint16_t *__restrict__ x, size_t rows,
+__device__ __forceinline__ void rows_body(const void *__restrict__ xv, size_t rows,
                                           size_t cols, float *__restrict__ out)
 {
+    constexpr int DT = Red::kDT;
+    constexpr bool NZ = Red::kNegZeroPad;
+    using T = typename Elem<DT>::T;
+    const T *__restrict__ x = static_cast<const T *>(xv);
     const int lane = threadIdx.x & 31;
     const size_t nw = ((size_t)gridDim.x * blockDim.x) >> 5;
     size_t r = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const size_t ngroups = (cols + kGroup - 1) / kGroup;
+    constexpr size_t G = group_len<DT>();
+    const size_t ngroups = (cols + G - 1) / G;
     if (r < rows && ngroups > 0) {
         uint4 q[8];
-        load_group<ALIGNED, Red::kFill>(q, x + r * cols, cols, 0, lane);
+        load_group<DT, ALIGNED, NZ>(q, x + r * cols, cols, 0, lane);
         for (;;) {
             const size_t nr = r + nw;
             const bool has_next = nr < rows;
@@ -305,9 +404,9 @@ __device__ __forceinline__ void rows_body(const uint16_t *__restrict__ x, size_t
             for (size_t g = 0; g < ngroups; g++) {
                 red.take(q);
                 if (g + 1 < ngroups)
-                    load_group<ALIGNED, Red::kFill>(q, x + r * cols, cols, (g + 1) * kGroup, lane);
+                    load_group<DT, ALIGNED, NZ>(q, x + r * cols, cols, (g + 1) * G, lane);
                 else if (has_next)
-                    load_group<ALIGNED, Red::kFill>(q, x + nr * cols, cols, 0, lane);
+                    load_group<DT, ALIGNED, NZ>(q, x + nr * cols, cols, 0, lane);
                 red.reduce(lane);
             }
             const float v = red.value(lane);

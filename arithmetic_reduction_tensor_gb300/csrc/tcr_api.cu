@@ -165,18 +165,31 @@ int default_R(int)
     return 4;
 }
 
-// The declared SHUFFLE_TREE team for a segment of L inputs at block size B:
-// one warp for short segments, else G blocks of B threads with about 16
-// vectors per thread, at most 152 * 1024 threads in the team.
-void shuffle_team(size_t L, int B, int *Bt, int *G)
+size_t elem_bytes(int dtype)
 {
-    if (L <= 8192) {
+    return dtype == TCR_F32 ? 4 : 2;
+}
+
+// Inputs per 16-byte vector: 8 of 16 bits, 4 of binary32.
+int vector_len(int dtype)
+{
+    return (int)(16 / elem_bytes(dtype));
+}
+
+// The declared SHUFFLE_TREE team for a segment of L inputs, in vectors of
+// V inputs, at block size B: one warp for segments of at most 1024
+// vectors, else G blocks of B threads with about 16 vectors per thread, at
+// most 152 * 1024 threads in the team.
+void shuffle_team(size_t L, int V, int B, int *Bt, int *G)
+{
+    const size_t nvec = (L + (size_t)V - 1) / (size_t)V;
+    if (nvec <= 1024) {
         *Bt = 32;
         *G = 1;
         return;
     }
-    const size_t per_block = (size_t)8 * (size_t)B * 16;
-    size_t g = (L + per_block - 1) / per_block;
+    const size_t per_block = (size_t)B * 16;
+    size_t g = (nvec + per_block - 1) / per_block;
     const size_t gmax = (size_t)kRuleSMs * 1024 / (size_t)B;
     if (g > gmax) g = gmax;
     if (g < 1) g = 1;
@@ -187,7 +200,7 @@ void shuffle_team(size_t L, int B, int *Bt, int *G)
 tcr_status check_mode(const tcr_mode &m, int *block, int *R)
 {
     if (m.kind < TCR_MMA_CHAIN || m.kind > TCR_MMA_CHAIN_TMEM) return TCR_ERR_INVALID_ARG;
-    if (m.dtype != TCR_F16 && m.dtype != TCR_BF16) return TCR_ERR_INVALID_ARG;
+    if (m.dtype != TCR_F16 && m.dtype != TCR_BF16 && m.dtype != TCR_F32) return TCR_ERR_INVALID_ARG;
     int b = m.block_threads == 0 ? kDefaultBlock : m.block_threads;
     if (b < 32 || b > 1024 || (b & (b - 1)) != 0) return TCR_ERR_INVALID_ARG;
     int r = 0;
@@ -202,9 +215,10 @@ tcr_status check_mode(const tcr_mode &m, int *block, int *R)
 
 void plan_chunked(Plan &p, int dev, Family fam)
 {
-    // each warp of a CTA covers 2^13 inputs of the CTA's chunk
+    // each warp of a CTA covers 2^kWarpSpanBytesLog2 bytes of the CTA's chunk
     p.path = kPathChunk;
-    p.chunk_log2 = kWarpSpanLog2 + log2_exact(p.block / 32);
+    p.chunk_log2 = kWarpSpanBytesLog2 - log2_exact((int)elem_bytes(p.dtype)) +
+                   log2_exact(p.block / 32);
     p.cps = (p.seg_len + ((size_t)1 << p.chunk_log2) - 1) >> p.chunk_log2;
     p.units = p.segments * p.cps;
     const size_t resident = (size_t)sm_count(dev) *
@@ -222,9 +236,10 @@ Plan make_plan(size_t segments, size_t seg_len, bool rows_call, const tcr_mode &
     Plan p;
     std::memset(&p, 0, sizeof p);
     p.kind = m.kind;
-    // the tcgen05 kernels reduce plain sums; sums of squares of that kind run
-    // the mma.sync contraction (MmaSqReducer)
-    if (p.kind == TCR_MMA_CHAIN_TMEM && op != kOpSum) p.kind = TCR_MMA_CHAIN;
+    // the tcgen05 kernels reduce plain sums of 16-bit inputs; sums of
+    // squares of that kind run the mma.sync contraction (MmaSqReducer), and
+    // binary32 inputs the mma.sync three-way split (MmaSplitReducer)
+    if (p.kind == TCR_MMA_CHAIN_TMEM && (op != kOpSum || m.dtype == TCR_F32)) p.kind = TCR_MMA_CHAIN;
     p.dtype = m.dtype;
     p.op = op;
     p.R = R;
@@ -238,7 +253,7 @@ Plan make_plan(size_t segments, size_t seg_len, bool rows_call, const tcr_mode &
     }
     const size_t sms = (size_t)sm_count(dev);
     if (m.kind == TCR_SHUFFLE_TREE) {
-        shuffle_team(seg_len, block, &p.team_threads, &p.team_blocks);
+        shuffle_team(seg_len, vector_len(p.dtype), block, &p.team_threads, &p.team_blocks);
         if (p.team_threads == 32 && p.team_blocks == 1) {
             // a team of one warp: pack one segment per warp, 8 per CTA
             p.path = kPathShuffleRowsWarp;
@@ -285,7 +300,7 @@ Plan make_plan(size_t segments, size_t seg_len, bool rows_call, const tcr_mode &
         return p;
     }
     const Family fam = m.kind == TCR_FIXED_ORDER ? kFixedF : kMmaF;
-    if (rows_call && seg_len <= kRowsWarpMaxCols) {
+    if (rows_call && seg_len <= kRowsWarpMaxBytes / elem_bytes(p.dtype)) {
         // one warp per row: the CTA size is a launch detail (the result does
         // not depend on it), fixed at kRowsBlock threads
         p.block = block = kRowsBlock;
@@ -308,7 +323,7 @@ bool fault_injected(const char *what)
     return e && std::strcmp(e, what) == 0;
 }
 
-tcr_status run_plan(const Plan &p, const uint16_t *x, float *out, cudaStream_t s, int dev)
+tcr_status run_plan(const Plan &p, const void *x, float *out, cudaStream_t s, int dev)
 {
     if (p.path == kPathEmpty) {
         if (fault_injected("launch")) return TCR_ERR_CUDA;
@@ -332,11 +347,12 @@ tcr_status run_plan(const Plan &p, const uint16_t *x, float *out, cudaStream_t s
     cudaError_t e = cudaSuccess;
     switch (p.path) {
     case kPathTmem:
-        e = launch_mma_tmem(p.dtype, p.R, x, p.seg_len, dst, p.grid, fault_injected("stall"), s);
+        e = launch_mma_tmem(p.dtype, p.R, (const uint16_t *)x, p.seg_len, dst, p.grid,
+                            fault_injected("stall"), s);
         break;
     case kPathTmemRows:
-        e = launch_mma_tmem_rows(p.dtype, p.R, x, p.segments, p.seg_len, dst, p.grid,
-                                 fault_injected("stall"), s);
+        e = launch_mma_tmem_rows(p.dtype, p.R, (const uint16_t *)x, p.segments, p.seg_len, dst,
+                                 p.grid, fault_injected("stall"), s);
         break;
     case kPathChunk:
         e = p.kind == TCR_FIXED_ORDER
@@ -379,8 +395,12 @@ tcr_status check_common(const void *x, size_t total, const float *out, const tcr
 {
     if (!out || ((uintptr_t)out & 3u) != 0) return TCR_ERR_INVALID_ARG;
     if (total >= kMaxInputs) return TCR_ERR_INVALID_ARG;
-    if (total > 0 && (!x || ((uintptr_t)x & 1u) != 0)) return TCR_ERR_INVALID_ARG;
-    return check_mode(mode, block, R);
+    tcr_status st = check_mode(mode, block, R);
+    if (st != TCR_OK) return st;
+    // x is aligned to its pattern type: 2 bytes, or 4 for binary32
+    if (total > 0 && (!x || ((uintptr_t)x & (elem_bytes(mode.dtype) - 1)) != 0))
+        return TCR_ERR_INVALID_ARG;
+    return TCR_OK;
 }
 
 bool mul_overflows(size_t a, size_t b)
@@ -398,7 +418,7 @@ tcr_status reduce_sum_op(const void *x, size_t n, float *out, const tcr_mode &mo
     if (dev < 0) return TCR_ERR_CUDA;
     const bool aligned = ((uintptr_t)x & 15u) == 0;
     Plan p = make_plan(1, n, false, mode, op, block, R, aligned, dev);
-    return run_plan(p, (const uint16_t *)x, out, (cudaStream_t)stream, dev);
+    return run_plan(p, x, out, (cudaStream_t)stream, dev);
 }
 
 tcr_status reduce_rows_op(const void *x, size_t rows, size_t cols, float *out,
@@ -414,9 +434,10 @@ tcr_status reduce_rows_op(const void *x, size_t rows, size_t cols, float *out,
     if (st != TCR_OK) return st;
     const int dev = current_device();
     if (dev < 0) return TCR_ERR_CUDA;
-    const bool aligned = ((uintptr_t)x & 15u) == 0 && (cols % 8) == 0;
+    // every row starts 16-byte aligned when x does and a row is whole vectors
+    const bool aligned = ((uintptr_t)x & 15u) == 0 && (cols % (size_t)vector_len(mode.dtype)) == 0;
     Plan p = make_plan(rows, cols, true, mode, op, block, R, aligned, dev);
-    return run_plan(p, (const uint16_t *)x, out, (cudaStream_t)stream, dev);
+    return run_plan(p, x, out, (cudaStream_t)stream, dev);
 }
 
 }  // namespace
@@ -467,11 +488,12 @@ tcr_status tcr_order_descriptor(size_t n, size_t rows, size_t cols, tcr_mode mod
                                                  : TCR_ORDER_TENSOR_CORE;
     desc->segment_len = seg_len;
     desc->segments = segments;
-    desc->vector_len = 8;
+    desc->vector_len = vector_len(mode.dtype);
+    desc->dtype = mode.dtype;
     desc->chain_R = (mode.kind == TCR_MMA_CHAIN || mode.kind == TCR_MMA_CHAIN_TMEM) ? R : 0;
     desc->pad_negative_zero = 1;
     if (mode.kind == TCR_SHUFFLE_TREE) {
-        shuffle_team(seg_len, block, &desc->team_threads, &desc->team_blocks);
+        shuffle_team(seg_len, desc->vector_len, block, &desc->team_threads, &desc->team_blocks);
     }
     desc->launch_grid = p.grid;
     desc->launch_block = p.path == kPathShuffleBlock ? p.team_threads : p.block;
@@ -486,14 +508,15 @@ tcr_status tcr_order_equivalent(const tcr_order_desc *a, const tcr_order_desc *b
 {
     if (!a || !b || !equivalent) return TCR_ERR_INVALID_ARG;
     *equivalent = 0;
-    if (a->kind != b->kind || a->order != b->order || a->segment_len != b->segment_len)
+    if (a->kind != b->kind || a->order != b->order || a->segment_len != b->segment_len ||
+        a->dtype != b->dtype || a->vector_len != b->vector_len || a->vector_len <= 0)
         return TCR_OK;
     switch (a->order) {
     case TCR_ORDER_BALANCED_TREE:
         *equivalent = 1;
         break;
     case TCR_ORDER_GRID_STRIDE: {
-        const size_t nvec = (a->segment_len + 7) / 8;
+        const size_t nvec = (a->segment_len + (size_t)a->vector_len - 1) / (size_t)a->vector_len;
         const size_t ta = (size_t)a->team_threads * (size_t)a->team_blocks;
         const size_t tb = (size_t)b->team_threads * (size_t)b->team_blocks;
         // one vector per thread at most: lane values are the vector trees,

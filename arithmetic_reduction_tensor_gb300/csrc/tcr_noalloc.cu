@@ -88,8 +88,10 @@ extern "C" tcr_status tcr_reduce_sum_noalloc(const void *x, size_t n, float *out
 {
     if (!out || ((uintptr_t)out & 3u) != 0) return TCR_ERR_INVALID_ARG;
     if (n >= ((size_t)1 << 40)) return TCR_ERR_INVALID_ARG;
-    if (n > 0 && (!x || ((uintptr_t)x & 1u) != 0)) return TCR_ERR_INVALID_ARG;
-    if (mode.dtype != TCR_F16 && mode.dtype != TCR_BF16) return TCR_ERR_INVALID_ARG;
+    if (mode.dtype != TCR_F16 && mode.dtype != TCR_BF16 && mode.dtype != TCR_F32)
+        return TCR_ERR_INVALID_ARG;
+    const int elem_log2 = mode.dtype == TCR_F32 ? 2 : 1;
+    if (n > 0 && (!x || ((uintptr_t)x & ((1u << elem_log2) - 1u)) != 0)) return TCR_ERR_INVALID_ARG;
     const int block = mode.block_threads == 0 ? 256 : mode.block_threads;
     if (block < 32 || block > 1024 || (block & (block - 1)) != 0) return TCR_ERR_INVALID_ARG;
     int R = 0;
@@ -102,10 +104,10 @@ extern "C" tcr_status tcr_reduce_sum_noalloc(const void *x, size_t n, float *out
         return TCR_ERR_INVALID_ARG;
     }
 
-    // chunk of 2^13 inputs per warp, as in the allocating entry point
+    // 2^kWarpSpanBytesLog2 bytes per warp, as in the allocating entry point
     int warps_log2 = 0;
     while ((32 << warps_log2) < block) warps_log2++;
-    const int chunk_log2 = kWarpSpanLog2 + warps_log2;
+    const int chunk_log2 = kWarpSpanBytesLog2 - elem_log2 + warps_log2;
     const size_t cps = (n + ((size_t)1 << chunk_log2) - 1) >> chunk_log2;
     if (cps > kNoAllocMaxPartials) return TCR_ERR_UNSUPPORTED;
 
@@ -128,11 +130,10 @@ extern "C" tcr_status tcr_reduce_sum_noalloc(const void *x, size_t n, float *out
     const size_t resident = (size_t)d.sms * (size_t)occ;
     const int grid = (int)(cps < resident ? cps : resident);
     float *dst = cps > 1 ? d.partials : out;
-    const uint16_t *xs = (const uint16_t *)x;
     cudaError_t e = mode.kind == TCR_FIXED_ORDER
-                        ? launch_fixed_chunk(mode.dtype, kOpSum, aligned, xs, n, cps, cps,
+                        ? launch_fixed_chunk(mode.dtype, kOpSum, aligned, x, n, cps, cps,
                                              chunk_log2, dst, grid, block, s)
-                        : launch_mma_chunk(mode.dtype, kOpSum, aligned, R, xs, n, cps, cps,
+                        : launch_mma_chunk(mode.dtype, kOpSum, aligned, R, x, n, cps, cps,
                                            chunk_log2, dst, grid, block, s);
     if (e == cudaSuccess && cps > 1) e = launch_combine(d.partials, 1, cps, out, s);
     return e == cudaSuccess ? TCR_OK : TCR_ERR_CUDA;

@@ -3,9 +3,9 @@
  *
  * The operation is the one stated by "GPU Tensor Cores for fast Arithmetic
  * Reductions" (arXiv 2001.05585), Abstract: the arithmetic reduction (sum)
- * of n numbers into one 32-bit floating-point result.  Inputs are binary16
- * or bfloat16; every result is binary32.  Three ways of computing it are
- * offered (tcr_kind):
+ * of n numbers into one 32-bit floating-point result.  Inputs are binary16,
+ * bfloat16 or binary32; every result is binary32.  Four ways of computing
+ * it are offered (tcr_kind):
  *
  *   TCR_MMA_CHAIN     the page's method: the inputs are laid out as 16x16
  *                     tiles and multiplied by an all-ones matrix on the tensor
@@ -17,21 +17,28 @@
  *                     the tensor core is the hardware's, so results are held
  *                     to an error bound, not to bits:
  *                     |result - exact| <= 2^-20 * sum|x_i| + 1e-6.
+ *                     Binary32 inputs are split exactly into three bfloat16
+ *                     parts (x = hi + mid + lo, hi = x rounded toward zero,
+ *                     the rest exact residuals) whose sums run on the
+ *                     tensor cores, three MMAs per 256 inputs; the split
+ *                     drops less than 2^-133 per input below 2^-110.
  *   TCR_SHUFFLE_TREE  the conventional GPU reduction the same Abstract
  *                     compares against, with its order declared (see
- *                     tcr_order_desc): grid-stride accumulation of 8-input
- *                     vectors, a warp butterfly, a tree over warps and a
- *                     tree over blocks.  Bit-identical to the CPU emulation
+ *                     tcr_order_desc): grid-stride accumulation of 16-byte
+ *                     vectors (8 inputs of 16 bits, 4 of binary32), a warp
+ *                     butterfly, a tree over warps and a tree over blocks.  Bit-identical to the CPU emulation
  *                     of that order.
  *   TCR_MMA_CHAIN_TMEM  the same method on the fifth-generation tensor cores:
  *                     inputs staged into shared memory by bulk asynchronous
  *                     copies, tcgen05.mma (M = 128, N = 16, K = 16; one MMA
  *                     per 2048 inputs) with the accumulator in tensor memory,
  *                     R MMAs per chain, chain sub-results read out to fp32
- *                     registers.  Same error bound as TCR_MMA_CHAIN.  Sums
- *                     only (tcr_reduce_rows returns TCR_ERR_UNSUPPORTED);
- *                     an x that is not 16-byte aligned is reduced by the
- *                     TCR_MMA_CHAIN kernel instead.
+ *                     registers; rows put 128 rows on D's 128 lanes and
+ *                     reach shared memory by 2-D tensor-map copies.  Same
+ *                     error bound as TCR_MMA_CHAIN.  16-bit sums only: an
+ *                     x that is not 16-byte aligned (or rows whose stride is
+ *                     not), sums of squares and binary32 inputs are reduced
+ *                     by the TCR_MMA_CHAIN kernels instead.
  *   TCR_FIXED_ORDER   a balanced binary tree over index order, padded with
  *                     -0.0 to a power of two ("Taming Bitwise Behavior in
  *                     GPU Kernels with Tensor Core", arXiv 2609.11356,
@@ -89,7 +96,8 @@ typedef enum {
 
 typedef enum {
     TCR_F16 = 0,    /* IEEE 754 binary16 */
-    TCR_BF16 = 1    /* bfloat16: the upper 16 bits of a binary32 */
+    TCR_BF16 = 1,   /* bfloat16: the upper 16 bits of a binary32 */
+    TCR_F32 = 2     /* IEEE 754 binary32 */
 } tcr_dtype;
 
 /*
@@ -115,9 +123,10 @@ typedef struct {
 
 /*
  * tcr_reduce_sum -- out[0] = sum of x[0 .. n-1].
- *   x       device pointer to n contiguous 16-bit inputs, 2-byte aligned (any
- *           16-byte misalignment is served by a slower load path with the
- *           same order).  May be NULL only when n == 0.
+ *   x       device pointer to n contiguous inputs of mode.dtype, aligned to
+ *           the input size (2 bytes, or 4 for TCR_F32; any 16-byte
+ *           misalignment is served by a slower load path with the same
+ *           order).  May be NULL only when n == 0.
  *   n       number of inputs, 0 <= n < 2^40.  n == 0 writes +0.0.
  *   out     device pointer to one float, 4-byte aligned.
  *   mode    see tcr_mode.
@@ -130,9 +139,9 @@ TCR_API tcr_status tcr_reduce_sum(const void *x, size_t n, float *out, tcr_mode 
 
 /*
  * tcr_reduce_rows -- out[r] = sum of x[r*cols .. r*cols + cols-1], r < rows.
- *   x       device pointer to a row-major rows x cols matrix of 16-bit inputs
- *           (row stride = cols), 2-byte aligned.  May be NULL only when
- *           rows * cols == 0.
+ *   x       device pointer to a row-major rows x cols matrix of inputs of
+ *           mode.dtype (row stride = cols), aligned to the input size.  May
+ *           be NULL only when rows * cols == 0.
  *   rows    number of rows (0 does nothing); cols: inputs per row (0 writes
  *           +0.0 to every out[r]).  rows * cols < 2^40.
  *   out     device pointer to rows floats, 4-byte aligned.
@@ -154,10 +163,12 @@ TCR_API tcr_status tcr_reduce_rows(const void *x, size_t rows, size_t cols, floa
  *                     leaves fl32(x_i * x_i) (one binary32 multiplication,
  *                     round to nearest; exact for binary16), bit-identical
  *                     to the CPU emulation of those orders.
- *   TCR_MMA_CHAIN     a dense contraction on the tensor cores: for each
- *                     16 x 16 tile A, D = A * A^T holds the rows' sums of
- *                     squares on its diagonal (two m16n8k16 MMAs per tile,
- *                     chains of R flushed to fp32).  Error bound
+ *   TCR_MMA_CHAIN     16-bit inputs: a dense contraction on the tensor
+ *                     cores: for each 16 x 16 tile A, D = A * A^T holds the
+ *                     rows' sums of squares on its diagonal (two m16n8k16
+ *                     MMAs per tile, chains of R flushed to fp32).  Binary32
+ *                     inputs: the leaves fl32(x_i * x_i), split and summed
+ *                     as the sum does.  Error bound
  *                     |result - exact| <= 2^-20 * sum x_i^2 + 1e-6.
  *   TCR_MMA_CHAIN_TMEM  runs as TCR_MMA_CHAIN.
  * tcr_order_descriptor describes these calls as well: the order does not
@@ -184,8 +195,9 @@ TCR_API tcr_status tcr_reduce_rows_sum_squares(const void *x, size_t rows, size_
  *   - Serves TCR_FIXED_ORDER and TCR_MMA_CHAIN; TCR_SHUFFLE_TREE returns
  *     TCR_ERR_UNSUPPORTED.
  *   - n is limited to 65536 chunks of 2^(13 + log2(block_threads / 32))
- *     inputs (2^32 inputs at the default 256 threads, 2^29 at 32); a larger
- *     n returns TCR_ERR_UNSUPPORTED before any GPU work.
+ *     16-bit inputs (2^32 inputs at the default 256 threads, 2^29 at 32),
+ *     half as many binary32 inputs; a larger n returns TCR_ERR_UNSUPPORTED
+ *     before any GPU work.
  *   - The first call on each device looks up the array's device address
  *     with that device current; make that first call before any stream
  *     capture.
@@ -214,7 +226,8 @@ typedef enum {
  *   order            tcr_order.
  *   segment_len      inputs per reduced segment (n, or cols).
  *   segments         number of results (1, or rows).
- *   vector_len       inputs per vector leaf group (8).
+ *   vector_len       inputs per 16-byte vector leaf group (8 for 16-bit
+ *                    inputs, 4 for binary32).
  *   team_threads     SHUFFLE_TREE: threads per block Bt of the team that
  *                    reduces one segment (32 means one warp per segment).
  *   team_blocks      SHUFFLE_TREE: blocks G per segment.  Thread g = b*Bt + t
@@ -224,7 +237,11 @@ typedef enum {
  *                    lane i^offset); a block is the balanced tree over its
  *                    warps; a segment is the balanced tree over its G blocks,
  *                    padded with -0.0.  A vector's value is the balanced tree
- *                    over its 8 inputs, missing inputs being -0.0.
+ *                    over its vector_len inputs, missing inputs being -0.0.
+ *                    The team is one warp (32, 1) when the segment has at
+ *                    most 1024 vectors, else Bt = block_threads and
+ *                    G = ceil(vectors / (16 * Bt)) clamped to
+ *                    1 .. 152 * 1024 / Bt.
  *   chain_R          MMA_CHAIN: MMAs per chain (after defaults).
  *   pad_negative_zero 1: padding inputs and absent subtrees are -0.0.
  *   launch_grid, launch_block, chunk_log2, partials, launches
@@ -233,6 +250,7 @@ typedef enum {
  *                    number of fp32 partials written to scratch (0 if none)
  *                    and the number of kernel launches.  For FIXED_ORDER they
  *                    never change the result.
+ *   dtype            tcr_dtype of the inputs (mode.dtype).
  */
 typedef struct {
     int kind;
@@ -249,6 +267,7 @@ typedef struct {
     int chunk_log2;
     size_t partials;
     int launches;
+    int dtype;
 } tcr_order_desc;
 
 /*
@@ -273,7 +292,7 @@ TCR_API tcr_status tcr_order_descriptor(size_t n, size_t rows, size_t cols, tcr_
  *                     of-two warp counts, so together they are one balanced
  *                     tree over warp index: the order is fixed by the team
  *                     size T = team_threads * team_blocks alone, and by
- *                     nothing at all once T >= the number of 8-input vectors
+ *                     nothing at all once T >= the number of vectors
  *                     (every thread then holds at most one);
  *   TCR_MMA_CHAIN(_TMEM) equivalent when chain_R, launch_block and chunk_log2
  *                     match (the tensor core's own order is fixed per shape).

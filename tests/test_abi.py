@@ -65,6 +65,9 @@ FAKE = 0x7F0000000000      # never dereferenced: every case below fails validati
     (FAKE, 1 << 40, FAKE, tcr.Mode(tcr.FIXED_ORDER)),            # n too large
     (FAKE, 10, FAKE, tcr.Mode(7)),                               # unknown kind
     (FAKE, 10, FAKE, tcr.Mode(tcr.FIXED_ORDER, dtype=5)),        # unknown dtype
+    (FAKE, 10, FAKE, tcr.Mode(tcr.FIXED_ORDER, dtype=3)),
+    (FAKE + 2, 10, FAKE, tcr.Mode(tcr.FIXED_ORDER, dtype=tcr.F32)),   # binary32 not 4-byte aligned
+    (FAKE + 2, 10, FAKE, tcr.Mode(tcr.MMA_CHAIN, dtype=tcr.F32)),
     (FAKE, 10, FAKE, tcr.Mode(tcr.MMA_CHAIN, R=9)),              # R out of range
     (FAKE, 10, FAKE, tcr.Mode(tcr.MMA_CHAIN, R=-1)),
     (FAKE, 10, FAKE, tcr.Mode(tcr.SHUFFLE_TREE, block_threads=48)),   # not a power of two
@@ -95,16 +98,53 @@ def test_descriptor_rejects_bad_arguments(lib):
         tcr.ERR_INVALID_ARG
 
 
-@pytest.mark.parametrize("L", [1, 100, 8192, 8193, 10_000, 1 << 20, 1 << 28, 1 << 30])
+@pytest.mark.parametrize("L", [1, 100, 4096, 4097, 8192, 8193, 10_000, 1 << 20, 1 << 28, 1 << 30])
 @pytest.mark.parametrize("block", [0, 32, 128, 1024])
-def test_shuffle_descriptor_matches_the_declared_rule(lib, L, block):
-    m = tcr.Mode(tcr.SHUFFLE_TREE, block_threads=block)
-    bt, g = spec.shuffle_team(L, block)
+@pytest.mark.parametrize("dtype", [tcr.F16, tcr.BF16, tcr.F32])
+def test_shuffle_descriptor_matches_the_declared_rule(lib, L, block, dtype):
+    m = tcr.Mode(tcr.SHUFFLE_TREE, block_threads=block, dtype=dtype)
+    bt, g = spec.shuffle_team(L, block, dtype)
     for d in (tcr.tcr_order_descriptor(n=L, mode=m), tcr.tcr_order_descriptor(rows=3, cols=L, mode=m)):
         assert d["order"] == tcr.ORDER_GRID_STRIDE
         assert (d["team_threads"], d["team_blocks"]) == (bt, g)
-        assert d["vector_len"] == 8 and d["pad_negative_zero"] == 1
+        assert d["vector_len"] == spec.vector_len(dtype) and d["pad_negative_zero"] == 1
+        assert d["dtype"] == dtype
         assert d["partials"] == (0 if g == 1 else d["segments"] * g)
+
+
+def test_binary32_descriptors(lib):
+    # a warp span is 16 KiB: 2^13 16-bit inputs, 2^12 binary32 inputs
+    for blk in (32, 256, 1024):
+        d16 = tcr.tcr_order_descriptor(n=1 << 24, mode=tcr.Mode(tcr.FIXED_ORDER, block_threads=blk))
+        d32 = tcr.tcr_order_descriptor(
+            n=1 << 24, mode=tcr.Mode(tcr.FIXED_ORDER, block_threads=blk, dtype=tcr.F32))
+        assert d32["chunk_log2"] == d16["chunk_log2"] - 1
+        assert d32["partials"] == 2 * d16["partials"]
+    # rows of up to 32 KiB take one warp each: 16384 16-bit or 8192 binary32 inputs
+    # (at 32 threads a chunked row is 2^12-input chunks, so 8193 makes 3)
+    m = tcr.Mode(tcr.FIXED_ORDER, block_threads=32, dtype=tcr.F32)
+    d = tcr.tcr_order_descriptor(rows=100, cols=8192, mode=m)
+    assert d["partials"] == 0 and d["launch_block"] == 256
+    d = tcr.tcr_order_descriptor(rows=100, cols=8193, mode=m)
+    assert d["partials"] == 300 and d["launch_block"] == 32
+    # the tcgen05 kind reduces binary32 inputs with the mma.sync split kernel
+    d = tcr.tcr_order_descriptor(n=1 << 24, mode=tcr.Mode(tcr.MMA_CHAIN_TMEM, dtype=tcr.F32))
+    dm = tcr.tcr_order_descriptor(n=1 << 24, mode=tcr.Mode(tcr.MMA_CHAIN, dtype=tcr.F32))
+    assert (d["launch_block"], d["chunk_log2"], d["partials"]) == \
+        (dm["launch_block"], dm["chunk_log2"], dm["partials"])
+
+
+def test_equivalence_needs_the_same_input_type(lib):
+    for kind in (tcr.FIXED_ORDER, tcr.SHUFFLE_TREE, tcr.MMA_CHAIN):
+        a = {"n": 100_000, "mode": tcr.Mode(kind)}
+        assert tcr.tcr_order_equivalent(a, a)
+        assert not tcr.tcr_order_equivalent(a, {"n": 100_000, "mode": tcr.Mode(kind, dtype=tcr.F32)})
+    f32 = tcr.Mode(tcr.SHUFFLE_TREE, dtype=tcr.F32)
+    # 3000 binary32 inputs are 750 vectors: every team of at least 750
+    # threads holds at most one vector per thread
+    assert tcr.tcr_order_equivalent(
+        {"n": 3000, "mode": tcr.Mode(tcr.SHUFFLE_TREE, block_threads=1024, dtype=tcr.F32)},
+        {"n": 3000, "mode": f32})
 
 
 def test_fixed_descriptor_is_the_balanced_tree(lib):
