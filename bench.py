@@ -449,11 +449,24 @@ def sweep_arm(args):
 def profile_arm(args):
     """A small case for ncu: each sum mode once on 2^28 fp16 values (512 MiB,
     larger than L2), each rows mode once on 32768 x 4096 rows (256 MiB), and
-    the tcgen05 MMA_CHAIN sum."""
+    the tcgen05 MMA_CHAIN sum and rows.  ``--profile-case f32``: the same
+    bytes in binary32 (2^27 sum, 32768 x 2048 rows), the three mma.sync-era
+    modes."""
     import torch
     import arithmetic_reduction_tensor_gb300 as tcr
     from arithmetic_reduction_tensor_gb300 import synth
     torch.cuda.set_device(0)
+    if args.profile_case == "f32":
+        x = torch.from_numpy(synth.generate(1 << 27, "uniform_pm1", synth.F32, seed=4).view(np.float32))
+        r = torch.from_numpy(synth.generate(32768 * 2048, "normal", synth.F32, seed=2).view(np.float32))
+        x, r = x.cuda(), r.cuda().view(32768, 2048)
+        for _ in range(args.steps):
+            for kind in (tcr.MMA_CHAIN, tcr.FIXED_ORDER, tcr.SHUFFLE_TREE):
+                tcr.tcr_reduce_sum(x, tcr.Mode(kind, dtype=tcr.F32))
+                tcr.tcr_reduce_rows(r, tcr.Mode(kind, dtype=tcr.F32))
+        torch.cuda.synchronize()
+        print("profile case done", flush=True)
+        return 0
     n = 1 << 28
     x = torch.from_numpy(synth.generate(n, "uniform_pm1", synth.F16, seed=4).view(np.int16)).cuda()
     r = torch.from_numpy(synth.generate(32768 * COLS, "normal", synth.F16, seed=2).view(np.int16))
@@ -470,8 +483,10 @@ def profile_arm(args):
 
 
 def extras_arm(args):
-    """Beyond the hot path: the sum of squares (2^30 sum and 65536 x 4096
-    rows, every mode), one JSON line per call."""
+    """Beyond the hot path, one JSON line per call: the sum of squares (2^30
+    sum and 65536 x 4096 rows, every mode) and binary32 inputs (2^29 sum and
+    65536 x 2048 rows -- the same bytes as the 16-bit workload -- every mode,
+    sums and sums of squares)."""
     import torch
     import arithmetic_reduction_tensor_gb300 as tcr
     from arithmetic_reduction_tensor_gb300 import synth
@@ -488,6 +503,18 @@ def extras_arm(args):
                       lambda m=m: tcr.tcr_reduce_sum_squares(xs, m, out=out[:1])))
         calls.append(("rows_sum_squares/" + tcr.KIND_NAMES[kind], 2 * ROWS * COLS + 4 * ROWS,
                       lambda m=m: tcr.tcr_reduce_rows_sum_squares(xr, m, out=out)))
+    n32, cols32 = N_SUM // 2, COLS // 2
+    fs = torch.from_numpy(synth.generate(n32, "uniform_pm1", synth.F32, seed=4).view(np.float32)).cuda()
+    fr = torch.from_numpy(synth.generate(ROWS * cols32, "normal", synth.F32, seed=2).view(np.float32))
+    fr = fr.cuda().view(ROWS, cols32)
+    for kind in (tcr.MMA_CHAIN, tcr.FIXED_ORDER, tcr.SHUFFLE_TREE):
+        m = tcr.Mode(kind, dtype=tcr.F32)
+        k = tcr.KIND_NAMES[kind]
+        calls.append(("f32_sum/" + k, 4 * n32 + 4, lambda m=m: tcr.tcr_reduce_sum(fs, m, out=out[:1])))
+        calls.append(("f32_rows/" + k, 4 * ROWS * cols32 + 4 * ROWS,
+                      lambda m=m: tcr.tcr_reduce_rows(fr, m, out=out)))
+        calls.append(("f32_sum_squares/" + k, 4 * n32 + 4,
+                      lambda m=m: tcr.tcr_reduce_sum_squares(fs, m, out=out[:1])))
     for name, nbytes, fn in calls:
         for _ in range(args.warmup):
             fn()
@@ -513,9 +540,10 @@ def main():
     ap.add_argument("--impl", choices=["tcr", "reference"], default="tcr")
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--extras", action="store_true",
-                    help="time the sum of squares calls (beyond the hot path) and exit")
-    ap.add_argument("--profile-case", action="store_true",
-                    help="run the small ncu case (2^28 sum, 32768 x 4096 rows) and exit")
+                    help="time the sum of squares and binary32 calls (beyond the hot path) and exit")
+    ap.add_argument("--profile-case", nargs="?", const="f16", choices=["f16", "f32"], default=None,
+                    help="run the small ncu case (2^28 sum, 32768 x 4096 rows; f32: the same "
+                         "bytes in binary32) and exit")
     ap.add_argument("--e2e-steps", type=int, default=0, help="0: max(3, steps // 40)")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     args = ap.parse_args()

@@ -76,3 +76,20 @@ def test_no_alloc_after_a_larger_call_and_limits(lib):
     assert st == tcr.ERR_UNSUPPORTED
     st = lib.tcr_reduce_sum_noalloc(small.data_ptr(), 10, o.data_ptr(), tcr.Mode(tcr.SHUFFLE_TREE), None)
     assert st == tcr.ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("kind", [tcr.FIXED_ORDER, tcr.MMA_CHAIN])
+@pytest.mark.parametrize("n", [3, 4097, (1 << 22) + 5])
+def test_no_alloc_binary32(lib, kind, n):
+    bits = synth.generate(n, "normal", tcr.F32, seed=n)
+    x = torch.from_numpy(bits.view(np.float32)).cuda()
+    mode = tcr.Mode(kind, dtype=tcr.F32)
+    ref = torch.full((1,), 5.0, device="cuda")
+    assert _call(lib.tcr_reduce_sum, x, ref, mode) == tcr.OK
+    o = torch.full((1,), 7.0, device="cuda")
+    assert _call(lib.tcr_reduce_sum_noalloc, x, o, mode) == tcr.OK
+    torch.cuda.synchronize()
+    # the same kernels and work split as the allocating call: the same bits
+    assert o.cpu().numpy().tobytes() == ref.cpu().numpy().tobytes()
+    if kind == tcr.FIXED_ORDER:
+        assert o.cpu().numpy()[0] == oracle.fixed_order(bits, tcr.F32)
