@@ -19,6 +19,9 @@ Functions (sources are cited in ``tcr_oracle.c``):
 ``shuffle_tree``       declared order of the conventional reduction
                        (grid-stride accumulation, warp butterfly, block tree,
                        grid tree).
+``blocked_order``      runs of 2^c inputs added left to right, then the
+                       balanced tree over the runs (a second declared order
+                       of the fixed-order mode).
 ``*_sq``, ``exact_sum_squares``
                        the same over the leaves x_i^2 (sum of squares).
 ``*_rows``             the same, one result per row.
@@ -90,6 +93,10 @@ def _load():
             lib.oracle_shuffle_tree_f32.restype = ctypes.c_float
             lib.oracle_shuffle_tree_rows_f32.argtypes = [u16p, sz, sz, i, i, i, i, i, f32p]
             lib.oracle_shuffle_tree_rows_f32.restype = None
+            lib.oracle_blocked_order_f32.argtypes = [u16p, sz, i, i, i]
+            lib.oracle_blocked_order_f32.restype = ctypes.c_float
+            lib.oracle_blocked_order_rows_f32.argtypes = [u16p, sz, sz, i, i, i, f32p]
+            lib.oracle_blocked_order_rows_f32.restype = None
             lib.oracle_leaves_f32.argtypes = [u16p, sz, i, f32p]
             lib.oracle_leaves_f32.restype = None
             _lib = lib
@@ -200,6 +207,24 @@ def shuffle_tree_rows(x, dtype: int, team_threads: int, team_blocks: int,
                                          team_threads,
                                          team_blocks, threads or default_threads(),
                                          out.ctypes.data_as(ctypes.POINTER(ctypes.c_float)))
+    return out
+
+
+def blocked_order(x, dtype: int, run_log2: int, threads: int | None = None) -> np.float32:
+    """Runs of 2^run_log2 inputs summed left to right, then the balanced tree
+    over the run values (-0.0 pad)."""
+    a = _bits(x, dtype).reshape(-1)
+    return np.float32(_load().oracle_blocked_order_f32(_u16p(a), a.size, dtype, run_log2,
+                                                       threads or default_threads()))
+
+
+def blocked_order_rows(x, dtype: int, run_log2: int, threads: int | None = None) -> np.ndarray:
+    a = _bits(x, dtype)
+    rows, cols = a.shape
+    out = np.empty(rows, np.float32)
+    _load().oracle_blocked_order_rows_f32(_u16p(a), rows, cols, dtype, run_log2,
+                                          threads or default_threads(),
+                                          out.ctypes.data_as(ctypes.POINTER(ctypes.c_float)))
     return out
 
 

@@ -438,6 +438,56 @@ void oracle_fixed_order_rows_f32(const void *x, size_t rows, size_t cols, int dt
 }
 
 /* ------------------------------------------------------------------ */
+/* Blocked-sequential-then-tree order ("Taming Bitwise Behavior in GPU
+ * Kernels with Tensor Core", Abstract: an order is pinned by a descriptor;
+ * this is a second declared order for the fixed-order mode, with a run
+ * length chosen by the caller).
+ *
+ * The segment of n inputs is cut into runs of C = 2^run_log2 consecutive
+ * inputs (the last one shorter).  A run's value is its leaves added left to
+ * right in binary32, starting from -0.0 (so a run of one input is that
+ * input).  The result is the balanced binary32 tree over the run values in
+ * run order, padded with -0.0 -- for C = 1 the plain fixed-order tree, for
+ * C >= n the plain left-to-right sum. */
+
+static float run_value(const void *x, size_t n, int dtype, size_t lo, size_t C)
+{
+    float s = -0.0f;
+    size_t hi = lo + C < n ? lo + C : n;
+    for (size_t i = lo; i < hi; i++) s = s + leaf_f32(raw_at(x, i, dtype), dtype);
+    return s;
+}
+
+static float blocked_order_any(const void *x, size_t n, int dtype, int run_log2, int threads)
+{
+    if (n == 0) return 0.0f;
+    if (run_log2 < 0 || run_log2 > 40) return NAN;
+    const size_t C = (size_t)1 << run_log2;
+    const size_t m = (n + C - 1) / C;       /* runs */
+    float *runs = (float *)malloc(m * sizeof(float));
+    int nt = threads > 0 ? threads : 1;
+#pragma omp parallel for num_threads(nt) schedule(dynamic, 64)
+    for (size_t r = 0; r < m; r++) runs[r] = run_value(x, n, dtype, r * C, C);
+    float v = tree_f32(runs, m);
+    free(runs);
+    return v;
+}
+
+float oracle_blocked_order_f32(const void *x, size_t n, int dtype, int run_log2, int threads)
+{
+    return blocked_order_any(x, n, dtype, run_log2, threads);
+}
+
+void oracle_blocked_order_rows_f32(const void *x, size_t rows, size_t cols, int dtype,
+                                   int run_log2, int threads, float *out)
+{
+    int nt = threads > 0 ? threads : 1;
+#pragma omp parallel for num_threads(nt) schedule(dynamic, 16)
+    for (size_t r = 0; r < rows; r++)
+        out[r] = blocked_order_any(raw_ptr(x, r * cols, dtype), cols, dtype, run_log2, 1);
+}
+
+/* ------------------------------------------------------------------ */
 /* Declared order of the conventional reduction (SHUFFLE_TREE).
  *
  * A segment of L inputs is split into vectors of V consecutive inputs, the

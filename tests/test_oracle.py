@@ -565,3 +565,71 @@ def test_f32_inputs_holding_16_bit_values_sum_like_them():
     assert oracle.exact_sum(w, F32) == oracle.exact_sum(h, F16)
     assert same_f32(oracle.fixed_order(w, F32), oracle.fixed_order(h, F16))
     assert oracle.exact_sum_squares(w, F32) == oracle.exact_sum_squares(h, F16)
+
+
+# ---------------------------------------------------------------- blocked order
+
+def np_blocked(bits, dtype, run_log2):
+    """Runs summed left to right by numpy's accumulate (a plain sequential
+    loop in float32), then the level-wise numpy tree over the runs."""
+    v = np_leaves(bits, dtype).astype(np.float32)
+    if v.size == 0:
+        return np.float32(0.0)
+    C = 1 << run_log2
+    m = -(-v.size // C)
+    e = np.full(m * C, -0.0, np.float32)
+    e[:v.size] = v
+    with np.errstate(over="ignore", invalid="ignore"):
+        runs = np.add.accumulate(e.reshape(m, C), axis=1, dtype=np.float32)[:, -1]
+    return np_tree(runs)
+
+
+def test_blocked_order_hand_worked_cases(golden_dir):
+    n_cases = 0
+    with open(os.path.join(golden_dir, "blocked_order_cases.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            c, bits, expect = [p.strip() for p in line.split("|")]
+            b = np.array([int(h, 16) for h in bits.split()], np.uint16)
+            got = oracle.blocked_order(b, F16, int(c), threads=1)
+            assert got == np.float32(float(Fraction(expect))), line
+            n_cases += 1
+    assert n_cases == 5
+
+
+@pytest.mark.parametrize("dtype", [F16, BF16, F32])
+@pytest.mark.parametrize("n", [1, 5, 8, 63, 64, 65, 1000, 4097, 100_003])
+@pytest.mark.parametrize("c", [0, 1, 2, 3, 5, 7, 12])
+def test_blocked_order_matches_numpy(dtype, n, c):
+    rng = np.random.default_rng(n * 16 + c)
+    bits = random_finite(rng, n, dtype) if n < 5000 else synth.generate(n, "normal", dtype, seed=n)
+    assert same_f32(oracle.blocked_order(bits, dtype, c, threads=3), np_blocked(bits, dtype, c))
+
+
+def test_blocked_order_limits_are_the_tree_and_the_sequential_sum():
+    bits = synth.generate(30_001, "uniform_pm1", F16, seed=46)
+    tree = oracle.fixed_order(bits, F16)
+    assert same_f32(oracle.blocked_order(bits, F16, 0), tree)
+    assert same_f32(oracle.blocked_order(bits, F16, 1), tree)       # runs of two = pairs
+    seq = np.float32(0.0)
+    for v in np_leaves(bits, F16):
+        seq = np.float32(seq + v)
+    for c in (15, 16, 20):                                           # one run
+        assert same_f32(oracle.blocked_order(bits, F16, c), seq)
+    # the orders differ in between: C = 4 is neither the tree nor the run of all
+    c4 = oracle.blocked_order(bits, F16, 2)
+    assert not same_f32(c4, seq) or not same_f32(c4, tree)
+
+
+def test_blocked_order_rows_and_degenerate():
+    x = synth.generate(21 * 3001, "normal", BF16, seed=47).reshape(21, 3001)
+    got = oracle.blocked_order_rows(x, BF16, 6)
+    for r in range(21):
+        assert same_f32(got[r], oracle.blocked_order(x[r], BF16, 6, threads=1))
+    assert oracle.blocked_order(np.zeros(0, np.uint16), F16, 4).tobytes() == \
+        np.float32(0.0).tobytes()
+    negz = oracle.blocked_order(np.full(9, 0x8000, np.uint16), F16, 2)
+    assert negz.tobytes() == np.float32(-0.0).tobytes()
+    assert np.isnan(oracle.blocked_order(np.array([0x3C00, 0x7E00], np.uint16), F16, 1))
