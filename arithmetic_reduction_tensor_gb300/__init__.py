@@ -25,7 +25,7 @@ from .build import LIB_PATH
 __all__ = [
     "MMA_CHAIN", "SHUFFLE_TREE", "FIXED_ORDER", "MMA_CHAIN_TMEM", "F16", "BF16", "F32",
     "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_CUDA",
-    "ORDER_TENSOR_CORE", "ORDER_GRID_STRIDE", "ORDER_BALANCED_TREE",
+    "ORDER_TENSOR_CORE", "ORDER_GRID_STRIDE", "ORDER_BALANCED_TREE", "ORDER_BLOCKED_TREE",
     "tcr_mode", "tcr_order_desc", "Mode", "TcrError", "c_api",
     "tcr_reduce_sum", "tcr_reduce_rows", "tcr_reduce_sum_squares", "tcr_reduce_rows_sum_squares",
     "tcr_order_descriptor", "tcr_order_equivalent", "tcr_status_string", "tcr_device_faults",
@@ -36,7 +36,7 @@ MMA_CHAIN, SHUFFLE_TREE, FIXED_ORDER, MMA_CHAIN_TMEM = 0, 1, 2, 3
 F16, BF16, F32 = 0, 1, 2
 DTYPE_NAMES = {F16: "f16", BF16: "bf16", F32: "f32"}
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA = 0, 1, 2, 3
-ORDER_TENSOR_CORE, ORDER_GRID_STRIDE, ORDER_BALANCED_TREE = 0, 1, 2
+ORDER_TENSOR_CORE, ORDER_GRID_STRIDE, ORDER_BALANCED_TREE, ORDER_BLOCKED_TREE = 0, 1, 2, 3
 
 KIND_NAMES = {MMA_CHAIN: "MMA_CHAIN", SHUFFLE_TREE: "SHUFFLE_TREE", FIXED_ORDER: "FIXED_ORDER",
               MMA_CHAIN_TMEM: "MMA_CHAIN_TMEM"}
@@ -44,12 +44,13 @@ KIND_NAMES = {MMA_CHAIN: "MMA_CHAIN", SHUFFLE_TREE: "SHUFFLE_TREE", FIXED_ORDER:
 
 class tcr_mode(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int), ("R", ctypes.c_int),
-                ("block_threads", ctypes.c_int), ("dtype", ctypes.c_int)]
+                ("block_threads", ctypes.c_int), ("dtype", ctypes.c_int),
+                ("run_log2", ctypes.c_int)]
 
     def __repr__(self):
         return (f"Mode({KIND_NAMES.get(self.kind, self.kind)}, R={self.R}, "
                 f"block_threads={self.block_threads}, "
-                f"dtype={DTYPE_NAMES.get(self.dtype, self.dtype)})")
+                f"dtype={DTYPE_NAMES.get(self.dtype, self.dtype)}, run_log2={self.run_log2})")
 
 
 class tcr_order_desc(ctypes.Structure):
@@ -60,15 +61,18 @@ class tcr_order_desc(ctypes.Structure):
                 ("pad_negative_zero", ctypes.c_int), ("launch_grid", ctypes.c_int),
                 ("launch_block", ctypes.c_int), ("chunk_log2", ctypes.c_int),
                 ("partials", ctypes.c_size_t), ("launches", ctypes.c_int),
-                ("dtype", ctypes.c_int)]
+                ("dtype", ctypes.c_int), ("run_log2", ctypes.c_int)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}
 
 
-def Mode(kind: int, R: int = 0, block_threads: int = 0, dtype: int = F16) -> tcr_mode:
-    """A ``tcr_mode`` (R is used by MMA_CHAIN only; 0 means the default)."""
-    return tcr_mode(kind, R, block_threads, dtype)
+def Mode(kind: int, R: int = 0, block_threads: int = 0, dtype: int = F16,
+         run_log2: int = 0) -> tcr_mode:
+    """A ``tcr_mode`` (R is used by MMA_CHAIN only, 0 meaning the default;
+    run_log2 by FIXED_ORDER only: runs of 2^run_log2 inputs added left to
+    right, then the balanced tree)."""
+    return tcr_mode(kind, R, block_threads, dtype, run_log2)
 
 
 class TcrError(RuntimeError):
@@ -177,7 +181,7 @@ def _sum_call(name, x, mode, out, stream):
     import torch
     if not x.is_cuda or not x.is_contiguous():
         raise ValueError("x must be a contiguous CUDA tensor")
-    m = tcr_mode(mode.kind, mode.R, mode.block_threads, _dtype_code(x, mode))
+    m = tcr_mode(mode.kind, mode.R, mode.block_threads, _dtype_code(x, mode), mode.run_log2)
     out = _check_out(out, x.device, 1)
     with torch.cuda.device(x.device):
         st = getattr(c_api(), name)(x.data_ptr() if x.numel() else None, x.numel(),
@@ -192,7 +196,7 @@ def _rows_call(name, x, mode, out, stream):
     if not x.is_cuda or not x.is_contiguous() or x.dim() != 2:
         raise ValueError("x must be a contiguous 2-D CUDA tensor")
     rows, cols = x.shape
-    m = tcr_mode(mode.kind, mode.R, mode.block_threads, _dtype_code(x, mode))
+    m = tcr_mode(mode.kind, mode.R, mode.block_threads, _dtype_code(x, mode), mode.run_log2)
     out = _check_out(out, x.device, rows)
     with torch.cuda.device(x.device):
         st = getattr(c_api(), name)(x.data_ptr() if x.numel() else None, rows, cols,

@@ -222,6 +222,79 @@ __device__ __forceinline__ float vec_tree(uint4 q)
     }
 }
 
+// (run + low leaf) + high leaf of a 32-bit word of two 16-bit inputs, one
+// asm statement (as pair_val): the leaves are unpacked where they are added.
+template <int DT>
+__device__ __forceinline__ float seq_pair(float run, uint32_t w)
+{
+    float r;
+    if constexpr (DT == kF16) {
+        asm("{\n\t.reg .b16 l, h;\n\t.reg .f32 a;\n\t"
+            "mov.b32 {l, h}, %2;\n\t"
+            "cvt.f32.f16 a, l;\n\t"
+            "add.rn.f32 %0, %1, a;\n\t"
+            "cvt.f32.f16 a, h;\n\t"
+            "add.rn.f32 %0, %0, a;\n\t}"
+            : "=&f"(r)
+            : "f"(run), "r"(w));
+    } else {
+        asm("{\n\t.reg .b32 a;\n\t"
+            "shl.b32 a, %2, 16;\n\t"
+            "add.rn.f32 %0, %1, a;\n\t"
+            "and.b32 a, %2, 0xffff0000;\n\t"
+            "add.rn.f32 %0, %0, a;\n\t}"
+            : "=&f"(r)
+            : "f"(run), "r"(w));
+    }
+    return r;
+}
+
+// ((x + y) + z) + w of four binary32 inputs, one asm statement.
+__device__ __forceinline__ float seq_quad32(uint32_t x, uint32_t y, uint32_t z, uint32_t w)
+{
+    float r;
+    asm("{\n\t.reg .f32 a;\n\t"
+        "add.rn.f32 a, %1, %2;\n\t"
+        "add.rn.f32 a, a, %3;\n\t"
+        "add.rn.f32 %0, a, %4;\n\t}"
+        : "=f"(r)
+        : "r"(x), "r"(y), "r"(z), "r"(w));
+    return r;
+}
+
+// Blocked order inside one vector: runs of 2^CLOG leaves added left to
+// right, then the balanced tree over the runs (2 <= CLOG <= log2 V; runs of
+// two leaves are the tree's own pairs).  A run starts from its first leaf,
+// which equals starting from -0.0.
+template <int DT, int CLOG>
+__device__ __forceinline__ float vec_runs(uint4 q)
+{
+    static_assert(CLOG >= 2 && (1 << CLOG) <= Elem<DT>::kPerVec, "run outside 4..V");
+    if constexpr (DT == kF32) {
+        return seq_quad32(q.x, q.y, q.z, q.w);
+    } else if constexpr (CLOG == 2) {
+        const float r0 = seq_pair<DT>(seq_pair<DT>(-0.0f, q.x), q.y);
+        const float r1 = seq_pair<DT>(seq_pair<DT>(-0.0f, q.z), q.w);
+        return __fadd_rn(r0, r1);
+    } else {
+        return seq_pair<DT>(seq_pair<DT>(seq_pair<DT>(seq_pair<DT>(-0.0f, q.x), q.y), q.z), q.w);
+    }
+}
+
+// run + (the leaves of a vector, left to right).
+template <int DT>
+__device__ __forceinline__ float vec_seq_add(float run, uint4 q)
+{
+    if constexpr (DT == kF32) {
+        run = __fadd_rn(run, __uint_as_float(q.x));
+        run = __fadd_rn(run, __uint_as_float(q.y));
+        run = __fadd_rn(run, __uint_as_float(q.z));
+        return __fadd_rn(run, __uint_as_float(q.w));
+    } else {
+        return seq_pair<DT>(seq_pair<DT>(seq_pair<DT>(seq_pair<DT>(run, q.x), q.y), q.z), q.w);
+    }
+}
+
 // ---------------------------------------------------------------- trees
 
 // Binary counter over a sequence of equal-height subtree values pushed in

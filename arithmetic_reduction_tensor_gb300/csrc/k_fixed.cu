@@ -19,57 +19,66 @@
 
 namespace tcr {
 
-template <int DT, int OP, bool ALIGNED>
+template <int DT, int OP, bool ALIGNED, int VRUN>
 __global__ void __launch_bounds__(1024)
 fixed_chunk_kernel(const void *__restrict__ x, size_t seg_len, size_t units, size_t cps,
                    int chunk_log2, float *__restrict__ dst)
 {
     // a warp span of 4 groups, < 2^3
-    chunk_body<FixedReducer<DT, OP, 3>, ALIGNED>(x, seg_len, units, cps, chunk_log2, dst);
+    chunk_body<FixedReducer<DT, OP, 3, VRUN>, ALIGNED>(x, seg_len, units, cps, chunk_log2, dst);
 }
 
-template <int DT, int OP, bool ALIGNED>
+template <int DT, int OP, bool ALIGNED, int VRUN>
 __global__ void __launch_bounds__(kRowsBlock, kRowsMinCtas)
 fixed_rows_warp_kernel(const void *__restrict__ x, size_t rows, size_t cols,
                        float *__restrict__ out)
 {
     // rows of at most kRowsWarpMaxBytes = 8 groups, < 2^4
-    rows_body<FixedReducer<DT, OP, 4>, ALIGNED>(x, rows, cols, out);
+    rows_body<FixedReducer<DT, OP, 4, VRUN>, ALIGNED>(x, rows, cols, out);
 }
 
 // ---------------------------------------------------------------- host
 
-template <int DT, int OP>
-static const void *pick_do(bool rows, bool aligned)
+template <int DT, int OP, int VRUN>
+static const void *pick_dov(bool rows, bool aligned)
 {
-    if (rows) return aligned ? (const void *)fixed_rows_warp_kernel<DT, OP, true>
-                             : (const void *)fixed_rows_warp_kernel<DT, OP, false>;
-    return aligned ? (const void *)fixed_chunk_kernel<DT, OP, true>
-                   : (const void *)fixed_chunk_kernel<DT, OP, false>;
+    if (rows) return aligned ? (const void *)fixed_rows_warp_kernel<DT, OP, true, VRUN>
+                             : (const void *)fixed_rows_warp_kernel<DT, OP, false, VRUN>;
+    return aligned ? (const void *)fixed_chunk_kernel<DT, OP, true, VRUN>
+                   : (const void *)fixed_chunk_kernel<DT, OP, false, VRUN>;
 }
 
+// vrun: 0 the balanced tree; 2 or 3 (sums only) runs of 4 or 8 inputs inside
+// a vector (3 for 16-bit inputs only)
 template <int DT>
-static const void *pick_d(bool rows, int op, bool aligned)
+static const void *pick_d(bool rows, int op, bool aligned, int vrun)
 {
-    return op == kOpSquares ? pick_do<DT, kOpSquares>(rows, aligned)
-                            : pick_do<DT, kOpSum>(rows, aligned);
+    if (vrun == 0)
+        return op == kOpSquares ? pick_dov<DT, kOpSquares, 0>(rows, aligned)
+                                : pick_dov<DT, kOpSum, 0>(rows, aligned);
+    if (op != kOpSum) return nullptr;
+    if (vrun == 2) return pick_dov<DT, kOpSum, 2>(rows, aligned);
+    if constexpr (Elem<DT>::kPerVec == 8) {
+        if (vrun == 3) return pick_dov<DT, kOpSum, 3>(rows, aligned);
+    }
+    return nullptr;
 }
 
-static const void *pick(bool rows, int dtype, int op, bool aligned)
+static const void *pick(bool rows, int dtype, int op, bool aligned, int vrun)
 {
     switch (dtype) {
-    case kF16: return pick_d<kF16>(rows, op, aligned);
-    case kBF16: return pick_d<kBF16>(rows, op, aligned);
-    case kF32: return pick_d<kF32>(rows, op, aligned);
+    case kF16: return pick_d<kF16>(rows, op, aligned, vrun);
+    case kBF16: return pick_d<kBF16>(rows, op, aligned, vrun);
+    case kF32: return pick_d<kF32>(rows, op, aligned, vrun);
     default: return nullptr;
     }
 }
 
 cudaError_t launch_fixed_chunk(int dtype, int op, bool aligned, const void *x, size_t seg_len,
                                size_t units, size_t cps, int chunk_log2, float *dst, int grid,
-                               int block, cudaStream_t stream)
+                               int block, cudaStream_t stream, int vrun)
 {
-    const void *k = pick(false, dtype, op, aligned);
+    const void *k = pick(false, dtype, op, aligned, vrun);
     if (!k) return cudaErrorInvalidValue;
     void *args[] = {(void *)&x, (void *)&seg_len, (void *)&units, (void *)&cps,
                     (void *)&chunk_log2, (void *)&dst};
@@ -78,17 +87,17 @@ cudaError_t launch_fixed_chunk(int dtype, int op, bool aligned, const void *x, s
 
 cudaError_t launch_fixed_rows_warp(int dtype, int op, bool aligned, const void *x, size_t rows,
                                    size_t cols, float *out, int grid, int block,
-                                   cudaStream_t stream)
+                                   cudaStream_t stream, int vrun)
 {
-    const void *k = pick(true, dtype, op, aligned);
+    const void *k = pick(true, dtype, op, aligned, vrun);
     if (!k) return cudaErrorInvalidValue;
     void *args[] = {(void *)&x, (void *)&rows, (void *)&cols, (void *)&out};
     return cudaLaunchKernel(k, dim3(grid), dim3(block), args, 0, stream);
 }
 
-int occupancy_fixed(bool rows, int dtype, int op, bool aligned, int block)
+int occupancy_fixed(bool rows, int dtype, int op, bool aligned, int block, int vrun)
 {
-    const void *k = pick(rows, dtype, op, aligned);
+    const void *k = pick(rows, dtype, op, aligned, vrun);
     int n = 0;
     if (!k || cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, block, 0) != cudaSuccess) {
         (void)cudaGetLastError();

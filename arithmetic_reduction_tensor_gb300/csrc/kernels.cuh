@@ -17,14 +17,25 @@ namespace tcr {
 // ---- FIXED_ORDER (balanced tree over index order)
 // Chunked: CTA work unit u = (segment u / cps, chunk u % cps); the chunk of
 // 2^chunk_log2 inputs is split evenly over the CTA's warps; dst[u] is the
-// chunk's aligned subtree.
+// chunk's aligned subtree.  vrun = 2 or 3 (sums only): the blocked order
+// with runs of 2^vrun inputs inside each vector (3: 16-bit inputs only).
 cudaError_t launch_fixed_chunk(int dtype, int op, bool aligned, const void *x, size_t seg_len,
                                size_t units, size_t cps, int chunk_log2, float *dst, int grid,
-                               int block, cudaStream_t stream);
+                               int block, cudaStream_t stream, int vrun = 0);
 // One warp per row, rows <= kRowsWarpMaxBytes long: out[r] = row tree.
 cudaError_t launch_fixed_rows_warp(int dtype, int op, bool aligned, const void *x, size_t rows,
                                    size_t cols, float *out, int grid, int block,
-                                   cudaStream_t stream);
+                                   cudaStream_t stream, int vrun = 0);
+
+// ---- FIXED_ORDER, blocked order with runs longer than a vector
+// (2^run_log2 inputs, run_log2 > log2 of the inputs per vector): each lane
+// owns one run of a round of 32 runs; dst[u] is the chunk's aligned subtree
+// (chunk 2^chunk_log2 = warps x span, span a whole number of rounds).  CTAs
+// of at most 256 threads.
+cudaError_t launch_blocked_chunk(int dtype, bool aligned, const void *x, size_t seg_len,
+                                 size_t units, size_t cps, int chunk_log2, int run_log2,
+                                 float *dst, int grid, int block, cudaStream_t stream);
+int occupancy_blocked(int dtype, bool aligned, int block);
 
 // ---- SHUFFLE_TREE (declared grid-stride order)
 // Block team: grid = segments * G CTAs of Bt threads; CTA (s, b) writes its
@@ -75,7 +86,7 @@ cudaError_t launch_combine(const float *partials, size_t segments, size_t count,
 
 // Resident CTAs per SM of each kernel at a block size (occupancy API);
 // `rows` selects the per-row variant.  0 if the query fails.
-int occupancy_fixed(bool rows, int dtype, int op, bool aligned, int block);
+int occupancy_fixed(bool rows, int dtype, int op, bool aligned, int block, int vrun = 0);
 int occupancy_shuffle(bool rows, int dtype, int op, bool aligned, int block);
 int occupancy_mma(bool rows, int dtype, int op, bool aligned, int R, int block);
 

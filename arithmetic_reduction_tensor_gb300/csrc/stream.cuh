@@ -98,7 +98,11 @@ __device__ __forceinline__ float group_tree(const float (&t)[8], int lane)
 // padded with -0.0.  LEVELS bounds the groups per span (< 2^LEVELS).  For
 // sums of squares the pad's leaf is (-0.0)^2 = +0.0, which is the identity
 // too, since every leaf is then at least +0.0.
-template <int DT, int OP, int LEVELS>
+//
+// VRUN > 0 (sums only): the blocked order with runs of 2^VRUN inputs inside a
+// vector -- each vector's value is vec_runs instead of its balanced tree;
+// the tree above the vectors is the same.
+template <int DT, int OP, int LEVELS, int VRUN = 0>
 struct FixedReducer {
     static constexpr int kDT = DT;
     static constexpr bool kNegZeroPad = true;
@@ -107,8 +111,13 @@ struct FixedReducer {
 
     __device__ __forceinline__ void take(const uint4 (&q)[8])
     {
+        if constexpr (VRUN > 0) {
 #pragma unroll
-        for (int k = 0; k < 8; k++) t[k] = vec_tree<DT, OP>(q[k]);
+            for (int k = 0; k < 8; k++) t[k] = vec_runs<DT, VRUN>(q[k]);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 8; k++) t[k] = vec_tree<DT, OP>(q[k]);
+        }
     }
     __device__ __forceinline__ void reduce(int lane) { tc.push(group_tree(t, lane)); }
     __device__ __forceinline__ float value(int) const { return tc.finish(); }

@@ -21,6 +21,7 @@ namespace {
 using namespace tcr;
 
 constexpr size_t kMaxInputs = (size_t)1 << 40;
+constexpr int kMaxRunLog2 = 16;
 constexpr int kDefaultBlock = 256;
 // GB300: 152 SMs.  Used only by the declared SHUFFLE_TREE team rule (so the
 // declared order is the same on every device) and as the launch-plan SM
@@ -98,7 +99,7 @@ cudaMemPool_t pool_for(int dev)
     return d.pool;
 }
 
-enum Family { kFixedF, kShuffleF, kMmaF };
+enum Family { kFixedF, kShuffleF, kMmaF, kBlockedF };
 
 int occupancy(int dev, Family fam, bool rows, int dtype, int op, bool aligned, int R, int block)
 {
@@ -111,7 +112,8 @@ int occupancy(int dev, Family fam, bool rows, int dtype, int op, bool aligned, i
     int n = 0;
     if (dev >= 0) {
         switch (fam) {
-        case kFixedF: n = occupancy_fixed(rows, dtype, op, aligned, block); break;
+        case kFixedF: n = occupancy_fixed(rows, dtype, op, aligned, block, R); break;
+        case kBlockedF: n = occupancy_blocked(dtype, aligned, block); break;
         case kShuffleF: n = occupancy_shuffle(rows, dtype, op, aligned, block); break;
         case kMmaF: n = occupancy_mma(rows, dtype, op, aligned, R, block); break;
         }
@@ -132,11 +134,14 @@ enum Path {
     kPathShuffleBlock,   // SHUFFLE block team (+ combine if G > 1)
     kPathShuffleRowsWarp, // SHUFFLE warp team, one warp per row
     kPathTmem,           // MMA_CHAIN on tcgen05 (+ combine if units > 1)
-    kPathTmemRows        // MMA_CHAIN rows on tcgen05 (+ combine if chunks > 1)
+    kPathTmemRows,       // MMA_CHAIN rows on tcgen05 (+ combine if chunks > 1)
+    kPathBlocked         // FIXED blocked order, runs longer than a vector (+ combine)
 };
 
 struct Plan {
     int kind, dtype, op, R, block;
+    int run_log2;            // blocked order: log2 run length (0: the plain tree)
+    int vrun;                // runs inside a vector: the warp-stream kernels' variant
     bool aligned;
     Path path;
     size_t segments, seg_len;
@@ -153,6 +158,13 @@ int log2_exact(int v)
     int l = 0;
     while ((1 << l) < v) l++;
     return l;
+}
+
+int ceil_log2_sz(size_t n)
+{
+    int h = 0;
+    while (((size_t)1 << h) < n) h++;
+    return h;
 }
 
 // Default chain length.  The Abstract of arXiv 2001.05585 finds R = 4 or 5
@@ -201,6 +213,8 @@ tcr_status check_mode(const tcr_mode &m, int *block, int *R)
 {
     if (m.kind < TCR_MMA_CHAIN || m.kind > TCR_MMA_CHAIN_TMEM) return TCR_ERR_INVALID_ARG;
     if (m.dtype != TCR_F16 && m.dtype != TCR_BF16 && m.dtype != TCR_F32) return TCR_ERR_INVALID_ARG;
+    if (m.run_log2 < 0 || m.run_log2 > kMaxRunLog2) return TCR_ERR_INVALID_ARG;
+    if (m.run_log2 != 0 && m.kind != TCR_FIXED_ORDER) return TCR_ERR_INVALID_ARG;
     int b = m.block_threads == 0 ? kDefaultBlock : m.block_threads;
     if (b < 32 || b > 1024 || (b & (b - 1)) != 0) return TCR_ERR_INVALID_ARG;
     int r = 0;
@@ -221,8 +235,48 @@ void plan_chunked(Plan &p, int dev, Family fam)
                    log2_exact(p.block / 32);
     p.cps = (p.seg_len + ((size_t)1 << p.chunk_log2) - 1) >> p.chunk_log2;
     p.units = p.segments * p.cps;
-    const size_t resident = (size_t)sm_count(dev) *
-                            (size_t)occupancy(dev, fam, false, p.dtype, p.op, p.aligned, p.R, p.block);
+    const size_t resident =
+        (size_t)sm_count(dev) *
+        (size_t)occupancy(dev, fam, false, p.dtype, p.op, p.aligned,
+                          fam == kFixedF ? p.vrun : p.R, p.block);
+    p.grid = (int)(p.units < resident ? p.units : resident);
+    p.partials = p.cps > 1 ? p.units : 0;
+    p.combine_count = p.cps;
+    p.launches = p.cps > 1 ? 2 : 1;
+}
+
+// The blocked order with runs longer than a vector: a warp's span is a
+// whole number of rounds (32 pieces of one or more runs) and at least 16 KiB (for rows: at least
+// the row, when the row is shorter); CTAs of up to 8 warps, fewer when that
+// leaves too few CTA work units to fill the GPU (the tree above the spans
+// is the same whatever the CTA size).
+void plan_blocked(Plan &p, bool rows_call, int dev)
+{
+    p.path = kPathBlocked;
+    const int sms = sm_count(dev);
+    const int s0 = kWarpSpanBytesLog2 - log2_exact((int)elem_bytes(p.dtype));
+    int span_log2 = s0;
+    if (rows_call && ceil_log2_sz(p.seg_len) < span_log2) span_log2 = ceil_log2_sz(p.seg_len);
+    // a round is 32 pieces of max(run, 8 vectors) inputs
+    const int lv = log2_exact(vector_len(p.dtype));
+    const int piece_log2 = p.run_log2 > lv + 3 ? p.run_log2 : lv + 3;
+    if (span_log2 < piece_log2 + 5) span_log2 = piece_log2 + 5;
+    int w = p.block / 32 < 8 ? p.block / 32 : 8;
+    if (rows_call) {
+        // no more warps than spans in a row
+        const size_t spans = (p.seg_len + ((size_t)1 << span_log2) - 1) >> span_log2;
+        while (w > 1 && (size_t)(w / 2) >= spans) w /= 2;
+    }
+    for (;;) {
+        p.chunk_log2 = span_log2 + log2_exact(w);
+        p.cps = (p.seg_len + ((size_t)1 << p.chunk_log2) - 1) >> p.chunk_log2;
+        p.units = p.segments * p.cps;
+        if (w == 1 || p.units >= (size_t)4 * (size_t)sms) break;
+        w /= 2;
+    }
+    p.block = 32 * w;
+    const size_t resident =
+        (size_t)sms * (size_t)occupancy(dev, kBlockedF, false, p.dtype, kOpSum, p.aligned, 0, p.block);
     p.grid = (int)(p.units < resident ? p.units : resident);
     p.partials = p.cps > 1 ? p.units : 0;
     p.combine_count = p.cps;
@@ -247,6 +301,7 @@ Plan make_plan(size_t segments, size_t seg_len, bool rows_call, const tcr_mode &
     p.aligned = aligned;
     p.segments = segments;
     p.seg_len = seg_len;
+    p.run_log2 = m.kind == TCR_FIXED_ORDER ? m.run_log2 : 0;
     if (segments == 0 || seg_len == 0) {
         p.path = kPathEmpty;
         return p;
@@ -299,7 +354,18 @@ Plan make_plan(size_t segments, size_t seg_len, bool rows_call, const tcr_mode &
         p.launches = p.units > 1 ? 2 : 1;
         return p;
     }
+    if (m.kind == TCR_FIXED_ORDER && m.run_log2 > 1) {
+        // blocked order: runs of at most a vector are the warp stream's
+        // vector leaves (vrun); longer runs have their own kernel
+        if ((1 << m.run_log2) <= vector_len(p.dtype)) {
+            p.vrun = m.run_log2;
+        } else {
+            plan_blocked(p, rows_call, dev);
+            return p;
+        }
+    }
     const Family fam = m.kind == TCR_FIXED_ORDER ? kFixedF : kMmaF;
+    const int occ_r = m.kind == TCR_FIXED_ORDER ? p.vrun : R;
     if (rows_call && seg_len <= kRowsWarpMaxBytes / elem_bytes(p.dtype)) {
         // one warp per row: the CTA size is a launch detail (the result does
         // not depend on it), fixed at kRowsBlock threads
@@ -307,7 +373,7 @@ Plan make_plan(size_t segments, size_t seg_len, bool rows_call, const tcr_mode &
         const size_t warps_per_cta = (size_t)block / 32;
         const size_t need = (segments + warps_per_cta - 1) / warps_per_cta;
         const size_t resident =
-            sms * (size_t)occupancy(dev, fam, true, p.dtype, op, aligned, R, block);
+            sms * (size_t)occupancy(dev, fam, true, p.dtype, op, aligned, occ_r, block);
         p.path = m.kind == TCR_FIXED_ORDER ? kPathFixedRowsWarp : kPathMmaRows;
         p.grid = (int)(need < resident ? need : resident);
         p.launches = 1;
@@ -357,13 +423,17 @@ tcr_status run_plan(const Plan &p, const void *x, float *out, cudaStream_t s, in
     case kPathChunk:
         e = p.kind == TCR_FIXED_ORDER
                 ? launch_fixed_chunk(p.dtype, p.op, p.aligned, x, p.seg_len, p.units, p.cps,
-                                     p.chunk_log2, dst, p.grid, p.block, s)
+                                     p.chunk_log2, dst, p.grid, p.block, s, p.vrun)
                 : launch_mma_chunk(p.dtype, p.op, p.aligned, p.R, x, p.seg_len, p.units, p.cps,
                                    p.chunk_log2, dst, p.grid, p.block, s);
         break;
     case kPathFixedRowsWarp:
         e = launch_fixed_rows_warp(p.dtype, p.op, p.aligned, x, p.segments, p.seg_len, dst,
-                                   p.grid, p.block, s);
+                                   p.grid, p.block, s, p.vrun);
+        break;
+    case kPathBlocked:
+        e = launch_blocked_chunk(p.dtype, p.aligned, x, p.seg_len, p.units, p.cps, p.chunk_log2,
+                                 p.run_log2, dst, p.grid, p.block, s);
         break;
     case kPathMmaRows:
         e = launch_mma_rows(p.dtype, p.op, p.aligned, p.R, x, p.segments, p.seg_len, dst,
@@ -414,6 +484,7 @@ tcr_status reduce_sum_op(const void *x, size_t n, float *out, const tcr_mode &mo
     int block = 0, R = 0;
     tcr_status st = check_common(x, n, out, mode, &block, &R);
     if (st != TCR_OK) return st;
+    if (op != kOpSum && mode.run_log2 != 0) return TCR_ERR_UNSUPPORTED;
     const int dev = current_device();
     if (dev < 0) return TCR_ERR_CUDA;
     const bool aligned = ((uintptr_t)x & 15u) == 0;
@@ -432,12 +503,24 @@ tcr_status reduce_rows_op(const void *x, size_t rows, size_t cols, float *out,
     int block = 0, R = 0;
     tcr_status st = check_common(x, rows * cols, out, mode, &block, &R);
     if (st != TCR_OK) return st;
+    if (op != kOpSum && mode.run_log2 != 0) return TCR_ERR_UNSUPPORTED;
     const int dev = current_device();
     if (dev < 0) return TCR_ERR_CUDA;
     // every row starts 16-byte aligned when x does and a row is whole vectors
     const bool aligned = ((uintptr_t)x & 15u) == 0 && (cols % (size_t)vector_len(mode.dtype)) == 0;
     Plan p = make_plan(rows, cols, true, mode, op, block, R, aligned, dev);
     return run_plan(p, x, out, (cudaStream_t)stream, dev);
+}
+
+// What a fixed-order descriptor's run length does: 0 for the plain tree
+// (runs of one or two inputs), the segment's tree height for one run
+// covering it (the left-to-right sum), else the run length itself.
+int effective_run_log2(const tcr_order_desc *d)
+{
+    int c = d->order == TCR_ORDER_BLOCKED_TREE ? d->run_log2 : 0;
+    const int h = ceil_log2_sz(d->segment_len);
+    if (c > h) c = h;
+    return c <= 1 ? 0 : c;
 }
 
 }  // namespace
@@ -483,9 +566,11 @@ tcr_status tcr_order_descriptor(size_t n, size_t rows, size_t cols, tcr_mode mod
     Plan p = make_plan(segments, seg_len, rows_call, mode, kOpSum, block, R, true, dev);
     std::memset(desc, 0, sizeof *desc);
     desc->kind = mode.kind;
-    desc->order = mode.kind == TCR_SHUFFLE_TREE  ? TCR_ORDER_GRID_STRIDE
-                  : mode.kind == TCR_FIXED_ORDER ? TCR_ORDER_BALANCED_TREE
-                                                 : TCR_ORDER_TENSOR_CORE;
+    desc->order = mode.kind == TCR_SHUFFLE_TREE ? TCR_ORDER_GRID_STRIDE
+                  : mode.kind == TCR_FIXED_ORDER
+                      ? (mode.run_log2 > 0 ? TCR_ORDER_BLOCKED_TREE : TCR_ORDER_BALANCED_TREE)
+                      : TCR_ORDER_TENSOR_CORE;
+    desc->run_log2 = mode.kind == TCR_FIXED_ORDER ? mode.run_log2 : 0;
     desc->segment_len = seg_len;
     desc->segments = segments;
     desc->vector_len = vector_len(mode.dtype);
@@ -497,7 +582,8 @@ tcr_status tcr_order_descriptor(size_t n, size_t rows, size_t cols, tcr_mode mod
     }
     desc->launch_grid = p.grid;
     desc->launch_block = p.path == kPathShuffleBlock ? p.team_threads : p.block;
-    desc->chunk_log2 = (p.path == kPathChunk || p.path == kPathTmem) ? p.chunk_log2 : 0;
+    desc->chunk_log2 =
+        (p.path == kPathChunk || p.path == kPathTmem || p.path == kPathBlocked) ? p.chunk_log2 : 0;
     desc->partials = p.partials;
     desc->launches = p.launches;
     return TCR_OK;
@@ -508,13 +594,17 @@ tcr_status tcr_order_equivalent(const tcr_order_desc *a, const tcr_order_desc *b
 {
     if (!a || !b || !equivalent) return TCR_ERR_INVALID_ARG;
     *equivalent = 0;
-    if (a->kind != b->kind || a->order != b->order || a->segment_len != b->segment_len ||
-        a->dtype != b->dtype || a->vector_len != b->vector_len || a->vector_len <= 0)
+    const bool tree_a = a->order == TCR_ORDER_BALANCED_TREE || a->order == TCR_ORDER_BLOCKED_TREE;
+    const bool tree_b = b->order == TCR_ORDER_BALANCED_TREE || b->order == TCR_ORDER_BLOCKED_TREE;
+    if (a->kind != b->kind || (a->order != b->order && !(tree_a && tree_b)) ||
+        a->segment_len != b->segment_len || a->dtype != b->dtype ||
+        a->vector_len != b->vector_len || a->vector_len <= 0)
         return TCR_OK;
+    if (tree_a) {
+        *equivalent = effective_run_log2(a) == effective_run_log2(b);
+        return TCR_OK;
+    }
     switch (a->order) {
-    case TCR_ORDER_BALANCED_TREE:
-        *equivalent = 1;
-        break;
     case TCR_ORDER_GRID_STRIDE: {
         const size_t nvec = (a->segment_len + (size_t)a->vector_len - 1) / (size_t)a->vector_len;
         const size_t ta = (size_t)a->team_threads * (size_t)a->team_blocks;

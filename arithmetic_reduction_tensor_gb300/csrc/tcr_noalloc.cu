@@ -92,6 +92,8 @@ extern "C" tcr_status tcr_reduce_sum_noalloc(const void *x, size_t n, float *out
         return TCR_ERR_INVALID_ARG;
     const int elem_log2 = mode.dtype == TCR_F32 ? 2 : 1;
     if (n > 0 && (!x || ((uintptr_t)x & ((1u << elem_log2) - 1u)) != 0)) return TCR_ERR_INVALID_ARG;
+    if (mode.run_log2 < 0 || mode.run_log2 > 16) return TCR_ERR_INVALID_ARG;
+    if (mode.run_log2 != 0) return TCR_ERR_UNSUPPORTED;     // the plain tree only
     const int block = mode.block_threads == 0 ? 256 : mode.block_threads;
     if (block < 32 || block > 1024 || (block & (block - 1)) != 0) return TCR_ERR_INVALID_ARG;
     int R = 0;

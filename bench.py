@@ -484,9 +484,10 @@ def profile_arm(args):
 
 def extras_arm(args):
     """Beyond the hot path, one JSON line per call: the sum of squares (2^30
-    sum and 65536 x 4096 rows, every mode) and binary32 inputs (2^29 sum and
+    sum and 65536 x 4096 rows, every mode), binary32 inputs (2^29 sum and
     65536 x 2048 rows -- the same bytes as the 16-bit workload -- every mode,
-    sums and sums of squares)."""
+    sums and sums of squares) and FIXED_ORDER's blocked order (runs of 2^c
+    inputs left to right, then the tree) on the 16-bit workload."""
     import torch
     import arithmetic_reduction_tensor_gb300 as tcr
     from arithmetic_reduction_tensor_gb300 import synth
@@ -515,6 +516,15 @@ def extras_arm(args):
                       lambda m=m: tcr.tcr_reduce_rows(fr, m, out=out)))
         calls.append(("f32_sum_squares/" + k, 4 * n32 + 4,
                       lambda m=m: tcr.tcr_reduce_sum_squares(fs, m, out=out[:1])))
+    # the blocked-sequential-then-tree order (FIXED_ORDER, runs of 2^c)
+    for c in (2, 3, 4, 6, 8, 10):
+        m = tcr.Mode(tcr.FIXED_ORDER, run_log2=c)
+        calls.append((f"blocked_sum/c={c}", 2 * N_SUM + 4,
+                      lambda m=m: tcr.tcr_reduce_sum(xs, m, out=out[:1])))
+    for c in (3, 5, 8):
+        m = tcr.Mode(tcr.FIXED_ORDER, run_log2=c)
+        calls.append((f"blocked_rows/c={c}", 2 * ROWS * COLS + 4 * ROWS,
+                      lambda m=m: tcr.tcr_reduce_rows(xr, m, out=out)))
     for name, nbytes, fn in calls:
         for _ in range(args.warmup):
             fn()

@@ -113,12 +113,26 @@ typedef enum {
  *                  of the declared order; for TCR_FIXED_ORDER it changes
  *                  only speed, never the result.
  *   dtype          tcr_dtype of the inputs.
+ *   run_log2       TCR_FIXED_ORDER sums only (0 for every other call): 0
+ *                  for the balanced tree over the inputs, or c in 1..16 for
+ *                  the blocked-sequential-then-tree order -- runs of 2^c
+ *                  consecutive inputs, each added left to right, then the
+ *                  balanced tree over the run values (-0.0 pad).  c = 1 is
+ *                  the plain tree (a run of two is a pair); c >= log2(n)
+ *                  the plain left-to-right sum.  A second declared order in
+ *                  the sense of "Taming Bitwise Behavior in GPU Kernels with
+ *                  Tensor Core" (arXiv 2609.11356), Abstract, with the run
+ *                  length chosen by the caller.  Each run is a serial chain:
+ *                  the GPU runs n / 2^c of them in parallel, so long runs
+ *                  on short inputs are slow.  Sums of squares with
+ *                  run_log2 != 0 return TCR_ERR_UNSUPPORTED.
  */
 typedef struct {
     int kind;
     int R;
     int block_threads;
     int dtype;
+    int run_log2;
 } tcr_mode;
 
 /*
@@ -192,8 +206,8 @@ TCR_API tcr_status tcr_reduce_rows_sum_squares(const void *x, size_t rows, size_
  * but the partials live in one fixed array of 65536 floats (256 KiB) in
  * device memory, held by every GPU that loads the library until the
  * process exits; no cudaMalloc, cudaFree or other allocating call is made.
- *   - Serves TCR_FIXED_ORDER and TCR_MMA_CHAIN; TCR_SHUFFLE_TREE returns
- *     TCR_ERR_UNSUPPORTED.
+ *   - Serves TCR_FIXED_ORDER (run_log2 = 0) and TCR_MMA_CHAIN;
+ *     TCR_SHUFFLE_TREE and a blocked order return TCR_ERR_UNSUPPORTED.
  *   - n is limited to 65536 chunks of 2^(13 + log2(block_threads / 32))
  *     16-bit inputs (2^32 inputs at the default 256 threads, 2^29 at 32),
  *     half as many binary32 inputs; a larger n returns TCR_ERR_UNSUPPORTED
@@ -214,7 +228,8 @@ TCR_API tcr_status tcr_reduce_sum_noalloc(const void *x, size_t n, float *out, t
 typedef enum {
     TCR_ORDER_TENSOR_CORE = 0,      /* MMA_CHAIN: inner order is the tensor core's */
     TCR_ORDER_GRID_STRIDE = 1,      /* SHUFFLE_TREE: see tcr_order_desc */
-    TCR_ORDER_BALANCED_TREE = 2     /* FIXED_ORDER: balanced tree over index order */
+    TCR_ORDER_BALANCED_TREE = 2,    /* FIXED_ORDER: balanced tree over index order */
+    TCR_ORDER_BLOCKED_TREE = 3      /* FIXED_ORDER, run_log2 > 0: runs left to right, then the tree */
 } tcr_order;
 
 /*
@@ -251,6 +266,8 @@ typedef enum {
  *                    and the number of kernel launches.  For FIXED_ORDER they
  *                    never change the result.
  *   dtype            tcr_dtype of the inputs (mode.dtype).
+ *   run_log2         TCR_ORDER_BLOCKED_TREE: log2 of the run length (as given
+ *                    in the mode); 0 otherwise.
  */
 typedef struct {
     int kind;
@@ -268,6 +285,7 @@ typedef struct {
     size_t partials;
     int launches;
     int dtype;
+    int run_log2;
 } tcr_order_desc;
 
 /*
@@ -287,7 +305,11 @@ TCR_API tcr_status tcr_order_descriptor(size_t n, size_t rows, size_t cols, tcr_
  * bit-equivalence classes of "Taming Bitwise Behavior in GPU Kernels with
  * Tensor Core" (arXiv 2609.11356), Abstract (an autotuner restricted to one
  * class).  Same kind, dtype and segment_len are required; then
- *   TCR_FIXED_ORDER   always equivalent (the tree depends on the length only);
+ *   TCR_FIXED_ORDER   equivalent when the run lengths agree once reduced to
+ *                     what they do: runs of 1 or 2 inputs are the plain tree,
+ *                     runs of at least the segment length the plain
+ *                     left-to-right sum (the tree depends on the length and
+ *                     the run length only);
  *   TCR_SHUFFLE_TREE  the block and grid trees are both balanced over power-
  *                     of-two warp counts, so together they are one balanced
  *                     tree over warp index: the order is fixed by the team

@@ -18,6 +18,11 @@ def vector_len(dtype: int = 0) -> int:
     return 4 if dtype == F32 else 8
 
 
+def span_log2(dtype: int = 0) -> int:
+    """log2 inputs of a 16 KiB warp span (the tree kernels' work per warp)."""
+    return 12 if dtype == F32 else 13
+
+
 def shuffle_team(L: int, block: int = 0, dtype: int = 0) -> tuple[int, int]:
     B = block or DEFAULT_BLOCK
     nvec = math.ceil(L / vector_len(dtype))

@@ -179,3 +179,47 @@ def test_python_binding_fails_loudly_without_cuda_tensors():
     torch = pytest.importorskip("torch")
     with pytest.raises(ValueError):
         tcr.tcr_reduce_sum(torch.zeros(4, dtype=torch.float16), tcr.Mode(tcr.FIXED_ORDER))
+
+
+def test_blocked_order_arguments(lib):
+    ok = tcr.Mode(tcr.FIXED_ORDER, run_log2=4)
+    d = tcr.tcr_order_desc()
+    assert lib.tcr_order_descriptor(1000, 0, 0, ok, ctypes.byref(d)) == tcr.OK
+    for bad in (tcr.Mode(tcr.FIXED_ORDER, run_log2=17), tcr.Mode(tcr.FIXED_ORDER, run_log2=-1),
+                tcr.Mode(tcr.MMA_CHAIN, run_log2=3), tcr.Mode(tcr.SHUFFLE_TREE, run_log2=2)):
+        assert lib.tcr_order_descriptor(1000, 0, 0, bad, ctypes.byref(d)) == tcr.ERR_INVALID_ARG
+        assert lib.tcr_reduce_sum(FAKE, 10, FAKE, bad, None) == tcr.ERR_INVALID_ARG
+    # sums of squares have no blocked order: refused before any GPU work
+    assert lib.tcr_reduce_sum_squares(FAKE, 10, FAKE, ok, None) == tcr.ERR_UNSUPPORTED
+    assert lib.tcr_reduce_rows_sum_squares(FAKE, 3, 10, FAKE, ok, None) == tcr.ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("dtype", [tcr.F16, tcr.F32])
+def test_blocked_order_descriptors(lib, dtype):
+    V = spec.vector_len(dtype)
+    for c in range(0, 17):
+        d = tcr.tcr_order_descriptor(n=1 << 28, mode=tcr.Mode(tcr.FIXED_ORDER, run_log2=c, dtype=dtype))
+        assert d["order"] == (tcr.ORDER_BLOCKED_TREE if c else tcr.ORDER_BALANCED_TREE)
+        assert d["run_log2"] == c
+        if (1 << c) > V:
+            # a warp span holds whole rounds of 32 runs: chunk >= 32 runs
+            assert d["chunk_log2"] >= c + 5
+            assert d["launch_block"] <= 256
+        else:
+            assert d["chunk_log2"] == spec.span_log2(dtype) + 3     # the tree's chunk at 256 threads
+        assert d["partials"] == -(-(1 << 28) // (1 << d["chunk_log2"]))
+
+
+def test_blocked_order_equivalence(lib):
+    def m(c, **kw):
+        return {"n": 100_000, "mode": tcr.Mode(tcr.FIXED_ORDER, run_log2=c, **kw)}
+    assert tcr.tcr_order_equivalent(m(0), m(1))                  # runs of two are the pairs
+    assert not tcr.tcr_order_equivalent(m(0), m(2))
+    assert not tcr.tcr_order_equivalent(m(5), m(6))
+    assert tcr.tcr_order_equivalent(m(5), m(5, block_threads=32))    # the CTA size never matters
+    assert tcr.tcr_order_equivalent(m(16), m(16, block_threads=1024))
+    # one run covering the segment (2^17 > 100 000): every longer run is the same sum
+    short = {"n": 1000, "mode": tcr.Mode(tcr.FIXED_ORDER, run_log2=10)}
+    longer = {"n": 1000, "mode": tcr.Mode(tcr.FIXED_ORDER, run_log2=16)}
+    assert tcr.tcr_order_equivalent(short, longer)
+    assert not tcr.tcr_order_equivalent(short, {"n": 1000, "mode": tcr.Mode(tcr.FIXED_ORDER, run_log2=9)})

@@ -93,3 +93,10 @@ def test_no_alloc_binary32(lib, kind, n):
     assert o.cpu().numpy().tobytes() == ref.cpu().numpy().tobytes()
     if kind == tcr.FIXED_ORDER:
         assert o.cpu().numpy()[0] == oracle.fixed_order(bits, tcr.F32)
+
+
+def test_no_alloc_refuses_the_blocked_order(lib):
+    x = torch.zeros(100, dtype=torch.float16, device="cuda")
+    o = torch.zeros(1, device="cuda")
+    m = tcr.Mode(tcr.FIXED_ORDER, run_log2=4)
+    assert lib.tcr_reduce_sum_noalloc(x.data_ptr(), 100, o.data_ptr(), m, None) == tcr.ERR_UNSUPPORTED
