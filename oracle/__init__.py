@@ -22,6 +22,8 @@ Functions (sources are cited in ``tcr_oracle.c``):
 ``blocked_order``      runs of 2^c inputs added left to right, then the
                        balanced tree over the runs (a second declared order
                        of the fixed-order mode).
+``mean_var``           per-row mean and variance from a row's sum and sum
+                       of squares (declared binary32 formula).
 ``*_sq``, ``exact_sum_squares``
                        the same over the leaves x_i^2 (sum of squares).
 ``*_rows``             the same, one result per row.
@@ -97,6 +99,8 @@ def _load():
             lib.oracle_blocked_order_f32.restype = ctypes.c_float
             lib.oracle_blocked_order_rows_f32.argtypes = [u16p, sz, sz, i, i, i, f32p]
             lib.oracle_blocked_order_rows_f32.restype = None
+            lib.oracle_mean_var_f32.argtypes = [f32p, f32p, sz, sz, f32p, f32p]
+            lib.oracle_mean_var_f32.restype = None
             lib.oracle_leaves_f32.argtypes = [u16p, sz, i, f32p]
             lib.oracle_leaves_f32.restype = None
             _lib = lib
@@ -226,6 +230,19 @@ def blocked_order_rows(x, dtype: int, run_log2: int, threads: int | None = None)
                                           threads or default_threads(),
                                           out.ctypes.data_as(ctypes.POINTER(ctypes.c_float)))
     return out
+
+
+def mean_var(s1, s2, cols: int) -> tuple[np.ndarray, np.ndarray]:
+    """Per-row mean and variance from the row sums s1 and sums of squares s2
+    (binary32, the declared formula of ``oracle_mean_var_f32``)."""
+    a = np.ascontiguousarray(s1, np.float32).reshape(-1)
+    b = np.ascontiguousarray(s2, np.float32).reshape(-1)
+    m = np.empty(a.size, np.float32)
+    v = np.empty(a.size, np.float32)
+    fp = ctypes.POINTER(ctypes.c_float)
+    _load().oracle_mean_var_f32(a.ctypes.data_as(fp), b.ctypes.data_as(fp), a.size, cols,
+                                m.ctypes.data_as(fp), v.ctypes.data_as(fp))
+    return m, v
 
 
 def leaves(x, dtype: int) -> np.ndarray:

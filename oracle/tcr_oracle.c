@@ -581,6 +581,27 @@ void oracle_shuffle_tree_rows_f32(const void *x, size_t rows, size_t cols, int d
         out[r] = shuffle_tree_any(raw_ptr(x, r * cols, dtype), cols, dtype, squares, Bt, G, 1);
 }
 
+/* ------------------------------------------------------------------ */
+/* Mean and variance of rows from their sum S1 and sum of squares S2 (the
+ * cascaded reductions named by the "RedFuser" title in the first page's list
+ * of work built on the method: two reductions of one row in one pass).  The
+ * formula, in binary32 with one rounding to nearest per operation:
+ *   m = S1 / n,  q = S2 / n,  v = q - m * m,  var = v < 0 ? +0 : v
+ * (n = cols as a binary32; a negative v can only come from rounding). */
+void oracle_mean_var_f32(const float *s1, const float *s2, size_t rows, size_t cols, float *mean,
+                         float *var)
+{
+    const float n = (float)cols;
+    for (size_t r = 0; r < rows; r++) {
+        const float m = s1[r] / n;
+        const float q = s2[r] / n;
+        const float mm = m * m;
+        const float v = q - mm;
+        mean[r] = m;
+        var[r] = v < 0.0f ? 0.0f : v;
+    }
+}
+
 /* Exact binary32 value of each input (used by the tests to compare the
  * decoder with independent conversions). */
 void oracle_leaves_f32(const void *x, size_t n, int dtype, float *out)

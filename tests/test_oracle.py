@@ -633,3 +633,38 @@ def test_blocked_order_rows_and_degenerate():
     negz = oracle.blocked_order(np.full(9, 0x8000, np.uint16), F16, 2)
     assert negz.tobytes() == np.float32(-0.0).tobytes()
     assert np.isnan(oracle.blocked_order(np.array([0x3C00, 0x7E00], np.uint16), F16, 1))
+
+
+# ---------------------------------------------------------------- mean / variance
+
+def test_mean_var_formula_against_float64():
+    # normal rows: the binary32 formula is within a few ulps of the float64
+    # mean and variance of the same sums
+    x = synth.generate(300 * 4096, "normal", F16, seed=53).reshape(300, 4096)
+    s1 = oracle.fixed_order_rows(x, F16)
+    s2 = oracle.fixed_order_rows(x, F16, squares=True)
+    m, v = oracle.mean_var(s1, s2, 4096)
+    m64 = s1.astype(np.float64) / 4096
+    v64 = s2.astype(np.float64) / 4096 - m64 * m64
+    assert np.all(np.abs(m - m64) <= 2.0 ** -23 * np.abs(m64) + 1e-30)
+    assert np.all(np.abs(v - v64) <= 2.0 ** -22 * (s2 / 4096) + 1e-30)
+    # and the float64 statistics of the data themselves, within the sums' rounding
+    xf = np.asarray(np_leaves(x.reshape(-1), F16), np.float64).reshape(300, 4096)
+    assert np.allclose(m, xf.mean(axis=1), rtol=0, atol=1e-5)
+    assert np.allclose(v, xf.var(axis=1), rtol=1e-5, atol=1e-6)
+
+
+def test_mean_var_special_cases():
+    # constant rows: variance exactly 0; [a, b]: ((a + b)/2, ((a - b)/2)^2)
+    s1 = np.array([7 * 5.0, 3.0 + 5.0, 0.0], np.float32)
+    s2 = np.array([7 * 25.0, 9.0 + 25.0, 0.0], np.float32)
+    m, v = oracle.mean_var(s1[:1], s2[:1], 7)
+    assert m[0] == 5.0 and v[0] == 0.0
+    m, v = oracle.mean_var(s1[1:2], s2[1:2], 2)
+    assert m[0] == 4.0 and v[0] == 1.0
+    # cancellation that would go negative is clamped to +0
+    m, v = oracle.mean_var(np.array([3.0000002], np.float32), np.array([3.0], np.float32), 3)
+    assert v[0] == 0.0 and np.signbit(v[0]) == False
+    # no inputs: 0 / 0
+    m, v = oracle.mean_var(np.zeros(1, np.float32), np.zeros(1, np.float32), 0)
+    assert np.isnan(m[0]) and np.isnan(v[0])
