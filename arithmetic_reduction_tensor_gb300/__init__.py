@@ -28,6 +28,7 @@ __all__ = [
     "ORDER_TENSOR_CORE", "ORDER_GRID_STRIDE", "ORDER_BALANCED_TREE", "ORDER_BLOCKED_TREE",
     "tcr_mode", "tcr_order_desc", "Mode", "TcrError", "c_api",
     "tcr_reduce_sum", "tcr_reduce_rows", "tcr_reduce_sum_squares", "tcr_reduce_rows_sum_squares",
+    "tcr_reduce_rows_moments", "tcr_reduce_rows_mean_var",
     "tcr_order_descriptor", "tcr_order_equivalent", "tcr_status_string", "tcr_device_faults",
     "FAULT_PIPELINE_WAIT",
 ]
@@ -104,6 +105,10 @@ def c_api() -> ctypes.CDLL:
             lib.tcr_reduce_sum_squares.restype = ctypes.c_int
             lib.tcr_reduce_rows_sum_squares.argtypes = [vp, sz, sz, vp, tcr_mode, vp]
             lib.tcr_reduce_rows_sum_squares.restype = ctypes.c_int
+            lib.tcr_reduce_rows_moments.argtypes = [vp, sz, sz, vp, vp, tcr_mode, vp]
+            lib.tcr_reduce_rows_moments.restype = ctypes.c_int
+            lib.tcr_reduce_rows_mean_var.argtypes = [vp, sz, sz, vp, vp, tcr_mode, vp]
+            lib.tcr_reduce_rows_mean_var.restype = ctypes.c_int
             lib.tcr_order_descriptor.argtypes = [sz, sz, sz, tcr_mode, ctypes.POINTER(tcr_order_desc)]
             lib.tcr_order_descriptor.restype = ctypes.c_int
             lib.tcr_order_equivalent.argtypes = [ctypes.POINTER(tcr_order_desc),
@@ -224,6 +229,35 @@ def tcr_reduce_sum_squares(x, mode: tcr_mode, out=None, stream=None):
 def tcr_reduce_rows_sum_squares(x, mode: tcr_mode, out=None, stream=None):
     """out[r] = sum of the squares of row r (``tcr_reduce_rows_sum_squares``)."""
     return _rows_call("tcr_reduce_rows_sum_squares", x, mode, out, stream)
+
+
+def _rows_pair_call(name, x, mode, out_a, out_b, stream):
+    import torch
+    if not x.is_cuda or not x.is_contiguous() or x.dim() != 2:
+        raise ValueError("x must be a contiguous 2-D CUDA tensor")
+    rows, cols = x.shape
+    m = tcr_mode(mode.kind, mode.R, mode.block_threads, _dtype_code(x, mode), mode.run_log2)
+    out_a = _check_out(out_a, x.device, rows)
+    out_b = _check_out(out_b, x.device, rows)
+    with torch.cuda.device(x.device):
+        st = getattr(c_api(), name)(x.data_ptr() if x.numel() else None, rows, cols,
+                                    out_a.data_ptr(), out_b.data_ptr(), m,
+                                    _stream_handle(x.device, stream))
+    if st != OK:
+        raise TcrError(st, name)
+    return (out_a[:rows], out_b[:rows]) if rows else (out_a[:0], out_b[:0])
+
+
+def tcr_reduce_rows_moments(x, mode: tcr_mode, sums=None, sums_of_squares=None, stream=None):
+    """(sums, sums of squares) of the rows of ``x`` in one pass
+    (``tcr_reduce_rows_moments``)."""
+    return _rows_pair_call("tcr_reduce_rows_moments", x, mode, sums, sums_of_squares, stream)
+
+
+def tcr_reduce_rows_mean_var(x, mode: tcr_mode, mean=None, var=None, stream=None):
+    """(mean, population variance) of the rows of ``x`` in one pass
+    (``tcr_reduce_rows_mean_var``)."""
+    return _rows_pair_call("tcr_reduce_rows_mean_var", x, mode, mean, var, stream)
 
 
 def _descriptor(n, rows, cols, mode) -> tcr_order_desc:

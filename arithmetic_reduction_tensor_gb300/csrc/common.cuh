@@ -295,6 +295,62 @@ __device__ __forceinline__ float vec_seq_add(float run, uint4 q)
     }
 }
 
+// Both vector trees at once -- of the leaves and of their squares -- each
+// leaf unpacked once, in one asm statement per vector (the values are those
+// of vec_tree<DT, kOpSum> and vec_tree<DT, kOpSquares>, operation for
+// operation).
+template <int DT>
+__device__ __forceinline__ void vec_tree_pair(uint4 q, float &ts, float &tq)
+{
+    if constexpr (DT == kF32) {
+        asm("{\n\t.reg .f32 a, b, c, d;\n\t"
+            "add.rn.f32 a, %2, %3;\n\t"
+            "add.rn.f32 b, %4, %5;\n\t"
+            "add.rn.f32 %0, a, b;\n\t"
+            "mul.rn.f32 a, %2, %2;\n\t"
+            "mul.rn.f32 b, %3, %3;\n\t"
+            "add.rn.f32 c, a, b;\n\t"
+            "mul.rn.f32 a, %4, %4;\n\t"
+            "mul.rn.f32 b, %5, %5;\n\t"
+            "add.rn.f32 d, a, b;\n\t"
+            "add.rn.f32 %1, c, d;\n\t}"
+            : "=&f"(ts), "=&f"(tq)
+            : "r"(q.x), "r"(q.y), "r"(q.z), "r"(q.w));
+    } else {
+        // per word i: s_i = lo + hi, r_i = lo*lo + hi*hi; then
+        // ts = (s0 + s1) + (s2 + s3), tq = (r0 + r1) + (r2 + r3)
+#define TCR_UNPACK_F16(W) "mov.b32 {l, h}, " W ";\n\tcvt.f32.f16 lo, l;\n\tcvt.f32.f16 hi, h;\n\t"
+#define TCR_UNPACK_BF16(W) "shl.b32 lo, " W ", 16;\n\tand.b32 hi, " W ", 0xffff0000;\n\t"
+#define TCR_PAIR_STEP(S, R) \
+    "add.rn.f32 " S ", lo, hi;\n\tmul.rn.f32 lo, lo, lo;\n\tmul.rn.f32 hi, hi, hi;\n\t" \
+    "add.rn.f32 " R ", lo, hi;\n\t"
+        if constexpr (DT == kF16) {
+            asm("{\n\t.reg .b16 l, h;\n\t.reg .f32 lo, hi, s0, s1, s2, s3, r0, r1, r2, r3;\n\t"
+                TCR_UNPACK_F16("%2") TCR_PAIR_STEP("s0", "r0")
+                TCR_UNPACK_F16("%3") TCR_PAIR_STEP("s1", "r1")
+                TCR_UNPACK_F16("%4") TCR_PAIR_STEP("s2", "r2")
+                TCR_UNPACK_F16("%5") TCR_PAIR_STEP("s3", "r3")
+                "add.rn.f32 s0, s0, s1;\n\tadd.rn.f32 s2, s2, s3;\n\tadd.rn.f32 %0, s0, s2;\n\t"
+                "add.rn.f32 r0, r0, r1;\n\tadd.rn.f32 r2, r2, r3;\n\tadd.rn.f32 %1, r0, r2;\n\t}"
+                : "=&f"(ts), "=&f"(tq)
+                : "r"(q.x), "r"(q.y), "r"(q.z), "r"(q.w));
+        } else {
+            asm("{\n\t.reg .f32 lo, hi, s0, s1, s2, s3, r0, r1, r2, r3;\n\t"
+                TCR_UNPACK_BF16("%2") TCR_PAIR_STEP("s0", "r0")
+                TCR_UNPACK_BF16("%3") TCR_PAIR_STEP("s1", "r1")
+                TCR_UNPACK_BF16("%4") TCR_PAIR_STEP("s2", "r2")
+                TCR_UNPACK_BF16("%5") TCR_PAIR_STEP("s3", "r3")
+                "add.rn.f32 s0, s0, s1;\n\tadd.rn.f32 s2, s2, s3;\n\tadd.rn.f32 %0, s0, s2;\n\t"
+                "add.rn.f32 r0, r0, r1;\n\tadd.rn.f32 r2, r2, r3;\n\tadd.rn.f32 %1, r0, r2;\n\t}"
+                : "=&f"(ts), "=&f"(tq)
+                : "r"(q.x), "r"(q.y), "r"(q.z), "r"(q.w));
+        }
+#undef TCR_UNPACK_F16
+#undef TCR_UNPACK_BF16
+#undef TCR_PAIR_STEP
+    }
+}
+
 // ---------------------------------------------------------------- trees
 
 // Binary counter over a sequence of equal-height subtree values pushed in
@@ -398,6 +454,20 @@ __device__ __forceinline__ void mma_ab(float &d0, float &d1, float &d2, float &d
             : "+f"(d0), "+f"(d1), "+f"(d2), "+f"(d3)
             : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
     }
+}
+
+// ---------------------------------------------------------------- moments
+
+// Mean and variance of n inputs from their sum s1 and sum of squares s2, in
+// binary32 with one rounding to nearest per operation:
+// m = s1 / n, v = s2 / n - m * m, a negative v (rounding only) becomes +0.
+__device__ __forceinline__ void mean_var_of(float s1, float s2, size_t n, float &m, float &v)
+{
+    const float nf = __ull2float_rn((unsigned long long)n);
+    m = __fdiv_rn(s1, nf);
+    const float q = __fdiv_rn(s2, nf);
+    v = __fsub_rn(q, __fmul_rn(m, m));
+    if (v < 0.0f) v = 0.0f;
 }
 
 // ---------------------------------------------------------------- PDL

@@ -18,16 +18,9 @@
 // a genuine contraction, two MMAs per tile.  Binary32 inputs are split
 // exactly into three bfloat16 parts on the CUDA cores and the parts summed
 // on the tensor cores, three MMAs per 256 inputs (MmaSplitReducer).
-#include <type_traits>
-
 #include "stream.cuh"
 
 namespace tcr {
-
-template <int DT, int R, int OP>
-using MmaRed = typename std::conditional<
-    DT == kF32, MmaSplitReducer<R, OP>,
-    typename std::conditional<OP == kOpSquares, MmaSqReducer<DT, R>, MmaReducer<DT, R>>::type>::type;
 
 template <int DT, int R, int OP, bool ALIGNED>
 __global__ void __launch_bounds__(1024)

@@ -78,6 +78,32 @@ cudaError_t read_device_faults(unsigned int *flags, bool clear);
 size_t tmem_rows_chunks(size_t cols);
 size_t tmem_rows_units(size_t rows, size_t cols);
 
+// ---- sums and sums of squares in one pass (rows; the mean/variance calls)
+// family: which mode's policies run side by side
+constexpr int kPairFixed = 0, kPairShuffle = 1, kPairMma = 2;
+// One warp per row (rows <= kRowsWarpMaxBytes): out_a[r], out_b[r] = the
+// row's sum and sum of squares, or (mean_var != 0) its mean and variance.
+cudaError_t launch_rows_pair(int family, int dtype, bool aligned, int R, const void *x, size_t rows,
+                             size_t cols, float *out_a, float *out_b, int mean_var, int grid,
+                             int block, cudaStream_t stream);
+cudaError_t launch_mma_rows_pair(int dtype, bool aligned, int R, const void *x, size_t rows,
+                                 size_t cols, float *out_a, float *out_b, int mean_var, int grid,
+                                 int block, cudaStream_t stream);
+// Chunked (FIXED, MMA): dst_a[u], dst_b[u] = work unit u's two partials.
+cudaError_t launch_chunk_pair(int family, int dtype, bool aligned, int R, const void *x,
+                              size_t seg_len, size_t units, size_t cps, int chunk_log2,
+                              float *dst_a, float *dst_b, int grid, int block, cudaStream_t stream);
+cudaError_t launch_mma_chunk_pair(int dtype, bool aligned, int R, const void *x, size_t seg_len,
+                                  size_t units, size_t cps, int chunk_log2, float *dst_a,
+                                  float *dst_b, int grid, int block, cudaStream_t stream);
+// SHUFFLE_TREE block team: CTA (s, b) writes its two block values.
+cudaError_t launch_shuffle_block_pair(int dtype, bool aligned, const void *x, size_t seg_len,
+                                      size_t segments, int G, float *dst_a, float *dst_b, int block,
+                                      cudaStream_t stream);
+// mean[r], var[r] from s1[r], s2[r] (waits for the producing launch).
+cudaError_t launch_mean_var(const float *s1, const float *s2, size_t rows, size_t cols, float *mean,
+                            float *var, cudaStream_t stream);
+
 // ---- combine: out[s] = balanced tree over partials[s*count .. s*count+count-1]
 // padded with -0.0; one CTA of 1024 threads per segment, or one thread per
 // segment when count is small (the same tree either way).

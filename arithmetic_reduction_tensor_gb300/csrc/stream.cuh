@@ -20,6 +20,8 @@
 // the next group's loads are in flight.
 #pragma once
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -318,6 +320,100 @@ struct MmaSplitReducer {
     }
 };
 
+// FIXED_ORDER, sum and sum of squares side by side (each leaf unpacked
+// once): the values of FixedReducer<DT, kOpSum> and <DT, kOpSquares>.
+template <int DT, int LEVELS>
+struct FixedPairReducer {
+    static constexpr int kDT = DT;
+    static constexpr bool kNegZeroPad = true;
+    TreeCounter<LEVELS> ca, cb;
+    float ta[8], tb[8];
+
+    __device__ __forceinline__ void take(const uint4 (&q)[8])
+    {
+#pragma unroll
+        for (int k = 0; k < 8; k++) vec_tree_pair<DT>(q[k], ta[k], tb[k]);
+    }
+    __device__ __forceinline__ void reduce(int lane)
+    {
+        ca.push(group_tree(ta, lane));
+        cb.push(group_tree(tb, lane));
+    }
+    __device__ __forceinline__ void value2(int, float &va, float &vb) const
+    {
+        va = ca.finish();
+        vb = cb.finish();
+    }
+};
+
+// SHUFFLE_TREE one-warp team, sum and sum of squares side by side.
+template <int DT>
+struct ShufflePairReducer {
+    static constexpr int kDT = DT;
+    static constexpr bool kNegZeroPad = true;
+    float acc_a = -0.0f, acc_b = -0.0f;
+    float ta[8], tb[8];
+
+    __device__ __forceinline__ void take(const uint4 (&q)[8])
+    {
+#pragma unroll
+        for (int k = 0; k < 8; k++) vec_tree_pair<DT>(q[k], ta[k], tb[k]);
+    }
+    __device__ __forceinline__ void reduce(int)
+    {
+#pragma unroll
+        for (int k = 0; k < 8; k++) {
+            acc_a = __fadd_rn(acc_a, ta[k]);
+            acc_b = __fadd_rn(acc_b, tb[k]);
+        }
+    }
+    __device__ __forceinline__ void value2(int, float &va, float &vb) const
+    {
+        float a = acc_a, b = acc_b;
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) {
+            a = __fadd_rn(a, __shfl_xor_sync(kFull, a, off));
+            b = __fadd_rn(b, __shfl_xor_sync(kFull, b, off));
+        }
+        va = a;
+        vb = b;
+    }
+};
+
+// The MMA_CHAIN policy of an input type and leaf operation.
+template <int DT, int R, int OP>
+using MmaRed = typename std::conditional<
+    DT == kF32, MmaSplitReducer<R, OP>,
+    typename std::conditional<OP == kOpSquares, MmaSqReducer<DT, R>, MmaReducer<DT, R>>::type>::type;
+
+// Two reductions of the same inputs in one pass -- a sum and a sum of
+// squares: both policies take every group, and their values come out
+// together.  Each value is the one its policy gives alone, bit for bit.
+template <class A, class B>
+struct PairReducer {
+    static_assert(A::kDT == B::kDT && A::kNegZeroPad == B::kNegZeroPad, "pair of unlike streams");
+    static constexpr int kDT = A::kDT;
+    static constexpr bool kNegZeroPad = A::kNegZeroPad;
+    A a;
+    B b;
+
+    __device__ __forceinline__ void take(const uint4 (&q)[8])
+    {
+        a.take(q);
+        b.take(q);
+    }
+    __device__ __forceinline__ void reduce(int lane)
+    {
+        a.reduce(lane);
+        b.reduce(lane);
+    }
+    __device__ __forceinline__ void value2(int lane, float &va, float &vb)
+    {
+        va = a.value(lane);
+        vb = b.value(lane);
+    }
+};
+
 // ---------------------------------------------------------------- kernels
 
 // Chunked: CTA work unit u = (segment u / cps, chunk u % cps); the chunk of
@@ -420,6 +516,104 @@ __device__ __forceinline__ void rows_body(const void *__restrict__ xv, size_t ro
             }
             const float v = red.value(lane);
             if (lane == 0) out[r] = v;
+            if (!has_next) break;
+            r = nr;
+        }
+    }
+}
+
+// ---------------------------------------------------------------- pairs
+
+// chunk_body for a PairReducer: dst_a[u], dst_b[u] are the chunk's two values.
+template <class Red, bool ALIGNED>
+__device__ __forceinline__ void chunk_pair_body(const void *__restrict__ xv, size_t seg_len,
+                                                size_t units, size_t cps, int chunk_log2,
+                                                float *__restrict__ dst_a,
+                                                float *__restrict__ dst_b)
+{
+    constexpr int DT = Red::kDT;
+    constexpr bool NZ = Red::kNegZeroPad;
+    using T = typename Elem<DT>::T;
+    const T *__restrict__ x = static_cast<const T *>(xv);
+    __shared__ float warp_val[2][32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    constexpr size_t span = span_len<DT>();
+    constexpr int ngroups = (int)(span / group_len<DT>());
+    for (size_t u = blockIdx.x; u < units; u += gridDim.x) {
+        const size_t s = u / cps;
+        const T *seg = x + s * seg_len;
+        const size_t base = ((u - s * cps) << chunk_log2) + (size_t)warp * span;
+        uint4 q[8];
+        load_group<DT, ALIGNED, NZ>(q, seg, seg_len, base, lane);
+        Red red;
+#pragma unroll 1
+        for (int g = 0; g < ngroups; g++) {
+            red.take(q);
+            if (g + 1 < ngroups)
+                load_group<DT, ALIGNED, NZ>(q, seg, seg_len, base + (size_t)(g + 1) * group_len<DT>(),
+                                            lane);
+            red.reduce(lane);
+        }
+        float va, vb;
+        red.value2(lane, va, vb);
+        if (lane == 0) {
+            warp_val[0][warp] = va;
+            warp_val[1][warp] = vb;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            const float a = warp_tree_lane_order(lane < nwarps ? warp_val[0][lane] : -0.0f);
+            const float b = warp_tree_lane_order(lane < nwarps ? warp_val[1][lane] : -0.0f);
+            if (lane == 0) {
+                dst_a[u] = a;
+                dst_b[u] = b;
+            }
+        }
+        __syncthreads();
+    }
+    pdl_launch_dependents();
+}
+
+// rows_body for a PairReducer: out_a[r], out_b[r] are the row's two values,
+// or (mean_var) the row's mean and variance computed from them.  The next
+// row's first group is loaded while the current row's last one is reduced.
+template <class Red, bool ALIGNED>
+__device__ __forceinline__ void rows_pair_body(const void *__restrict__ xv, size_t rows,
+                                               size_t cols, float *__restrict__ out_a,
+                                               float *__restrict__ out_b, int mean_var)
+{
+    constexpr int DT = Red::kDT;
+    constexpr bool NZ = Red::kNegZeroPad;
+    using T = typename Elem<DT>::T;
+    const T *__restrict__ x = static_cast<const T *>(xv);
+    const int lane = threadIdx.x & 31;
+    const size_t nw = ((size_t)gridDim.x * blockDim.x) >> 5;
+    size_t r = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    constexpr size_t G = group_len<DT>();
+    const size_t ngroups = (cols + G - 1) / G;
+    if (r < rows && ngroups > 0) {
+        uint4 q[8];
+        load_group<DT, ALIGNED, NZ>(q, x + r * cols, cols, 0, lane);
+        for (;;) {
+            const size_t nr = r + nw;
+            const bool has_next = nr < rows;
+            Red red;
+#pragma unroll 1
+            for (size_t g = 0; g < ngroups; g++) {
+                red.take(q);
+                if (g + 1 < ngroups)
+                    load_group<DT, ALIGNED, NZ>(q, x + r * cols, cols, (g + 1) * G, lane);
+                else if (has_next)
+                    load_group<DT, ALIGNED, NZ>(q, x + nr * cols, cols, 0, lane);
+                red.reduce(lane);
+            }
+            float va, vb;
+            red.value2(lane, va, vb);
+            if (lane == 0) {
+                if (mean_var) mean_var_of(va, vb, cols, va, vb);
+                out_a[r] = va;
+                out_b[r] = vb;
+            }
             if (!has_next) break;
             r = nr;
         }

@@ -523,6 +523,86 @@ int effective_run_log2(const tcr_order_desc *d)
     return c <= 1 ? 0 : c;
 }
 
+// The sum and sum of squares of every row in one pass (mean_var == 0:
+// out_a = sums, out_b = sums of squares) or their mean and variance.
+tcr_status run_pair_plan(const Plan &p, const void *x, float *out_a, float *out_b, int mean_var,
+                         cudaStream_t s, int dev)
+{
+    if (p.path == kPathEmpty) {
+        if (fault_injected("launch")) return TCR_ERR_CUDA;
+        // no inputs: sums +0.0; mean and variance 0 / 0 (NaN)
+        const int byte = mean_var ? 0xff : 0;
+        if (cudaMemsetAsync(out_a, byte, p.segments * sizeof(float), s) != cudaSuccess ||
+            cudaMemsetAsync(out_b, byte, p.segments * sizeof(float), s) != cudaSuccess)
+            return TCR_ERR_CUDA;
+        return TCR_OK;
+    }
+    const int family = p.kind == TCR_FIXED_ORDER ? kPairFixed
+                       : p.kind == TCR_SHUFFLE_TREE ? kPairShuffle
+                                                    : kPairMma;
+    if (p.path == kPathFixedRowsWarp || p.path == kPathMmaRows || p.path == kPathShuffleRowsWarp) {
+        if (fault_injected("launch")) return TCR_ERR_CUDA;
+        return launch_rows_pair(family, p.dtype, p.aligned, p.R, x, p.segments, p.seg_len, out_a,
+                                out_b, mean_var, p.grid, p.block, s) == cudaSuccess
+                   ? TCR_OK
+                   : TCR_ERR_CUDA;
+    }
+    if (p.path != kPathChunk && p.path != kPathShuffleBlock) return TCR_ERR_UNSUPPORTED;
+    // scratch: two partial arrays, and the two sums per row before the
+    // mean/variance epilogue
+    const size_t np = p.partials;
+    const size_t nt = mean_var ? p.segments : 0;
+    float *scratch = nullptr;
+    if (np + nt > 0) {
+        if (fault_injected("alloc")) return TCR_ERR_CUDA;
+        cudaMemPool_t pool = pool_for(dev);
+        if (!pool) return TCR_ERR_CUDA;
+        if (cudaMallocFromPoolAsync((void **)&scratch, 2 * (np + nt) * sizeof(float), pool, s) !=
+            cudaSuccess)
+            return TCR_ERR_CUDA;
+    }
+    if (fault_injected("launch")) {
+        if (scratch) (void)cudaFreeAsync(scratch, s);
+        return TCR_ERR_CUDA;
+    }
+    float *sum_a = mean_var ? scratch + 2 * np : out_a;
+    float *sum_b = mean_var ? scratch + 2 * np + nt : out_b;
+    float *dst_a = np ? scratch : sum_a;
+    float *dst_b = np ? scratch + np : sum_b;
+    cudaError_t e = p.path == kPathChunk
+                        ? launch_chunk_pair(family, p.dtype, p.aligned, p.R, x, p.seg_len, p.units,
+                                            p.cps, p.chunk_log2, dst_a, dst_b, p.grid, p.block, s)
+                        : launch_shuffle_block_pair(p.dtype, p.aligned, x, p.seg_len, p.segments,
+                                                    p.team_blocks, dst_a, dst_b, p.team_threads, s);
+    if (e == cudaSuccess && np) e = launch_combine(dst_a, p.segments, p.combine_count, sum_a, s);
+    if (e == cudaSuccess && np) e = launch_combine(dst_b, p.segments, p.combine_count, sum_b, s);
+    if (e == cudaSuccess && mean_var)
+        e = launch_mean_var(sum_a, sum_b, p.segments, p.seg_len, out_a, out_b, s);
+    if (scratch) {
+        cudaError_t f = cudaFreeAsync(scratch, s);
+        if (e == cudaSuccess) e = f;
+    }
+    return e == cudaSuccess ? TCR_OK : TCR_ERR_CUDA;
+}
+
+tcr_status reduce_rows_pair(const void *x, size_t rows, size_t cols, float *out_a, float *out_b,
+                            const tcr_mode &mode, int mean_var, void *stream)
+{
+    if (mul_overflows(rows, cols)) return TCR_ERR_INVALID_ARG;
+    int block = 0, R = 0;
+    if (rows == 0) return check_mode(mode, &block, &R);
+    tcr_status st = check_common(x, rows * cols, out_a, mode, &block, &R);
+    if (st != TCR_OK) return st;
+    if (!out_b || ((uintptr_t)out_b & 3u) != 0) return TCR_ERR_INVALID_ARG;
+    if (mode.run_log2 != 0) return TCR_ERR_UNSUPPORTED;     // squares have no blocked order
+    const int dev = current_device();
+    if (dev < 0) return TCR_ERR_CUDA;
+    const bool aligned = ((uintptr_t)x & 15u) == 0 && (cols % (size_t)vector_len(mode.dtype)) == 0;
+    // planned as the sum of squares (the tcgen05 kind runs the mma.sync pair)
+    Plan p = make_plan(rows, cols, true, mode, kOpSquares, block, R, aligned, dev);
+    return run_pair_plan(p, x, out_a, out_b, mean_var, (cudaStream_t)stream, dev);
+}
+
 }  // namespace
 
 extern "C" {
@@ -547,6 +627,18 @@ tcr_status tcr_reduce_rows_sum_squares(const void *x, size_t rows, size_t cols, 
                                        tcr_mode mode, void *stream)
 {
     return reduce_rows_op(x, rows, cols, out, mode, kOpSquares, stream);
+}
+
+tcr_status tcr_reduce_rows_moments(const void *x, size_t rows, size_t cols, float *sums,
+                                   float *sums_of_squares, tcr_mode mode, void *stream)
+{
+    return reduce_rows_pair(x, rows, cols, sums, sums_of_squares, mode, 0, stream);
+}
+
+tcr_status tcr_reduce_rows_mean_var(const void *x, size_t rows, size_t cols, float *mean,
+                                    float *var, tcr_mode mode, void *stream)
+{
+    return reduce_rows_pair(x, rows, cols, mean, var, mode, 1, stream);
 }
 
 tcr_status tcr_order_descriptor(size_t n, size_t rows, size_t cols, tcr_mode mode,

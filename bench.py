@@ -486,8 +486,9 @@ def extras_arm(args):
     """Beyond the hot path, one JSON line per call: the sum of squares (2^30
     sum and 65536 x 4096 rows, every mode), binary32 inputs (2^29 sum and
     65536 x 2048 rows -- the same bytes as the 16-bit workload -- every mode,
-    sums and sums of squares) and FIXED_ORDER's blocked order (runs of 2^c
-    inputs left to right, then the tree) on the 16-bit workload."""
+    sums and sums of squares), FIXED_ORDER's blocked order (runs of 2^c
+    inputs left to right, then the tree) on the 16-bit workload, and the
+    fused row moments (sum and sum of squares, mean and variance, one pass)."""
     import torch
     import arithmetic_reduction_tensor_gb300 as tcr
     from arithmetic_reduction_tensor_gb300 import synth
@@ -525,6 +526,15 @@ def extras_arm(args):
         m = tcr.Mode(tcr.FIXED_ORDER, run_log2=c)
         calls.append((f"blocked_rows/c={c}", 2 * ROWS * COLS + 4 * ROWS,
                       lambda m=m: tcr.tcr_reduce_rows(xr, m, out=out)))
+    # the fused row moments: sum and sum of squares (and mean/variance) in one pass
+    out2 = torch.empty(ROWS, dtype=torch.float32, device="cuda")
+    for kind in (tcr.MMA_CHAIN, tcr.FIXED_ORDER, tcr.SHUFFLE_TREE):
+        m = tcr.Mode(kind)
+        k = tcr.KIND_NAMES[kind]
+        calls.append(("rows_moments/" + k, 2 * ROWS * COLS + 8 * ROWS,
+                      lambda m=m: tcr.tcr_reduce_rows_moments(xr, m, sums=out, sums_of_squares=out2)))
+        calls.append(("rows_mean_var/" + k, 2 * ROWS * COLS + 8 * ROWS,
+                      lambda m=m: tcr.tcr_reduce_rows_mean_var(xr, m, mean=out, var=out2)))
     for name, nbytes, fn in calls:
         for _ in range(args.warmup):
             fn()

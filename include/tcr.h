@@ -194,6 +194,34 @@ TCR_API tcr_status tcr_reduce_rows_sum_squares(const void *x, size_t rows, size_
                                                float *out, tcr_mode mode, void *stream);
 
 /*
+ * tcr_reduce_rows_moments -- for every row r < rows, in one pass over x:
+ *   sums[r]            = the row's sum, as tcr_reduce_rows computes it, and
+ *   sums_of_squares[r] = the row's sum of squares, as
+ *                        tcr_reduce_rows_sum_squares computes it
+ * (bit for bit in TCR_FIXED_ORDER and TCR_SHUFFLE_TREE: the same orders;
+ * within the same bounds in TCR_MMA_CHAIN; TCR_MMA_CHAIN_TMEM runs as
+ * TCR_MMA_CHAIN).  Two reductions of one input fused so that it is read
+ * once: the cascaded reductions named by the "RedFuser" title in the first
+ * page's list of work built on the method.  Arguments, layout and errors are
+ * those of tcr_reduce_rows; sums and sums_of_squares are device arrays of
+ * rows floats, 4-byte aligned.  A mode with run_log2 != 0 returns
+ * TCR_ERR_UNSUPPORTED.
+ *
+ * tcr_reduce_rows_mean_var -- the same pass, then per row (n = cols as a
+ * binary32, one rounding to nearest per operation):
+ *   mean[r] = S1 / n,  var[r] = S2 / n - mean[r] * mean[r], or +0.0 where
+ *   that is negative (rounding only)
+ * from the row's sum S1 and sum of squares S2 above: the population
+ * variance by the one-pass formula, exact to a few ulps of S2 / n when the
+ * mean is small against the spread (|mean| large against the standard
+ * deviation loses digits to cancellation).  cols == 0 gives NaN for both.
+ */
+TCR_API tcr_status tcr_reduce_rows_moments(const void *x, size_t rows, size_t cols, float *sums,
+                                           float *sums_of_squares, tcr_mode mode, void *stream);
+TCR_API tcr_status tcr_reduce_rows_mean_var(const void *x, size_t rows, size_t cols, float *mean,
+                                            float *var, tcr_mode mode, void *stream);
+
+/*
  * tcr_reduce_sum_noalloc -- tcr_reduce_sum for callers that must not
  * allocate device memory while they run: a service that reserved its whole
  * device-memory budget at start-up and treats any later allocation as a

@@ -223,3 +223,17 @@ def test_blocked_order_equivalence(lib):
     longer = {"n": 1000, "mode": tcr.Mode(tcr.FIXED_ORDER, run_log2=16)}
     assert tcr.tcr_order_equivalent(short, longer)
     assert not tcr.tcr_order_equivalent(short, {"n": 1000, "mode": tcr.Mode(tcr.FIXED_ORDER, run_log2=9)})
+
+
+def test_moments_reject_bad_arguments(lib):
+    m = tcr.Mode(tcr.FIXED_ORDER)
+    for fn in (lib.tcr_reduce_rows_moments, lib.tcr_reduce_rows_mean_var):
+        assert fn(FAKE, 3, 5, FAKE, None, m, None) == tcr.ERR_INVALID_ARG        # second output NULL
+        assert fn(FAKE, 3, 5, None, FAKE, m, None) == tcr.ERR_INVALID_ARG
+        assert fn(FAKE, 3, 5, FAKE, FAKE + 2, m, None) == tcr.ERR_INVALID_ARG    # misaligned output
+        assert fn(FAKE + 1, 3, 5, FAKE, FAKE, m, None) == tcr.ERR_INVALID_ARG    # misaligned input
+        assert fn(FAKE, 3, 5, FAKE, FAKE, tcr.Mode(tcr.MMA_CHAIN, R=9), None) == tcr.ERR_INVALID_ARG
+        assert fn(FAKE, 1 << 21, 1 << 21, FAKE, FAKE, m, None) == tcr.ERR_INVALID_ARG
+        assert fn(FAKE, 3, 5, FAKE, FAKE, tcr.Mode(tcr.FIXED_ORDER, run_log2=2), None) == \
+            tcr.ERR_UNSUPPORTED
+        assert fn(None, 0, 5, None, None, m, None) == tcr.OK                    # no rows
