@@ -24,6 +24,9 @@ Functions (sources are cited in ``tcr_oracle.c``):
                        of the fixed-order mode).
 ``mean_var``           per-row mean and variance from a row's sum and sum
                        of squares (declared binary32 formula).
+``gemm_f64``, ``gemm_splitk``
+                       C = A W^T in binary64, and the declared split-K order
+                       (balanced tree over once-rounded split partials).
 ``*_sq``, ``exact_sum_squares``
                        the same over the leaves x_i^2 (sum of squares).
 ``*_rows``             the same, one result per row.
@@ -101,6 +104,10 @@ def _load():
             lib.oracle_blocked_order_rows_f32.restype = None
             lib.oracle_mean_var_f32.argtypes = [f32p, f32p, sz, sz, f32p, f32p]
             lib.oracle_mean_var_f32.restype = None
+            lib.oracle_gemm_f64.argtypes = [u16p, u16p, sz, sz, sz, i, i, f64p, f64p]
+            lib.oracle_gemm_f64.restype = None
+            lib.oracle_gemm_splitk_f32.argtypes = [u16p, u16p, sz, sz, sz, i, i, sz, i, f32p]
+            lib.oracle_gemm_splitk_f32.restype = None
             lib.oracle_leaves_f32.argtypes = [u16p, sz, i, f32p]
             lib.oracle_leaves_f32.restype = None
             _lib = lib
@@ -243,6 +250,32 @@ def mean_var(s1, s2, cols: int) -> tuple[np.ndarray, np.ndarray]:
     _load().oracle_mean_var_f32(a.ctypes.data_as(fp), b.ctypes.data_as(fp), a.size, cols,
                                 m.ctypes.data_as(fp), v.ctypes.data_as(fp))
     return m, v
+
+
+def gemm_f64(A, W, dtype: int, threads: int | None = None) -> tuple[np.ndarray, np.ndarray]:
+    """(A @ W.T as binary64 sums of exact products, the same sum of |products|);
+    A is M x K, W is N x K, 16-bit patterns."""
+    a, w = _bits(A, dtype), _bits(W, dtype)
+    M, K = a.shape
+    N = w.shape[0]
+    out = np.empty((M, N), np.float64)
+    aout = np.empty((M, N), np.float64)
+    fp = ctypes.POINTER(ctypes.c_double)
+    _load().oracle_gemm_f64(_u16p(a), _u16p(w), M, N, K, dtype, threads or default_threads(),
+                            out.ctypes.data_as(fp), aout.ctypes.data_as(fp))
+    return out, aout
+
+
+def gemm_splitk(A, W, dtype: int, splits: int, k_split: int, threads: int | None = None) -> np.ndarray:
+    """The declared split-K order over exactly summed, once-rounded partials."""
+    a, w = _bits(A, dtype), _bits(W, dtype)
+    M, K = a.shape
+    N = w.shape[0]
+    out = np.empty((M, N), np.float32)
+    _load().oracle_gemm_splitk_f32(_u16p(a), _u16p(w), M, N, K, dtype, splits, k_split,
+                                   threads or default_threads(),
+                                   out.ctypes.data_as(ctypes.POINTER(ctypes.c_float)))
+    return out
 
 
 def leaves(x, dtype: int) -> np.ndarray:

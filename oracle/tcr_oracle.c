@@ -602,6 +602,67 @@ void oracle_mean_var_f32(const float *s1, const float *s2, size_t rows, size_t c
     }
 }
 
+/* ------------------------------------------------------------------ */
+/* Split-K GEMM ("Taming Bitwise Behavior in GPU Kernels with Tensor Core",
+ * Abstract: the descriptor of reduction order covers GEMM, including the
+ * split-K partitioning of K).  C = A * W^T with A (M x K) and W (N x K)
+ * row-major 16-bit inputs.
+ *
+ * oracle_gemm_f64: every element as a binary64 sum of the exact products
+ * a_ik * w_jk (each exact in binary64) in k order, and the same sum of
+ * |a_ik * w_jk| -- the reference for the error bound.
+ *
+ * oracle_gemm_splitk_f32: the declared order with each split's partial
+ * taken exactly (as far as binary64 holds it) and rounded once to
+ * binary32: P_s = fl32(sum over k in [s * k_split, (s + 1) * k_split)),
+ * C = the balanced binary32 tree over P_0 .. P_{S-1} (-0.0 pad).  Where
+ * every partial is exact in binary32 and the tensor core adds it without
+ * rounding (small integers, one scale per split), this is the GPU's result
+ * bit for bit; elsewhere the two differ by the tensor core's rounding. */
+
+void oracle_gemm_f64(const void *A, const void *W, size_t M, size_t N, size_t K, int dtype,
+                     int threads, double *out, double *abs_out)
+{
+    int nt = threads > 0 ? threads : 1;
+#pragma omp parallel for num_threads(nt) schedule(dynamic, 1)
+    for (size_t i = 0; i < M; i++) {
+        for (size_t j = 0; j < N; j++) {
+            double acc = 0.0, aacc = 0.0;
+            for (size_t k = 0; k < K; k++) {
+                const double p = (double)leaf_f32(raw_at(A, i * K + k, dtype), dtype) *
+                                 (double)leaf_f32(raw_at(W, j * K + k, dtype), dtype);
+                acc += p;
+                aacc += fabs(p);
+            }
+            out[i * N + j] = acc;
+            abs_out[i * N + j] = aacc;
+        }
+    }
+}
+
+void oracle_gemm_splitk_f32(const void *A, const void *W, size_t M, size_t N, size_t K, int dtype,
+                            int splits, size_t k_split, int threads, float *out)
+{
+    int nt = threads > 0 ? threads : 1;
+#pragma omp parallel for num_threads(nt) schedule(dynamic, 1)
+    for (size_t i = 0; i < M; i++) {
+        float *part = (float *)malloc((size_t)(splits > 0 ? splits : 1) * sizeof(float));
+        for (size_t j = 0; j < N; j++) {
+            for (int s = 0; s < splits; s++) {
+                const size_t k0 = (size_t)s * k_split;
+                const size_t k1 = k0 + k_split < K ? k0 + k_split : K;
+                double acc = 0.0;
+                for (size_t k = k0; k < k1; k++)
+                    acc += (double)leaf_f32(raw_at(A, i * K + k, dtype), dtype) *
+                           (double)leaf_f32(raw_at(W, j * K + k, dtype), dtype);
+                part[s] = (float)acc;
+            }
+            out[i * N + j] = tree_f32(part, (size_t)splits);
+        }
+        free(part);
+    }
+}
+
 /* Exact binary32 value of each input (used by the tests to compare the
  * decoder with independent conversions). */
 void oracle_leaves_f32(const void *x, size_t n, int dtype, float *out)

@@ -668,3 +668,83 @@ def test_mean_var_special_cases():
     # no inputs: 0 / 0
     m, v = oracle.mean_var(np.zeros(1, np.float32), np.zeros(1, np.float32), 0)
     assert np.isnan(m[0]) and np.isnan(v[0])
+
+
+# ---------------------------------------------------------------- split-K GEMM
+
+def test_gemm_f64_matches_numpy_and_brute_force():
+    rng = np.random.default_rng(70)
+    for dtype, (M, N, K) in ((F16, (5, 7, 33)), (BF16, (9, 4, 130)), (F16, (1, 1, 1))):
+        A = synth.generate(M * K, "normal", dtype, seed=M).reshape(M, K)
+        W = synth.generate(N * K, "normal", dtype, seed=N + 100).reshape(N, K)
+        c, a = oracle.gemm_f64(A, W, dtype, threads=2)
+        fa = np_leaves(A.reshape(-1), dtype).astype(np.float64).reshape(M, K)
+        fw = np_leaves(W.reshape(-1), dtype).astype(np.float64).reshape(N, K)
+        assert np.allclose(c, fa @ fw.T, rtol=1e-12, atol=1e-12)
+        assert np.allclose(a, np.abs(fa) @ np.abs(fw).T, rtol=1e-12, atol=1e-12)
+    # exact on a tiny case (every product and partial sum exact in binary64)
+    A = random_finite(rng, 12, F16).reshape(3, 4)
+    W = random_finite(rng, 20, F16).reshape(5, 4)
+    c, _ = oracle.gemm_f64(A, W, F16)
+    fa = np_leaves(A.reshape(-1), F16).reshape(3, 4)
+    fw = np_leaves(W.reshape(-1), F16).reshape(5, 4)
+    for i in range(3):
+        for j in range(5):
+            exact = sum((Fraction(float(fa[i, k])) * Fraction(float(fw[j, k])) for k in range(4)),
+                        Fraction(0))
+            assert abs(Fraction(c[i, j]) - exact) <= abs(exact) * Fraction(1, 2 ** 50)
+
+
+def exact_partials_operands(M, N, K, k_split, scales, dtype, seed):
+    """Small integers in A; in W, integers times 2^-scales[s] on split s: every
+    split's partial is an exact binary32 value that any order of addition
+    reaches without rounding, so only the combine of the splits rounds."""
+    rng = np.random.default_rng(seed)
+    a = rng.integers(-8, 9, (M, K)).astype(np.float64)
+    w = rng.integers(-8, 9, (N, K)).astype(np.float64)
+    for s, e in enumerate(scales):
+        w[:, s * k_split:(s + 1) * k_split] *= 2.0 ** -e
+    if dtype == F16:
+        return a.astype(np.float16).view(np.uint16), w.astype(np.float16).view(np.uint16)
+    def bf(x):
+        return (x.astype(np.float32).view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+    return bf(a), bf(w)
+
+
+def test_gemm_splitk_declared_combine_hand_worked():
+    # K = 256 in 4 splits of 64: row 0 of A all ones; column 0 of W has 1.0
+    # in split 0 and 2^-24 once in each other split -> P = (1, t, t, t);
+    # the tree (1 + t) + (t + t): 1 + t ties to 1, + 2^-23 -> 1 + 2^-23.
+    # One split rounds the exact 1 + 3 * 2^-24 once: halfway between 1 + 2^-23
+    # and 1 + 2^-22, to even -> 1 + 2^-22.
+    A = np.full((1, 256), 0x3C00, np.uint16)
+    W = np.zeros((1, 256), np.uint16)
+    W[0, 0] = 0x3C00
+    W[0, 64] = W[0, 128] = W[0, 192] = 0x0001
+    assert oracle.gemm_splitk(A, W, F16, 4, 64)[0, 0] == np.float32(1 + 2.0 ** -23)
+    assert oracle.gemm_splitk(A, W, F16, 1, 256)[0, 0] == np.float32(1 + 2.0 ** -22)
+    c, _ = oracle.gemm_f64(A, W, F16)
+    assert c[0, 0] == 1 + 3 * 2.0 ** -24
+
+
+@pytest.mark.parametrize("dtype", [F16, BF16])
+def test_gemm_splitk_exact_partials_and_bound(dtype):
+    M, N, K, ks = 7, 9, 320, 64
+    scales = (0, 13, 24, 7, 20)
+    A, W = exact_partials_operands(M, N, K, ks, scales, dtype, seed=71)
+    got = oracle.gemm_splitk(A, W, dtype, 5, ks)
+    # each partial exactly, then the tree in numpy
+    fa = np_leaves(A.reshape(-1), dtype).astype(np.float64).reshape(M, K)
+    fw = np_leaves(W.reshape(-1), dtype).astype(np.float64).reshape(N, K)
+    parts = np.stack([(fa[:, s * ks:(s + 1) * ks] @ fw[:, s * ks:(s + 1) * ks].T).astype(np.float32)
+                      for s in range(5)])
+    for i in range(M):
+        for j in range(N):
+            assert same_f32(got[i, j], np_tree(parts[:, i, j]))
+    # general inputs: within the rounding of the partials and of the tree
+    A = synth.generate(6 * 500, "normal", dtype, seed=72).reshape(6, 500)
+    W = synth.generate(5 * 500, "normal", dtype, seed=73).reshape(5, 500)
+    c, a = oracle.gemm_f64(A, W, dtype)
+    for S, ks in ((1, 512), (4, 128), (8, 64)):
+        g = oracle.gemm_splitk(A, W, dtype, S, ks).astype(np.float64)
+        assert np.all(np.abs(g - c) <= 2.0 ** -24 * (1 + int(np.ceil(np.log2(S))) * 2) * a + 1e-30)
