@@ -30,7 +30,7 @@ __all__ = [
     "tcr_reduce_sum", "tcr_reduce_rows", "tcr_reduce_sum_squares", "tcr_reduce_rows_sum_squares",
     "tcr_reduce_rows_moments", "tcr_reduce_rows_mean_var",
     "tcr_order_descriptor", "tcr_order_equivalent", "tcr_status_string", "tcr_device_faults",
-    "FAULT_PIPELINE_WAIT",
+    "FAULT_PIPELINE_WAIT", "tcr_gemm_desc", "tcr_gemm_descriptor", "tcr_gemm_splitk",
 ]
 
 MMA_CHAIN, SHUFFLE_TREE, FIXED_ORDER, MMA_CHAIN_TMEM = 0, 1, 2, 3
@@ -63,6 +63,18 @@ class tcr_order_desc(ctypes.Structure):
                 ("launch_block", ctypes.c_int), ("chunk_log2", ctypes.c_int),
                 ("partials", ctypes.c_size_t), ("launches", ctypes.c_int),
                 ("dtype", ctypes.c_int), ("run_log2", ctypes.c_int)]
+
+    def as_dict(self):
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+class tcr_gemm_desc(ctypes.Structure):
+    _fields_ = [("M", ctypes.c_size_t), ("N", ctypes.c_size_t), ("K", ctypes.c_size_t),
+                ("dtype", ctypes.c_int), ("splits", ctypes.c_int), ("k_split", ctypes.c_size_t),
+                ("tile_m", ctypes.c_int), ("tile_n", ctypes.c_int), ("tile_k", ctypes.c_int),
+                ("combine_order", ctypes.c_int), ("workspace_bytes", ctypes.c_size_t),
+                ("launch_grid", ctypes.c_int), ("launch_block", ctypes.c_int),
+                ("launches", ctypes.c_int)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -115,6 +127,11 @@ def c_api() -> ctypes.CDLL:
                                                  ctypes.POINTER(tcr_order_desc),
                                                  ctypes.POINTER(ctypes.c_int)]
             lib.tcr_order_equivalent.restype = ctypes.c_int
+            lib.tcr_gemm_descriptor.argtypes = [sz, sz, sz, ctypes.c_int, ctypes.c_int,
+                                                ctypes.POINTER(tcr_gemm_desc)]
+            lib.tcr_gemm_descriptor.restype = ctypes.c_int
+            lib.tcr_gemm_splitk.argtypes = [vp, vp, vp, sz, sz, sz, ctypes.c_int, ctypes.c_int, vp]
+            lib.tcr_gemm_splitk.restype = ctypes.c_int
             lib.tcr_device_faults.argtypes = [ctypes.POINTER(ctypes.c_uint), ctypes.c_int]
             lib.tcr_device_faults.restype = ctypes.c_int
             lib.tcr_status_string.argtypes = [ctypes.c_int]
@@ -286,3 +303,48 @@ def tcr_order_equivalent(call_a: dict, call_b: dict) -> bool:
     if st != OK:
         raise TcrError(st, "tcr_order_equivalent")
     return bool(eq.value)
+
+
+# ------------------------------------------------------------------ GEMM
+
+def tcr_gemm_descriptor(M: int, N: int, K: int, splits: int = 0, dtype: int = F16) -> dict:
+    """The K partition and launch plan of a split-K GEMM (``tcr_gemm_descriptor``)."""
+    d = tcr_gemm_desc()
+    st = c_api().tcr_gemm_descriptor(M, N, K, splits, dtype, ctypes.byref(d))
+    if st != OK:
+        raise TcrError(st, "tcr_gemm_descriptor")
+    return d.as_dict()
+
+
+def tcr_gemm_splitk(A, W, splits: int = 0, out=None, stream=None, dtype: int | None = None):
+    """C = A @ W.T in binary32 with the declared split-K combine
+    (``tcr_gemm_splitk``); A is M x K, W is N x K, both contiguous CUDA
+    tensors of float16 or bfloat16 (or raw 16-bit patterns with ``dtype``)."""
+    import torch
+    if not (A.is_cuda and W.is_cuda and A.is_contiguous() and W.is_contiguous()
+            and A.dim() == 2 and W.dim() == 2):
+        raise ValueError("A and W must be contiguous 2-D CUDA tensors")
+    if A.shape[1] != W.shape[1]:
+        raise ValueError(f"inner dimensions differ: {tuple(A.shape)} vs {tuple(W.shape)}")
+    if A.dtype != W.dtype:
+        raise ValueError("A and W must have the same dtype")
+    if dtype is None:
+        if A.dtype == torch.float16:
+            dtype = F16
+        elif A.dtype == torch.bfloat16:
+            dtype = BF16
+        else:
+            raise TypeError(f"A must be float16 or bfloat16 (or pass dtype), got {A.dtype}")
+    M, K = A.shape
+    N = W.shape[0]
+    if out is None:
+        out = torch.empty(M, N, dtype=torch.float32, device=A.device)
+    if out.dtype != torch.float32 or not out.is_contiguous() or out.numel() < M * N:
+        raise ValueError("out must be a contiguous float32 tensor with M * N elements")
+    with torch.cuda.device(A.device):
+        st = c_api().tcr_gemm_splitk(A.data_ptr() if A.numel() else None,
+                                     W.data_ptr() if W.numel() else None, out.data_ptr(),
+                                     M, N, K, splits, dtype, _stream_handle(A.device, stream))
+    if st != OK:
+        raise TcrError(st, "tcr_gemm_splitk")
+    return out

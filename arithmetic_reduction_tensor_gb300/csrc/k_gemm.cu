@@ -1,0 +1,390 @@
+// k_gemm.cu -- split-K GEMM with a declared, bit-reproducible K-partition
+// combine.
+//
+// "Taming Bitwise Behavior in GPU Kernels with Tensor Core" (arXiv
+// 2609.11356), Abstract: reduction order is the primary cause of bitwise
+// differences, and a descriptor of reduction order -- for GEMM including the
+// split-K partitioning of K -- pins it down.  Here C = A * W^T (A: M x K, W:
+// N x K, both row-major 16-bit, C: M x N binary32) with K cut into S splits
+// of k_split columns (a multiple of 64; the last split shorter):
+//
+//   P_s = the tensor core's sum over split s (one chain of tcgen05 MMAs,
+//         K = 16 each, accumulating in one fp32 TMEM tile), s = 0 .. S-1;
+//   C   = the balanced binary32 tree over P_0 .. P_{S-1} in split order
+//         (-0.0 pad), formed by a second kernel -- never by atomics, so C
+//         does not depend on which CTA finished first.
+//
+// A work unit is one 128 x 128 output tile of one split.  CTA roles (192
+// threads, one persistent CTA per SM), as in the tcgen05 reduction kernels:
+//   warp 0, lane 0   producer: per stage one 64-column x 128-row box of A
+//                    and one of W (2-D tensor maps, 128-byte swizzle: the
+//                    SWIZZLE_128B K-major operand layout) into a 5-stage
+//                    shared-memory ring, completion by transaction count;
+//   warp 1           owns the TMEM allocation (two 128-column fp32 tiles);
+//                    lane 0 issues tcgen05.mma.cta_group::1.kind::f16 with
+//                    M = 128, N = 128 -- four per stage, the k-th slice 32
+//                    bytes further in both operands -- and commits a stage
+//                    when its MMAs are done and a tile when the split is;
+//   warps 2..5       epilogue: thread m reads row m of the tile from TMEM
+//                    (tcgen05.ld 32x32b, 32 columns at a time) and stores it
+//                    to P_s (or straight to C when S = 1).
+// Every mbarrier wait gives up after about a second, raises g_gemm_fault,
+// drains its own copies and MMAs, frees TMEM and writes NaN to its tiles.
+#include <cstring>
+
+#include "kernels.cuh"
+#include "tc05.cuh"
+
+namespace tcr {
+
+constexpr int kGmBM = 128;                       // tile rows (TMEM lanes)
+constexpr int kGmBN = 128;                       // tile columns (MMA N)
+constexpr int kGmBK = 64;                        // K per box: one 128-byte swizzle row
+constexpr int kGmBoxBytes = 128 * kGmBK * 2;     // 16 KiB, A and W boxes alike
+constexpr int kGmStageBytes = 2 * kGmBoxBytes;   // 32 KiB
+constexpr int kGmStages = 5;                     // 160 KiB ring
+constexpr int kGmDBuffers = 2;
+constexpr uint32_t kGmTmemCols = kGmDBuffers * kGmBN;     // 256
+constexpr int kGmThreads = 192;
+constexpr int kGmEpilogueThreads = 128;
+constexpr int kGmOffBars = kGmStages * kGmStageBytes;
+// barriers: full[S], empty[S], dfull[D], dempty[D], drain
+constexpr int kGmNumBars = 2 * kGmStages + 2 * kGmDBuffers + 1;
+constexpr int kGmOffMisc = kGmOffBars + 8 * kGmNumBars;
+constexpr int kGmSmemBytes = kGmOffMisc + 64 + 1024;   // + alignment slack
+
+__device__ unsigned int g_gemm_fault;
+
+__device__ __forceinline__ bool gm_wait(uint32_t bar, uint32_t parity, volatile uint32_t *abort)
+{
+    return mbar_wait_f(bar, parity, abort, &g_gemm_fault);
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tc_ld_row32(uint32_t taddr, float (&v)[32])
+{
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int j = 0; j < 32; j++) v[j] = __uint_as_float(r[j]);
+}
+
+struct GemmArgs {
+    size_t M, N;
+    int kboxes;            // 64-column boxes of K
+    int kbps;              // boxes per split
+    int splits;            // S
+    int tiles_m, tiles_n;
+    size_t units;          // tiles_m * tiles_n * splits
+    float *out;            // C when splits == 1, else P (splits x M x N)
+};
+
+template <int DT>
+__global__ void __launch_bounds__(kGmThreads, 1)
+gemm_splitk_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant__ CUtensorMap tmw,
+                   const GemmArgs g)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const uint32_t sbase = smem_addr(smem);
+    const uint32_t ring = sbase;
+    const uint32_t bars = sbase + kGmOffBars;
+    auto full_bar = [&](int s) { return bars + 8u * (uint32_t)s; };
+    auto empty_bar = [&](int s) { return bars + 8u * (uint32_t)(kGmStages + s); };
+    auto dfull_bar = [&](int b) { return bars + 8u * (uint32_t)(2 * kGmStages + b); };
+    auto dempty_bar = [&](int b) { return bars + 8u * (uint32_t)(2 * kGmStages + kGmDBuffers + b); };
+    const uint32_t drain_bar = bars + 8u * (uint32_t)(2 * kGmStages + 2 * kGmDBuffers);
+    uint32_t *misc = (uint32_t *)(smem + kGmOffMisc);
+    volatile uint32_t *tmem_holder = misc;
+    volatile uint32_t *abort = misc + 1;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // unit u = (split s, tile row tm, tile column tn), tn fastest
+    auto decode = [&](size_t u, int &s, int &tm, int &tn) {
+        tn = (int)(u % (size_t)g.tiles_n);
+        const size_t r = u / (size_t)g.tiles_n;
+        tm = (int)(r % (size_t)g.tiles_m);
+        s = (int)(r / (size_t)g.tiles_m);
+    };
+    auto split_boxes = [&](int s) {
+        const int b0 = s * g.kbps;
+        return min(g.kbps, g.kboxes - b0);
+    };
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kGmStages; s++) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < kGmDBuffers; b++) {
+            mbar_init(dfull_bar(b), 1);
+            mbar_init(dempty_bar(b), kGmEpilogueThreads);
+        }
+        mbar_init(drain_bar, 1);
+        *abort = 0u;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tma) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmw) : "memory");
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(smem_addr((const void *)tmem_holder)), "r"(kGmTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == 0) {
+        // ---------------- producer
+        if (lane == 0) {
+            int st = 0;
+            uint32_t phase = 0;
+            bool armed[kGmStages];
+            uint32_t armed_phase[kGmStages];
+            for (int i = 0; i < kGmStages; i++) {
+                armed[i] = false;
+                armed_phase[i] = 0;
+            }
+            for (size_t u = blockIdx.x; u < g.units && !*abort; u += gridDim.x) {
+                int s, tm, tn;
+                decode(u, s, tm, tn);
+                const int nb = split_boxes(s);
+                bool ok = true;
+                for (int j = 0; j < nb; j++) {
+                    if (!gm_wait(empty_bar(st), phase ^ 1u, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t dst = ring + (uint32_t)st * kGmStageBytes;
+                    const int kc = (s * g.kbps + j) * kGmBK;      // a multiple of 64 columns
+                    mbar_arrive_expect_tx(full_bar(st), (uint32_t)kGmStageBytes);
+                    tma_load_2d(dst, &tma, kc, tm * kGmBM, full_bar(st));
+                    tma_load_2d(dst + kGmBoxBytes, &tmw, kc, tn * kGmBN, full_bar(st));
+                    armed[st] = true;
+                    armed_phase[st] = phase;
+                    if (++st == kGmStages) {
+                        st = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+            }
+            if (*abort) {
+                for (int i = 0; i < kGmStages; i++) {
+                    if (!armed[i]) continue;
+                    const uint64_t t0 = global_ns();
+                    while (!mbar_try_wait(full_bar(i), armed_phase[i]) &&
+                           global_ns() - t0 < kWaitLimitNs) {
+                    }
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---------------- MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = instr_desc_n<DT, (uint32_t)kGmBN>();
+            const uint64_t ring_desc = smem_desc_sw128(ring);
+            constexpr uint64_t kKStep = 32u >> 4;                       // 16 columns = 32 bytes
+            constexpr uint64_t kBoxStep = (uint64_t)kGmBoxBytes >> 4;
+            constexpr uint64_t kStageStep = (uint64_t)kGmStageBytes >> 4;
+            int st = 0, b = 0;
+            uint32_t phase = 0, dphase = 0;
+            for (size_t u = blockIdx.x; u < g.units && !*abort; u += gridDim.x) {
+                int s, tm, tn;
+                decode(u, s, tm, tn);
+                const int nb = split_boxes(s);
+                if (!gm_wait(dempty_bar(b), ((dphase >> b) & 1u) ^ 1u, abort)) break;
+                tc_fence_after();
+                const uint32_t d = tmem + (uint32_t)b * kGmBN;
+                bool ok = true;
+                for (int j = 0; j < nb; j++) {
+                    if (!gm_wait(full_bar(st), phase, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t a_desc = ring_desc + (uint64_t)st * kStageStep;
+                    const uint64_t w_desc = a_desc + kBoxStep;
+#pragma unroll
+                    for (int k = 0; k < 4; k++)
+                        tc_mma(d, a_desc + (uint64_t)k * kKStep, w_desc + (uint64_t)k * kKStep, idesc,
+                               (j > 0 || k > 0) ? 1u : 0u);
+                    tc_commit(empty_bar(st));
+                    if (++st == kGmStages) {
+                        st = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                tc_commit(dfull_bar(b));
+                dphase ^= 1u << b;
+                b ^= 1;
+            }
+            tc_commit(drain_bar);
+            const uint64_t t0 = global_ns();
+            while (!mbar_try_wait(drain_bar, 0u) && global_ns() - t0 < kWaitLimitNs) {
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---------------- epilogue: thread m stores row m of the tile
+        const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+        const int m = 32 * (warp & 3) + lane;
+        int b = 0;
+        uint32_t dphase = 0;
+        const size_t mn = g.M * g.N;
+        for (size_t u = blockIdx.x; u < g.units; u += gridDim.x) {
+            int s, tm, tn;
+            decode(u, s, tm, tn);
+            float *out = g.out + (size_t)s * mn;
+            const size_t row = (size_t)tm * kGmBM + (size_t)m;
+            const size_t col0 = (size_t)tn * kGmBN;
+            // tcgen05.ld is warp-collective: a warp reads the tile only if
+            // every lane's wait succeeded
+            const bool ready = !*abort && gm_wait(dfull_bar(b), (dphase >> b) & 1u, abort);
+            const bool live = __all_sync(kFull, ready);
+            if (live) tc_fence_after();
+#pragma unroll 1
+            for (int c = 0; c < kGmBN / 32; c++) {
+                float v[32];
+                if (live) {
+                    tc_ld_row32(tmem + lane_base + (uint32_t)b * kGmBN + (uint32_t)(32 * c), v);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; j++) v[j] = __int_as_float(0x7fc00000);
+                }
+                if (row < g.M) {
+                    float *dst = out + row * g.N + col0 + (size_t)(32 * c);
+                    const size_t left = g.N - (col0 + (size_t)(32 * c));
+                    if (col0 + (size_t)(32 * c) >= g.N) continue;
+                    if (left >= 32 && (((uintptr_t)dst) & 15u) == 0) {
+#pragma unroll
+                        for (int j = 0; j < 32; j += 4)
+                            *reinterpret_cast<float4 *>(dst + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; j++)
+                            if ((size_t)j < left) dst[j] = v[j];
+                    }
+                }
+            }
+            if (live) {
+                tc_fence_before();
+                mbar_arrive(dempty_bar(b));
+            }
+            dphase ^= 1u << b;
+            b ^= 1;
+        }
+    }
+
+    pdl_launch_dependents();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kGmTmemCols)
+                     : "memory");
+    }
+}
+
+// C[i] = balanced binary32 tree over P[s * mn + i], s = 0 .. splits-1, in
+// split order, -0.0 pad (a binary counter over the splits).
+__global__ void splitk_combine_kernel(const float *__restrict__ P, size_t mn, int splits,
+                                      float *__restrict__ C)
+{
+    pdl_wait_primary();
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < mn;
+         i += (size_t)gridDim.x * blockDim.x) {
+        TreeCounter<7> tc;
+        for (int s = 0; s < splits; s++) tc.push(__ldg(P + (size_t)s * mn + i));
+        C[i] = tc.finish();
+    }
+}
+
+// ---------------------------------------------------------------- host
+
+int gemm_tile_m() { return kGmBM; }
+int gemm_tile_n() { return kGmBN; }
+int gemm_tile_k() { return kGmBK; }
+int gemm_block_threads() { return kGmThreads; }
+
+cudaError_t launch_gemm_splitk(int dtype, const void *A, const void *W, size_t M, size_t N, size_t K,
+                               int splits, int kbps, float *out, int grid, cudaStream_t stream)
+{
+    void *k = dtype == kF16 ? (void *)gemm_splitk_kernel<kF16> : dtype == kBF16 ? (void *)gemm_splitk_kernel<kBF16>
+                                                                                : nullptr;
+    if (!k) return cudaErrorInvalidValue;
+    PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    if (!encode) return cudaErrorNotSupported;
+    alignas(64) CUtensorMap ma, mw;
+    const cuuint32_t box[2] = {kGmBK, 128};
+    const cuuint32_t estride[2] = {1, 1};
+    const cuuint64_t gstride[1] = {(cuuint64_t)K * 2};
+    const cuuint64_t da[2] = {(cuuint64_t)K, (cuuint64_t)M};
+    const cuuint64_t dw[2] = {(cuuint64_t)K, (cuuint64_t)N};
+    if (encode(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, (void *)A, da, gstride, box, estride,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+        encode(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, (void *)W, dw, gstride, box, estride,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    cudaError_t e = set_smem_once(k, kGmSmemBytes);
+    if (e != cudaSuccess) return e;
+    GemmArgs g;
+    g.M = M;
+    g.N = N;
+    g.kboxes = (int)((K + kGmBK - 1) / kGmBK);
+    g.kbps = kbps;
+    g.splits = splits;
+    g.tiles_m = (int)((M + kGmBM - 1) / kGmBM);
+    g.tiles_n = (int)((N + kGmBN - 1) / kGmBN);
+    g.units = (size_t)g.tiles_m * (size_t)g.tiles_n * (size_t)splits;
+    g.out = out;
+    void *args[] = {(void *)&ma, (void *)&mw, (void *)&g};
+    return cudaLaunchKernel(k, dim3(grid), dim3(kGmThreads), args, kGmSmemBytes, stream);
+}
+
+cudaError_t launch_splitk_combine(const float *P, size_t mn, int splits, float *C, cudaStream_t stream)
+{
+    if (mn == 0) return cudaSuccess;
+    const size_t blocks = (mn + 255) / 256;
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3((unsigned)(blocks < 152 * 8 ? blocks : 152 * 8));
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, splitk_combine_kernel, P, mn, splits, C);
+}
+
+cudaError_t read_gemm_faults(unsigned int *flags, bool clear)
+{
+    cudaError_t e = cudaMemcpyFromSymbol(flags, g_gemm_fault, sizeof(unsigned int));
+    if (e != cudaSuccess || !clear) return e;
+    const unsigned int zero = 0u;
+    return cudaMemcpyToSymbol(g_gemm_fault, &zero, sizeof(unsigned int));
+}
+
+}  // namespace tcr

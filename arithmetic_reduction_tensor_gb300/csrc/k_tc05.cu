@@ -32,14 +32,8 @@
 // raises a device-wide fault flag, drains its own copies and MMAs (again
 // with a limit), frees its TMEM and writes NaN as its partials, so a broken
 // pipeline shows up as a NaN result, never as a hang.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-#include <mutex>
-#include <utility>
-#include <vector>
-
-#include "common.cuh"
 #include "kernels.cuh"
+#include "tc05.cuh"
 
 namespace tcr {
 
@@ -55,7 +49,6 @@ constexpr int kTcEpilogueThreads = 128;
 constexpr int kTcDBuffers = 8;                      // chains the MMA may run ahead
 constexpr uint32_t kTcDBufferStride = 32;           // columns per D buffer (N = 16 used)
 constexpr uint32_t kTcTmemCols = kTcDBuffers * kTcDBufferStride;    // 256
-constexpr uint64_t kWaitLimitNs = 1000000000ull;    // about one second
 
 // Dynamic shared memory layout (offsets from a 1024-byte aligned base).
 constexpr int kTcOffRing = 0;
@@ -68,130 +61,16 @@ constexpr int kTcSmemBytes = kTcOffMisc + 64 + 1024;                    // + ali
 
 __device__ unsigned int g_tc05_fault;               // non-zero once any wait gave up
 
-// ---------------------------------------------------------------- PTX
-
-__device__ __forceinline__ uint32_t smem_addr(const void *p)
-{
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ uint64_t global_ns()
-{
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar)
-{
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Wait for the phase of parity `parity` of `bar` to complete, giving up
-// after about a second (or soon after another role gave up).
+// Waits of these kernels give up into g_tc05_fault.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile uint32_t *abort)
 {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_ns();
-    for (uint32_t i = 1;; i++) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 63u) == 0u) {
-            if (*abort) return false;
-            if (global_ns() - t0 > kWaitLimitNs) {
-                *abort = 1u;
-                atomicOr(&g_tc05_fault, 1u);
-                return false;
-            }
-        }
-    }
+    return mbar_wait_f(bar, parity, abort, &g_tc05_fault);
 }
 
-__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void *src, uint32_t bytes,
-                                              uint32_t bar)
-{
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
-        : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// Shared-memory matrix descriptor, no swizzle, K-major: 8-row x 16-byte
-// core matrices; lbo = byte step between core matrices along K, sbo = byte
-// step between 8-row groups; bits 46..48 hold the fixed value 0b001.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo)
-{
-    return (uint64_t)((addr >> 4) & 0x3fffu) | ((uint64_t)((lbo >> 4) & 0x3fffu) << 16) |
-           ((uint64_t)((sbo >> 4) & 0x3fffu) << 32) | (1ull << 46);
-}
-
-// Instruction descriptor of kind::f16: D fp32 (bits 4-5 = 1), A and B
-// binary16 (0) or bfloat16 (1) in bits 7-9 and 10-12, both K-major, N >> 3
-// in bits 17-22, M >> 4 in bits 24-28.
 template <int DT>
 __device__ __forceinline__ uint32_t instr_desc()
 {
-    constexpr uint32_t ab = DT == kF16 ? 0u : 1u;
-    return (1u << 4) | (ab << 7) | (ab << 10) | ((16u >> 3) << 17) | ((128u >> 4) << 24);
-}
-
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// Arrive once on `bar` when every tcgen05 operation this thread issued so
-// far has completed.
-__device__ __forceinline__ void tc_commit(uint32_t bar)
-{
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-                 ::"r"(bar)
-                 : "memory");
-}
-
-__device__ __forceinline__ float tc_ld_lane(uint32_t taddr)
-{
-    uint32_t v;
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(v) : "r"(taddr) : "memory");
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-    return __uint_as_float(v);
-}
-
-__device__ __forceinline__ void named_sync(uint32_t id, uint32_t threads)
-{
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+    return instr_desc_n<DT, 16>();
 }
 
 // ---------------------------------------------------------------- kernel
@@ -453,25 +332,6 @@ constexpr int kTcRowsNumBars = 2 * kTcRowsStages + 2 * kTcDBuffers + 1;
 constexpr int kTcRowsOffMisc = kTcRowsOffBars + 8 * kTcRowsNumBars;
 constexpr int kTcRowsSmemBytes = kTcRowsOffMisc + 64 + 1024;
 
-// SWIZZLE_128B K-major descriptor: 8-row groups 1024 bytes apart (the
-// leading-dimension field is not used by this layout), swizzle code 2 in
-// bits 61..63; the atom base is 1024-byte aligned, so the base offset is 0.
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr)
-{
-    return (uint64_t)((addr >> 4) & 0x3fffu) | ((uint64_t)1 << 16) |
-           ((uint64_t)(1024u >> 4) << 32) | (1ull << 46) | (2ull << 61);
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
-                                            uint32_t bar)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
-        "[%0], [%1, {%2, %3}], [%4];"
-        ::"r"(dst), "l"((uint64_t)map), "r"(c0), "r"(c1), "r"(bar)
-        : "memory");
-}
-
 template <int DT, int R>
 __global__ void __launch_bounds__(kTcThreads, 1)
 mma_tmem_rows_kernel(const __grid_constant__ CUtensorMap tmap, size_t rows, size_t cols,
@@ -685,22 +545,6 @@ mma_tmem_rows_kernel(const __grid_constant__ CUtensorMap tmap, size_t rows, size
 
 // ---------------------------------------------------------------- host
 
-// The shared-memory opt-in is a per-kernel attribute: set it once per
-// device and kernel instance.
-static cudaError_t set_smem_once(void *k, int bytes)
-{
-    static std::mutex mu;
-    static std::vector<std::pair<int, void *>> done;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return cudaGetLastError();
-    std::lock_guard<std::mutex> lk(mu);
-    for (auto &d : done)
-        if (d.first == dev && d.second == k) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    if (e == cudaSuccess) done.emplace_back(dev, k);
-    return e;
-}
-
 template <int DT>
 static void *pick_dt(int R)
 {
@@ -753,25 +597,6 @@ static void *pick_rows_dt(int R)
     case 8: return (void *)mma_tmem_rows_kernel<DT, 8>;
     default: return nullptr;
     }
-}
-
-// cuTensorMapEncodeTiled through the runtime's driver entry point, so the
-// library does not link the driver library itself.
-static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
-{
-    static std::once_flag once;
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
-        else
-            (void)cudaGetLastError();
-    });
-    return fn;
 }
 
 size_t tmem_rows_chunks(size_t cols)

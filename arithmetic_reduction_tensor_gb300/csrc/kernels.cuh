@@ -104,6 +104,20 @@ cudaError_t launch_shuffle_block_pair(int dtype, bool aligned, const void *x, si
 cudaError_t launch_mean_var(const float *s1, const float *s2, size_t rows, size_t cols, float *mean,
                             float *var, cudaStream_t stream);
 
+// ---- split-K GEMM, C = A * W^T (k_gemm.cu): A M x K, W N x K row-major
+// 16-bit (16-byte aligned, K a multiple of 8), out = C (splits == 1) or the
+// partials P (splits x M x N); split s covers 64-column boxes
+// [s * kbps, min((s + 1) * kbps, ceil(K / 64))).  One persistent CTA per SM.
+cudaError_t launch_gemm_splitk(int dtype, const void *A, const void *W, size_t M, size_t N, size_t K,
+                               int splits, int kbps, float *out, int grid, cudaStream_t stream);
+// C[i] = balanced tree over P[s * mn + i] in split order (waits for the GEMM).
+cudaError_t launch_splitk_combine(const float *P, size_t mn, int splits, float *C, cudaStream_t stream);
+cudaError_t read_gemm_faults(unsigned int *flags, bool clear);
+int gemm_tile_m();
+int gemm_tile_n();
+int gemm_tile_k();
+int gemm_block_threads();
+
 // ---- combine: out[s] = balanced tree over partials[s*count .. s*count+count-1]
 // padded with -0.0; one CTA of 1024 threads per segment, or one thread per
 // segment when count is small (the same tree either way).

@@ -603,6 +603,51 @@ tcr_status reduce_rows_pair(const void *x, size_t rows, size_t cols, float *out_
     return run_pair_plan(p, x, out_a, out_b, mean_var, (cudaStream_t)stream, dev);
 }
 
+// ---------------------------------------------------------------- GEMM
+
+constexpr int kGemmMaxSplits = 64;
+
+struct GemmPlan {
+    int splits, kbps, grid;
+    size_t k_split, workspace;
+};
+
+tcr_status gemm_check(size_t M, size_t N, size_t K, int splits, int dtype)
+{
+    if (dtype != TCR_F16 && dtype != TCR_BF16) return TCR_ERR_INVALID_ARG;
+    if (M >= ((size_t)1 << 31) || N >= ((size_t)1 << 31) || K >= ((size_t)1 << 31))
+        return TCR_ERR_INVALID_ARG;
+    if (K % 8 != 0) return TCR_ERR_INVALID_ARG;
+    if (splits < 0 || splits > kGemmMaxSplits) return TCR_ERR_INVALID_ARG;
+    return TCR_OK;
+}
+
+// The K partition: a fixed function of (M, N, K, splits) -- never of the
+// device -- so the declared order is the same on every GPU.
+GemmPlan gemm_plan(size_t M, size_t N, size_t K, int splits, int dev)
+{
+    GemmPlan g;
+    const size_t tiles = ((M + gemm_tile_m() - 1) / gemm_tile_m()) *
+                         ((N + gemm_tile_n() - 1) / gemm_tile_n());
+    const size_t kboxes = (K + gemm_tile_k() - 1) / gemm_tile_k();
+    size_t s = (size_t)splits;
+    if (s == 0) {
+        s = tiles >= (size_t)kRuleSMs ? 1 : (2 * (size_t)kRuleSMs + tiles - 1) / (tiles ? tiles : 1);
+        if (s > 16) s = 16;
+    }
+    if (s > kboxes) s = kboxes;
+    if (s < 1) s = 1;
+    const size_t kbps = kboxes ? (kboxes + s - 1) / s : 1;
+    g.kbps = (int)kbps;
+    g.splits = kboxes ? (int)((kboxes + kbps - 1) / kbps) : 1;
+    g.k_split = kbps * (size_t)gemm_tile_k();
+    g.workspace = g.splits > 1 ? (size_t)g.splits * M * N * sizeof(float) : 0;
+    const size_t units = tiles * (size_t)g.splits;
+    const size_t sms = (size_t)sm_count(dev);
+    g.grid = (int)(units < sms ? units : sms);
+    return g;
+}
+
 }  // namespace
 
 extern "C" {
@@ -639,6 +684,66 @@ tcr_status tcr_reduce_rows_mean_var(const void *x, size_t rows, size_t cols, flo
                                     float *var, tcr_mode mode, void *stream)
 {
     return reduce_rows_pair(x, rows, cols, mean, var, mode, 1, stream);
+}
+
+tcr_status tcr_gemm_descriptor(size_t M, size_t N, size_t K, int splits, int dtype,
+                               tcr_gemm_desc *desc)
+{
+    if (!desc) return TCR_ERR_INVALID_ARG;
+    tcr_status st = gemm_check(M, N, K, splits, dtype);
+    if (st != TCR_OK) return st;
+    const GemmPlan g = gemm_plan(M, N, K, splits, current_device());
+    std::memset(desc, 0, sizeof *desc);
+    desc->M = M;
+    desc->N = N;
+    desc->K = K;
+    desc->dtype = dtype;
+    desc->splits = g.splits;
+    desc->k_split = g.k_split;
+    desc->tile_m = gemm_tile_m();
+    desc->tile_n = gemm_tile_n();
+    desc->tile_k = gemm_tile_k();
+    desc->combine_order = TCR_ORDER_BALANCED_TREE;
+    desc->workspace_bytes = g.workspace;
+    desc->launch_grid = g.grid;
+    desc->launch_block = gemm_block_threads();
+    desc->launches = (M * N == 0) ? 0 : (K == 0 ? 0 : (g.splits > 1 ? 2 : 1));
+    return TCR_OK;
+}
+
+tcr_status tcr_gemm_splitk(const void *A, const void *W, float *C, size_t M, size_t N, size_t K,
+                           int splits, int dtype, void *stream)
+{
+    tcr_status st = gemm_check(M, N, K, splits, dtype);
+    if (st != TCR_OK) return st;
+    if (M == 0 || N == 0) return TCR_OK;
+    if (!C || ((uintptr_t)C & 3u) != 0) return TCR_ERR_INVALID_ARG;
+    if (K > 0 && (!A || !W || ((uintptr_t)A & 15u) != 0 || ((uintptr_t)W & 15u) != 0))
+        return TCR_ERR_INVALID_ARG;
+    const int dev = current_device();
+    if (dev < 0) return TCR_ERR_CUDA;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (K == 0)
+        return cudaMemsetAsync(C, 0, M * N * sizeof(float), s) == cudaSuccess ? TCR_OK : TCR_ERR_CUDA;
+    const GemmPlan g = gemm_plan(M, N, K, splits, dev);
+    float *P = nullptr;
+    if (g.splits > 1) {
+        if (fault_injected("alloc")) return TCR_ERR_CUDA;
+        cudaMemPool_t pool = pool_for(dev);
+        if (!pool) return TCR_ERR_CUDA;
+        if (cudaMallocFromPoolAsync((void **)&P, g.workspace, pool, s) != cudaSuccess) return TCR_ERR_CUDA;
+    }
+    if (fault_injected("launch")) {
+        if (P) (void)cudaFreeAsync(P, s);
+        return TCR_ERR_CUDA;
+    }
+    cudaError_t e = launch_gemm_splitk(dtype, A, W, M, N, K, g.splits, g.kbps, P ? P : C, g.grid, s);
+    if (e == cudaSuccess && P) e = launch_splitk_combine(P, M * N, g.splits, C, s);
+    if (P) {
+        cudaError_t f = cudaFreeAsync(P, s);
+        if (e == cudaSuccess) e = f;
+    }
+    return e == cudaSuccess ? TCR_OK : TCR_ERR_CUDA;
 }
 
 tcr_status tcr_order_descriptor(size_t n, size_t rows, size_t cols, tcr_mode mode,
@@ -718,7 +823,11 @@ tcr_status tcr_device_faults(unsigned int *flags, int clear)
 {
     if (!flags) return TCR_ERR_INVALID_ARG;
     if (current_device() < 0) return TCR_ERR_CUDA;
-    return read_device_faults(flags, clear != 0) == cudaSuccess ? TCR_OK : TCR_ERR_CUDA;
+    unsigned int a = 0, g = 0;
+    if (read_device_faults(&a, clear != 0) != cudaSuccess || read_gemm_faults(&g, clear != 0) != cudaSuccess)
+        return TCR_ERR_CUDA;
+    *flags = a | g;
+    return TCR_OK;
 }
 
 const char *tcr_status_string(tcr_status status)

@@ -352,9 +352,56 @@ TCR_API tcr_status tcr_order_equivalent(const tcr_order_desc *a, const tcr_order
                                         int *equivalent);
 
 /*
+ * Split-K GEMM with a declared K-partition combine -- the GEMM part of the
+ * descriptor of reduction order of "Taming Bitwise Behavior in GPU Kernels
+ * with Tensor Core" (arXiv 2609.11356), Abstract, which pins GEMM results
+ * down by declaring how K is partitioned and how the partitions combine.
+ *
+ *   C (M x N, binary32, row-major) = A * W^T
+ *   A: M x K, W: N x K, row-major binary16 or bfloat16 (dtype, both alike)
+ *
+ * K is cut into S splits of k_split columns (a multiple of 64; the last
+ * split shorter).  P_s, the sum over split s, is one chain of tensor-core
+ * MMAs accumulating in fp32 (the tensor core's own order inside, as in
+ * TCR_MMA_CHAIN); C is the balanced binary32 tree over P_0 .. P_{S-1} in
+ * split order (-0.0 pad), formed by a second kernel, never by atomics.  So
+ * the bits of C depend only on (A, W, M, N, K, dtype, S, k_split) -- not on
+ * the grid, the scheduling of CTAs or the GPU model -- and two calls with
+ * equal descriptors give identical bits.  Error bound per element:
+ *   |C - exact| <= (2^-22 * k_split / 16 + 2^-24 * ceil(log2 S)) * sum_k |a_ik w_jk| + 1e-30.
+ *
+ * tcr_gemm_descriptor -- fill *desc for a call (host only).
+ *   splits  0 for the default rule -- S = 1 when the 128 x 128 output tiles
+ *           number at least 152, else min(16, ceil(304 / tiles)) -- or the
+ *           requested S in 1..64; either is then limited to ceil(K / 64)
+ *           and reported as the effective S with its k_split.
+ * tcr_gemm_splitk -- the GEMM.  A and W are device pointers, 16-byte
+ *   aligned; C a device pointer, 4-byte aligned; M, N, K < 2^31 and K a
+ *   multiple of 8 (the 16-byte row pitch of the tensor-map copies), else
+ *   TCR_ERR_INVALID_ARG.  K == 0 writes +0.0 everywhere; S > 1 takes S x M x
+ *   N floats of pool scratch and launches the combine.
+ */
+typedef struct {
+    size_t M, N, K;
+    int dtype;
+    int splits;              /* effective S */
+    size_t k_split;          /* K columns per split */
+    int tile_m, tile_n, tile_k;
+    int combine_order;       /* TCR_ORDER_BALANCED_TREE, over splits */
+    size_t workspace_bytes;  /* pool scratch of the call */
+    int launch_grid, launch_block;
+    int launches;
+} tcr_gemm_desc;
+
+TCR_API tcr_status tcr_gemm_descriptor(size_t M, size_t N, size_t K, int splits, int dtype,
+                                       tcr_gemm_desc *desc);
+TCR_API tcr_status tcr_gemm_splitk(const void *A, const void *W, float *C, size_t M, size_t N,
+                                   size_t K, int splits, int dtype, void *stream);
+
+/*
  * tcr_device_faults -- the fault word of the current device: bit 0
  * (TCR_FAULT_PIPELINE_WAIT) is set when a wait inside a TCR_MMA_CHAIN_TMEM
- * kernel gave up after its limit of about one second (the kernel then
+ * or split-K GEMM kernel gave up after its limit of about one second (the kernel then
  * drained its own copies and tensor-core work, freed its tensor memory and
  * wrote NaN partials, so that call's result is NaN).  The word stays set
  * until cleared: clear != 0 resets it after reading.  Synchronous with

@@ -40,3 +40,21 @@ def default_R(block: int = 0) -> int:
 def mma_tolerance(abs_sum: float) -> float:
     """|gpu - exact| <= 2^-20 * sum|x_i| + 1e-6."""
     return 2.0 ** -20 * abs_sum + 1e-6
+
+
+def gemm_splits(M: int, N: int, K: int, splits: int = 0) -> tuple[int, int]:
+    """(effective S, k_split) of a split-K GEMM, from the rule stated in
+    include/tcr.h: S = 1 when the 128 x 128 tiles number at least 152, else
+    min(16, ceil(304 / tiles)); a requested S is taken as given; either is
+    limited to ceil(K / 64) boxes, split evenly in whole boxes."""
+    tiles = math.ceil(M / 128) * math.ceil(N / 128)
+    kboxes = math.ceil(K / 64)
+    s = splits or (1 if tiles >= 152 else min(16, math.ceil(304 / max(tiles, 1))))
+    s = max(1, min(s, kboxes))
+    kbps = math.ceil(kboxes / s) if kboxes else 1
+    return (math.ceil(kboxes / kbps) if kboxes else 1), kbps * 64
+
+
+def gemm_bound(k_split: int, S: int, abs_sum):
+    """|C - exact| <= (2^-22 * k_split / 16 + 2^-24 * ceil(log2 S)) * sum|a w| + 1e-30."""
+    return (2.0 ** -22 * k_split / 16 + 2.0 ** -24 * math.ceil(math.log2(S))) * abs_sum + 1e-30

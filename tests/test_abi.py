@@ -237,3 +237,20 @@ def test_moments_reject_bad_arguments(lib):
         assert fn(FAKE, 3, 5, FAKE, FAKE, tcr.Mode(tcr.FIXED_ORDER, run_log2=2), None) == \
             tcr.ERR_UNSUPPORTED
         assert fn(None, 0, 5, None, None, m, None) == tcr.OK                    # no rows
+
+
+def test_gemm_descriptor_rule(lib):
+    for (M, N, K, S) in ((4096, 4096, 4096, 0), (1024, 1024, 8192, 0), (100, 100, 64, 0),
+                         (128, 128, 1000, 0), (64, 64, 8, 5), (2048, 2048, 512, 64)):
+        d = tcr.tcr_gemm_descriptor(M, N, K, S)
+        assert (d["splits"], d["k_split"]) == spec.gemm_splits(M, N, K, S)
+        assert d["combine_order"] == tcr.ORDER_BALANCED_TREE
+        assert d["workspace_bytes"] == (d["splits"] * M * N * 4 if d["splits"] > 1 else 0)
+        assert d["launches"] == (2 if d["splits"] > 1 else 1)
+    bad = tcr.tcr_gemm_desc()
+    for args in ((64, 64, 12, 0, 0), (64, 64, 64, 65, 0), (64, 64, 64, -1, 0), (64, 64, 64, 0, 2),
+                 (1 << 31, 64, 64, 0, 0)):
+        assert lib.tcr_gemm_descriptor(*args, ctypes.byref(bad)) == tcr.ERR_INVALID_ARG
+    assert lib.tcr_gemm_splitk(FAKE, FAKE, FAKE, 8, 8, 12, 0, 0, None) == tcr.ERR_INVALID_ARG
+    assert lib.tcr_gemm_splitk(FAKE + 8, FAKE, FAKE, 8, 8, 16, 0, 0, None) == tcr.ERR_INVALID_ARG
+    assert lib.tcr_gemm_splitk(FAKE, FAKE, FAKE + 2, 8, 8, 16, 0, 0, None) == tcr.ERR_INVALID_ARG
