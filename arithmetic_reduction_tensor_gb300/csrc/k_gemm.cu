@@ -14,17 +14,22 @@
 //         (-0.0 pad), formed by a second kernel -- never by atomics, so C
 //         does not depend on which CTA finished first.
 //
-// A work unit is one 128 x 128 output tile of one split.  CTA roles (192
-// threads, one persistent CTA per SM), as in the tcgen05 reduction kernels:
-//   warp 0, lane 0   producer: per stage one 64-column x 128-row box of A
-//                    and one of W (2-D tensor maps, 128-byte swizzle: the
-//                    SWIZZLE_128B K-major operand layout) into a 5-stage
-//                    shared-memory ring, completion by transaction count;
-//   warp 1           owns the TMEM allocation (two 128-column fp32 tiles);
-//                    lane 0 issues tcgen05.mma.cta_group::1.kind::f16 with
-//                    M = 128, N = 128 -- four per stage, the k-th slice 32
-//                    bytes further in both operands -- and commits a stage
-//                    when its MMAs are done and a tile when the split is;
+// A work unit is one 128 x 256 output tile of one split; units are ordered
+// in groups of 8 tile rows (tile column outermost within a group) so that
+// the CTAs in flight share A and W tiles through L2 -- the order of units
+// never changes a result.  CTA roles (192 threads, one persistent CTA per
+// SM), as in the tcgen05 reduction kernels:
+//   warp 0, lane 0   producer: per stage a 64-column x 128-row box of A and
+//                    a 64-column x 256-row box of W (2-D tensor maps,
+//                    128-byte swizzle: the SWIZZLE_128B K-major operand
+//                    layout) into a 4-stage shared-memory ring, completion
+//                    by transaction count;
+//   warp 1           owns the TMEM allocation (two 256-column fp32 tiles, all
+//                    512 columns); lane 0 issues
+//                    tcgen05.mma.cta_group::1.kind::f16 with M = 128,
+//                    N = 256 -- four per stage, the k-th slice 32 bytes
+//                    further in both operands -- and commits a stage when
+//                    its MMAs are done and a tile when the split is;
 //   warps 2..5       epilogue: thread m reads row m of the tile from TMEM
 //                    (tcgen05.ld 32x32b, 32 columns at a time) and stores it
 //                    to P_s (or straight to C when S = 1).
@@ -38,13 +43,15 @@
 namespace tcr {
 
 constexpr int kGmBM = 128;                       // tile rows (TMEM lanes)
-constexpr int kGmBN = 128;                       // tile columns (MMA N)
+constexpr int kGmBN = 256;                       // tile columns (MMA N, the most for M = 128)
 constexpr int kGmBK = 64;                        // K per box: one 128-byte swizzle row
-constexpr int kGmBoxBytes = 128 * kGmBK * 2;     // 16 KiB, A and W boxes alike
-constexpr int kGmStageBytes = 2 * kGmBoxBytes;   // 32 KiB
-constexpr int kGmStages = 5;                     // 160 KiB ring
+constexpr int kGmABoxBytes = kGmBM * kGmBK * 2;  // 16 KiB
+constexpr int kGmWBoxBytes = kGmBN * kGmBK * 2;  // 32 KiB
+constexpr int kGmStageBytes = kGmABoxBytes + kGmWBoxBytes;   // 48 KiB
+constexpr int kGmStages = 4;                     // 192 KiB ring
 constexpr int kGmDBuffers = 2;
-constexpr uint32_t kGmTmemCols = kGmDBuffers * kGmBN;     // 256
+constexpr uint32_t kGmTmemCols = kGmDBuffers * kGmBN;     // 512: all of TMEM
+constexpr int kGmGroupM = 8;                     // tile rows per raster group (L2 reuse)
 constexpr int kGmThreads = 192;
 constexpr int kGmEpilogueThreads = 128;
 constexpr int kGmOffBars = kGmStages * kGmStageBytes;
@@ -110,12 +117,19 @@ gemm_splitk_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constan
     volatile uint32_t *abort = misc + 1;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // unit u = (split s, tile row tm, tile column tn), tn fastest
+    // unit u = (split s, tile t); tiles in groups of kGmGroupM tile rows,
+    // the tile row fastest within a group
     auto decode = [&](size_t u, int &s, int &tm, int &tn) {
-        tn = (int)(u % (size_t)g.tiles_n);
-        const size_t r = u / (size_t)g.tiles_n;
-        tm = (int)(r % (size_t)g.tiles_m);
-        s = (int)(r / (size_t)g.tiles_m);
+        const size_t tiles = (size_t)g.tiles_m * (size_t)g.tiles_n;
+        s = (int)(u / tiles);
+        const size_t t = u - (size_t)s * tiles;
+        const size_t group = (size_t)kGmGroupM * (size_t)g.tiles_n;
+        const size_t first = (t / group) * kGmGroupM;
+        const size_t in_group = (size_t)g.tiles_m - first < (size_t)kGmGroupM ? (size_t)g.tiles_m - first
+                                                                             : (size_t)kGmGroupM;
+        const size_t r = t % group;
+        tm = (int)(first + r % in_group);
+        tn = (int)(r / in_group);
     };
     auto split_boxes = [&](int s) {
         const int b0 = s * g.kbps;
@@ -174,7 +188,7 @@ gemm_splitk_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constan
                     const int kc = (s * g.kbps + j) * kGmBK;      // a multiple of 64 columns
                     mbar_arrive_expect_tx(full_bar(st), (uint32_t)kGmStageBytes);
                     tma_load_2d(dst, &tma, kc, tm * kGmBM, full_bar(st));
-                    tma_load_2d(dst + kGmBoxBytes, &tmw, kc, tn * kGmBN, full_bar(st));
+                    tma_load_2d(dst + kGmABoxBytes, &tmw, kc, tn * kGmBN, full_bar(st));
                     armed[st] = true;
                     armed_phase[st] = phase;
                     if (++st == kGmStages) {
@@ -201,7 +215,7 @@ gemm_splitk_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constan
             const uint32_t idesc = instr_desc_n<DT, (uint32_t)kGmBN>();
             const uint64_t ring_desc = smem_desc_sw128(ring);
             constexpr uint64_t kKStep = 32u >> 4;                       // 16 columns = 32 bytes
-            constexpr uint64_t kBoxStep = (uint64_t)kGmBoxBytes >> 4;
+            constexpr uint64_t kBoxStep = (uint64_t)kGmABoxBytes >> 4;
             constexpr uint64_t kStageStep = (uint64_t)kGmStageBytes >> 4;
             int st = 0, b = 0;
             uint32_t phase = 0, dphase = 0;
@@ -334,15 +348,16 @@ cudaError_t launch_gemm_splitk(int dtype, const void *A, const void *W, size_t M
     PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
     if (!encode) return cudaErrorNotSupported;
     alignas(64) CUtensorMap ma, mw;
-    const cuuint32_t box[2] = {kGmBK, 128};
+    const cuuint32_t abox[2] = {kGmBK, kGmBM};
+    const cuuint32_t wbox[2] = {kGmBK, kGmBN};
     const cuuint32_t estride[2] = {1, 1};
     const cuuint64_t gstride[1] = {(cuuint64_t)K * 2};
     const cuuint64_t da[2] = {(cuuint64_t)K, (cuuint64_t)M};
     const cuuint64_t dw[2] = {(cuuint64_t)K, (cuuint64_t)N};
-    if (encode(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, (void *)A, da, gstride, box, estride,
+    if (encode(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, (void *)A, da, gstride, abox, estride,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
-        encode(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, (void *)W, dw, gstride, box, estride,
+        encode(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, (void *)W, dw, gstride, wbox, estride,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;

@@ -627,13 +627,15 @@ tcr_status gemm_check(size_t M, size_t N, size_t K, int splits, int dtype)
 GemmPlan gemm_plan(size_t M, size_t N, size_t K, int splits, int dev)
 {
     GemmPlan g;
+    // the default: as many splits as fill one wave of 152 CTAs with tiles x S
+    // units, at most 32
     const size_t tiles = ((M + gemm_tile_m() - 1) / gemm_tile_m()) *
                          ((N + gemm_tile_n() - 1) / gemm_tile_n());
     const size_t kboxes = (K + gemm_tile_k() - 1) / gemm_tile_k();
     size_t s = (size_t)splits;
     if (s == 0) {
-        s = tiles >= (size_t)kRuleSMs ? 1 : (2 * (size_t)kRuleSMs + tiles - 1) / (tiles ? tiles : 1);
-        if (s > 16) s = 16;
+        s = tiles >= (size_t)kRuleSMs ? 1 : (size_t)kRuleSMs / (tiles ? tiles : 1);
+        if (s > 32) s = 32;
     }
     if (s > kboxes) s = kboxes;
     if (s < 1) s = 1;

@@ -552,6 +552,51 @@ def extras_arm(args):
     return 0
 
 
+def load_bf16_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, "fallback"
+
+
+def gemm_arm(args):
+    """The split-K GEMM with the declared combine: TFLOP/s (2 M N K per call)
+    against the measured bf16 GEMM peak, for square shapes at S = 1 and
+    K-heavy shapes at the default S and at S = 1."""
+    import torch
+    import arithmetic_reduction_tensor_gb300 as tcr
+    torch.cuda.set_device(0)
+    peak, src = load_bf16_peak()
+    gen = torch.Generator(device="cuda").manual_seed(5)
+    cases = [(4096, 4096, 4096, 0), (8192, 8192, 8192, 0), (1024, 1024, 16384, 0),
+             (1024, 1024, 16384, 1), (512, 512, 32768, 0), (512, 512, 32768, 1)]
+    for M, N, K, S in cases:
+        A = torch.randn(M, K, device="cuda", generator=gen).to(torch.bfloat16)
+        W = torch.randn(N, K, device="cuda", generator=gen).to(torch.bfloat16)
+        C = torch.empty(M, N, device="cuda")
+        d = tcr.tcr_gemm_descriptor(M, N, K, S, tcr.BF16)
+        for _ in range(args.warmup):
+            tcr.tcr_gemm_splitk(A, W, splits=S, out=C)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(args.steps):
+            tcr.tcr_gemm_splitk(A, W, splits=S, out=C)
+        e1.record()
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / args.steps
+        tflops = 2.0 * M * N * K / us / 1e6
+        print(json.dumps({"gemm": f"{M}x{N}x{K} bf16", "splits": d["splits"], "k_split": d["k_split"],
+                          "us": round(us, 2), "tflops": round(tflops, 1), "peak_tflops": peak,
+                          "frac": round(tflops / peak, 4), "peak_source": src, "steps": args.steps}),
+              flush=True)
+        del A, W, C
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -564,6 +609,8 @@ def main():
     ap.add_argument("--profile-case", nargs="?", const="f16", choices=["f16", "f32"], default=None,
                     help="run the small ncu case (2^28 sum, 32768 x 4096 rows; f32: the same "
                          "bytes in binary32) and exit")
+    ap.add_argument("--gemm", action="store_true",
+                    help="time the split-K GEMM with the declared combine (TFLOP/s) and exit")
     ap.add_argument("--e2e-steps", type=int, default=0, help="0: max(3, steps // 40)")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     args = ap.parse_args()
@@ -590,6 +637,9 @@ def main():
     if args.extras:
         build_library()
         return extras_arm(args)
+    if args.gemm:
+        build_library()
+        return gemm_arm(args)
 
     torch.cuda.set_device(local)
     init_dist(world, "nccl")

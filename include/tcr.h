@@ -371,10 +371,14 @@ TCR_API tcr_status tcr_order_equivalent(const tcr_order_desc *a, const tcr_order
  *   |C - exact| <= (2^-22 * k_split / 16 + 2^-24 * ceil(log2 S)) * sum_k |a_ik w_jk| + 1e-30.
  *
  * tcr_gemm_descriptor -- fill *desc for a call (host only).
- *   splits  0 for the default rule -- S = 1 when the 128 x 128 output tiles
- *           number at least 152, else min(16, ceil(304 / tiles)) -- or the
- *           requested S in 1..64; either is then limited to ceil(K / 64)
- *           and reported as the effective S with its k_split.
+ *   splits  0 for the default rule -- with T the number of 128 x 256 output
+ *           tiles, S = 1 when T >= 152, else min(32, floor(152 / T)): the
+ *           most splits that keep the T x S work units within one wave of
+ *           152 CTAs -- or the requested S in 1..64; either is then limited
+ *           to ceil(K / 64) and reported as the effective S with its
+ *           k_split (whole 64-column boxes per split, the last split
+ *           shorter).  The rule depends on (M, N, K) only, never on the
+ *           device, so the declared order is the same on every GPU.
  * tcr_gemm_splitk -- the GEMM.  A and W are device pointers, 16-byte
  *   aligned; C a device pointer, 4-byte aligned; M, N, K < 2^31 and K a
  *   multiple of 8 (the 16-byte row pitch of the tensor-map copies), else

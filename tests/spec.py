@@ -44,12 +44,12 @@ def mma_tolerance(abs_sum: float) -> float:
 
 def gemm_splits(M: int, N: int, K: int, splits: int = 0) -> tuple[int, int]:
     """(effective S, k_split) of a split-K GEMM, from the rule stated in
-    include/tcr.h: S = 1 when the 128 x 128 tiles number at least 152, else
-    min(16, ceil(304 / tiles)); a requested S is taken as given; either is
+    include/tcr.h: with T the 128 x 256 output tiles, S = 1 when T >= 152,
+    else min(32, floor(152 / T)); a requested S is taken as given; either is
     limited to ceil(K / 64) boxes, split evenly in whole boxes."""
-    tiles = math.ceil(M / 128) * math.ceil(N / 128)
+    tiles = math.ceil(M / 128) * math.ceil(N / 256)
     kboxes = math.ceil(K / 64)
-    s = splits or (1 if tiles >= 152 else min(16, math.ceil(304 / max(tiles, 1))))
+    s = splits or (1 if tiles >= 152 else min(32, 152 // max(tiles, 1)))
     s = max(1, min(s, kboxes))
     kbps = math.ceil(kboxes / s) if kboxes else 1
     return (math.ceil(kboxes / kbps) if kboxes else 1), kbps * 64
