@@ -319,7 +319,10 @@ gemm_splitk_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constan
 }
 
 // C[i] = balanced binary32 tree over P[s * mn + i], s = 0 .. splits-1, in
-// split order, -0.0 pad (a binary counter over the splits).
+// split order, -0.0 pad (a binary counter over the splits), one element per
+// thread.  (Four elements per thread with 16-byte loads, and eight loads
+// issued ahead of their additions, both measured slower: fewer threads in
+// flight.)
 __global__ void splitk_combine_kernel(const float *__restrict__ P, size_t mn, int splits,
                                       float *__restrict__ C)
 {

@@ -116,15 +116,18 @@ KERNEL_SOURCE = {
     "fixed_chunk_kernel": "k_fixed.cu", "fixed_rows_warp_kernel": "k_fixed.cu",
     "shuffle_block_kernel": "k_shuffle.cu", "shuffle_rows_warp_kernel": "k_shuffle.cu",
     "combine_kernel": "k_combine.cu", "mma_tmem_kernel": "k_tc05.cu",
-    "mma_tmem_rows_kernel": "k_tc05.cu",
+    "mma_tmem_rows_kernel": "k_tc05.cu", "gemm_splitk_kernel": "k_gemm.cu",
 }
+# headers a kernel's source includes beyond the shared device headers
+KERNEL_HEADERS = {"k_tc05.cu": ("tc05.cuh",), "k_gemm.cu": ("tc05.cuh",)}
 
 
 def source_hash(kernel: str) -> str:
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "arithmetic_reduction_tensor_gb300", "csrc")
-    for f in ("common.cuh", "config.cuh", "stream.cuh", KERNEL_SOURCE[kernel]):
+    src = KERNEL_SOURCE[kernel]
+    for f in ("common.cuh", "config.cuh", "stream.cuh") + KERNEL_HEADERS.get(src, ()) + (src,):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
@@ -451,11 +454,22 @@ def profile_arm(args):
     larger than L2), each rows mode once on 32768 x 4096 rows (256 MiB), and
     the tcgen05 MMA_CHAIN sum and rows.  ``--profile-case f32``: the same
     bytes in binary32 (2^27 sum, 32768 x 2048 rows), the three mma.sync-era
-    modes."""
+    modes.  ``--profile-case gemm``: the split-K GEMM on 4096^3 (one split)
+    and 1024 x 1024 x 16384 (the default split)."""
     import torch
     import arithmetic_reduction_tensor_gb300 as tcr
     from arithmetic_reduction_tensor_gb300 import synth
     torch.cuda.set_device(0)
+    if args.profile_case == "gemm":
+        gen = torch.Generator(device="cuda").manual_seed(5)
+        for M, N, K, S in ((4096, 4096, 4096, 1), (1024, 1024, 16384, 0)):
+            A = torch.randn(M, K, device="cuda", generator=gen).to(torch.bfloat16)
+            W = torch.randn(N, K, device="cuda", generator=gen).to(torch.bfloat16)
+            for _ in range(args.steps):
+                tcr.tcr_gemm_splitk(A, W, splits=S)
+        torch.cuda.synchronize()
+        print("profile case done", flush=True)
+        return 0
     if args.profile_case == "f32":
         x = torch.from_numpy(synth.generate(1 << 27, "uniform_pm1", synth.F32, seed=4).view(np.float32))
         r = torch.from_numpy(synth.generate(32768 * 2048, "normal", synth.F32, seed=2).view(np.float32))
@@ -606,9 +620,10 @@ def main():
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--extras", action="store_true",
                     help="time the sum of squares and binary32 calls (beyond the hot path) and exit")
-    ap.add_argument("--profile-case", nargs="?", const="f16", choices=["f16", "f32"], default=None,
+    ap.add_argument("--profile-case", nargs="?", const="f16", choices=["f16", "f32", "gemm"],
+                    default=None,
                     help="run the small ncu case (2^28 sum, 32768 x 4096 rows; f32: the same "
-                         "bytes in binary32) and exit")
+                         "bytes in binary32; gemm: 4096^3 and 1024^2 x 16384 bf16) and exit")
     ap.add_argument("--gemm", action="store_true",
                     help="time the split-K GEMM with the declared combine (TFLOP/s) and exit")
     ap.add_argument("--e2e-steps", type=int, default=0, help="0: max(3, steps // 40)")
