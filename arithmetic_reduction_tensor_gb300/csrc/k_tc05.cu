@@ -320,12 +320,12 @@ mma_tmem_kernel(const uint16_t *__restrict__ x, size_t n, size_t units, float *_
 // chain's columns.  Work unit: 128 rows x kTcRowsChunkCols columns, one
 // partial per row and unit; the tensor map zero-fills rows and columns past
 // the matrix.
-constexpr int kTcRowsChunkCols = 512;                 // columns per work unit
+constexpr int kTcRowsChunkCols = 1024;                // columns per work unit
 constexpr int kTcRowsBoxCols = 64;                    // columns per tensor-map box
 constexpr int kTcRowsBoxBytes = 128 * kTcRowsBoxCols * 2;     // 16 KiB
-constexpr int kTcRowsBoxesPerStage = 2;               // 32 KiB, 8 MMAs per stage
+constexpr int kTcRowsBoxesPerStage = 4;               // 64 KiB, 16 MMAs per stage
 constexpr int kTcRowsStageBytes = kTcRowsBoxBytes * kTcRowsBoxesPerStage;
-constexpr int kTcRowsStages = 6;                      // 192 KiB ring
+constexpr int kTcRowsStages = 3;                      // 192 KiB ring
 constexpr int kTcRowsOffOnes = kTcRowsStages * kTcRowsStageBytes;
 constexpr int kTcRowsOffBars = kTcRowsOffOnes + 1024;
 constexpr int kTcRowsNumBars = 2 * kTcRowsStages + 2 * kTcDBuffers + 1;
