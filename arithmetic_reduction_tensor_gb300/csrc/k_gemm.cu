@@ -95,6 +95,7 @@ struct GemmArgs {
     int tiles_m, tiles_n;
     size_t units;          // tiles_m * tiles_n * splits
     float *out;            // C when splits == 1, else P (splits x M x N)
+    uint32_t inject_stall; // withhold the first tile's publication (tests of the failure path)
 };
 
 template <int DT>
@@ -219,6 +220,7 @@ gemm_splitk_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constan
             constexpr uint64_t kStageStep = (uint64_t)kGmStageBytes >> 4;
             int st = 0, b = 0;
             uint32_t phase = 0, dphase = 0;
+            bool withhold = g.inject_stall != 0u;
             for (size_t u = blockIdx.x; u < g.units && !*abort; u += gridDim.x) {
                 int s, tm, tn;
                 decode(u, s, tm, tn);
@@ -246,7 +248,10 @@ gemm_splitk_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constan
                     }
                 }
                 if (!ok) break;
-                tc_commit(dfull_bar(b));
+                if (withhold)
+                    withhold = false;
+                else
+                    tc_commit(dfull_bar(b));
                 dphase ^= 1u << b;
                 b ^= 1;
             }
@@ -343,7 +348,8 @@ int gemm_tile_k() { return kGmBK; }
 int gemm_block_threads() { return kGmThreads; }
 
 cudaError_t launch_gemm_splitk(int dtype, const void *A, const void *W, size_t M, size_t N, size_t K,
-                               int splits, int kbps, float *out, int grid, cudaStream_t stream)
+                               int splits, int kbps, float *out, int grid, bool inject_stall,
+                               cudaStream_t stream)
 {
     void *k = dtype == kF16 ? (void *)gemm_splitk_kernel<kF16> : dtype == kBF16 ? (void *)gemm_splitk_kernel<kBF16>
                                                                                 : nullptr;
@@ -376,6 +382,7 @@ cudaError_t launch_gemm_splitk(int dtype, const void *A, const void *W, size_t M
     g.tiles_n = (int)((N + kGmBN - 1) / kGmBN);
     g.units = (size_t)g.tiles_m * (size_t)g.tiles_n * (size_t)splits;
     g.out = out;
+    g.inject_stall = inject_stall ? 1u : 0u;
     void *args[] = {(void *)&ma, (void *)&mw, (void *)&g};
     return cudaLaunchKernel(k, dim3(grid), dim3(kGmThreads), args, kGmSmemBytes, stream);
 }

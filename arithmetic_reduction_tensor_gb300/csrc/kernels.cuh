@@ -108,8 +108,11 @@ cudaError_t launch_mean_var(const float *s1, const float *s2, size_t rows, size_
 // 16-bit (16-byte aligned, K a multiple of 8), out = C (splits == 1) or the
 // partials P (splits x M x N); split s covers 64-column boxes
 // [s * kbps, min((s + 1) * kbps, ceil(K / 64))).  One persistent CTA per SM.
+// inject_stall: withhold the first tile's publication so that a wait runs
+// out its limit (tests of the failure path only).
 cudaError_t launch_gemm_splitk(int dtype, const void *A, const void *W, size_t M, size_t N, size_t K,
-                               int splits, int kbps, float *out, int grid, cudaStream_t stream);
+                               int splits, int kbps, float *out, int grid, bool inject_stall,
+                               cudaStream_t stream);
 // C[i] = balanced tree over P[s * mn + i] in split order (waits for the GEMM).
 cudaError_t launch_splitk_combine(const float *P, size_t mn, int splits, float *C, cudaStream_t stream);
 cudaError_t read_gemm_faults(unsigned int *flags, bool clear);

@@ -739,7 +739,8 @@ tcr_status tcr_gemm_splitk(const void *A, const void *W, float *C, size_t M, siz
         if (P) (void)cudaFreeAsync(P, s);
         return TCR_ERR_CUDA;
     }
-    cudaError_t e = launch_gemm_splitk(dtype, A, W, M, N, K, g.splits, g.kbps, P ? P : C, g.grid, s);
+    cudaError_t e = launch_gemm_splitk(dtype, A, W, M, N, K, g.splits, g.kbps, P ? P : C, g.grid,
+                                       fault_injected("stall"), s);
     if (e == cudaSuccess && P) e = launch_splitk_combine(P, M * N, g.splits, C, s);
     if (P) {
         cudaError_t f = cudaFreeAsync(P, s);
