@@ -227,14 +227,23 @@ tcr_status check_mode(const tcr_mode &m, int *block, int *R)
     return TCR_OK;
 }
 
-void plan_chunked(Plan &p, int dev, Family fam)
+// may_shrink: the CTA size is free to choose (FIXED_ORDER, whose bits never
+// depend on it, or a default block size): small inputs then get smaller
+// CTAs until there are two work units per SM of the 152 the rules assume --
+// a fixed function of the input length, so MMA_CHAIN's chunking (reported
+// by the descriptor) is the same on every device.
+void plan_chunked(Plan &p, int dev, Family fam, bool may_shrink)
 {
     // each warp of a CTA covers 2^kWarpSpanBytesLog2 bytes of the CTA's chunk
     p.path = kPathChunk;
-    p.chunk_log2 = kWarpSpanBytesLog2 - log2_exact((int)elem_bytes(p.dtype)) +
-                   log2_exact(p.block / 32);
-    p.cps = (p.seg_len + ((size_t)1 << p.chunk_log2) - 1) >> p.chunk_log2;
-    p.units = p.segments * p.cps;
+    const int span_log2 = kWarpSpanBytesLog2 - log2_exact((int)elem_bytes(p.dtype));
+    for (;;) {
+        p.chunk_log2 = span_log2 + log2_exact(p.block / 32);
+        p.cps = (p.seg_len + ((size_t)1 << p.chunk_log2) - 1) >> p.chunk_log2;
+        p.units = p.segments * p.cps;
+        if (!may_shrink || p.block <= 32 || p.units >= (size_t)2 * kRuleSMs) break;
+        p.block /= 2;
+    }
     const size_t resident =
         (size_t)sm_count(dev) *
         (size_t)occupancy(dev, fam, false, p.dtype, p.op, p.aligned,
@@ -379,7 +388,7 @@ Plan make_plan(size_t segments, size_t seg_len, bool rows_call, const tcr_mode &
         p.launches = 1;
         return p;
     }
-    plan_chunked(p, dev, fam);
+    plan_chunked(p, dev, fam, m.kind == TCR_FIXED_ORDER || m.block_threads == 0);
     return p;
 }
 

@@ -106,11 +106,20 @@ extern "C" tcr_status tcr_reduce_sum_noalloc(const void *x, size_t n, float *out
         return TCR_ERR_INVALID_ARG;
     }
 
-    // 2^kWarpSpanBytesLog2 bytes per warp, as in the allocating entry point
+    // 2^kWarpSpanBytesLog2 bytes per warp, and the same choice of CTA size
+    // for small inputs, as in the allocating entry point
+    int block_used = block;
     int warps_log2 = 0;
-    while ((32 << warps_log2) < block) warps_log2++;
-    const int chunk_log2 = kWarpSpanBytesLog2 - elem_log2 + warps_log2;
-    const size_t cps = (n + ((size_t)1 << chunk_log2) - 1) >> chunk_log2;
+    while ((32 << warps_log2) < block_used) warps_log2++;
+    int chunk_log2 = kWarpSpanBytesLog2 - elem_log2 + warps_log2;
+    size_t cps = (n + ((size_t)1 << chunk_log2) - 1) >> chunk_log2;
+    const bool may_shrink = mode.kind == TCR_FIXED_ORDER || mode.block_threads == 0;
+    while (may_shrink && block_used > 32 && cps < (size_t)2 * 152) {
+        block_used /= 2;
+        warps_log2--;
+        chunk_log2--;
+        cps = (n + ((size_t)1 << chunk_log2) - 1) >> chunk_log2;
+    }
     if (cps > kNoAllocMaxPartials) return TCR_ERR_UNSUPPORTED;
 
     int dev = -1;
@@ -126,17 +135,17 @@ extern "C" tcr_status tcr_reduce_sum_noalloc(const void *x, size_t n, float *out
     if (st != TCR_OK) return st;
 
     const bool aligned = ((uintptr_t)x & 15u) == 0;
-    int occ = mode.kind == TCR_FIXED_ORDER ? occupancy_fixed(false, mode.dtype, kOpSum, aligned, block)
-                                           : occupancy_mma(false, mode.dtype, kOpSum, aligned, R, block);
+    int occ = mode.kind == TCR_FIXED_ORDER ? occupancy_fixed(false, mode.dtype, kOpSum, aligned, block_used)
+                                           : occupancy_mma(false, mode.dtype, kOpSum, aligned, R, block_used);
     if (occ <= 0) occ = 1;
     const size_t resident = (size_t)d.sms * (size_t)occ;
     const int grid = (int)(cps < resident ? cps : resident);
     float *dst = cps > 1 ? d.partials : out;
     cudaError_t e = mode.kind == TCR_FIXED_ORDER
                         ? launch_fixed_chunk(mode.dtype, kOpSum, aligned, x, n, cps, cps,
-                                             chunk_log2, dst, grid, block, s)
+                                             chunk_log2, dst, grid, block_used, s)
                         : launch_mma_chunk(mode.dtype, kOpSum, aligned, R, x, n, cps, cps,
-                                           chunk_log2, dst, grid, block, s);
+                                           chunk_log2, dst, grid, block_used, s);
     if (e == cudaSuccess && cps > 1) e = launch_combine(d.partials, 1, cps, out, s);
     return e == cudaSuccess ? TCR_OK : TCR_ERR_CUDA;
 }

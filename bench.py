@@ -563,6 +563,28 @@ def extras_arm(args):
         gbps = nbytes / us / 1e3
         print(json.dumps({"extra": name, "us": round(us, 2), "gbps": round(gbps, 1),
                           "frac": round(gbps / peak, 4), "steps": args.steps}), flush=True)
+    # small inputs (2^20 fp16, 2 MiB -- launch-bound): each call timed alone
+    # between two writes of a 256 MiB buffer, so its input is not in L2
+    x20 = xs[:1 << 20]
+    flush = torch.empty(1 << 26, dtype=torch.float32, device="cuda")
+    for kind in (tcr.MMA_CHAIN, tcr.FIXED_ORDER, tcr.SHUFFLE_TREE, tcr.MMA_CHAIN_TMEM):
+        m = tcr.Mode(kind)
+        for _ in range(args.warmup):
+            tcr.tcr_reduce_sum(x20, m, out=out[:1])
+        times = []
+        for _ in range(args.steps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            tcr.tcr_reduce_sum(x20, m, out=out[:1])
+            e1.record()
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1) * 1e3)
+        us = statistics.median(times)
+        print(json.dumps({"extra": "small_sum_2p20/" + tcr.KIND_NAMES[kind], "us": round(us, 2),
+                          "gbps": round(2 * (1 << 20) / us / 1e3, 1), "l2": "flushed",
+                          "launches": tcr.tcr_order_descriptor(n=1 << 20, mode=m)["launches"],
+                          "statistic": "median", "steps": args.steps}), flush=True)
     return 0
 
 

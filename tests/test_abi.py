@@ -113,11 +113,12 @@ def test_shuffle_descriptor_matches_the_declared_rule(lib, L, block, dtype):
 
 
 def test_binary32_descriptors(lib):
-    # a warp span is 16 KiB: 2^13 16-bit inputs, 2^12 binary32 inputs
+    # a warp span is 16 KiB: 2^13 16-bit inputs, 2^12 binary32 inputs (at a
+    # length where no CTA size is shrunk)
     for blk in (32, 256, 1024):
-        d16 = tcr.tcr_order_descriptor(n=1 << 24, mode=tcr.Mode(tcr.FIXED_ORDER, block_threads=blk))
+        d16 = tcr.tcr_order_descriptor(n=1 << 28, mode=tcr.Mode(tcr.FIXED_ORDER, block_threads=blk))
         d32 = tcr.tcr_order_descriptor(
-            n=1 << 24, mode=tcr.Mode(tcr.FIXED_ORDER, block_threads=blk, dtype=tcr.F32))
+            n=1 << 28, mode=tcr.Mode(tcr.FIXED_ORDER, block_threads=blk, dtype=tcr.F32))
         assert d32["chunk_log2"] == d16["chunk_log2"] - 1
         assert d32["partials"] == 2 * d16["partials"]
     # rows of up to 32 KiB take one warp each: 16384 16-bit or 8192 binary32 inputs
@@ -254,3 +255,24 @@ def test_gemm_descriptor_rule(lib):
     assert lib.tcr_gemm_splitk(FAKE, FAKE, FAKE, 8, 8, 12, 0, 0, None) == tcr.ERR_INVALID_ARG
     assert lib.tcr_gemm_splitk(FAKE + 8, FAKE, FAKE, 8, 8, 16, 0, 0, None) == tcr.ERR_INVALID_ARG
     assert lib.tcr_gemm_splitk(FAKE, FAKE, FAKE + 2, 8, 8, 16, 0, 0, None) == tcr.ERR_INVALID_ARG
+
+
+
+def test_small_inputs_get_smaller_ctas(lib):
+    # FIXED_ORDER (bits independent of the CTA size) and default-size MMA_CHAIN
+    # halve the CTA, from the requested (or default 256) size, until there are
+    # 2 x 152 work units of 2^13 x warps inputs or the CTA is one warp; a
+    # caller's MMA_CHAIN block size is kept
+    def expected(n, blk):
+        while blk > 32 and -(-n // (8192 * (blk // 32))) < 304:
+            blk //= 2
+        return blk
+    for n in (1 << 20, 1 << 22, 1 << 24, 1 << 26, 1 << 30):
+        for m, start in ((tcr.Mode(tcr.FIXED_ORDER), 256),
+                         (tcr.Mode(tcr.FIXED_ORDER, block_threads=1024), 1024),
+                         (tcr.Mode(tcr.MMA_CHAIN), 256)):
+            d = tcr.tcr_order_descriptor(n=n, mode=m)
+            assert d["launch_block"] == expected(n, start), (n, m)
+    assert tcr.tcr_order_descriptor(n=1 << 20, mode=tcr.Mode(tcr.FIXED_ORDER))["launch_block"] == 32
+    d = tcr.tcr_order_descriptor(n=1 << 20, mode=tcr.Mode(tcr.MMA_CHAIN, block_threads=256))
+    assert d["launch_block"] == 256
