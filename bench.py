@@ -564,16 +564,19 @@ def extras_arm(args):
         print(json.dumps({"extra": name, "us": round(us, 2), "gbps": round(gbps, 1),
                           "frac": round(gbps / peak, 4), "steps": args.steps}), flush=True)
     # small inputs (2^20 fp16, 2 MiB -- launch-bound): each call timed alone
-    # between two writes of a 256 MiB buffer, so its input is not in L2
+    # after a read of a 256 MiB buffer (which evicts the input from L2 and,
+    # unlike a write, leaves no dirty lines whose write-back the call would
+    # wait behind); the GPU is busy with that read while the call is enqueued,
+    # so the events see device time only
     x20 = xs[:1 << 20]
-    flush = torch.empty(1 << 26, dtype=torch.float32, device="cuda")
+    flush = torch.ones(1 << 26, dtype=torch.float32, device="cuda")
     for kind in (tcr.MMA_CHAIN, tcr.FIXED_ORDER, tcr.SHUFFLE_TREE, tcr.MMA_CHAIN_TMEM):
         m = tcr.Mode(kind)
         for _ in range(args.warmup):
             tcr.tcr_reduce_sum(x20, m, out=out[:1])
         times = []
         for _ in range(args.steps):
-            flush.zero_()
+            flush.sum()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
             tcr.tcr_reduce_sum(x20, m, out=out[:1])
