@@ -59,6 +59,12 @@
  * cudaFreeAsync on `stream`), so concurrent calls on different streams do
  * not share scratch.  The library keeps no other state between calls except
  * per-device launch-plan caches.  Every call runs on the current device.
+ * Calls may come from several host threads at once, each on its own stream.
+ * After one eager call of a kind on a device (which fills that device's
+ * caches and sets the kernels' attributes), the reduction, rows, moments and
+ * GEMM calls may be captured into a CUDA graph on a capturing stream; each
+ * replay gives the eager call's bits.  (Not tcr_reduce_sum_noalloc, which
+ * makes no such statement.)
  *
  * Errors.  Invalid arguments return TCR_ERR_INVALID_ARG before any GPU work
  * and leave *out untouched.  A CUDA error (allocation or launch) returns
