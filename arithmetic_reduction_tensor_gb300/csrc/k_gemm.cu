@@ -365,10 +365,10 @@ cudaError_t launch_gemm_splitk(int dtype, const void *A, const void *W, size_t M
     const cuuint64_t dw[2] = {(cuuint64_t)K, (cuuint64_t)N};
     if (encode(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, (void *)A, da, gstride, abox, estride,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
         encode(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, (void *)W, dw, gstride, wbox, estride,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     cudaError_t e = set_smem_once(k, kGmSmemBytes);
     if (e != cudaSuccess) return e;
