@@ -1,0 +1,58 @@
+// k_packed.cu -- launcher of the packed short-row kernels (packed.cuh).
+#include "packed.cuh"
+
+namespace tcr {
+
+static const void *pick(int family, int dtype, int op, int R, int vlog, bool aligned)
+{
+    switch (family) {
+    case kPackedFixed: return packed_pick_fixed(dtype, op, vlog, aligned);
+    case kPackedShuffle: return packed_pick_shuffle(dtype, op, vlog, aligned);
+    case kPackedMma: return op == kOpSum ? packed_pick_mma(dtype, vlog, R, aligned) : nullptr;
+    default: return nullptr;
+    }
+}
+
+int packed_rows_vlog(int family, size_t cols, int vector_len)
+{
+    const size_t nvec = (cols + (size_t)vector_len - 1) / (size_t)vector_len;
+    int v = 0;
+    while (((size_t)1 << v) < nvec) v++;
+    if (family == kPackedMma && v < 2) v = 2;
+    return v <= kPackedMaxVlog ? v : -1;
+}
+
+bool packed_rows_supported(int family, int dtype, int op, size_t cols, int vector_len, bool aligned)
+{
+    const int v = packed_rows_vlog(family, cols, vector_len);
+    return cols > 0 && v >= 0 && pick(family, dtype, op, 1, v, aligned) != nullptr;
+}
+
+size_t packed_rows_groups(size_t rows, int vlog)
+{
+    const size_t rpg = (size_t)256 >> vlog;
+    return (rows + rpg - 1) / rpg;
+}
+
+cudaError_t launch_packed_rows(int family, int dtype, int op, int R, bool aligned, const void *x,
+                               size_t rows, size_t cols, int vlog, float *out, int grid, int block,
+                               cudaStream_t stream)
+{
+    const void *k = pick(family, dtype, op, R, vlog, aligned);
+    if (!k || block != kRowsBlock) return cudaErrorInvalidValue;
+    void *args[] = {(void *)&x, (void *)&rows, (void *)&cols, (void *)&out};
+    return cudaLaunchKernel(k, dim3(grid), dim3(block), args, 0, stream);
+}
+
+int occupancy_packed(int family, int dtype, int op, int R, int vlog, bool aligned)
+{
+    const void *k = pick(family, dtype, op, R, vlog, aligned);
+    int n = 0;
+    if (!k || cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, kRowsBlock, 0) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+}  // namespace tcr

@@ -56,6 +56,21 @@ cudaError_t launch_mma_chunk(int dtype, int op, bool aligned, int R, const void 
 cudaError_t launch_mma_rows(int dtype, int op, bool aligned, int R, const void *x, size_t rows,
                             size_t cols, float *out, int grid, int block, cudaStream_t stream);
 
+// ---- short rows, several to a warp group (packed.cuh): family kPackedFixed
+// (FIXED_ORDER), kPackedShuffle (SHUFFLE_TREE, one-warp team) or kPackedMma
+// (MMA_CHAIN, 16-bit sums).  A row takes 2^vlog vector slots
+// (packed_rows_vlog: -1 when the row is too long to pack); `aligned` as for
+// the launch (x 16-byte aligned and rows whole vectors); CTAs of kRowsBlock
+// threads, one warp per group of 256 >> vlog rows.
+constexpr int kPackedFixed = 0, kPackedShuffle = 1, kPackedMma = 2;
+int packed_rows_vlog(int family, size_t cols, int vector_len);
+bool packed_rows_supported(int family, int dtype, int op, size_t cols, int vector_len, bool aligned);
+size_t packed_rows_groups(size_t rows, int vlog);
+cudaError_t launch_packed_rows(int family, int dtype, int op, int R, bool aligned, const void *x,
+                               size_t rows, size_t cols, int vlog, float *out, int grid, int block,
+                               cudaStream_t stream);
+int occupancy_packed(int family, int dtype, int op, int R, int vlog, bool aligned);
+
 // ---- MMA_CHAIN on tcgen05 (bulk copies into shared memory, D in TMEM):
 // one persistent CTA per SM; dst[u] is the partial of work unit u (2^16
 // inputs, see tmem_unit_log2); x must be 16-byte aligned.

@@ -1,0 +1,431 @@
+// packed.cuh -- short rows, several to a warp group.
+//
+// The one-warp-per-row kernels walk a row in groups of 8 warp loads x 32
+// lanes = 256 vectors (16 bytes each), so a row of a few hundred inputs
+// leaves most of its group's loads empty and the warp holds too few bytes
+// in flight.  Here a matrix whose rows hold at most 128 vectors is packed:
+// a row gets W = 2^VLOG vector slots (the least power of two covering it;
+// at least 4 for MMA_CHAIN), and a group's 256 slots hold 256 / W rows --
+// lane j of load k holds slot 32 k + j, i.e. vector (32 k + j) mod W of
+// group row (32 k + j) / W.  Slots past a row's vectors, or of rows past the
+// matrix, read as the mode's pad (-0.0; zero bits for the tensor cores).
+// The next group's loads are issued before the current group is reduced.
+//
+// Each mode keeps the order it declares for a row:
+//
+//   FIXED_ORDER   the vectors' trees, then the balanced tree over the row's
+//                 vectors in lane order: lane pairs (j, j^1), then (j, j^2),
+//                 ... within a sub-warp of W lanes (VLOG <= 5), or the whole
+//                 load's tree followed by the tree over the row's loads
+//                 (VLOG 6, 7) -- aligned subtrees of the row's balanced tree
+//                 padded with -0.0;
+//   SHUFFLE_TREE  the one-warp team: lane j of the row adds its vectors in
+//                 load order from -0.0, then the butterfly with offsets 16,
+//                 8, 4, 2, 1.  A row of W < 32 slots sits in a sub-warp whose
+//                 missing lanes would hold -0.0, so the butterfly's steps
+//                 with offsets >= W add -0.0 (no change) and the rest run
+//                 inside the sub-warp;
+//   MMA_CHAIN     16-bit sums: one m16n8k16 MMA against ones per load.  D
+//                 row g of the MMA sums lane quad g's four vectors (d0 + d2),
+//                 so a row of at least one quad is the sum over its quads; a
+//                 row spanning L loads chains its L MMAs, flushed every R.
+//
+// The lane-pair steps use a reduce-scatter: a lane carries one value per
+// load (or row), and at each of the first steps the two lanes of a pair
+// split the values -- the lane whose offset bit is set keeps the upper
+// half -- so 8 values need 4 + 2 + 1 shuffles instead of 3 x 8.  Every sum
+// is still the sum of the same two operands (addition commutes bit for
+// bit), so the order is unchanged; only which lane forms it differs.
+#pragma once
+
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace tcr {
+
+constexpr int kPackedMaxVlog = 7;         // rows of at most 128 vectors
+
+// One reduce-scatter step over H value pairs: v[i] (i < H) becomes the sum
+// over lanes j, j^o of the item kept, item_base advancing by H in the lane
+// that keeps the upper half.
+template <int H>
+__device__ __forceinline__ void rs_step(float (&v)[8], int lane, int o, int &item_base)
+{
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < H; i++) {
+        const float keep = up ? v[i + H] : v[i];
+        const float send = up ? v[i] : v[i + H];
+        v[i] = __fadd_rn(keep, __shfl_xor_sync(kFull, send, o));
+    }
+    if (up) item_base += H;
+}
+
+// NS reduce-scatter steps over 8 items with offsets o1, o2, o3 (the first
+// NS of them), leaving 8 >> NS values: v[i] = item item_base + i.
+template <int NS>
+__device__ __forceinline__ void rs_steps(float (&v)[8], int lane, int o1, int o2, int o3, int &item_base)
+{
+    if constexpr (NS >= 1) rs_step<4>(v, lane, o1, item_base);
+    if constexpr (NS >= 2) rs_step<2>(v, lane, o2, item_base);
+    if constexpr (NS >= 3) rs_step<1>(v, lane, o3, item_base);
+}
+
+// ---------------------------------------------------------------- loads
+//
+// Aligned rows (x 16-byte aligned, rows whole vectors): slot (k, lane) is
+// one 16-byte load of its vector.
+//
+// Other rows: the group's rows are contiguous, so the vector of slot
+// (k, lane) -- inputs e .. e + V - 1 of the group, e = row * cols + V * v --
+// lies in 16-byte granule (hoff + e * EB) / 16 of the group (hoff: the
+// group's byte offset in its first granule) and the next one.  Each slot
+// loads its first granule whole (it holds an input of the matrix, so the
+// load stays inside the data); the second one is the first granule of the
+// next slot.  Inside a row that slot holds vector v + 1 (or, past the
+// row's last vector, the granule after it).  After a row's last slot it is
+// the next row's first slot, whose granule holds the row's end: when the
+// last vector reaches into a second granule, the row ends inside that
+// granule, so it is the one the next row starts in.  For the last row of
+// the matrix the slot of the row past it loads that granule when it still
+// holds data, and the group's own last slot takes the first granule of the
+// rows after the group from one extra load (lane 31).  The vector is
+// shifted out of the two granules when the group is reduced, while the
+// next group's loads are in flight.
+
+struct PackedGeom {
+    const uint4 *gbase;   // the group's first granule
+    uint32_t hoff;        // byte offset of the group's first input in it
+    uint32_t glim;        // last granule index (from gbase) inside the data
+};
+
+template <int DT>
+__device__ __forceinline__ PackedGeom packed_geom(const typename Elem<DT>::T *x, size_t rows, size_t cols,
+                                                  size_t row0)
+{
+    const uintptr_t a = (uintptr_t)(x + row0 * cols);
+    const uintptr_t last = (uintptr_t)(x + rows * cols) - 1;
+    const uintptr_t gaddr = a & ~(uintptr_t)15;
+    const size_t gl = (size_t)(last - gaddr) >> 4;
+    PackedGeom g;
+    g.gbase = reinterpret_cast<const uint4 *>(gaddr);
+    g.hoff = (uint32_t)(a & 15);
+    g.glim = gl > 0xffffffffu ? 0xffffffffu : (uint32_t)gl;
+    return g;
+}
+
+// Load k (0..7) of the group whose first row is row0.
+template <int DT, bool ALIGNED, bool NEGZERO, int VLOG>
+__device__ __forceinline__ uint4 load_slot(const typename Elem<DT>::T *x, size_t rows, size_t cols,
+                                           size_t row0, const PackedGeom &gm, int k, int lane)
+{
+    constexpr int V = Elem<DT>::kPerVec;
+    constexpr uint32_t EB = sizeof(typename Elem<DT>::T);
+    const uint32_t f = fill_word<DT, NEGZERO>();
+    const int slot = 32 * k + lane;
+    const uint32_t rr = (uint32_t)(slot >> VLOG);
+    const uint32_t v = (uint32_t)(slot & ((1 << VLOG) - 1));
+    const uint32_t c = (uint32_t)cols;                   // at most 128 vectors
+    if constexpr (ALIGNED) {
+        if (!(row0 + rr < rows && V * v < c)) return make_uint4(f, f, f, f);
+        return ld_vec<DT, true, NEGZERO>(x + (row0 + rr) * cols, cols, v);
+    } else {
+        // slots up to the one after the row's last vector, and the first
+        // slot of the row past the matrix
+        if (!((row0 + rr < rows && V * v < c + V) || (row0 + rr == rows && v == 0)))
+            return make_uint4(f, f, f, f);
+        const uint32_t gi = (gm.hoff + (rr * c + V * v) * EB) >> 4;
+        return gi <= gm.glim ? ld_stream(gm.gbase + gi) : make_uint4(f, f, f, f);
+    }
+}
+
+// Unaligned rows: the first granule of the rows after the group (lane 31).
+template <int DT, int VLOG>
+__device__ __forceinline__ uint4 load_tail(size_t rows, size_t cols, size_t row0, const PackedGeom &gm,
+                                           int lane)
+{
+    constexpr uint32_t EB = sizeof(typename Elem<DT>::T);
+    constexpr uint32_t RPG = 256u >> VLOG;
+    uint4 r = make_uint4(0u, 0u, 0u, 0u);
+    if (lane == 31 && row0 + RPG <= rows) {
+        const uint32_t gi = (gm.hoff + RPG * (uint32_t)cols * EB) >> 4;
+        if (gi <= gm.glim) r = ld_stream(gm.gbase + gi);
+    }
+    return r;
+}
+
+template <int DT, bool ALIGNED, bool NEGZERO, int VLOG>
+__device__ __forceinline__ void load_packed(uint4 (&q)[8], const typename Elem<DT>::T *x, size_t rows,
+                                            size_t cols, size_t row0, const PackedGeom &gm, int lane)
+{
+#pragma unroll
+    for (int k = 0; k < 8; k++) q[k] = load_slot<DT, ALIGNED, NEGZERO, VLOG>(x, rows, cols, row0, gm, k, lane);
+}
+
+// The vector of slot (k, lane) of an unaligned group from the granules in
+// q: this lane's q[k] and the next slot's (lane + 1's; lane 0's q[k + 1]
+// for lane 31; the tail granule qt for the group's last slot), shifted by
+// the vector's byte offset; inputs past the row, and every input of a row
+// past the matrix, read as the fill.  Every lane of the warp takes part
+// (shuffles).
+template <int DT, bool NEGZERO, int VLOG>
+__device__ __forceinline__ uint4 unaligned_vec(const uint4 (&q)[8], const uint4 &qt, int k, int lane,
+                                               uint32_t hoff, size_t rows, size_t cols, size_t row0)
+{
+    constexpr int V = Elem<DT>::kPerVec;
+    constexpr int EB = (int)sizeof(typename Elem<DT>::T);
+    const uint4 lo = q[k];
+    // lane j reads lane j + 1's value; lane 0 sends the next load's
+    // granule, for lane 31
+    uint4 snd = lo;
+    if (k < 7 && lane == 0) snd = q[k < 7 ? k + 1 : k];
+    const int src = (lane + 1) & 31;
+    uint4 hi;
+    hi.x = __shfl_sync(kFull, snd.x, src);
+    hi.y = __shfl_sync(kFull, snd.y, src);
+    hi.z = __shfl_sync(kFull, snd.z, src);
+    hi.w = __shfl_sync(kFull, snd.w, src);
+    if (k == 7 && lane == 31) hi = qt;
+    const int slot = 32 * k + lane;
+    const uint32_t rr = (uint32_t)(slot >> VLOG);
+    const int v = slot & ((1 << VLOG) - 1);
+    const uint32_t sb = (hoff + (rr * (uint32_t)cols + (uint32_t)(V * v)) * EB) & 15u;
+    int cnt = (int)cols - V * v;
+    cnt = cnt < 0 ? 0 : (cnt > V ? V : cnt);
+    if (!(row0 + rr < rows)) cnt = 0;
+    // shift the 8 words by sb bytes: 2 words, 1 word, then half a word
+    const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+    const uint32_t p = sb >> 2;
+    uint32_t u[6], t[5], o[4];
+#pragma unroll
+    for (int i = 0; i < 6; i++) u[i] = (p & 2) ? w[i + 2] : w[i];
+#pragma unroll
+    for (int i = 0; i < 5; i++) t[i] = (p & 1) ? u[i + 1] : u[i];
+    const uint32_t hs = (sb & 2u) << 3;                  // 0 or 16 (0 for binary32)
+    const uint32_t f = fill_word<DT, NEGZERO>();
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        o[i] = __funnelshift_r(t[i], t[i + 1], hs);
+        // keep the low bits of the word that hold inputs below cnt
+        const int kb = cnt * 8 * EB - 32 * i;
+        const uint32_t m = __funnelshift_lc(0xffffffffu, 0u, (uint32_t)(kb < 0 ? 0 : kb));
+        o[i] = (o[i] & m) | (f & ~m);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// Row values of a group for FIXED_ORDER and SHUFFLE_TREE; t[k] = the
+// lane's vector tree of load k.  Writes out[row] for the group's rows.
+template <int MODE, int VLOG>
+__device__ __forceinline__ void packed_tree_rows(float (&t)[8], int lane, size_t row0, size_t rows,
+                                                 float *__restrict__ out)
+{
+    constexpr int W = 1 << VLOG;
+    if constexpr (VLOG <= 5) {
+        constexpr int NS = VLOG < 3 ? VLOG : 3;
+        constexpr int M = 8 >> NS;               // values left per lane
+        int base = 0;
+        bool writer;
+        if constexpr (MODE == kPackedFixed) {
+            // ascending offsets 1, 2, 4 (scatter), then 8, 16 below W
+            rs_steps<NS>(t, lane, 1, 2, 4, base);
+#pragma unroll
+            for (int o = 8; o < W; o <<= 1) t[0] = __fadd_rn(t[0], __shfl_xor_sync(kFull, t[0], o));
+            writer = (lane & (W - 1)) < (1 << NS);
+        } else {
+            // the one-warp butterfly: offsets W/2, W/4, W/8 (scatter), then
+            // the rest down to 1; the lane's start value -0.0 + t is t
+            rs_steps<NS>(t, lane, W >> 1, W >> 2, W >> 3, base);
+#pragma unroll
+            for (int o = W >> 4; o >= 1; o >>= 1) t[0] = __fadd_rn(t[0], __shfl_xor_sync(kFull, t[0], o));
+            writer = (lane & ((W >> NS) - 1)) == 0;
+        }
+        if (writer) {
+#pragma unroll
+            for (int i = 0; i < M; i++) {
+                const size_t row = row0 + (size_t)((base + i) * (32 >> VLOG) + (lane >> VLOG));
+                if (row < rows) out[row] = t[i];
+            }
+        }
+    } else {
+        constexpr int LL = VLOG - 5;             // log2 loads per row
+        constexpr int L = 1 << LL;
+        constexpr int M = 8 >> LL;               // rows per group
+        if constexpr (MODE == kPackedFixed) {
+            // each load's tree (scatter 1, 2, 4, then 8, 16); loads k, k^1
+            // then sit in lanes j, j^4 and loads k, k^2 in lanes j, j^2
+            int base = 0;
+            rs_steps<3>(t, lane, 1, 2, 4, base);
+            t[0] = __fadd_rn(t[0], __shfl_xor_sync(kFull, t[0], 8));
+            t[0] = __fadd_rn(t[0], __shfl_xor_sync(kFull, t[0], 16));
+            t[0] = __fadd_rn(t[0], __shfl_xor_sync(kFull, t[0], 4));
+            if constexpr (LL >= 2) t[0] = __fadd_rn(t[0], __shfl_xor_sync(kFull, t[0], 2));
+            const size_t row = row0 + (size_t)(base >> LL);
+            if (lane < M && row < rows) out[row] = t[0];
+        } else {
+            // lane j adds its vectors of each row in load order, then the
+            // butterfly 16, 8, 4, 2, 1 over the M row values
+            float a[8];
+#pragma unroll
+            for (int r = 0; r < 8; r++) a[r] = 0.f;
+#pragma unroll
+            for (int r = 0; r < M; r++) {
+                float s = -0.0f;
+#pragma unroll
+                for (int k = 0; k < L; k++) s = __fadd_rn(s, t[r * L + k]);
+                a[r] = s;
+            }
+            constexpr int NS = LL == 1 ? 2 : 1;  // log2 M
+            int base = 0;
+            if constexpr (NS == 2) {
+                rs_step<2>(a, lane, 16, base);
+                rs_step<1>(a, lane, 8, base);
+            } else {
+                rs_step<1>(a, lane, 16, base);
+            }
+#pragma unroll
+            for (int o = 16 >> NS; o >= 1; o >>= 1) a[0] = __fadd_rn(a[0], __shfl_xor_sync(kFull, a[0], o));
+            const size_t row = row0 + (size_t)base;
+            if ((lane & ((32 >> NS) - 1)) == 0 && row < rows) out[row] = a[0];
+        }
+    }
+}
+
+// The packed kernel: one warp per group of 256 / W rows, grid-stride over
+// the groups.  R is the chain length of MMA_CHAIN (rows of 6 or 7 VLOG
+// only; 1 otherwise).
+template <int DT, int OP, int MODE, int VLOG, int R, bool ALIGNED>
+__global__ void __launch_bounds__(kRowsBlock, kRowsMinCtas)
+packed_rows_kernel(const void *__restrict__ xv, size_t rows, size_t cols, float *__restrict__ out)
+{
+    static_assert(MODE != kPackedMma || VLOG >= 2, "a tensor-core row is at least one lane quad");
+    using T = typename Elem<DT>::T;
+    constexpr bool NZ = MODE != kPackedMma;
+    const T *__restrict__ x = static_cast<const T *>(xv);
+    const int lane = threadIdx.x & 31;
+    const size_t nw = ((size_t)gridDim.x * blockDim.x) >> 5;
+    constexpr size_t RPG = (size_t)256 >> VLOG;          // rows per group
+    const size_t groups = (rows + RPG - 1) / RPG;
+    size_t gi = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (gi >= groups) return;
+    uint4 q[8], qt = make_uint4(0u, 0u, 0u, 0u);
+    PackedGeom gm{};
+    if constexpr (!ALIGNED) {
+        gm = packed_geom<DT>(x, rows, cols, gi * RPG);
+        qt = load_tail<DT, VLOG>(rows, cols, gi * RPG, gm, lane);
+    }
+    load_packed<DT, ALIGNED, NZ, VLOG>(q, x, rows, cols, gi * RPG, gm, lane);
+    for (;;) {
+        const size_t row0 = gi * RPG;
+        const size_t ngi = gi + nw;
+        const bool has_next = ngi < groups;
+        const uint32_t hoff = gm.hoff;                   // this group's (unaligned rows)
+        if constexpr (!ALIGNED)
+            if (has_next) gm = packed_geom<DT>(x, rows, cols, ngi * RPG);
+        // the vector of load k of this group
+        auto vec = [&](int k) -> uint4 {
+            if constexpr (ALIGNED) return q[k];
+            else return unaligned_vec<DT, NZ, VLOG>(q, qt, k, lane, hoff, rows, cols, row0);
+        };
+        // after the last load of this group is consumed: the next group's tail
+        auto next_tail = [&]() {
+            if constexpr (!ALIGNED)
+                if (has_next) qt = load_tail<DT, VLOG>(rows, cols, ngi * RPG, gm, lane);
+        };
+        if constexpr (MODE == kPackedMma) {
+            // each load's next-group load is issued as soon as the load has
+            // been consumed, so few registers are live beside the loads in
+            // flight (the same below for the trees)
+            float v[8];
+            const size_t nrow0 = ngi * RPG;
+            if constexpr (VLOG <= 5) {
+                // one MMA per load: lane quad g's total is d0 + d2
+#pragma unroll
+                for (int k = 0; k < 8; k++) {
+                    float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
+                    const uint4 a = vec(k);
+                    mma_ones<DT>(d0, d1, d2, d3, a.x, a.y, a.z, a.w);
+                    if (has_next) q[k] = load_slot<DT, ALIGNED, NZ, VLOG>(x, rows, cols, nrow0, gm, k, lane);
+                    v[k] = __fadd_rn(d0, d2);
+                }
+                next_tail();
+            } else {
+                // a row's L loads: chains of R MMAs, each chain's d0 and d2
+                // added into the row's two accumulators
+                constexpr int L = 1 << (VLOG - 5), M = 8 / L;
+#pragma unroll
+                for (int r = 0; r < 8; r++) v[r] = 0.f;
+#pragma unroll
+                for (int r = 0; r < M; r++) {
+                    float lo = 0.f, hi = 0.f, d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
+#pragma unroll
+                    for (int k = 0; k < L; k++) {
+                        const int j = r * L + k;
+                        const uint4 a = vec(j);
+                        mma_ones<DT>(d0, d1, d2, d3, a.x, a.y, a.z, a.w);
+                        if (has_next) q[j] = load_slot<DT, ALIGNED, NZ, VLOG>(x, rows, cols, nrow0, gm, j, lane);
+                        if ((k + 1) % R == 0 || k == L - 1) {
+                            lo = __fadd_rn(lo, d0);
+                            hi = __fadd_rn(hi, d2);
+                            d0 = d1 = d2 = d3 = 0.f;
+                        }
+                    }
+                    v[r] = __fadd_rn(lo, hi);
+                }
+                next_tail();
+            }
+            // sums over the row's lane quads: ascending offsets 4, 8, 16
+            if constexpr (VLOG <= 5) {
+                constexpr int NS = VLOG - 2;           // offsets 4 .. W/2, all scattered
+                constexpr int M = 8 >> NS;
+                int base = 0;
+                rs_steps<NS>(v, lane, 4, 8, 16, base);
+                if ((lane & 3) == 0) {
+#pragma unroll
+                    for (int i = 0; i < M; i++) {
+                        const size_t row = row0 + (size_t)((base + i) * (32 >> VLOG) + (lane >> VLOG));
+                        if (row < rows) out[row] = v[i];
+                    }
+                }
+            } else {
+                constexpr int NS = VLOG == 6 ? 2 : 1;  // log2 rows per group
+                int base = 0;
+                if constexpr (NS == 2) {
+                    rs_step<2>(v, lane, 4, base);
+                    rs_step<1>(v, lane, 8, base);
+                } else {
+                    rs_step<1>(v, lane, 4, base);
+                }
+#pragma unroll
+                for (int o = 4 << NS; o < 32; o <<= 1) v[0] = __fadd_rn(v[0], __shfl_xor_sync(kFull, v[0], o));
+                const size_t row = row0 + (size_t)base;
+                if ((lane & 3) == 0 && lane < (4 << NS) && row < rows) out[row] = v[0];
+            }
+        } else {
+            float t[8];
+#pragma unroll
+            for (int k = 0; k < 8; k++) {
+                t[k] = vec_tree<DT, OP>(vec(k));
+                if (has_next) q[k] = load_slot<DT, ALIGNED, NZ, VLOG>(x, rows, cols, ngi * RPG, gm, k, lane);
+                if constexpr (VLOG == 0) {
+                    // a row is one vector: its value is the vector's tree
+                    // (SHUFFLE_TREE: -0.0 + tree, the same bits)
+                    const size_t row = row0 + (size_t)(32 * k + lane);
+                    if (row < rows) out[row] = t[k];
+                }
+            }
+            next_tail();
+            if constexpr (VLOG > 0) packed_tree_rows<MODE, VLOG>(t, lane, row0, rows, out);
+        }
+        if (!has_next) break;
+        gi = ngi;
+    }
+}
+
+// Kernel pointers of each mode (k_packed_*.cu); nullptr where the mode has
+// no packed kernel for the arguments.
+const void *packed_pick_fixed(int dtype, int op, int vlog, bool aligned);
+const void *packed_pick_shuffle(int dtype, int op, int vlog, bool aligned);
+const void *packed_pick_mma(int dtype, int vlog, int R, bool aligned);
+
+}  // namespace tcr

@@ -99,7 +99,7 @@ cudaMemPool_t pool_for(int dev)
     return d.pool;
 }
 
-enum Family { kFixedF, kShuffleF, kMmaF, kBlockedF };
+enum Family { kFixedF, kShuffleF, kMmaF, kBlockedF, kPackedF };
 
 int occupancy(int dev, Family fam, bool rows, int dtype, int op, bool aligned, int R, int block)
 {
@@ -116,6 +116,10 @@ int occupancy(int dev, Family fam, bool rows, int dtype, int op, bool aligned, i
         case kBlockedF: n = occupancy_blocked(dtype, aligned, block); break;
         case kShuffleF: n = occupancy_shuffle(rows, dtype, op, aligned, block); break;
         case kMmaF: n = occupancy_mma(rows, dtype, op, aligned, R, block); break;
+        case kPackedF:
+            // R carries the packed family, the row width and the chain length
+            n = occupancy_packed(R / 100, dtype, op, R % 10, (R / 10) % 10, aligned);
+            break;
         }
     }
     if (n <= 0) n = 1;
@@ -135,13 +139,15 @@ enum Path {
     kPathShuffleRowsWarp, // SHUFFLE warp team, one warp per row
     kPathTmem,           // MMA_CHAIN on tcgen05 (+ combine if units > 1)
     kPathTmemRows,       // MMA_CHAIN rows on tcgen05 (+ combine if chunks > 1)
-    kPathBlocked         // FIXED blocked order, runs longer than a vector (+ combine)
+    kPathBlocked,        // FIXED blocked order, runs longer than a vector (+ combine)
+    kPathPackedRows      // short rows, several to a warp group (FIXED, SHUFFLE, MMA)
 };
 
 struct Plan {
     int kind, dtype, op, R, block;
     int run_log2;            // blocked order: log2 run length (0: the plain tree)
     int vrun;                // runs inside a vector: the warp-stream kernels' variant
+    int packed, vlog;        // packed rows: kernel family, log2 vector slots per row
     bool aligned;
     Path path;
     size_t segments, seg_len;
@@ -292,9 +298,31 @@ void plan_blocked(Plan &p, bool rows_call, int dev)
     p.launches = p.cps > 1 ? 2 : 1;
 }
 
+constexpr size_t kTmemRowsMinCols = 256;
+
+// Short rows, several to a warp group: one launch of kRowsBlock threads,
+// as many CTAs as there are groups of 8 warps' rows, at most a full wave.
+void plan_packed(Plan &p, int family, int dev)
+{
+    p.path = kPathPackedRows;
+    p.packed = family;
+    p.vlog = packed_rows_vlog(family, p.seg_len, vector_len(p.dtype));
+    p.block = kRowsBlock;
+    const size_t warps_per_cta = (size_t)p.block / 32;
+    const size_t groups = packed_rows_groups(p.segments, p.vlog);
+    const size_t need = (groups + warps_per_cta - 1) / warps_per_cta;
+    const int key = family * 100 + p.vlog * 10 + (p.R > 0 ? p.R : 1);
+    const size_t resident = (size_t)sm_count(dev) *
+                            (size_t)occupancy(dev, kPackedF, true, p.dtype, p.op, p.aligned, key, p.block);
+    p.grid = (int)(need < resident ? need : resident);
+    p.launches = 1;
+}
+
 // Plans tcr_reduce_sum (rows == 0: one segment of n) or tcr_reduce_rows.
+// allow_packed: rows short enough to share a warp group take the packed
+// kernels (single reductions only; the fused pairs run one warp per row).
 Plan make_plan(size_t segments, size_t seg_len, bool rows_call, const tcr_mode &m, int op,
-               int block, int R, bool aligned, int dev)
+               int block, int R, bool aligned, int dev, bool allow_packed = true)
 {
     Plan p;
     std::memset(&p, 0, sizeof p);
@@ -318,7 +346,10 @@ Plan make_plan(size_t segments, size_t seg_len, bool rows_call, const tcr_mode &
     const size_t sms = (size_t)sm_count(dev);
     if (m.kind == TCR_SHUFFLE_TREE) {
         shuffle_team(seg_len, vector_len(p.dtype), block, &p.team_threads, &p.team_blocks);
-        if (p.team_threads == 32 && p.team_blocks == 1) {
+        if (p.team_threads == 32 && p.team_blocks == 1 && rows_call && allow_packed &&
+            packed_rows_supported(kPackedShuffle, p.dtype, op, seg_len, vector_len(p.dtype), aligned)) {
+            plan_packed(p, kPackedShuffle, dev);
+        } else if (p.team_threads == 32 && p.team_blocks == 1) {
             // a team of one warp: pack one segment per warp, 8 per CTA
             p.path = kPathShuffleRowsWarp;
             p.block = kRowsBlock;
@@ -337,6 +368,9 @@ Plan make_plan(size_t segments, size_t seg_len, bool rows_call, const tcr_mode &
         }
         return p;
     }
+    // rows of fewer than 256 inputs run the packed mma.sync kernel: a
+    // 128-row tile of them is mostly the tensor map's fill
+    if (p.kind == TCR_MMA_CHAIN_TMEM && rows_call && seg_len < kTmemRowsMinCols) p.kind = TCR_MMA_CHAIN;
     if (p.kind == TCR_MMA_CHAIN_TMEM && rows_call && aligned && segments < ((size_t)1 << 31) &&
         seg_len < ((size_t)1 << 31)) {
         // 128 rows per MMA tile, 2-D tensor-map copies; one CTA per SM
@@ -375,6 +409,13 @@ Plan make_plan(size_t segments, size_t seg_len, bool rows_call, const tcr_mode &
     }
     const Family fam = m.kind == TCR_FIXED_ORDER ? kFixedF : kMmaF;
     const int occ_r = m.kind == TCR_FIXED_ORDER ? p.vrun : R;
+    if (rows_call && allow_packed && p.vrun == 0) {
+        const int pf = m.kind == TCR_FIXED_ORDER ? kPackedFixed : kPackedMma;
+        if (packed_rows_supported(pf, p.dtype, op, seg_len, vector_len(p.dtype), aligned)) {
+            plan_packed(p, pf, dev);
+            return p;
+        }
+    }
     if (rows_call && seg_len <= kRowsWarpMaxBytes / elem_bytes(p.dtype)) {
         // one warp per row: the CTA size is a launch detail (the result does
         // not depend on it), fixed at kRowsBlock threads
@@ -455,6 +496,10 @@ tcr_status run_plan(const Plan &p, const void *x, float *out, cudaStream_t s, in
     case kPathShuffleRowsWarp:
         e = launch_shuffle_rows_warp(p.dtype, p.op, p.aligned, x, p.segments, p.seg_len, dst,
                                      p.grid, p.block, s);
+        break;
+    case kPathPackedRows:
+        e = launch_packed_rows(p.packed, p.dtype, p.op, p.R, p.aligned, x, p.segments, p.seg_len,
+                               p.vlog, dst, p.grid, p.block, s);
         break;
     default:
         e = cudaErrorInvalidValue;
@@ -608,7 +653,7 @@ tcr_status reduce_rows_pair(const void *x, size_t rows, size_t cols, float *out_
     if (dev < 0) return TCR_ERR_CUDA;
     const bool aligned = ((uintptr_t)x & 15u) == 0 && (cols % (size_t)vector_len(mode.dtype)) == 0;
     // planned as the sum of squares (the tcgen05 kind runs the mma.sync pair)
-    Plan p = make_plan(rows, cols, true, mode, kOpSquares, block, R, aligned, dev);
+    Plan p = make_plan(rows, cols, true, mode, kOpSquares, block, R, aligned, dev, false);
     return run_pair_plan(p, x, out_a, out_b, mean_var, (cudaStream_t)stream, dev);
 }
 
@@ -771,8 +816,10 @@ tcr_status tcr_order_descriptor(size_t n, size_t rows, size_t cols, tcr_mode mod
     const size_t seg_len = rows_call ? cols : n;
     if (segments * seg_len >= kMaxInputs) return TCR_ERR_INVALID_ARG;
     const int dev = current_device();
-    // the plan of an aligned input; a misaligned one differs only in speed
-    Plan p = make_plan(segments, seg_len, rows_call, mode, kOpSum, block, R, true, dev);
+    // the plan of a 16-byte aligned x (rows: aligned when they are whole
+    // vectors); another alignment differs only in speed
+    const bool aligned = !rows_call || cols % (size_t)vector_len(mode.dtype) == 0;
+    Plan p = make_plan(segments, seg_len, rows_call, mode, kOpSum, block, R, aligned, dev);
     std::memset(desc, 0, sizeof *desc);
     desc->kind = mode.kind;
     desc->order = mode.kind == TCR_SHUFFLE_TREE ? TCR_ORDER_GRID_STRIDE

@@ -37,8 +37,10 @@
  *                     reach shared memory by 2-D tensor-map copies.  Same
  *                     error bound as TCR_MMA_CHAIN.  16-bit sums only: an
  *                     x that is not 16-byte aligned (or rows whose stride is
- *                     not), sums of squares and binary32 inputs are reduced
- *                     by the TCR_MMA_CHAIN kernels instead.
+ *                     not), rows of fewer than 256 inputs (a tile of 128
+ *                     such rows fills less than one K = 16 column block per
+ *                     64-input box), sums of squares and binary32 inputs
+ *                     are reduced by the TCR_MMA_CHAIN kernels instead.
  *   TCR_FIXED_ORDER   a balanced binary tree over index order, padded with
  *                     -0.0 to a power of two ("Taming Bitwise Behavior in
  *                     GPU Kernels with Tensor Core", arXiv 2609.11356,
@@ -168,7 +170,14 @@ TCR_API tcr_status tcr_reduce_sum(const void *x, size_t n, float *out, tcr_mode 
  * Each row is reduced exactly as tcr_reduce_sum would reduce it alone for
  * TCR_FIXED_ORDER and TCR_SHUFFLE_TREE (the order depends on cols only, never
  * on rows: results are batch invariant).  Short rows need no scratch and one
- * launch; long rows use per-row partials and a combine launch.
+ * launch; long rows use per-row partials and a combine launch.  Rows of at
+ * most 128 16-byte vectors (1024 16-bit or 512 binary32 inputs) are packed
+ * several to a warp (TCR_MMA_CHAIN: 16-bit inputs); when x or the row
+ * stride is not 16-byte aligned those kernels read whole 16-byte aligned
+ * granules that hold inputs of the matrix -- up to 15 bytes before x or
+ * after its last input, never outside the granules the data touches (an
+ * allocation from cudaMalloc is 256-byte aligned, so such a granule lies
+ * inside it).
  */
 TCR_API tcr_status tcr_reduce_rows(const void *x, size_t rows, size_t cols, float *out, tcr_mode mode,
                            void *stream);

@@ -112,6 +112,34 @@ def test_shuffle_descriptor_matches_the_declared_rule(lib, L, block, dtype):
         assert d["partials"] == (0 if g == 1 else d["segments"] * g)
 
 
+def test_short_rows_are_packed(lib):
+    # rows of at most 128 vectors share a warp group: 256 / 2^v rows per warp
+    # (2^v vector slots per row, at least 4 for MMA_CHAIN), 8 warps per CTA,
+    # one launch, no scratch; longer rows take one warp each.  (Without a
+    # device the plan assumes 152 SMs and one resident CTA per SM.)
+    def grid(rows, cols, kind, dtype=tcr.F16):
+        d = tcr.tcr_order_descriptor(rows=rows, cols=cols, mode=tcr.Mode(kind, dtype=dtype))
+        assert (d["launch_block"], d["launches"], d["partials"]) == (256, 1, 0)
+        return d["launch_grid"]
+
+    for kind in (tcr.FIXED_ORDER, tcr.SHUFFLE_TREE, tcr.MMA_CHAIN):
+        assert grid(1000, 64, kind) == 4              # 8 vectors: 32 rows a warp
+        assert grid(1000, 65, kind) == 8              # 9 vectors: 16 rows a warp
+        assert grid(1000, 1024, kind) == 63           # 128 vectors: 2 rows a warp
+        assert grid(1000, 1025, kind) == 125          # one warp per row
+        assert grid(10 ** 6, 100, kind) == 152        # at most one wave
+    # rows that are not whole vectors pack the same way
+    assert grid(1000, 255, tcr.FIXED_ORDER) == 16     # 32 vectors: 8 rows a warp
+    assert grid(1000, 1020, tcr.SHUFFLE_TREE) == 63   # 128 vectors: 2 rows a warp
+    assert grid(1000, 8, tcr.FIXED_ORDER) == 1        # one vector: 256 rows a warp
+    assert grid(1000, 8, tcr.MMA_CHAIN) == 2          # one lane quad: 64 rows a warp
+    assert grid(1000, 64, tcr.FIXED_ORDER, tcr.F32) == 8
+    assert grid(1000, 512, tcr.SHUFFLE_TREE, tcr.F32) == 63
+    assert grid(1000, 513, tcr.SHUFFLE_TREE, tcr.F32) == 125
+    # binary32 MMA_CHAIN (the three-way split) keeps one warp per row
+    assert grid(1000, 64, tcr.MMA_CHAIN, tcr.F32) == 125
+
+
 def test_binary32_descriptors(lib):
     # a warp span is 16 KiB: 2^13 16-bit inputs, 2^12 binary32 inputs (at a
     # length where no CTA size is shrunk)
