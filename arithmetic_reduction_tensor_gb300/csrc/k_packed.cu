@@ -3,12 +3,12 @@
 
 namespace tcr {
 
-static const void *pick(int family, int dtype, int op, int R, int vlog, bool aligned)
+static const void *pick(int family, int dtype, int op, int R, int vlog, bool aligned, bool pair)
 {
     switch (family) {
-    case kPackedFixed: return packed_pick_fixed(dtype, op, vlog, aligned);
-    case kPackedShuffle: return packed_pick_shuffle(dtype, op, vlog, aligned);
-    case kPackedMma: return op == kOpSum ? packed_pick_mma(dtype, vlog, R, aligned) : nullptr;
+    case kPackedFixed: return packed_pick_fixed(dtype, op, vlog, aligned, pair);
+    case kPackedShuffle: return packed_pick_shuffle(dtype, op, vlog, aligned, pair);
+    case kPackedMma: return packed_pick_mma(dtype, op, vlog, R, aligned, pair);
     default: return nullptr;
     }
 }
@@ -22,10 +22,11 @@ int packed_rows_vlog(int family, size_t cols, int vector_len)
     return v <= kPackedMaxVlog ? v : -1;
 }
 
-bool packed_rows_supported(int family, int dtype, int op, size_t cols, int vector_len, bool aligned)
+bool packed_rows_supported(int family, int dtype, int op, size_t cols, int vector_len, bool aligned,
+                           bool pair)
 {
     const int v = packed_rows_vlog(family, cols, vector_len);
-    return cols > 0 && v >= 0 && pick(family, dtype, op, 1, v, aligned) != nullptr;
+    return cols > 0 && v >= 0 && pick(family, dtype, op, 1, v, aligned, pair) != nullptr;
 }
 
 size_t packed_rows_groups(size_t rows, int vlog)
@@ -38,15 +39,28 @@ cudaError_t launch_packed_rows(int family, int dtype, int op, int R, bool aligne
                                size_t rows, size_t cols, int vlog, float *out, int grid, int block,
                                cudaStream_t stream)
 {
-    const void *k = pick(family, dtype, op, R, vlog, aligned);
+    const void *k = pick(family, dtype, op, R, vlog, aligned, false);
     if (!k || block != kRowsBlock) return cudaErrorInvalidValue;
-    void *args[] = {(void *)&x, (void *)&rows, (void *)&cols, (void *)&out};
+    float *none = nullptr;
+    int mv = 0;
+    void *args[] = {(void *)&x, (void *)&rows, (void *)&cols, (void *)&out, (void *)&none, (void *)&mv};
     return cudaLaunchKernel(k, dim3(grid), dim3(block), args, 0, stream);
 }
 
-int occupancy_packed(int family, int dtype, int op, int R, int vlog, bool aligned)
+cudaError_t launch_packed_rows_pair(int family, int dtype, int R, bool aligned, const void *x,
+                                    size_t rows, size_t cols, int vlog, float *out_a, float *out_b,
+                                    int mean_var, int grid, int block, cudaStream_t stream)
 {
-    const void *k = pick(family, dtype, op, R, vlog, aligned);
+    const void *k = pick(family, dtype, kOpSum, R, vlog, aligned, true);
+    if (!k || block != kRowsBlock) return cudaErrorInvalidValue;
+    void *args[] = {(void *)&x, (void *)&rows, (void *)&cols, (void *)&out_a, (void *)&out_b,
+                    (void *)&mean_var};
+    return cudaLaunchKernel(k, dim3(grid), dim3(block), args, 0, stream);
+}
+
+int occupancy_packed(int family, int dtype, int op, int R, int vlog, bool aligned, bool pair)
+{
+    const void *k = pick(family, dtype, op, R, vlog, aligned, pair);
     int n = 0;
     if (!k || cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, kRowsBlock, 0) != cudaSuccess) {
         (void)cudaGetLastError();

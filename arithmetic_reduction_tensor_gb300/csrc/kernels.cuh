@@ -63,13 +63,19 @@ cudaError_t launch_mma_rows(int dtype, int op, bool aligned, int R, const void *
 // the launch (x 16-byte aligned and rows whole vectors); CTAs of kRowsBlock
 // threads, one warp per group of 256 >> vlog rows.
 constexpr int kPackedFixed = 0, kPackedShuffle = 1, kPackedMma = 2;
+// pair: the kernel of tcr_reduce_rows_moments / _mean_var (out_a, out_b
+// as for launch_rows_pair; op ignored).
 int packed_rows_vlog(int family, size_t cols, int vector_len);
-bool packed_rows_supported(int family, int dtype, int op, size_t cols, int vector_len, bool aligned);
+bool packed_rows_supported(int family, int dtype, int op, size_t cols, int vector_len, bool aligned,
+                           bool pair);
 size_t packed_rows_groups(size_t rows, int vlog);
 cudaError_t launch_packed_rows(int family, int dtype, int op, int R, bool aligned, const void *x,
                                size_t rows, size_t cols, int vlog, float *out, int grid, int block,
                                cudaStream_t stream);
-int occupancy_packed(int family, int dtype, int op, int R, int vlog, bool aligned);
+cudaError_t launch_packed_rows_pair(int family, int dtype, int R, bool aligned, const void *x,
+                                    size_t rows, size_t cols, int vlog, float *out_a, float *out_b,
+                                    int mean_var, int grid, int block, cudaStream_t stream);
+int occupancy_packed(int family, int dtype, int op, int R, int vlog, bool aligned, bool pair);
 
 // ---- MMA_CHAIN on tcgen05 (bulk copies into shared memory, D in TMEM):
 // one persistent CTA per SM; dst[u] is the partial of work unit u (2^16

@@ -25,10 +25,15 @@
 //                 missing lanes would hold -0.0, so the butterfly's steps
 //                 with offsets >= W add -0.0 (no change) and the rest run
 //                 inside the sub-warp;
-//   MMA_CHAIN     16-bit sums: one m16n8k16 MMA against ones per load.  D
-//                 row g of the MMA sums lane quad g's four vectors (d0 + d2),
-//                 so a row of at least one quad is the sum over its quads; a
-//                 row spanning L loads chains its L MMAs, flushed every R.
+//   MMA_CHAIN     one m16n8k16 tile against ones per load.  D row g of the
+//                 MMA sums lane quad g's four vectors (d0 + d2), so a row of
+//                 at least one quad is the sum over its quads; a row
+//                 spanning L loads chains its L tiles, flushed every R.
+//                 Squares: the tile's A * A^T diagonal.  Binary32: each
+//                 input (or its square) split exactly into three bfloat16
+//                 parts, a lane's hi and mid parts forming one tile and its
+//                 lo parts a second one chained into the same accumulator
+//                 (so a D row still holds one quad's inputs only).
 //
 // The lane-pair steps use a reduce-scatter: a lane carries one value per
 // load (or row), and at each of the first steps the two lanes of a pair
@@ -40,6 +45,7 @@
 
 #include "common.cuh"
 #include "kernels.cuh"
+#include "stream.cuh"
 
 namespace tcr {
 
@@ -214,18 +220,54 @@ __device__ __forceinline__ uint4 unaligned_vec(const uint4 (&q)[8], const uint4 
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-// Row values of a group for FIXED_ORDER and SHUFFLE_TREE; t[k] = the
-// lane's vector tree of load k.  Writes out[row] for the group's rows.
+// ---------------------------------------------------------------- rows of a group
+//
+// packed_reduce turns a lane's per-load values t[k] (FIXED_ORDER and
+// SHUFFLE_TREE: vector trees; MMA_CHAIN: lane-quad totals for VLOG <= 5,
+// per-row quad totals t[r] for VLOG 6, 7) into row values: afterwards the
+// lane holds packed_m() values t[0..M-1], t[i] being group row
+// packed_row(base, i, lane) when `writer` is set.
+
 template <int MODE, int VLOG>
-__device__ __forceinline__ void packed_tree_rows(float (&t)[8], int lane, size_t row0, size_t rows,
-                                                 float *__restrict__ out)
+__host__ __device__ constexpr int packed_m()
+{
+    if (VLOG > 5) return 1;
+    if (MODE == kPackedMma) return 8 >> (VLOG - 2);
+    return 8 >> (VLOG < 3 ? VLOG : 3);
+}
+
+template <int MODE, int VLOG>
+__device__ __forceinline__ uint32_t packed_row(int base, int i, int lane)
+{
+    if constexpr (VLOG <= 5) return (uint32_t)((base + i) * (32 >> VLOG) + (lane >> VLOG));
+    else if constexpr (MODE == kPackedFixed) return (uint32_t)(base >> (VLOG - 5));
+    else return (uint32_t)base;
+}
+
+template <int MODE, int VLOG>
+__device__ __forceinline__ int packed_reduce(float (&t)[8], int lane, bool &writer)
 {
     constexpr int W = 1 << VLOG;
-    if constexpr (VLOG <= 5) {
+    int base = 0;
+    if constexpr (MODE == kPackedMma) {
+        // sums over the row's lane quads: ascending offsets 4, 8, 16
+        if constexpr (VLOG <= 5) {
+            rs_steps<VLOG - 2>(t, lane, 4, 8, 16, base);   // offsets 4 .. W/2
+            writer = (lane & 3) == 0;
+        } else {
+            constexpr int NS = VLOG == 6 ? 2 : 1;          // log2 rows per group
+            if constexpr (NS == 2) {
+                rs_step<2>(t, lane, 4, base);
+                rs_step<1>(t, lane, 8, base);
+            } else {
+                rs_step<1>(t, lane, 4, base);
+            }
+#pragma unroll
+            for (int o = 4 << NS; o < 32; o <<= 1) t[0] = __fadd_rn(t[0], __shfl_xor_sync(kFull, t[0], o));
+            writer = (lane & 3) == 0 && lane < (4 << NS);
+        }
+    } else if constexpr (VLOG <= 5) {
         constexpr int NS = VLOG < 3 ? VLOG : 3;
-        constexpr int M = 8 >> NS;               // values left per lane
-        int base = 0;
-        bool writer;
         if constexpr (MODE == kPackedFixed) {
             // ascending offsets 1, 2, 4 (scatter), then 8, 16 below W
             rs_steps<NS>(t, lane, 1, 2, 4, base);
@@ -240,67 +282,117 @@ __device__ __forceinline__ void packed_tree_rows(float (&t)[8], int lane, size_t
             for (int o = W >> 4; o >= 1; o >>= 1) t[0] = __fadd_rn(t[0], __shfl_xor_sync(kFull, t[0], o));
             writer = (lane & ((W >> NS) - 1)) == 0;
         }
-        if (writer) {
-#pragma unroll
-            for (int i = 0; i < M; i++) {
-                const size_t row = row0 + (size_t)((base + i) * (32 >> VLOG) + (lane >> VLOG));
-                if (row < rows) out[row] = t[i];
-            }
-        }
     } else {
-        constexpr int LL = VLOG - 5;             // log2 loads per row
+        constexpr int LL = VLOG - 5;                     // log2 loads per row
         constexpr int L = 1 << LL;
-        constexpr int M = 8 >> LL;               // rows per group
+        constexpr int M = 8 >> LL;                       // rows per group
         if constexpr (MODE == kPackedFixed) {
             // each load's tree (scatter 1, 2, 4, then 8, 16); loads k, k^1
             // then sit in lanes j, j^4 and loads k, k^2 in lanes j, j^2
-            int base = 0;
             rs_steps<3>(t, lane, 1, 2, 4, base);
             t[0] = __fadd_rn(t[0], __shfl_xor_sync(kFull, t[0], 8));
             t[0] = __fadd_rn(t[0], __shfl_xor_sync(kFull, t[0], 16));
             t[0] = __fadd_rn(t[0], __shfl_xor_sync(kFull, t[0], 4));
             if constexpr (LL >= 2) t[0] = __fadd_rn(t[0], __shfl_xor_sync(kFull, t[0], 2));
-            const size_t row = row0 + (size_t)(base >> LL);
-            if (lane < M && row < rows) out[row] = t[0];
+            writer = lane < M;
         } else {
             // lane j adds its vectors of each row in load order, then the
             // butterfly 16, 8, 4, 2, 1 over the M row values
-            float a[8];
-#pragma unroll
-            for (int r = 0; r < 8; r++) a[r] = 0.f;
 #pragma unroll
             for (int r = 0; r < M; r++) {
-                float s = -0.0f;
+                float a = -0.0f;
 #pragma unroll
-                for (int k = 0; k < L; k++) s = __fadd_rn(s, t[r * L + k]);
-                a[r] = s;
+                for (int k = 0; k < L; k++) a = __fadd_rn(a, t[r * L + k]);
+                t[r] = a;
             }
-            constexpr int NS = LL == 1 ? 2 : 1;  // log2 M
-            int base = 0;
+            constexpr int NS = LL == 1 ? 2 : 1;          // log2 M
             if constexpr (NS == 2) {
-                rs_step<2>(a, lane, 16, base);
-                rs_step<1>(a, lane, 8, base);
+                rs_step<2>(t, lane, 16, base);
+                rs_step<1>(t, lane, 8, base);
             } else {
-                rs_step<1>(a, lane, 16, base);
+                rs_step<1>(t, lane, 16, base);
             }
 #pragma unroll
-            for (int o = 16 >> NS; o >= 1; o >>= 1) a[0] = __fadd_rn(a[0], __shfl_xor_sync(kFull, a[0], o));
-            const size_t row = row0 + (size_t)base;
-            if ((lane & ((32 >> NS) - 1)) == 0 && row < rows) out[row] = a[0];
+            for (int o = 16 >> NS; o >= 1; o >>= 1) t[0] = __fadd_rn(t[0], __shfl_xor_sync(kFull, t[0], o));
+            writer = (lane & ((32 >> NS) - 1)) == 0;
         }
     }
+    return base;
+}
+
+// A row's result: out_a[row] = a (single reductions, or a pair's first
+// value), out_b[row] = b (pairs), or the mean and variance from the pair.
+template <bool PAIR>
+__device__ __forceinline__ void packed_store(float *__restrict__ out_a, float *__restrict__ out_b,
+                                             size_t row, float a, float b, size_t cols, int mean_var)
+{
+    if constexpr (PAIR) {
+        if (mean_var) mean_var_of(a, b, cols, a, b);
+        out_b[row] = b;
+    }
+    out_a[row] = a;
+}
+
+// The diagonal of A * A^T of one m16n8k16 tile (two MMAs, see MmaSqReducer
+// in stream.cuh): lane quad g's sum of squares, in every lane of the quad.
+template <int DT>
+__device__ __forceinline__ void mma_sq_quad(const uint4 &a, float &p0, float &p1, float &p2, float &p3,
+                                            float &q0, float &q1, float &q2, float &q3)
+{
+    mma_ab<DT>(p0, p1, p2, p3, a.x, a.y, a.z, a.w, a.x, a.z);
+    mma_ab<DT>(q0, q1, q2, q3, a.x, a.y, a.z, a.w, a.y, a.w);
+}
+__device__ __forceinline__ float sq_diag(int lane, float p0, float p1, float q2, float q3)
+{
+    // D[g][g] and D[g+8][g+8] sit in lane (g, g / 2): d0 / d2 for even g,
+    // d1 / d3 for odd g
+    const int g = lane >> 2;
+    return (g & 1) ? __fadd_rn(p1, q3) : __fadd_rn(p0, q2);
+}
+__device__ __forceinline__ float quad_bcast(float v, int lane)
+{
+    const int g = lane >> 2;
+    return __shfl_sync(kFull, v, 4 * g + (g >> 1));
+}
+
+// Binary32: D += the tiles of load a's leaves (inputs for kOpSum, their
+// binary32 squares for kOpSquares) split into bfloat16 parts (split_bf16x3
+// in stream.cuh): A rows g / g+8 take the hi and mid parts of the lane
+// quad's inputs 0, 1 / 2, 3, then a second tile their lo parts, so d0 + d2
+// is lane quad g's total.
+template <int LOP>
+__device__ __forceinline__ void mma_f32_tiles(const uint4 &a, float &d0, float &d1, float &d2, float &d3)
+{
+    uint32_t h0, m0, l0, h1, m1, l1;
+    split_bf16x3<LOP>(a.x, a.y, h0, m0, l0);
+    split_bf16x3<LOP>(a.z, a.w, h1, m1, l1);
+    mma_ones<kBF16>(d0, d1, d2, d3, h0, h1, m0, m1);
+    mma_ones<kBF16>(d0, d1, d2, d3, l0, l1, 0u, 0u);
 }
 
 // The packed kernel: one warp per group of 256 / W rows, grid-stride over
-// the groups.  R is the chain length of MMA_CHAIN (rows of 6 or 7 VLOG
-// only; 1 otherwise).
-template <int DT, int OP, int MODE, int VLOG, int R, bool ALIGNED>
-__global__ void __launch_bounds__(kRowsBlock, kRowsMinCtas)
-packed_rows_kernel(const void *__restrict__ xv, size_t rows, size_t cols, float *__restrict__ out)
+// the groups.  PAIR: the sum and the sum of squares of every row in one
+// pass (out_a, out_b), or their mean and variance (mean_var != 0); else
+// the reduction OP into out_a.  R is the chain length of MMA_CHAIN (rows of
+// VLOG 6 or 7 only; 1 otherwise).
+// The tensor-core squares and binary32 splits hold two or three tiles'
+// accumulators (or the split parts) beside the loads in flight: they get
+// the registers of 2 resident CTAs per SM instead of 3.
+template <int DT, int MODE, int OP, bool PAIR>
+__host__ __device__ constexpr int packed_min_ctas()
+{
+    return MODE == kPackedMma && (PAIR || OP == kOpSquares || DT == kF32) ? 2 : kRowsMinCtas;
+}
+
+template <int DT, int OP, int MODE, int VLOG, int R, bool ALIGNED, bool PAIR>
+__global__ void __launch_bounds__(kRowsBlock, packed_min_ctas<DT, MODE, OP, PAIR>())
+packed_rows_kernel(const void *__restrict__ xv, size_t rows, size_t cols, float *__restrict__ out_a,
+                   float *__restrict__ out_b, int mean_var)
 {
     static_assert(MODE != kPackedMma || VLOG >= 2, "a tensor-core row is at least one lane quad");
     using T = typename Elem<DT>::T;
     constexpr bool NZ = MODE != kPackedMma;
+    constexpr int M = packed_m<MODE, VLOG>();
     const T *__restrict__ x = static_cast<const T *>(xv);
     const int lane = threadIdx.x & 31;
     const size_t nw = ((size_t)gridDim.x * blockDim.x) >> 5;
@@ -319,103 +411,130 @@ packed_rows_kernel(const void *__restrict__ xv, size_t rows, size_t cols, float 
         const size_t row0 = gi * RPG;
         const size_t ngi = gi + nw;
         const bool has_next = ngi < groups;
+        const size_t nrow0 = ngi * RPG;
         const uint32_t hoff = gm.hoff;                   // this group's (unaligned rows)
         if constexpr (!ALIGNED)
-            if (has_next) gm = packed_geom<DT>(x, rows, cols, ngi * RPG);
+            if (has_next) gm = packed_geom<DT>(x, rows, cols, nrow0);
         // the vector of load k of this group
         auto vec = [&](int k) -> uint4 {
             if constexpr (ALIGNED) return q[k];
             else return unaligned_vec<DT, NZ, VLOG>(q, qt, k, lane, hoff, rows, cols, row0);
         };
-        // after the last load of this group is consumed: the next group's tail
-        auto next_tail = [&]() {
+        // once load k of this group is consumed: the next group's load k
+        // (and after the last one its tail), so few registers are live
+        // beside the loads in flight.  An unaligned vector is a copy made
+        // from the granules, so the next load may replace them before the
+        // vector is reduced; an aligned one is the loaded register itself.
+        auto next = [&](int k) {
+            if (has_next) q[k] = load_slot<DT, ALIGNED, NZ, VLOG>(x, rows, cols, nrow0, gm, k, lane);
             if constexpr (!ALIGNED)
-                if (has_next) qt = load_tail<DT, VLOG>(rows, cols, ngi * RPG, gm, lane);
+                if (k == 7 && has_next) qt = load_tail<DT, VLOG>(rows, cols, nrow0, gm, lane);
         };
+        float ta[8], tb[8];
         if constexpr (MODE == kPackedMma) {
-            // each load's next-group load is issued as soon as the load has
-            // been consumed, so few registers are live beside the loads in
-            // flight (the same below for the trees)
-            float v[8];
-            const size_t nrow0 = ngi * RPG;
+            // sums: tiles against ones; squares: the tiles' A * A^T diagonals
+            // (pairs: sums into ta, squares into tb)
+            constexpr bool SUM = PAIR || OP == kOpSum;
+            constexpr bool SQ = PAIR || OP == kOpSquares;
+            float(&tq)[8] = PAIR ? tb : ta;
             if constexpr (VLOG <= 5) {
-                // one MMA per load: lane quad g's total is d0 + d2
+                // one tile per load: lane quad g's total is d0 + d2, its sum
+                // of squares the tile's diagonal
 #pragma unroll
                 for (int k = 0; k < 8; k++) {
-                    float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
                     const uint4 a = vec(k);
-                    mma_ones<DT>(d0, d1, d2, d3, a.x, a.y, a.z, a.w);
-                    if (has_next) q[k] = load_slot<DT, ALIGNED, NZ, VLOG>(x, rows, cols, nrow0, gm, k, lane);
-                    v[k] = __fadd_rn(d0, d2);
+                    if constexpr (!ALIGNED) next(k);
+                    float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
+                    if constexpr (DT == kF32) {
+                        if constexpr (SUM) mma_f32_tiles<kOpSum>(a, d0, d1, d2, d3);
+                        if constexpr (SQ) {
+                            float e0 = 0.f, e1 = 0.f, e2 = 0.f, e3 = 0.f;
+                            mma_f32_tiles<kOpSquares>(a, e0, e1, e2, e3);
+                            tq[k] = __fadd_rn(e0, e2);
+                        }
+                    } else {
+                        if constexpr (SUM) mma_ones<DT>(d0, d1, d2, d3, a.x, a.y, a.z, a.w);
+                        if constexpr (SQ) {
+                            float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f, r0 = 0.f, r1 = 0.f, r2 = 0.f,
+                                  r3 = 0.f;
+                            mma_sq_quad<DT>(a, p0, p1, p2, p3, r0, r1, r2, r3);
+                            tq[k] = quad_bcast(sq_diag(lane, p0, p1, r2, r3), lane);
+                        }
+                    }
+                    if constexpr (ALIGNED) next(k);
+                    if constexpr (SUM) ta[k] = __fadd_rn(d0, d2);
                 }
-                next_tail();
             } else {
-                // a row's L loads: chains of R MMAs, each chain's d0 and d2
-                // added into the row's two accumulators
-                constexpr int L = 1 << (VLOG - 5), M = 8 / L;
+                // a row's L loads: chains of R tiles, each chain's d0 and d2
+                // (its diagonal) added into the row's accumulators
+                constexpr int L = 1 << (VLOG - 5), MR = 8 / L;
 #pragma unroll
-                for (int r = 0; r < 8; r++) v[r] = 0.f;
-#pragma unroll
-                for (int r = 0; r < M; r++) {
+                for (int r = 0; r < MR; r++) {
                     float lo = 0.f, hi = 0.f, d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
+                    float sq = 0.f, p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f, r0 = 0.f, r1 = 0.f, r2 = 0.f,
+                          r3 = 0.f;
 #pragma unroll
                     for (int k = 0; k < L; k++) {
                         const int j = r * L + k;
                         const uint4 a = vec(j);
-                        mma_ones<DT>(d0, d1, d2, d3, a.x, a.y, a.z, a.w);
-                        if (has_next) q[j] = load_slot<DT, ALIGNED, NZ, VLOG>(x, rows, cols, nrow0, gm, j, lane);
-                        if ((k + 1) % R == 0 || k == L - 1) {
-                            lo = __fadd_rn(lo, d0);
-                            hi = __fadd_rn(hi, d2);
-                            d0 = d1 = d2 = d3 = 0.f;
+                        if constexpr (!ALIGNED) next(j);
+                        const bool fl = (k + 1) % R == 0 || k == L - 1;     // chain ends
+                        if constexpr (SUM) {
+                            if constexpr (DT == kF32) mma_f32_tiles<kOpSum>(a, d0, d1, d2, d3);
+                            else mma_ones<DT>(d0, d1, d2, d3, a.x, a.y, a.z, a.w);
+                            if (fl) {
+                                lo = __fadd_rn(lo, d0);
+                                hi = __fadd_rn(hi, d2);
+                                d0 = d1 = d2 = d3 = 0.f;
+                            }
                         }
+                        if constexpr (SQ && DT == kF32) {
+                            // the squares' tiles: p0 / p2 as the sums' d0 / d2
+                            mma_f32_tiles<kOpSquares>(a, p0, p1, p2, p3);
+                            if (fl) {
+                                sq = __fadd_rn(sq, __fadd_rn(p0, p2));
+                                p0 = p1 = p2 = p3 = 0.f;
+                            }
+                        } else if constexpr (SQ) {
+                            mma_sq_quad<DT>(a, p0, p1, p2, p3, r0, r1, r2, r3);
+                            if (fl) {
+                                sq = __fadd_rn(sq, sq_diag(lane, p0, p1, r2, r3));
+                                p0 = p1 = p2 = p3 = r0 = r1 = r2 = r3 = 0.f;
+                            }
+                        }
+                        if constexpr (ALIGNED) next(j);
                     }
-                    v[r] = __fadd_rn(lo, hi);
+                    if constexpr (SUM) ta[r] = __fadd_rn(lo, hi);
+                    if constexpr (SQ) tq[r] = DT == kF32 ? sq : quad_bcast(sq, lane);
                 }
-                next_tail();
-            }
-            // sums over the row's lane quads: ascending offsets 4, 8, 16
-            if constexpr (VLOG <= 5) {
-                constexpr int NS = VLOG - 2;           // offsets 4 .. W/2, all scattered
-                constexpr int M = 8 >> NS;
-                int base = 0;
-                rs_steps<NS>(v, lane, 4, 8, 16, base);
-                if ((lane & 3) == 0) {
-#pragma unroll
-                    for (int i = 0; i < M; i++) {
-                        const size_t row = row0 + (size_t)((base + i) * (32 >> VLOG) + (lane >> VLOG));
-                        if (row < rows) out[row] = v[i];
-                    }
-                }
-            } else {
-                constexpr int NS = VLOG == 6 ? 2 : 1;  // log2 rows per group
-                int base = 0;
-                if constexpr (NS == 2) {
-                    rs_step<2>(v, lane, 4, base);
-                    rs_step<1>(v, lane, 8, base);
-                } else {
-                    rs_step<1>(v, lane, 4, base);
-                }
-#pragma unroll
-                for (int o = 4 << NS; o < 32; o <<= 1) v[0] = __fadd_rn(v[0], __shfl_xor_sync(kFull, v[0], o));
-                const size_t row = row0 + (size_t)base;
-                if ((lane & 3) == 0 && lane < (4 << NS) && row < rows) out[row] = v[0];
             }
         } else {
-            float t[8];
 #pragma unroll
             for (int k = 0; k < 8; k++) {
-                t[k] = vec_tree<DT, OP>(vec(k));
-                if (has_next) q[k] = load_slot<DT, ALIGNED, NZ, VLOG>(x, rows, cols, ngi * RPG, gm, k, lane);
+                const uint4 a = vec(k);
+                if constexpr (!ALIGNED) next(k);
+                if constexpr (PAIR) vec_tree_pair<DT>(a, ta[k], tb[k]);
+                else ta[k] = vec_tree<DT, OP>(a);
+                if constexpr (ALIGNED) next(k);
                 if constexpr (VLOG == 0) {
                     // a row is one vector: its value is the vector's tree
                     // (SHUFFLE_TREE: -0.0 + tree, the same bits)
                     const size_t row = row0 + (size_t)(32 * k + lane);
-                    if (row < rows) out[row] = t[k];
+                    if (row < rows) packed_store<PAIR>(out_a, out_b, row, ta[k], tb[k], cols, mean_var);
                 }
             }
-            next_tail();
-            if constexpr (VLOG > 0) packed_tree_rows<MODE, VLOG>(t, lane, row0, rows, out);
+        }
+        if constexpr (MODE == kPackedMma || VLOG > 0) {
+            bool writer;
+            const int base = packed_reduce<MODE, VLOG>(ta, lane, writer);
+            if constexpr (PAIR) packed_reduce<MODE, VLOG>(tb, lane, writer);
+            if (writer) {
+#pragma unroll
+                for (int i = 0; i < M; i++) {
+                    const size_t row = row0 + packed_row<MODE, VLOG>(base, i, lane);
+                    if (row < rows) packed_store<PAIR>(out_a, out_b, row, ta[i], tb[i], cols, mean_var);
+                }
+            }
         }
         if (!has_next) break;
         gi = ngi;
@@ -424,8 +543,9 @@ packed_rows_kernel(const void *__restrict__ xv, size_t rows, size_t cols, float 
 
 // Kernel pointers of each mode (k_packed_*.cu); nullptr where the mode has
 // no packed kernel for the arguments.
-const void *packed_pick_fixed(int dtype, int op, int vlog, bool aligned);
-const void *packed_pick_shuffle(int dtype, int op, int vlog, bool aligned);
-const void *packed_pick_mma(int dtype, int vlog, int R, bool aligned);
+// pair: the sum-and-squares kernel (op ignored).
+const void *packed_pick_fixed(int dtype, int op, int vlog, bool aligned, bool pair);
+const void *packed_pick_shuffle(int dtype, int op, int vlog, bool aligned, bool pair);
+const void *packed_pick_mma(int dtype, int op, int vlog, int R, bool aligned, bool pair);
 
 }  // namespace tcr

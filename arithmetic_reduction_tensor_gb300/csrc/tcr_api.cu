@@ -117,8 +117,9 @@ int occupancy(int dev, Family fam, bool rows, int dtype, int op, bool aligned, i
         case kShuffleF: n = occupancy_shuffle(rows, dtype, op, aligned, block); break;
         case kMmaF: n = occupancy_mma(rows, dtype, op, aligned, R, block); break;
         case kPackedF:
-            // R carries the packed family, the row width and the chain length
-            n = occupancy_packed(R / 100, dtype, op, R % 10, (R / 10) % 10, aligned);
+            // R carries the pair flag, the packed family, the row width and
+            // the chain length
+            n = occupancy_packed((R / 100) % 10, dtype, op, R % 10, (R / 10) % 10, aligned, R >= 1000);
             break;
         }
     }
@@ -302,7 +303,7 @@ constexpr size_t kTmemRowsMinCols = 256;
 
 // Short rows, several to a warp group: one launch of kRowsBlock threads,
 // as many CTAs as there are groups of 8 warps' rows, at most a full wave.
-void plan_packed(Plan &p, int family, int dev)
+void plan_packed(Plan &p, int family, bool pair, int dev)
 {
     p.path = kPathPackedRows;
     p.packed = family;
@@ -311,18 +312,19 @@ void plan_packed(Plan &p, int family, int dev)
     const size_t warps_per_cta = (size_t)p.block / 32;
     const size_t groups = packed_rows_groups(p.segments, p.vlog);
     const size_t need = (groups + warps_per_cta - 1) / warps_per_cta;
-    const int key = family * 100 + p.vlog * 10 + (p.R > 0 ? p.R : 1);
+    const int key = (pair ? 1000 : 0) + family * 100 + p.vlog * 10 + (p.R > 0 ? p.R : 1);
     const size_t resident = (size_t)sm_count(dev) *
                             (size_t)occupancy(dev, kPackedF, true, p.dtype, p.op, p.aligned, key, p.block);
     p.grid = (int)(need < resident ? need : resident);
     p.launches = 1;
 }
 
-// Plans tcr_reduce_sum (rows == 0: one segment of n) or tcr_reduce_rows.
-// allow_packed: rows short enough to share a warp group take the packed
-// kernels (single reductions only; the fused pairs run one warp per row).
+// Plans tcr_reduce_sum (rows == 0: one segment of n) or tcr_reduce_rows;
+// pair: the sum and sum of squares of every row in one pass (planned as
+// the sum of squares).  Rows short enough to share a warp group take the
+// packed kernels.
 Plan make_plan(size_t segments, size_t seg_len, bool rows_call, const tcr_mode &m, int op,
-               int block, int R, bool aligned, int dev, bool allow_packed = true)
+               int block, int R, bool aligned, int dev, bool pair = false)
 {
     Plan p;
     std::memset(&p, 0, sizeof p);
@@ -346,9 +348,10 @@ Plan make_plan(size_t segments, size_t seg_len, bool rows_call, const tcr_mode &
     const size_t sms = (size_t)sm_count(dev);
     if (m.kind == TCR_SHUFFLE_TREE) {
         shuffle_team(seg_len, vector_len(p.dtype), block, &p.team_threads, &p.team_blocks);
-        if (p.team_threads == 32 && p.team_blocks == 1 && rows_call && allow_packed &&
-            packed_rows_supported(kPackedShuffle, p.dtype, op, seg_len, vector_len(p.dtype), aligned)) {
-            plan_packed(p, kPackedShuffle, dev);
+        if (p.team_threads == 32 && p.team_blocks == 1 && rows_call &&
+            packed_rows_supported(kPackedShuffle, p.dtype, op, seg_len, vector_len(p.dtype), aligned,
+                                  pair)) {
+            plan_packed(p, kPackedShuffle, pair, dev);
         } else if (p.team_threads == 32 && p.team_blocks == 1) {
             // a team of one warp: pack one segment per warp, 8 per CTA
             p.path = kPathShuffleRowsWarp;
@@ -409,10 +412,10 @@ Plan make_plan(size_t segments, size_t seg_len, bool rows_call, const tcr_mode &
     }
     const Family fam = m.kind == TCR_FIXED_ORDER ? kFixedF : kMmaF;
     const int occ_r = m.kind == TCR_FIXED_ORDER ? p.vrun : R;
-    if (rows_call && allow_packed && p.vrun == 0) {
+    if (rows_call && p.vrun == 0) {
         const int pf = m.kind == TCR_FIXED_ORDER ? kPackedFixed : kPackedMma;
-        if (packed_rows_supported(pf, p.dtype, op, seg_len, vector_len(p.dtype), aligned)) {
-            plan_packed(p, pf, dev);
+        if (packed_rows_supported(pf, p.dtype, op, seg_len, vector_len(p.dtype), aligned, pair)) {
+            plan_packed(p, pf, pair, dev);
             return p;
         }
     }
@@ -594,6 +597,13 @@ tcr_status run_pair_plan(const Plan &p, const void *x, float *out_a, float *out_
     const int family = p.kind == TCR_FIXED_ORDER ? kPairFixed
                        : p.kind == TCR_SHUFFLE_TREE ? kPairShuffle
                                                     : kPairMma;
+    if (p.path == kPathPackedRows) {
+        if (fault_injected("launch")) return TCR_ERR_CUDA;
+        return launch_packed_rows_pair(p.packed, p.dtype, p.R, p.aligned, x, p.segments, p.seg_len,
+                                       p.vlog, out_a, out_b, mean_var, p.grid, p.block, s) == cudaSuccess
+                   ? TCR_OK
+                   : TCR_ERR_CUDA;
+    }
     if (p.path == kPathFixedRowsWarp || p.path == kPathMmaRows || p.path == kPathShuffleRowsWarp) {
         if (fault_injected("launch")) return TCR_ERR_CUDA;
         return launch_rows_pair(family, p.dtype, p.aligned, p.R, x, p.segments, p.seg_len, out_a,
@@ -653,7 +663,7 @@ tcr_status reduce_rows_pair(const void *x, size_t rows, size_t cols, float *out_
     if (dev < 0) return TCR_ERR_CUDA;
     const bool aligned = ((uintptr_t)x & 15u) == 0 && (cols % (size_t)vector_len(mode.dtype)) == 0;
     // planned as the sum of squares (the tcgen05 kind runs the mma.sync pair)
-    Plan p = make_plan(rows, cols, true, mode, kOpSquares, block, R, aligned, dev, false);
+    Plan p = make_plan(rows, cols, true, mode, kOpSquares, block, R, aligned, dev, true);
     return run_pair_plan(p, x, out_a, out_b, mean_var, (cudaStream_t)stream, dev);
 }
 

@@ -136,8 +136,9 @@ def test_short_rows_are_packed(lib):
     assert grid(1000, 64, tcr.FIXED_ORDER, tcr.F32) == 8
     assert grid(1000, 512, tcr.SHUFFLE_TREE, tcr.F32) == 63
     assert grid(1000, 513, tcr.SHUFFLE_TREE, tcr.F32) == 125
-    # binary32 MMA_CHAIN (the three-way split) keeps one warp per row
-    assert grid(1000, 64, tcr.MMA_CHAIN, tcr.F32) == 125
+    # binary32 MMA_CHAIN (the three-way split) packs the same way
+    assert grid(1000, 64, tcr.MMA_CHAIN, tcr.F32) == 8
+    assert grid(1000, 8, tcr.MMA_CHAIN, tcr.F32) == 2     # two vectors: one lane quad each
 
 
 def test_binary32_descriptors(lib):

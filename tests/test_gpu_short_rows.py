@@ -84,14 +84,17 @@ def test_fixed_and_shuffle_bit_exact(dtype):
                 (cols, squares)
 
 
-@pytest.mark.parametrize("dtype", [F16, BF16])
+@pytest.mark.parametrize("dtype", [F16, BF16, F32])
 @pytest.mark.parametrize("R", [1, 2, 3, 4, 8])
 def test_mma_chain_within_tolerance(dtype, R):
-    for cols in COLS16:
+    for cols in (COLS32 if dtype == F32 else COLS16):
         rows = rows_for(cols, dtype)
         x = synth.generate(rows * cols, "uniform_pm1", dtype, seed=cols + R).reshape(rows, cols)
         e, a = oracle.exact_sum_rows(x, dtype)
         assert within_mma_tolerance(rows_call(x, tcr.Mode(tcr.MMA_CHAIN, R=R, dtype=dtype)), e, a), cols
+        e2, _ = oracle.exact_sum_rows(x, dtype, squares=True)
+        got = rows_call(x, tcr.Mode(tcr.MMA_CHAIN, R=R, dtype=dtype), squares=True)
+        assert within_mma_tolerance(got, e2, e2), cols
 
 
 @pytest.mark.parametrize("dtype", [F16, F32])
@@ -175,3 +178,60 @@ def test_descriptor_reports_one_launch_and_no_scratch():
         for kind in (tcr.FIXED_ORDER, tcr.SHUFFLE_TREE, tcr.MMA_CHAIN):
             d = tcr.tcr_order_descriptor(rows=1 << 20, cols=cols, mode=tcr.Mode(kind, dtype=dtype))
             assert d["launches"] == 1 and d["partials"] == 0 and d["launch_block"] == 256
+
+
+# ---------------------------------------------------------------- row moments
+
+def moments_call(t, mode, mean_var=False):
+    f = tcr.tcr_reduce_rows_mean_var if mean_var else tcr.tcr_reduce_rows_moments
+    a, b = f(t, mode)
+    return a.cpu().numpy(), b.cpu().numpy()
+
+
+@pytest.mark.parametrize("dtype", [F16, BF16, F32])
+def test_moments_of_short_rows(dtype):
+    # both sums bit-exact to the single-reduction orders, the mean and
+    # variance to the oracle's binary32 formula on them; MMA_CHAIN within
+    # the bound of each sum
+    for cols in (COLS32 if dtype == F32 else COLS16):
+        rows = rows_for(cols, dtype)
+        x = synth.generate(rows * cols, "normal", dtype, seed=3 * cols).reshape(rows, cols)
+        t = dev(x).view(rows, cols)
+        f1, f2 = oracle.fixed_order_rows(x, dtype), oracle.fixed_order_rows(x, dtype, squares=True)
+        s1, s2 = moments_call(t, tcr.Mode(tcr.FIXED_ORDER, dtype=dtype))
+        assert same_bits(s1, f1) and same_bits(s2, f2), cols
+        m, v = moments_call(t, tcr.Mode(tcr.FIXED_ORDER, dtype=dtype), mean_var=True)
+        om, ov = oracle.mean_var(f1, f2, cols)
+        assert same_bits(m, om) and same_bits(v, ov), cols
+        bt, g = spec.shuffle_team(cols, 0, dtype)
+        g1 = oracle.shuffle_tree_rows(x, dtype, bt, g)
+        g2 = oracle.shuffle_tree_rows(x, dtype, bt, g, squares=True)
+        s1, s2 = moments_call(t, tcr.Mode(tcr.SHUFFLE_TREE, dtype=dtype))
+        assert same_bits(s1, g1) and same_bits(s2, g2), cols
+        e1, a1 = oracle.exact_sum_rows(x, dtype)
+        e2, _ = oracle.exact_sum_rows(x, dtype, squares=True)
+        for R in (1, 2, 4):
+            s1, s2 = moments_call(t, tcr.Mode(tcr.MMA_CHAIN, R=R, dtype=dtype))
+            assert within_mma_tolerance(s1, e1, a1) and within_mma_tolerance(s2, e2, e2), (cols, R)
+
+
+@pytest.mark.parametrize("offset", [1, 5])
+def test_moments_of_misaligned_short_rows(offset):
+    for cols in (7, 31, 64, 100, 255, 777):
+        rows = 513
+        x = synth.generate(rows * cols + offset, "normal", BF16, seed=cols + offset)
+        t = dev(x)[offset:].view(rows, cols)
+        xs = x[offset:].reshape(rows, cols)
+        f1, f2 = oracle.fixed_order_rows(xs, BF16), oracle.fixed_order_rows(xs, BF16, squares=True)
+        m, v = moments_call(t, tcr.Mode(tcr.FIXED_ORDER, dtype=BF16), mean_var=True)
+        om, ov = oracle.mean_var(f1, f2, cols)
+        assert same_bits(m, om) and same_bits(v, ov), cols
+        e1, a1 = oracle.exact_sum_rows(xs, BF16)
+        e2, _ = oracle.exact_sum_rows(xs, BF16, squares=True)
+        s1, s2 = moments_call(t, tcr.Mode(tcr.MMA_CHAIN, dtype=BF16))
+        assert within_mma_tolerance(s1, e1, a1) and within_mma_tolerance(s2, e2, e2), cols
+        # the fused pass gives the single calls' bits
+        for kind in (tcr.FIXED_ORDER, tcr.SHUFFLE_TREE, tcr.MMA_CHAIN):
+            s1, s2 = moments_call(t, tcr.Mode(kind, dtype=BF16))
+            assert same_bits(s1, tcr.tcr_reduce_rows(t, tcr.Mode(kind, dtype=BF16)).cpu().numpy())
+            assert same_bits(s2, tcr.tcr_reduce_rows_sum_squares(t, tcr.Mode(kind, dtype=BF16)).cpu().numpy())
