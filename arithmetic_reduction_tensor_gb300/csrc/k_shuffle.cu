@@ -84,6 +84,80 @@ __device__ __forceinline__ float grid_stride_acc(const typename Elem<DT>::T *seg
     return acc;
 }
 
+// The same accumulation for a segment that does not start 16-byte aligned
+// (see the unaligned segments of stream.cuh): thread g loads the 16-byte
+// granule holding the first input of each of its vectors, lane 31 also the
+// granule after it (the next vector belongs to the next warp's lane 0), and
+// the vector is shifted out of its two granules by the segment's byte
+// offset, P words then hs bits -- the same in every thread.  Four vectors
+// in flight (their granules take the registers of eight vectors).  The loop
+// runs while any lane of the warp has a vector, so every lane takes part
+// in the shuffles; vectors past the segment are -0.0.
+template <int DT, int OP, int P>
+__device__ __forceinline__ float grid_stride_acc_unaligned(const typename Elem<DT>::T *seg, size_t len,
+                                                           size_t first, size_t stride, uint32_t hs)
+{
+    constexpr int U = kShuffleUnroll / 2;
+    constexpr int V = Elem<DT>::kPerVec;
+    constexpr size_t EB = sizeof(typename Elem<DT>::T);
+    const int lane = threadIdx.x & 31;
+    const uintptr_t a = (uintptr_t)seg;
+    const uint4 *g0 = reinterpret_cast<const uint4 *>(a & ~(uintptr_t)15);
+    const size_t glim = ((size_t)(a & 15) + len * EB - 1) >> 4;      // last granule
+    const size_t nvec = (len + V - 1) / V;
+    const uint32_t f = Elem<DT>::kNegZeroWord;
+    const uint4 pad = make_uint4(f, f, f, f);
+    auto load = [&](size_t v0, uint4 (&q)[U], uint4 (&qt)[U]) {
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+            const size_t v = v0 + (size_t)u * stride;
+            q[u] = v <= glim ? ld_stream(g0 + v) : pad;
+            qt[u] = (lane == 31 && v + 1 <= glim) ? ld_stream(g0 + v + 1) : pad;
+        }
+    };
+    float acc = -0.0f;
+    size_t v0 = first;
+    if (v0 - (size_t)lane >= nvec) return acc;
+    uint4 q[U], qt[U];
+    load(v0, q, qt);
+    for (;;) {
+        // the warp's last vector of this batch lies past a whole vector:
+        // mask the inputs past the segment
+        const bool tail = (v0 - (size_t)lane + 31 + (size_t)(U - 1) * stride + 1) * V > len;
+        float t[U];
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+            uint4 hi;
+            hi.x = __shfl_down_sync(kFull, q[u].x, 1);
+            hi.y = __shfl_down_sync(kFull, q[u].y, 1);
+            hi.z = __shfl_down_sync(kFull, q[u].z, 1);
+            hi.w = __shfl_down_sync(kFull, q[u].w, 1);
+            if (lane == 31) hi = qt[u];
+            const uint32_t w[8] = {q[u].x, q[u].y, q[u].z, q[u].w, hi.x, hi.y, hi.z, hi.w};
+            uint32_t o[4] = {__funnelshift_r(w[P], w[P + 1], hs), __funnelshift_r(w[P + 1], w[P + 2], hs),
+                             __funnelshift_r(w[P + 2], w[P + 3], hs), __funnelshift_r(w[P + 3], w[P + 4], hs)};
+            if (tail) {
+                const long long left = (long long)len - (long long)(V * (v0 + (size_t)u * stride));
+                const int cnt = left <= 0 ? 0 : (left >= V ? V : (int)left);
+#pragma unroll
+                for (int i = 0; i < 4; i++) {
+                    const int kb = cnt * 8 * (int)EB - 32 * i;
+                    const uint32_t m = __funnelshift_lc(0xffffffffu, 0u, (uint32_t)(kb < 0 ? 0 : kb));
+                    o[i] = (o[i] & m) | (f & ~m);
+                }
+            }
+            t[u] = vec_tree<DT, OP>(make_uint4(o[0], o[1], o[2], o[3]));
+        }
+        v0 += (size_t)U * stride;
+        const bool more = v0 - (size_t)lane < nvec;      // the same in every lane
+        if (more) load(v0, q, qt);
+#pragma unroll
+        for (int u = 0; u < U; u++) acc = __fadd_rn(acc, t[u]);
+        if (!more) break;
+    }
+    return acc;
+}
+
 template <int DT, int OP, bool ALIGNED>
 __global__ void __launch_bounds__(1024)
 shuffle_block_kernel(const void *__restrict__ xv, size_t seg_len, int G, float *__restrict__ dst)
@@ -95,7 +169,19 @@ shuffle_block_kernel(const void *__restrict__ xv, size_t seg_len, int G, float *
     const size_t b = blockIdx.x - s * (unsigned)G;
     const T *seg = static_cast<const T *>(xv) + s * seg_len;
     const size_t stride = (size_t)G * blockDim.x;
-    float acc = grid_stride_acc<DT, OP, ALIGNED>(seg, seg_len, b * blockDim.x + threadIdx.x, stride);
+    const size_t first = b * blockDim.x + threadIdx.x;
+    float acc;
+    if constexpr (ALIGNED) {
+        acc = grid_stride_acc<DT, OP, true>(seg, seg_len, first, stride);
+    } else {
+        const uint32_t sb = (uint32_t)((uintptr_t)seg & 15), hs = (sb & 3u) * 8u;
+        switch (sb >> 2) {                               // the same in every thread
+        case 0: acc = grid_stride_acc_unaligned<DT, OP, 0>(seg, seg_len, first, stride, hs); break;
+        case 1: acc = grid_stride_acc_unaligned<DT, OP, 1>(seg, seg_len, first, stride, hs); break;
+        case 2: acc = grid_stride_acc_unaligned<DT, OP, 2>(seg, seg_len, first, stride, hs); break;
+        default: acc = grid_stride_acc_unaligned<DT, OP, 3>(seg, seg_len, first, stride, hs); break;
+        }
+    }
     pdl_launch_dependents();
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(kFull, acc, off));

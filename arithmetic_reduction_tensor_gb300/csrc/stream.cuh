@@ -48,6 +48,135 @@ __device__ __forceinline__ void load_group(uint4 (&q)[8], const typename Elem<DT
     }
 }
 
+// ---------------------------------------------------------------- unaligned segments
+//
+// A segment that does not start 16-byte aligned (a misaligned x, or rows
+// whose stride is not whole vectors) is read in whole 16-byte aligned
+// granules, numbered from the one holding the segment's first byte: vector
+// v (inputs V v .. V v + V - 1) starts in granule v, at the segment's byte
+// offset sb in its granule (the same for every vector), and ends in granule
+// v + 1.  Lane j of load k loads granule v of its vector; the next granule
+// is lane j + 1's (lane 0's of load k + 1 for lane 31, one extra load by
+// lane 31 after load 7).  A granule is loaded only when it holds a byte of
+// the segment, so the loads stay inside the 16-byte granules the data
+// touches.  The vectors are shifted out of the granules (realign_group)
+// when the group is reduced, while the next group's loads are in flight.
+
+template <int DT, bool NEGZERO>
+__device__ __forceinline__ void load_group_raw(uint4 (&q)[8], uint4 &qt, const typename Elem<DT>::T *seg,
+                                               size_t len, size_t gbase, int lane)
+{
+    constexpr int V = Elem<DT>::kPerVec;
+    constexpr size_t EB = sizeof(typename Elem<DT>::T);
+    const uintptr_t a = (uintptr_t)seg;
+    const uint4 *g0 = reinterpret_cast<const uint4 *>(a & ~(uintptr_t)15);
+    const size_t glim = ((size_t)(a & 15) + len * EB - 1) >> 4;     // last granule
+    const size_t v0 = gbase / V + (size_t)lane;
+    const uint32_t f = fill_word<DT, NEGZERO>();
+#pragma unroll
+    for (int k = 0; k < 8; k++) {
+        const size_t v = v0 + 32 * (size_t)k;
+        q[k] = v <= glim ? ld_stream(g0 + v) : make_uint4(f, f, f, f);
+    }
+    qt = make_uint4(f, f, f, f);
+    if (lane == 31 && gbase / V + 256 <= glim) qt = ld_stream(g0 + gbase / V + 256);
+}
+
+// Shift every vector of a group out of its two granules: P whole words,
+// then hs bits (0 or 16; always 0 for binary32) -- P and hs are the same
+// for the whole warp.
+template <int DT, int P>
+__device__ __forceinline__ void shift_group(uint4 (&q)[8], const uint4 &qt, uint32_t hs, int lane)
+{
+    const int src = (lane + 1) & 31;
+#pragma unroll
+    for (int k = 0; k < 8; k++) {
+        const uint4 lo = q[k];
+        uint4 snd = lo;
+        if (k < 7 && lane == 0) snd = q[k < 7 ? k + 1 : k];
+        uint4 hi;
+        hi.x = __shfl_sync(kFull, snd.x, src);
+        hi.y = __shfl_sync(kFull, snd.y, src);
+        hi.z = __shfl_sync(kFull, snd.z, src);
+        hi.w = __shfl_sync(kFull, snd.w, src);
+        if (k == 7 && lane == 31) hi = qt;
+        const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+        // (for binary32 hs is 0 and the funnel shifts are moves; written as
+        // shifts they keep the compiler from hoisting the moves across the
+        // group, which made the binary32 instances spill)
+        q[k] = make_uint4(__funnelshift_r(w[P], w[P + 1], hs), __funnelshift_r(w[P + 1], w[P + 2], hs),
+                          __funnelshift_r(w[P + 2], w[P + 3], hs), __funnelshift_r(w[P + 3], w[P + 4], hs));
+    }
+}
+
+// The raw granules of a group (q, qt) into its 8 vectors, in place; inputs
+// past len read as the fill.
+template <int DT, bool NEGZERO>
+__device__ __forceinline__ void realign_group(uint4 (&q)[8], const uint4 &qt,
+                                              const typename Elem<DT>::T *seg, size_t len, size_t gbase,
+                                              int lane)
+{
+    constexpr int V = Elem<DT>::kPerVec;
+    constexpr int EB = (int)sizeof(typename Elem<DT>::T);
+    const uint32_t sb = (uint32_t)((uintptr_t)seg & 15);
+    const uint32_t hs = (sb & 3u) * 8u;
+    switch (sb >> 2) {                                   // the same in every lane
+    case 0:
+        if (sb != 0) shift_group<DT, 0>(q, qt, hs, lane);
+        break;
+    case 1: shift_group<DT, 1>(q, qt, hs, lane); break;
+    case 2: shift_group<DT, 2>(q, qt, hs, lane); break;
+    default: shift_group<DT, 3>(q, qt, hs, lane); break;
+    }
+    if (gbase + group_len<DT>() > len) {
+        // the segment's last group: inputs past len become the fill
+        const uint32_t f = fill_word<DT, NEGZERO>();
+#pragma unroll
+        for (int k = 0; k < 8; k++) {
+            const long long left = (long long)len - (long long)(gbase + (size_t)V * (32 * k + lane));
+            const int cnt = left <= 0 ? 0 : (left >= V ? V : (int)left);
+            uint32_t o[4] = {q[k].x, q[k].y, q[k].z, q[k].w};
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                const int kb = cnt * 8 * EB - 32 * i;
+                const uint32_t m = __funnelshift_lc(0xffffffffu, 0u, (uint32_t)(kb < 0 ? 0 : kb));
+                o[i] = (o[i] & m) | (f & ~m);
+            }
+            q[k] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+    }
+}
+
+// The group of loads in flight: for 16-byte aligned segments its 8
+// vectors; for the others the raw granules, made into vectors by ready()
+// just before the group is reduced -- or, when REALIGN is off (a reducer
+// already bound by its own arithmetic, for which input-sized loads cost
+// less than the shifts), the vectors loaded input by input.
+template <int DT, bool ALIGNED, bool NEGZERO, bool REALIGN = true>
+struct GroupIn {
+    using T = typename Elem<DT>::T;
+    static constexpr bool kRaw = !ALIGNED && REALIGN;
+    uint4 q[8];
+    uint4 qt;
+
+    __device__ __forceinline__ void load(const T *seg, size_t len, size_t gbase, int lane)
+    {
+        if constexpr (kRaw) load_group_raw<DT, NEGZERO>(q, qt, seg, len, gbase, lane);
+        else load_group<DT, ALIGNED, NEGZERO>(q, seg, len, gbase, lane);
+    }
+    __device__ __forceinline__ void ready(const T *seg, size_t len, size_t gbase, int lane)
+    {
+        if constexpr (kRaw) realign_group<DT, NEGZERO>(q, qt, seg, len, gbase, lane);
+    }
+};
+
+// Whether a reducer's unaligned segments are read as granules (its
+// kRealign, true when it has none).
+template <class Red, class = void>
+struct realigns : std::true_type {};
+template <class Red>
+struct realigns<Red, std::void_t<decltype(Red::kRealign)>> : std::bool_constant<Red::kRealign> {};
+
 // ---------------------------------------------------------------- trees
 
 // t[k]: the lane's vector subtree of warp load k (k = 0..7) of a group.
@@ -279,6 +408,9 @@ template <int R, int OP>
 struct MmaSplitReducer {
     static constexpr int kDT = kF32;
     static constexpr bool kNegZeroPad = false;
+    // the split issues about 7 instructions per input: unaligned inputs are
+    // loaded input by input (4-byte loads) rather than shifted out of granules
+    static constexpr bool kRealign = false;
     float h0 = 0.f, h1 = 0.f, h2 = 0.f, h3 = 0.f;    // D_hi
     float m0 = 0.f, m1 = 0.f, m2 = 0.f, m3 = 0.f;    // D_ml
     float acc_lo = 0.f, acc_hi = 0.f;
@@ -394,6 +526,7 @@ struct PairReducer {
     static_assert(A::kDT == B::kDT && A::kNegZeroPad == B::kNegZeroPad, "pair of unlike streams");
     static constexpr int kDT = A::kDT;
     static constexpr bool kNegZeroPad = A::kNegZeroPad;
+    static constexpr bool kRealign = realigns<A>::value && realigns<B>::value;
     A a;
     B b;
 
@@ -441,8 +574,8 @@ __device__ __forceinline__ void chunk_body(const void *__restrict__ xv, size_t s
         size_t s = u / cps;
         const T *seg = x + s * seg_len;
         size_t base = ((u - s * cps) << chunk_log2) + (size_t)warp * span;
-        uint4 q[8];
-        load_group<DT, ALIGNED, NZ>(q, seg, seg_len, base, lane);
+        GroupIn<DT, ALIGNED, NZ, realigns<Red>::value> in;
+        in.load(seg, seg_len, base, lane);
         for (;;) {
             const size_t nu = u + gridDim.x;
             const bool has_next = nu < units;
@@ -458,12 +591,12 @@ __device__ __forceinline__ void chunk_body(const void *__restrict__ xv, size_t s
             // the loop fits the 64 registers a 1024-thread CTA allows
 #pragma unroll 1
             for (int g = 0; g < ngroups; g++) {
-                red.take(q);
+                in.ready(seg, seg_len, base + (size_t)g * group_len<DT>(), lane);
+                red.take(in.q);
                 if (g + 1 < ngroups)
-                    load_group<DT, ALIGNED, NZ>(q, seg, seg_len,
-                                                base + (size_t)(g + 1) * group_len<DT>(), lane);
+                    in.load(seg, seg_len, base + (size_t)(g + 1) * group_len<DT>(), lane);
                 else if (has_next)
-                    load_group<DT, ALIGNED, NZ>(q, nseg, seg_len, nbase, lane);
+                    in.load(nseg, seg_len, nbase, lane);
                 red.reduce(lane);
             }
             const float v = red.value(lane);
@@ -499,19 +632,20 @@ __device__ __forceinline__ void rows_body(const void *__restrict__ xv, size_t ro
     constexpr size_t G = group_len<DT>();
     const size_t ngroups = (cols + G - 1) / G;
     if (r < rows && ngroups > 0) {
-        uint4 q[8];
-        load_group<DT, ALIGNED, NZ>(q, x + r * cols, cols, 0, lane);
+        GroupIn<DT, ALIGNED, NZ, realigns<Red>::value> in;
+        in.load(x + r * cols, cols, 0, lane);
         for (;;) {
             const size_t nr = r + nw;
             const bool has_next = nr < rows;
             Red red;
 #pragma unroll 1
             for (size_t g = 0; g < ngroups; g++) {
-                red.take(q);
+                in.ready(x + r * cols, cols, g * G, lane);
+                red.take(in.q);
                 if (g + 1 < ngroups)
-                    load_group<DT, ALIGNED, NZ>(q, x + r * cols, cols, (g + 1) * G, lane);
+                    in.load(x + r * cols, cols, (g + 1) * G, lane);
                 else if (has_next)
-                    load_group<DT, ALIGNED, NZ>(q, x + nr * cols, cols, 0, lane);
+                    in.load(x + nr * cols, cols, 0, lane);
                 red.reduce(lane);
             }
             const float v = red.value(lane);
@@ -543,15 +677,14 @@ __device__ __forceinline__ void chunk_pair_body(const void *__restrict__ xv, siz
         const size_t s = u / cps;
         const T *seg = x + s * seg_len;
         const size_t base = ((u - s * cps) << chunk_log2) + (size_t)warp * span;
-        uint4 q[8];
-        load_group<DT, ALIGNED, NZ>(q, seg, seg_len, base, lane);
+        GroupIn<DT, ALIGNED, NZ, realigns<Red>::value> in;
+        in.load(seg, seg_len, base, lane);
         Red red;
 #pragma unroll 1
         for (int g = 0; g < ngroups; g++) {
-            red.take(q);
-            if (g + 1 < ngroups)
-                load_group<DT, ALIGNED, NZ>(q, seg, seg_len, base + (size_t)(g + 1) * group_len<DT>(),
-                                            lane);
+            in.ready(seg, seg_len, base + (size_t)g * group_len<DT>(), lane);
+            red.take(in.q);
+            if (g + 1 < ngroups) in.load(seg, seg_len, base + (size_t)(g + 1) * group_len<DT>(), lane);
             red.reduce(lane);
         }
         float va, vb;
@@ -592,19 +725,20 @@ __device__ __forceinline__ void rows_pair_body(const void *__restrict__ xv, size
     constexpr size_t G = group_len<DT>();
     const size_t ngroups = (cols + G - 1) / G;
     if (r < rows && ngroups > 0) {
-        uint4 q[8];
-        load_group<DT, ALIGNED, NZ>(q, x + r * cols, cols, 0, lane);
+        GroupIn<DT, ALIGNED, NZ, realigns<Red>::value> in;
+        in.load(x + r * cols, cols, 0, lane);
         for (;;) {
             const size_t nr = r + nw;
             const bool has_next = nr < rows;
             Red red;
 #pragma unroll 1
             for (size_t g = 0; g < ngroups; g++) {
-                red.take(q);
+                in.ready(x + r * cols, cols, g * G, lane);
+                red.take(in.q);
                 if (g + 1 < ngroups)
-                    load_group<DT, ALIGNED, NZ>(q, x + r * cols, cols, (g + 1) * G, lane);
+                    in.load(x + r * cols, cols, (g + 1) * G, lane);
                 else if (has_next)
-                    load_group<DT, ALIGNED, NZ>(q, x + nr * cols, cols, 0, lane);
+                    in.load(x + nr * cols, cols, 0, lane);
                 red.reduce(lane);
             }
             float va, vb;
