@@ -455,7 +455,9 @@ def profile_arm(args):
     the tcgen05 MMA_CHAIN sum and rows.  ``--profile-case f32``: the same
     bytes in binary32 (2^27 sum, 32768 x 2048 rows), the three mma.sync-era
     modes.  ``--profile-case gemm``: the split-K GEMM on 4096^3 (one split)
-    and 1024 x 1024 x 16384 (the default split)."""
+    and 1024 x 1024 x 16384 (the default split).  ``--profile-case short``:
+    the packed short-row kernels, each mode once on 4194304 x 64 fp16 rows
+    (512 MiB) and once on 2684354 x 100 (rows not 16-byte aligned)."""
     import torch
     import arithmetic_reduction_tensor_gb300 as tcr
     from arithmetic_reduction_tensor_gb300 import synth
@@ -467,6 +469,17 @@ def profile_arm(args):
             W = torch.randn(N, K, device="cuda", generator=gen).to(torch.bfloat16)
             for _ in range(args.steps):
                 tcr.tcr_gemm_splitk(A, W, splits=S)
+        torch.cuda.synchronize()
+        print("profile case done", flush=True)
+        return 0
+    if args.profile_case == "short":
+        n = 1 << 28
+        x = torch.from_numpy(synth.generate(n, "normal", synth.F16, seed=2).view(np.int16)).cuda()
+        shapes = ((n // 64, 64), (n // 100, 100))
+        for _ in range(args.steps):
+            for rows, cols in shapes:
+                for kind in (tcr.MMA_CHAIN, tcr.FIXED_ORDER, tcr.SHUFFLE_TREE):
+                    tcr.tcr_reduce_rows(x[:rows * cols].view(rows, cols), tcr.Mode(kind))
         torch.cuda.synchronize()
         print("profile case done", flush=True)
         return 0
@@ -501,8 +514,12 @@ def extras_arm(args):
     sum and 65536 x 4096 rows, every mode), binary32 inputs (2^29 sum and
     65536 x 2048 rows -- the same bytes as the 16-bit workload -- every mode,
     sums and sums of squares), FIXED_ORDER's blocked order (runs of 2^c
-    inputs left to right, then the tree) on the 16-bit workload, and the
-    fused row moments (sum and sum of squares, mean and variance, one pass)."""
+    inputs left to right, then the tree) on the 16-bit workload, the
+    fused row moments (sum and sum of squares, mean and variance, one pass),
+    short rows (views of the 2^30 sum input as rows of 64, 256 and 1024
+    inputs, rows of 100 whose starts are not 16-byte aligned, row moments of
+    768), long rows of 4095 inputs and the sum from a base one input past a
+    16-byte boundary."""
     import torch
     import arithmetic_reduction_tensor_gb300 as tcr
     from arithmetic_reduction_tensor_gb300 import synth
@@ -549,6 +566,37 @@ def extras_arm(args):
                       lambda m=m: tcr.tcr_reduce_rows_moments(xr, m, sums=out, sums_of_squares=out2)))
         calls.append(("rows_mean_var/" + k, 2 * ROWS * COLS + 8 * ROWS,
                       lambda m=m: tcr.tcr_reduce_rows_mean_var(xr, m, mean=out, var=out2)))
+    # short rows (packed several to a warp), unaligned rows and base: views
+    # of the sum input, every row its own segment
+    kinds4 = (tcr.MMA_CHAIN, tcr.FIXED_ORDER, tcr.SHUFFLE_TREE, tcr.MMA_CHAIN_TMEM)
+    for cols in (64, 256, 1024):
+        v = xs.view(N_SUM // cols, cols)
+        o = torch.empty(N_SUM // cols, dtype=torch.float32, device="cuda")
+        for kind in kinds4:
+            m = tcr.Mode(kind)
+            calls.append((f"short_rows_{cols}/" + tcr.KIND_NAMES[kind], 2 * N_SUM + 4 * (N_SUM // cols),
+                          lambda m=m, v=v, o=o: tcr.tcr_reduce_rows(v, m, out=o)))
+    for cols in (100, 4095):
+        nr = N_SUM // cols
+        v = xs[:nr * cols].view(nr, cols)
+        o = torch.empty(nr, dtype=torch.float32, device="cuda")
+        for kind in kinds4:
+            m = tcr.Mode(kind)
+            calls.append((f"unaligned_rows_{cols}/" + tcr.KIND_NAMES[kind], 2 * nr * cols + 4 * nr,
+                          lambda m=m, v=v, o=o: tcr.tcr_reduce_rows(v, m, out=o)))
+    xm = xs[1:]
+    for kind in kinds4:
+        m = tcr.Mode(kind)
+        calls.append(("unaligned_sum/" + tcr.KIND_NAMES[kind], 2 * (N_SUM - 1) + 4,
+                      lambda m=m: tcr.tcr_reduce_sum(xm, m, out=out[:1])))
+    nr768 = N_SUM // 768
+    v768 = xs[:nr768 * 768].view(nr768, 768)
+    oa = torch.empty(nr768, dtype=torch.float32, device="cuda")
+    ob = torch.empty(nr768, dtype=torch.float32, device="cuda")
+    for kind in (tcr.MMA_CHAIN, tcr.FIXED_ORDER, tcr.SHUFFLE_TREE):
+        m = tcr.Mode(kind)
+        calls.append(("short_rows_768_mean_var/" + tcr.KIND_NAMES[kind], 2 * nr768 * 768 + 8 * nr768,
+                      lambda m=m: tcr.tcr_reduce_rows_mean_var(v768, m, mean=oa, var=ob)))
     for name, nbytes, fn in calls:
         for _ in range(args.warmup):
             fn()
@@ -645,10 +693,11 @@ def main():
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--extras", action="store_true",
                     help="time the sum of squares and binary32 calls (beyond the hot path) and exit")
-    ap.add_argument("--profile-case", nargs="?", const="f16", choices=["f16", "f32", "gemm"],
+    ap.add_argument("--profile-case", nargs="?", const="f16", choices=["f16", "f32", "gemm", "short"],
                     default=None,
                     help="run the small ncu case (2^28 sum, 32768 x 4096 rows; f32: the same "
-                         "bytes in binary32; gemm: 4096^3 and 1024^2 x 16384 bf16) and exit")
+                         "bytes in binary32; gemm: 4096^3 and 1024^2 x 16384 bf16; short: packed "
+                         "rows of 64 and 100 fp16) and exit")
     ap.add_argument("--gemm", action="store_true",
                     help="time the split-K GEMM with the declared combine (TFLOP/s) and exit")
     ap.add_argument("--e2e-steps", type=int, default=0, help="0: max(3, steps // 40)")
