@@ -1,5 +1,6 @@
 """The later paths at full size: the blocked order on the 2^30-input sum, the
-fused row moments on the 65536 x 4096 rows, binary32 at 2^29, and large
+fused row moments on the 65536 x 4096 rows, binary32 at 2^29, the 2^30 sum
+seen as short rows (packed kernels) and from a misaligned base, and large
 split-K GEMMs on sampled elements (the oracle computes those one by one)."""
 import numpy as np
 import pytest
@@ -44,6 +45,32 @@ def test_blocked_order_on_the_2p30_sum(sum_2p30, c):
     x, t = sum_2p30
     got = np.float32(tcr.tcr_reduce_sum(t, tcr.Mode(tcr.FIXED_ORDER, run_log2=c)).cpu().numpy()[0])
     assert same_bits(got, oracle.blocked_order(x, F16, c))
+
+
+@pytest.mark.parametrize("cols", [64, 100])
+def test_the_2p30_sum_as_short_rows(sum_2p30, cols):
+    # every row of the full input through the packed kernels (rows of 100 are
+    # not 16-byte aligned); the oracle's row emulation runs on all of them
+    x, t = sum_2p30
+    rows = (1 << 30) // cols
+    xr = x[:rows * cols].reshape(rows, cols)
+    tr = t[:rows * cols].view(rows, cols)
+    got = tcr.tcr_reduce_rows(tr, tcr.Mode(tcr.FIXED_ORDER)).cpu().numpy()
+    assert same_bits(got, oracle.fixed_order_rows(xr, F16))
+    got = tcr.tcr_reduce_rows(tr, tcr.Mode(tcr.SHUFFLE_TREE)).cpu().numpy()
+    assert same_bits(got, oracle.shuffle_tree_rows(xr, F16, *spec.shuffle_team(cols)))
+    e, a = oracle.exact_sum_rows(xr, F16)
+    got = tcr.tcr_reduce_rows(tr, tcr.Mode(tcr.MMA_CHAIN)).cpu().numpy()
+    assert np.all(np.abs(got - e) <= spec.mma_tolerance(a))
+
+
+def test_the_2p30_sum_from_a_misaligned_base(sum_2p30):
+    x, t = sum_2p30
+    xs, ts = x[1:], t[1:]
+    assert same_bits(tcr.tcr_reduce_sum(ts, tcr.Mode(tcr.FIXED_ORDER)).cpu().numpy(),
+                     oracle.fixed_order(xs, F16))
+    assert same_bits(tcr.tcr_reduce_sum(ts, tcr.Mode(tcr.SHUFFLE_TREE)).cpu().numpy(),
+                     oracle.shuffle_tree(xs, F16, *spec.shuffle_team(xs.size)))
 
 
 def test_moments_on_the_65536x4096_rows():

@@ -235,3 +235,17 @@ def test_moments_of_misaligned_short_rows(offset):
             s1, s2 = moments_call(t, tcr.Mode(kind, dtype=BF16))
             assert same_bits(s1, tcr.tcr_reduce_rows(t, tcr.Mode(kind, dtype=BF16)).cpu().numpy())
             assert same_bits(s2, tcr.tcr_reduce_rows_sum_squares(t, tcr.Mode(kind, dtype=BF16)).cpu().numpy())
+
+
+@pytest.mark.parametrize("dtype", [F16, BF16])
+def test_every_16_bit_pattern_converts_exactly(dtype):
+    # rows of one input: each row's value is that input's binary32 leaf, so
+    # the GPU's conversion of all 65536 patterns is compared with the
+    # oracle's decoder (itself pinned to numpy); squares give fl32(x * x)
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16).reshape(-1, 1)
+    leaves = oracle.leaves(bits.reshape(-1), dtype)
+    for kind in (tcr.FIXED_ORDER, tcr.SHUFFLE_TREE):
+        assert same_bits(rows_call(bits, tcr.Mode(kind, dtype=dtype)), leaves)
+        with np.errstate(over="ignore", invalid="ignore"):
+            sq = (leaves * leaves).astype(np.float32)
+        assert same_bits(rows_call(bits, tcr.Mode(kind, dtype=dtype), squares=True), sq)
