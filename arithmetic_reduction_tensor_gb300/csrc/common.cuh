@@ -35,17 +35,11 @@ struct Elem<kF32> {
     static constexpr uint32_t kNegZeroWord = 0x80000000u;
 };
 
-// Inputs per warp group (8 warp loads of 32 vectors) and per warp span
-// (2^kWarpSpanBytesLog2 bytes) of an input type.
+// Inputs per warp group (8 warp loads of 32 vectors) of an input type.
 template <int DT>
 __host__ __device__ constexpr size_t group_len()
 {
     return (size_t)256 * Elem<DT>::kPerVec;
-}
-template <int DT>
-__host__ __device__ constexpr size_t span_len()
-{
-    return ((size_t)1 << kWarpSpanBytesLog2) / sizeof(typename Elem<DT>::T);
 }
 
 // ---------------------------------------------------------------- loads

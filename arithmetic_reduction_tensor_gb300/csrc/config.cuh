@@ -14,11 +14,13 @@ namespace tcr {
 constexpr int kOpSum = 0;
 constexpr int kOpSquares = 1;
 
-// Bytes per warp group of the stream kernels: 8 warp loads of 512 bytes
-// (2048 16-bit inputs, 1024 binary32 inputs).
-constexpr size_t kGroupBytes = 4096;
-// Bytes per warp of one CTA work unit (chunk) of the chunked kernels:
-// 2^14 = 4 groups (2^13 16-bit inputs, 2^12 binary32 inputs).
+// Bytes per warp group of the stream kernels (log2): 8 warp loads of 512
+// bytes (2048 16-bit inputs, 1024 binary32 inputs).
+constexpr int kGroupBytesLog2 = 12;
+// Bytes per warp of one CTA work unit (chunk) of the chunked kernels (log2):
+// 2^14 = 4 groups (2^13 16-bit inputs, 2^12 binary32 inputs); inputs too
+// small to give every SM two work units get shorter spans, down to one
+// group.
 constexpr int kWarpSpanBytesLog2 = 14;
 // Longest row served by one warp, in bytes (8 groups: 16384 16-bit or 8192
 // binary32 inputs); longer rows go through the chunked kernels

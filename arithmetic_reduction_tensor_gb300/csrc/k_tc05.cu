@@ -42,8 +42,9 @@ constexpr int kTcTileBytes = kTcTileInputs * 2;     // 4 KiB
 constexpr int kTcTilesPerStage = 8;                 // 32 KiB bulk copies
 constexpr int kTcStageBytes = kTcTileBytes * kTcTilesPerStage;
 constexpr int kTcStages = 6;                        // 192 KiB in flight per SM
-constexpr int kTcUnitLog2 = 16;                     // work unit: 2^16 inputs
-constexpr int kTcTilesPerUnit = (1 << kTcUnitLog2) / kTcTileInputs;   // 32
+constexpr int kTcUnitLog2 = 16;                     // work unit: 2^16 inputs ...
+constexpr int kTcMinUnitLog2 = 11;                  // ... down to one tile for small inputs
+constexpr size_t kTcMinUnits = 2 * 152;             // the units small inputs are cut into
 constexpr int kTcThreads = 192;
 constexpr int kTcEpilogueThreads = 128;
 constexpr int kTcDBuffers = 8;                      // chains the MMA may run ahead
@@ -75,21 +76,23 @@ __device__ __forceinline__ uint32_t instr_desc()
 
 // ---------------------------------------------------------------- kernel
 
-// Work unit u covers inputs [u * 2^16, min(n, (u+1) * 2^16)); its whole
-// 2048-input tiles go through the tensor cores, the inputs past the last
-// whole tile of the array (fewer than 2048) are added by the epilogue.
-__device__ __forceinline__ int unit_tiles(size_t n, size_t u)
+// Work unit u covers inputs [u * 2^L, min(n, (u+1) * 2^L)), L = unit_log2
+// (16, or less for small inputs: tmem_unit_log2); its whole 2048-input
+// tiles go through the tensor cores, the inputs past the last whole tile of
+// the array (fewer than 2048) are added by the epilogue.
+__device__ __forceinline__ int unit_tiles(size_t n, size_t u, int unit_log2)
 {
-    const size_t base = u << kTcUnitLog2;
+    const size_t base = u << unit_log2;
     const size_t left = n - base;
     const size_t t = left / kTcTileInputs;
-    return (int)(t < (size_t)kTcTilesPerUnit ? t : (size_t)kTcTilesPerUnit);
+    const size_t per_unit = (size_t)1 << (unit_log2 - kTcMinUnitLog2);
+    return (int)(t < per_unit ? t : per_unit);
 }
 
 template <int DT, int R>
 __global__ void __launch_bounds__(kTcThreads, 1)
-mma_tmem_kernel(const uint16_t *__restrict__ x, size_t n, size_t units, float *__restrict__ dst,
-                uint32_t inject_stall)
+mma_tmem_kernel(const uint16_t *__restrict__ x, size_t n, size_t units, int unit_log2,
+                float *__restrict__ dst, uint32_t inject_stall)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -154,8 +157,8 @@ mma_tmem_kernel(const uint16_t *__restrict__ x, size_t n, size_t units, float *_
                 armed_phase[i] = 0;
             }
             for (size_t u = blockIdx.x; u < units && !*abort; u += gridDim.x) {
-                const int tiles = unit_tiles(n, u);
-                const uint16_t *src = x + (u << kTcUnitLog2);
+                const int tiles = unit_tiles(n, u, unit_log2);
+                const uint16_t *src = x + (u << unit_log2);
                 for (int t0 = 0; t0 < tiles; t0 += kTcTilesPerStage) {
                     const int nt = min(kTcTilesPerStage, tiles - t0);
                     if (!mbar_wait(empty_bar(s), phase ^ 1u, abort)) break;
@@ -214,7 +217,7 @@ mma_tmem_kernel(const uint16_t *__restrict__ x, size_t n, size_t units, float *_
                 if (++b == kTcDBuffers) b = 0;
             };
             for (size_t u = blockIdx.x; u < units && !*abort; u += gridDim.x) {
-                const int tiles = unit_tiles(n, u);
+                const int tiles = unit_tiles(n, u, unit_log2);
                 int in_chain = 0;
                 for (int t0 = 0; t0 < tiles && !*abort; t0 += kTcTilesPerStage) {
                     const int nt = min(kTcTilesPerStage, tiles - t0);
@@ -264,7 +267,7 @@ mma_tmem_kernel(const uint16_t *__restrict__ x, size_t n, size_t units, float *_
         int b = 0;
         uint32_t dphase = 0u;
         for (size_t u = blockIdx.x; u < units; u += gridDim.x) {
-            const int tiles = unit_tiles(n, u);
+            const int tiles = unit_tiles(n, u, unit_log2);
             const int chains = (tiles + R - 1) / R;
             float acc = 0.f;
             for (int c = 0; c < chains && !*abort; c++) {
@@ -278,9 +281,9 @@ mma_tmem_kernel(const uint16_t *__restrict__ x, size_t n, size_t units, float *_
                 if (++b == kTcDBuffers) b = 0;
             }
             // inputs of this unit past its whole tiles (only in the last unit)
-            const size_t base = u << kTcUnitLog2;
+            const size_t base = u << unit_log2;
             const size_t tail_lo = base + (size_t)tiles * kTcTileInputs;
-            size_t tail_hi = base + ((size_t)1 << kTcUnitLog2);
+            size_t tail_hi = base + ((size_t)1 << unit_log2);
             if (tail_hi > n) tail_hi = n;
             for (size_t i = tail_lo + (size_t)et; i < tail_hi; i += kTcEpilogueThreads)
                 acc = __fadd_rn(acc, DT == kF16 ? leaf_lo<kF16>(__ldg(x + i)) : leaf_lo<kBF16>(__ldg(x + i)));
@@ -561,14 +564,25 @@ static void *pick_dt(int R)
     }
 }
 
+// 2^16 inputs per unit (one unit -- one launch, no partials -- up to 2^16
+// inputs); above that halved while it leaves fewer than two units per SM of
+// the 152 the rules assume, down to one tile.  A function of n only, so the
+// chunking (and MMA_CHAIN's bits) is the same on every device.
+int tmem_unit_log2(size_t n)
+{
+    int l = kTcUnitLog2;
+    if (n <= ((size_t)1 << kTcUnitLog2)) return l;
+    while (l > kTcMinUnitLog2 && ((n + ((size_t)1 << l) - 1) >> l) < kTcMinUnits) l--;
+    return l;
+}
+
 size_t tmem_units(size_t n)
 {
-    return (n + ((size_t)1 << kTcUnitLog2) - 1) >> kTcUnitLog2;
+    const int l = tmem_unit_log2(n);
+    return (n + ((size_t)1 << l) - 1) >> l;
 }
 
 int tmem_block_threads() { return kTcThreads; }
-
-int tmem_unit_log2() { return kTcUnitLog2; }
 
 cudaError_t launch_mma_tmem(int dtype, int R, const uint16_t *x, size_t n, float *dst, int grid,
                             bool inject_stall, cudaStream_t stream)
@@ -578,8 +592,10 @@ cudaError_t launch_mma_tmem(int dtype, int R, const uint16_t *x, size_t n, float
     cudaError_t e = set_smem_once(k, kTcSmemBytes);
     if (e != cudaSuccess) return e;
     size_t units = tmem_units(n);
+    int unit_log2 = tmem_unit_log2(n);
     uint32_t stall = inject_stall ? 1u : 0u;
-    void *args[] = {(void *)&x, (void *)&n, (void *)&units, (void *)&dst, (void *)&stall};
+    void *args[] = {(void *)&x, (void *)&n, (void *)&units, (void *)&unit_log2, (void *)&dst,
+                    (void *)&stall};
     return cudaLaunchKernel(k, dim3(grid), dim3(kTcThreads), args, kTcSmemBytes, stream);
 }
 

@@ -79,14 +79,14 @@ int occupancy_packed(int family, int dtype, int op, int R, int vlog, bool aligne
 
 // ---- MMA_CHAIN on tcgen05 (bulk copies into shared memory, D in TMEM):
 // one persistent CTA per SM; dst[u] is the partial of work unit u (2^16
-// inputs, see tmem_unit_log2); x must be 16-byte aligned.
-// inject_stall: withhold the first chain's publication so that a wait runs
-// out its limit (tests of the failure path only).
+// inputs, fewer for small n: 2^tmem_unit_log2(n)); x must be 16-byte
+// aligned.  inject_stall: withhold the first chain's publication so that a
+// wait runs out its limit (tests of the failure path only).
 cudaError_t launch_mma_tmem(int dtype, int R, const uint16_t *x, size_t n, float *dst, int grid,
                             bool inject_stall, cudaStream_t stream);
 size_t tmem_units(size_t n);
 int tmem_block_threads();
-int tmem_unit_log2();
+int tmem_unit_log2(size_t n);
 // Rows: D's 128 lanes are 128 consecutive rows, the inputs reach shared
 // memory by 2-D tensor-map copies; dst[row * chunks + c] is row `row`'s
 // partial over column chunk c (tmem_rows_chunks(cols) chunks per row).

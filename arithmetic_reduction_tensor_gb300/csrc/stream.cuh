@@ -564,11 +564,12 @@ __device__ __forceinline__ void chunk_body(const void *__restrict__ xv, size_t s
     const T *__restrict__ x = static_cast<const T *>(xv);
     __shared__ float warp_val[32];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-    // every warp span is 2^kWarpSpanBytesLog2 bytes (chunk_log2 = log2 of
-    // the span's inputs + log2 warps), so the groups per span are a
-    // compile-time constant
-    constexpr size_t span = span_len<DT>();
-    constexpr int ngroups = (int)(span / group_len<DT>());
+    // the chunk is one span per warp: chunk_log2 = log2 of the span's inputs
+    // + log2 warps; a span is a whole number of groups (16 KiB, or 4-8 KiB
+    // for small inputs, chosen by the host)
+    const int span_log2 = chunk_log2 - (31 - __clz(nwarps));
+    const size_t span = (size_t)1 << span_log2;
+    const int ngroups = (int)(span / group_len<DT>());
     size_t u = blockIdx.x;
     if (u < units) {
         size_t s = u / cps;
@@ -671,8 +672,9 @@ __device__ __forceinline__ void chunk_pair_body(const void *__restrict__ xv, siz
     const T *__restrict__ x = static_cast<const T *>(xv);
     __shared__ float warp_val[2][32];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-    constexpr size_t span = span_len<DT>();
-    constexpr int ngroups = (int)(span / group_len<DT>());
+    const int span_log2 = chunk_log2 - (31 - __clz(nwarps));     // as in chunk_body
+    const size_t span = (size_t)1 << span_log2;
+    const int ngroups = (int)(span / group_len<DT>());
     for (size_t u = blockIdx.x; u < units; u += gridDim.x) {
         const size_t s = u / cps;
         const T *seg = x + s * seg_len;

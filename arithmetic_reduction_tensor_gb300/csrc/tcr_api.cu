@@ -235,21 +235,41 @@ tcr_status check_mode(const tcr_mode &m, int *block, int *R)
 }
 
 // may_shrink: the CTA size is free to choose (FIXED_ORDER, whose bits never
-// depend on it, or a default block size): small inputs then get smaller
-// CTAs until there are two work units per SM of the 152 the rules assume --
-// a fixed function of the input length, so MMA_CHAIN's chunking (reported
-// by the descriptor) is the same on every device.
+// depend on it, or a default block size): a sum small enough for one CTA
+// whose warps take at most two groups each (2^17 16-bit or 2^16 binary32
+// inputs) is one work unit -- one launch, no partials, no scratch; larger
+// small inputs get smaller CTAs, then shorter warp spans (16 KiB down to
+// one 4 KiB group), until there are two work units per SM of the 152 the
+// rules assume.  Both are fixed functions of the input length, so
+// MMA_CHAIN's chunking (reported by the descriptor) is the same on every
+// device.
 void plan_chunked(Plan &p, int dev, Family fam, bool may_shrink)
 {
-    // each warp of a CTA covers 2^kWarpSpanBytesLog2 bytes of the CTA's chunk
     p.path = kPathChunk;
-    const int span_log2 = kWarpSpanBytesLog2 - log2_exact((int)elem_bytes(p.dtype));
-    for (;;) {
-        p.chunk_log2 = span_log2 + log2_exact(p.block / 32);
-        p.cps = (p.seg_len + ((size_t)1 << p.chunk_log2) - 1) >> p.chunk_log2;
-        p.units = p.segments * p.cps;
-        if (!may_shrink || p.block <= 32 || p.units >= (size_t)2 * kRuleSMs) break;
-        p.block /= 2;
+    int span_log2 = kWarpSpanBytesLog2 - log2_exact((int)elem_bytes(p.dtype));
+    const int group_log2 = kGroupBytesLog2 - log2_exact((int)elem_bytes(p.dtype));
+    if (may_shrink && p.segments == 1 && p.seg_len <= ((size_t)1 << (group_log2 + 1 + 5))) {
+        // one CTA: spans of one group (two above 32 groups), as few warps as cover it
+        span_log2 = p.seg_len > ((size_t)1 << (group_log2 + 5)) ? group_log2 + 1 : group_log2;
+        int warps = 1;
+        while (((size_t)warps << span_log2) < p.seg_len) warps *= 2;
+        p.block = 32 * warps;
+        p.chunk_log2 = span_log2 + log2_exact(warps);
+        p.cps = 1;
+        p.units = 1;
+    } else {
+        for (;;) {
+            p.chunk_log2 = span_log2 + log2_exact(p.block / 32);
+            p.cps = (p.seg_len + ((size_t)1 << p.chunk_log2) - 1) >> p.chunk_log2;
+            p.units = p.segments * p.cps;
+            if (!may_shrink || p.units >= (size_t)2 * kRuleSMs) break;
+            if (p.block > 32)
+                p.block /= 2;
+            else if (span_log2 > group_log2)
+                span_log2--;
+            else
+                break;
+        }
     }
     const size_t resident =
         (size_t)sm_count(dev) *
@@ -391,7 +411,7 @@ Plan make_plan(size_t segments, size_t seg_len, bool rows_call, const tcr_mode &
         // one persistent CTA per SM (its shared-memory ring fills the SM)
         p.path = kPathTmem;
         p.block = tmem_block_threads();
-        p.chunk_log2 = tmem_unit_log2();
+        p.chunk_log2 = tmem_unit_log2(seg_len);
         p.units = tmem_units(seg_len);
         p.cps = p.units;
         p.grid = (int)(p.units < sms ? p.units : sms);

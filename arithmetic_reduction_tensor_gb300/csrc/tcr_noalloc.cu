@@ -107,17 +107,36 @@ extern "C" tcr_status tcr_reduce_sum_noalloc(const void *x, size_t n, float *out
     }
 
     // 2^kWarpSpanBytesLog2 bytes per warp, and the same choice of CTA size
-    // for small inputs, as in the allocating entry point
+    // and span for small inputs, as in the allocating entry point
     int block_used = block;
     int warps_log2 = 0;
     while ((32 << warps_log2) < block_used) warps_log2++;
-    int chunk_log2 = kWarpSpanBytesLog2 - elem_log2 + warps_log2;
+    int span_log2 = kWarpSpanBytesLog2 - elem_log2;
+    const int group_log2 = kGroupBytesLog2 - elem_log2;
+    int chunk_log2 = span_log2 + warps_log2;
     size_t cps = (n + ((size_t)1 << chunk_log2) - 1) >> chunk_log2;
     const bool may_shrink = mode.kind == TCR_FIXED_ORDER || mode.block_threads == 0;
-    while (may_shrink && block_used > 32 && cps < (size_t)2 * 152) {
-        block_used /= 2;
-        warps_log2--;
-        chunk_log2--;
+    const bool one_cta = may_shrink && n <= ((size_t)1 << (group_log2 + 1 + 5));
+    if (one_cta) {
+        // one CTA, as in the allocating entry point
+        span_log2 = n > ((size_t)1 << (group_log2 + 5)) ? group_log2 + 1 : group_log2;
+        block_used = 32;
+        warps_log2 = 0;
+        while (((size_t)block_used << (span_log2 - 5)) < n) {
+            block_used *= 2;
+            warps_log2++;
+        }
+        chunk_log2 = span_log2 + warps_log2;
+        cps = 1;
+    }
+    while (may_shrink && !one_cta && cps < (size_t)2 * 152 && (block_used > 32 || span_log2 > group_log2)) {
+        if (block_used > 32) {
+            block_used /= 2;
+            warps_log2--;
+        } else {
+            span_log2--;
+        }
+        chunk_log2 = span_log2 + warps_log2;
         cps = (n + ((size_t)1 << chunk_log2) - 1) >> chunk_log2;
     }
     if (cps > kNoAllocMaxPartials) return TCR_ERR_UNSUPPORTED;

@@ -151,12 +151,15 @@ def test_binary32_descriptors(lib):
         assert d32["chunk_log2"] == d16["chunk_log2"] - 1
         assert d32["partials"] == 2 * d16["partials"]
     # rows of up to 32 KiB take one warp each: 16384 16-bit or 8192 binary32 inputs
-    # (at 32 threads a chunked row is 2^12-input chunks, so 8193 makes 3)
+    # (at 32 threads a chunked row is 2^12-input chunks, so 8193 makes 3 --
+    # 300 work units, fewer than two per SM, so the spans halve: 5 per row)
     m = tcr.Mode(tcr.FIXED_ORDER, block_threads=32, dtype=tcr.F32)
     d = tcr.tcr_order_descriptor(rows=100, cols=8192, mode=m)
     assert d["partials"] == 0 and d["launch_block"] == 256
     d = tcr.tcr_order_descriptor(rows=100, cols=8193, mode=m)
-    assert d["partials"] == 300 and d["launch_block"] == 32
+    assert d["partials"] == 500 and d["launch_block"] == 32 and d["chunk_log2"] == 11
+    d = tcr.tcr_order_descriptor(rows=200, cols=8193, mode=m)
+    assert d["partials"] == 600 and d["chunk_log2"] == 12
     # the tcgen05 kind reduces binary32 inputs with the mma.sync split kernel
     d = tcr.tcr_order_descriptor(n=1 << 24, mode=tcr.Mode(tcr.MMA_CHAIN_TMEM, dtype=tcr.F32))
     dm = tcr.tcr_order_descriptor(n=1 << 24, mode=tcr.Mode(tcr.MMA_CHAIN, dtype=tcr.F32))
@@ -288,20 +291,58 @@ def test_gemm_descriptor_rule(lib):
 
 
 def test_small_inputs_get_smaller_ctas(lib):
-    # FIXED_ORDER (bits independent of the CTA size) and default-size MMA_CHAIN
-    # halve the CTA, from the requested (or default 256) size, until there are
-    # 2 x 152 work units of 2^13 x warps inputs or the CTA is one warp; a
-    # caller's MMA_CHAIN block size is kept
+    # FIXED_ORDER (bits independent of the CTA size) and default-size MMA_CHAIN:
+    # a sum of at most 2^17 inputs is one CTA (spans of one 2^11-input group,
+    # two above 2^16 inputs; as few warps as cover it), one launch; larger
+    # ones halve the CTA, from the requested (or default 256) size, then the
+    # warp span (2^13 inputs down to one group), until there are 2 x 152
+    # work units of span x warps inputs or neither can shrink; a caller's
+    # MMA_CHAIN block size is kept
     def expected(n, blk):
-        while blk > 32 and -(-n // (8192 * (blk // 32))) < 304:
-            blk //= 2
-        return blk
-    for n in (1 << 20, 1 << 22, 1 << 24, 1 << 26, 1 << 30):
+        if n <= 1 << 17:
+            span = 12 if n > 1 << 16 else 11
+            warps = 1
+            while warps << span < n:
+                warps *= 2
+            return 32 * warps, span + warps.bit_length() - 1
+        span = 13
+        while -(-n // ((1 << span) * (blk // 32))) < 304:
+            if blk > 32:
+                blk //= 2
+            elif span > 11:
+                span -= 1
+            else:
+                break
+        return blk, span + (blk // 32).bit_length() - 1
+    for n in (1, 5000, 1 << 14, 1 << 17, (1 << 17) + 1, 1 << 20, 1 << 22, 1 << 24, 1 << 26, 1 << 30):
         for m, start in ((tcr.Mode(tcr.FIXED_ORDER), 256),
                          (tcr.Mode(tcr.FIXED_ORDER, block_threads=1024), 1024),
                          (tcr.Mode(tcr.MMA_CHAIN), 256)):
             d = tcr.tcr_order_descriptor(n=n, mode=m)
-            assert d["launch_block"] == expected(n, start), (n, m)
-    assert tcr.tcr_order_descriptor(n=1 << 20, mode=tcr.Mode(tcr.FIXED_ORDER))["launch_block"] == 32
+            assert (d["launch_block"], d["chunk_log2"]) == expected(n, start), (n, m)
+    d = tcr.tcr_order_descriptor(n=1 << 20, mode=tcr.Mode(tcr.FIXED_ORDER))
+    assert (d["launch_block"], d["chunk_log2"], d["partials"]) == (32, 11, 512)
+    d = tcr.tcr_order_descriptor(n=1 << 14, mode=tcr.Mode(tcr.MMA_CHAIN))
+    assert (d["launch_block"], d["chunk_log2"], d["partials"], d["launches"]) == (256, 14, 0, 1)
+    d = tcr.tcr_order_descriptor(n=100_000, mode=tcr.Mode(tcr.FIXED_ORDER))
+    assert (d["launch_block"], d["chunk_log2"], d["partials"], d["launches"]) == (1024, 17, 0, 1)
     d = tcr.tcr_order_descriptor(n=1 << 20, mode=tcr.Mode(tcr.MMA_CHAIN, block_threads=256))
-    assert d["launch_block"] == 256
+    assert (d["launch_block"], d["chunk_log2"]) == (256, 16)
+
+
+def test_tcgen05_units_shrink_for_small_inputs(lib):
+    # the tcgen05 sum's work unit is 2^16 inputs (one unit, one launch, up to
+    # 2^16 inputs), above that halved while it leaves fewer than 2 x 152
+    # units, down to one 2048-input tile
+    def expected(n):
+        l = 16
+        while n > 1 << 16 and l > 11 and -(-n // (1 << l)) < 304:
+            l -= 1
+        return l, -(-n // (1 << l))
+    for n in (1, 2048, 1 << 16, (1 << 16) + 1, 100_000, 1 << 20, 1 << 24, 1 << 26, 1 << 30):
+        d = tcr.tcr_order_descriptor(n=n, mode=tcr.Mode(tcr.MMA_CHAIN_TMEM))
+        l, units = expected(n)
+        assert d["chunk_log2"] == l, n
+        assert d["partials"] == (units if units > 1 else 0), n
+    assert tcr.tcr_order_descriptor(n=1 << 20, mode=tcr.Mode(tcr.MMA_CHAIN_TMEM))["chunk_log2"] == 11
+    assert tcr.tcr_order_descriptor(n=1 << 30, mode=tcr.Mode(tcr.MMA_CHAIN_TMEM))["chunk_log2"] == 16
