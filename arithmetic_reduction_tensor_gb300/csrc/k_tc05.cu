@@ -32,6 +32,8 @@
 // raises a device-wide fault flag, drains its own copies and MMAs (again
 // with a limit), frees its TMEM and writes NaN as its partials, so a broken
 // pipeline shows up as a NaN result, never as a hang.
+#include <cstring>
+
 #include "kernels.cuh"
 #include "tc05.cuh"
 
@@ -72,6 +74,43 @@ template <int DT>
 __device__ __forceinline__ uint32_t instr_desc()
 {
     return instr_desc_n<DT, 16>();
+}
+
+// Issue NM MMAs (k = 0 .. NM-1) in chains of R: a chain starts on a free D
+// buffer (begin), its first MMA overwrites D, the rest accumulate, and its
+// end publishes D (end).  The boundaries are compile-time constants: MMAs
+// issued under run-time chain logic issued several times slower.  Returns
+// false when a wait gave up.
+template <int R, int NM, class Begin, class End, class Issue>
+__device__ __forceinline__ bool issue_chains(Begin &begin, End &end, Issue &issue)
+{
+#pragma unroll
+    for (int k = 0; k < NM; k++) {
+        if (k % R == 0 && !begin()) return false;
+        issue(k, k % R != 0 ? 1u : 0u);
+        if (k % R == R - 1 || k == NM - 1) end();
+    }
+    return true;
+}
+
+// Chains of R over n MMAs that run through stages of P: a chain ends with
+// its stage, so each whole stage holds ceil(P / R) chains.
+template <int R, int P>
+__device__ __forceinline__ int stage_chains(int n)
+{
+    return (n / P) * ((P + R - 1) / R) + (n % P + R - 1) / R;
+}
+
+// issue_chains for a run-time count 1 <= nm <= NM
+template <int R, int NM, class Begin, class End, class Issue>
+__device__ __forceinline__ bool issue_chains_upto(int nm, Begin &begin, End &end, Issue &issue)
+{
+    if constexpr (NM == 1) {
+        return issue_chains<R, 1>(begin, end, issue);
+    } else {
+        if (nm >= NM) return issue_chains<R, NM>(begin, end, issue);
+        return issue_chains_upto<R, NM - 1>(nm, begin, end, issue);
+    }
 }
 
 // ---------------------------------------------------------------- kernel
@@ -216,39 +255,82 @@ mma_tmem_kernel(const uint16_t *__restrict__ x, size_t n, size_t units, int unit
                 dphase ^= 1u << b;
                 if (++b == kTcDBuffers) b = 0;
             };
-            for (size_t u = blockIdx.x; u < units && !*abort; u += gridDim.x) {
-                const int tiles = unit_tiles(n, u, unit_log2);
-                int in_chain = 0;
-                for (int t0 = 0; t0 < tiles && !*abort; t0 += kTcTilesPerStage) {
-                    const int nt = min(kTcTilesPerStage, tiles - t0);
-                    if (!mbar_wait(full_bar(s), phase, abort)) break;
-                    tc_fence_after();
-                    const uint64_t sdesc = ring_desc + (uint64_t)s * kStageStep;
-                    bool ok = true;
-                    if (kTcTilesPerStage % R == 0 && nt == kTcTilesPerStage) {
-                        // whole stage, chains aligned to it: static boundaries
+            if constexpr (kTcTilesPerStage % R == 0) {
+                // R divides a stage: chains fall on stage boundaries, the
+                // whole-stage issue has static boundaries
+                for (size_t u = blockIdx.x; u < units && !*abort; u += gridDim.x) {
+                    const int tiles = unit_tiles(n, u, unit_log2);
+                    int in_chain = 0;
+                    for (int t0 = 0; t0 < tiles && !*abort; t0 += kTcTilesPerStage) {
+                        const int nt = min(kTcTilesPerStage, tiles - t0);
+                        if (!mbar_wait(full_bar(s), phase, abort)) break;
+                        tc_fence_after();
+                        const uint64_t sdesc = ring_desc + (uint64_t)s * kStageStep;
+                        bool ok = true;
+                        if (kTcTilesPerStage % R == 0 && nt == kTcTilesPerStage) {
+                            // whole stage, chains aligned to it: static boundaries
 #pragma unroll
-                        for (int t = 0; t < kTcTilesPerStage; t++) {
-                            if (t % R == 0 && !(ok = begin_chain())) break;
-                            tc_mma(tmem + (uint32_t)b * kTcDBufferStride, sdesc + (uint64_t)t * kTileStep,
-                                   b_desc, idesc, t % R != 0 ? 1u : 0u);
-                            if (t % R == R - 1) end_chain();
-                        }
-                    } else {
-                        for (int t = 0; t < nt; t++) {
-                            if (in_chain == 0 && !(ok = begin_chain())) break;
-                            tc_mma(tmem + (uint32_t)b * kTcDBufferStride, sdesc + (uint64_t)t * kTileStep,
-                                   b_desc, idesc, in_chain > 0 ? 1u : 0u);
-                            if (++in_chain == R || t0 + t + 1 == tiles) {
-                                end_chain();
-                                in_chain = 0;
+                            for (int t = 0; t < kTcTilesPerStage; t++) {
+                                if (t % R == 0 && !(ok = begin_chain())) break;
+                                tc_mma(tmem + (uint32_t)b * kTcDBufferStride, sdesc + (uint64_t)t * kTileStep,
+                                       b_desc, idesc, t % R != 0 ? 1u : 0u);
+                                if (t % R == R - 1) end_chain();
+                            }
+                        } else {
+                            for (int t = 0; t < nt; t++) {
+                                if (in_chain == 0 && !(ok = begin_chain())) break;
+                                tc_mma(tmem + (uint32_t)b * kTcDBufferStride, sdesc + (uint64_t)t * kTileStep,
+                                       b_desc, idesc, in_chain > 0 ? 1u : 0u);
+                                if (++in_chain == R || t0 + t + 1 == tiles) {
+                                    end_chain();
+                                    in_chain = 0;
+                                }
                             }
                         }
+                        tc_commit(empty_bar(s));                  // stage may be refilled
+                        if (++s == kTcStages) {
+                            s = 0;
+                            phase ^= 1u;
+                        }
+                        if (!ok) break;
                     }
-                    tc_commit(empty_bar(s));                  // stage may be refilled
-                    if (++s == kTcStages) {
-                        s = 0;
-                        phase ^= 1u;
+                }
+            } else {
+                // chains end with their stage (R does not divide it)
+                for (size_t u = blockIdx.x; u < units && !*abort; u += gridDim.x) {
+                    const int tiles = unit_tiles(n, u, unit_log2);
+                    bool ok = true;
+                    for (int t0 = 0; t0 < tiles && ok; t0 += kTcTilesPerStage) {
+                        const int nt = min(kTcTilesPerStage, tiles - t0);
+                        if (!mbar_wait(full_bar(s), phase, abort)) break;
+                        tc_fence_after();
+                        const uint64_t sdesc = ring_desc + (uint64_t)s * kStageStep;
+                        // the stage's tiles in chains of R (a chain ends with its stage)
+                        if (nt == kTcTilesPerStage) {
+                            // whole stage: static chain boundaries (the MMAs issue
+                            // several times slower under run-time chain logic)
+#pragma unroll
+                            for (int t = 0; t < kTcTilesPerStage; t++) {
+                                if (t % R == 0 && !(ok = begin_chain())) break;
+                                tc_mma(tmem + (uint32_t)b * kTcDBufferStride, sdesc + (uint64_t)t * kTileStep,
+                                       b_desc, idesc, t % R != 0 ? 1u : 0u);
+                                if (t % R == R - 1 || t == kTcTilesPerStage - 1) end_chain();
+                            }
+                        } else {
+                            // a unit's last, partial stage (the array's end; every stage
+                            // of the units of fewer than 8 tiles that small inputs use)
+                            for (int t = 0; t < nt; t++) {
+                                if (t % R == 0 && !(ok = begin_chain())) break;
+                                tc_mma(tmem + (uint32_t)b * kTcDBufferStride, sdesc + (uint64_t)t * kTileStep,
+                                       b_desc, idesc, t % R != 0 ? 1u : 0u);
+                                if (t % R == R - 1 || t == nt - 1) end_chain();
+                            }
+                        }
+                        tc_commit(empty_bar(s));                  // stage may be refilled
+                        if (++s == kTcStages) {
+                            s = 0;
+                            phase ^= 1u;
+                        }
                     }
                     if (!ok) break;
                 }
@@ -268,10 +350,12 @@ mma_tmem_kernel(const uint16_t *__restrict__ x, size_t n, size_t units, int unit
         uint32_t dphase = 0u;
         for (size_t u = blockIdx.x; u < units; u += gridDim.x) {
             const int tiles = unit_tiles(n, u, unit_log2);
-            const int chains = (tiles + R - 1) / R;
+            const int chains = stage_chains<R, kTcTilesPerStage>(tiles);
             float acc = 0.f;
-            for (int c = 0; c < chains && !*abort; c++) {
-                if (!mbar_wait(dfull_bar(b), (dphase >> b) & 1u, abort)) break;
+            for (int c = 0; c < chains; c++) {
+                // the warp takes the wait's outcome together: tcgen05.ld is warp-wide
+                const bool ok = !*abort && mbar_wait(dfull_bar(b), (dphase >> b) & 1u, abort);
+                if (!__all_sync(kFull, ok)) break;
                 tc_fence_after();
                 const float v = tc_ld_lane(tmem + lane_base + (uint32_t)b * kTcDBufferStride);
                 acc = __fadd_rn(acc, v);
@@ -312,33 +396,43 @@ mma_tmem_kernel(const uint16_t *__restrict__ x, size_t n, size_t units, int unit
 
 // ---------------------------------------------------------------- rows
 
-// Rows: D's 128 lanes are 128 consecutive data rows.  A 2-D tensor map over
-// the row-major matrix (dims: cols, rows) with a 64-column x 128-row box and
-// the 128-byte swizzle lands a row block as 128 rows of 128 bytes (8-row
-// atoms of 1024 bytes, the 16-byte chunks of row r permuted by r mod 8) --
-// the SWIZZLE_128B K-major layout the MMA descriptor names, so one box is
-// four MMAs of K = 16, the k-th starting 32 bytes further.  The swizzle only
-// permutes chunks within a row, so each MMA row still holds one data row.
-// The column of D read out after a chain holds the 128 rows' sums over that
-// chain's columns.  Work unit: 128 rows x kTcRowsChunkCols columns, one
-// partial per row and unit; the tensor map zero-fills rows and columns past
-// the matrix.
-constexpr int kTcRowsChunkCols = 1024;                // columns per work unit
-constexpr int kTcRowsBoxCols = 64;                    // columns per tensor-map box
-constexpr int kTcRowsBoxBytes = 128 * kTcRowsBoxCols * 2;     // 16 KiB
-constexpr int kTcRowsBoxesPerStage = 4;               // 64 KiB, 16 MMAs per stage
-constexpr int kTcRowsStageBytes = kTcRowsBoxBytes * kTcRowsBoxesPerStage;
-constexpr int kTcRowsStages = 3;                      // 192 KiB ring
+// Rows: one MMA tile holds 16 data rows, 8 TMEM lanes to a row.  A 64 KiB
+// stage of the ring holds 16 G rows x S columns, row-major with a pitch of
+// 2S bytes (S = 2048 columns and G = 1 for rows of more than 1024 columns,
+// S = 1024 and G = 2 for rows of 768 to 1024; the library sends shorter
+// rows to the mma.sync kernels), brought in by one 3-D tensor-map box (rows
+// of whole 128-column blocks) or one 1-D bulk copy per row: either reads
+// each row's bytes contiguously, 4 KiB at a time on long rows.
+// Read through a K-major descriptor with no swizzle whose 8-row groups are
+// one stage row apart and whose two K halves are 128 bytes apart, lane
+// 8g + i of an MMA takes 16 inputs of data row g of its group (bytes 16i and
+// 128 + 16i of the MMA's 256-byte column slice), so D lanes 8g .. 8g+7 hold
+// row g's partial sums; the next MMA of a chain takes the next 128 columns
+// of the same rows.  The MMAs cover a row's whole 128-column slices; the
+// last cols % 128 inputs of a row are added by the epilogue from global
+// memory, and rows past the matrix are neither copied nor stored (their
+// lanes hold stale values that no row uses).  Work unit: 16 G rows x the
+// whole row, or chunks of kTcRowsMaxChunkCols columns of longer rows; per
+// row group the epilogue adds the chain results per lane, then each row's 8
+// lanes by an xor butterfly.
+constexpr int kTcRowsGroup = 16;                       // data rows per MMA tile
+constexpr int kTcRowsMmaCols = 128;                    // columns per MMA and row
+constexpr int kTcRowsStageCols = 2048;                 // S of long rows (4 KiB a row)
+constexpr int kTcRowsMinStageCols = 1024;              // S of the shortest rows (G = 2)
+constexpr int kTcRowsStageBytes = kTcRowsGroup * kTcRowsStageCols * 2;     // 64 KiB
+constexpr int kTcRowsStages = 3;                       // 192 KiB ring
+constexpr size_t kTcRowsMaxChunkCols = 8192;           // columns per work unit, at most
 constexpr int kTcRowsOffOnes = kTcRowsStages * kTcRowsStageBytes;
 constexpr int kTcRowsOffBars = kTcRowsOffOnes + 1024;
 constexpr int kTcRowsNumBars = 2 * kTcRowsStages + 2 * kTcDBuffers + 1;
 constexpr int kTcRowsOffMisc = kTcRowsOffBars + 8 * kTcRowsNumBars;
 constexpr int kTcRowsSmemBytes = kTcRowsOffMisc + 64 + 1024;
 
-template <int DT, int R>
+template <int DT, int R, bool SHORT>
 __global__ void __launch_bounds__(kTcThreads, 1)
-mma_tmem_rows_kernel(const __grid_constant__ CUtensorMap tmap, size_t rows, size_t cols,
-                     size_t cpr, size_t units, float *__restrict__ dst, uint32_t inject_stall)
+mma_tmem_rows_kernel(const __grid_constant__ CUtensorMap tmap, int use_map, const uint16_t *__restrict__ x,
+                     size_t rows, size_t cols, size_t chunk_cols, size_t cpr, size_t units, int stage_cols,
+                     float *__restrict__ dst, uint32_t inject_stall)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -356,11 +450,32 @@ mma_tmem_rows_kernel(const __grid_constant__ CUtensorMap tmap, size_t rows, size
     volatile uint32_t *abort = misc + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // boxes (64 columns) of work unit u
-    auto unit_boxes = [&](size_t u) -> int {
-        const size_t c0 = (u % cpr) * kTcRowsChunkCols;
-        const size_t nc = cols - c0 < (size_t)kTcRowsChunkCols ? cols - c0 : (size_t)kTcRowsChunkCols;
-        return (int)((nc + kTcRowsBoxCols - 1) / kTcRowsBoxCols);
+    // G: row groups per unit (SHORT: rows of at most 1024 columns, G >= 2)
+    const int groups = SHORT ? kTcRowsStageCols / stage_cols : 1;
+    const int unit_rows = kTcRowsGroup * groups;
+    const uint32_t pitch = 2u * (uint32_t)stage_cols;               // bytes per stage row
+    // columns of column chunk c of a row, and of them the whole 128-column slices
+    auto unit_cols = [&](size_t c) -> int {
+        const size_t c0 = c * chunk_cols;
+        return (int)(cols - c0 < chunk_cols ? cols - c0 : chunk_cols);
+    };
+    auto mma_cols = [&](int nc) -> int { return nc - nc % kTcRowsMmaCols; };
+    // work unit u = (row block u / cpr, column chunk u % cpr), walked
+    // u = blockIdx.x, + gridDim.x, ... with the quotient and remainder
+    // carried (no 64-bit division per unit)
+    struct Unit {
+        size_t u, blk, chunk;
+    };
+    const size_t step_blk = gridDim.x / cpr, step_chunk = gridDim.x % cpr;
+    auto first_unit = [&]() -> Unit { return {blockIdx.x, blockIdx.x / cpr, blockIdx.x % cpr}; };
+    auto next_unit = [&](Unit &w) {
+        w.u += gridDim.x;
+        w.blk += step_blk;
+        w.chunk += step_chunk;
+        if (w.chunk >= cpr) {
+            w.chunk -= cpr;
+            w.blk++;
+        }
     };
 
     {
@@ -380,7 +495,7 @@ mma_tmem_rows_kernel(const __grid_constant__ CUtensorMap tmap, size_t rows, size
         mbar_init(drain_bar, 1);
         *abort = 0u;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmap) : "memory");
+        if (use_map) asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmap) : "memory");
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     if (warp == 1) {
@@ -395,56 +510,71 @@ mma_tmem_rows_kernel(const __grid_constant__ CUtensorMap tmap, size_t rows, size
     const uint32_t tmem = *tmem_holder;
 
     if (warp == 0) {
-        // ---------------- producer: one 64-column x 128-row box per stage
-        if (lane == 0) {
-            int s = 0;
-            uint32_t phase = 0;
-            bool armed[kTcRowsStages];
-            uint32_t armed_phase[kTcRowsStages];
-            for (int i = 0; i < kTcRowsStages; i++) {
-                armed[i] = false;
-                armed_phase[i] = 0;
-            }
-            for (size_t u = blockIdx.x; u < units && !*abort; u += gridDim.x) {
-                const int row0 = (int)((u / cpr) * 128);
-                const int col0 = (int)((u % cpr) * kTcRowsChunkCols);
-                const int boxes = unit_boxes(u);
-                for (int j = 0; j < boxes; j += kTcRowsBoxesPerStage) {
-                    const int nb = min(kTcRowsBoxesPerStage, boxes - j);
-                    if (!mbar_wait(empty_bar(s), phase ^ 1u, abort)) break;
-                    mbar_arrive_expect_tx(full_bar(s), (uint32_t)nb * kTcRowsBoxBytes);
-                    for (int q = 0; q < nb; q++)
-                        tma_load_2d(ring + (uint32_t)s * kTcRowsStageBytes + (uint32_t)q * kTcRowsBoxBytes,
-                                    &tmap, col0 + (j + q) * kTcRowsBoxCols, row0, full_bar(s));
-                    armed[s] = true;
-                    armed_phase[s] = phase;
-                    if (++s == kTcRowsStages) {
-                        s = 0;
-                        phase ^= 1u;
+        // ---------------- producer: a stage is one 3-D tensor-map box (whole
+        // 128-column rows), else one bulk copy per row, rows spread over the lanes
+        int s = 0;
+        uint32_t phase = 0;
+        bool armed[kTcRowsStages];
+        uint32_t armed_phase[kTcRowsStages];
+        for (int i = 0; i < kTcRowsStages; i++) {
+            armed[i] = false;
+            armed_phase[i] = 0;
+        }
+        bool ok = true;
+        for (Unit w = first_unit(); w.u < units && ok; next_unit(w)) {
+            const size_t row0 = w.blk * (size_t)unit_rows;
+            const size_t col0 = w.chunk * chunk_cols;
+            const int live = (int)(rows - row0 < (size_t)unit_rows ? rows - row0 : (size_t)unit_rows);
+            const int mc = mma_cols(unit_cols(w.chunk));
+            for (int c = 0; c < mc; c += stage_cols) {
+                const int sc = min(stage_cols, mc - c);
+                const uint32_t row_bytes = (uint32_t)sc * 2u;
+                if (lane == 0) {
+                    ok = !*abort && mbar_wait(empty_bar(s), phase ^ 1u, abort);
+                    if (ok && use_map) {
+                        // box: 128 columns x S / 128 column blocks x 16 G rows (64 KiB,
+                        // blocks and rows past the matrix zero-filled)
+                        mbar_arrive_expect_tx(full_bar(s), (uint32_t)kTcRowsStageBytes);
+                        tma_load_3d(ring + (uint32_t)s * kTcRowsStageBytes, &tmap, 0,
+                                    (int)((col0 + (size_t)c) / kTcRowsMmaCols), (int)row0, full_bar(s));
+                    } else if (ok) {
+                        mbar_arrive_expect_tx(full_bar(s), (uint32_t)live * row_bytes);
                     }
                 }
+                ok = __shfl_sync(kFull, ok, 0);
+                if (!ok) break;
+                if (!use_map)
+                    for (int r = lane; r < live; r += 32)
+                        bulk_copy_g2s(ring + (uint32_t)s * kTcRowsStageBytes + (uint32_t)r * pitch,
+                                      x + (row0 + (size_t)r) * cols + col0 + (size_t)c, row_bytes, full_bar(s));
+                armed[s] = true;
+                armed_phase[s] = phase;
+                if (++s == kTcRowsStages) {
+                    s = 0;
+                    phase ^= 1u;
+                }
             }
-            if (*abort) {
-                for (int i = 0; i < kTcRowsStages; i++) {
-                    if (!armed[i]) continue;
-                    const uint64_t t0 = global_ns();
-                    while (!mbar_try_wait(full_bar(i), armed_phase[i]) &&
-                           global_ns() - t0 < kWaitLimitNs) {
-                    }
+        }
+        if (lane == 0 && *abort) {
+            for (int i = 0; i < kTcRowsStages; i++) {
+                if (!armed[i]) continue;
+                const uint64_t t0 = global_ns();
+                while (!mbar_try_wait(full_bar(i), armed_phase[i]) && global_ns() - t0 < kWaitLimitNs) {
                 }
             }
         }
         __syncwarp();
     } else if (warp == 1) {
-        // ---------------- MMA issuer: four MMAs (K = 16) per stage
+        // ---------------- MMA issuer
         if (lane == 0) {
             const uint32_t idesc = instr_desc<DT>();
             const uint64_t b_desc = smem_desc(ones, 128, 256);
-            const uint64_t ring_desc = smem_desc_sw128(ring);
-            constexpr uint64_t kKStep = 32u >> 4;                    // 16 columns = 32 bytes
-            constexpr uint64_t kBoxStep = (uint64_t)kTcRowsBoxBytes >> 4;
+            // 8-row groups one stage row apart, K halves 128 bytes apart
+            const uint64_t ring_desc = smem_desc(ring, 128, pitch);
+            constexpr uint64_t kMmaStep = (uint64_t)(kTcRowsMmaCols * 2) >> 4;      // 256 bytes
             constexpr uint64_t kStageStep = (uint64_t)kTcRowsStageBytes >> 4;
-            constexpr int kMmasPerStage = 4 * kTcRowsBoxesPerStage;
+            constexpr int kMmasPerStage = kTcRowsStageCols / kTcRowsMmaCols;         // 16 (G = 1)
+            const uint64_t group_step = (uint64_t)(kTcRowsGroup * pitch) >> 4;
             int s = 0, b = 0;
             uint32_t phase = 0, dphase = 0u;
             auto begin_chain = [&]() -> bool {
@@ -461,40 +591,56 @@ mma_tmem_rows_kernel(const __grid_constant__ CUtensorMap tmap, size_t rows, size
                 dphase ^= 1u << b;
                 if (++b == kTcDBuffers) b = 0;
             };
-            for (size_t u = blockIdx.x; u < units && !*abort; u += gridDim.x) {
-                const int boxes = unit_boxes(u);
-                const int mmas = 4 * boxes;
-                int in_chain = 0;
+            for (Unit w = first_unit(); w.u < units && !*abort; next_unit(w)) {
+                const int mmas = mma_cols(unit_cols(w.chunk)) / kTcRowsMmaCols;    // per row group
                 bool ok = true;
-                for (int j = 0; j < boxes && ok; j += kTcRowsBoxesPerStage) {
-                    const int nm = 4 * min(kTcRowsBoxesPerStage, boxes - j);
-                    if (!mbar_wait(full_bar(s), phase, abort)) {
-                        ok = false;
-                        break;
+                if constexpr (!SHORT) {
+                    // one row group; its chains run along the row, each ending with its stage
+                    for (int done = 0; done < mmas && ok; done += kMmasPerStage) {
+                        const int nm = min(kMmasPerStage, mmas - done);
+                        if (!mbar_wait(full_bar(s), phase, abort)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint64_t sdesc = ring_desc + (uint64_t)s * kStageStep;
+                        if (nm == kMmasPerStage) {
+                            // whole stage: static chain boundaries (the MMAs issue
+                            // several times slower under run-time chain logic)
+#pragma unroll
+                            for (int k = 0; k < kMmasPerStage; k++) {
+                                if (k % R == 0 && !(ok = begin_chain())) break;
+                                tc_mma(tmem + (uint32_t)b * kTcDBufferStride, sdesc + (uint64_t)k * kMmaStep,
+                                       b_desc, idesc, k % R != 0 ? 1u : 0u);
+                                if (k % R == R - 1 || k == kMmasPerStage - 1) end_chain();
+                            }
+                        } else {
+                            // the row's (or chunk's) last, partial stage
+                            auto issue = [&](int k, uint32_t acc) {
+                                tc_mma(tmem + (uint32_t)b * kTcDBufferStride, sdesc + (uint64_t)k * kMmaStep,
+                                       b_desc, idesc, acc);
+                            };
+                            ok = issue_chains_upto<R, kMmasPerStage - 1>(nm, begin_chain, end_chain, issue);
+                        }
+                        tc_commit(empty_bar(s));
+                        if (++s == kTcRowsStages) {
+                            s = 0;
+                            phase ^= 1u;
+                        }
                     }
+                } else {
+                    // G row groups of short rows in one stage, each row group its own chains
+                    if (!mbar_wait(full_bar(s), phase, abort)) break;
                     tc_fence_after();
                     const uint64_t sdesc = ring_desc + (uint64_t)s * kStageStep;
-                    // MMA k of the stage: box k / 4, 32-byte slice k % 4
-                    if (kMmasPerStage % R == 0 && nm == kMmasPerStage) {
-#pragma unroll
-                        for (int k = 0; k < kMmasPerStage; k++) {
-                            if (k % R == 0 && !(ok = begin_chain())) break;
-                            tc_mma(tmem + (uint32_t)b * kTcDBufferStride,
-                                   sdesc + (uint64_t)(k / 4) * kBoxStep + (uint64_t)(k % 4) * kKStep,
-                                   b_desc, idesc, k % R != 0 ? 1u : 0u);
-                            if (k % R == R - 1) end_chain();
-                        }
-                    } else {
-                        for (int k = 0; k < nm; k++) {
-                            if (in_chain == 0 && !(ok = begin_chain())) break;
-                            tc_mma(tmem + (uint32_t)b * kTcDBufferStride,
-                                   sdesc + (uint64_t)(k / 4) * kBoxStep + (uint64_t)(k % 4) * kKStep,
-                                   b_desc, idesc, in_chain > 0 ? 1u : 0u);
-                            if (++in_chain == R || 4 * j + k + 1 == mmas) {
-                                end_chain();
-                                in_chain = 0;
-                            }
-                        }
+                    for (int j = 0; j < groups && ok; j++) {
+                        const uint64_t gdesc = sdesc + (uint64_t)j * group_step;
+                        auto issue = [&](int k, uint32_t acc) {
+                            tc_mma(tmem + (uint32_t)b * kTcDBufferStride, gdesc + (uint64_t)k * kMmaStep, b_desc,
+                                   idesc, acc);
+                        };
+                        // a row group of short rows has at most 8 MMAs (S = 1024 columns)
+                        ok = issue_chains_upto<R, kMmasPerStage / 2>(mmas, begin_chain, end_chain, issue);
                     }
                     tc_commit(empty_bar(s));
                     if (++s == kTcRowsStages) {
@@ -511,27 +657,43 @@ mma_tmem_rows_kernel(const __grid_constant__ CUtensorMap tmap, size_t rows, size
         }
         __syncwarp();
     } else {
-        // ---------------- epilogue: thread m holds row row0 + m of the unit
-        const int et = threadIdx.x - 64;
+        // ---------------- epilogue: TMEM lane m = 8g + i holds part of row g of a row group
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-        const int m = 32 * (warp & 3) + lane;              // TMEM lane = row in the block
-        (void)et;
+        const int m = 32 * (warp & 3) + lane;
         int b = 0;
         uint32_t dphase = 0u;
-        for (size_t u = blockIdx.x; u < units; u += gridDim.x) {
-            const int chains = (4 * unit_boxes(u) + R - 1) / R;
-            float acc = 0.f;
-            for (int c = 0; c < chains && !*abort; c++) {
-                if (!mbar_wait(dfull_bar(b), (dphase >> b) & 1u, abort)) break;
-                tc_fence_after();
-                acc = __fadd_rn(acc, tc_ld_lane(tmem + lane_base + (uint32_t)b * kTcDBufferStride));
-                tc_fence_before();
-                mbar_arrive(dempty_bar(b));
-                dphase ^= 1u << b;
-                if (++b == kTcDBuffers) b = 0;
+        for (Unit w = first_unit(); w.u < units; next_unit(w)) {
+            const int nc = unit_cols(w.chunk);
+            const int mc = mma_cols(nc);
+            const int chains = stage_chains<R, kTcRowsStageCols / kTcRowsMmaCols>(mc / kTcRowsMmaCols);
+            for (int j = 0; j < groups; j++) {
+                float acc = 0.f;
+                for (int c = 0; c < chains; c++) {
+                    // the warp takes the wait's outcome together: tcgen05.ld is warp-wide
+                    const bool ok = !*abort && mbar_wait(dfull_bar(b), (dphase >> b) & 1u, abort);
+                    if (!__all_sync(kFull, ok)) break;
+                    tc_fence_after();
+                    acc = __fadd_rn(acc, tc_ld_lane(tmem + lane_base + (uint32_t)b * kTcDBufferStride));
+                    tc_fence_before();
+                    mbar_arrive(dempty_bar(b));
+                    dphase ^= 1u << b;
+                    if (++b == kTcDBuffers) b = 0;
+                }
+                const size_t row = w.blk * (size_t)unit_rows + (size_t)(kTcRowsGroup * j + (m >> 3));
+                if (row < rows) {
+                    // the row's last nc - mc inputs of the unit (fewer than 128):
+                    // lane i adds inputs i, i + 8, ...
+                    const uint16_t *t = x + row * cols + w.chunk * chunk_cols;
+                    for (int q = mc + (m & 7); q < nc; q += 8)
+                        acc = __fadd_rn(acc, DT == kF16 ? leaf_lo<kF16>(__ldg(t + q)) : leaf_lo<kBF16>(__ldg(t + q)));
+                }
+                // the row's 8 lanes (aligned within the warp): every lane gets the same bits
+                acc = __fadd_rn(acc, __shfl_xor_sync(kFull, acc, 1));
+                acc = __fadd_rn(acc, __shfl_xor_sync(kFull, acc, 2));
+                acc = __fadd_rn(acc, __shfl_xor_sync(kFull, acc, 4));
+                if ((m & 7) == 0 && row < rows)
+                    dst[row * cpr + w.chunk] = *abort ? __int_as_float(0x7fc00000) : acc;
             }
-            const size_t row = (u / cpr) * 128 + (size_t)m;
-            if (row < rows) dst[row * cpr + (u % cpr)] = *abort ? __int_as_float(0x7fc00000) : acc;
         }
     }
 
@@ -599,54 +761,85 @@ cudaError_t launch_mma_tmem(int dtype, int R, const uint16_t *x, size_t n, float
     return cudaLaunchKernel(k, dim3(grid), dim3(kTcThreads), args, kTcSmemBytes, stream);
 }
 
-template <int DT>
+template <int DT, bool SHORT>
 static void *pick_rows_dt(int R)
 {
     switch (R) {
-    case 1: return (void *)mma_tmem_rows_kernel<DT, 1>;
-    case 2: return (void *)mma_tmem_rows_kernel<DT, 2>;
-    case 3: return (void *)mma_tmem_rows_kernel<DT, 3>;
-    case 4: return (void *)mma_tmem_rows_kernel<DT, 4>;
-    case 5: return (void *)mma_tmem_rows_kernel<DT, 5>;
-    case 6: return (void *)mma_tmem_rows_kernel<DT, 6>;
-    case 7: return (void *)mma_tmem_rows_kernel<DT, 7>;
-    case 8: return (void *)mma_tmem_rows_kernel<DT, 8>;
+    case 1: return (void *)mma_tmem_rows_kernel<DT, 1, SHORT>;
+    case 2: return (void *)mma_tmem_rows_kernel<DT, 2, SHORT>;
+    case 3: return (void *)mma_tmem_rows_kernel<DT, 3, SHORT>;
+    case 4: return (void *)mma_tmem_rows_kernel<DT, 4, SHORT>;
+    case 5: return (void *)mma_tmem_rows_kernel<DT, 5, SHORT>;
+    case 6: return (void *)mma_tmem_rows_kernel<DT, 6, SHORT>;
+    case 7: return (void *)mma_tmem_rows_kernel<DT, 7, SHORT>;
+    case 8: return (void *)mma_tmem_rows_kernel<DT, 8, SHORT>;
     default: return nullptr;
     }
 }
 
+// Work units: 16 G rows (G = row groups per stage, tmem_rows_stage_cols)
+// x the whole row up to kTcRowsMaxChunkCols columns, else chunks of that
+// many.  A function of cols only, so a row's chains (and MMA_CHAIN's bits)
+// do not depend on the number of rows or the device.
 size_t tmem_rows_chunks(size_t cols)
 {
-    return (cols + kTcRowsChunkCols - 1) / kTcRowsChunkCols;
+    return (cols + kTcRowsMaxChunkCols - 1) / kTcRowsMaxChunkCols;
+}
+
+// S: the columns of a row in one stage -- 2048, or 1024 for rows whose
+// whole 128-column slices fit 1024 columns; G = 2048 / S row groups share a
+// stage.
+static int tmem_rows_stage_cols(size_t cols)
+{
+    const size_t mc = (cols < kTcRowsMaxChunkCols ? cols : kTcRowsMaxChunkCols) / kTcRowsMmaCols *
+                      kTcRowsMmaCols;
+    int s = kTcRowsMinStageCols;
+    while (s < kTcRowsStageCols && (size_t)s < mc) s *= 2;
+    return s;
 }
 
 size_t tmem_rows_units(size_t rows, size_t cols)
 {
-    return ((rows + 127) / 128) * tmem_rows_chunks(cols);
+    const size_t unit_rows = (size_t)kTcRowsGroup * (kTcRowsStageCols / tmem_rows_stage_cols(cols));
+    return ((rows + unit_rows - 1) / unit_rows) * tmem_rows_chunks(cols);
 }
 
 cudaError_t launch_mma_tmem_rows(int dtype, int R, const uint16_t *x, size_t rows, size_t cols,
                                  float *dst, int grid, bool inject_stall, cudaStream_t stream)
 {
-    void *k = dtype == kF16 ? pick_rows_dt<kF16>(R) : pick_rows_dt<kBF16>(R);
+    int stage_cols = tmem_rows_stage_cols(cols);
+    const bool short_rows = stage_cols < kTcRowsStageCols;
+    void *k = dtype == kF16 ? (short_rows ? pick_rows_dt<kF16, true>(R) : pick_rows_dt<kF16, false>(R))
+                            : (short_rows ? pick_rows_dt<kBF16, true>(R) : pick_rows_dt<kBF16, false>(R));
     if (!k) return cudaErrorInvalidValue;
-    PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
-    if (!encode) return cudaErrorNotSupported;
-    alignas(64) CUtensorMap map;
-    const cuuint64_t gdim[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    const cuuint64_t gstride[1] = {(cuuint64_t)cols * 2};
-    const cuuint32_t box[2] = {kTcRowsBoxCols, 128};
-    const cuuint32_t estride[2] = {1, 1};
-    if (encode(&map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, (void *)x, gdim, gstride, box, estride,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return cudaErrorInvalidValue;
     cudaError_t e = set_smem_once(k, kTcRowsSmemBytes);
     if (e != cudaSuccess) return e;
+    size_t chunk_cols = kTcRowsMaxChunkCols;
     size_t cpr = tmem_rows_chunks(cols);
     size_t units = tmem_rows_units(rows, cols);
+    // rows of whole 128-column blocks: a 3-D view (128 columns, cols / 128
+    // blocks, rows) whose 64 KiB box is one stage as laid out above
+    alignas(64) CUtensorMap map;
+    std::memset(&map, 0, sizeof map);
+    int use_map = 0;
+    if (cols % kTcRowsMmaCols == 0) {
+        PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+        if (!encode) return cudaErrorNotSupported;
+        const cuuint64_t gdim[3] = {(cuuint64_t)kTcRowsMmaCols, (cuuint64_t)(cols / kTcRowsMmaCols),
+                                    (cuuint64_t)rows};
+        const cuuint64_t gstride[2] = {(cuuint64_t)kTcRowsMmaCols * 2, (cuuint64_t)cols * 2};
+        const cuuint32_t box[3] = {(cuuint32_t)kTcRowsMmaCols, (cuuint32_t)(stage_cols / kTcRowsMmaCols),
+                                   (cuuint32_t)(kTcRowsGroup * (kTcRowsStageCols / stage_cols))};
+        const cuuint32_t estride[3] = {1, 1, 1};
+        if (encode(&map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, (void *)x, gdim, gstride, box, estride,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+        use_map = 1;
+    }
     uint32_t stall = inject_stall ? 1u : 0u;
-    void *args[] = {(void *)&map, (void *)&rows, (void *)&cols, (void *)&cpr, (void *)&units,
+    void *args[] = {(void *)&map, (void *)&use_map, (void *)&x, (void *)&rows, (void *)&cols,
+                    (void *)&chunk_cols, (void *)&cpr, (void *)&units, (void *)&stage_cols,
                     (void *)&dst, (void *)&stall};
     return cudaLaunchKernel(k, dim3(grid), dim3(kTcThreads), args, kTcRowsSmemBytes, stream);
 }

@@ -87,9 +87,10 @@ cudaError_t launch_mma_tmem(int dtype, int R, const uint16_t *x, size_t n, float
 size_t tmem_units(size_t n);
 int tmem_block_threads();
 int tmem_unit_log2(size_t n);
-// Rows: D's 128 lanes are 128 consecutive rows, the inputs reach shared
-// memory by 2-D tensor-map copies; dst[row * chunks + c] is row `row`'s
-// partial over column chunk c (tmem_rows_chunks(cols) chunks per row).
+// Rows: one MMA tile holds 16 rows (8 of D's lanes to a row), the inputs
+// reach shared memory by 2-D tensor-map copies; dst[row * chunks + c] is
+// row `row`'s partial over column chunk c (tmem_rows_chunks(cols) chunks
+// per row; one chunk: dst is the output).
 // x must be 16-byte aligned and cols a multiple of 8, rows and cols < 2^31.
 cudaError_t launch_mma_tmem_rows(int dtype, int R, const uint16_t *x, size_t rows, size_t cols,
                                  float *dst, int grid, bool inject_stall, cudaStream_t stream);

@@ -431,6 +431,17 @@ packed_rows_kernel(const void *__restrict__ xv, size_t rows, size_t cols, float 
                 if (k == 7 && has_next) qt = load_tail<DT, VLOG>(rows, cols, nrow0, gm, lane);
         };
         float ta[8], tb[8];
+        // a load past the end of every row of the group (rows spanning 2 or
+        // 4 loads with fewer vectors than slots, e.g. 96 of 128): every
+        // vector of it is the pad, so the trees skip it -- the pad tree is
+        // -0.0 (+0.0 for squares).  The MMA path keeps its straight-line
+        // chain (a branch there cost more than the zero tiles it saves)
+        auto pad_load = [&](int k) -> bool {
+            if constexpr (VLOG >= 6)
+                return (size_t)(32 * Elem<DT>::kPerVec) * (size_t)(k & ((1 << (VLOG - 5)) - 1)) >= cols;
+            else
+                return false;
+        };
         if constexpr (MODE == kPackedMma) {
             // sums: tiles against ones; squares: the tiles' A * A^T diagonals
             // (pairs: sums into ta, squares into tb)
@@ -511,6 +522,12 @@ packed_rows_kernel(const void *__restrict__ xv, size_t rows, size_t cols, float 
         } else {
 #pragma unroll
             for (int k = 0; k < 8; k++) {
+                if (pad_load(k)) {
+                    ta[k] = (!PAIR && OP == kOpSquares) ? 0.0f : -0.0f;
+                    tb[k] = 0.0f;
+                    next(k);
+                    continue;
+                }
                 const uint4 a = vec(k);
                 if constexpr (!ALIGNED) next(k);
                 if constexpr (PAIR) vec_tree_pair<DT>(a, ta[k], tb[k]);

@@ -319,7 +319,7 @@ void plan_blocked(Plan &p, bool rows_call, int dev)
     p.launches = p.cps > 1 ? 2 : 1;
 }
 
-constexpr size_t kTmemRowsMinCols = 256;
+constexpr size_t kTmemRowsMinCols = 768;
 
 // Short rows, several to a warp group: one launch of kRowsBlock threads,
 // as many CTAs as there are groups of 8 warps' rows, at most a full wave.
@@ -391,12 +391,13 @@ Plan make_plan(size_t segments, size_t seg_len, bool rows_call, const tcr_mode &
         }
         return p;
     }
-    // rows of fewer than 256 inputs run the packed mma.sync kernel: a
-    // 128-row tile of them is mostly the tensor map's fill
+    // rows of fewer than 768 inputs run the packed mma.sync kernel: the
+    // tcgen05 kernel would put 4 or 8 row groups, each its own chains and
+    // read-out, in a 64 KiB stage -- its epilogue then bounds it
     if (p.kind == TCR_MMA_CHAIN_TMEM && rows_call && seg_len < kTmemRowsMinCols) p.kind = TCR_MMA_CHAIN;
     if (p.kind == TCR_MMA_CHAIN_TMEM && rows_call && aligned && segments < ((size_t)1 << 31) &&
         seg_len < ((size_t)1 << 31)) {
-        // 128 rows per MMA tile, 2-D tensor-map copies; one CTA per SM
+        // 16 rows per MMA tile, 2-D tensor-map copies; one CTA per SM
         p.path = kPathTmemRows;
         p.block = tmem_block_threads();
         p.cps = tmem_rows_chunks(seg_len);

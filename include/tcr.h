@@ -33,14 +33,18 @@
  *                     copies, tcgen05.mma (M = 128, N = 16, K = 16; one MMA
  *                     per 2048 inputs) with the accumulator in tensor memory,
  *                     R MMAs per chain, chain sub-results read out to fp32
- *                     registers; rows put 128 rows on D's 128 lanes and
- *                     reach shared memory by 2-D tensor-map copies.  Same
+ *                     registers; rows put 16 rows on an MMA tile (8 of D's
+ *                     lanes to a row, chains running along the row) and
+ *                     reach shared memory by 3-D tensor-map or per-row bulk
+ *                     copies.  A chain never spans two shared-memory stages
+ *                     (8 MMAs for sums, 16 for rows); when R does not
+ *                     divide that, a stage's last chain is shorter.  Same
  *                     error bound as TCR_MMA_CHAIN.  16-bit sums only: an
  *                     x that is not 16-byte aligned (or rows whose stride is
- *                     not), rows of fewer than 256 inputs (a tile of 128
- *                     such rows fills less than one K = 16 column block per
- *                     64-input box), sums of squares and binary32 inputs
- *                     are reduced by the TCR_MMA_CHAIN kernels instead.
+ *                     not), rows of fewer than 768 inputs (a 64 KiB stage of
+ *                     them holds too little work per MMA chain), sums of
+ *                     squares and binary32 inputs are reduced by the
+ *                     TCR_MMA_CHAIN kernels instead.
  *   TCR_FIXED_ORDER   a balanced binary tree over index order, padded with
  *                     -0.0 to a power of two ("Taming Bitwise Behavior in
  *                     GPU Kernels with Tensor Core", arXiv 2609.11356,

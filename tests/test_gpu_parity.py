@@ -312,7 +312,12 @@ def test_mma_chain_tmem_misaligned():
 
 
 TMEM_ROW_SHAPES = [(1, 8), (3, 64), (127, 512), (128, 512), (129, 520), (200, 4096), (256, 1000),
-                   (1000, 4096), (5, 100_000), (300, 8192), (4099, 640)]
+                   (1000, 4096), (5, 100_000), (300, 8192), (4099, 640),
+                   # shorter rows that run the mma.sync kernels, two and one
+                   # row groups to a stage, tails under 128 inputs, a last
+                   # chunk with no whole 128-input slice
+                   (333, 256), (3000, 768), (77, 904), (40, 1032), (33, 1152), (17, 2056),
+                   (70, 8256)]
 
 
 @pytest.mark.parametrize("dtype", [F16, BF16])
@@ -323,6 +328,18 @@ def test_mma_chain_tmem_rows_within_tolerance(dtype, shape, R):
     x = inputs(rows * cols, dtype, "uniform01", seed=rows + cols).reshape(rows, cols)
     s, a = oracle.exact_sum_rows(x, dtype)
     assert_within_mma_tolerance(gpu_rows(x, tcr.Mode(tcr.MMA_CHAIN_TMEM, R=R, dtype=dtype)), s, a)
+
+
+@pytest.mark.parametrize("cols", [768, 1000, 4096, 8256])
+def test_mma_chain_tmem_rows_batch_invariant(cols):
+    # a row's chains depend on cols only: the row alone gives the same bits
+    rows = 300
+    x = inputs(rows * cols, F16, "uniform_pm1", seed=cols).reshape(rows, cols)
+    t = dev(x)
+    whole = tcr.tcr_reduce_rows(t, tcr.Mode(tcr.MMA_CHAIN_TMEM)).cpu().numpy()
+    for r in (0, 17, 128, 299):
+        alone = tcr.tcr_reduce_rows(t[r:r + 1], tcr.Mode(tcr.MMA_CHAIN_TMEM)).cpu().numpy()
+        assert same_bits(alone, whole[r:r + 1])
 
 
 def test_mma_chain_tmem_rows_signed_and_stable():
