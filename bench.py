@@ -764,8 +764,10 @@ def main():
         avg_us = statistics.fmean(ms) * 1e3
         gbps = nbytes / avg_us / 1e3
         calls_out[name] = {"us": round(avg_us, 2), "gbps": round(gbps, 1),
+                           "gelem_per_s": round(call_elements(name) / avg_us / 1e3, 1),
                            "frac": round(gbps / peak, 4), "launches": launches}
     dom = max(calls_out, key=lambda k: calls_out[k]["us"])
+    elements_per_step = sum(call_elements(m[0]) for m in meta)
     launches = sum(m[2] for m in meta) * args.steps
 
     if rank != 0:
@@ -782,7 +784,12 @@ def main():
                    "mma_chain_R": tcr.tcr_order_descriptor(n=N_SUM, mode=tcr.Mode(tcr.MMA_CHAIN))["chain_R"]},
         "frac_of_peak": round(value / world / peak, 4),
         "peak_gbs": peak, "peak_source": peak_src,
+        "gelem_per_s": round(elements_per_step * args.steps * world / max_s / 1e9, 1),
         "calls": calls_out,
+        # page 1 reports about 3.2x for its tensor-core reduction over a
+        # conventional GPU reduction, on hardware the page does not name
+        "mma_chain_over_shuffle_tree": round(calls_out["sum/SHUFFLE_TREE"]["us"] /
+                                             calls_out["sum/MMA_CHAIN"]["us"], 3),
         "roofline": {"bound": "hbm", "kernel": KERNEL_OF[dom], "call": dom,
                      "achieved": calls_out[dom]["gbps"], "peak": peak, "unit": "GB/s",
                      "frac": calls_out[dom]["frac"], "traffic": recorded_traffic(KERNEL_OF[dom]),
@@ -798,8 +805,13 @@ def main():
     return 0
 
 
+def call_elements(name: str) -> int:
+    """Inputs one bench call reduces."""
+    return N_SUM if name.startswith("sum/") else ROWS * COLS
+
+
 def build_calls_meta():
-    """(name, algorithmic bytes, launches) of the six calls of a step."""
+    """(name, algorithmic bytes, launches) of the eight calls of a step."""
     import arithmetic_reduction_tensor_gb300 as tcr
     meta = []
     for kind in (tcr.MMA_CHAIN, tcr.FIXED_ORDER, tcr.SHUFFLE_TREE):
