@@ -36,6 +36,7 @@ __global__ void __launch_bounds__(32 * kBlockedMaxWarps, 4)
 blocked_chunk_kernel(const void *__restrict__ xv, size_t seg_len, size_t units, size_t cps,
                      int chunk_log2, int run_log2, float *__restrict__ dst)
 {
+    pdl_launch_dependents();   // the combine may launch now; it waits for this grid to finish
     using T = typename Elem<DT>::T;
     constexpr int V = Elem<DT>::kPerVec;
     constexpr int LV = V == 8 ? 3 : 2;
@@ -119,7 +120,6 @@ blocked_chunk_kernel(const void *__restrict__ xv, size_t seg_len, size_t units, 
         }
         __syncthreads();
     }
-    pdl_launch_dependents();
 }
 
 // ---------------------------------------------------------------- host

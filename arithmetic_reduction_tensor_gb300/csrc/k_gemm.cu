@@ -103,6 +103,7 @@ __global__ void __launch_bounds__(kGmThreads, 1)
 gemm_splitk_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant__ CUtensorMap tmw,
                    const GemmArgs g)
 {
+    pdl_launch_dependents();   // the combine may launch now; it waits for this grid to finish
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const uint32_t sbase = smem_addr(smem);
@@ -312,7 +313,6 @@ gemm_splitk_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constan
         }
     }
 
-    pdl_launch_dependents();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();

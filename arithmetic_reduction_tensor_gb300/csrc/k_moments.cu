@@ -56,6 +56,7 @@ __global__ void __launch_bounds__(1024)
 shuffle_block_pair_kernel(const void *__restrict__ xv, size_t seg_len, int G,
                           float *__restrict__ dst_a, float *__restrict__ dst_b)
 {
+    pdl_launch_dependents();   // the combine may launch now; it waits for this grid to finish
     using T = typename Elem<DT>::T;
     constexpr int V = Elem<DT>::kPerVec;
     constexpr int U = 4;
@@ -94,7 +95,6 @@ shuffle_block_pair_kernel(const void *__restrict__ xv, size_t seg_len, int G,
             acc_b = __fadd_rn(acc_b, tb[u]);
         }
     }
-    pdl_launch_dependents();
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) {
         acc_a = __fadd_rn(acc_a, __shfl_xor_sync(kFull, acc_a, off));

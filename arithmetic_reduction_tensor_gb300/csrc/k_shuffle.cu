@@ -162,6 +162,7 @@ template <int DT, int OP, bool ALIGNED>
 __global__ void __launch_bounds__(1024)
 shuffle_block_kernel(const void *__restrict__ xv, size_t seg_len, int G, float *__restrict__ dst)
 {
+    pdl_launch_dependents();   // the combine may launch now; it waits for this grid to finish
     using T = typename Elem<DT>::T;
     __shared__ float warp_val[32];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
@@ -182,7 +183,6 @@ shuffle_block_kernel(const void *__restrict__ xv, size_t seg_len, int G, float *
         default: acc = grid_stride_acc_unaligned<DT, OP, 3>(seg, seg_len, first, stride, hs); break;
         }
     }
-    pdl_launch_dependents();
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(kFull, acc, off));
     if (lane == 0) warp_val[warp] = acc;

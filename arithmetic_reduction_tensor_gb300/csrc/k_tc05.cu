@@ -133,6 +133,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 mma_tmem_kernel(const uint16_t *__restrict__ x, size_t n, size_t units, int unit_log2,
                 float *__restrict__ dst, uint32_t inject_stall)
 {
+    pdl_launch_dependents();   // the combine may launch now; it waits for this grid to finish
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const uint32_t sbase = smem_addr(smem);
@@ -383,7 +384,6 @@ mma_tmem_kernel(const uint16_t *__restrict__ x, size_t n, size_t units, int unit
         }
     }
 
-    pdl_launch_dependents();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -434,6 +434,7 @@ mma_tmem_rows_kernel(const __grid_constant__ CUtensorMap tmap, int use_map, cons
                      size_t rows, size_t cols, size_t chunk_cols, size_t cpr, size_t units, int stage_cols,
                      float *__restrict__ dst, uint32_t inject_stall)
 {
+    pdl_launch_dependents();   // the combine may launch now; it waits for this grid to finish
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const uint32_t sbase = smem_addr(smem);
@@ -697,7 +698,6 @@ mma_tmem_rows_kernel(const __grid_constant__ CUtensorMap tmap, int use_map, cons
         }
     }
 
-    pdl_launch_dependents();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();

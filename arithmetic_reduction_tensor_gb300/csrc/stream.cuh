@@ -558,6 +558,7 @@ __device__ __forceinline__ void chunk_body(const void *__restrict__ xv, size_t s
                                            size_t units, size_t cps, int chunk_log2,
                                            float *__restrict__ dst)
 {
+    pdl_launch_dependents();   // the combine may launch now; it waits for this grid to finish
     constexpr int DT = Red::kDT;
     constexpr bool NZ = Red::kNegZeroPad;
     using T = typename Elem<DT>::T;
@@ -614,7 +615,6 @@ __device__ __forceinline__ void chunk_body(const void *__restrict__ xv, size_t s
             base = nbase;
         }
     }
-    pdl_launch_dependents();
 }
 
 // One warp per row (rows of at most 2^LEVELS groups): out[r] is the row's
@@ -666,6 +666,7 @@ __device__ __forceinline__ void chunk_pair_body(const void *__restrict__ xv, siz
                                                 float *__restrict__ dst_a,
                                                 float *__restrict__ dst_b)
 {
+    pdl_launch_dependents();   // the combine may launch now; it waits for this grid to finish
     constexpr int DT = Red::kDT;
     constexpr bool NZ = Red::kNegZeroPad;
     using T = typename Elem<DT>::T;
@@ -706,7 +707,6 @@ __device__ __forceinline__ void chunk_pair_body(const void *__restrict__ xv, siz
         }
         __syncthreads();
     }
-    pdl_launch_dependents();
 }
 
 // rows_body for a PairReducer: out_a[r], out_b[r] are the row's two values,
