@@ -3,10 +3,12 @@ benchmark times (default block size and chain length unless the workload
 names others).
 
   sum of 2^20 binary16 values, U[-1,1], seed 0     MMA_CHAIN(R=4), FIXED_ORDER
-  sum of 2^28 binary16 values, U[0,1), seed 1      MMA_CHAIN R x block sweep, SHUFFLE_TREE
-  65536 x 4096 binary16 rows, N(0,1), seed 2       all three modes
-  sum of 2^29 bfloat16 values +-2^e, seed 3        MMA_CHAIN against the exact sum
+  sum of 2^28 binary16 values, U[0,1), seed 1      MMA_CHAIN R x block sweep, SHUFFLE_TREE,
+                                                   MMA_CHAIN_TMEM by R
+  65536 x 4096 binary16 rows, N(0,1), seed 2       all three modes and MMA_CHAIN_TMEM
+  sum of 2^29 bfloat16 values +-2^e, seed 3        MMA_CHAIN (both kinds) against the exact sum
   sum of 2^30 binary16 values, U[-1,1], seed 4     FIXED_ORDER, 10 runs, bit-exact; MMA_CHAIN
+                                                   (both kinds), SHUFFLE_TREE
 """
 import numpy as np
 import pytest
@@ -55,6 +57,8 @@ def test_sum_2p28_f16_sweep_and_shuffle():
         for block in (32, 128, 256, 1024):
             got = run_sum(t, tcr.Mode(tcr.MMA_CHAIN, R=R, block_threads=block))
             assert_within_mma_tolerance(got, exact, abs_sum)
+    for R in (1, 2, 3, 4, 5, 8):
+        assert_within_mma_tolerance(run_sum(t, tcr.Mode(tcr.MMA_CHAIN_TMEM, R=R)), exact, abs_sum)
     bt, g = spec.shuffle_team(x.size)
     assert same_bits(run_sum(t, tcr.Mode(tcr.SHUFFLE_TREE)), oracle.shuffle_tree(x, F16, bt, g))
     assert same_bits(run_sum(t, tcr.Mode(tcr.FIXED_ORDER)), oracle.fixed_order(x, F16))
@@ -72,6 +76,10 @@ def test_rows_65536x4096_f16():
     for R in (0, 1, 4):
         got = tcr.tcr_reduce_rows(t, tcr.Mode(tcr.MMA_CHAIN, R=R)).cpu().numpy()
         assert_within_mma_tolerance(got, s, a)
+    # the tcgen05 kernel as the bench times it (R = 4), and chains that end with their stage
+    for R in (0, 3, 5, 8):
+        got = tcr.tcr_reduce_rows(t, tcr.Mode(tcr.MMA_CHAIN_TMEM, R=R)).cpu().numpy()
+        assert_within_mma_tolerance(got, s, a)
 
 
 def test_sum_2p29_bf16_cancellation():
@@ -80,6 +88,8 @@ def test_sum_2p29_bf16_cancellation():
     exact, abs_sum = oracle.exact_sum(x, BF16)
     for R in (0, 1, 4, 5, 8):
         assert_within_mma_tolerance(run_sum(t, tcr.Mode(tcr.MMA_CHAIN, R=R, dtype=BF16)), exact, abs_sum)
+    for R in (0, 3, 5):
+        assert_within_mma_tolerance(run_sum(t, tcr.Mode(tcr.MMA_CHAIN_TMEM, R=R, dtype=BF16)), exact, abs_sum)
     assert same_bits(run_sum(t, tcr.Mode(tcr.FIXED_ORDER, dtype=BF16)), oracle.fixed_order(x, BF16))
 
 
@@ -94,6 +104,7 @@ def test_sum_2p30_f16_fixed_order_ten_runs():
     assert same_bits(got, np.full(10, ref, np.float32))
     exact, abs_sum = oracle.exact_sum(x, F16)
     assert_within_mma_tolerance(run_sum(t, tcr.Mode(tcr.MMA_CHAIN)), exact, abs_sum)
+    assert_within_mma_tolerance(run_sum(t, tcr.Mode(tcr.MMA_CHAIN_TMEM)), exact, abs_sum)
     assert same_bits(run_sum(t, tcr.Mode(tcr.SHUFFLE_TREE)),
                      oracle.shuffle_tree(x, F16, *spec.shuffle_team(x.size)))
 
