@@ -1,16 +1,28 @@
 // k_packed.cu -- launcher of the packed short-row kernels (packed.cuh).
+#include <cstdint>
+
 #include "packed.cuh"
 
 namespace tcr {
 
-static const void *pick(int family, int dtype, int op, int R, int vlog, bool aligned, bool pair)
+static const void *pick(int family, int dtype, int op, int R, int vlog, int align, bool pair)
 {
     switch (family) {
-    case kPackedFixed: return packed_pick_fixed(dtype, op, vlog, aligned, pair);
-    case kPackedShuffle: return packed_pick_shuffle(dtype, op, vlog, aligned, pair);
-    case kPackedMma: return packed_pick_mma(dtype, op, vlog, R, aligned, pair);
+    case kPackedFixed: return packed_pick_fixed(dtype, op, vlog, align, pair);
+    case kPackedShuffle: return packed_pick_shuffle(dtype, op, vlog, align, pair);
+    case kPackedMma: return packed_pick_mma(dtype, op, vlog, R, align, pair);
     default: return nullptr;
     }
+}
+
+// Rows that are not 16-byte aligned but all start on an 8-byte boundary (x
+// 8-byte aligned, a row a whole number of 8-byte words) are read with 8-byte
+// loads instead of as realigned granules: the same vectors, the same bits.
+static int align_class(int dtype, bool aligned, const void *x, size_t cols)
+{
+    if (aligned) return 1;
+    const size_t eb = dtype == kF32 ? 4 : 2;
+    return ((uintptr_t)x & 7u) == 0 && (cols * eb) % 8 == 0 ? 2 : 0;
 }
 
 int packed_rows_vlog(int family, size_t cols, int vector_len)
@@ -26,7 +38,7 @@ bool packed_rows_supported(int family, int dtype, int op, size_t cols, int vecto
                            bool pair)
 {
     const int v = packed_rows_vlog(family, cols, vector_len);
-    return cols > 0 && v >= 0 && pick(family, dtype, op, 1, v, aligned, pair) != nullptr;
+    return cols > 0 && v >= 0 && pick(family, dtype, op, 1, v, aligned ? 1 : 0, pair) != nullptr;
 }
 
 size_t packed_rows_groups(size_t rows, int vlog)
@@ -39,7 +51,7 @@ cudaError_t launch_packed_rows(int family, int dtype, int op, int R, bool aligne
                                size_t rows, size_t cols, int vlog, float *out, int grid, int block,
                                cudaStream_t stream)
 {
-    const void *k = pick(family, dtype, op, R, vlog, aligned, false);
+    const void *k = pick(family, dtype, op, R, vlog, align_class(dtype, aligned, x, cols), false);
     if (!k || block != kRowsBlock) return cudaErrorInvalidValue;
     float *none = nullptr;
     int mv = 0;
@@ -51,7 +63,7 @@ cudaError_t launch_packed_rows_pair(int family, int dtype, int R, bool aligned, 
                                     size_t rows, size_t cols, int vlog, float *out_a, float *out_b,
                                     int mean_var, int grid, int block, cudaStream_t stream)
 {
-    const void *k = pick(family, dtype, kOpSum, R, vlog, aligned, true);
+    const void *k = pick(family, dtype, kOpSum, R, vlog, align_class(dtype, aligned, x, cols), true);
     if (!k || block != kRowsBlock) return cudaErrorInvalidValue;
     void *args[] = {(void *)&x, (void *)&rows, (void *)&cols, (void *)&out_a, (void *)&out_b,
                     (void *)&mean_var};
@@ -60,7 +72,7 @@ cudaError_t launch_packed_rows_pair(int family, int dtype, int R, bool aligned, 
 
 int occupancy_packed(int family, int dtype, int op, int R, int vlog, bool aligned, bool pair)
 {
-    const void *k = pick(family, dtype, op, R, vlog, aligned, pair);
+    const void *k = pick(family, dtype, op, R, vlog, aligned ? 1 : 0, pair);
     int n = 0;
     if (!k || cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, kRowsBlock, 0) != cudaSuccess) {
         (void)cudaGetLastError();

@@ -8,44 +8,53 @@
 
 namespace tcr {
 
-template <int DT, int OP, bool AL, bool P>
+template <int DT, int OP, int AL, bool P>
 static const void *pick(int vlog, int R)
 {
     switch (vlog) {
-    case 2: return (const void *)packed_rows_kernel<DT, OP, kPackedMma, 2, 1, AL, P>;
-    case 3: return (const void *)packed_rows_kernel<DT, OP, kPackedMma, 3, 1, AL, P>;
-    case 4: return (const void *)packed_rows_kernel<DT, OP, kPackedMma, 4, 1, AL, P>;
-    case 5: return (const void *)packed_rows_kernel<DT, OP, kPackedMma, 5, 1, AL, P>;
+    case 2: return (const void *)packed_rows_kernel<DT, OP, kPackedMma, 2, 1, AL != 0, P, AL == 2>;
+    case 3: return (const void *)packed_rows_kernel<DT, OP, kPackedMma, 3, 1, AL != 0, P, AL == 2>;
+    case 4: return (const void *)packed_rows_kernel<DT, OP, kPackedMma, 4, 1, AL != 0, P, AL == 2>;
+    case 5: return (const void *)packed_rows_kernel<DT, OP, kPackedMma, 5, 1, AL != 0, P, AL == 2>;
     case 6:
-        return R == 1 ? (const void *)packed_rows_kernel<DT, OP, kPackedMma, 6, 1, AL, P>
-                      : (const void *)packed_rows_kernel<DT, OP, kPackedMma, 6, 2, AL, P>;
+        return R == 1 ? (const void *)packed_rows_kernel<DT, OP, kPackedMma, 6, 1, AL != 0, P, AL == 2>
+                      : (const void *)packed_rows_kernel<DT, OP, kPackedMma, 6, 2, AL != 0, P, AL == 2>;
     case 7:
         switch (R) {
-        case 1: return (const void *)packed_rows_kernel<DT, OP, kPackedMma, 7, 1, AL, P>;
-        case 2: return (const void *)packed_rows_kernel<DT, OP, kPackedMma, 7, 2, AL, P>;
-        case 3: return (const void *)packed_rows_kernel<DT, OP, kPackedMma, 7, 3, AL, P>;
-        default: return (const void *)packed_rows_kernel<DT, OP, kPackedMma, 7, 4, AL, P>;
+        case 1: return (const void *)packed_rows_kernel<DT, OP, kPackedMma, 7, 1, AL != 0, P, AL == 2>;
+        case 2: return (const void *)packed_rows_kernel<DT, OP, kPackedMma, 7, 2, AL != 0, P, AL == 2>;
+        case 3: return (const void *)packed_rows_kernel<DT, OP, kPackedMma, 7, 3, AL != 0, P, AL == 2>;
+        default: return (const void *)packed_rows_kernel<DT, OP, kPackedMma, 7, 4, AL != 0, P, AL == 2>;
         }
     default: return nullptr;
     }
 }
 
-template <int DT>
-static const void *by_pair(int op, int vlog, int R, bool aligned, bool pair)
+template <int DT, int OP, bool P>
+static const void *by_align(int vlog, int R, int align)
 {
-    if (pair) return aligned ? pick<DT, kOpSum, true, true>(vlog, R) : pick<DT, kOpSum, false, true>(vlog, R);
-    if (op == kOpSquares)
-        return aligned ? pick<DT, kOpSquares, true, false>(vlog, R) : pick<DT, kOpSquares, false, false>(vlog, R);
-    return aligned ? pick<DT, kOpSum, true, false>(vlog, R) : pick<DT, kOpSum, false, false>(vlog, R);
+    switch (align) {
+    case 0: return pick<DT, OP, 0, P>(vlog, R);
+    case 1: return pick<DT, OP, 1, P>(vlog, R);
+    default: return pick<DT, OP, 2, P>(vlog, R);
+    }
 }
 
-const void *packed_pick_mma(int dtype, int op, int vlog, int R, bool aligned, bool pair)
+template <int DT>
+static const void *by_pair(int op, int vlog, int R, int align, bool pair)
 {
-    if (R < 1 || R > 8) return nullptr;
+    if (pair) return by_align<DT, kOpSum, true>(vlog, R, align);
+    if (op == kOpSquares) return by_align<DT, kOpSquares, false>(vlog, R, align);
+    return by_align<DT, kOpSum, false>(vlog, R, align);
+}
+
+const void *packed_pick_mma(int dtype, int op, int vlog, int R, int align, bool pair)
+{
+    if (R < 1 || R > 8 || align < 0 || align > 2) return nullptr;
     switch (dtype) {
-    case kF16: return by_pair<kF16>(op, vlog, R, aligned, pair);
-    case kBF16: return by_pair<kBF16>(op, vlog, R, aligned, pair);
-    case kF32: return by_pair<kF32>(op, vlog, R, aligned, pair);
+    case kF16: return by_pair<kF16>(op, vlog, R, align, pair);
+    case kBF16: return by_pair<kBF16>(op, vlog, R, align, pair);
+    case kF32: return by_pair<kF32>(op, vlog, R, align, pair);
     default: return nullptr;
     }
 }

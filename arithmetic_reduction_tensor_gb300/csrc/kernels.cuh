@@ -60,8 +60,10 @@ cudaError_t launch_mma_rows(int dtype, int op, bool aligned, int R, const void *
 // (FIXED_ORDER), kPackedShuffle (SHUFFLE_TREE, one-warp team) or kPackedMma
 // (MMA_CHAIN, 16-bit sums).  A row takes 2^vlog vector slots
 // (packed_rows_vlog: -1 when the row is too long to pack); `aligned` as for
-// the launch (x 16-byte aligned and rows whole vectors); CTAs of kRowsBlock
-// threads, one warp per group of 256 >> vlog rows.
+// the launch (x 16-byte aligned and rows whole vectors; other rows that all
+// start on an 8-byte boundary are read with 8-byte loads, the rest as
+// realigned 16-byte granules); CTAs of kRowsBlock threads, one warp per
+// group of 256 >> vlog rows.
 constexpr int kPackedFixed = 0, kPackedShuffle = 1, kPackedMma = 2;
 // pair: the kernel of tcr_reduce_rows_moments / _mean_var (out_a, out_b
 // as for launch_rows_pair; op ignored).

@@ -120,8 +120,33 @@ __device__ __forceinline__ PackedGeom packed_geom(const typename Elem<DT>::T *x,
     return g;
 }
 
-// Load k (0..7) of the group whose first row is row0.
-template <int DT, bool ALIGNED, bool NEGZERO, int VLOG>
+// Vector v (v * V < len) of a row that starts on an 8-byte boundary and is
+// a whole number of 8-byte words long: two 8-byte streaming loads, or for
+// the row's last vector when it holds only one word, that word and the
+// fill -- the same patterns a 16-byte load of an aligned row gives, with no
+// realignment.  (Measured against loads kept in L1 and against a branch
+// around the second load: both slower on most widths.)
+template <int DT, bool NEGZERO>
+__device__ __forceinline__ uint4 ld_vec_half(const typename Elem<DT>::T *seg, size_t len, size_t v)
+{
+    constexpr int V = Elem<DT>::kPerVec;
+    const uint2 *p = reinterpret_cast<const uint2 *>(seg + V * v);
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+    // the second word as a predicated load (no branch, so the loads of a
+    // group still issue together); it keeps the fill when not taken
+    r.z = r.w = fill_word<DT, NEGZERO>();
+    const uint32_t whole = V * v + V <= len ? 1u : 0u;
+    asm("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %3, 0;\n\t@q ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];\n\t}"
+        : "+r"(r.z), "+r"(r.w)
+        : "l"(p + 1), "r"(whole));
+    return r;
+}
+
+// Load k (0..7) of the group whose first row is row0.  HALF (with ALIGNED):
+// every row starts on an 8-byte boundary and is a whole number of 8-byte
+// words long; x may not be 16-byte aligned.
+template <int DT, bool ALIGNED, bool NEGZERO, int VLOG, bool HALF = false>
 __device__ __forceinline__ uint4 load_slot(const typename Elem<DT>::T *x, size_t rows, size_t cols,
                                            size_t row0, const PackedGeom &gm, int k, int lane)
 {
@@ -134,7 +159,8 @@ __device__ __forceinline__ uint4 load_slot(const typename Elem<DT>::T *x, size_t
     const uint32_t c = (uint32_t)cols;                   // at most 128 vectors
     if constexpr (ALIGNED) {
         if (!(row0 + rr < rows && V * v < c)) return make_uint4(f, f, f, f);
-        return ld_vec<DT, true, NEGZERO>(x + (row0 + rr) * cols, cols, v);
+        if constexpr (HALF) return ld_vec_half<DT, NEGZERO>(x + (row0 + rr) * cols, cols, v);
+        else return ld_vec<DT, true, NEGZERO>(x + (row0 + rr) * cols, cols, v);
     } else {
         // slots up to the one after the row's last vector, and the first
         // slot of the row past the matrix
@@ -160,12 +186,13 @@ __device__ __forceinline__ uint4 load_tail(size_t rows, size_t cols, size_t row0
     return r;
 }
 
-template <int DT, bool ALIGNED, bool NEGZERO, int VLOG>
+template <int DT, bool ALIGNED, bool NEGZERO, int VLOG, bool HALF = false>
 __device__ __forceinline__ void load_packed(uint4 (&q)[8], const typename Elem<DT>::T *x, size_t rows,
                                             size_t cols, size_t row0, const PackedGeom &gm, int lane)
 {
 #pragma unroll
-    for (int k = 0; k < 8; k++) q[k] = load_slot<DT, ALIGNED, NEGZERO, VLOG>(x, rows, cols, row0, gm, k, lane);
+    for (int k = 0; k < 8; k++)
+        q[k] = load_slot<DT, ALIGNED, NEGZERO, VLOG, HALF>(x, rows, cols, row0, gm, k, lane);
 }
 
 // The vector of slot (k, lane) of an unaligned group from the granules in
@@ -384,7 +411,7 @@ __host__ __device__ constexpr int packed_min_ctas()
     return MODE == kPackedMma && (PAIR || OP == kOpSquares || DT == kF32) ? 2 : kRowsMinCtas;
 }
 
-template <int DT, int OP, int MODE, int VLOG, int R, bool ALIGNED, bool PAIR>
+template <int DT, int OP, int MODE, int VLOG, int R, bool ALIGNED, bool PAIR, bool HALF = false>
 __global__ void __launch_bounds__(kRowsBlock, packed_min_ctas<DT, MODE, OP, PAIR>())
 packed_rows_kernel(const void *__restrict__ xv, size_t rows, size_t cols, float *__restrict__ out_a,
                    float *__restrict__ out_b, int mean_var)
@@ -406,7 +433,7 @@ packed_rows_kernel(const void *__restrict__ xv, size_t rows, size_t cols, float 
         gm = packed_geom<DT>(x, rows, cols, gi * RPG);
         qt = load_tail<DT, VLOG>(rows, cols, gi * RPG, gm, lane);
     }
-    load_packed<DT, ALIGNED, NZ, VLOG>(q, x, rows, cols, gi * RPG, gm, lane);
+    load_packed<DT, ALIGNED, NZ, VLOG, HALF>(q, x, rows, cols, gi * RPG, gm, lane);
     for (;;) {
         const size_t row0 = gi * RPG;
         const size_t ngi = gi + nw;
@@ -426,7 +453,7 @@ packed_rows_kernel(const void *__restrict__ xv, size_t rows, size_t cols, float 
         // from the granules, so the next load may replace them before the
         // vector is reduced; an aligned one is the loaded register itself.
         auto next = [&](int k) {
-            if (has_next) q[k] = load_slot<DT, ALIGNED, NZ, VLOG>(x, rows, cols, nrow0, gm, k, lane);
+            if (has_next) q[k] = load_slot<DT, ALIGNED, NZ, VLOG, HALF>(x, rows, cols, nrow0, gm, k, lane);
             if constexpr (!ALIGNED)
                 if (k == 7 && has_next) qt = load_tail<DT, VLOG>(rows, cols, nrow0, gm, lane);
         };
@@ -561,8 +588,10 @@ packed_rows_kernel(const void *__restrict__ xv, size_t rows, size_t cols, float 
 // Kernel pointers of each mode (k_packed_*.cu); nullptr where the mode has
 // no packed kernel for the arguments.
 // pair: the sum-and-squares kernel (op ignored).
-const void *packed_pick_fixed(int dtype, int op, int vlog, bool aligned, bool pair);
-const void *packed_pick_shuffle(int dtype, int op, int vlog, bool aligned, bool pair);
-const void *packed_pick_mma(int dtype, int op, int vlog, int R, bool aligned, bool pair);
+// align: 0 rows read as whole granules and realigned, 1 16-byte aligned
+// rows, 2 rows that all start on an 8-byte boundary (loads of 8 bytes)
+const void *packed_pick_fixed(int dtype, int op, int vlog, int align, bool pair);
+const void *packed_pick_shuffle(int dtype, int op, int vlog, int align, bool pair);
+const void *packed_pick_mma(int dtype, int op, int vlog, int R, int align, bool pair);
 
 }  // namespace tcr

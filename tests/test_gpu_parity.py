@@ -317,7 +317,10 @@ TMEM_ROW_SHAPES = [(1, 8), (3, 64), (127, 512), (128, 512), (129, 520), (200, 40
                    # row groups to a stage, tails under 128 inputs, a last
                    # chunk with no whole 128-input slice
                    (333, 256), (3000, 768), (77, 904), (40, 1032), (33, 1152), (17, 2056),
-                   (70, 8256)]
+                   (70, 8256),
+                   # several 8192-column chunks through the tensor-map path (whole
+                   # 128-column blocks) and through per-row copies
+                   (40, 20480), (9, 16512), (11, 24584)]
 
 
 @pytest.mark.parametrize("dtype", [F16, BF16])

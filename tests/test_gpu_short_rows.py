@@ -48,11 +48,13 @@ def within_mma_tolerance(got, exact, abs_sum):
     return bool(np.all(err <= spec.mma_tolerance(np.asarray(abs_sum))))
 
 
-# row widths around every packing width (2^v vectors, v = 0..7) and past the last
-COLS16 = [1, 5, 8, 9, 16, 17, 31, 32, 33, 63, 64, 65, 100, 127, 128, 129, 255, 256, 257,
-          383, 511, 512, 513, 777, 1000, 1023, 1024, 1025]
-COLS32 = [1, 3, 4, 5, 8, 13, 16, 31, 32, 33, 64, 100, 128, 129, 255, 256, 257, 400, 511,
-          512, 513]
+# row widths around every packing width (2^v vectors, v = 0..7) and past the last;
+# widths of an odd number of 8-byte words (12, 36, ... for 16-bit inputs, 6, 50, ...
+# for binary32) make every other row start 8 bytes into a granule: 8-byte loads
+COLS16 = [1, 5, 8, 9, 12, 16, 17, 31, 32, 33, 36, 63, 64, 65, 100, 127, 128, 129, 132, 255, 256,
+          257, 383, 511, 512, 513, 516, 777, 1000, 1020, 1023, 1024, 1025]
+COLS32 = [1, 3, 4, 5, 6, 8, 13, 16, 31, 32, 33, 50, 64, 100, 102, 128, 129, 255, 256, 257, 258,
+          400, 510, 511, 512, 513]
 
 
 def rows_for(cols, dtype):
@@ -98,13 +100,14 @@ def test_mma_chain_within_tolerance(dtype, R):
 
 
 @pytest.mark.parametrize("dtype", [F16, F32])
-@pytest.mark.parametrize("offset", [1, 3, 4, 7])
+@pytest.mark.parametrize("offset", [1, 2, 3, 4, 7])
 def test_misaligned_base_and_rows(dtype, offset):
     # a base `offset` inputs past a 16-byte boundary: rows start at every
     # offset in their granule; widths around each packing width, whole
-    # vectors or not (a row gets one slot more than vectors)
-    for cols in ((7, 8, 15, 31, 63, 64, 100, 127, 249, 255, 256, 333, 1001, 1017) if dtype == F16
-                 else (3, 4, 7, 31, 32, 100, 127, 255, 256, 509)):
+    # vectors or not (a row gets one slot more than vectors); a base 8 bytes
+    # past the boundary with rows of whole 8-byte words takes 8-byte loads
+    for cols in ((7, 8, 12, 15, 31, 36, 63, 64, 100, 127, 249, 255, 256, 333, 516, 1001, 1017)
+                 if dtype == F16 else (3, 4, 6, 7, 31, 32, 50, 100, 127, 255, 256, 258, 509)):
         rows = 777
         x = synth.generate(rows * cols + offset, "normal", dtype, seed=cols + offset)
         t = dev(x)[offset:].view(rows, cols)
@@ -215,9 +218,9 @@ def test_moments_of_short_rows(dtype):
             assert within_mma_tolerance(s1, e1, a1) and within_mma_tolerance(s2, e2, e2), (cols, R)
 
 
-@pytest.mark.parametrize("offset", [1, 5])
+@pytest.mark.parametrize("offset", [1, 4, 5])
 def test_moments_of_misaligned_short_rows(offset):
-    for cols in (7, 31, 64, 100, 255, 777):
+    for cols in (7, 31, 36, 64, 100, 255, 516, 777):
         rows = 513
         x = synth.generate(rows * cols + offset, "normal", BF16, seed=cols + offset)
         t = dev(x)[offset:].view(rows, cols)
