@@ -124,13 +124,23 @@ __device__ __forceinline__ PackedGeom packed_geom(const typename Elem<DT>::T *x,
 // a whole number of 8-byte words long: two 8-byte streaming loads, or for
 // the row's last vector when it holds only one word, that word and the
 // fill -- the same patterns a 16-byte load of an aligned row gives, with no
-// realignment.  (Measured against loads kept in L1 and against a branch
-// around the second load: both slower on most widths.)
-template <int DT, bool NEGZERO>
+// realignment.  BRANCH (the trees on rows of 33 to 128 vectors): both words
+// through L1 when the vector is whole, else the element-wise masked load --
+// measured faster there, slower on every other kind of row.
+template <int DT, bool NEGZERO, bool BRANCH = false>
 __device__ __forceinline__ uint4 ld_vec_half(const typename Elem<DT>::T *seg, size_t len, size_t v)
 {
     constexpr int V = Elem<DT>::kPerVec;
     const uint2 *p = reinterpret_cast<const uint2 *>(seg + V * v);
+    if constexpr (BRANCH) {
+        if (V * v + V <= len) {
+            uint4 w;
+            asm("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(w.x), "=r"(w.y) : "l"(p));
+            asm("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(w.z), "=r"(w.w) : "l"(p + 1));
+            return w;
+        }
+        return ld_vec_masked<DT, NEGZERO>(seg, len, v);
+    }
     uint4 r;
     asm("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
     // the second word as a predicated load (no branch, so the loads of a
@@ -146,7 +156,7 @@ __device__ __forceinline__ uint4 ld_vec_half(const typename Elem<DT>::T *seg, si
 // Load k (0..7) of the group whose first row is row0.  HALF (with ALIGNED):
 // every row starts on an 8-byte boundary and is a whole number of 8-byte
 // words long; x may not be 16-byte aligned.
-template <int DT, bool ALIGNED, bool NEGZERO, int VLOG, bool HALF = false>
+template <int DT, bool ALIGNED, bool NEGZERO, int VLOG, bool HALF = false, bool BR = false>
 __device__ __forceinline__ uint4 load_slot(const typename Elem<DT>::T *x, size_t rows, size_t cols,
                                            size_t row0, const PackedGeom &gm, int k, int lane)
 {
@@ -159,7 +169,7 @@ __device__ __forceinline__ uint4 load_slot(const typename Elem<DT>::T *x, size_t
     const uint32_t c = (uint32_t)cols;                   // at most 128 vectors
     if constexpr (ALIGNED) {
         if (!(row0 + rr < rows && V * v < c)) return make_uint4(f, f, f, f);
-        if constexpr (HALF) return ld_vec_half<DT, NEGZERO>(x + (row0 + rr) * cols, cols, v);
+        if constexpr (HALF) return ld_vec_half<DT, NEGZERO, BR>(x + (row0 + rr) * cols, cols, v);
         else return ld_vec<DT, true, NEGZERO>(x + (row0 + rr) * cols, cols, v);
     } else {
         // slots up to the one after the row's last vector, and the first
@@ -186,13 +196,13 @@ __device__ __forceinline__ uint4 load_tail(size_t rows, size_t cols, size_t row0
     return r;
 }
 
-template <int DT, bool ALIGNED, bool NEGZERO, int VLOG, bool HALF = false>
+template <int DT, bool ALIGNED, bool NEGZERO, int VLOG, bool HALF = false, bool BR = false>
 __device__ __forceinline__ void load_packed(uint4 (&q)[8], const typename Elem<DT>::T *x, size_t rows,
                                             size_t cols, size_t row0, const PackedGeom &gm, int lane)
 {
 #pragma unroll
     for (int k = 0; k < 8; k++)
-        q[k] = load_slot<DT, ALIGNED, NEGZERO, VLOG, HALF>(x, rows, cols, row0, gm, k, lane);
+        q[k] = load_slot<DT, ALIGNED, NEGZERO, VLOG, HALF, BR>(x, rows, cols, row0, gm, k, lane);
 }
 
 // The vector of slot (k, lane) of an unaligned group from the granules in
@@ -433,7 +443,8 @@ packed_rows_kernel(const void *__restrict__ xv, size_t rows, size_t cols, float 
         gm = packed_geom<DT>(x, rows, cols, gi * RPG);
         qt = load_tail<DT, VLOG>(rows, cols, gi * RPG, gm, lane);
     }
-    load_packed<DT, ALIGNED, NZ, VLOG, HALF>(q, x, rows, cols, gi * RPG, gm, lane);
+    constexpr bool BR = MODE != kPackedMma && VLOG >= 6;     // the form of ld_vec_half
+    load_packed<DT, ALIGNED, NZ, VLOG, HALF, BR>(q, x, rows, cols, gi * RPG, gm, lane);
     for (;;) {
         const size_t row0 = gi * RPG;
         const size_t ngi = gi + nw;
@@ -453,7 +464,7 @@ packed_rows_kernel(const void *__restrict__ xv, size_t rows, size_t cols, float 
         // from the granules, so the next load may replace them before the
         // vector is reduced; an aligned one is the loaded register itself.
         auto next = [&](int k) {
-            if (has_next) q[k] = load_slot<DT, ALIGNED, NZ, VLOG, HALF>(x, rows, cols, nrow0, gm, k, lane);
+            if (has_next) q[k] = load_slot<DT, ALIGNED, NZ, VLOG, HALF, BR>(x, rows, cols, nrow0, gm, k, lane);
             if constexpr (!ALIGNED)
                 if (k == 7 && has_next) qt = load_tail<DT, VLOG>(rows, cols, nrow0, gm, lane);
         };
