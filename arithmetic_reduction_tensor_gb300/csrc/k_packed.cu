@@ -15,14 +15,15 @@ static const void *pick(int family, int dtype, int op, int R, int vlog, int alig
     }
 }
 
-// Rows that are not 16-byte aligned but all start on an 8-byte boundary (x
-// 8-byte aligned, a row a whole number of 8-byte words) are read with 8-byte
-// loads instead of as realigned granules: the same vectors, the same bits.
+// Rows that are not 16-byte aligned but all start on a 4-byte boundary (x
+// 4-byte aligned, a row a whole number of 4-byte words) are read with 8-byte
+// loads (8-byte boundaries and words) or 4-byte loads instead of as
+// realigned granules: the same vectors, the same bits.
 static int align_class(int dtype, bool aligned, const void *x, size_t cols)
 {
     if (aligned) return 1;
     const size_t eb = dtype == kF32 ? 4 : 2;
-    return ((uintptr_t)x & 7u) == 0 && (cols * eb) % 8 == 0 ? 2 : 0;
+    return ((uintptr_t)x & 3u) == 0 && (cols * eb) % 4 == 0 ? 2 : 0;
 }
 
 int packed_rows_vlog(int family, size_t cols, int vector_len)

@@ -126,11 +126,30 @@ __device__ __forceinline__ PackedGeom packed_geom(const typename Elem<DT>::T *x,
 // fill -- the same patterns a 16-byte load of an aligned row gives, with no
 // realignment.  BRANCH (the trees on rows of 33 to 128 vectors): both words
 // through L1 when the vector is whole, else the element-wise masked load --
-// measured faster there, slower on every other kind of row.
+// measured faster there, slower on every other kind of row.  `words`: the
+// rows start on 4-byte boundaries only (and are whole 4-byte words): four
+// 4-byte loads through L1 (the four of a warp share their lines), the words
+// past the row the fill.
 template <int DT, bool NEGZERO, bool BRANCH = false>
-__device__ __forceinline__ uint4 ld_vec_half(const typename Elem<DT>::T *seg, size_t len, size_t v)
+__device__ __forceinline__ uint4 ld_vec_half(const typename Elem<DT>::T *seg, size_t len, size_t v,
+                                             bool words)
 {
     constexpr int V = Elem<DT>::kPerVec;
+    constexpr uint32_t EB = sizeof(typename Elem<DT>::T);
+    if (words) {
+        const uint32_t *p4 = reinterpret_cast<const uint32_t *>(seg + V * v);
+        const size_t left = len - V * v;
+        const uint32_t nb = left >= (size_t)V ? 16u : (uint32_t)left * EB;     // bytes of the row here
+        const uint32_t f = fill_word<DT, NEGZERO>();
+        uint4 r = make_uint4(0u, f, f, f);
+        asm("ld.global.nc.u32 %0, [%1];" : "=r"(r.x) : "l"(p4));
+        asm("{\n\t.reg .pred q;\n\tsetp.gt.u32 q, %3, 4;\n\t@q ld.global.nc.u32 %0, [%4];\n\t"
+            "setp.gt.u32 q, %3, 8;\n\t@q ld.global.nc.u32 %1, [%5];\n\t"
+            "setp.gt.u32 q, %3, 12;\n\t@q ld.global.nc.u32 %2, [%6];\n\t}"
+            : "+r"(r.y), "+r"(r.z), "+r"(r.w)
+            : "r"(nb), "l"(p4 + 1), "l"(p4 + 2), "l"(p4 + 3));
+        return r;
+    }
     const uint2 *p = reinterpret_cast<const uint2 *>(seg + V * v);
     if constexpr (BRANCH) {
         if (V * v + V <= len) {
@@ -154,11 +173,13 @@ __device__ __forceinline__ uint4 ld_vec_half(const typename Elem<DT>::T *seg, si
 }
 
 // Load k (0..7) of the group whose first row is row0.  HALF (with ALIGNED):
-// every row starts on an 8-byte boundary and is a whole number of 8-byte
-// words long; x may not be 16-byte aligned.
+// every row starts on a 4-byte boundary and is a whole number of 4-byte
+// words long (on 8-byte boundaries and of 8-byte words unless `words`); x
+// may not be 16-byte aligned.
 template <int DT, bool ALIGNED, bool NEGZERO, int VLOG, bool HALF = false, bool BR = false>
 __device__ __forceinline__ uint4 load_slot(const typename Elem<DT>::T *x, size_t rows, size_t cols,
-                                           size_t row0, const PackedGeom &gm, int k, int lane)
+                                           size_t row0, const PackedGeom &gm, int k, int lane,
+                                           bool words = false)
 {
     constexpr int V = Elem<DT>::kPerVec;
     constexpr uint32_t EB = sizeof(typename Elem<DT>::T);
@@ -169,7 +190,7 @@ __device__ __forceinline__ uint4 load_slot(const typename Elem<DT>::T *x, size_t
     const uint32_t c = (uint32_t)cols;                   // at most 128 vectors
     if constexpr (ALIGNED) {
         if (!(row0 + rr < rows && V * v < c)) return make_uint4(f, f, f, f);
-        if constexpr (HALF) return ld_vec_half<DT, NEGZERO, BR>(x + (row0 + rr) * cols, cols, v);
+        if constexpr (HALF) return ld_vec_half<DT, NEGZERO, BR>(x + (row0 + rr) * cols, cols, v, words);
         else return ld_vec<DT, true, NEGZERO>(x + (row0 + rr) * cols, cols, v);
     } else {
         // slots up to the one after the row's last vector, and the first
@@ -198,11 +219,12 @@ __device__ __forceinline__ uint4 load_tail(size_t rows, size_t cols, size_t row0
 
 template <int DT, bool ALIGNED, bool NEGZERO, int VLOG, bool HALF = false, bool BR = false>
 __device__ __forceinline__ void load_packed(uint4 (&q)[8], const typename Elem<DT>::T *x, size_t rows,
-                                            size_t cols, size_t row0, const PackedGeom &gm, int lane)
+                                            size_t cols, size_t row0, const PackedGeom &gm, int lane,
+                                            bool words = false)
 {
 #pragma unroll
     for (int k = 0; k < 8; k++)
-        q[k] = load_slot<DT, ALIGNED, NEGZERO, VLOG, HALF, BR>(x, rows, cols, row0, gm, k, lane);
+        q[k] = load_slot<DT, ALIGNED, NEGZERO, VLOG, HALF, BR>(x, rows, cols, row0, gm, k, lane, words);
 }
 
 // The vector of slot (k, lane) of an unaligned group from the granules in
@@ -444,7 +466,9 @@ packed_rows_kernel(const void *__restrict__ xv, size_t rows, size_t cols, float 
         qt = load_tail<DT, VLOG>(rows, cols, gi * RPG, gm, lane);
     }
     constexpr bool BR = MODE != kPackedMma && VLOG >= 6;     // the form of ld_vec_half
-    load_packed<DT, ALIGNED, NZ, VLOG, HALF, BR>(q, x, rows, cols, gi * RPG, gm, lane);
+    // rows on 4-byte but not 8-byte boundaries, or not whole 8-byte words
+    const bool words = HALF && ((((uintptr_t)xv) & 7u) != 0 || ((cols * sizeof(T)) & 7u) != 0);
+    load_packed<DT, ALIGNED, NZ, VLOG, HALF, BR>(q, x, rows, cols, gi * RPG, gm, lane, words);
     for (;;) {
         const size_t row0 = gi * RPG;
         const size_t ngi = gi + nw;
@@ -464,7 +488,8 @@ packed_rows_kernel(const void *__restrict__ xv, size_t rows, size_t cols, float 
         // from the granules, so the next load may replace them before the
         // vector is reduced; an aligned one is the loaded register itself.
         auto next = [&](int k) {
-            if (has_next) q[k] = load_slot<DT, ALIGNED, NZ, VLOG, HALF, BR>(x, rows, cols, nrow0, gm, k, lane);
+            if (has_next)
+                q[k] = load_slot<DT, ALIGNED, NZ, VLOG, HALF, BR>(x, rows, cols, nrow0, gm, k, lane, words);
             if constexpr (!ALIGNED)
                 if (k == 7 && has_next) qt = load_tail<DT, VLOG>(rows, cols, nrow0, gm, lane);
         };

@@ -50,9 +50,12 @@ def within_mma_tolerance(got, exact, abs_sum):
 
 # row widths around every packing width (2^v vectors, v = 0..7) and past the last;
 # widths of an odd number of 8-byte words (12, 36, ... for 16-bit inputs, 6, 50, ...
-# for binary32) make every other row start 8 bytes into a granule: 8-byte loads
-COLS16 = [1, 5, 8, 9, 12, 16, 17, 31, 32, 33, 36, 63, 64, 65, 100, 127, 128, 129, 132, 255, 256,
-          257, 383, 511, 512, 513, 516, 777, 1000, 1020, 1023, 1024, 1025]
+# for binary32) make every other row start 8 bytes into a granule: 8-byte loads;
+# an odd number of 4-byte words (10, 50, ... 16-bit, every odd binary32 width):
+# 4-byte loads
+COLS16 = [1, 5, 8, 9, 10, 12, 16, 17, 31, 32, 33, 36, 50, 63, 64, 65, 100, 127, 128, 129, 130,
+          132, 255, 256, 257, 383, 511, 512, 513, 514, 516, 777, 1000, 1020, 1022, 1023, 1024,
+          1025]
 COLS32 = [1, 3, 4, 5, 6, 8, 13, 16, 31, 32, 33, 50, 64, 100, 102, 128, 129, 255, 256, 257, 258,
           400, 510, 511, 512, 513]
 
