@@ -177,11 +177,12 @@ TCR_API tcr_status tcr_reduce_sum(const void *x, size_t n, float *out, tcr_mode 
  * launch; long rows use per-row partials and a combine launch.  Rows of at
  * most 128 16-byte vectors (1024 16-bit or 512 binary32 inputs) are packed
  * several to a warp; when x or the row stride is not 16-byte aligned but
- * every row starts on an 8-byte boundary those kernels read 8-byte words of
- * the rows only; otherwise they read whole 16-byte aligned granules that
- * hold inputs of the matrix -- up to 15 bytes before x or after its last
- * input, never outside the granules the data touches (an allocation from
- * cudaMalloc is 256-byte aligned, so such a granule lies inside it).
+ * every row starts on a 4-byte boundary and is a whole number of 4-byte
+ * words, those kernels read 8- or 4-byte words of the rows only; otherwise
+ * they read whole 16-byte aligned granules that hold inputs of the matrix
+ * -- up to 15 bytes before x or after its last input, never outside the
+ * granules the data touches (an allocation from cudaMalloc is 256-byte
+ * aligned, so such a granule lies inside it).
  */
 TCR_API tcr_status tcr_reduce_rows(const void *x, size_t rows, size_t cols, float *out, tcr_mode mode,
                            void *stream);
