@@ -410,11 +410,12 @@ mma_tmem_kernel(const uint16_t *__restrict__ x, size_t n, size_t units, int unit
 // row g's partial sums; the next MMA of a chain takes the next 128 columns
 // of the same rows.  The MMAs cover a row's whole 128-column slices; the
 // last cols % 128 inputs of a row are added by the epilogue from global
-// memory, and rows past the matrix are neither copied nor stored (their
-// lanes hold stale values that no row uses).  Work unit: 16 G rows x the
-// whole row, or chunks of kTcRowsMaxChunkCols columns of longer rows; per
-// row group the epilogue adds the chain results per lane, then each row's 8
-// lanes by an xor butterfly.
+// memory; rows past the matrix are zero-filled by the tensor map or not
+// copied at all (their lanes then hold stale values), and never stored.
+// Work unit: 16 G rows x the whole row, or chunks of kTcRowsMaxChunkCols
+// columns of longer rows; a chain ends with its stage; per row group the
+// epilogue adds the chain results per lane, then each row's 8 lanes by an
+// xor butterfly.
 constexpr int kTcRowsGroup = 16;                       // data rows per MMA tile
 constexpr int kTcRowsMmaCols = 128;                    // columns per MMA and row
 constexpr int kTcRowsStageCols = 2048;                 // S of long rows (4 KiB a row)
