@@ -346,3 +346,22 @@ def test_tcgen05_units_shrink_for_small_inputs(lib):
         assert d["partials"] == (units if units > 1 else 0), n
     assert tcr.tcr_order_descriptor(n=1 << 20, mode=tcr.Mode(tcr.MMA_CHAIN_TMEM))["chunk_log2"] == 11
     assert tcr.tcr_order_descriptor(n=1 << 30, mode=tcr.Mode(tcr.MMA_CHAIN_TMEM))["chunk_log2"] == 16
+
+
+def test_tmem_rows_plan(lib):
+    # the tcgen05 rows kernel (192 threads): work units of 16 rows x the
+    # whole row up to 8192 columns (32 rows for rows of 768..1024 inputs),
+    # longer rows in 8192-column chunks with per-row partials and a combine;
+    # rows under 768 inputs and rows that are not whole 16-byte vectors go
+    # to the mma.sync kernels.  (Without a device the plan assumes 152 SMs.)
+    def plan(rows, cols):
+        d = tcr.tcr_order_descriptor(rows=rows, cols=cols, mode=tcr.Mode(tcr.MMA_CHAIN_TMEM))
+        return d["launch_block"], d["launch_grid"], d["partials"], d["launches"]
+
+    assert plan(1000, 4096) == (192, 63, 0, 1)              # 63 units of 16 rows
+    assert plan(65536, 4096) == (192, 152, 0, 1)            # one CTA per SM
+    assert plan(3000, 768) == (192, 94, 0, 1)               # two row groups per unit
+    assert plan(7, 8192) == (192, 1, 0, 1)
+    assert plan(100, 20000) == (192, 21, 300, 2)            # 3 chunks per row
+    assert plan(100, 512)[0] == 256                         # packed mma.sync rows
+    assert plan(1000, 4100)[0] == 256                       # not whole vectors
