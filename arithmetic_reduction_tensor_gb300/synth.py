@@ -23,6 +23,21 @@ Distributions (the workload recipes of the benchmark configurations):
                  element 2k = r cos t, element 2k+1 = r sin t
 ``pow2``         sign = bit 63 of word(i); e = -20 + (low 32 bits mod 31);
                  the value is sign * 2^e (exact in every storage type)
+``exact_int``    integers built per 16-byte vector (V = 8 inputs of 16 bits,
+                 V = 4 of binary32; vector v holds elements V v .. V v + V - 1,
+                 each drawing on its own word w = word(i), h = w >> 32):
+                 element 0 is a = +-A (sign: bit 63 of w), element 1 is -a;
+                 elements 2 .. V - 2 are (h mod 9) - 4; element V - 1 is
+                 s - (the sum of elements 2 .. V - 2), s = +1 if bit 63 of
+                 its word is set, else -1.  A is 1024 + (h mod 1024) for
+                 binary16 (11 significant bits), (128 + (h mod 128)) *
+                 2^((h >> 8) mod 9) for bfloat16, and 2^19 + (h mod 2^19)
+                 for binary32 (20 significant bits, so a three-way bfloat16
+                 split of it has all three parts).  Every vector sums to
+                 exactly +-1, so the total is a small integer, dropping or
+                 repeating any one vector changes it, and a partial sum that
+                 keeps each aligned pair (a, -a) together is an integer far
+                 below 2^24: binary32 adds it without rounding in any order.
 
 Rounding to the storage type: binary16 and binary32 take the binary64 value
 rounded to nearest even in one step (numpy's casts); bfloat16 takes the
@@ -45,7 +60,7 @@ _M1 = np.uint64(0xBF58476D1CE4E5B9)
 _M2 = np.uint64(0x94D049BB133111EB)
 _CHUNK = 1 << 22
 
-DISTRIBUTIONS = ("uniform_pm1", "uniform01", "normal", "pow2")
+DISTRIBUTIONS = ("uniform_pm1", "uniform01", "normal", "pow2", "exact_int")
 
 
 def _words(seed: int, start: int, count: int) -> np.ndarray:
@@ -111,7 +126,33 @@ def _chunk(dist: str, dtype: int, seed: int, start: int, count: int) -> np.ndarr
         subnormal = np.left_shift(np.uint16(1), np.clip(e + 24, 0, 15).astype(np.uint16))
         mag = np.where(e >= -14, normal, subnormal).astype(np.uint16)
         return (sign << np.uint16(15)) | mag
+    if dist == "exact_int":
+        return _exact_int(dtype, seed, start, count)
     raise ValueError(f"unknown distribution {dist!r}")
+
+
+def _exact_int(dtype: int, seed: int, start: int, count: int) -> np.ndarray:
+    V = 4 if dtype == F32 else 8
+    p0 = start - start % V                      # whole vectors around the slice
+    nv = (start + count - p0 + V - 1) // V
+    w = _words(seed, p0, nv * V).reshape(nv, V)
+    h = (w >> np.uint64(32)).astype(np.int64)
+    neg = (w >> np.uint64(63)).astype(bool)
+    v = np.empty((nv, V), np.int64)
+    if dtype == F16:
+        A = 1024 + h[:, 0] % 1024
+    elif dtype == BF16:
+        A = (128 + h[:, 0] % 128) << ((h[:, 0] >> 8) % 9)
+    else:
+        A = (1 << 19) + h[:, 0] % (1 << 19)
+    v[:, 0] = np.where(neg[:, 0], -A, A)
+    v[:, 1] = -v[:, 0]
+    v[:, 2:V - 1] = h[:, 2:V - 1] % 9 - 4
+    s = np.where(neg[:, V - 1], 1, -1)
+    v[:, V - 1] = s - v[:, 2:V - 1].sum(axis=1)
+    flat = v.reshape(-1)[start - p0:start - p0 + count]
+    # every value is an integer exact in the storage type: the casts are exact
+    return _to_bits(flat.astype(np.float64), dtype)
 
 
 def generate(n: int, dist: str, dtype: int = F16, seed: int = 0, start: int = 0,

@@ -63,3 +63,43 @@ def test_binary32_patterns_round_the_same_binary64_values():
     p = synth.as_float(synth.generate(1 << 16, "pow2", synth.F32, seed=3), synth.F32)
     p16 = synth.as_float(synth.generate(1 << 16, "pow2", synth.F16, seed=3), synth.F16)
     assert np.array_equal(p, p16)
+
+
+def test_exact_int_vectors_sum_to_one_and_open_with_a_pair():
+    for dt, V, lo, hi in ((synth.F16, 8, 1024, 2047), (synth.BF16, 8, 128, 255 << 8),
+                          (synth.F32, 4, 1 << 19, (1 << 20) - 1)):
+        b = synth.generate(3 * (1 << 22) + 5 * V, "exact_int", dt, seed=7)
+        f = synth.as_float(b, dt).astype(np.float64).reshape(-1, V)
+        assert np.all(f == np.round(f))                 # integers, exact in the type
+        assert set(np.unique(f.sum(axis=1))) == {-1.0, 1.0}
+        assert np.array_equal(f[:, 1], -f[:, 0])
+        a = np.abs(f[:, 0])
+        assert a.min() >= lo and a.max() <= hi
+        assert np.all(np.abs(f[:, 2:V - 1]) <= 4)
+        # slices that start inside a vector give the same elements
+        part = synth.generate(1001, "exact_int", dt, seed=7, start=(1 << 22) - 3)
+        assert np.array_equal(part, b[(1 << 22) - 3:(1 << 22) + 998])
+
+
+def test_exact_int_split_parts_all_in_use():
+    # the binary32 a's have 20 significant bits: truncated to bfloat16 (hi)
+    # they leave a residual whose top 8 bits (mid) and the rest (lo) are both
+    # nonzero for most a (lo for about 4 in 5)
+    b = synth.generate(1 << 16, "exact_int", synth.F32, seed=8).reshape(-1, 4)[:, 0]
+    hi = b & np.uint32(0xFFFF0000)
+    r = b.view(np.float32).astype(np.float64) - hi.view(np.float32).astype(np.float64)
+    mid = (np.abs(r).astype(np.float32).view(np.uint32) & np.uint32(0xFFFF0000)).view(np.float32)
+    lo = np.abs(r) - mid
+    assert np.mean(r != 0) > 0.99 and np.mean(lo != 0) > 0.75
+
+
+def test_exact_int_dropping_or_repeating_a_vector_changes_the_sum():
+    import oracle
+    b = synth.generate(1 << 16, "exact_int", synth.F16, seed=9)
+    total, _ = oracle.exact_sum(b, synth.F16)
+    rng = np.random.default_rng(0)
+    for v in rng.integers(0, (1 << 16) // 8, 20):
+        dropped = np.concatenate([b[:8 * v], b[8 * v + 8:]])
+        repeated = np.concatenate([b[:8 * v + 8], b[8 * v:]])
+        assert abs(oracle.exact_sum(dropped, synth.F16)[0] - total) == 1
+        assert abs(oracle.exact_sum(repeated, synth.F16)[0] - total) == 1
