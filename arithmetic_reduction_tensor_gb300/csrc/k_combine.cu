@@ -116,4 +116,12 @@ cudaError_t launch_combine(const float *partials, size_t segments, size_t count,
     return cudaLaunchKernelEx(&cfg, combine_kernel, partials, count, out);
 }
 
+cudaError_t preload_combine()
+{
+    cudaFuncAttributes a;
+    cudaError_t e = cudaFuncGetAttributes(&a, combine_kernel);
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, combine_rows_kernel);
+    return e;
+}
+
 }  // namespace tcr

@@ -95,6 +95,17 @@ cudaError_t launch_fixed_rows_warp(int dtype, int op, bool aligned, const void *
     return cudaLaunchKernel(k, dim3(grid), dim3(block), args, 0, stream);
 }
 
+cudaError_t preload_fixed_chunk_sums()
+{
+    for (int dt : {kF16, kBF16, kF32})
+        for (bool aligned : {true, false}) {
+            cudaFuncAttributes a;
+            const cudaError_t e = cudaFuncGetAttributes(&a, pick(false, dt, kOpSum, aligned, 0));
+            if (e != cudaSuccess) return e;
+        }
+    return cudaSuccess;
+}
+
 int occupancy_fixed(bool rows, int dtype, int op, bool aligned, int block, int vrun)
 {
     const void *k = pick(rows, dtype, op, aligned, vrun);

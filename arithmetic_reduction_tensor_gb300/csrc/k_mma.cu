@@ -102,6 +102,18 @@ cudaError_t launch_mma_rows(int dtype, int op, bool aligned, int R, const void *
     return cudaLaunchKernel(k, dim3(grid), dim3(block), args, 0, stream);
 }
 
+cudaError_t preload_mma_chunk_sums()
+{
+    for (int R = 1; R <= 8; R++)
+        for (int dt : {kF16, kBF16, kF32})
+            for (bool aligned : {true, false}) {
+                cudaFuncAttributes a;
+                const cudaError_t e = cudaFuncGetAttributes(&a, pick(false, dt, kOpSum, aligned, R));
+                if (e != cudaSuccess) return e;
+            }
+    return cudaSuccess;
+}
+
 int occupancy_mma(bool rows, int dtype, int op, bool aligned, int R, int block)
 {
     void *k = pick(rows, dtype, op, aligned, R);

@@ -151,6 +151,14 @@ int gemm_block_threads();
 cudaError_t launch_combine(const float *partials, size_t segments, size_t count, float *out,
                            cudaStream_t stream);
 
+// Make the driver load every variant of a kernel family now (one
+// cudaFuncGetAttributes per variant), so that no later launch of them loads
+// code: the chunk kernels' sums (FIXED_ORDER plain tree; MMA_CHAIN at every
+// R), for every input type and alignment, and the two combine kernels.
+cudaError_t preload_fixed_chunk_sums();
+cudaError_t preload_mma_chunk_sums();
+cudaError_t preload_combine();
+
 // Resident CTAs per SM of each kernel at a block size (occupancy API);
 // `rows` selects the per-row variant.  0 if the query fails.
 int occupancy_fixed(bool rows, int dtype, int op, bool aligned, int block, int vrun = 0);

@@ -15,18 +15,11 @@
 
 #include "../../include/tcr.h"
 #include "kernels.cuh"
+#include "plan.h"
 
-namespace {
+namespace tcr {
+namespace plan {
 
-using namespace tcr;
-
-constexpr size_t kMaxInputs = (size_t)1 << 40;
-constexpr int kMaxRunLog2 = 16;
-constexpr int kDefaultBlock = 256;
-// GB300: 152 SMs.  Used only by the declared SHUFFLE_TREE team rule (so the
-// declared order is the same on every device) and as the launch-plan SM
-// count when no device can be queried.
-constexpr int kRuleSMs = 152;
 
 // -------------------------------------------------------------- devices
 
@@ -99,7 +92,6 @@ cudaMemPool_t pool_for(int dev)
     return d.pool;
 }
 
-enum Family { kFixedF, kShuffleF, kMmaF, kBlockedF, kPackedF };
 
 int occupancy(int dev, Family fam, bool rows, int dtype, int op, bool aligned, int R, int block)
 {
@@ -128,37 +120,6 @@ int occupancy(int dev, Family fam, bool rows, int dtype, int op, bool aligned, i
     g_occ.emplace_back(key, n);
     return n;
 }
-
-// -------------------------------------------------------------- planning
-
-enum Path {
-    kPathEmpty,          // nothing to reduce: memset out to +0.0
-    kPathChunk,          // FIXED / MMA chunked kernel (+ combine if cps > 1)
-    kPathFixedRowsWarp,  // FIXED, one warp per row
-    kPathMmaRows,        // MMA, one warp per row
-    kPathShuffleBlock,   // SHUFFLE block team (+ combine if G > 1)
-    kPathShuffleRowsWarp, // SHUFFLE warp team, one warp per row
-    kPathTmem,           // MMA_CHAIN on tcgen05 (+ combine if units > 1)
-    kPathTmemRows,       // MMA_CHAIN rows on tcgen05 (+ combine if chunks > 1)
-    kPathBlocked,        // FIXED blocked order, runs longer than a vector (+ combine)
-    kPathPackedRows      // short rows, several to a warp group (FIXED, SHUFFLE, MMA)
-};
-
-struct Plan {
-    int kind, dtype, op, R, block;
-    int run_log2;            // blocked order: log2 run length (0: the plain tree)
-    int vrun;                // runs inside a vector: the warp-stream kernels' variant
-    int packed, vlog;        // packed rows: kernel family, log2 vector slots per row
-    bool aligned;
-    Path path;
-    size_t segments, seg_len;
-    int grid, chunk_log2;
-    size_t cps, units;       // chunks per segment, CTA work units
-    int team_threads, team_blocks;
-    size_t partials;         // fp32 scratch entries (0: writes out directly)
-    size_t combine_count;    // partials per segment for the combine
-    int launches;
-};
 
 int log2_exact(int v)
 {
@@ -195,6 +156,116 @@ int vector_len(int dtype)
     return (int)(16 / elem_bytes(dtype));
 }
 
+tcr_status check_mode(const tcr_mode &m, int *block, int *R)
+{
+    if (m.kind < TCR_MMA_CHAIN || m.kind > TCR_MMA_CHAIN_TMEM) return TCR_ERR_INVALID_ARG;
+    if (m.dtype != TCR_F16 && m.dtype != TCR_BF16 && m.dtype != TCR_F32) return TCR_ERR_INVALID_ARG;
+    if (m.run_log2 < 0 || m.run_log2 > kMaxRunLog2) return TCR_ERR_INVALID_ARG;
+    if (m.run_log2 != 0 && m.kind != TCR_FIXED_ORDER) return TCR_ERR_INVALID_ARG;
+    int b = m.block_threads == 0 ? kDefaultBlock : m.block_threads;
+    if (b < 32 || b > 1024 || (b & (b - 1)) != 0) return TCR_ERR_INVALID_ARG;
+    int r = 0;
+    if (m.kind == TCR_MMA_CHAIN || m.kind == TCR_MMA_CHAIN_TMEM) {
+        if (m.R < 0 || m.R > 8) return TCR_ERR_INVALID_ARG;
+        r = m.R == 0 ? default_R(b) : m.R;
+    }
+    *block = b;
+    *R = r;
+    return TCR_OK;
+}
+
+tcr_status check_common(const void *x, size_t total, const float *out, const tcr_mode &mode,
+                        int *block, int *R)
+{
+    if (!out || ((uintptr_t)out & 3u) != 0) return TCR_ERR_INVALID_ARG;
+    if (total >= kMaxInputs) return TCR_ERR_INVALID_ARG;
+    tcr_status st = check_mode(mode, block, R);
+    if (st != TCR_OK) return st;
+    // x is aligned to its pattern type: 2 bytes, or 4 for binary32
+    if (total > 0 && (!x || ((uintptr_t)x & (elem_bytes(mode.dtype) - 1)) != 0))
+        return TCR_ERR_INVALID_ARG;
+    return TCR_OK;
+}
+
+// may_shrink: the CTA size is free to choose (FIXED_ORDER, whose bits never
+// depend on it, or a default block size): a sum small enough for one CTA
+// whose warps take at most two groups each (2^17 16-bit or 2^16 binary32
+// inputs) is one work unit -- one launch, no partials, no scratch; larger
+// small inputs get smaller CTAs, then shorter warp spans (16 KiB down to
+// one 4 KiB group), until there are two work units per SM of the 152 the
+// rules assume.  Both are fixed functions of the input length, so
+// MMA_CHAIN's chunking (reported by the descriptor) is the same on every
+// device.
+ChunkSplit chunk_split(size_t segments, size_t seg_len, int dtype, int block, bool may_shrink)
+{
+    ChunkSplit c;
+    int span_log2 = kWarpSpanBytesLog2 - log2_exact((int)elem_bytes(dtype));
+    const int group_log2 = kGroupBytesLog2 - log2_exact((int)elem_bytes(dtype));
+    if (may_shrink && segments == 1 && seg_len <= ((size_t)1 << (group_log2 + 1 + 5))) {
+        // one CTA: spans of one group (two above 32 groups), as few warps as cover it
+        span_log2 = seg_len > ((size_t)1 << (group_log2 + 5)) ? group_log2 + 1 : group_log2;
+        int warps = 1;
+        while (((size_t)warps << span_log2) < seg_len) warps *= 2;
+        c.block = 32 * warps;
+        c.chunk_log2 = span_log2 + log2_exact(warps);
+        c.cps = 1;
+        return c;
+    }
+    c.block = block;
+    for (;;) {
+        c.chunk_log2 = span_log2 + log2_exact(c.block / 32);
+        c.cps = (seg_len + ((size_t)1 << c.chunk_log2) - 1) >> c.chunk_log2;
+        if (!may_shrink || segments * c.cps >= (size_t)2 * kRuleSMs) break;
+        if (c.block > 32)
+            c.block /= 2;
+        else if (span_log2 > group_log2)
+            span_log2--;
+        else
+            break;
+    }
+    return c;
+}
+
+}  // namespace plan
+}  // namespace tcr
+
+namespace {
+
+using namespace tcr;
+using namespace tcr::plan;
+
+// -------------------------------------------------------------- planning
+
+enum Path {
+    kPathEmpty,          // nothing to reduce: memset out to +0.0
+    kPathChunk,          // FIXED / MMA chunked kernel (+ combine if cps > 1)
+    kPathFixedRowsWarp,  // FIXED, one warp per row
+    kPathMmaRows,        // MMA, one warp per row
+    kPathShuffleBlock,   // SHUFFLE block team (+ combine if G > 1)
+    kPathShuffleRowsWarp, // SHUFFLE warp team, one warp per row
+    kPathTmem,           // MMA_CHAIN on tcgen05 (+ combine if units > 1)
+    kPathTmemRows,       // MMA_CHAIN rows on tcgen05 (+ combine if chunks > 1)
+    kPathBlocked,        // FIXED blocked order, runs longer than a vector (+ combine)
+    kPathPackedRows      // short rows, several to a warp group (FIXED, SHUFFLE, MMA)
+};
+
+struct Plan {
+    int kind, dtype, op, R, block;
+    int run_log2;            // blocked order: log2 run length (0: the plain tree)
+    int vrun;                // runs inside a vector: the warp-stream kernels' variant
+    int packed, vlog;        // packed rows: kernel family, log2 vector slots per row
+    bool aligned;
+    Path path;
+    size_t segments, seg_len;
+    int grid, chunk_log2;
+    size_t cps, units;       // chunks per segment, CTA work units
+    int team_threads, team_blocks;
+    size_t partials;         // fp32 scratch entries (0: writes out directly)
+    size_t combine_count;    // partials per segment for the combine
+    int launches;
+};
+
+
 // The declared SHUFFLE_TREE team for a segment of L inputs, in vectors of
 // V inputs, at block size B: one warp for segments of at most 1024
 // vectors, else G blocks of B threads with about 16 vectors per thread, at
@@ -216,61 +287,18 @@ void shuffle_team(size_t L, int V, int B, int *Bt, int *G)
     *G = (int)g;
 }
 
-tcr_status check_mode(const tcr_mode &m, int *block, int *R)
-{
-    if (m.kind < TCR_MMA_CHAIN || m.kind > TCR_MMA_CHAIN_TMEM) return TCR_ERR_INVALID_ARG;
-    if (m.dtype != TCR_F16 && m.dtype != TCR_BF16 && m.dtype != TCR_F32) return TCR_ERR_INVALID_ARG;
-    if (m.run_log2 < 0 || m.run_log2 > kMaxRunLog2) return TCR_ERR_INVALID_ARG;
-    if (m.run_log2 != 0 && m.kind != TCR_FIXED_ORDER) return TCR_ERR_INVALID_ARG;
-    int b = m.block_threads == 0 ? kDefaultBlock : m.block_threads;
-    if (b < 32 || b > 1024 || (b & (b - 1)) != 0) return TCR_ERR_INVALID_ARG;
-    int r = 0;
-    if (m.kind == TCR_MMA_CHAIN || m.kind == TCR_MMA_CHAIN_TMEM) {
-        if (m.R < 0 || m.R > 8) return TCR_ERR_INVALID_ARG;
-        r = m.R == 0 ? default_R(b) : m.R;
-    }
-    *block = b;
-    *R = r;
-    return TCR_OK;
-}
 
-// may_shrink: the CTA size is free to choose (FIXED_ORDER, whose bits never
-// depend on it, or a default block size): a sum small enough for one CTA
-// whose warps take at most two groups each (2^17 16-bit or 2^16 binary32
-// inputs) is one work unit -- one launch, no partials, no scratch; larger
-// small inputs get smaller CTAs, then shorter warp spans (16 KiB down to
-// one 4 KiB group), until there are two work units per SM of the 152 the
-// rules assume.  Both are fixed functions of the input length, so
-// MMA_CHAIN's chunking (reported by the descriptor) is the same on every
-// device.
+// The chunked kernels' plan: the work split of chunk_split, a grid of at most
+// one wave of resident CTAs, and a combine launch when a segment has several
+// chunks.
 void plan_chunked(Plan &p, int dev, Family fam, bool may_shrink)
 {
     p.path = kPathChunk;
-    int span_log2 = kWarpSpanBytesLog2 - log2_exact((int)elem_bytes(p.dtype));
-    const int group_log2 = kGroupBytesLog2 - log2_exact((int)elem_bytes(p.dtype));
-    if (may_shrink && p.segments == 1 && p.seg_len <= ((size_t)1 << (group_log2 + 1 + 5))) {
-        // one CTA: spans of one group (two above 32 groups), as few warps as cover it
-        span_log2 = p.seg_len > ((size_t)1 << (group_log2 + 5)) ? group_log2 + 1 : group_log2;
-        int warps = 1;
-        while (((size_t)warps << span_log2) < p.seg_len) warps *= 2;
-        p.block = 32 * warps;
-        p.chunk_log2 = span_log2 + log2_exact(warps);
-        p.cps = 1;
-        p.units = 1;
-    } else {
-        for (;;) {
-            p.chunk_log2 = span_log2 + log2_exact(p.block / 32);
-            p.cps = (p.seg_len + ((size_t)1 << p.chunk_log2) - 1) >> p.chunk_log2;
-            p.units = p.segments * p.cps;
-            if (!may_shrink || p.units >= (size_t)2 * kRuleSMs) break;
-            if (p.block > 32)
-                p.block /= 2;
-            else if (span_log2 > group_log2)
-                span_log2--;
-            else
-                break;
-        }
-    }
+    const ChunkSplit c = chunk_split(p.segments, p.seg_len, p.dtype, p.block, may_shrink);
+    p.block = c.block;
+    p.chunk_log2 = c.chunk_log2;
+    p.cps = c.cps;
+    p.units = p.segments * c.cps;
     const size_t resident =
         (size_t)sm_count(dev) *
         (size_t)occupancy(dev, fam, false, p.dtype, p.op, p.aligned,
@@ -538,18 +566,6 @@ tcr_status run_plan(const Plan &p, const void *x, float *out, cudaStream_t s, in
     return e == cudaSuccess ? TCR_OK : TCR_ERR_CUDA;
 }
 
-tcr_status check_common(const void *x, size_t total, const float *out, const tcr_mode &mode,
-                        int *block, int *R)
-{
-    if (!out || ((uintptr_t)out & 3u) != 0) return TCR_ERR_INVALID_ARG;
-    if (total >= kMaxInputs) return TCR_ERR_INVALID_ARG;
-    tcr_status st = check_mode(mode, block, R);
-    if (st != TCR_OK) return st;
-    // x is aligned to its pattern type: 2 bytes, or 4 for binary32
-    if (total > 0 && (!x || ((uintptr_t)x & (elem_bytes(mode.dtype) - 1)) != 0))
-        return TCR_ERR_INVALID_ARG;
-    return TCR_OK;
-}
 
 bool mul_overflows(size_t a, size_t b)
 {

@@ -17,9 +17,12 @@
 // Behaviour a caller must know:
 //  * The array holds kNoAllocMaxPartials floats (256 KiB) on every GPU that
 //    loads the library, for as long as the process runs.
-//  * The first call on each device looks up the array's device address
-//    (cudaGetSymbolAddress) with that device current; make that first call
-//    before any stream capture.
+//  * The first call on each device, with that device current, looks up the
+//    array's device address (cudaGetSymbolAddress) and makes the driver
+//    load every kernel this entry point can launch (the runtime otherwise
+//    loads each kernel at its first launch, and loading code reserves
+//    device memory): after that first call no call loads anything.  Make
+//    the first call before any stream capture.
 //  * Every call on a device uses the same array, and it keeps whatever the
 //    last call left there.  Nothing in it needs clearing: the reduction
 //    kernel writes every partial slot the combine kernel then reads, in the
@@ -27,19 +30,25 @@
 //    (two streams, or two host threads without ordering between them) race
 //    on the array and give wrong results: order them on one stream or with
 //    events.
-//  * Only the chunked kernels are served (TCR_FIXED_ORDER and TCR_MMA_CHAIN);
-//    TCR_SHUFFLE_TREE returns TCR_ERR_UNSUPPORTED.  An n whose chunk count
-//    exceeds the array returns TCR_ERR_UNSUPPORTED before any GPU work.
+//  * Only the chunked kernels are served (TCR_FIXED_ORDER with the plain
+//    tree, TCR_MMA_CHAIN), with the work split of tcr_reduce_sum (one plan
+//    function serves both), so the results are tcr_reduce_sum's bit for bit.
+//    TCR_SHUFFLE_TREE, TCR_MMA_CHAIN_TMEM and a blocked order return
+//    TCR_ERR_UNSUPPORTED; an n whose chunk count exceeds the array returns
+//    TCR_ERR_UNSUPPORTED before any GPU work; malformed arguments return
+//    TCR_ERR_INVALID_ARG exactly as for tcr_reduce_sum.
 //  * No cudaMalloc, cudaFree or allocating library routine is called.
 #include <cstdint>
 #include <mutex>
 
 #include "../../include/tcr.h"
 #include "kernels.cuh"
+#include "plan.h"
 
 namespace {
 
 using namespace tcr;
+using namespace tcr::plan;
 
 constexpr size_t kNoAllocMaxPartials = 65536;
 constexpr int kMaxDevices = 64;
@@ -50,34 +59,29 @@ static __device__ __align__(256) float g_noalloc_partials[kNoAllocMaxPartials];
 struct NoAllocDevice {
     bool ready = false;
     float *partials = nullptr;   // device address of g_noalloc_partials
-    int sms = 0;
 };
 
 std::mutex g_noalloc_mu;
 NoAllocDevice g_noalloc_dev[kMaxDevices];
 
-// Set-up, once per device, with that device current.
-tcr_status noalloc_setup(int dev, NoAllocDevice *out)
+// Set-up, once per device, with that device current: the array's address,
+// and every kernel variant this entry point launches loaded.
+tcr_status noalloc_setup(int dev, float **partials)
 {
     std::lock_guard<std::mutex> lk(g_noalloc_mu);
     NoAllocDevice &d = g_noalloc_dev[dev];
     if (!d.ready) {
         void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_partials) != cudaSuccess || p == nullptr) {
-            (void)cudaGetLastError();
-            return TCR_ERR_CUDA;
-        }
-        int sms = 0;
-        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-            sms <= 0) {
+        if (cudaGetSymbolAddress(&p, g_noalloc_partials) != cudaSuccess || p == nullptr ||
+            preload_fixed_chunk_sums() != cudaSuccess || preload_mma_chunk_sums() != cudaSuccess ||
+            preload_combine() != cudaSuccess) {
             (void)cudaGetLastError();
             return TCR_ERR_CUDA;
         }
         d.partials = (float *)p;
-        d.sms = sms;
         d.ready = true;
     }
-    *out = d;
+    *partials = d.partials;
     return TCR_OK;
 }
 
@@ -86,85 +90,39 @@ tcr_status noalloc_setup(int dev, NoAllocDevice *out)
 extern "C" tcr_status tcr_reduce_sum_noalloc(const void *x, size_t n, float *out, tcr_mode mode,
                                              void *stream)
 {
-    if (!out || ((uintptr_t)out & 3u) != 0) return TCR_ERR_INVALID_ARG;
-    if (n >= ((size_t)1 << 40)) return TCR_ERR_INVALID_ARG;
-    if (mode.dtype != TCR_F16 && mode.dtype != TCR_BF16 && mode.dtype != TCR_F32)
-        return TCR_ERR_INVALID_ARG;
-    const int elem_log2 = mode.dtype == TCR_F32 ? 2 : 1;
-    if (n > 0 && (!x || ((uintptr_t)x & ((1u << elem_log2) - 1u)) != 0)) return TCR_ERR_INVALID_ARG;
-    if (mode.run_log2 < 0 || mode.run_log2 > 16) return TCR_ERR_INVALID_ARG;
+    int block = 0, R = 0;
+    tcr_status st = check_common(x, n, out, mode, &block, &R);
+    if (st != TCR_OK) return st;
+    if (mode.kind != TCR_FIXED_ORDER && mode.kind != TCR_MMA_CHAIN) return TCR_ERR_UNSUPPORTED;
     if (mode.run_log2 != 0) return TCR_ERR_UNSUPPORTED;     // the plain tree only
-    const int block = mode.block_threads == 0 ? 256 : mode.block_threads;
-    if (block < 32 || block > 1024 || (block & (block - 1)) != 0) return TCR_ERR_INVALID_ARG;
-    int R = 0;
-    if (mode.kind == TCR_MMA_CHAIN) {
-        if (mode.R < 0 || mode.R > 8) return TCR_ERR_INVALID_ARG;
-        R = mode.R != 0 ? mode.R : 4;    // the same default as tcr_reduce_sum
-    } else if (mode.kind == TCR_SHUFFLE_TREE) {
-        return TCR_ERR_UNSUPPORTED;
-    } else if (mode.kind != TCR_FIXED_ORDER) {
-        return TCR_ERR_INVALID_ARG;
-    }
 
-    // 2^kWarpSpanBytesLog2 bytes per warp, and the same choice of CTA size
-    // and span for small inputs, as in the allocating entry point
-    int block_used = block;
-    int warps_log2 = 0;
-    while ((32 << warps_log2) < block_used) warps_log2++;
-    int span_log2 = kWarpSpanBytesLog2 - elem_log2;
-    const int group_log2 = kGroupBytesLog2 - elem_log2;
-    int chunk_log2 = span_log2 + warps_log2;
-    size_t cps = (n + ((size_t)1 << chunk_log2) - 1) >> chunk_log2;
-    const bool may_shrink = mode.kind == TCR_FIXED_ORDER || mode.block_threads == 0;
-    const bool one_cta = may_shrink && n <= ((size_t)1 << (group_log2 + 1 + 5));
-    if (one_cta) {
-        // one CTA, as in the allocating entry point
-        span_log2 = n > ((size_t)1 << (group_log2 + 5)) ? group_log2 + 1 : group_log2;
-        block_used = 32;
-        warps_log2 = 0;
-        while (((size_t)block_used << (span_log2 - 5)) < n) {
-            block_used *= 2;
-            warps_log2++;
-        }
-        chunk_log2 = span_log2 + warps_log2;
-        cps = 1;
-    }
-    while (may_shrink && !one_cta && cps < (size_t)2 * 152 && (block_used > 32 || span_log2 > group_log2)) {
-        if (block_used > 32) {
-            block_used /= 2;
-            warps_log2--;
-        } else {
-            span_log2--;
-        }
-        chunk_log2 = span_log2 + warps_log2;
-        cps = (n + ((size_t)1 << chunk_log2) - 1) >> chunk_log2;
-    }
-    if (cps > kNoAllocMaxPartials) return TCR_ERR_UNSUPPORTED;
+    // the split of tcr_reduce_sum for this mode (the CTA size is free for
+    // FIXED_ORDER and for a default block size)
+    const ChunkSplit c = chunk_split(1, n, mode.dtype, block,
+                                     mode.kind == TCR_FIXED_ORDER || mode.block_threads == 0);
+    if (c.cps > kNoAllocMaxPartials) return TCR_ERR_UNSUPPORTED;
 
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
-        (void)cudaGetLastError();
-        return TCR_ERR_CUDA;
-    }
+    const int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices) return TCR_ERR_CUDA;
     cudaStream_t s = (cudaStream_t)stream;
     if (n == 0) return cudaMemsetAsync(out, 0, sizeof(float), s) == cudaSuccess ? TCR_OK : TCR_ERR_CUDA;
 
-    NoAllocDevice d;
-    tcr_status st = noalloc_setup(dev, &d);
+    float *partials = nullptr;
+    st = noalloc_setup(dev, &partials);
     if (st != TCR_OK) return st;
 
     const bool aligned = ((uintptr_t)x & 15u) == 0;
-    int occ = mode.kind == TCR_FIXED_ORDER ? occupancy_fixed(false, mode.dtype, kOpSum, aligned, block_used)
-                                           : occupancy_mma(false, mode.dtype, kOpSum, aligned, R, block_used);
-    if (occ <= 0) occ = 1;
-    const size_t resident = (size_t)d.sms * (size_t)occ;
-    const int grid = (int)(cps < resident ? cps : resident);
-    float *dst = cps > 1 ? d.partials : out;
-    cudaError_t e = mode.kind == TCR_FIXED_ORDER
-                        ? launch_fixed_chunk(mode.dtype, kOpSum, aligned, x, n, cps, cps,
-                                             chunk_log2, dst, grid, block_used, s)
-                        : launch_mma_chunk(mode.dtype, kOpSum, aligned, R, x, n, cps, cps,
-                                           chunk_log2, dst, grid, block_used, s);
-    if (e == cudaSuccess && cps > 1) e = launch_combine(d.partials, 1, cps, out, s);
+    const bool fixed = mode.kind == TCR_FIXED_ORDER;
+    const size_t resident =
+        (size_t)sm_count(dev) *
+        (size_t)occupancy(dev, fixed ? kFixedF : kMmaF, false, mode.dtype, kOpSum, aligned,
+                          fixed ? 0 : R, c.block);
+    const int grid = (int)(c.cps < resident ? c.cps : resident);
+    float *dst = c.cps > 1 ? partials : out;
+    cudaError_t e = fixed ? launch_fixed_chunk(mode.dtype, kOpSum, aligned, x, n, c.cps, c.cps,
+                                               c.chunk_log2, dst, grid, c.block, s)
+                          : launch_mma_chunk(mode.dtype, kOpSum, aligned, R, x, n, c.cps, c.cps,
+                                             c.chunk_log2, dst, grid, c.block, s);
+    if (e == cudaSuccess && c.cps > 1) e = launch_combine(partials, 1, c.cps, out, s);
     return e == cudaSuccess ? TCR_OK : TCR_ERR_CUDA;
 }

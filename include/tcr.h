@@ -250,24 +250,28 @@ TCR_API tcr_status tcr_reduce_rows_mean_var(const void *x, size_t rows, size_t c
  * The pages have no counterpart to this entry point; it is an interface
  * choice of this library.
  *
- * Same arguments and results as tcr_reduce_sum (caller-owned x and out),
- * but the partials live in one fixed array of 65536 floats (256 KiB) in
- * device memory, held by every GPU that loads the library until the
- * process exits; no cudaMalloc, cudaFree or other allocating call is made.
- *   - Serves TCR_FIXED_ORDER (run_log2 = 0) and TCR_MMA_CHAIN;
- *     TCR_SHUFFLE_TREE and a blocked order return TCR_ERR_UNSUPPORTED.
+ * Same arguments as tcr_reduce_sum (caller-owned x and out), but the
+ * partials live in one fixed array of 65536 floats (256 KiB) in device
+ * memory, held by every GPU that loads the library until the process exits;
+ * no cudaMalloc, cudaFree or other allocating call is made.
+ *   - Serves TCR_FIXED_ORDER (run_log2 = 0) and TCR_MMA_CHAIN, with the work
+ *     split of tcr_reduce_sum (one plan function serves both), so results
+ *     are tcr_reduce_sum's bit for bit.  TCR_SHUFFLE_TREE, TCR_MMA_CHAIN_TMEM
+ *     and a blocked order return TCR_ERR_UNSUPPORTED; malformed arguments
+ *     return TCR_ERR_INVALID_ARG exactly as tcr_reduce_sum does.
  *   - n is limited to 65536 chunks of 2^(13 + log2(block_threads / 32))
  *     16-bit inputs (2^32 inputs at the default 256 threads, 2^29 at 32),
  *     half as many binary32 inputs; a larger n returns TCR_ERR_UNSUPPORTED
  *     before any GPU work.
- *   - The first call on each device looks up the array's device address
- *     with that device current; make that first call before any stream
- *     capture.
+ *   - The first call on each device, with that device current, looks up the
+ *     array's device address and has the driver load every kernel this
+ *     entry point can launch (the runtime otherwise loads a kernel at its
+ *     first launch, and loading code takes device memory): later calls load
+ *     nothing.  Make that first call before any stream capture.
  *   - All calls on a device share the array, which keeps the last call's
  *     contents (nothing needs clearing: each call writes every partial it
  *     reads).  Calls that overlap on the GPU race on it: order them on one
  *     stream or with events.
- * Results are the same as tcr_reduce_sum's for the same mode.
  */
 TCR_API tcr_status tcr_reduce_sum_noalloc(const void *x, size_t n, float *out, tcr_mode mode,
                                           void *stream);

@@ -77,6 +77,23 @@ FAKE = 0x7F0000000000      # never dereferenced: every case below fails validati
 def test_sum_rejects_bad_arguments_before_gpu_work(lib, args):
     x, n, out, mode = args
     assert lib.tcr_reduce_sum(x, n, out, mode, None) == tcr.ERR_INVALID_ARG
+    # the entry point without allocation checks its arguments the same way
+    f = lib.tcr_reduce_sum_noalloc
+    f.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, tcr.tcr_mode, ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    assert f(x, n, out, mode, None) == tcr.ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("mode", [tcr.Mode(tcr.SHUFFLE_TREE), tcr.Mode(tcr.MMA_CHAIN_TMEM),
+                                  tcr.Mode(tcr.FIXED_ORDER, run_log2=3)])
+def test_noalloc_refuses_what_it_does_not_serve_before_gpu_work(lib, mode):
+    f = lib.tcr_reduce_sum_noalloc
+    f.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, tcr.tcr_mode, ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    assert f(FAKE, 10, FAKE, mode, None) == tcr.ERR_UNSUPPORTED
+    # more chunks than its fixed array holds: 65536 chunks of 2^16 inputs (8
+    # warps of 2^13) at 256 threads
+    assert f(FAKE, 65536 * 8192 * 8 + 1, FAKE, tcr.Mode(tcr.FIXED_ORDER), None) == tcr.ERR_UNSUPPORTED
 
 
 def test_rows_rejects_bad_arguments(lib):
