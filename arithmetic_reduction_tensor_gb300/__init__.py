@@ -31,6 +31,7 @@ __all__ = [
     "tcr_reduce_rows_moments", "tcr_reduce_rows_mean_var",
     "tcr_order_descriptor", "tcr_order_equivalent", "tcr_status_string", "tcr_device_faults",
     "FAULT_PIPELINE_WAIT", "tcr_gemm_desc", "tcr_gemm_descriptor", "tcr_gemm_splitk",
+    "tcr_reduce_sum_noalloc", "tcr_read_probe",
 ]
 
 MMA_CHAIN, SHUFFLE_TREE, FIXED_ORDER, MMA_CHAIN_TMEM = 0, 1, 2, 3
@@ -134,6 +135,10 @@ def c_api() -> ctypes.CDLL:
             lib.tcr_gemm_splitk.restype = ctypes.c_int
             lib.tcr_device_faults.argtypes = [ctypes.POINTER(ctypes.c_uint), ctypes.c_int]
             lib.tcr_device_faults.restype = ctypes.c_int
+            lib.tcr_reduce_sum_noalloc.argtypes = [vp, sz, vp, tcr_mode, vp]
+            lib.tcr_reduce_sum_noalloc.restype = ctypes.c_int
+            lib.tcr_read_probe.argtypes = [vp, sz, vp, ctypes.c_int, ctypes.c_int, vp]
+            lib.tcr_read_probe.restype = ctypes.c_int
             lib.tcr_status_string.argtypes = [ctypes.c_int]
             lib.tcr_status_string.restype = ctypes.c_char_p
             _lib = lib
@@ -236,6 +241,32 @@ def tcr_reduce_sum(x, mode: tcr_mode, out=None, stream=None):
 def tcr_reduce_rows(x, mode: tcr_mode, out=None, stream=None):
     """out[r] = sum of row r of the contiguous 2-D CUDA tensor ``x`` (``tcr_reduce_rows``)."""
     return _rows_call("tcr_reduce_rows", x, mode, out, stream)
+
+
+def tcr_reduce_sum_noalloc(x, mode: tcr_mode, out=None, stream=None):
+    """``tcr_reduce_sum`` without device allocation (``tcr_reduce_sum_noalloc``:
+    FIXED_ORDER and MMA_CHAIN; the partials live in the library's fixed
+    device array).  A new ``out`` is allocated here by torch when none is
+    given: callers that must not allocate pass their own."""
+    return _sum_call("tcr_reduce_sum_noalloc", x, mode, out, stream)
+
+
+def tcr_read_probe(x, ctas_per_sm: int = 0, block_threads: int = 0, out=None, stream=None):
+    """Stream the bytes of the contiguous CUDA tensor ``x`` in and XOR their
+    32-bit words into ``out`` (``tcr_read_probe``, a measurement aid: the
+    read ceiling of the GPU).  Returns ``out`` (an int32 tensor of one)."""
+    import torch
+    if not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous CUDA tensor")
+    nbytes = x.numel() * x.element_size()
+    if out is None:
+        out = torch.empty(1, dtype=torch.int32, device=x.device)
+    with torch.cuda.device(x.device):
+        st = c_api().tcr_read_probe(x.data_ptr() if nbytes else None, nbytes, out.data_ptr(),
+                                    ctas_per_sm, block_threads, _stream_handle(x.device, stream))
+    if st != OK:
+        raise TcrError(st, "tcr_read_probe")
+    return out
 
 
 def tcr_reduce_sum_squares(x, mode: tcr_mode, out=None, stream=None):

@@ -15,6 +15,15 @@ synthetic inputs resident in HBM:
 rank's device time (CUDA events on the launching stream).  Both inputs are
 far larger than the 129 MB L2, so no flush is needed between calls.
 
+The same JSON line also carries the other configurations of the workload
+(``configs``): the 2^20 binary16 sum (L2 flushed before every call by
+writing 640 MiB and then reading 256 MiB, outside the timed events; median
+of at least 20 calls), the R x block sweep on 2^28 values in [0, 1), and the
+2^29 bfloat16 cancellation sum; the read ceiling of the GPU (the best of a
+grid sweep of a read-only probe kernel over the 2 GiB input), against which
+every fraction is also given; and the oracle on the host cores, all cores
+and one.
+
 ``--impl reference`` times the CPU oracle instead (the reference arm),
 on a bounded sample of the same workload.  ``--sweep`` prints one line per
 (R, block) point of the MMA_CHAIN sweep on 2^28 values in [0, 1).
@@ -334,6 +343,138 @@ def time_e2e(xs, xr, calls_factory, steps: int, world: int):
     return t0.elapsed_time(t1) / 1e3, h2d, d2h
 
 
+def read_ceiling(x):
+    """Best GB/s of the read-only probe kernel (tcr_read_probe) over the
+    bytes of x, across grid shapes; median of 10 launches per shape."""
+    import torch
+    import arithmetic_reduction_tensor_gb300 as tcr
+    nbytes = x.numel() * x.element_size()
+    out = torch.empty(1, dtype=torch.int32, device=x.device)
+    best = None
+    for block in (256, 512, 1024):
+        for ctas in (1, 2, 4, 8):
+            if block * ctas > 2048:
+                continue
+            for _ in range(2):
+                tcr.tcr_read_probe(x, ctas, block, out=out)
+            times = []
+            for _ in range(10):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                tcr.tcr_read_probe(x, ctas, block, out=out)
+                e1.record()
+                torch.cuda.synchronize()
+                times.append(e0.elapsed_time(e1) * 1e3)
+            gbps = nbytes / statistics.median(times) / 1e3
+            if best is None or gbps > best["gbps"]:
+                best = {"gbps": round(gbps, 1), "ctas_per_sm": ctas, "block": block}
+    best.update({"bytes": nbytes, "kernel": "read_probe_kernel",
+                 "how": "16-byte streaming loads, 8 in flight per thread, XOR of the words; "
+                        "best grid shape, median of 10 launches each"})
+    return best
+
+
+def timed_median_us(fn, iters: int, warmup: int, before=None):
+    """Median device time of fn() in microseconds (CUDA events around each
+    call on the current stream); before() runs ahead of each call, outside
+    the events."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    times = []
+    for _ in range(iters):
+        if before is not None:
+            before()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1) * 1e3)
+    return statistics.median(times)
+
+
+def time_configs(args, device, ceiling_gbps: float):
+    """The workload's other configurations, each call timed alone:
+    the 2^20 binary16 sum (seed 0) with L2 flushed before every call; the
+    MMA_CHAIN R x block sweep and SHUFFLE_TREE / FIXED_ORDER by block on 2^28
+    values in [0, 1) (seed 1); the 2^29 bfloat16 sum of +-2^e (seed 3)."""
+    import torch
+    import arithmetic_reduction_tensor_gb300 as tcr
+    from arithmetic_reduction_tensor_gb300 import synth
+    peak, _ = load_peaks()
+    iters = max(20, min(args.steps, 50))
+    out = torch.empty(1, dtype=torch.float32, device=device)
+    launches = 0
+
+    def entry(nbytes, us, mode, n):
+        nonlocal launches
+        launches += (iters + 3) * tcr.tcr_order_descriptor(n=n, mode=mode)["launches"]
+        gbps = nbytes / us / 1e3
+        return {"us": round(us, 2), "gbps": round(gbps, 1), "frac": round(gbps / peak, 4),
+                "frac_of_read_ceiling": round(gbps / ceiling_gbps, 4)}
+
+    res = {}
+    # 2^20: 2 MiB, resident in L2 unless flushed.  Writing 640 MiB (about 5x
+    # L2) evicts it; reading 256 MiB afterwards replaces the dirty lines that
+    # write leaves with clean ones, so the timed call does not wait behind
+    # their write-back.  The flush keeps the GPU busy while the call is
+    # enqueued, so the events see device time only.
+    n1 = 1 << 20
+    x1 = torch.from_numpy(synth.generate(n1, "uniform_pm1", synth.F16, seed=0).view(np.int16)).to(device)
+    wbuf = torch.empty(640 << 18, dtype=torch.float32, device=device)
+    rbuf = torch.ones(1 << 26, dtype=torch.float32, device=device)
+
+    def flush():
+        wbuf.zero_()
+        rbuf.sum()
+
+    c1 = {}
+    for kind in (tcr.MMA_CHAIN, tcr.FIXED_ORDER, tcr.SHUFFLE_TREE, tcr.MMA_CHAIN_TMEM):
+        m = tcr.Mode(kind, R=4 if kind in (tcr.MMA_CHAIN, tcr.MMA_CHAIN_TMEM) else 0)
+        us = timed_median_us(lambda m=m: tcr.tcr_reduce_sum(x1, m, out=out), iters, 3, flush)
+        c1[tcr.KIND_NAMES[kind]] = entry(2 * n1 + 4, us, m, n1)
+        c1[tcr.KIND_NAMES[kind]]["launches"] = tcr.tcr_order_descriptor(n=n1, mode=m)["launches"]
+    res["sum_2p20_f16"] = {"input": "2^20 fp16 U[-1,1) seed 0", "calls": c1,
+                           "l2": "flushed before every call: 640 MiB written, then 256 MiB read, "
+                                 "outside the timed events",
+                           "statistic": f"median of {iters}"}
+    del x1, wbuf, rbuf
+    torch.cuda.empty_cache()
+
+    n2 = 1 << 28
+    x2 = torch.from_numpy(synth.generate(n2, "uniform01", synth.F16, seed=1).view(np.int16)).to(device)
+    points = [(tcr.SHUFFLE_TREE, 0, b) for b in (32, 128, 256, 1024)]
+    points += [(tcr.FIXED_ORDER, 0, b) for b in (32, 128, 256, 1024)]
+    points += [(tcr.MMA_CHAIN, R, b) for R in (1, 2, 4, 5) for b in (32, 128, 256, 1024)]
+    points += [(tcr.MMA_CHAIN_TMEM, R, 0) for R in (1, 2, 4, 5, 8)]
+    sweep = []
+    for kind, R, b in points:
+        m = tcr.Mode(kind, R=R, block_threads=b)
+        us = timed_median_us(lambda m=m: tcr.tcr_reduce_sum(x2, m, out=out), iters, 3)
+        e = entry(2 * n2 + 4, us, m, n2)
+        e.update({"kind": tcr.KIND_NAMES[kind], "R": R, "block": b})
+        sweep.append(e)
+    res["sum_2p28_f16_sweep"] = {"input": "2^28 fp16 U[0,1) seed 1, 512 MiB (larger than L2)",
+                                 "points": sweep, "statistic": f"median of {iters}"}
+    del x2
+    torch.cuda.empty_cache()
+
+    n4 = 1 << 29
+    x4 = torch.from_numpy(synth.generate(n4, "pow2", synth.BF16, seed=3).view(np.int16)).to(device)
+    c4 = {}
+    for kind in (tcr.MMA_CHAIN, tcr.MMA_CHAIN_TMEM, tcr.FIXED_ORDER, tcr.SHUFFLE_TREE):
+        m = tcr.Mode(kind, dtype=tcr.BF16)
+        us = timed_median_us(lambda m=m: tcr.tcr_reduce_sum(x4, m, out=out), iters, 3)
+        c4[tcr.KIND_NAMES[kind]] = entry(2 * n4 + 4, us, m, n4)
+    res["sum_2p29_bf16"] = {"input": "2^29 bf16 +-2^e, e in [-20, 10], seed 3, 1 GiB", "calls": c4,
+                            "statistic": f"median of {iters}"}
+    del x4
+    torch.cuda.empty_cache()
+    res["launches"] = launches
+    return res
+
+
 # ------------------------------------------------------------ CPU oracle
 
 def oracle_pass(xs_sample, xr_sample, threads: int):
@@ -363,16 +504,23 @@ def cpu_samples(xs, xr, budget_s: float, threads: int):
 
 
 def cpu_baseline(xs, xr, budget_s: float = 10.0):
+    """The oracle on all host cores and on one, each on a sample sized for
+    about budget_s seconds."""
     import oracle
-    threads = oracle.default_threads()
-    s, r = cpu_samples(xs, xr, budget_s, threads)
-    t = time.perf_counter()
-    nbytes = oracle_pass(s, r, threads)
-    dt = time.perf_counter() - t
-    return {"value": round(nbytes / dt / 1e9, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": f"first {s.size} of the 2^30 sum inputs and first {r.shape[0]} of the 65536 "
-                      f"rows; exact sum, fixed-order tree and shuffle-tree emulation of each",
-            "seconds": round(dt, 3)}
+    legs = []
+    for threads in (oracle.default_threads(), 1):
+        s, r = cpu_samples(xs, xr, budget_s, threads)
+        t = time.perf_counter()
+        nbytes = oracle_pass(s, r, threads)
+        dt = time.perf_counter() - t
+        legs.append({"value": round(nbytes / dt / 1e9, 4), "unit": UNIT, "cores": threads,
+                     "kind": "oracle",
+                     "sample": f"first {s.size} of the 2^30 sum inputs and first {r.shape[0]} of the "
+                               f"65536 rows; exact sum, fixed-order tree and shuffle-tree emulation of each",
+                     "seconds": round(dt, 3)})
+    line = legs[0]
+    line["single_thread"] = legs[1]
+    return line
 
 
 # ------------------------------------------------------------ arms
@@ -745,10 +893,13 @@ def main():
     clocks = ClockSampler(uuid)
     clocks.start()
     total_s, per_call_ms = time_device(calls, args.steps, args.warmup, world)
+    ceiling = read_ceiling(x_sum)
     e2e_steps = args.e2e_steps or max(3, args.steps // 40)
     del x_sum, x_rows, calls
     torch.cuda.empty_cache()
     e2e_s, h2d, d2h = time_e2e(xs, xr, build_calls, e2e_steps, world)
+    torch.cuda.empty_cache()
+    configs = time_configs(args, device, ceiling["gbps"])
     clk = clocks.stop()
 
     meta = build_calls_meta()
@@ -761,12 +912,17 @@ def main():
 
     calls_out = {}
     for (name, nbytes, launches), ms in zip(meta, per_call_ms):
+        med_us = statistics.median(ms) * 1e3
         avg_us = statistics.fmean(ms) * 1e3
-        gbps = nbytes / avg_us / 1e3
-        calls_out[name] = {"us": round(avg_us, 2), "gbps": round(gbps, 1),
-                           "gelem_per_s": round(call_elements(name) / avg_us / 1e3, 1),
-                           "frac": round(gbps / peak, 4), "launches": launches}
-    dom = max(calls_out, key=lambda k: calls_out[k]["us"])
+        gbps = nbytes / med_us / 1e3
+        calls_out[name] = {"us": round(med_us, 2), "us_mean": round(avg_us, 2), "gbps": round(gbps, 1),
+                           "gelem_per_s": round(call_elements(name) / med_us / 1e3, 1),
+                           "frac": round(gbps / peak, 4),
+                           "frac_of_read_ceiling": round(gbps / ceiling["gbps"], 4),
+                           "launches": launches}
+    dom = max(calls_out, key=lambda k: calls_out[k]["us_mean"])
+    dom_nbytes = dict((m[0], m[1]) for m in meta)[dom]
+    dom_gbps = dom_nbytes / calls_out[dom]["us_mean"] / 1e3
     elements_per_step = sum(call_elements(m[0]) for m in meta)
     launches = sum(m[2] for m in meta) * args.steps
 
@@ -784,6 +940,8 @@ def main():
                    "mma_chain_R": tcr.tcr_order_descriptor(n=N_SUM, mode=tcr.Mode(tcr.MMA_CHAIN))["chain_R"]},
         "frac_of_peak": round(value / world / peak, 4),
         "peak_gbs": peak, "peak_source": peak_src,
+        "read_ceiling": ceiling,
+        "frac_of_read_ceiling": round(value / world / ceiling["gbps"], 4),
         "gelem_per_s": round(elements_per_step * args.steps * world / max_s / 1e9, 1),
         "calls": calls_out,
         # page 1 reports about 3.2x for its tensor-core reduction over a
@@ -791,13 +949,16 @@ def main():
         "mma_chain_over_shuffle_tree": round(calls_out["sum/SHUFFLE_TREE"]["us"] /
                                              calls_out["sum/MMA_CHAIN"]["us"], 3),
         "roofline": {"bound": "hbm", "kernel": KERNEL_OF[dom], "call": dom,
-                     "achieved": calls_out[dom]["gbps"], "peak": peak, "unit": "GB/s",
-                     "frac": calls_out[dom]["frac"], "traffic": recorded_traffic(KERNEL_OF[dom]),
-                     "duration": "whole call (reduction + combine launch)",
-                     "peak_source": peak_src},
+                     "achieved": round(dom_gbps, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(dom_gbps / peak, 4), "traffic": recorded_traffic(KERNEL_OF[dom]),
+                     "duration": "mean of the timed calls, whole call (reduction + combine launch)",
+                     "peak_source": peak_src,
+                     "read_ceiling": ceiling["gbps"],
+                     "frac_of_read_ceiling": round(dom_gbps / ceiling["gbps"], 4)},
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "gpu_launches": launches,
+        "configs": configs,
         "clocks": clk,
         "cpu_baseline": cpu,
     }

@@ -440,6 +440,23 @@ TCR_API tcr_status tcr_gemm_splitk(const void *A, const void *W, float *C, size_
 #define TCR_FAULT_PIPELINE_WAIT 1u
 TCR_API tcr_status tcr_device_faults(unsigned int *flags, int clear);
 
+/*
+ * tcr_read_probe -- a measurement aid, not part of the reduction method:
+ * the read ceiling of the current GPU.  A kernel streams `bytes` bytes at x
+ * in with the reduction kernels' 16-byte streaming loads (eight in flight
+ * per thread) and writes the XOR of all their 32-bit words to *out (so the
+ * loads cannot be optimised away); time it to learn what a read-only kernel
+ * reaches on this GPU, beside the copy bandwidth that counts a read and a
+ * write.  x: device pointer, 16-byte aligned; bytes a multiple of 16; out:
+ * device word, 4-byte aligned (set to 0 first, on the stream, so the call is
+ * a memset and one kernel launch).  Grid: ctas_per_sm CTAs (0: as many as
+ * fit) of block_threads threads (0: 512; else a power of two in 32..1024)
+ * on every SM.  TCR_ERR_INVALID_ARG on a bad argument, TCR_ERR_CUDA if the
+ * device cannot be queried or the launch fails.  Asynchronous.
+ */
+TCR_API tcr_status tcr_read_probe(const void *x, size_t bytes, unsigned int *out, int ctas_per_sm,
+                                  int block_threads, void *stream);
+
 /* Static English text for a status code; never NULL. */
 TCR_API const char *tcr_status_string(tcr_status status);
 
