@@ -141,9 +141,9 @@ def test_past_2p32_inputs():
     # from a misaligned base, through the realigning loads
     e1 = exact_f32(x[1:], F16)
     assert sum_bits(t[1:], tcr.Mode(MMA)) == bits_of(e1)
-    # as 65537 rows of 65536 (rows through the chunked kernels, row offsets
+    # as 65536 rows of 65536 (rows through the chunked kernels, row offsets
     # past 2^32 bytes)
-    rows, cols = 65537, 65536
+    rows, cols = 65536, 65536
     xr = x[:rows * cols].reshape(rows, cols)
     er = exact_rows_f32(xr, F16)
     for kind in (MMA, TMEM):
