@@ -469,7 +469,11 @@ __device__ __forceinline__ void mean_var_of(float s1, float s2, size_t n, float 
 // Programmatic dependent launch: a producing kernel lets the next kernel
 // on the stream start launching; the consumer waits until the producer has
 // completed and its writes are visible.  Both are no-ops for a kernel
-// launched without the attribute.
+// launched without the attribute.  Every kernel of the library triggers its
+// dependents as it starts, and every kernel launched with the attribute
+// (a call's first kernel, its combines) waits before its first global
+// memory access -- the wait covers the kernel before it on the stream,
+// whichever it is.
 __device__ __forceinline__ void pdl_launch_dependents()
 {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

@@ -37,6 +37,7 @@ blocked_chunk_kernel(const void *__restrict__ xv, size_t seg_len, size_t units, 
                      int chunk_log2, int run_log2, float *__restrict__ dst)
 {
     pdl_launch_dependents();   // the combine may launch now; it waits for this grid to finish
+    pdl_wait_primary();        // the stream's previous kernel has finished
     using T = typename Elem<DT>::T;
     constexpr int V = Elem<DT>::kPerVec;
     constexpr int LV = V == 8 ? 3 : 2;
@@ -145,8 +146,7 @@ cudaError_t launch_blocked_chunk(int dtype, bool aligned, const void *x, size_t 
     if (!k || block < 32 || block > 32 * kBlockedMaxWarps) return cudaErrorInvalidValue;
     void *args[] = {(void *)&x, (void *)&seg_len, (void *)&units, (void *)&cps,
                     (void *)&chunk_log2, (void *)&run_log2, (void *)&dst};
-    return cudaLaunchKernel(k, dim3(grid), dim3(block), args, kStageBytesPerWarp * (block / 32),
-                            stream);
+    return launch_first(k, dim3(grid), dim3(block), args, kStageBytesPerWarp * (block / 32), stream);
 }
 
 int occupancy_blocked(int dtype, bool aligned, int block)

@@ -43,6 +43,7 @@ combine_kernel(const float *__restrict__ partials, size_t count, float *__restri
 {
     __shared__ float warp_val[32];
     // the partials are written by the kernel launched just before this one
+    pdl_launch_dependents();   // the next call's first kernel may launch; it waits for this one
     pdl_wait_primary();
     const float *p = partials + (size_t)blockIdx.x * count;
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
@@ -83,6 +84,7 @@ __global__ void __launch_bounds__(256)
 combine_rows_kernel(const float *__restrict__ partials, size_t segments, size_t count,
                     float *__restrict__ out)
 {
+    pdl_launch_dependents();   // the next call's first kernel may launch; it waits for this one
     pdl_wait_primary();
     const size_t r = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (r >= segments) return;

@@ -82,7 +82,7 @@ cudaError_t launch_fixed_chunk(int dtype, int op, bool aligned, const void *x, s
     if (!k) return cudaErrorInvalidValue;
     void *args[] = {(void *)&x, (void *)&seg_len, (void *)&units, (void *)&cps,
                     (void *)&chunk_log2, (void *)&dst};
-    return cudaLaunchKernel(k, dim3(grid), dim3(block), args, 0, stream);
+    return launch_first(k, dim3(grid), dim3(block), args, 0, stream);
 }
 
 cudaError_t launch_fixed_rows_warp(int dtype, int op, bool aligned, const void *x, size_t rows,
@@ -92,7 +92,7 @@ cudaError_t launch_fixed_rows_warp(int dtype, int op, bool aligned, const void *
     const void *k = pick(true, dtype, op, aligned, vrun);
     if (!k) return cudaErrorInvalidValue;
     void *args[] = {(void *)&x, (void *)&rows, (void *)&cols, (void *)&out};
-    return cudaLaunchKernel(k, dim3(grid), dim3(block), args, 0, stream);
+    return launch_first(k, dim3(grid), dim3(block), args, 0, stream);
 }
 
 cudaError_t preload_fixed_chunk_sums()

@@ -164,6 +164,9 @@ gemm_splitk_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constan
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
+    // the set-up above ran beside the stream's previous kernel; global
+    // memory is touched only after it has finished
+    pdl_wait_primary();
 
     if (warp == 0) {
         // ---------------- producer
@@ -331,6 +334,7 @@ gemm_splitk_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constan
 __global__ void splitk_combine_kernel(const float *__restrict__ P, size_t mn, int splits,
                                       float *__restrict__ C)
 {
+    pdl_launch_dependents();
     pdl_wait_primary();
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < mn;
          i += (size_t)gridDim.x * blockDim.x) {
@@ -384,7 +388,7 @@ cudaError_t launch_gemm_splitk(int dtype, const void *A, const void *W, size_t M
     g.out = out;
     g.inject_stall = inject_stall ? 1u : 0u;
     void *args[] = {(void *)&ma, (void *)&mw, (void *)&g};
-    return cudaLaunchKernel(k, dim3(grid), dim3(kGmThreads), args, kGmSmemBytes, stream);
+    return launch_first(k, dim3(grid), dim3(kGmThreads), args, kGmSmemBytes, stream);
 }
 
 cudaError_t launch_splitk_combine(const float *P, size_t mn, int splits, float *C, cudaStream_t stream)

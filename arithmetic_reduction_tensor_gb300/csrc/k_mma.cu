@@ -90,7 +90,7 @@ cudaError_t launch_mma_chunk(int dtype, int op, bool aligned, int R, const void 
     if (!k) return cudaErrorInvalidValue;
     void *args[] = {(void *)&x, (void *)&seg_len, (void *)&units, (void *)&cps,
                     (void *)&chunk_log2, (void *)&dst};
-    return cudaLaunchKernel(k, dim3(grid), dim3(block), args, 0, stream);
+    return launch_first(k, dim3(grid), dim3(block), args, 0, stream);
 }
 
 cudaError_t launch_mma_rows(int dtype, int op, bool aligned, int R, const void *x, size_t rows,
@@ -99,7 +99,7 @@ cudaError_t launch_mma_rows(int dtype, int op, bool aligned, int R, const void *
     void *k = pick(true, dtype, op, aligned, R);
     if (!k) return cudaErrorInvalidValue;
     void *args[] = {(void *)&x, (void *)&rows, (void *)&cols, (void *)&out};
-    return cudaLaunchKernel(k, dim3(grid), dim3(block), args, 0, stream);
+    return launch_first(k, dim3(grid), dim3(block), args, 0, stream);
 }
 
 cudaError_t preload_mma_chunk_sums()

@@ -57,6 +57,7 @@ shuffle_block_pair_kernel(const void *__restrict__ xv, size_t seg_len, int G,
                           float *__restrict__ dst_a, float *__restrict__ dst_b)
 {
     pdl_launch_dependents();   // the combine may launch now; it waits for this grid to finish
+    pdl_wait_primary();        // the stream's previous kernel has finished
     using T = typename Elem<DT>::T;
     constexpr int V = Elem<DT>::kPerVec;
     constexpr int U = 4;
@@ -120,6 +121,7 @@ __global__ void mean_var_kernel(const float *__restrict__ s1, const float *__res
                                 size_t rows, size_t cols, float *__restrict__ mean,
                                 float *__restrict__ var)
 {
+    pdl_launch_dependents();
     pdl_wait_primary();
     for (size_t r = (size_t)blockIdx.x * blockDim.x + threadIdx.x; r < rows;
          r += (size_t)gridDim.x * blockDim.x) {
@@ -169,7 +171,7 @@ cudaError_t launch_rows_pair(int family, int dtype, bool aligned, int R, const v
     if (!k) return cudaErrorInvalidValue;
     void *args[] = {(void *)&x, (void *)&rows, (void *)&cols, (void *)&out_a, (void *)&out_b,
                     (void *)&mean_var};
-    return cudaLaunchKernel(k, dim3(grid), dim3(block), args, 0, stream);
+    return launch_first(k, dim3(grid), dim3(block), args, 0, stream);
 }
 
 cudaError_t launch_chunk_pair(int family, int dtype, bool aligned, int R, const void *x,
@@ -183,7 +185,7 @@ cudaError_t launch_chunk_pair(int family, int dtype, bool aligned, int R, const 
     if (!k) return cudaErrorInvalidValue;
     void *args[] = {(void *)&x, (void *)&seg_len, (void *)&units, (void *)&cps,
                     (void *)&chunk_log2, (void *)&dst_a, (void *)&dst_b};
-    return cudaLaunchKernel(k, dim3(grid), dim3(block), args, 0, stream);
+    return launch_first(k, dim3(grid), dim3(block), args, 0, stream);
 }
 
 cudaError_t launch_shuffle_block_pair(int dtype, bool aligned, const void *x, size_t seg_len,
@@ -193,7 +195,7 @@ cudaError_t launch_shuffle_block_pair(int dtype, bool aligned, const void *x, si
     const void *k = pick(3, dtype, aligned);
     if (!k) return cudaErrorInvalidValue;
     void *args[] = {(void *)&x, (void *)&seg_len, (void *)&G, (void *)&dst_a, (void *)&dst_b};
-    return cudaLaunchKernel(k, dim3((unsigned)(segments * (size_t)G)), dim3(block), args, 0, stream);
+    return launch_first(k, dim3((unsigned)(segments * (size_t)G)), dim3(block), args, 0, stream);
 }
 
 cudaError_t launch_mean_var(const float *s1, const float *s2, size_t rows, size_t cols, float *mean,

@@ -68,7 +68,7 @@ cudaError_t launch_mma_rows_pair(int dtype, bool aligned, int R, const void *x, 
     if (!k) return cudaErrorInvalidValue;
     void *args[] = {(void *)&x, (void *)&rows, (void *)&cols, (void *)&out_a, (void *)&out_b,
                     (void *)&mean_var};
-    return cudaLaunchKernel(k, dim3(grid), dim3(block), args, 0, stream);
+    return launch_first(k, dim3(grid), dim3(block), args, 0, stream);
 }
 
 cudaError_t launch_mma_chunk_pair(int dtype, bool aligned, int R, const void *x, size_t seg_len,
@@ -79,7 +79,7 @@ cudaError_t launch_mma_chunk_pair(int dtype, bool aligned, int R, const void *x,
     if (!k) return cudaErrorInvalidValue;
     void *args[] = {(void *)&x, (void *)&seg_len, (void *)&units, (void *)&cps,
                     (void *)&chunk_log2, (void *)&dst_a, (void *)&dst_b};
-    return cudaLaunchKernel(k, dim3(grid), dim3(block), args, 0, stream);
+    return launch_first(k, dim3(grid), dim3(block), args, 0, stream);
 }
 
 }  // namespace tcr

@@ -57,7 +57,7 @@ cudaError_t launch_packed_rows(int family, int dtype, int op, int R, bool aligne
     float *none = nullptr;
     int mv = 0;
     void *args[] = {(void *)&x, (void *)&rows, (void *)&cols, (void *)&out, (void *)&none, (void *)&mv};
-    return cudaLaunchKernel(k, dim3(grid), dim3(block), args, 0, stream);
+    return launch_first(k, dim3(grid), dim3(block), args, 0, stream);
 }
 
 cudaError_t launch_packed_rows_pair(int family, int dtype, int R, bool aligned, const void *x,
@@ -68,7 +68,7 @@ cudaError_t launch_packed_rows_pair(int family, int dtype, int R, bool aligned, 
     if (!k || block != kRowsBlock) return cudaErrorInvalidValue;
     void *args[] = {(void *)&x, (void *)&rows, (void *)&cols, (void *)&out_a, (void *)&out_b,
                     (void *)&mean_var};
-    return cudaLaunchKernel(k, dim3(grid), dim3(block), args, 0, stream);
+    return launch_first(k, dim3(grid), dim3(block), args, 0, stream);
 }
 
 int occupancy_packed(int family, int dtype, int op, int R, int vlog, bool aligned, bool pair)

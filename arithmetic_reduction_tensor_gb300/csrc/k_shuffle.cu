@@ -163,6 +163,7 @@ __global__ void __launch_bounds__(1024)
 shuffle_block_kernel(const void *__restrict__ xv, size_t seg_len, int G, float *__restrict__ dst)
 {
     pdl_launch_dependents();   // the combine may launch now; it waits for this grid to finish
+    pdl_wait_primary();        // the stream's previous kernel has finished
     using T = typename Elem<DT>::T;
     __shared__ float warp_val[32];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
@@ -238,8 +239,7 @@ cudaError_t launch_shuffle_block(int dtype, int op, bool aligned, const void *x,
     const void *k = pick(false, dtype, op, aligned);
     if (!k) return cudaErrorInvalidValue;
     void *args[] = {(void *)&x, (void *)&seg_len, (void *)&G, (void *)&dst};
-    return cudaLaunchKernel(k, dim3((unsigned)(segments * (size_t)G)), dim3(block), args, 0,
-                            stream);
+    return launch_first(k, dim3((unsigned)(segments * (size_t)G)), dim3(block), args, 0, stream);
 }
 
 cudaError_t launch_shuffle_rows_warp(int dtype, int op, bool aligned, const void *x, size_t rows,
@@ -249,7 +249,7 @@ cudaError_t launch_shuffle_rows_warp(int dtype, int op, bool aligned, const void
     const void *k = pick(true, dtype, op, aligned);
     if (!k) return cudaErrorInvalidValue;
     void *args[] = {(void *)&x, (void *)&rows, (void *)&cols, (void *)&out};
-    return cudaLaunchKernel(k, dim3(grid), dim3(block), args, 0, stream);
+    return launch_first(k, dim3(grid), dim3(block), args, 0, stream);
 }
 
 int occupancy_shuffle(bool rows, int dtype, int op, bool aligned, int block)

@@ -53,13 +53,18 @@ constexpr int kTcDBuffers = 8;                      // chains the MMA may run ah
 constexpr uint32_t kTcDBufferStride = 32;           // columns per D buffer (N = 16 used)
 constexpr uint32_t kTcTmemCols = kTcDBuffers * kTcDBufferStride;    // 256
 
+constexpr uint32_t kTcClcSlots = 16;                // cancellation responses in flight
+constexpr uint32_t kTcRecent = 32;                  // units the producer remembers (abort path)
+
 // Dynamic shared memory layout (offsets from a 1024-byte aligned base).
 constexpr int kTcOffRing = 0;
 constexpr int kTcOffOnes = kTcOffRing + kTcStages * kTcStageBytes;     // 512 B of ones
+constexpr int kTcOffClc = kTcOffOnes + 512;                             // 16 B per response
 constexpr int kTcOffBars = kTcOffOnes + 1024;
-// barriers: full[S], empty[S], dfull[B], dempty[B], drain
-constexpr int kTcNumBars = 2 * kTcStages + 2 * kTcDBuffers + 1;
-constexpr int kTcOffMisc = kTcOffBars + 8 * kTcNumBars;                 // tmem addr, abort, red[4]
+static_assert(512 + 16 * kTcClcSlots <= 1024, "responses fit beside the ones");
+// barriers: full[S], empty[S], dfull[B], dempty[B], drain, clc_full[C], clc_empty[C]
+constexpr int kTcNumBars = 2 * kTcStages + 2 * kTcDBuffers + 1 + 2 * kTcClcSlots;
+constexpr int kTcOffMisc = kTcOffBars + 8 * kTcNumBars;     // tmem addr, abort, red[4], next unit
 constexpr int kTcSmemBytes = kTcOffMisc + 64 + 1024;                    // + alignment slack
 
 __device__ unsigned int g_tc05_fault;               // non-zero once any wait gave up
@@ -130,8 +135,8 @@ __device__ __forceinline__ int unit_tiles(size_t n, size_t u, int unit_log2)
 
 template <int DT, int R>
 __global__ void __launch_bounds__(kTcThreads, 1)
-mma_tmem_kernel(const uint16_t *__restrict__ x, size_t n, size_t units, int unit_log2,
-                float *__restrict__ dst, uint32_t inject_stall)
+mma_tmem_kernel(const uint16_t *__restrict__ x, size_t n, int unit_log2, float *__restrict__ dst,
+                uint32_t inject_stall)
 {
     pdl_launch_dependents();   // the combine may launch now; it waits for this grid to finish
     extern __shared__ uint8_t smem_raw[];
@@ -145,10 +150,16 @@ mma_tmem_kernel(const uint16_t *__restrict__ x, size_t n, size_t units, int unit
     auto dfull_bar = [&](int b) { return bars + 8u * (uint32_t)(2 * kTcStages + b); };
     auto dempty_bar = [&](int b) { return bars + 8u * (uint32_t)(2 * kTcStages + kTcDBuffers + b); };
     const uint32_t drain_bar = bars + 8u * (uint32_t)(2 * kTcStages + 2 * kTcDBuffers);
+    auto clc_full_bar = [&](uint32_t k) { return drain_bar + 8u * (1u + k % kTcClcSlots); };
+    auto clc_empty_bar = [&](uint32_t k) { return drain_bar + 8u * (1u + kTcClcSlots + k % kTcClcSlots); };
+    auto clc_resp = [&](uint32_t k) { return sbase + kTcOffClc + 16u * (k % kTcClcSlots); };
+    auto clc_parity = [](uint32_t k) { return (k / kTcClcSlots) & 1u; };
     uint32_t *misc = (uint32_t *)(smem + kTcOffMisc);
     volatile uint32_t *tmem_holder = misc;
     volatile uint32_t *abort = misc + 1;
     float *red = (float *)(misc + 4);
+    volatile uint32_t *next_unit = misc + 8;       // the epilogue's next unit, or
+    volatile uint32_t *more_units = misc + 9;      // none (more_units == 0)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -168,6 +179,10 @@ mma_tmem_kernel(const uint16_t *__restrict__ x, size_t n, size_t units, int unit
             mbar_init(dempty_bar(b), kTcEpilogueThreads);
         }
         mbar_init(drain_bar, 1);
+        for (uint32_t k = 0; k < kTcClcSlots; k++) {
+            mbar_init(clc_full_bar(k), 1);
+            mbar_init(clc_empty_bar(k), 2);        // the MMA issuer and the epilogue
+        }
         *abort = 0u;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -183,7 +198,14 @@ mma_tmem_kernel(const uint16_t *__restrict__ x, size_t n, size_t units, int unit
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
+    // the set-up above ran beside the stream's previous kernel; global
+    // memory is touched only after it has finished
+    pdl_wait_primary();
 
+    // The CTA's k-th unit is blockIdx.x for k = 0, then the CTA the k-th
+    // cancellation request took over (one CTA of the grid per unit): each
+    // role walks the same sequence, reading response k - 1 from slot
+    // (k - 1) mod kTcClcSlots once its unit k - 1 is done.
     if (warp == 0) {
         // ---------------- producer
         if (lane == 0) {
@@ -196,16 +218,33 @@ mma_tmem_kernel(const uint16_t *__restrict__ x, size_t n, size_t units, int unit
                 armed[i] = false;
                 armed_phase[i] = 0;
             }
-            for (size_t u = blockIdx.x; u < units && !*abort; u += gridDim.x) {
+            uint32_t recent[kTcRecent];     // the last units started, for the abort path
+            uint32_t u = blockIdx.x, k = 0;
+            bool asked = false;             // request k is in flight
+            // request k: asked while unit k's last stage streams in, so that
+            // the unit taken over is claimed as late as the pipeline allows
+            auto ask = [&]() -> bool {
+                if (!mbar_wait(clc_empty_bar(k), clc_parity(k) ^ 1u, abort)) return false;
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                mbar_arrive_expect_tx(clc_full_bar(k), 16);
+                clc_try_cancel(clc_resp(k), clc_full_bar(k));
+                asked = true;
+                return true;
+            };
+            for (;;) {
+                recent[k % kTcRecent] = u;
                 const int tiles = unit_tiles(n, u, unit_log2);
-                const uint16_t *src = x + (u << unit_log2);
-                for (int t0 = 0; t0 < tiles; t0 += kTcTilesPerStage) {
-                    const int nt = min(kTcTilesPerStage, tiles - t0);
-                    if (!mbar_wait(empty_bar(s), phase ^ 1u, abort)) break;
+                const int stages = (tiles + kTcTilesPerStage - 1) / kTcTilesPerStage;
+                const uint16_t *src = x + ((size_t)u << unit_log2);
+                bool ok = stages > 0 || ask();
+                for (int st = 0; st < stages && ok; st++) {
+                    if (st == stages - 1 && !(ok = ask())) break;
+                    if (!(ok = mbar_wait(empty_bar(s), phase ^ 1u, abort))) break;
+                    const int nt = min(kTcTilesPerStage, tiles - st * kTcTilesPerStage);
                     const uint32_t bytes = (uint32_t)nt * kTcTileBytes;
                     mbar_arrive_expect_tx(full_bar(s), bytes);
-                    bulk_copy_g2s(ring + (uint32_t)s * kTcStageBytes, src + (size_t)t0 * kTcTileInputs,
-                                  bytes, full_bar(s));
+                    bulk_copy_g2s(ring + (uint32_t)s * kTcStageBytes,
+                                  src + (size_t)st * kTcTilesPerStage * kTcTileInputs, bytes, full_bar(s));
                     armed[s] = true;
                     armed_phase[s] = phase;
                     if (++s == kTcStages) {
@@ -213,16 +252,37 @@ mma_tmem_kernel(const uint16_t *__restrict__ x, size_t n, size_t units, int unit
                         phase ^= 1u;
                     }
                 }
+                if (!ok || !mbar_wait(clc_full_bar(k), clc_parity(k), abort)) break;
+                asked = false;
+                uint32_t next;
+                if (!clc_query(clc_resp(k), &next)) break;
+                u = next;
+                k++;
             }
             if (*abort) {
                 // let the copies already issued land before the CTA exits
 #pragma unroll
-                for (int i = 0; i < kTcStages; i++) {
-                    if (!armed[i]) continue;
-                    const uint64_t t0 = global_ns();
-                    while (!mbar_try_wait(full_bar(i), armed_phase[i]) &&
-                           global_ns() - t0 < kWaitLimitNs) {
-                    }
+                for (int i = 0; i < kTcStages; i++)
+                    if (armed[i]) (void)mbar_wait_limited(full_bar(i), armed_phase[i]);
+                // the units started may lack a partial (the epilogue stops at
+                // the failed unit): mark them NaN -- a finished one among them
+                // may lose its value, the sum is NaN either way
+                const float nan = __int_as_float(0x7fc00000);
+                for (uint32_t j = 0; j < kTcRecent && j <= k; j++) dst[recent[(k - j) % kTcRecent]] = nan;
+                // take over every CTA still waiting to launch and mark its unit
+                if (!asked) {
+                    mbar_arrive_expect_tx(clc_full_bar(k), 16);
+                    clc_try_cancel(clc_resp(k), clc_full_bar(k));
+                }
+                for (;;) {
+                    uint32_t v;
+                    if (!mbar_wait_limited(clc_full_bar(k), clc_parity(k)) || !clc_query(clc_resp(k), &v))
+                        break;
+                    dst[v] = nan;
+                    k++;
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    mbar_arrive_expect_tx(clc_full_bar(k), 16);
+                    clc_try_cancel(clc_resp(k), clc_full_bar(k));
                 }
             }
         }
@@ -245,102 +305,70 @@ mma_tmem_kernel(const uint16_t *__restrict__ x, size_t n, size_t units, int unit
                 tc_fence_after();
                 return true;
             };
-            // A host-requested stall leaves the first chain unpublished, so
+            // A host-requested stall leaves the first stage's last chain
+            // unpublished (the epilogue waits for a stage's last chain), so
             // the epilogue's wait runs out its limit (failure-path test).
             bool withhold = inject_stall != 0u;
-            auto end_chain = [&]() {
-                if (withhold)
+            auto end_chain = [&](bool ends_stage) {
+                if (withhold && ends_stage)
                     withhold = false;
                 else
                     tc_commit(dfull_bar(b));      // chain sub-result ready
                 dphase ^= 1u << b;
                 if (++b == kTcDBuffers) b = 0;
             };
-            if constexpr (kTcTilesPerStage % R == 0) {
-                // R divides a stage: chains fall on stage boundaries, the
-                // whole-stage issue has static boundaries
-                for (size_t u = blockIdx.x; u < units && !*abort; u += gridDim.x) {
-                    const int tiles = unit_tiles(n, u, unit_log2);
-                    int in_chain = 0;
-                    for (int t0 = 0; t0 < tiles && !*abort; t0 += kTcTilesPerStage) {
-                        const int nt = min(kTcTilesPerStage, tiles - t0);
-                        if (!mbar_wait(full_bar(s), phase, abort)) break;
-                        tc_fence_after();
-                        const uint64_t sdesc = ring_desc + (uint64_t)s * kStageStep;
-                        bool ok = true;
-                        if (kTcTilesPerStage % R == 0 && nt == kTcTilesPerStage) {
-                            // whole stage, chains aligned to it: static boundaries
+            // one unit's MMAs: chains of R, each ending with its stage
+            // (when R divides a stage they fall on stage boundaries anyway);
+            // a whole stage is issued with static chain boundaries -- MMAs
+            // issued under run-time chain logic issue several times slower
+            auto unit_mmas = [&](int tiles) -> bool {
+                bool ok = true;
+                for (int t0 = 0; t0 < tiles && ok; t0 += kTcTilesPerStage) {
+                    const int nt = min(kTcTilesPerStage, tiles - t0);
+                    if (!mbar_wait(full_bar(s), phase, abort)) return false;
+                    tc_fence_after();
+                    const uint64_t sdesc = ring_desc + (uint64_t)s * kStageStep;
+                    if (nt == kTcTilesPerStage) {
 #pragma unroll
-                            for (int t = 0; t < kTcTilesPerStage; t++) {
-                                if (t % R == 0 && !(ok = begin_chain())) break;
-                                tc_mma(tmem + (uint32_t)b * kTcDBufferStride, sdesc + (uint64_t)t * kTileStep,
-                                       b_desc, idesc, t % R != 0 ? 1u : 0u);
-                                if (t % R == R - 1) end_chain();
-                            }
-                        } else {
-                            for (int t = 0; t < nt; t++) {
-                                if (in_chain == 0 && !(ok = begin_chain())) break;
-                                tc_mma(tmem + (uint32_t)b * kTcDBufferStride, sdesc + (uint64_t)t * kTileStep,
-                                       b_desc, idesc, in_chain > 0 ? 1u : 0u);
-                                if (++in_chain == R || t0 + t + 1 == tiles) {
-                                    end_chain();
-                                    in_chain = 0;
-                                }
-                            }
+                        for (int t = 0; t < kTcTilesPerStage; t++) {
+                            if (t % R == 0 && !(ok = begin_chain())) break;
+                            tc_mma(tmem + (uint32_t)b * kTcDBufferStride, sdesc + (uint64_t)t * kTileStep,
+                                   b_desc, idesc, t % R != 0 ? 1u : 0u);
+                            if (t % R == R - 1 || t == kTcTilesPerStage - 1)
+                                end_chain(t == kTcTilesPerStage - 1);
                         }
-                        tc_commit(empty_bar(s));                  // stage may be refilled
-                        if (++s == kTcStages) {
-                            s = 0;
-                            phase ^= 1u;
-                        }
-                        if (!ok) break;
-                    }
-                }
-            } else {
-                // chains end with their stage (R does not divide it)
-                for (size_t u = blockIdx.x; u < units && !*abort; u += gridDim.x) {
-                    const int tiles = unit_tiles(n, u, unit_log2);
-                    bool ok = true;
-                    for (int t0 = 0; t0 < tiles && ok; t0 += kTcTilesPerStage) {
-                        const int nt = min(kTcTilesPerStage, tiles - t0);
-                        if (!mbar_wait(full_bar(s), phase, abort)) break;
-                        tc_fence_after();
-                        const uint64_t sdesc = ring_desc + (uint64_t)s * kStageStep;
-                        // the stage's tiles in chains of R (a chain ends with its stage)
-                        if (nt == kTcTilesPerStage) {
-                            // whole stage: static chain boundaries (the MMAs issue
-                            // several times slower under run-time chain logic)
-#pragma unroll
-                            for (int t = 0; t < kTcTilesPerStage; t++) {
-                                if (t % R == 0 && !(ok = begin_chain())) break;
-                                tc_mma(tmem + (uint32_t)b * kTcDBufferStride, sdesc + (uint64_t)t * kTileStep,
-                                       b_desc, idesc, t % R != 0 ? 1u : 0u);
-                                if (t % R == R - 1 || t == kTcTilesPerStage - 1) end_chain();
-                            }
-                        } else {
-                            // a unit's last, partial stage (the array's end; every stage
-                            // of the units of fewer than 8 tiles that small inputs use)
-                            for (int t = 0; t < nt; t++) {
-                                if (t % R == 0 && !(ok = begin_chain())) break;
-                                tc_mma(tmem + (uint32_t)b * kTcDBufferStride, sdesc + (uint64_t)t * kTileStep,
-                                       b_desc, idesc, t % R != 0 ? 1u : 0u);
-                                if (t % R == R - 1 || t == nt - 1) end_chain();
-                            }
-                        }
-                        tc_commit(empty_bar(s));                  // stage may be refilled
-                        if (++s == kTcStages) {
-                            s = 0;
-                            phase ^= 1u;
+                    } else {
+                        // a unit's last, partial stage (the array's end; every stage
+                        // of the units of fewer than 8 tiles that small inputs use)
+                        for (int t = 0; t < nt; t++) {
+                            if (t % R == 0 && !(ok = begin_chain())) break;
+                            tc_mma(tmem + (uint32_t)b * kTcDBufferStride, sdesc + (uint64_t)t * kTileStep,
+                                   b_desc, idesc, t % R != 0 ? 1u : 0u);
+                            if (t % R == R - 1 || t == nt - 1) end_chain(t == nt - 1);
                         }
                     }
-                    if (!ok) break;
+                    tc_commit(empty_bar(s));                  // stage may be refilled
+                    if (++s == kTcStages) {
+                        s = 0;
+                        phase ^= 1u;
+                    }
                 }
+                return ok;
+            };
+            uint32_t u = blockIdx.x, k = 0;
+            for (;;) {
+                if (!unit_mmas(unit_tiles(n, u, unit_log2)) || *abort) break;
+                if (!mbar_wait(clc_full_bar(k), clc_parity(k), abort)) break;
+                uint32_t next;
+                const bool more = clc_query(clc_resp(k), &next);
+                mbar_arrive(clc_empty_bar(k));
+                if (!more) break;
+                u = next;
+                k++;
             }
             // every MMA issued has completed once the drain barrier flips
             tc_commit(drain_bar);
-            const uint64_t t0 = global_ns();
-            while (!mbar_try_wait(drain_bar, 0u) && global_ns() - t0 < kWaitLimitNs) {
-            }
+            (void)mbar_wait_limited(drain_bar, 0u);
         }
         __syncwarp();
     } else {
@@ -349,24 +377,34 @@ mma_tmem_kernel(const uint16_t *__restrict__ x, size_t n, size_t units, int unit
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
         int b = 0;
         uint32_t dphase = 0u;
-        for (size_t u = blockIdx.x; u < units; u += gridDim.x) {
+        uint32_t u = blockIdx.x, k = 0;
+        for (;;) {
             const int tiles = unit_tiles(n, u, unit_log2);
-            const int chains = stage_chains<R, kTcTilesPerStage>(tiles);
             float acc = 0.f;
-            for (int c = 0; c < chains; c++) {
+            for (int t0 = 0; t0 < tiles; t0 += kTcTilesPerStage) {
+                // the stage's chains (a chain ends with its stage): wait for the
+                // last one -- its commit covers every MMA issued before it --
+                // then read them together and add them in chain order
+                const int nc = (min(kTcTilesPerStage, tiles - t0) + R - 1) / R;
+                const int bl = (b + nc - 1) % kTcDBuffers;
                 // the warp takes the wait's outcome together: tcgen05.ld is warp-wide
-                const bool ok = !*abort && mbar_wait(dfull_bar(b), (dphase >> b) & 1u, abort);
+                const bool ok = !*abort && mbar_wait(dfull_bar(bl), (dphase >> bl) & 1u, abort);
                 if (!__all_sync(kFull, ok)) break;
                 tc_fence_after();
-                const float v = tc_ld_lane(tmem + lane_base + (uint32_t)b * kTcDBufferStride);
-                acc = __fadd_rn(acc, v);
+                uint32_t v[8];
+                tc_ld_chain_cols(tmem + lane_base, b, nc, v);
+#pragma unroll
+                for (int i = 0; i < 8; i++)
+                    if (i < nc) acc = __fadd_rn(acc, __uint_as_float(v[i]));
                 tc_fence_before();
-                mbar_arrive(dempty_bar(b));
-                dphase ^= 1u << b;
-                if (++b == kTcDBuffers) b = 0;
+                for (int i = 0; i < nc; i++) {
+                    mbar_arrive(dempty_bar(b));
+                    dphase ^= 1u << b;
+                    if (++b == kTcDBuffers) b = 0;
+                }
             }
             // inputs of this unit past its whole tiles (only in the last unit)
-            const size_t base = u << unit_log2;
+            const size_t base = (size_t)u << unit_log2;
             const size_t tail_lo = base + (size_t)tiles * kTcTileInputs;
             size_t tail_hi = base + ((size_t)1 << unit_log2);
             if (tail_hi > n) tail_hi = n;
@@ -379,8 +417,20 @@ mma_tmem_kernel(const uint16_t *__restrict__ x, size_t n, size_t units, int unit
             if (et == 0) {
                 float v = __fadd_rn(__fadd_rn(red[0], red[1]), __fadd_rn(red[2], red[3]));
                 dst[u] = *abort ? __int_as_float(0x7fc00000) : v;
+                // the next unit, for all four warps (one decision: the named
+                // barriers below need every epilogue thread)
+                uint32_t next = 0, more = 0;
+                if (!*abort && mbar_wait(clc_full_bar(k), clc_parity(k), abort)) {
+                    more = clc_query(clc_resp(k), &next) ? 1u : 0u;
+                    mbar_arrive(clc_empty_bar(k));
+                }
+                *next_unit = next;
+                *more_units = more;
             }
             named_sync(1, kTcEpilogueThreads);
+            if (!*more_units) break;
+            u = *next_unit;
+            k++;
         }
     }
 
@@ -510,6 +560,9 @@ mma_tmem_rows_kernel(const __grid_constant__ CUtensorMap tmap, int use_map, cons
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
+    // the set-up above ran beside the stream's previous kernel; global
+    // memory is touched only after it has finished
+    pdl_wait_primary();
 
     if (warp == 0) {
         // ---------------- producer: a stage is one 3-D tensor-map box (whole
@@ -709,6 +762,353 @@ mma_tmem_rows_kernel(const __grid_constant__ CUtensorMap tmap, int use_map, cons
     }
 }
 
+// ---------------------------------------------------------------- rows, flat
+
+// Rows of 1024 k columns, k a divisor or a multiple of 16, laid out one
+// after the other (row stride = cols): the matrix is read as the flat array
+// it is, in the sum kernel's 32 KiB bulk copies, and only the MMA's view of
+// a stage follows the rows.  A K-major descriptor with no swizzle, K halves
+// 128 bytes apart and 8-row groups 2048 bytes apart gives MMA m of a stage
+// (m = 0 .. 7, 256 bytes further each) lanes 8g + i the 16-byte pieces at
+// 2048 g + 256 m + 16 i and + 128: over the stage's 8 MMAs the 8 lanes of
+// group g take its 2 KiB (1024 inputs) g, which lies inside one row.  Row j
+// of a stage of whole rows (k <= 16: 16 / k rows a stage) is TMEM lanes
+// 8 k j .. 8 k (j + 1) - 1, a row of 16 384 inputs or more fills all 128
+// lanes of each of its stages.  The epilogue adds a lane's chain results
+// over the row's stages, then the row's lanes: an xor butterfly inside a
+// warp, then the warps' totals in lane-quarter order, the same for every
+// row whatever its position -- a row's bits depend on its inputs and cols
+// only.  Every stage is 8 MMAs with static chain boundaries; lanes of the
+// groups past the matrix in a unit's last stage read stale shared memory
+// and are never stored.  Work unit: 65 536 / cols whole rows (65 536
+// inputs), or one chunk of 65 536 columns of a longer row (partials merged
+// by the rows combine).  One CTA per unit; the resident CTAs take over the
+// rest by cluster launch control, as in the sum kernel.
+constexpr int kFlatGroupInputs = 1024;                      // inputs of a lane group per stage
+constexpr size_t kFlatUnitInputs = (size_t)1 << 16;         // 4 stages
+// an MMA takes 256 bytes of each of the 16 lane groups: 8 MMAs cover a group's 2 KiB
+constexpr int kFlatMmasPerStage = 2 * kFlatGroupInputs / (kTcRowsMmaCols * 2);
+static_assert(kFlatMmasPerStage == 8 && 16 * 2 * kFlatGroupInputs == kTcStageBytes,
+              "16 lane groups of 2 KiB fill a stage, 8 MMAs of 4 KiB");
+
+__host__ __device__ inline bool flat_rows_shape(size_t cols)
+{
+    if (cols == 0 || cols % kFlatGroupInputs != 0) return false;
+    const size_t k = cols / kFlatGroupInputs;
+    return 16 % k == 0 || k % 16 == 0;
+}
+
+template <int DT, int R>
+__global__ void __launch_bounds__(kTcThreads, 1)
+mma_tmem_rows_flat_kernel(const uint16_t *__restrict__ x, uint32_t rows, uint32_t cols, uint32_t unit_rows,
+                          uint32_t chunk_cols, uint32_t cpr, float *__restrict__ dst, uint32_t inject_stall)
+{
+    pdl_launch_dependents();   // the combine may launch now; it waits for this grid to finish
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const uint32_t sbase = smem_addr(smem);
+    const uint32_t ring = sbase + kTcOffRing;
+    const uint32_t ones = sbase + kTcOffOnes;
+    const uint32_t bars = sbase + kTcOffBars;
+    auto full_bar = [&](int s) { return bars + 8u * (uint32_t)s; };
+    auto empty_bar = [&](int s) { return bars + 8u * (uint32_t)(kTcStages + s); };
+    auto dfull_bar = [&](int b) { return bars + 8u * (uint32_t)(2 * kTcStages + b); };
+    auto dempty_bar = [&](int b) { return bars + 8u * (uint32_t)(2 * kTcStages + kTcDBuffers + b); };
+    const uint32_t drain_bar = bars + 8u * (uint32_t)(2 * kTcStages + 2 * kTcDBuffers);
+    auto clc_full_bar = [&](uint32_t k) { return drain_bar + 8u * (1u + k % kTcClcSlots); };
+    auto clc_empty_bar = [&](uint32_t k) { return drain_bar + 8u * (1u + kTcClcSlots + k % kTcClcSlots); };
+    auto clc_resp = [&](uint32_t k) { return sbase + kTcOffClc + 16u * (k % kTcClcSlots); };
+    auto clc_parity = [](uint32_t k) { return (k / kTcClcSlots) & 1u; };
+    uint32_t *misc = (uint32_t *)(smem + kTcOffMisc);
+    volatile uint32_t *tmem_holder = misc;
+    volatile uint32_t *abort = misc + 1;
+    volatile float *red = (volatile float *)(misc + 4);
+    volatile uint32_t *next_unit = misc + 8;
+    volatile uint32_t *more_units = misc + 9;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t k_groups = cols / kFlatGroupInputs;             // lane groups per row
+    // unit u: row block u / cpr (unit_rows rows), column chunk u % cpr
+    // (chunk_cols columns); its inputs are contiguous
+    auto unit_row0 = [&](uint32_t u) { return (size_t)(u / cpr) * unit_rows; };
+    auto unit_col0 = [&](uint32_t u) { return (size_t)(u % cpr) * chunk_cols; };
+    auto unit_inputs = [&](uint32_t u) -> size_t {
+        const size_t r0 = unit_row0(u), c0 = unit_col0(u);
+        const size_t live = rows - r0 < unit_rows ? rows - r0 : unit_rows;
+        const size_t nc = cols - c0 < chunk_cols ? cols - c0 : chunk_cols;
+        return live * nc;
+    };
+    auto unit_stages = [&](uint32_t u) {
+        return (int)((unit_inputs(u) + kTcStageBytes / 2 - 1) / (kTcStageBytes / 2));
+    };
+
+    {
+        const uint32_t one2 = DT == kF16 ? 0x3c003c00u : 0x3f803f80u;
+        uint32_t *o = (uint32_t *)(smem + kTcOffOnes);
+        for (int i = threadIdx.x; i < 128; i += blockDim.x) o[i] = one2;
+    }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kTcStages; s++) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < kTcDBuffers; b++) {
+            mbar_init(dfull_bar(b), 1);
+            mbar_init(dempty_bar(b), kTcEpilogueThreads);
+        }
+        mbar_init(drain_bar, 1);
+        for (uint32_t k = 0; k < kTcClcSlots; k++) {
+            mbar_init(clc_full_bar(k), 1);
+            mbar_init(clc_empty_bar(k), 2);
+        }
+        *abort = 0u;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(smem_addr((const void *)tmem_holder)), "r"(kTcTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+    // the set-up above ran beside the stream's previous kernel; global
+    // memory is touched only after it has finished
+    pdl_wait_primary();
+
+    if (warp == 0) {
+        // ---------------- producer: the unit's contiguous inputs, 32 KiB a stage
+        if (lane == 0) {
+            int s = 0;
+            uint32_t phase = 0;
+            bool armed[kTcStages];
+            uint32_t armed_phase[kTcStages];
+#pragma unroll
+            for (int i = 0; i < kTcStages; i++) {
+                armed[i] = false;
+                armed_phase[i] = 0;
+            }
+            uint32_t recent[kTcRecent];
+            uint32_t u = blockIdx.x, k = 0;
+            bool asked = false;
+            auto ask = [&]() -> bool {
+                if (!mbar_wait(clc_empty_bar(k), clc_parity(k) ^ 1u, abort)) return false;
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                mbar_arrive_expect_tx(clc_full_bar(k), 16);
+                clc_try_cancel(clc_resp(k), clc_full_bar(k));
+                asked = true;
+                return true;
+            };
+            for (;;) {
+                recent[k % kTcRecent] = u;
+                const size_t total = unit_inputs(u);
+                const int stages = unit_stages(u);
+                const uint16_t *src = x + unit_row0(u) * cols + unit_col0(u);
+                bool ok = true;
+                for (int st = 0; st < stages && ok; st++) {
+                    if (st == stages - 1 && !(ok = ask())) break;
+                    if (!(ok = mbar_wait(empty_bar(s), phase ^ 1u, abort))) break;
+                    const size_t i0 = (size_t)st * (kTcStageBytes / 2);
+                    const size_t left = total - i0;
+                    const uint32_t bytes = (uint32_t)(left < (size_t)kTcStageBytes / 2 ? left * 2 : kTcStageBytes);
+                    mbar_arrive_expect_tx(full_bar(s), bytes);
+                    bulk_copy_g2s(ring + (uint32_t)s * kTcStageBytes, src + i0, bytes, full_bar(s));
+                    armed[s] = true;
+                    armed_phase[s] = phase;
+                    if (++s == kTcStages) {
+                        s = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok || !mbar_wait(clc_full_bar(k), clc_parity(k), abort)) break;
+                asked = false;
+                uint32_t next;
+                if (!clc_query(clc_resp(k), &next)) break;
+                u = next;
+                k++;
+            }
+            if (*abort) {
+#pragma unroll
+                for (int i = 0; i < kTcStages; i++)
+                    if (armed[i]) (void)mbar_wait_limited(full_bar(i), armed_phase[i]);
+                // the rows of the units started, and of every unit taken over
+                // from here, are marked NaN (see the sum kernel)
+                const float nan = __int_as_float(0x7fc00000);
+                auto mark = [&](uint32_t v) {
+                    const size_t r0 = unit_row0(v);
+                    for (size_t r = r0; r < r0 + unit_rows && r < rows; r++) dst[r * cpr + v % cpr] = nan;
+                };
+                for (uint32_t j = 0; j < kTcRecent && j <= k; j++) mark(recent[(k - j) % kTcRecent]);
+                if (!asked) {
+                    mbar_arrive_expect_tx(clc_full_bar(k), 16);
+                    clc_try_cancel(clc_resp(k), clc_full_bar(k));
+                }
+                for (;;) {
+                    uint32_t v;
+                    if (!mbar_wait_limited(clc_full_bar(k), clc_parity(k)) || !clc_query(clc_resp(k), &v))
+                        break;
+                    mark(v);
+                    k++;
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    mbar_arrive_expect_tx(clc_full_bar(k), 16);
+                    clc_try_cancel(clc_resp(k), clc_full_bar(k));
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---------------- MMA issuer: 8 MMAs a stage, chains of R ending with it
+        if (lane == 0) {
+            const uint32_t idesc = instr_desc<DT>();
+            const uint64_t b_desc = smem_desc(ones, 128, 256);
+            const uint64_t ring_desc = smem_desc(ring, 128, 2 * kFlatGroupInputs);
+            constexpr uint64_t kMmaStep = (uint64_t)(kTcRowsMmaCols * 2) >> 4;    // 256 bytes
+            constexpr uint64_t kStageStep = kTcStageBytes >> 4;
+            int s = 0, b = 0;
+            uint32_t phase = 0, dphase = 0u;
+            auto begin_chain = [&]() -> bool {
+                if (!mbar_wait(dempty_bar(b), ((dphase >> b) & 1u) ^ 1u, abort)) return false;
+                tc_fence_after();
+                return true;
+            };
+            // a host-requested stall withholds the first stage's last chain
+            bool withhold = inject_stall != 0u;
+            auto end_chain = [&](bool ends_stage) {
+                if (withhold && ends_stage)
+                    withhold = false;
+                else
+                    tc_commit(dfull_bar(b));
+                dphase ^= 1u << b;
+                if (++b == kTcDBuffers) b = 0;
+            };
+            uint32_t u = blockIdx.x, k = 0;
+            bool ok = true;
+            for (;;) {
+                const int stages = unit_stages(u);
+                for (int st = 0; st < stages && ok; st++) {
+                    if (!(ok = mbar_wait(full_bar(s), phase, abort))) break;
+                    tc_fence_after();
+                    const uint64_t sdesc = ring_desc + (uint64_t)s * kStageStep;
+#pragma unroll
+                    for (int m = 0; m < kFlatMmasPerStage; m++) {
+                        if (m % R == 0 && !(ok = begin_chain())) break;
+                        tc_mma(tmem + (uint32_t)b * kTcDBufferStride, sdesc + (uint64_t)m * kMmaStep, b_desc,
+                               idesc, m % R != 0 ? 1u : 0u);
+                        if (m % R == R - 1 || m == kFlatMmasPerStage - 1) end_chain(m == kFlatMmasPerStage - 1);
+                    }
+                    tc_commit(empty_bar(s));
+                    if (++s == kTcStages) {
+                        s = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok || *abort) break;
+                if (!mbar_wait(clc_full_bar(k), clc_parity(k), abort)) break;
+                uint32_t next;
+                const bool more = clc_query(clc_resp(k), &next);
+                mbar_arrive(clc_empty_bar(k));
+                if (!more) break;
+                u = next;
+                k++;
+            }
+            tc_commit(drain_bar);
+            (void)mbar_wait_limited(drain_bar, 0u);
+        }
+        __syncwarp();
+    } else {
+        // ---------------- epilogue: TMEM lane L = 32 q + lane, group L / 8
+        const int q = warp & 3;
+        const int et = threadIdx.x - 64;
+        const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+        const uint32_t L = 32u * (uint32_t)q + (uint32_t)lane;
+        constexpr int kChains = (kFlatMmasPerStage + R - 1) / R;
+        // rows of a stage (k <= 16) or stages of a row chunk (k >= 16)
+        const uint32_t lanes_per_row = k_groups <= 16 ? 8u * k_groups : 128u;
+        const uint32_t rows_per_stage = k_groups <= 16 ? 16u / k_groups : 1u;
+        const uint32_t stages_per_row = k_groups <= 16 ? 1u : k_groups / 16u;
+        int b = 0;
+        uint32_t dphase = 0u;
+        uint32_t u = blockIdx.x, k = 0;
+        for (;;) {
+            const int stages = unit_stages(u);
+            const size_t r0 = unit_row0(u);
+            const uint32_t chunk = u % cpr;
+            float acc = 0.f;
+            bool ok = true;
+            for (int st = 0; st < stages; st++) {
+                // the stage's chains: wait for the last (its commit covers the
+                // MMAs before it), read them together, add them in chain order
+                const int bl = (b + kChains - 1) % kTcDBuffers;
+                const bool w_ok = ok && !*abort && mbar_wait(dfull_bar(bl), (dphase >> bl) & 1u, abort);
+                ok = __all_sync(kFull, w_ok);
+                if (ok) {
+                    tc_fence_after();
+                    uint32_t v[8];
+                    tc_ld_chain_cols(tmem + lane_base, b, kChains, v);
+#pragma unroll
+                    for (int i = 0; i < kChains; i++) acc = __fadd_rn(acc, __uint_as_float(v[i]));
+                    tc_fence_before();
+#pragma unroll
+                    for (int i = 0; i < kChains; i++) {
+                        mbar_arrive(dempty_bar(b));
+                        dphase ^= 1u << b;
+                        if (++b == kTcDBuffers) b = 0;
+                    }
+                }
+                if ((uint32_t)(st + 1) % stages_per_row != 0 && st + 1 != stages) continue;
+                // the stage ends rows (or the row's chunk): add each row's lanes
+                for (uint32_t off = 1; off < 32u && off < lanes_per_row; off <<= 1)
+                    acc = __fadd_rn(acc, __shfl_xor_sync(kFull, acc, (int)off));
+                const size_t row = r0 + (size_t)st / stages_per_row * rows_per_stage + L / lanes_per_row;
+                const float nan = __int_as_float(0x7fc00000);
+                if (lanes_per_row <= 32u) {
+                    if ((L & (lanes_per_row - 1u)) == 0 && row < rows)
+                        dst[row * cpr + chunk] = (*abort || !ok) ? nan : acc;
+                } else {
+                    // two or four warps to a row: their totals in lane-quarter order
+                    if (lane == 0) red[q] = acc;
+                    named_sync(1, kTcEpilogueThreads);
+                    if (lanes_per_row == 64u && lane == 0 && (q & 1) == 0 && row < rows) {
+                        const float v = __fadd_rn(red[q], red[q + 1]);
+                        dst[row * cpr + chunk] = (*abort || !ok) ? nan : v;
+                    } else if (lanes_per_row == 128u && et == 0 && row < rows) {
+                        const float v = __fadd_rn(__fadd_rn(red[0], red[1]), __fadd_rn(red[2], red[3]));
+                        dst[row * cpr + chunk] = (*abort || !ok) ? nan : v;
+                    }
+                    named_sync(1, kTcEpilogueThreads);
+                }
+                acc = 0.f;
+            }
+            if (et == 0) {
+                uint32_t next = 0, more = 0;
+                if (!*abort && mbar_wait(clc_full_bar(k), clc_parity(k), abort)) {
+                    more = clc_query(clc_resp(k), &next) ? 1u : 0u;
+                    mbar_arrive(clc_empty_bar(k));
+                }
+                *next_unit = next;
+                *more_units = more;
+            }
+            named_sync(1, kTcEpilogueThreads);
+            if (!*more_units) break;
+            u = *next_unit;
+            k++;
+            named_sync(1, kTcEpilogueThreads);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kTcTmemCols)
+                     : "memory");
+    }
+}
+
 // ---------------------------------------------------------------- host
 
 template <int DT>
@@ -754,12 +1154,14 @@ cudaError_t launch_mma_tmem(int dtype, int R, const uint16_t *x, size_t n, float
     if (!k) return cudaErrorInvalidValue;
     cudaError_t e = set_smem_once(k, kTcSmemBytes);
     if (e != cudaSuccess) return e;
-    size_t units = tmem_units(n);
+    // one CTA per unit: the CTAs running take over those still waiting to
+    // launch (cluster launch control), so fast SMs take more units
+    const size_t units = tmem_units(n);
+    if (units != (size_t)grid) return cudaErrorInvalidValue;
     int unit_log2 = tmem_unit_log2(n);
     uint32_t stall = inject_stall ? 1u : 0u;
-    void *args[] = {(void *)&x, (void *)&n, (void *)&units, (void *)&unit_log2, (void *)&dst,
-                    (void *)&stall};
-    return cudaLaunchKernel(k, dim3(grid), dim3(kTcThreads), args, kTcSmemBytes, stream);
+    void *args[] = {(void *)&x, (void *)&n, (void *)&unit_log2, (void *)&dst, (void *)&stall};
+    return launch_first(k, dim3(grid), dim3(kTcThreads), args, kTcSmemBytes, stream);
 }
 
 template <int DT, bool SHORT>
@@ -784,7 +1186,15 @@ static void *pick_rows_dt(int R)
 // do not depend on the number of rows or the device.
 size_t tmem_rows_chunks(size_t cols)
 {
+    if (flat_rows_shape(cols)) return (cols + kFlatUnitInputs - 1) / kFlatUnitInputs;
     return (cols + kTcRowsMaxChunkCols - 1) / kTcRowsMaxChunkCols;
+}
+
+// Rows of the flat layout: 65 536 / cols whole rows a unit, or one row
+// (its chunks of 65 536 columns being units of their own).
+static size_t flat_unit_rows(size_t cols)
+{
+    return cols < kFlatUnitInputs ? kFlatUnitInputs / cols : 1;
 }
 
 // S: the columns of a row in one stage -- 2048, or 1024 for rows whose
@@ -801,6 +1211,10 @@ static int tmem_rows_stage_cols(size_t cols)
 
 size_t tmem_rows_units(size_t rows, size_t cols)
 {
+    if (flat_rows_shape(cols)) {
+        const size_t ur = flat_unit_rows(cols);
+        return ((rows + ur - 1) / ur) * tmem_rows_chunks(cols);
+    }
     const size_t unit_rows = (size_t)kTcRowsGroup * (kTcRowsStageCols / tmem_rows_stage_cols(cols));
     return ((rows + unit_rows - 1) / unit_rows) * tmem_rows_chunks(cols);
 }
@@ -808,6 +1222,32 @@ size_t tmem_rows_units(size_t rows, size_t cols)
 cudaError_t launch_mma_tmem_rows(int dtype, int R, const uint16_t *x, size_t rows, size_t cols,
                                  float *dst, int grid, bool inject_stall, cudaStream_t stream)
 {
+    uint32_t stall = inject_stall ? 1u : 0u;
+    if (flat_rows_shape(cols)) {
+        // one CTA per unit, the resident ones taking over the rest
+        void *k = nullptr;
+        switch (R) {
+#define TCR_FLAT_CASE(r)                                                                              \
+    case r:                                                                                           \
+        k = dtype == kF16 ? (void *)mma_tmem_rows_flat_kernel<kF16, r> : (void *)mma_tmem_rows_flat_kernel<kBF16, r>; \
+        break;
+            TCR_FLAT_CASE(1) TCR_FLAT_CASE(2) TCR_FLAT_CASE(3) TCR_FLAT_CASE(4)
+            TCR_FLAT_CASE(5) TCR_FLAT_CASE(6) TCR_FLAT_CASE(7) TCR_FLAT_CASE(8)
+#undef TCR_FLAT_CASE
+        default: return cudaErrorInvalidValue;
+        }
+        const size_t units = tmem_rows_units(rows, cols);
+        if (units != (size_t)grid || rows >= ((size_t)1 << 31) || cols >= ((size_t)1 << 31))
+            return cudaErrorInvalidValue;
+        cudaError_t e = set_smem_once(k, kTcSmemBytes);
+        if (e != cudaSuccess) return e;
+        uint32_t r32 = (uint32_t)rows, c32 = (uint32_t)cols, ur = (uint32_t)flat_unit_rows(cols);
+        uint32_t cc = (uint32_t)(cols < kFlatUnitInputs ? cols : kFlatUnitInputs);
+        uint32_t cpr = (uint32_t)tmem_rows_chunks(cols);
+        void *args[] = {(void *)&x, (void *)&r32, (void *)&c32, (void *)&ur, (void *)&cc, (void *)&cpr,
+                        (void *)&dst, (void *)&stall};
+        return launch_first(k, dim3(grid), dim3(kTcThreads), args, kTcSmemBytes, stream);
+    }
     int stage_cols = tmem_rows_stage_cols(cols);
     const bool short_rows = stage_cols < kTcRowsStageCols;
     void *k = dtype == kF16 ? (short_rows ? pick_rows_dt<kF16, true>(R) : pick_rows_dt<kF16, false>(R))
@@ -838,11 +1278,17 @@ cudaError_t launch_mma_tmem_rows(int dtype, int R, const uint16_t *x, size_t row
             return cudaErrorInvalidValue;
         use_map = 1;
     }
-    uint32_t stall = inject_stall ? 1u : 0u;
     void *args[] = {(void *)&map, (void *)&use_map, (void *)&x, (void *)&rows, (void *)&cols,
                     (void *)&chunk_cols, (void *)&cpr, (void *)&units, (void *)&stage_cols,
                     (void *)&dst, (void *)&stall};
-    return cudaLaunchKernel(k, dim3(grid), dim3(kTcThreads), args, kTcRowsSmemBytes, stream);
+    return launch_first(k, dim3(grid), dim3(kTcThreads), args, kTcRowsSmemBytes, stream);
+}
+
+int tmem_rows_grid(size_t rows, size_t cols, size_t sms)
+{
+    const size_t units = tmem_rows_units(rows, cols);
+    if (flat_rows_shape(cols)) return units < ((size_t)1 << 31) ? (int)units : 0;
+    return (int)(units < sms ? units : sms);
 }
 
 cudaError_t read_device_faults(unsigned int *flags, bool clear)

@@ -14,6 +14,27 @@
 
 namespace tcr {
 
+// A call's first kernel is launched with programmatic stream serialization:
+// it may become resident, and run the set-up before its griddepcontrol.wait,
+// while the stream's previous kernel finishes (every kernel launched this
+// way waits before its first global memory access, and the library's
+// kernels let their dependents launch as they start).
+inline cudaError_t launch_first(const void *k, dim3 grid, dim3 block, void **args, size_t smem,
+                                cudaStream_t stream)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, k, args);
+}
+
 // ---- FIXED_ORDER (balanced tree over index order)
 // Chunked: CTA work unit u = (segment u / cps, chunk u % cps); the chunk of
 // 2^chunk_log2 inputs is split evenly over the CTA's warps; dst[u] is the
@@ -101,6 +122,10 @@ cudaError_t launch_mma_tmem_rows(int dtype, int R, const uint16_t *x, size_t row
 cudaError_t read_device_faults(unsigned int *flags, bool clear);
 size_t tmem_rows_chunks(size_t cols);
 size_t tmem_rows_units(size_t rows, size_t cols);
+// CTAs to launch for the rows: one per unit for rows of 1024 k columns (k a
+// divisor or a multiple of 16, read as a flat array), else at most one per
+// SM; 0 when there are too many units for one launch.
+int tmem_rows_grid(size_t rows, size_t cols, size_t sms);
 
 // ---- sums and sums of squares in one pass (rows; the mean/variance calls)
 // family: which mode's policies run side by side

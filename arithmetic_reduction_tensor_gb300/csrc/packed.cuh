@@ -449,6 +449,8 @@ packed_rows_kernel(const void *__restrict__ xv, size_t rows, size_t cols, float 
                    float *__restrict__ out_b, int mean_var)
 {
     static_assert(MODE != kPackedMma || VLOG >= 2, "a tensor-core row is at least one lane quad");
+    pdl_launch_dependents();
+    pdl_wait_primary();        // the stream's previous kernel has finished
     using T = typename Elem<DT>::T;
     constexpr bool NZ = MODE != kPackedMma;
     constexpr int M = packed_m<MODE, VLOG>();

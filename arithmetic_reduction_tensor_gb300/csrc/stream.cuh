@@ -559,6 +559,7 @@ __device__ __forceinline__ void chunk_body(const void *__restrict__ xv, size_t s
                                            float *__restrict__ dst)
 {
     pdl_launch_dependents();   // the combine may launch now; it waits for this grid to finish
+    pdl_wait_primary();        // the stream's previous kernel has finished
     constexpr int DT = Red::kDT;
     constexpr bool NZ = Red::kNegZeroPad;
     using T = typename Elem<DT>::T;
@@ -623,6 +624,8 @@ template <class Red, bool ALIGNED>
 __device__ __forceinline__ void rows_body(const void *__restrict__ xv, size_t rows,
                                           size_t cols, float *__restrict__ out)
 {
+    pdl_launch_dependents();
+    pdl_wait_primary();        // the stream's previous kernel has finished
     constexpr int DT = Red::kDT;
     constexpr bool NZ = Red::kNegZeroPad;
     using T = typename Elem<DT>::T;
@@ -667,6 +670,7 @@ __device__ __forceinline__ void chunk_pair_body(const void *__restrict__ xv, siz
                                                 float *__restrict__ dst_b)
 {
     pdl_launch_dependents();   // the combine may launch now; it waits for this grid to finish
+    pdl_wait_primary();        // the stream's previous kernel has finished
     constexpr int DT = Red::kDT;
     constexpr bool NZ = Red::kNegZeroPad;
     using T = typename Elem<DT>::T;
@@ -717,6 +721,8 @@ __device__ __forceinline__ void rows_pair_body(const void *__restrict__ xv, size
                                                size_t cols, float *__restrict__ out_a,
                                                float *__restrict__ out_b, int mean_var)
 {
+    pdl_launch_dependents();
+    pdl_wait_primary();        // the stream's previous kernel has finished
     constexpr int DT = Red::kDT;
     constexpr bool NZ = Red::kNegZeroPad;
     using T = typename Elem<DT>::T;

@@ -131,12 +131,75 @@ __device__ __forceinline__ void tc_commit(uint32_t bar)
                  : "memory");
 }
 
+// Column 0 of the n D buffers b0, b0 + 1, ... (mod 8; buffer b at columns
+// `base + 32 b`) for the calling thread's TMEM lane, n <= 8, the loads
+// issued together and waited for once; v[i] for i >= n is left unchanged.
+// Warp-collective: b0 and n must be the same in every lane.
+__device__ __forceinline__ void tc_ld_chain_cols(uint32_t base, int b0, int n, uint32_t (&v)[8])
+{
+#pragma unroll
+    for (int i = 0; i < 8; i++)
+        if (i < n)
+            asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];"
+                         : "=r"(v[i])
+                         : "r"(base + 32u * (uint32_t)((b0 + i) & 7))
+                         : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]), "+r"(v[6]),
+                   "+r"(v[7])
+                 :
+                 : "memory");
+}
+
 __device__ __forceinline__ float tc_ld_lane(uint32_t taddr)
 {
     uint32_t v;
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(v) : "r"(taddr) : "memory");
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
     return __uint_as_float(v);
+}
+
+// Cluster launch control (sm_100 and later): ask the hardware to cancel the
+// launch of a CTA of this grid that has not started yet, so that the asking
+// CTA runs that CTA's work instead.  The 16-byte response lands in shared
+// memory at `resp` (16-byte aligned) and completes 16 transaction bytes on
+// `bar`.  Once a response has said that nothing was cancelled, the CTA must
+// not ask again.
+__device__ __forceinline__ void clc_try_cancel(uint32_t resp, uint32_t bar)
+{
+    asm volatile(
+        "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];"
+        ::"r"(resp), "r"(bar)
+        : "memory");
+}
+
+// Read a completed response: true and the cancelled CTA's x index, or false
+// when no CTA was left to cancel.
+__device__ __forceinline__ bool clc_query(uint32_t resp, uint32_t *ctaid_x)
+{
+    uint32_t ok, x;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b128 c;\n\t"
+        "ld.shared.b128 c, [%2];\n\t"
+        "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, c;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t"
+        "mov.u32 %1, 0;\n\t"
+        "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, c;\n\t"
+        "}"
+        : "=r"(ok), "=r"(x)
+        : "r"(resp)
+        : "memory");
+    *ctaid_x = x;
+    return ok != 0;
+}
+
+// Wait for a phase with a time limit and no abort flag (drain paths).
+__device__ __forceinline__ bool mbar_wait_limited(uint32_t bar, uint32_t parity)
+{
+    const uint64_t t0 = global_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+    return true;
 }
 
 __device__ __forceinline__ void named_sync(uint32_t id, uint32_t threads)

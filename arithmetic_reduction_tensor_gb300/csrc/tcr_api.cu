@@ -424,26 +424,29 @@ Plan make_plan(size_t segments, size_t seg_len, bool rows_call, const tcr_mode &
     // read-out, in a 64 KiB stage -- its epilogue then bounds it
     if (p.kind == TCR_MMA_CHAIN_TMEM && rows_call && seg_len < kTmemRowsMinCols) p.kind = TCR_MMA_CHAIN;
     if (p.kind == TCR_MMA_CHAIN_TMEM && rows_call && aligned && segments < ((size_t)1 << 31) &&
-        seg_len < ((size_t)1 << 31)) {
-        // 16 rows per MMA tile, 2-D tensor-map copies; one CTA per SM
+        seg_len < ((size_t)1 << 31) && tmem_rows_grid(segments, seg_len, sms) > 0) {
+        // rows of 1024 k columns as one flat array of 32 KiB copies (one CTA
+        // per unit), else 16 rows per MMA tile by tensor-map boxes (one CTA
+        // per SM)
         p.path = kPathTmemRows;
         p.block = tmem_block_threads();
         p.cps = tmem_rows_chunks(seg_len);
         p.units = tmem_rows_units(segments, seg_len);
-        p.grid = (int)(p.units < sms ? p.units : sms);
+        p.grid = tmem_rows_grid(segments, seg_len, sms);
         p.partials = p.cps > 1 ? segments * p.cps : 0;
         p.combine_count = p.cps;
         p.launches = p.cps > 1 ? 2 : 1;
         return p;
     }
-    if (p.kind == TCR_MMA_CHAIN_TMEM && !rows_call && aligned) {
-        // one persistent CTA per SM (its shared-memory ring fills the SM)
+    if (p.kind == TCR_MMA_CHAIN_TMEM && !rows_call && aligned && tmem_units(seg_len) < ((size_t)1 << 31)) {
+        // one CTA per unit, one resident per SM (its shared-memory ring fills
+        // the SM); the resident CTAs take over the units of those waiting
         p.path = kPathTmem;
         p.block = tmem_block_threads();
         p.chunk_log2 = tmem_unit_log2(seg_len);
         p.units = tmem_units(seg_len);
         p.cps = p.units;
-        p.grid = (int)(p.units < sms ? p.units : sms);
+        p.grid = (int)p.units;
         p.partials = p.units > 1 ? p.units : 0;
         p.combine_count = p.units;
         p.launches = p.units > 1 ? 2 : 1;

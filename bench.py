@@ -12,8 +12,13 @@ synthetic inputs resident in HBM:
 
 ``value`` is the algorithmic bytes of a step (2 bytes read per input plus
 4 bytes written per result) times the steps of all ranks, over the slowest
-rank's device time (CUDA events on the launching stream).  Both inputs are
-far larger than the 129 MB L2, so no flush is needed between calls.
+rank's device time (CUDA events on the launching stream, around all steps
+and nothing between the calls: the library launches each call's first
+kernel as a programmatic dependent of the kernel before it, which an event
+between the two would serialise).  Per call, ``us`` is the average of the
+call repeated back to back between two events, ``us_isolated_median`` the
+median with events around each call.  Both inputs are far larger than the
+129 MB L2, so no flush is needed between calls.
 
 The same JSON line also carries the other configurations of the workload
 (``configs``): the 2^20 binary16 sum (L2 flushed before every call by
@@ -271,31 +276,51 @@ def build_calls(x_sum, x_rows):
 
 
 def time_device(calls, steps: int, warmup: int, world: int):
+    """The timed region: `steps` steps of every call, back to back, with CUDA
+    events only around the whole region (an event between two calls would
+    hold the next call's launch until the previous one has finished, which
+    the library's programmatic dependent launches otherwise overlap).
+    Then, per call: the same call `steps` times back to back between two
+    events (its average duration, launches overlapped as in a step), and
+    `steps` times with events around each call (the median of isolated
+    calls)."""
     import torch
+    stream = torch.cuda.current_stream()
+    ev = lambda: torch.cuda.Event(enable_timing=True)
     for _ in range(warmup):
         for _, fn, _, _ in calls:
             fn()
-    stream = torch.cuda.current_stream()
-    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in calls] for _ in range(steps)]
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0, t1 = ev(), ev()
     torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
     t0.record(stream)
     for s in range(steps):
-        for c, (_, fn, _, _) in enumerate(calls):
-            ev[s][c][0].record(stream)
+        for _, fn, _, _ in calls:
             fn()
-            ev[s][c][1].record(stream)
     t1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
     total_s = t0.elapsed_time(t1) / 1e3
-    per_call_ms = [[ev[s][c][0].elapsed_time(ev[s][c][1]) for s in range(steps)]
-                   for c in range(len(calls))]
-    return total_s, per_call_ms
+    per_call_avg_ms, per_call_ms = [], []
+    for _, fn, _, _ in calls:
+        for _ in range(3):
+            fn()
+        a, b = ev(), ev()
+        a.record(stream)
+        for _ in range(steps):
+            fn()
+        b.record(stream)
+        pairs = [(ev(), ev()) for _ in range(steps)]
+        for e0, e1 in pairs:
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        per_call_avg_ms.append(a.elapsed_time(b) / steps)
+        per_call_ms.append([e0.elapsed_time(e1) for e0, e1 in pairs])
+    return total_s, per_call_avg_ms, per_call_ms
 
 
 def time_e2e(xs, xr, calls_factory, steps: int, world: int):
@@ -355,43 +380,36 @@ def read_ceiling(x):
         for ctas in (1, 2, 4, 8):
             if block * ctas > 2048:
                 continue
-            for _ in range(2):
-                tcr.tcr_read_probe(x, ctas, block, out=out)
-            times = []
-            for _ in range(10):
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record()
-                tcr.tcr_read_probe(x, ctas, block, out=out)
-                e1.record()
-                torch.cuda.synchronize()
-                times.append(e0.elapsed_time(e1) * 1e3)
-            gbps = nbytes / statistics.median(times) / 1e3
+            us = timed_median_us(lambda: tcr.tcr_read_probe(x, ctas, block, out=out), 10, 2)
+            gbps = nbytes / us / 1e3
             if best is None or gbps > best["gbps"]:
                 best = {"gbps": round(gbps, 1), "ctas_per_sm": ctas, "block": block}
     best.update({"bytes": nbytes, "kernel": "read_probe_kernel",
                  "how": "16-byte streaming loads, 8 in flight per thread, XOR of the words; "
-                        "best grid shape, median of 10 launches each"})
+                        "best grid shape, median of 10 launches each, queued back to back"})
     return best
 
 
 def timed_median_us(fn, iters: int, warmup: int, before=None):
     """Median device time of fn() in microseconds (CUDA events around each
-    call on the current stream); before() runs ahead of each call, outside
-    the events."""
+    call on the current stream).  Without before(), the calls are queued
+    back to back and synchronised once, so the GPU never waits for the
+    host between them; before() (an L2 flush) runs ahead of each call,
+    outside its events, and keeps the GPU busy while the call is queued."""
     import torch
     for _ in range(warmup):
         fn()
-    times = []
-    for _ in range(iters):
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(iters)]
+    torch.cuda.synchronize()
+    for e0, e1 in ev:
         if before is not None:
             before()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         fn()
         e1.record()
-        torch.cuda.synchronize()
-        times.append(e0.elapsed_time(e1) * 1e3)
-    return statistics.median(times)
+    torch.cuda.synchronize()
+    return statistics.median(e0.elapsed_time(e1) * 1e3 for e0, e1 in ev)
 
 
 def time_configs(args, device, ceiling_gbps: float):
@@ -892,7 +910,7 @@ def main():
         pass
     clocks = ClockSampler(uuid)
     clocks.start()
-    total_s, per_call_ms = time_device(calls, args.steps, args.warmup, world)
+    total_s, per_call_avg_ms, per_call_ms = time_device(calls, args.steps, args.warmup, world)
     ceiling = read_ceiling(x_sum)
     e2e_steps = args.e2e_steps or max(3, args.steps // 40)
     del x_sum, x_rows, calls
@@ -911,18 +929,19 @@ def main():
     peak, peak_src = load_peaks()
 
     calls_out = {}
-    for (name, nbytes, launches), ms in zip(meta, per_call_ms):
+    for (name, nbytes, launches), avg_ms, ms in zip(meta, per_call_avg_ms, per_call_ms):
+        avg_us = avg_ms * 1e3
         med_us = statistics.median(ms) * 1e3
-        avg_us = statistics.fmean(ms) * 1e3
-        gbps = nbytes / med_us / 1e3
-        calls_out[name] = {"us": round(med_us, 2), "us_mean": round(avg_us, 2), "gbps": round(gbps, 1),
-                           "gelem_per_s": round(call_elements(name) / med_us / 1e3, 1),
+        gbps = nbytes / avg_us / 1e3
+        calls_out[name] = {"us": round(avg_us, 2), "gbps": round(gbps, 1),
+                           "gelem_per_s": round(call_elements(name) / avg_us / 1e3, 1),
                            "frac": round(gbps / peak, 4),
                            "frac_of_read_ceiling": round(gbps / ceiling["gbps"], 4),
+                           "us_isolated_median": round(med_us, 2),
                            "launches": launches}
-    dom = max(calls_out, key=lambda k: calls_out[k]["us_mean"])
+    dom = max(calls_out, key=lambda k: calls_out[k]["us"])
     dom_nbytes = dict((m[0], m[1]) for m in meta)[dom]
-    dom_gbps = dom_nbytes / calls_out[dom]["us_mean"] / 1e3
+    dom_gbps = dom_nbytes / calls_out[dom]["us"] / 1e3
     elements_per_step = sum(call_elements(m[0]) for m in meta)
     launches = sum(m[2] for m in meta) * args.steps
 
@@ -951,7 +970,8 @@ def main():
         "roofline": {"bound": "hbm", "kernel": KERNEL_OF[dom], "call": dom,
                      "achieved": round(dom_gbps, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(dom_gbps / peak, 4), "traffic": recorded_traffic(KERNEL_OF[dom]),
-                     "duration": "mean of the timed calls, whole call (reduction + combine launch)",
+                     "duration": "average of the call repeated back to back between two events "
+                                 "(the whole call: reduction + combine launch)",
                      "peak_source": peak_src,
                      "read_ceiling": ceiling["gbps"],
                      "frac_of_read_ceiling": round(dom_gbps / ceiling["gbps"], 4)},

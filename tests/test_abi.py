@@ -366,19 +366,27 @@ def test_tcgen05_units_shrink_for_small_inputs(lib):
 
 
 def test_tmem_rows_plan(lib):
-    # the tcgen05 rows kernel (192 threads): work units of 16 rows x the
-    # whole row up to 8192 columns (32 rows for rows of 768..1024 inputs),
-    # longer rows in 8192-column chunks with per-row partials and a combine;
-    # rows under 768 inputs and rows that are not whole 16-byte vectors go
-    # to the mma.sync kernels.  (Without a device the plan assumes 152 SMs.)
+    # the tcgen05 rows kernels (192 threads).  Rows of 1024 k columns, k a
+    # divisor or a multiple of 16, are read as one flat array: a unit is
+    # 65536 / cols whole rows (65536 inputs) or a 65536-column chunk of a
+    # longer row (per-row partials and a combine), one CTA per unit.  Other
+    # rows: units of 16 rows x the whole row up to 8192 columns (32 rows for
+    # rows of 768..1024 inputs), longer rows in 8192-column chunks, at most
+    # one CTA per SM.  Rows under 768 inputs and rows that are not whole
+    # 16-byte vectors go to the mma.sync kernels.  (Without a device the
+    # plan assumes 152 SMs.)
     def plan(rows, cols):
         d = tcr.tcr_order_descriptor(rows=rows, cols=cols, mode=tcr.Mode(tcr.MMA_CHAIN_TMEM))
         return d["launch_block"], d["launch_grid"], d["partials"], d["launches"]
 
     assert plan(1000, 4096) == (192, 63, 0, 1)              # 63 units of 16 rows
-    assert plan(65536, 4096) == (192, 152, 0, 1)            # one CTA per SM
+    assert plan(65536, 4096) == (192, 4096, 0, 1)           # one CTA per unit
+    assert plan(65, 1024) == (192, 2, 0, 1)                 # 64 rows a unit
+    assert plan(10, 16384) == (192, 3, 0, 1)                # 4 rows a unit
+    assert plan(9, 49152) == (192, 9, 0, 1)                 # a row a unit
+    assert plan(100, 131072) == (192, 200, 200, 2)          # 2 chunks per row
     assert plan(3000, 768) == (192, 94, 0, 1)               # two row groups per unit
-    assert plan(7, 8192) == (192, 1, 0, 1)
+    assert plan(3000, 3072) == (192, 152, 0, 1)             # 3 groups a row: 16-row tiles
     assert plan(100, 20000) == (192, 21, 300, 2)            # 3 chunks per row
     assert plan(100, 512)[0] == 256                         # packed mma.sync rows
     assert plan(1000, 4100)[0] == 256                       # not whole vectors
