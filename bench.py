@@ -69,7 +69,7 @@ KERNEL_OF = {
     "rows/FIXED_ORDER": "fixed_rows_warp_kernel",
     "rows/SHUFFLE_TREE": "shuffle_rows_warp_kernel",
     "sum/MMA_CHAIN_TMEM": "mma_tmem_kernel",
-    "rows/MMA_CHAIN_TMEM": "mma_tmem_rows_kernel",
+    "rows/MMA_CHAIN_TMEM": "mma_tmem_rows_flat_kernel",
 }
 
 
@@ -130,7 +130,8 @@ KERNEL_SOURCE = {
     "fixed_chunk_kernel": "k_fixed.cu", "fixed_rows_warp_kernel": "k_fixed.cu",
     "shuffle_block_kernel": "k_shuffle.cu", "shuffle_rows_warp_kernel": "k_shuffle.cu",
     "combine_kernel": "k_combine.cu", "mma_tmem_kernel": "k_tc05.cu",
-    "mma_tmem_rows_kernel": "k_tc05.cu", "gemm_splitk_kernel": "k_gemm.cu",
+    "mma_tmem_rows_kernel": "k_tc05.cu", "mma_tmem_rows_flat_kernel": "k_tc05.cu",
+    "gemm_splitk_kernel": "k_gemm.cu",
 }
 # headers a kernel's source includes beyond the shared device headers
 KERNEL_HEADERS = {"k_tc05.cu": ("tc05.cuh",), "k_gemm.cu": ("tc05.cuh",)}
