@@ -33,12 +33,21 @@
  *                     copies, tcgen05.mma (M = 128, N = 16, K = 16; one MMA
  *                     per 2048 inputs) with the accumulator in tensor memory,
  *                     R MMAs per chain, chain sub-results read out to fp32
- *                     registers; rows put 16 rows on an MMA tile (8 of D's
- *                     lanes to a row, chains running along the row) and
- *                     reach shared memory by 3-D tensor-map or per-row bulk
- *                     copies.  A chain never spans two shared-memory stages
- *                     (8 MMAs for sums, 16 for rows); when R does not
- *                     divide that, a stage's last chain is shorter.  Same
+ *                     registers.  Rows of 1024 k columns (k a divisor or
+ *                     a multiple of 16) are read as the flat array they
+ *                     are, 32 KiB at a time, each MMA lane group taking 1024
+ *                     inputs of one row (a row is 8 k of D's lanes, or all
+ *                     128 for k >= 16); other rows put 16 rows on an MMA
+ *                     tile (8 lanes to a row, chains running along the row)
+ *                     and reach shared memory by 3-D tensor-map or per-row
+ *                     bulk copies.  A chain never spans two shared-memory
+ *                     stages (8 MMAs for sums and flat rows, 16 for 16-row
+ *                     tiles); when R does not divide that, a stage's last
+ *                     chain is shorter.  The sum and the flat rows launch
+ *                     one CTA per work unit and the resident CTAs take over
+ *                     the units of those not yet started (cluster launch
+ *                     control), so the result does not depend on which SM
+ *                     runs which unit.  Same
  *                     error bound as TCR_MMA_CHAIN.  16-bit sums only: an
  *                     x that is not 16-byte aligned (or rows whose stride is
  *                     not), rows of fewer than 768 inputs (a 64 KiB stage of
@@ -71,6 +80,16 @@
  * GEMM calls may be captured into a CUDA graph on a capturing stream; each
  * replay gives the eager call's bits.  (Not tcr_reduce_sum_noalloc, which
  * makes no such statement.)
+ *
+ * Kernel overlap.  A call's kernels are launched as programmatic dependents
+ * of the kernel before them on the stream (programmatic stream
+ * serialization): they may start, and run set-up that touches no global
+ * memory, while that kernel finishes, and wait for it (griddepcontrol.wait)
+ * before their first global memory access; they also let the next kernel
+ * on the stream launch early.  A caller's kernel launched right after a
+ * call without that attribute runs after the call's last kernel as usual;
+ * one launched with it must execute griddepcontrol.wait
+ * (cudaGridDependencySynchronize) before it reads the call's results.
  *
  * Errors.  Invalid arguments return TCR_ERR_INVALID_ARG before any GPU work
  * and leave *out untouched.  A CUDA error (allocation or launch) returns
