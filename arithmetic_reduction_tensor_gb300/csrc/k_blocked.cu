@@ -123,6 +123,99 @@ blocked_chunk_kernel(const void *__restrict__ xv, size_t seg_len, size_t units, 
     }
 }
 
+// Rows of at most 16 pieces (a row's pieces padded to 2^lpr, lpr <= 4): a
+// round of 32 pieces holds 32 >> lpr whole rows, lane group i (2^lpr
+// lanes) row i's pieces in order; the passes, the stage and the lanes' runs
+// are those of blocked_chunk_kernel, and the round ends in each row's tree
+// over its pieces -- the lane-order butterfly over its 2^lpr lanes.  With
+// one row to a round, the pieces past the row are -0.0 and the butterfly's
+// upper levels would add only -0.0 to the row's tree, so the bits are the
+// same; the round is no longer half padding.  Each warp walks the rounds
+// grid-stride; there are no partials.
+template <int DT, bool ALIGNED>
+__global__ void __launch_bounds__(32 * kBlockedMaxWarps, 4)
+blocked_rows_kernel(const void *__restrict__ xv, size_t rows, size_t cols, int run_log2, int lpr,
+                    float *__restrict__ out)
+{
+    pdl_launch_dependents();
+    pdl_wait_primary();        // the stream's previous kernel has finished
+    using T = typename Elem<DT>::T;
+    constexpr int V = Elem<DT>::kPerVec;
+    constexpr int LV = V == 8 ? 3 : 2;
+    extern __shared__ uint4 stage[];                  // kStageBytesPerWarp per warp
+    const T *__restrict__ x = static_cast<const T *>(xv);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int piece_log2 = run_log2 > LV + 3 ? run_log2 : LV + 3;
+    const int passes = 1 << (piece_log2 - LV - 3);
+    const int vrun_log2 = run_log2 - LV;
+    const bool short_runs = run_log2 < LV + 3;
+    const size_t rpr = (size_t)32 >> lpr;                     // rows per round
+    const size_t rounds = (rows + rpr - 1) / rpr;
+    const size_t nw = ((size_t)gridDim.x * blockDim.x) >> 5;
+    const uint32_t nz = Elem<DT>::kNegZeroWord;
+    uint4 *buf = stage + warp * (32 * kStageRow);
+    // slot k of this lane at pass p of round r: vector lane mod 8 of piece
+    // 4k + lane / 8, i.e. of piece q of row i of the round
+    auto load = [&](size_t r, int p, int k) -> uint4 {
+        const int piece = 4 * k + (lane >> 3);
+        const size_t row = r * rpr + (size_t)(piece >> lpr);
+        const size_t e = ((size_t)(piece & ((1 << lpr) - 1)) << piece_log2) + ((size_t)p << (LV + 3)) +
+                         (size_t)(lane & 7) * V;
+        if (row >= rows || e >= cols) return make_uint4(nz, nz, nz, nz);
+        return ld_vec<DT, ALIGNED, true>(x + row * cols, cols, e / V);
+    };
+    size_t r = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (r >= rounds) return;
+    uint4 q[8];
+#pragma unroll
+    for (int k = 0; k < 8; k++) q[k] = load(r, 0, k);
+    TreeCounter<3> lane_tc;       // short runs of the lane's piece (at most 4)
+    float run = -0.0f;
+    int p = 0;
+#pragma unroll 1
+    for (;;) {
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < 8; k++) buf[(4 * k + (lane >> 3)) * kStageRow + (lane & 7)] = q[k];
+        __syncwarp();
+        size_t nr = r;
+        int np = p + 1;
+        if (np == passes) {
+            np = 0;
+            nr = r + nw;
+        }
+        const bool more = nr < rounds;
+        if (more) {
+#pragma unroll
+            for (int k = 0; k < 8; k++) q[k] = load(nr, np, k);
+        }
+#pragma unroll
+        for (int k = 0; k < 8; k++) {
+            run = vec_seq_add<DT>(run, buf[lane * kStageRow + k]);
+            if (short_runs && ((k + 1) & ((1 << vrun_log2) - 1)) == 0) {
+                lane_tc.push(run);
+                run = -0.0f;
+            }
+        }
+        if (p == passes - 1) {
+            float piece = run;
+            if (short_runs) {
+                piece = lane_tc.finish();
+                lane_tc = TreeCounter<3>();
+            }
+            // the row's tree over its 2^lpr pieces, in lane order
+            for (int off = 1; off < (1 << lpr); off <<= 1)
+                piece = __fadd_rn(piece, __shfl_xor_sync(kFull, piece, off));
+            const size_t row = r * rpr + (size_t)(lane >> lpr);
+            if ((lane & ((1 << lpr) - 1)) == 0 && row < rows) out[row] = piece;
+            run = -0.0f;
+        }
+        if (!more) break;
+        r = nr;
+        p = np;
+    }
+}
+
 // ---------------------------------------------------------------- host
 
 static const void *pick(int dtype, bool aligned)
@@ -147,6 +240,41 @@ cudaError_t launch_blocked_chunk(int dtype, bool aligned, const void *x, size_t 
     void *args[] = {(void *)&x, (void *)&seg_len, (void *)&units, (void *)&cps,
                     (void *)&chunk_log2, (void *)&run_log2, (void *)&dst};
     return launch_first(k, dim3(grid), dim3(block), args, kStageBytesPerWarp * (block / 32), stream);
+}
+
+static const void *pick_rows(int dtype, bool aligned)
+{
+    switch (dtype) {
+    case kF16: return aligned ? (const void *)blocked_rows_kernel<kF16, true>
+                              : (const void *)blocked_rows_kernel<kF16, false>;
+    case kBF16: return aligned ? (const void *)blocked_rows_kernel<kBF16, true>
+                               : (const void *)blocked_rows_kernel<kBF16, false>;
+    case kF32: return aligned ? (const void *)blocked_rows_kernel<kF32, true>
+                              : (const void *)blocked_rows_kernel<kF32, false>;
+    default: return nullptr;
+    }
+}
+
+cudaError_t launch_blocked_rows(int dtype, bool aligned, const void *x, size_t rows, size_t cols,
+                                int run_log2, int lpr, float *out, int grid, int block, cudaStream_t stream)
+{
+    const void *k = pick_rows(dtype, aligned);
+    if (!k || block < 32 || block > 32 * kBlockedMaxWarps || lpr < 0 || lpr > 4) return cudaErrorInvalidValue;
+    void *args[] = {(void *)&x, (void *)&rows, (void *)&cols, (void *)&run_log2, (void *)&lpr, (void *)&out};
+    return launch_first(k, dim3(grid), dim3(block), args, kStageBytesPerWarp * (block / 32), stream);
+}
+
+int occupancy_blocked_rows(int dtype, bool aligned, int block)
+{
+    const void *k = pick_rows(dtype, aligned);
+    int n = 0;
+    if (!k || cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, block,
+                                                            kStageBytesPerWarp * (block / 32)) !=
+                  cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return n;
 }
 
 int occupancy_blocked(int dtype, bool aligned, int block)

@@ -57,6 +57,12 @@ cudaError_t launch_blocked_chunk(int dtype, bool aligned, const void *x, size_t 
                                  size_t units, size_t cps, int chunk_log2, int run_log2,
                                  float *dst, int grid, int block, cudaStream_t stream);
 int occupancy_blocked(int dtype, bool aligned, int block);
+// Rows whose pieces (max(run, 8 vectors) inputs each), padded to 2^lpr,
+// number at most 16 (lpr <= 4): 32 >> lpr whole rows to a warp's round,
+// out[r] = row r's value; one launch, no partials.
+cudaError_t launch_blocked_rows(int dtype, bool aligned, const void *x, size_t rows, size_t cols,
+                                int run_log2, int lpr, float *out, int grid, int block, cudaStream_t stream);
+int occupancy_blocked_rows(int dtype, bool aligned, int block);
 
 // ---- SHUFFLE_TREE (declared grid-stride order)
 // Block team: grid = segments * G CTAs of Bt threads; CTA (s, b) writes its

@@ -105,7 +105,9 @@ int occupancy(int dev, Family fam, bool rows, int dtype, int op, bool aligned, i
     if (dev >= 0) {
         switch (fam) {
         case kFixedF: n = occupancy_fixed(rows, dtype, op, aligned, block, R); break;
-        case kBlockedF: n = occupancy_blocked(dtype, aligned, block); break;
+        case kBlockedF:
+            n = rows ? occupancy_blocked_rows(dtype, aligned, block) : occupancy_blocked(dtype, aligned, block);
+            break;
         case kShuffleF: n = occupancy_shuffle(rows, dtype, op, aligned, block); break;
         case kMmaF: n = occupancy_mma(rows, dtype, op, aligned, R, block); break;
         case kPackedF:
@@ -246,6 +248,7 @@ enum Path {
     kPathTmem,           // MMA_CHAIN on tcgen05 (+ combine if units > 1)
     kPathTmemRows,       // MMA_CHAIN rows on tcgen05 (+ combine if chunks > 1)
     kPathBlocked,        // FIXED blocked order, runs longer than a vector (+ combine)
+    kPathBlockedRows,    // FIXED blocked order, rows of at most 16 pieces: several to a round
     kPathPackedRows      // short rows, several to a warp group (FIXED, SHUFFLE, MMA)
 };
 
@@ -318,6 +321,31 @@ void plan_blocked(Plan &p, bool rows_call, int dev)
 {
     p.path = kPathBlocked;
     const int sms = sm_count(dev);
+    if (rows_call) {
+        // rows of at most 16 pieces (a piece: max(run, 8 vectors) inputs),
+        // padded to 2^lpr: 32 >> lpr rows to a warp's round, one launch
+        const int lv0 = log2_exact(vector_len(p.dtype));
+        const int pl = p.run_log2 > lv0 + 3 ? p.run_log2 : lv0 + 3;
+        const int h = ceil_log2_sz(p.seg_len);
+        const int lpr = h > pl ? h - pl : 0;
+        if (lpr <= 4) {
+            p.path = kPathBlockedRows;
+            p.vlog = lpr;
+            p.block = 32 * 8;
+            const size_t rounds = (p.segments + ((size_t)32 >> lpr) - 1) / ((size_t)32 >> lpr);
+            const size_t need = (rounds + 7) / 8;
+            const size_t resident =
+                (size_t)sms * (size_t)occupancy(dev, kBlockedF, true, p.dtype, kOpSum, p.aligned, 0, p.block);
+            p.grid = (int)(need < resident ? need : resident);
+            p.units = rounds;
+            p.cps = 1;
+            p.chunk_log2 = 0;
+            p.partials = 0;
+            p.combine_count = 1;
+            p.launches = 1;
+            return;
+        }
+    }
     const int s0 = kWarpSpanBytesLog2 - log2_exact((int)elem_bytes(p.dtype));
     int span_log2 = s0;
     if (rows_call && ceil_log2_sz(p.seg_len) < span_log2) span_log2 = ceil_log2_sz(p.seg_len);
@@ -539,6 +567,10 @@ tcr_status run_plan(const Plan &p, const void *x, float *out, cudaStream_t s, in
     case kPathBlocked:
         e = launch_blocked_chunk(p.dtype, p.aligned, x, p.seg_len, p.units, p.cps, p.chunk_log2,
                                  p.run_log2, dst, p.grid, p.block, s);
+        break;
+    case kPathBlockedRows:
+        e = launch_blocked_rows(p.dtype, p.aligned, x, p.segments, p.seg_len, p.run_log2, p.vlog, dst,
+                                p.grid, p.block, s);
         break;
     case kPathMmaRows:
         e = launch_mma_rows(p.dtype, p.op, p.aligned, p.R, x, p.segments, p.seg_len, dst,
