@@ -162,12 +162,17 @@ cudaError_t launch_mean_var(const float *s1, const float *s2, size_t rows, size_
 // ---- split-K GEMM, C = A * W^T (k_gemm.cu): A M x K, W N x K row-major
 // 16-bit (16-byte aligned, K a multiple of 8), out = C (splits == 1) or the
 // partials P (splits x M x N); split s covers 64-column boxes
-// [s * kbps, min((s + 1) * kbps, ceil(K / 64))).  One persistent CTA per SM.
+// [s * kbps, min((s + 1) * kbps, ceil(K / 64))).  Persistent CTA pairs
+// (clusters of two SMs, 256 x 256 tiles, tcgen05.mma.cta_group::2), or one
+// CTA per SM with 128 x 256 tiles where a pair cannot be scheduled.
 // inject_stall: withhold the first tile's publication so that a wait runs
 // out its limit (tests of the failure path only).
 cudaError_t launch_gemm_splitk(int dtype, const void *A, const void *W, size_t M, size_t N, size_t K,
-                               int splits, int kbps, float *out, int grid, bool inject_stall,
-                               cudaStream_t stream);
+                               int splits, int kbps, float *out, bool inject_stall, cudaStream_t stream);
+// The grid launch_gemm_splitk uses, and the output tile it works in.
+int gemm_launch_grid(size_t M, size_t N, int splits);
+int gemm_tile_m_run();
+int gemm_tile_n_run();
 // C[i] = balanced tree over P[s * mn + i] in split order (waits for the GEMM).
 cudaError_t launch_splitk_combine(const float *P, size_t mn, int splits, float *C, cudaStream_t stream);
 cudaError_t read_gemm_faults(unsigned int *flags, bool clear);

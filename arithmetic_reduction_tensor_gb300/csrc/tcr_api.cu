@@ -838,12 +838,12 @@ tcr_status tcr_gemm_descriptor(size_t M, size_t N, size_t K, int splits, int dty
     desc->dtype = dtype;
     desc->splits = g.splits;
     desc->k_split = g.k_split;
-    desc->tile_m = gemm_tile_m();
-    desc->tile_n = gemm_tile_n();
+    desc->tile_m = (current_device() >= 0) ? gemm_tile_m_run() : gemm_tile_m();
+    desc->tile_n = (current_device() >= 0) ? gemm_tile_n_run() : gemm_tile_n();
     desc->tile_k = gemm_tile_k();
     desc->combine_order = TCR_ORDER_BALANCED_TREE;
     desc->workspace_bytes = g.workspace;
-    desc->launch_grid = g.grid;
+    desc->launch_grid = (current_device() >= 0) ? gemm_launch_grid(M, N, g.splits) : g.grid;
     desc->launch_block = gemm_block_threads();
     desc->launches = (M * N == 0) ? 0 : (K == 0 ? 0 : (g.splits > 1 ? 2 : 1));
     return TCR_OK;
@@ -875,7 +875,7 @@ tcr_status tcr_gemm_splitk(const void *A, const void *W, float *C, size_t M, siz
         if (P) (void)cudaFreeAsync(P, s);
         return TCR_ERR_CUDA;
     }
-    cudaError_t e = launch_gemm_splitk(dtype, A, W, M, N, K, g.splits, g.kbps, P ? P : C, g.grid,
+    cudaError_t e = launch_gemm_splitk(dtype, A, W, M, N, K, g.splits, g.kbps, P ? P : C,
                                        fault_injected("stall"), s);
     if (e == cudaSuccess && P) e = launch_splitk_combine(P, M * N, g.splits, C, s);
     if (P) {

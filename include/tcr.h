@@ -410,7 +410,11 @@ TCR_API tcr_status tcr_order_equivalent(const tcr_order_desc *a, const tcr_order
  * split order (-0.0 pad), formed by a second kernel, never by atomics.  So
  * the bits of C depend only on (A, W, M, N, K, dtype, S, k_split) -- not on
  * the grid, the scheduling of CTAs or the GPU model -- and two calls with
- * equal descriptors give identical bits.  Error bound per element:
+ * equal descriptors give identical bits.  The MMAs run on pairs of SMs
+ * (clusters of two CTAs issuing tcgen05.mma.cta_group::2 on 256 x 256
+ * output tiles, each SM holding half of each operand tile) where the device
+ * can co-schedule a pair, else one SM per 128 x 256 tile; the descriptor's
+ * tile_m, tile_n and launch_grid report which.  Error bound per element:
  *   |C - exact| <= (2^-22 * k_split / 16 + 2^-24 * ceil(log2 S)) * sum_k |a_ik w_jk| + 1e-30.
  *
  * tcr_gemm_descriptor -- fill *desc for a call (host only).
