@@ -35,6 +35,7 @@
 //                    to P_s (or straight to C when S = 1).
 // Every mbarrier wait gives up after about a second, raises g_gemm_fault,
 // drains its own copies and MMAs, frees TMEM and writes NaN to its tiles.
+#include <cstdlib>
 #include <cstring>
 
 #include "kernels.cuh"
@@ -684,9 +685,13 @@ int gemm_block_threads() { return kGmThreads; }
 
 // The CTA pairs of the pair kernel that can be resident at once on the
 // current device (a pair needs two SMs of one GPC), cached per device; 0
-// when a pair cannot be scheduled (the one-SM kernel runs instead).
+// when a pair cannot be scheduled (the one-SM kernel runs instead), or when
+// TCR_GEMM_ONE_SM is set in the environment (the one-SM kernel on request,
+// e.g. to test it on a device that does schedule pairs).
 int gemm_resident_pairs()
 {
+    const char *one = std::getenv("TCR_GEMM_ONE_SM");
+    if (one && one[0] != '\0' && one[0] != '0') return 0;
     static std::mutex mu;
     static std::vector<std::pair<int, int>> cache;
     int dev = 0;

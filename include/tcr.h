@@ -413,8 +413,9 @@ TCR_API tcr_status tcr_order_equivalent(const tcr_order_desc *a, const tcr_order
  * equal descriptors give identical bits.  The MMAs run on pairs of SMs
  * (clusters of two CTAs issuing tcgen05.mma.cta_group::2 on 256 x 256
  * output tiles, each SM holding half of each operand tile) where the device
- * can co-schedule a pair, else one SM per 128 x 256 tile; the descriptor's
- * tile_m, tile_n and launch_grid report which.  Error bound per element:
+ * can co-schedule a pair, else one SM per 128 x 256 tile (also when the
+ * environment variable TCR_GEMM_ONE_SM is set to a non-zero value); the
+ * descriptor's tile_m, tile_n and launch_grid report which.  Error bound per element:
  *   |C - exact| <= (2^-22 * k_split / 16 + 2^-24 * ceil(log2 S)) * sum_k |a_ik w_jk| + 1e-30.
  *
  * tcr_gemm_descriptor -- fill *desc for a call (host only).

@@ -63,7 +63,10 @@ def test_wait_limit_reports_nan_and_fault_word_then_recovers(monkeypatch):
     assert tcr.tcr_device_faults() == 0
 
 
-def test_gemm_wait_limit_reports_nan_and_fault_word_then_recovers(monkeypatch):
+@pytest.mark.parametrize("kernel", ["pair", "one_sm"])
+def test_gemm_wait_limit_reports_nan_and_fault_word_then_recovers(monkeypatch, kernel):
+    if kernel == "one_sm":
+        monkeypatch.setenv("TCR_GEMM_ONE_SM", "1")
     M, N, K = 512, 768, 1024
     ab = synth.generate(M * K, "normal", tcr.BF16, seed=23).reshape(M, K)
     wb = synth.generate(N * K, "normal", tcr.BF16, seed=24).reshape(N, K)

@@ -31,6 +31,15 @@ def gpu():
     torch.cuda.set_device(0)
 
 
+@pytest.fixture(autouse=True, params=["pair", "one_sm"])
+def gemm_kernel(request, monkeypatch):
+    # every test on both kernels: CTA pairs (the default where pairs can be
+    # scheduled) and one SM per tile (TCR_GEMM_ONE_SM)
+    if request.param == "one_sm":
+        monkeypatch.setenv("TCR_GEMM_ONE_SM", "1")
+    return request.param
+
+
 def dev(bits, dtype):
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda().view(TORCH_DT[dtype])
 
@@ -123,3 +132,15 @@ def test_degenerate_and_rejected():
         tcr.tcr_gemm_splitk(torch.zeros(4, 16, dtype=torch.float16, device="cuda"),
                             torch.zeros(4, 16, dtype=torch.float16, device="cuda"), splits=65)
     assert tcr.tcr_device_faults() == 0
+
+
+def test_descriptor_reports_the_kernel(gemm_kernel):
+    # a GB300 schedules CTA pairs: 256 x 256 tiles, two CTAs per pair; on
+    # request one SM per 128 x 256 tile
+    d = tcr.tcr_gemm_descriptor(4096, 4096, 4096, 0, BF16)
+    if gemm_kernel == "pair":
+        assert (d["tile_m"], d["tile_n"]) == (256, 256)
+        assert d["launch_grid"] % 2 == 0 and 2 <= d["launch_grid"] <= 152
+    else:
+        assert (d["tile_m"], d["tile_n"]) == (128, 256)
+        assert d["launch_grid"] <= 152
