@@ -46,7 +46,7 @@ constexpr int kTcStageBytes = kTcTileBytes * kTcTilesPerStage;
 constexpr int kTcStages = 6;                        // 192 KiB in flight per SM
 constexpr int kTcUnitLog2 = 16;                     // work unit: 2^16 inputs ...
 constexpr int kTcMinUnitLog2 = 11;                  // ... down to one tile for small inputs
-constexpr size_t kTcMinUnits = 2 * 152;             // the units small inputs are cut into
+constexpr size_t kTcMinUnits = 152 / 2;            // the units small inputs are cut into
 constexpr int kTcThreads = 192;
 constexpr int kTcEpilogueThreads = 128;
 constexpr int kTcDBuffers = 8;                      // chains the MMA may run ahead
@@ -1128,9 +1128,11 @@ static void *pick_dt(int R)
 }
 
 // 2^16 inputs per unit (one unit -- one launch, no partials -- up to 2^16
-// inputs); above that halved while it leaves fewer than two units per SM of
-// the 152 the rules assume, down to one tile.  A function of n only, so the
-// chunking (and MMA_CHAIN's bits) is the same on every device.
+// inputs); above that halved while it leaves fewer than one unit per two
+// SMs of the 152 the rules assume, down to one tile: every unit a CTA takes
+// over costs it a cancellation round trip, which small inputs cannot hide.
+// A function of n only, so the chunking (and MMA_CHAIN's bits) is the same
+// on every device.
 int tmem_unit_log2(size_t n)
 {
     int l = kTcUnitLog2;

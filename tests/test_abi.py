@@ -349,11 +349,11 @@ def test_small_inputs_get_smaller_ctas(lib):
 
 def test_tcgen05_units_shrink_for_small_inputs(lib):
     # the tcgen05 sum's work unit is 2^16 inputs (one unit, one launch, up to
-    # 2^16 inputs), above that halved while it leaves fewer than 2 x 152
+    # 2^16 inputs), above that halved while it leaves fewer than 152 / 2
     # units, down to one 2048-input tile
     def expected(n):
         l = 16
-        while n > 1 << 16 and l > 11 and -(-n // (1 << l)) < 304:
+        while n > 1 << 16 and l > 11 and -(-n // (1 << l)) < 76:
             l -= 1
         return l, -(-n // (1 << l))
     for n in (1, 2048, 1 << 16, (1 << 16) + 1, 100_000, 1 << 20, 1 << 24, 1 << 26, 1 << 30):
@@ -361,7 +361,7 @@ def test_tcgen05_units_shrink_for_small_inputs(lib):
         l, units = expected(n)
         assert d["chunk_log2"] == l, n
         assert d["partials"] == (units if units > 1 else 0), n
-    assert tcr.tcr_order_descriptor(n=1 << 20, mode=tcr.Mode(tcr.MMA_CHAIN_TMEM))["chunk_log2"] == 11
+    assert tcr.tcr_order_descriptor(n=1 << 20, mode=tcr.Mode(tcr.MMA_CHAIN_TMEM))["chunk_log2"] == 13
     assert tcr.tcr_order_descriptor(n=1 << 30, mode=tcr.Mode(tcr.MMA_CHAIN_TMEM))["chunk_log2"] == 16
 
 
