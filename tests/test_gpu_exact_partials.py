@@ -236,3 +236,26 @@ def test_sum_of_squares_exact(dtype):
     tr = t[:rows * cols].view(rows, cols)
     for R in (0, 1, 8):
         assert np.array_equal(rows_bits(tr, tcr.Mode(MMA, R=R, dtype=dtype), squares=True), er)
+
+
+# The tcgen05 rows kernel for rows of 1024 k columns (k a divisor or a
+# multiple of 16) reads the matrix as a flat array: a row is 8 k TMEM lanes
+# inside one warp (k = 1, 2, 4), two or four warps (k = 8, 16), or all 128
+# lanes over several stages (k = 32, 48, 64), or chunks of 65536 columns
+# with partials and the rows combine (k = 80, 128).  Row counts that leave a
+# partial last unit.
+FLAT_SHAPES = [(65, 1024), (33, 2048), (17, 4096), (9, 8192), (5, 16384), (3, 32768),
+               (2, 49152), (3, 65536), (2, 81920), (2, 131072)]
+
+
+@pytest.mark.parametrize("dtype", [F16, BF16])
+@pytest.mark.parametrize("shape", FLAT_SHAPES)
+def test_flat_tcgen05_rows_every_lane_layout(dtype, shape):
+    rows, cols = shape
+    x = synth.generate(rows * cols, "exact_int", dtype, seed=cols + rows).reshape(rows, cols)
+    t = to_dev(x.reshape(-1)).view(rows, cols)
+    e = bits_of(exact_rows_f32(x, dtype))
+    for R in (0, 1, 3, 5, 8):
+        assert np.array_equal(rows_bits(t, tcr.Mode(TMEM, R=R, dtype=dtype)), e), (shape, R)
+    # a single row alone gives its bits (no dependence on the row count)
+    assert np.array_equal(rows_bits(t[rows - 1:rows], tcr.Mode(TMEM, dtype=dtype)), e[rows - 1:rows])
