@@ -14,24 +14,33 @@
 // in whatever slot, so a contiguous 4 KiB of input is a valid A tile as it
 // lies in memory: no layout transform, no swizzle.
 //
-// CTA roles (192 threads, one persistent CTA per SM):
+// CTA roles (192 threads; one CTA per work unit, one resident per SM):
 //   warp 0, lane 0   producer: 32 KiB bulk copies (8 tiles) global -> a
 //                    6-stage shared-memory ring, completion by mbarrier
-//                    transaction count;
+//                    transaction count; while a unit's last stage streams
+//                    in it asks the hardware to cancel a CTA that has not
+//                    launched yet (cluster launch control) and takes that
+//                    CTA's unit next -- the other roles read the same
+//                    answers, so fast SMs take more units;
 //   warp 1           owns the TMEM allocation; lane 0 issues the MMAs:
 //                    R per chain into one of 8 D buffers, the first of a
 //                    chain without accumulate, tcgen05.commit after a chain
 //                    (D full) and after a stage (stage free);
 //   warps 2..5       epilogue: each thread reads its TMEM lane of column 0
-//                    of a full D buffer, adds it to its fp32 accumulator and
-//                    frees the buffer; at the end of a work unit (2^16
-//                    inputs) the 128 accumulators and any tail inputs past
-//                    the last whole tile are reduced into the unit's partial.
+//                    of a stage's full D buffers (one wait for the stage's
+//                    last chain, the loads issued together), adds them to
+//                    its fp32 accumulator and frees the buffers; at the end
+//                    of a work unit (2^16 inputs) the 128 accumulators and
+//                    any tail inputs past the last whole tile are reduced
+//                    into the unit's partial.
+// The set-up (barriers, ones, TMEM) runs before griddepcontrol.wait, beside
+// the stream's previous kernel (programmatic dependent launch).
 //
 // Every wait on an mbarrier gives up after about one second: the CTA then
 // raises a device-wide fault flag, drains its own copies and MMAs (again
-// with a limit), frees its TMEM and writes NaN as its partials, so a broken
-// pipeline shows up as a NaN result, never as a hang.
+// with a limit), frees its TMEM and writes NaN as its partials (and as the
+// partials of every unit it still takes over), so a broken pipeline shows
+// up as a NaN result, never as a hang.
 #include <cstring>
 
 #include "kernels.cuh"

@@ -107,20 +107,26 @@ cudaError_t launch_packed_rows_pair(int family, int dtype, int R, bool aligned, 
 int occupancy_packed(int family, int dtype, int op, int R, int vlog, bool aligned, bool pair);
 
 // ---- MMA_CHAIN on tcgen05 (bulk copies into shared memory, D in TMEM):
-// one persistent CTA per SM; dst[u] is the partial of work unit u (2^16
-// inputs, fewer for small n: 2^tmem_unit_log2(n)); x must be 16-byte
-// aligned.  inject_stall: withhold the first chain's publication so that a
-// wait runs out its limit (tests of the failure path only).
+// grid = tmem_units(n), one CTA per work unit, one resident per SM taking
+// over the units of those not yet launched; dst[u] is the partial of work
+// unit u (2^16 inputs, fewer for small n: 2^tmem_unit_log2(n)); x must be
+// 16-byte aligned.  inject_stall: withhold the publication of the chain the
+// epilogue waits for first, so that a wait runs out its limit (tests of the
+// failure path only).
 cudaError_t launch_mma_tmem(int dtype, int R, const uint16_t *x, size_t n, float *dst, int grid,
                             bool inject_stall, cudaStream_t stream);
 size_t tmem_units(size_t n);
 int tmem_block_threads();
 int tmem_unit_log2(size_t n);
-// Rows: one MMA tile holds 16 rows (8 of D's lanes to a row), the inputs
-// reach shared memory by 2-D tensor-map copies; dst[row * chunks + c] is
-// row `row`'s partial over column chunk c (tmem_rows_chunks(cols) chunks
-// per row; one chunk: dst is the output).
-// x must be 16-byte aligned and cols a multiple of 8, rows and cols < 2^31.
+// Rows: rows of 1024 k columns (k a divisor or a multiple of 16) as one
+// flat array of 32 KiB bulk copies, each lane group taking 1024 inputs of
+// one row (grid = the units, one CTA per unit, taken over as for sums);
+// other rows with one MMA tile holding 16 rows (8 of D's lanes to a row)
+// from 3-D tensor-map or per-row bulk copies (at most one CTA per SM; grid
+// from tmem_rows_grid).  dst[row * chunks + c] is row `row`'s partial over
+// column chunk c (tmem_rows_chunks(cols) chunks per row; one chunk: dst is
+// the output).  x must be 16-byte aligned and cols a multiple of 8, rows
+// and cols < 2^31.
 cudaError_t launch_mma_tmem_rows(int dtype, int R, const uint16_t *x, size_t rows, size_t cols,
                                  float *dst, int grid, bool inject_stall, cudaStream_t stream);
 // The device word the tcgen05 kernels set when a wait gave up (bit 0);
