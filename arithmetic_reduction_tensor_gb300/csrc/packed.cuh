@@ -261,11 +261,35 @@ __device__ __forceinline__ uint4 unaligned_vec(const uint4 (&q)[8], const uint4 
     // shift the 8 words by sb bytes: 2 words, 1 word, then half a word
     const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
     const uint32_t p = sb >> 2;
-    uint32_t u[6], t[5], o[4];
+    uint32_t t[5], o[4];
+    if constexpr (VLOG >= 5) {
+        // a load holds vectors of one row only, so sb is the same in every
+        // lane: a warp-uniform branch picks the words (no per-lane selects)
+        switch (p) {
+        case 0:
 #pragma unroll
-    for (int i = 0; i < 6; i++) u[i] = (p & 2) ? w[i + 2] : w[i];
+            for (int i = 0; i < 5; i++) t[i] = w[i];
+            break;
+        case 1:
 #pragma unroll
-    for (int i = 0; i < 5; i++) t[i] = (p & 1) ? u[i + 1] : u[i];
+            for (int i = 0; i < 5; i++) t[i] = w[i + 1];
+            break;
+        case 2:
+#pragma unroll
+            for (int i = 0; i < 5; i++) t[i] = w[i + 2];
+            break;
+        default:
+#pragma unroll
+            for (int i = 0; i < 5; i++) t[i] = w[i + 3];
+            break;
+        }
+    } else {
+        uint32_t u[6];
+#pragma unroll
+        for (int i = 0; i < 6; i++) u[i] = (p & 2) ? w[i + 2] : w[i];
+#pragma unroll
+        for (int i = 0; i < 5; i++) t[i] = (p & 1) ? u[i + 1] : u[i];
+    }
     const uint32_t hs = (sb & 2u) << 3;                  // 0 or 16 (0 for binary32)
     const uint32_t f = fill_word<DT, NEGZERO>();
 #pragma unroll
@@ -499,10 +523,14 @@ packed_rows_kernel(const void *__restrict__ xv, size_t rows, size_t cols, float 
         // a load past the end of every row of the group (rows spanning 2 or
         // 4 loads with fewer vectors than slots, e.g. 96 of 128): every
         // vector of it is the pad, so the trees skip it -- the pad tree is
-        // -0.0 (+0.0 for squares).  The MMA path keeps its straight-line
-        // chain (a branch there cost more than the zero tiles it saves)
+        // -0.0 (+0.0 for squares).  Aligned rows only: around the realigning
+        // shuffles of other rows the branch left the trees waiting on their
+        // loads (rows of 1001: 2.9 against 5.0 TB/s without it), and the
+        // realigned pad vectors give the same -0.0 trees.  The MMA path keeps
+        // its straight-line chain (a branch there cost more than the zero
+        // tiles it saves)
         auto pad_load = [&](int k) -> bool {
-            if constexpr (VLOG >= 6)
+            if constexpr (VLOG >= 6 && ALIGNED)
                 return (size_t)(32 * Elem<DT>::kPerVec) * (size_t)(k & ((1 << (VLOG - 5)) - 1)) >= cols;
             else
                 return false;
