@@ -350,7 +350,7 @@ constexpr int kG2BM = 256;                       // tile rows of the pair (128 p
 constexpr int kG2BN = 256;                       // tile columns (128 W rows per CTA)
 constexpr int kG2HalfBytes = 128 * kGmBK * 2;    // 16 KiB: a CTA's half of a box
 constexpr int kG2StageBytes = 2 * kG2HalfBytes;  // its A half + its W half
-constexpr int kG2Stages = 6;                     // 192 KiB ring
+constexpr int kG2Stages = 7;                     // 224 KiB ring (230.6 KB of shared memory in all)
 constexpr int kG2DBuffers = 2;                   // accumulators: a tile's epilogue beside the next's MMAs
 constexpr uint32_t kG2TmemCols = kG2DBuffers * kG2BN;    // 512: all of TMEM
 constexpr int kG2OffBars = kG2Stages * kG2StageBytes;
@@ -358,6 +358,7 @@ constexpr int kG2OffBars = kG2Stages * kG2StageBytes;
 constexpr int kG2NumBars = 2 * kG2Stages + 2 * kG2DBuffers + 1;
 constexpr int kG2OffMisc = kG2OffBars + 8 * kG2NumBars;
 constexpr int kG2SmemBytes = kG2OffMisc + 64 + 1024;
+static_assert(kG2SmemBytes <= 232448, "the pair kernel's shared memory fits one SM's 227 KiB");
 
 // Instruction descriptor of kind::f16 for the pair: M = 256, N = 256.
 template <int DT>
