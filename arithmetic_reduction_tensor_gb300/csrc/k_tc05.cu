@@ -16,7 +16,7 @@
 //
 // CTA roles (192 threads; one CTA per work unit, one resident per SM):
 //   warp 0, lane 0   producer: 32 KiB bulk copies (8 tiles) global -> a
-//                    6-stage shared-memory ring, completion by mbarrier
+//                    5-stage shared-memory ring, completion by mbarrier
 //                    transaction count; while a unit's last stage streams
 //                    in it asks the hardware to cancel a CTA that has not
 //                    launched yet (cluster launch control) and takes that
@@ -52,7 +52,7 @@ constexpr int kTcTileInputs = 2048;                 // one MMA: 128 x 16 inputs
 constexpr int kTcTileBytes = kTcTileInputs * 2;     // 4 KiB
 constexpr int kTcTilesPerStage = 8;                 // 32 KiB bulk copies
 constexpr int kTcStageBytes = kTcTileBytes * kTcTilesPerStage;
-constexpr int kTcStages = 6;                        // 192 KiB in flight per SM
+constexpr int kTcStages = 5;                        // 160 KiB in flight per SM (6 and 7: slower)
 constexpr int kTcUnitLog2 = 16;                     // work unit: 2^16 inputs ...
 constexpr int kTcMinUnitLog2 = 11;                  // ... down to one tile for small inputs
 constexpr size_t kTcMinUnits = 152 / 2;            // the units small inputs are cut into

@@ -80,12 +80,20 @@ __device__ __forceinline__ bool mbar_wait_f(uint32_t bar, uint32_t parity, volat
     }
 }
 
+// One bulk copy of `bytes` (a multiple of 16, both addresses 16-byte
+// aligned) from global memory into this CTA's shared memory, completing on
+// mbarrier `bar`.  The inputs are read once, so the copy carries an L2
+// evict-first policy: L2 drops its lines ahead of lines that other data
+// (partials, outputs) may still need.
 __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void *src, uint32_t bytes,
                                               uint32_t bar)
 {
+    uint64_t policy;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
     asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1], %2, [%3], %4;"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar), "l"(policy)
         : "memory");
 }
 
