@@ -264,30 +264,4 @@ cudaError_t launch_blocked_rows(int dtype, bool aligned, const void *x, size_t r
     return launch_first(k, dim3(grid), dim3(block), args, kStageBytesPerWarp * (block / 32), stream);
 }
 
-int occupancy_blocked_rows(int dtype, bool aligned, int block)
-{
-    const void *k = pick_rows(dtype, aligned);
-    int n = 0;
-    if (!k || cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, block,
-                                                            kStageBytesPerWarp * (block / 32)) !=
-                  cudaSuccess) {
-        (void)cudaGetLastError();
-        return 0;
-    }
-    return n;
-}
-
-int occupancy_blocked(int dtype, bool aligned, int block)
-{
-    const void *k = pick(dtype, aligned);
-    int n = 0;
-    if (!k || cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, block,
-                                                            kStageBytesPerWarp * (block / 32)) !=
-                  cudaSuccess) {
-        (void)cudaGetLastError();
-        return 0;
-    }
-    return n;
-}
-
 }  // namespace tcr

@@ -106,15 +106,4 @@ cudaError_t preload_fixed_chunk_sums()
     return cudaSuccess;
 }
 
-int occupancy_fixed(bool rows, int dtype, int op, bool aligned, int block, int vrun)
-{
-    const void *k = pick(rows, dtype, op, aligned, vrun);
-    int n = 0;
-    if (!k || cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, block, 0) != cudaSuccess) {
-        (void)cudaGetLastError();
-        return 0;
-    }
-    return n;
-}
-
 }  // namespace tcr

@@ -114,15 +114,4 @@ cudaError_t preload_mma_chunk_sums()
     return cudaSuccess;
 }
 
-int occupancy_mma(bool rows, int dtype, int op, bool aligned, int R, int block)
-{
-    void *k = pick(rows, dtype, op, aligned, R);
-    int n = 0;
-    if (!k || cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, block, 0) != cudaSuccess) {
-        (void)cudaGetLastError();
-        return 0;
-    }
-    return n;
-}
-
 }  // namespace tcr

@@ -252,15 +252,4 @@ cudaError_t launch_shuffle_rows_warp(int dtype, int op, bool aligned, const void
     return launch_first(k, dim3(grid), dim3(block), args, 0, stream);
 }
 
-int occupancy_shuffle(bool rows, int dtype, int op, bool aligned, int block)
-{
-    const void *k = pick(rows, dtype, op, aligned);
-    int n = 0;
-    if (!k || cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, block, 0) != cudaSuccess) {
-        (void)cudaGetLastError();
-        return 0;
-    }
-    return n;
-}
-
 }  // namespace tcr

@@ -56,13 +56,11 @@ cudaError_t launch_fixed_rows_warp(int dtype, int op, bool aligned, const void *
 cudaError_t launch_blocked_chunk(int dtype, bool aligned, const void *x, size_t seg_len,
                                  size_t units, size_t cps, int chunk_log2, int run_log2,
                                  float *dst, int grid, int block, cudaStream_t stream);
-int occupancy_blocked(int dtype, bool aligned, int block);
 // Rows whose pieces (max(run, 8 vectors) inputs each), padded to 2^lpr,
 // number at most 16 (lpr <= 4): 32 >> lpr whole rows to a warp's round,
 // out[r] = row r's value; one launch, no partials.
 cudaError_t launch_blocked_rows(int dtype, bool aligned, const void *x, size_t rows, size_t cols,
                                 int run_log2, int lpr, float *out, int grid, int block, cudaStream_t stream);
-int occupancy_blocked_rows(int dtype, bool aligned, int block);
 
 // ---- SHUFFLE_TREE (declared grid-stride order)
 // Block team: grid = segments * G CTAs of Bt threads; CTA (s, b) writes its
@@ -201,10 +199,5 @@ cudaError_t preload_fixed_chunk_sums();
 cudaError_t preload_mma_chunk_sums();
 cudaError_t preload_combine();
 
-// Resident CTAs per SM of each kernel at a block size (occupancy API);
-// `rows` selects the per-row variant.  0 if the query fails.
-int occupancy_fixed(bool rows, int dtype, int op, bool aligned, int block, int vrun = 0);
-int occupancy_shuffle(bool rows, int dtype, int op, bool aligned, int block);
-int occupancy_mma(bool rows, int dtype, int op, bool aligned, int R, int block);
 
 }  // namespace tcr

@@ -24,7 +24,7 @@ constexpr int kDefaultBlock = 256;
 constexpr int kRuleSMs = 152;
 
 // Kernel families of the occupancy cache.
-enum Family { kFixedF, kShuffleF, kMmaF, kBlockedF, kPackedF };
+enum Family { kPackedF };
 
 // The current device, or -1 (the CUDA error is cleared).
 int current_device();
@@ -56,6 +56,14 @@ struct ChunkSplit {
     size_t cps;       // chunks per segment
 };
 ChunkSplit chunk_split(size_t segments, size_t seg_len, int dtype, int block, bool may_shrink);
+
+// The grid of a warp-stream kernel launched with one CTA per work unit
+// (CTAs walk the units grid-stride, so a grid clamped to the launch limit
+// still covers them all).
+inline int unit_grid(size_t units)
+{
+    return (int)(units < (size_t)0x7fffffff ? units : (size_t)0x7fffffff);
+}
 
 }  // namespace plan
 }  // namespace tcr

@@ -552,7 +552,8 @@ struct PairReducer {
 // Chunked: CTA work unit u = (segment u / cps, chunk u % cps); the chunk of
 // 2^chunk_log2 inputs is split into one aligned span per warp; dst[u] is
 // the balanced tree over the CTA's warp values (warp order, -0.0 pad).
-// Persistent: CTA b takes units b, b + grid, b + 2*grid, ...
+// CTA b takes units b, b + grid, b + 2*grid, ... (launched with one CTA
+// per unit, so a CTA normally takes one).
 template <class Red, bool ALIGNED>
 __device__ __forceinline__ void chunk_body(const void *__restrict__ xv, size_t seg_len,
                                            size_t units, size_t cps, int chunk_log2,
@@ -619,7 +620,8 @@ __device__ __forceinline__ void chunk_body(const void *__restrict__ xv, size_t s
 }
 
 // One warp per row (rows of at most 2^LEVELS groups): out[r] is the row's
-// value.  Persistent: warp w takes rows w, w + warps, w + 2*warps, ...
+// value.  Warp w takes rows w, w + warps, w + 2*warps, ... (launched with
+// one warp per row, so a warp normally takes one).
 template <class Red, bool ALIGNED>
 __device__ __forceinline__ void rows_body(const void *__restrict__ xv, size_t rows,
                                           size_t cols, float *__restrict__ out)

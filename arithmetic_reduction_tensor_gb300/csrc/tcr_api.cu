@@ -104,12 +104,6 @@ int occupancy(int dev, Family fam, bool rows, int dtype, int op, bool aligned, i
     int n = 0;
     if (dev >= 0) {
         switch (fam) {
-        case kFixedF: n = occupancy_fixed(rows, dtype, op, aligned, block, R); break;
-        case kBlockedF:
-            n = rows ? occupancy_blocked_rows(dtype, aligned, block) : occupancy_blocked(dtype, aligned, block);
-            break;
-        case kShuffleF: n = occupancy_shuffle(rows, dtype, op, aligned, block); break;
-        case kMmaF: n = occupancy_mma(rows, dtype, op, aligned, R, block); break;
         case kPackedF:
             // R carries the pair flag, the packed family, the row width and
             // the chain length
@@ -291,10 +285,21 @@ void shuffle_team(size_t L, int V, int B, int *Bt, int *G)
 }
 
 
-// The chunked kernels' plan: the work split of chunk_split, a grid of at most
-// one wave of resident CTAs, and a combine launch when a segment has several
-// chunks.
-void plan_chunked(Plan &p, int dev, Family fam, bool may_shrink)
+// Grids of the warp-stream kernels.  Their CTAs walk work units (chunks,
+// rows) grid-stride, so any grid gives the same bits.  They are launched
+// with one CTA per unit (per 8 rows): the hardware block scheduler hands
+// the next CTA to whichever SM frees a slot, so the SMs end within a unit
+// of each other, and the CTAs resident beside a starting one keep the SM's
+// loads in flight.  One persistent wave with units dealt round-robin ran
+// 7-12 us longer on 2^30-input sums and 2 us on 65536 x 4096 rows: the
+// static split left SMs streaming alone at the end.  Packed short rows keep
+// a warp's next group in flight while it reduces the current one, so they
+// take a few waves rather than one group per warp.
+constexpr size_t kPackedWaves = 8;
+
+// The chunked kernels' plan: the work split of chunk_split, one CTA per
+// unit, and a combine launch when a segment has several chunks.
+void plan_chunked(Plan &p, bool may_shrink)
 {
     p.path = kPathChunk;
     const ChunkSplit c = chunk_split(p.segments, p.seg_len, p.dtype, p.block, may_shrink);
@@ -302,11 +307,7 @@ void plan_chunked(Plan &p, int dev, Family fam, bool may_shrink)
     p.chunk_log2 = c.chunk_log2;
     p.cps = c.cps;
     p.units = p.segments * c.cps;
-    const size_t resident =
-        (size_t)sm_count(dev) *
-        (size_t)occupancy(dev, fam, false, p.dtype, p.op, p.aligned,
-                          fam == kFixedF ? p.vrun : p.R, p.block);
-    p.grid = (int)(p.units < resident ? p.units : resident);
+    p.grid = unit_grid(p.units);
     p.partials = p.cps > 1 ? p.units : 0;
     p.combine_count = p.cps;
     p.launches = p.cps > 1 ? 2 : 1;
@@ -333,10 +334,7 @@ void plan_blocked(Plan &p, bool rows_call, int dev)
             p.vlog = lpr;
             p.block = 32 * 8;
             const size_t rounds = (p.segments + ((size_t)32 >> lpr) - 1) / ((size_t)32 >> lpr);
-            const size_t need = (rounds + 7) / 8;
-            const size_t resident =
-                (size_t)sms * (size_t)occupancy(dev, kBlockedF, true, p.dtype, kOpSum, p.aligned, 0, p.block);
-            p.grid = (int)(need < resident ? need : resident);
+            p.grid = unit_grid((rounds + 7) / 8);
             p.units = rounds;
             p.cps = 1;
             p.chunk_log2 = 0;
@@ -367,9 +365,7 @@ void plan_blocked(Plan &p, bool rows_call, int dev)
         w /= 2;
     }
     p.block = 32 * w;
-    const size_t resident =
-        (size_t)sms * (size_t)occupancy(dev, kBlockedF, false, p.dtype, kOpSum, p.aligned, 0, p.block);
-    p.grid = (int)(p.units < resident ? p.units : resident);
+    p.grid = unit_grid(p.units);
     p.partials = p.cps > 1 ? p.units : 0;
     p.combine_count = p.cps;
     p.launches = p.cps > 1 ? 2 : 1;
@@ -378,7 +374,8 @@ void plan_blocked(Plan &p, bool rows_call, int dev)
 constexpr size_t kTmemRowsMinCols = 768;
 
 // Short rows, several to a warp group: one launch of kRowsBlock threads,
-// as many CTAs as there are groups of 8 warps' rows, at most a full wave.
+// as many CTAs as there are groups of 8 warps' rows, at most kPackedWaves
+// full waves.
 void plan_packed(Plan &p, int family, bool pair, int dev)
 {
     p.path = kPathPackedRows;
@@ -391,7 +388,7 @@ void plan_packed(Plan &p, int family, bool pair, int dev)
     const int key = (pair ? 1000 : 0) + family * 100 + p.vlog * 10 + (p.R > 0 ? p.R : 1);
     const size_t resident = (size_t)sm_count(dev) *
                             (size_t)occupancy(dev, kPackedF, true, p.dtype, p.op, p.aligned, key, p.block);
-    p.grid = (int)(need < resident ? need : resident);
+    p.grid = unit_grid(need < kPackedWaves * resident ? need : kPackedWaves * resident);
     p.launches = 1;
 }
 
@@ -434,9 +431,7 @@ Plan make_plan(size_t segments, size_t seg_len, bool rows_call, const tcr_mode &
             p.block = kRowsBlock;
             const size_t warps_per_cta = (size_t)p.block / 32;
             const size_t need = (segments + warps_per_cta - 1) / warps_per_cta;
-            const size_t resident =
-                sms * (size_t)occupancy(dev, kShuffleF, true, p.dtype, op, aligned, 0, p.block);
-            p.grid = (int)(need < resident ? need : resident);
+            p.grid = unit_grid(need);
             p.launches = 1;
         } else {
             p.path = kPathShuffleBlock;
@@ -490,8 +485,6 @@ Plan make_plan(size_t segments, size_t seg_len, bool rows_call, const tcr_mode &
             return p;
         }
     }
-    const Family fam = m.kind == TCR_FIXED_ORDER ? kFixedF : kMmaF;
-    const int occ_r = m.kind == TCR_FIXED_ORDER ? p.vrun : R;
     if (rows_call && p.vrun == 0) {
         const int pf = m.kind == TCR_FIXED_ORDER ? kPackedFixed : kPackedMma;
         if (packed_rows_supported(pf, p.dtype, op, seg_len, vector_len(p.dtype), aligned, pair)) {
@@ -505,14 +498,12 @@ Plan make_plan(size_t segments, size_t seg_len, bool rows_call, const tcr_mode &
         p.block = block = kRowsBlock;
         const size_t warps_per_cta = (size_t)block / 32;
         const size_t need = (segments + warps_per_cta - 1) / warps_per_cta;
-        const size_t resident =
-            sms * (size_t)occupancy(dev, fam, true, p.dtype, op, aligned, occ_r, block);
         p.path = m.kind == TCR_FIXED_ORDER ? kPathFixedRowsWarp : kPathMmaRows;
-        p.grid = (int)(need < resident ? need : resident);
+        p.grid = unit_grid(need);
         p.launches = 1;
         return p;
     }
-    plan_chunked(p, dev, fam, m.kind == TCR_FIXED_ORDER || m.block_threads == 0);
+    plan_chunked(p, m.kind == TCR_FIXED_ORDER || m.block_threads == 0);
     return p;
 }
 

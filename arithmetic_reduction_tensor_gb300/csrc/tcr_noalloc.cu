@@ -113,11 +113,7 @@ extern "C" tcr_status tcr_reduce_sum_noalloc(const void *x, size_t n, float *out
 
     const bool aligned = ((uintptr_t)x & 15u) == 0;
     const bool fixed = mode.kind == TCR_FIXED_ORDER;
-    const size_t resident =
-        (size_t)sm_count(dev) *
-        (size_t)occupancy(dev, fixed ? kFixedF : kMmaF, false, mode.dtype, kOpSum, aligned,
-                          fixed ? 0 : R, c.block);
-    const int grid = (int)(c.cps < resident ? c.cps : resident);
+    const int grid = unit_grid(c.cps);      // one CTA per chunk, as tcr_reduce_sum launches
     float *dst = c.cps > 1 ? partials : out;
     cudaError_t e = fixed ? launch_fixed_chunk(mode.dtype, kOpSum, aligned, x, n, c.cps, c.cps,
                                                c.chunk_log2, dst, grid, c.block, s)

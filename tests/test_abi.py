@@ -144,7 +144,7 @@ def test_short_rows_are_packed(lib):
         assert grid(1000, 65, kind) == 8              # 9 vectors: 16 rows a warp
         assert grid(1000, 1024, kind) == 63           # 128 vectors: 2 rows a warp
         assert grid(1000, 1025, kind) == 125          # one warp per row
-        assert grid(10 ** 6, 100, kind) == 152        # at most one wave
+        assert grid(10 ** 6, 100, kind) == 8 * 152    # at most eight waves
     # rows that are not whole vectors pack the same way
     assert grid(1000, 255, tcr.FIXED_ORDER) == 16     # 32 vectors: 8 rows a warp
     assert grid(1000, 1020, tcr.SHUFFLE_TREE) == 63   # 128 vectors: 2 rows a warp
