@@ -14,9 +14,9 @@
 // in whatever slot, so a contiguous 4 KiB of input is a valid A tile as it
 // lies in memory: no layout transform, no swizzle.
 //
-// CTA roles (192 threads; one CTA per work unit, one resident per SM):
+// CTA roles (192 threads; one CTA per work unit, two resident per SM):
 //   warp 0, lane 0   producer: 32 KiB bulk copies (8 tiles) global -> a
-//                    5-stage shared-memory ring, completion by mbarrier
+//                    2-stage shared-memory ring, completion by mbarrier
 //                    transaction count; while a unit's last stage streams
 //                    in it asks the hardware to cancel a CTA that has not
 //                    launched yet (cluster launch control) and takes that
@@ -52,15 +52,26 @@ constexpr int kTcTileInputs = 2048;                 // one MMA: 128 x 16 inputs
 constexpr int kTcTileBytes = kTcTileInputs * 2;     // 4 KiB
 constexpr int kTcTilesPerStage = 8;                 // 32 KiB bulk copies
 constexpr int kTcStageBytes = kTcTileBytes * kTcTilesPerStage;
-constexpr int kTcStages = 5;                        // 160 KiB in flight per SM (6 and 7: slower)
+constexpr int kTcStages = 2;                        // 64 KiB a CTA, 128 KiB in flight per SM
+// Resident CTAs of the sum and flat rows kernels, and the shared-memory
+// carveout their launches ask for (percent of the 228 KiB maximum: the
+// 164 KiB configuration).  Two CTAs per SM take over units faster than one
+// with a deeper ring; three need the 228 KiB configuration, and an SM keeps
+// its configuration while the stream's next kernel runs on it: with 28 KiB
+// (or 60 KiB) of L1 left, the streaming kernels after a tcgen05 call ran
+// about 14% slower.
+constexpr int kTcCtasPerSm = 2;
+constexpr int kTcCarveoutPercent = 72;
+constexpr int kTcCarveoutBytes = 164 * 1024;
 constexpr int kTcUnitLog2 = 16;                     // work unit: 2^16 inputs ...
 constexpr int kTcMinUnitLog2 = 11;                  // ... down to one tile for small inputs
 constexpr size_t kTcMinUnits = 152 / 2;            // the units small inputs are cut into
 constexpr int kTcThreads = 192;
 constexpr int kTcEpilogueThreads = 128;
 constexpr int kTcDBuffers = 8;                      // chains the MMA may run ahead
-constexpr uint32_t kTcDBufferStride = 32;           // columns per D buffer (N = 16 used)
-constexpr uint32_t kTcTmemCols = kTcDBuffers * kTcDBufferStride;    // 256
+constexpr uint32_t kTcDBufferStride = 16;           // columns per D buffer (N = 16)
+constexpr uint32_t kTcTmemCols = kTcDBuffers * kTcDBufferStride;    // 128
+static_assert(kTcCtasPerSm * kTcTmemCols <= 512, "the resident CTAs' TMEM fits an SM's 512 columns");
 
 constexpr uint32_t kTcClcSlots = 16;                // cancellation responses in flight
 constexpr uint32_t kTcRecent = 32;                  // units the producer remembers (abort path)
@@ -75,6 +86,9 @@ static_assert(512 + 16 * kTcClcSlots <= 1024, "responses fit beside the ones");
 constexpr int kTcNumBars = 2 * kTcStages + 2 * kTcDBuffers + 1 + 2 * kTcClcSlots;
 constexpr int kTcOffMisc = kTcOffBars + 8 * kTcNumBars;     // tmem addr, abort, red[4], next unit
 constexpr int kTcSmemBytes = kTcOffMisc + 64 + 1024;                    // + alignment slack
+// an SM has 228 KiB of shared memory, of which each CTA reserves 1 KiB
+static_assert(kTcCtasPerSm * (kTcSmemBytes + 1024) <= kTcCarveoutBytes,
+              "the resident CTAs fit the carveout (each CTA reserves 1 KiB more)");
 
 __device__ unsigned int g_tc05_fault;               // non-zero once any wait gave up
 
@@ -143,7 +157,7 @@ __device__ __forceinline__ int unit_tiles(size_t n, size_t u, int unit_log2)
 }
 
 template <int DT, int R>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
 mma_tmem_kernel(const uint16_t *__restrict__ x, size_t n, int unit_log2, float *__restrict__ dst,
                 uint32_t inject_stall)
 {
@@ -401,7 +415,7 @@ mma_tmem_kernel(const uint16_t *__restrict__ x, size_t n, int unit_log2, float *
                 if (!__all_sync(kFull, ok)) break;
                 tc_fence_after();
                 uint32_t v[8];
-                tc_ld_chain_cols(tmem + lane_base, b, nc, v);
+                tc_ld_chain_cols(tmem + lane_base, kTcDBufferStride, b, nc, v);
 #pragma unroll
                 for (int i = 0; i < 8; i++)
                     if (i < nc) acc = __fadd_rn(acc, __uint_as_float(v[i]));
@@ -808,7 +822,7 @@ __host__ __device__ inline bool flat_rows_shape(size_t cols)
 }
 
 template <int DT, int R>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
 mma_tmem_rows_flat_kernel(const uint16_t *__restrict__ x, uint32_t rows, uint32_t cols, uint32_t unit_rows,
                           uint32_t chunk_cols, uint32_t cpr, float *__restrict__ dst, uint32_t inject_stall)
 {
@@ -1056,7 +1070,7 @@ mma_tmem_rows_flat_kernel(const uint16_t *__restrict__ x, uint32_t rows, uint32_
                 if (ok) {
                     tc_fence_after();
                     uint32_t v[8];
-                    tc_ld_chain_cols(tmem + lane_base, b, kChains, v);
+                    tc_ld_chain_cols(tmem + lane_base, kTcDBufferStride, b, kChains, v);
 #pragma unroll
                     for (int i = 0; i < kChains; i++) acc = __fadd_rn(acc, __uint_as_float(v[i]));
                     tc_fence_before();
@@ -1163,7 +1177,7 @@ cudaError_t launch_mma_tmem(int dtype, int R, const uint16_t *x, size_t n, float
 {
     void *k = dtype == kF16 ? pick_dt<kF16>(R) : pick_dt<kBF16>(R);
     if (!k) return cudaErrorInvalidValue;
-    cudaError_t e = set_smem_once(k, kTcSmemBytes);
+    cudaError_t e = set_smem_once(k, kTcSmemBytes, kTcCarveoutPercent);
     if (e != cudaSuccess) return e;
     // one CTA per unit: the CTAs running take over those still waiting to
     // launch (cluster launch control), so fast SMs take more units
@@ -1250,7 +1264,7 @@ cudaError_t launch_mma_tmem_rows(int dtype, int R, const uint16_t *x, size_t row
         const size_t units = tmem_rows_units(rows, cols);
         if (units != (size_t)grid || rows >= ((size_t)1 << 31) || cols >= ((size_t)1 << 31))
             return cudaErrorInvalidValue;
-        cudaError_t e = set_smem_once(k, kTcSmemBytes);
+        cudaError_t e = set_smem_once(k, kTcSmemBytes, kTcCarveoutPercent);
         if (e != cudaSuccess) return e;
         uint32_t r32 = (uint32_t)rows, c32 = (uint32_t)cols, ur = (uint32_t)flat_unit_rows(cols);
         uint32_t cc = (uint32_t)(cols < kFlatUnitInputs ? cols : kFlatUnitInputs);

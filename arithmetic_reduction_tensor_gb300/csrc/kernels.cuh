@@ -105,7 +105,7 @@ cudaError_t launch_packed_rows_pair(int family, int dtype, int R, bool aligned, 
 int occupancy_packed(int family, int dtype, int op, int R, int vlog, bool aligned, bool pair);
 
 // ---- MMA_CHAIN on tcgen05 (bulk copies into shared memory, D in TMEM):
-// grid = tmem_units(n), one CTA per work unit, one resident per SM taking
+// grid = tmem_units(n), one CTA per work unit, two resident per SM taking
 // over the units of those not yet launched; dst[u] is the partial of work
 // unit u (2^16 inputs, fewer for small n: 2^tmem_unit_log2(n)); x must be
 // 16-byte aligned.  inject_stall: withhold the publication of the chain the

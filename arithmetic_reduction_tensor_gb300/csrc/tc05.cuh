@@ -140,17 +140,18 @@ __device__ __forceinline__ void tc_commit(uint32_t bar)
 }
 
 // Column 0 of the n D buffers b0, b0 + 1, ... (mod 8; buffer b at columns
-// `base + 32 b`) for the calling thread's TMEM lane, n <= 8, the loads
+// `base + stride * b`) for the calling thread's TMEM lane, n <= 8, the loads
 // issued together and waited for once; v[i] for i >= n is left unchanged.
 // Warp-collective: b0 and n must be the same in every lane.
-__device__ __forceinline__ void tc_ld_chain_cols(uint32_t base, int b0, int n, uint32_t (&v)[8])
+__device__ __forceinline__ void tc_ld_chain_cols(uint32_t base, uint32_t stride, int b0, int n,
+                                                 uint32_t (&v)[8])
 {
 #pragma unroll
     for (int i = 0; i < 8; i++)
         if (i < n)
             asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];"
                          : "=r"(v[i])
-                         : "r"(base + 32u * (uint32_t)((b0 + i) & 7))
+                         : "r"(base + stride * (uint32_t)((b0 + i) & 7))
                          : "memory");
     asm volatile("tcgen05.wait::ld.sync.aligned;"
                  : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]), "+r"(v[6]),
@@ -246,9 +247,10 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
 
 // ---------------------------------------------------------------- host
 
-// The shared-memory opt-in is a per-kernel attribute: set it once per
-// device and kernel instance.
-inline cudaError_t set_smem_once(void *k, int bytes)
+// The shared-memory opt-in (and, where given, the preferred shared-memory
+// carveout, in percent of the maximum) are per-kernel attributes: set them
+// once per device and kernel instance.
+inline cudaError_t set_smem_once(void *k, int bytes, int carveout_percent = -1)
 {
     static std::mutex mu;
     static std::vector<std::pair<int, void *>> done;
@@ -258,6 +260,8 @@ inline cudaError_t set_smem_once(void *k, int bytes)
     for (auto &d : done)
         if (d.first == dev && d.second == k) return cudaSuccess;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && carveout_percent >= 0)
+        e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, carveout_percent);
     if (e == cudaSuccess) done.emplace_back(dev, k);
     return e;
 }

@@ -462,8 +462,8 @@ Plan make_plan(size_t segments, size_t seg_len, bool rows_call, const tcr_mode &
         return p;
     }
     if (p.kind == TCR_MMA_CHAIN_TMEM && !rows_call && aligned && tmem_units(seg_len) < ((size_t)1 << 31)) {
-        // one CTA per unit, one resident per SM (its shared-memory ring fills
-        // the SM); the resident CTAs take over the units of those waiting
+        // one CTA per unit, two resident per SM; the resident CTAs take
+        // over the units of those waiting
         p.path = kPathTmem;
         p.block = tmem_block_threads();
         p.chunk_log2 = tmem_unit_log2(seg_len);
