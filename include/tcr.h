@@ -326,8 +326,7 @@ typedef enum {
  *                    over its vector_len inputs, missing inputs being -0.0.
  *                    The team is one warp (32, 1) when the segment has at
  *                    most 1024 vectors, else Bt = block_threads and
- *                    G = ceil(vectors / (16 * Bt)) clamped to
- *                    1 .. 152 * 1024 / Bt.
+ *                    G = ceil(vectors / (16 * Bt)).
  *   chain_R          MMA_CHAIN: MMAs per chain (after defaults).
  *   pad_negative_zero 1: padding inputs and absent subtrees are -0.0.
  *   launch_grid, launch_block, chunk_log2, partials, launches

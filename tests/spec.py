@@ -4,7 +4,7 @@ The SHUFFLE_TREE order of a segment of L inputs at block size B is fixed by
 its team (Bt threads per block, G blocks).  With V inputs per 16-byte vector
 (8 for 16-bit inputs, 4 for binary32) and nvec = ceil(L / V) vectors: one
 warp (Bt = 32, G = 1) when nvec <= 1024, otherwise Bt = B and
-G = ceil(nvec / (B * 16)) clamped to [1, 152 * 1024 / B].  Written here from
+G = ceil(nvec / (B * 16)).  Written here from
 that statement, not taken from the library, so that a test can check the
 library's descriptor against it and feed the oracle with it.
 """
@@ -29,7 +29,7 @@ def shuffle_team(L: int, block: int = 0, dtype: int = 0) -> tuple[int, int]:
     if nvec <= 1024:
         return 32, 1
     g = math.ceil(nvec / (B * 16))
-    return B, max(1, min(g, 152 * 1024 // B))
+    return B, max(1, g)
 
 
 def default_R(block: int = 0) -> int:
