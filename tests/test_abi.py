@@ -206,6 +206,28 @@ def test_fixed_descriptor_is_the_balanced_tree(lib):
         assert d["launches"] == 2
 
 
+def test_warp_stream_kernels_launch_one_cta_per_unit(lib):
+    # The chunked sums, the one-warp rows, the blocked order and the
+    # SHUFFLE_TREE block team launch every work unit as its own CTA (the
+    # block scheduler balances the SMs; the bits do not depend on the grid):
+    # launch_grid equals the partials of a sum, one CTA per 8 rows of the
+    # one-warp rows kernels; packed short rows take at most eight waves.
+    for kind in (tcr.MMA_CHAIN, tcr.FIXED_ORDER, tcr.SHUFFLE_TREE):
+        d = tcr.tcr_order_descriptor(n=1 << 30, mode=tcr.Mode(kind))
+        assert d["launch_grid"] == d["partials"] > 152 * 8
+        d = tcr.tcr_order_descriptor(rows=65536, cols=4096, mode=tcr.Mode(kind))
+        assert (d["launch_grid"], d["launch_block"], d["partials"]) == (65536 // 8, 256, 0)
+    # the declared SHUFFLE_TREE team of a 2^30 sum: about 16 vectors per
+    # thread, no cap at one wave of resident blocks
+    d = tcr.tcr_order_descriptor(n=1 << 30, mode=tcr.Mode(tcr.SHUFFLE_TREE))
+    assert (d["team_threads"], d["team_blocks"]) == (256, (1 << 27) // (256 * 16))
+    # blocked order: a sum's chunks, and rows of at most 16 runs, 8 warp rounds a CTA
+    d = tcr.tcr_order_descriptor(n=1 << 30, mode=tcr.Mode(tcr.FIXED_ORDER, run_log2=8))
+    assert d["launch_grid"] == d["partials"]
+    d = tcr.tcr_order_descriptor(rows=65536, cols=4096, mode=tcr.Mode(tcr.FIXED_ORDER, run_log2=8))
+    assert d["launch_grid"] == 65536 // 2 // 8 and d["partials"] == 0
+
+
 def test_mma_descriptor_defaults_R_by_block(lib):
     for blk in (32, 64, 128, 256, 512, 1024):
         d = tcr.tcr_order_descriptor(n=1 << 20, mode=tcr.Mode(tcr.MMA_CHAIN, block_threads=blk))
