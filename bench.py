@@ -378,7 +378,7 @@ def read_ceiling(x):
     out = torch.empty(1, dtype=torch.int32, device=x.device)
     best = None
     for block in (256, 512, 1024):
-        for ctas in (1, 2, 4, 8):
+        for ctas in (-1, 1, 2, 4, 8):          # -1: one CTA per chunk of 8 x block vectors
             if block * ctas > 2048:
                 continue
             us = timed_median_us(lambda: tcr.tcr_read_probe(x, ctas, block, out=out), 10, 2)
@@ -387,7 +387,8 @@ def read_ceiling(x):
                 best = {"gbps": round(gbps, 1), "ctas_per_sm": ctas, "block": block}
     best.update({"bytes": nbytes, "kernel": "read_probe_kernel",
                  "how": "16-byte streaming loads, 8 in flight per thread, XOR of the words; "
-                        "best grid shape, median of 10 launches each, queued back to back"})
+                        "best grid shape (1-8 resident CTAs per SM striding over the input, or one "
+                        "CTA per chunk: ctas_per_sm -1), median of 10 launches each, queued back to back"})
     return best
 
 

@@ -474,8 +474,12 @@ TCR_API tcr_status tcr_device_faults(unsigned int *flags, int clear);
  * device word, 4-byte aligned (set to 0 first, on the stream, so the call is
  * a memset and one kernel launch).  Grid: ctas_per_sm CTAs (0: as many as
  * fit) of block_threads threads (0: 512; else a power of two in 32..1024)
- * on every SM.  TCR_ERR_INVALID_ARG on a bad argument, TCR_ERR_CUDA if the
- * device cannot be queried or the launch fails.  Asynchronous.
+ * on every SM, each thread striding over the whole input; or, for
+ * ctas_per_sm = -1, one CTA per 8 x block_threads vectors (each thread eight
+ * loads in flight, the block scheduler placing the CTAs -- the launch shape
+ * of the reduction kernels).  TCR_ERR_INVALID_ARG on a bad argument,
+ * TCR_ERR_CUDA if the device cannot be queried or the launch fails.
+ * Asynchronous.
  */
 TCR_API tcr_status tcr_read_probe(const void *x, size_t bytes, unsigned int *out, int ctas_per_sm,
                                   int block_threads, void *stream);

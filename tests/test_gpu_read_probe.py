@@ -20,7 +20,7 @@ def gpu():
 
 
 @pytest.mark.parametrize("nwords", [0, 4, 4 * 1001, 1 << 20, (1 << 24) + 36])
-@pytest.mark.parametrize("ctas,block", [(0, 0), (1, 1024), (4, 256), (8, 128)])
+@pytest.mark.parametrize("ctas,block", [(0, 0), (1, 1024), (4, 256), (8, 128), (-1, 0), (-1, 1024), (-1, 32)])
 def test_probe_reads_every_word(nwords, ctas, block):
     rng = np.random.default_rng(nwords + block)
     w = rng.integers(0, 1 << 32, nwords, dtype=np.uint64).astype(np.uint32)
