@@ -91,6 +91,14 @@
  * one launched with it must execute griddepcontrol.wait
  * (cudaGridDependencySynchronize) before it reads the call's results.
  *
+ * Shared memory and L1.  An SM keeps its shared-memory / L1 split while
+ * CTAs stream onto it, so a kernel that needs a large split leaves the
+ * next kernels on the stream a small L1.  The TCR_MMA_CHAIN_TMEM sum and
+ * flat-rows kernels ask for the 164 KiB configuration (92 KiB of L1 left);
+ * the 16-row tcgen05 rows kernel and tcr_gemm_splitk need 196-228 KiB
+ * (28-60 KiB left), and streaming kernels that followed such a split on
+ * the same SMs were measured about 14% slower.
+ *
  * Errors.  Invalid arguments return TCR_ERR_INVALID_ARG before any GPU work
  * and leave *out untouched.  A CUDA error (allocation or launch) returns
  * TCR_ERR_CUDA; the CUDA error itself is left to cudaGetLastError /
