@@ -625,7 +625,12 @@ def profile_arm(args):
     modes.  ``--profile-case gemm``: the split-K GEMM on 4096^3 (one split)
     and 1024 x 1024 x 16384 (the default split).  ``--profile-case short``:
     the packed short-row kernels, each mode once on 4194304 x 64 fp16 rows
-    (512 MiB) and once on 2684354 x 100 (rows not 16-byte aligned)."""
+    (512 MiB) and once on 2684354 x 100 (rows not 16-byte aligned).
+    ``--profile-case odd``: FIXED_ORDER and MMA_CHAIN on rows of odd length
+    (536334 x 1001 and 1046502 x 513 fp16, every other row on a 2-byte
+    boundary).  ``--profile-case blocked``: FIXED_ORDER's blocked order on
+    the 2^28 fp16 sum with runs of 256 and on 32768 x 4096 rows with runs of
+    32 and 256."""
     import torch
     import arithmetic_reduction_tensor_gb300 as tcr
     from arithmetic_reduction_tensor_gb300 import synth
@@ -648,6 +653,28 @@ def profile_arm(args):
             for rows, cols in shapes:
                 for kind in (tcr.MMA_CHAIN, tcr.FIXED_ORDER, tcr.SHUFFLE_TREE):
                     tcr.tcr_reduce_rows(x[:rows * cols].view(rows, cols), tcr.Mode(kind))
+        torch.cuda.synchronize()
+        print("profile case done", flush=True)
+        return 0
+    if args.profile_case == "odd":
+        n = 1 << 29
+        x = torch.from_numpy(synth.generate(n, "normal", synth.F16, seed=2).view(np.int16)).cuda()
+        shapes = ((n // 1001, 1001), (n // 513, 513))
+        for _ in range(args.steps):
+            for rows, cols in shapes:
+                for kind in (tcr.FIXED_ORDER, tcr.MMA_CHAIN):
+                    tcr.tcr_reduce_rows(x[:rows * cols].view(rows, cols), tcr.Mode(kind))
+        torch.cuda.synchronize()
+        print("profile case done", flush=True)
+        return 0
+    if args.profile_case == "blocked":
+        x = torch.from_numpy(synth.generate(1 << 28, "uniform_pm1", synth.F16, seed=4).view(np.int16)).cuda()
+        r = torch.from_numpy(synth.generate(32768 * COLS, "normal", synth.F16, seed=2).view(np.int16))
+        r = r.cuda().view(32768, COLS)
+        for _ in range(args.steps):
+            tcr.tcr_reduce_sum(x, tcr.Mode(tcr.FIXED_ORDER, run_log2=8))
+            tcr.tcr_reduce_rows(r, tcr.Mode(tcr.FIXED_ORDER, run_log2=5))
+            tcr.tcr_reduce_rows(r, tcr.Mode(tcr.FIXED_ORDER, run_log2=8))
         torch.cuda.synchronize()
         print("profile case done", flush=True)
         return 0
@@ -884,7 +911,7 @@ def main():
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--extras", action="store_true",
                     help="time the sum of squares and binary32 calls (beyond the hot path) and exit")
-    ap.add_argument("--profile-case", nargs="?", const="f16", choices=["f16", "f32", "gemm", "short"],
+    ap.add_argument("--profile-case", nargs="?", const="f16", choices=["f16", "f32", "gemm", "short", "odd", "blocked"],
                     default=None,
                     help="run the small ncu case (2^28 sum, 32768 x 4096 rows; f32: the same "
                          "bytes in binary32; gemm: 4096^3 and 1024^2 x 16384 bf16; short: packed "
